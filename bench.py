@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA serving step (libkda_gb300.so) on GB300.
+
+Headline step: one kda_decode call (T = 1) over a 512-row serving batch:
+H = 12, K = V = 128, bf16 state pool of 640 slots, q/k/v strided views of a
+fused [512, 4672] bf16 projection buffer, about 5% of the rows inactive.
+value = algorithmic state GB/s (bytes the method must move / kernel time),
+measured with CUDA events around each call on the launching stream, with L2
+flushed (a 2 x L2 write) between calls. The same line carries:
+  e2e          the same metric through the public binding with this step's
+               inputs copied from pinned host memory and the output copied
+               back inside the timed region (the pool stays resident);
+  roofline     the decode kernel's achieved GB/s against the measured HBM peak;
+  cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload;
+  sweep        T=1 decode at B = 1..512, T=8 verify and T=8 ring verify at
+               B = 1, 32, 512 (0/50/100% of rows folding), all L2-cold.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-sweep]
+
+For N > 1, launch one process per GPU with torch.distributed.run; each rank
+processes its own batch and pool (no data exchange), the timed region is
+bracketed by barriers and the time taken is the maximum over ranks.
+--impl reference times the CPU oracle (the only other implementation of this
+path) on the same workload, a bounded sample of rows per step.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+# the CPU oracle runs single-threaded; its reported core count relies on this
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_attention_ssm_step_gb300 import kda, traffic, workloads  # noqa: E402
+
+METRIC = "KDA decode µs/step and state GB/s (% HBM peak) at B=1..512, T=1 and T=8"
+WORKLOAD = ("T=1 KDA decode, B=512, H=12, K=V=128, bf16 state pool [640,12,128,128] ~N(0,0.02^2), "
+            "q/k/v strided views of a fused bf16 [512,4672] projection buffer, ~5% of rows inactive")
+B_HEAD, N_HEAD, SEED_HEAD = 512, 640, 2
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "kda_decode_b512_ncu.md")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+
+def kernel_source_hash():
+    """Hash of the CUDA sources; a profile summary taken from other sources is stale."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_attention_ssm_step_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        peaks = json.load(open(path))
+        return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per launch of the decode kernel from the committed ncu summary,
+    or None when the summary is missing or was taken from different sources."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("source_hash", "traffic_bytes_per_launch")):
+            k, v = line.strip().strip("`").split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_hash") != kernel_source_hash() or "traffic_bytes_per_launch" not in vals:
+        return None
+    return float(vals["traffic_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        self.cmd = cmd
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.2)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.1)
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    if n_gpus != world and world > 1:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device=None):
+    """Largest value of x over all ranks (x itself when there is one rank)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class L2Flush:
+    def __init__(self, device):
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=device)
+        self.nbytes = self.buf.numel() * 4
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def time_calls(fn, steps, warmup, before=None, world=1):
+    """Per-call device time (ms) of fn() with CUDA events on the current stream;
+    before() runs outside the event pair ahead of every call."""
+    for _ in range(warmup):
+        if before:
+            before()
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in evs:
+        if before:
+            before()
+        s.record()
+        fn()
+        e.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+def decode_call(wd, out):
+    return lambda: kda.kda_decode(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
+                                  wd.A_log, wd.dt_bias, out=out)
+
+
+def n_active(w):
+    idx = w.state_indices.to(torch.int64)
+    return int(((idx >= 0) & (idx < w.N)).sum())
+
+
+def headline(dev, steps, warmup, world, rank):
+    w = workloads.decode_inputs(B_HEAD, N_HEAD, seed=SEED_HEAD + rank, layout="fused", inactive_frac=0.05)
+    wd = w.to(dev)
+    out = torch.empty((B_HEAD, 12, 128), dtype=torch.bfloat16, device=dev)
+    flush = L2Flush(dev)
+    act = n_active(w)
+    nbytes = traffic.decode_bytes(act, B_HEAD - act)
+    with ClockSampler(dev) as clk:
+        times = time_calls(decode_call(wd, out), steps, warmup, before=flush, world=world)
+    total_ms = max_over_ranks(sum(times), world, dev)
+    return dict(w=w, wd=wd, out=out, times=times, total_ms=total_ms, nbytes=nbytes, clocks=clk.summary(),
+                active=act, flush=flush)
+
+
+def e2e(dev, h, steps, warmup, world):
+    """Same call through the binding, host inputs in pinned memory copied in and the output copied out."""
+    w, wd, out, flush = h["w"], h["wd"], h["out"], h["flush"]
+    host_in = {name: getattr(w, name).pin_memory() for name in ("qkv", "g_raw", "beta_logit", "state_indices")}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def step():
+        for name, t in host_in.items():
+            getattr(wd, name).copy_(t, non_blocking=True)
+        kda.kda_decode(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit, wd.A_log,
+                       wd.dt_bias, out=out)
+        host_out.copy_(out, non_blocking=True)
+
+    times = time_calls(step, steps, warmup, before=flush, world=world)
+    total_ms = max_over_ranks(sum(times), world, dev)
+    return total_ms, h2d, d2h
+
+
+def sweep(dev, steps=20, warmup=3):
+    flush = L2Flush(dev)
+    res = {"t1_decode": [], "t8_verify": [], "t8_ring_w32": []}
+    for B in (1, 8, 16, 32, 64, 128, 256, 512):
+        w = workloads.decode_inputs(B, B + 128, seed=10 + B, layout="fused")
+        wd = w.to(dev)
+        out = torch.empty((B, 12, 128), dtype=torch.bfloat16, device=dev)
+        t = statistics.median(time_calls(decode_call(wd, out), steps, warmup, before=flush))
+        nb = traffic.decode_bytes(B)
+        res["t1_decode"].append({"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1),
+                                 "config": kda.kda_select_config(B, 1)})
+        del w, wd
+    for B in (1, 32, 512):
+        w = workloads.decode_inputs(B, B + 64, seed=20 + B, T=8)
+        wd = w.to(dev)
+        out = torch.empty((B, 8, 12, 128), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_verify(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
+                                    wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
+        t = statistics.median(time_calls(fn, steps, warmup, before=flush))
+        nb = traffic.verify_bytes(B, 8)
+        res["t8_verify"].append({"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1)})
+        del w, wd
+    for B in (1, 32, 512):
+        for fold in (0.0, 0.5, 1.0):
+            w = workloads.ring_inputs(B, B + 64, T=8, W=32, flush_min=9, fold_frac=fold, seed=30 + B)
+            wd = w.to(dev)
+            saved = {k: v.clone() for k, v in wd.ring.items() if isinstance(v, torch.Tensor)}
+            st0 = wd.state.clone()
+            out = torch.empty((B, 8, 12, 128), dtype=torch.bfloat16, device=dev)
+            r = wd.ring
+
+            def restore():
+                wd.state.copy_(st0)
+                for k, v in saved.items():
+                    r[k].copy_(v)
+                flush()
+
+            fn = lambda: kda.kda_verify_ring(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
+                                             wd.beta_logit, wd.A_log, wd.dt_bias, r["k_cache"], r["u_cache"],
+                                             r["g_cache"], r["hist_len"], 9, out=out)
+            t = statistics.median(time_calls(fn, steps, warmup, before=restore))
+            idx = w.state_indices.to(torch.int64)
+            hists = [int(w.ring["hist_len"][n]) for n in idx]
+            nb = traffic.ring_bytes(hists, 8, 9)
+            res["t8_ring_w32"].append({"B": B, "fold": fold, "us": round(t * 1e3, 2),
+                                       "GB/s": round(nb / t / 1e6, 1)})
+            del w, wd, saved, st0
+    return res
+
+
+def cpu_baseline(seconds=10.0):
+    """The fp64 oracle, as it stands, on 16 active rows of the headline workload."""
+    import oracle
+
+    w = workloads.decode_inputs(B_HEAD, N_HEAD, seed=SEED_HEAD, layout="fused", inactive_frac=0.05)
+    idx = w.state_indices.to(torch.int64)
+    rows = [b for b in range(B_HEAD) if 0 <= int(idx[b]) < N_HEAD][:16]
+    sub = w.select_rows(rows)
+    f = lambda t: t.double().numpy()  # noqa: E731
+    args = (f(sub.state), sub.state_indices.numpy(), f(sub.q), f(sub.k), f(sub.v), f(sub.g_raw),
+            f(sub.beta_logit), f(sub.A_log), f(sub.dt_bias))
+    oracle.kda_decode(*args)  # first touch of the arrays
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.kda_decode(*args)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 200:
+            break
+    per_call = el / n
+    return {"value": round(traffic.decode_bytes(len(rows)) / per_call / 1e9, 6), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{len(rows)} active rows of the B=512 workload per call, {n} calls in {el:.1f} s "
+                      f"({per_call * 1e3:.1f} ms per call), numpy fp64, one thread"}
+
+
+def run_gpu(args):
+    rank, world, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+
+    h = headline(dev, args.steps, args.warmup, world, rank)
+    e2e_ms, h2d, d2h = e2e(dev, h, args.steps, args.warmup, world)
+    if rank != 0:
+        return
+    ms_per_step = h["total_ms"] / args.steps
+    gbs = h["nbytes"] * world * args.steps / (h["total_ms"] / 1e3) / 1e9
+    per_launch_gbs = h["nbytes"] / (statistics.mean(h["times"]) / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B_HEAD, "T": 1, "H": 12, "K": 128, "V": 128, "pool": N_HEAD,
+                   "active_rows": h["active"], "bytes_per_step": h["nbytes"],
+                   "l2": f"flushed between steps ({h['flush'].nbytes >> 20} MiB write, outside the timed calls)",
+                   "parallelism": f"{world} GPU(s), one independent batch and pool per GPU, no collective on the data path"},
+        "e2e": {"value": round(h["nbytes"] * world * args.steps / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
+                "us_per_step": round(e2e_ms / args.steps * 1e3, 2),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "roofline": {"kernel": "kda_step_kernel<128,bulk,T=1>", "bound": "hbm",
+                     "achieved": round(per_launch_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(per_launch_gbs / peak, 4), "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "traffic": profiled_traffic(), "algorithmic_bytes": h["nbytes"]},
+        "gpu_launches": args.steps,
+        "clocks": h["clocks"],
+        "context_b200_pages": {"B512_direct_us": 63.82, "B512_effective_TBps": 6.43,
+                               "note": "B200 numbers from the pages, no inactive rows; context only"},
+    }
+    if not args.no_sweep:
+        line["sweep"] = sweep(dev)
+    line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    w = workloads.decode_inputs(B_HEAD, N_HEAD, seed=SEED_HEAD, layout="fused", inactive_frac=0.05)
+    idx = w.state_indices.to(torch.int64)
+    rows = [b for b in range(B_HEAD) if 0 <= int(idx[b]) < N_HEAD][:8]
+    sub = w.select_rows(rows)
+    f = lambda t: t.double().numpy()  # noqa: E731
+    args_ = (f(sub.state), sub.state_indices.numpy(), f(sub.q), f(sub.k), f(sub.v), f(sub.g_raw),
+             f(sub.beta_logit), f(sub.A_log), f(sub.dt_bias))
+    for _ in range(args.warmup):
+        oracle.kda_decode(*args_)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.kda_decode(*args_)
+    el = time.perf_counter() - t0
+    nbytes = traffic.decode_bytes(len(rows))
+    gbs = nbytes * args.steps / el / 1e9
+    sample = f"{len(rows)} active rows of the B=512 workload per step, numpy fp64, one thread"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B_HEAD, "T": 1, "H": 12, "K": 128, "V": 128, "pool": N_HEAD},
+        "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the B / T / fold sweep")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+// kda_api.cu - the C ABI: host-side argument validation, launch-configuration
+// selection and dispatch. No device memory is read, nothing is allocated and
+// nothing synchronizes; kernels go on the caller's stream.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "kda.h"
+#include "kda_launch.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+kda_status fail(kda_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+kda_status ok() {
+  g_err[0] = '\0';
+  return KDA_OK;
+}
+
+// Rows of V per CTA, by configuration index.
+constexpr int kTileV[] = {8, 16, 32, 64, 128};
+constexpr int kNumConfigs = sizeof(kTileV) / sizeof(kTileV[0]);
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Byte extent [lo, hi) touched by a strided bf16 view [B][T][H][D].
+void view_extent(const void* ptr, int B, int T, int H, int D, int64_t bs, int64_t ts, int64_t hs,
+                 uintptr_t& lo, uintptr_t& hi) {
+  lo = reinterpret_cast<uintptr_t>(ptr);
+  const int64_t last = (int64_t)(B - 1) * bs + (int64_t)(T - 1) * ts + (int64_t)(H - 1) * hs + (D - 1);
+  hi = lo + (uintptr_t)(last + 1) * 2;
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+kda_status check_view(const char* name, const kda_view& v, int D) {
+  (void)D;
+  if (v.ptr == nullptr) return fail(KDA_EINVAL, "%s.ptr is NULL", name);
+  if (!aligned(v.ptr, 2)) return fail(KDA_EINVAL, "%s.ptr is not 2-byte aligned", name);
+  if (v.b_stride < 0 || v.t_stride < 0 || v.h_stride < 0)
+    return fail(KDA_EINVAL, "%s has a negative stride", name);
+  return KDA_OK;
+}
+
+// Checks shared by the three calls. On success, sets *bulk.
+kda_status check_params(const kda_params* p, int T, bool* bulk) {
+  if (p == nullptr) return fail(KDA_EINVAL, "params is NULL");
+  if (p->B < 0) return fail(KDA_EINVAL, "B = %d is negative", p->B);
+  if (p->N < 0) return fail(KDA_EINVAL, "N = %d is negative", p->N);
+  if (p->K != 128 || p->V != 128) return fail(KDA_EUNSUPPORTED, "K = %d, V = %d: only 128 x 128", p->K, p->V);
+  if (p->H < 1 || p->H > 64) return fail(KDA_EUNSUPPORTED, "H = %d outside 1..64", p->H);
+  if (T < 1 || T > KDA_MAX_T) return fail(KDA_EUNSUPPORTED, "T = %d outside 1..%d", T, KDA_MAX_T);
+  if ((long long)p->B * p->H * 128 > 0x7fffffffLL)
+    return fail(KDA_EUNSUPPORTED, "B * H = %lld is too large for one launch", (long long)p->B * p->H);
+  if (p->config_override < -1 || p->config_override >= kNumConfigs)
+    return fail(KDA_EINVAL, "config_override = %d outside -1..%d", p->config_override, kNumConfigs - 1);
+  if (!(p->lower_bound == p->lower_bound) || p->lower_bound > 3.0e38f || p->lower_bound < -3.0e38f)
+    return fail(KDA_EINVAL, "lower_bound is not finite");
+  if (!(p->scale == p->scale) || p->scale > 3.0e38f || p->scale < -3.0e38f)
+    return fail(KDA_EINVAL, "scale is not finite");
+  kda_status s;
+  if ((s = check_view("q", p->q, 128)) != KDA_OK) return s;
+  if ((s = check_view("k", p->k, 128)) != KDA_OK) return s;
+  if ((s = check_view("v", p->v, 128)) != KDA_OK) return s;
+  if ((s = check_view("g_raw", p->g_raw, 128)) != KDA_OK) return s;
+  if ((s = check_view("beta_logit", p->beta_logit, 1)) != KDA_OK) return s;
+  if (p->A_log == nullptr || !aligned(p->A_log, 4)) return fail(KDA_EINVAL, "A_log is NULL or not 4-byte aligned");
+  if (p->dt_bias == nullptr || !aligned(p->dt_bias, 4))
+    return fail(KDA_EINVAL, "dt_bias is NULL or not 4-byte aligned");
+  if (p->state_indices == nullptr || !aligned(p->state_indices, 4))
+    return fail(KDA_EINVAL, "state_indices is NULL or not 4-byte aligned");
+  if (p->out == nullptr || !aligned(p->out, 2)) return fail(KDA_EINVAL, "out is NULL or not 2-byte aligned");
+  if (p->out_b_stride < 0 || p->out_t_stride < 0 || p->out_h_stride < 0)
+    return fail(KDA_EINVAL, "out has a negative stride");
+  if (p->error_word != nullptr && !aligned(p->error_word, 4))
+    return fail(KDA_EINVAL, "error_word is not 4-byte aligned");
+  const int64_t slot = (int64_t)p->H * 128 * 128;
+  if (p->N > 0) {
+    if (p->state == nullptr) return fail(KDA_EINVAL, "state is NULL with N = %d", p->N);
+    if (!aligned(p->state, 2)) return fail(KDA_EINVAL, "state is not 2-byte aligned");
+    if (p->N > 1 && p->state_slot_stride < slot)
+      return fail(KDA_EINVAL, "state_slot_stride = %lld < H*V*K = %lld", (long long)p->state_slot_stride,
+                  (long long)slot);
+  }
+  *bulk = p->N > 0 && aligned(p->state, 16) && (p->N == 1 || p->state_slot_stride % 8 == 0);
+  if (p->B > 0 && p->N > 0) {
+    uintptr_t o0, o1, s0, s1;
+    view_extent(p->out, p->B, T, p->H, 128, p->out_b_stride, p->out_t_stride, p->out_h_stride, o0, o1);
+    s0 = reinterpret_cast<uintptr_t>(p->state);
+    s1 = s0 + (uintptr_t)((int64_t)(p->N - 1) * p->state_slot_stride + slot) * 2;
+    if (overlaps(o0, o1, s0, s1)) return fail(KDA_EINVAL, "out overlaps the state pool");
+  }
+  return KDA_OK;
+}
+
+int pick_tile(const kda_params* p, int T) {
+  const int cfg = p->config_override >= 0 ? p->config_override : kda_select_config(p->B, T);
+  return kTileV[cfg];
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kda_num_configs(void) { return kNumConfigs; }
+
+int32_t kda_config_tile_v(int32_t config) {
+  if (config < 0 || config >= kNumConfigs) return -1;
+  return kTileV[config];
+}
+
+// Smaller tiles for small batches, so that B * H * (128 / TV) CTAs still cover
+// the 152 SMs of a GB300 several times over; whole-head tiles once a batch
+// fills the machine on its own.
+int32_t kda_select_config(int32_t B, int32_t T) {
+  if (B < 0 || T < 1 || T > KDA_MAX_T) return -1;
+  const long long heads = (long long)B * 12;
+  if (heads <= 12) return 0;    // 8 rows
+  if (heads <= 96) return 1;    // 16 rows
+  if (heads <= 384) return 2;   // 32 rows
+  if (heads <= 1536) return 3;  // 64 rows
+  return 4;                     // 128 rows
+}
+
+const char* kda_last_error(void) { return g_err; }
+
+kda_status kda_decode(const kda_params* p, void* stream) {
+  bool bulk = false;
+  kda_status s = check_params(p, 1, &bulk);
+  if (s != KDA_OK) return s;
+  if (p->B == 0) return ok();
+  cudaError_t e = kda::launch_step(*p, 1, pick_tile(p, 1), bulk, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_decode launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+kda_status kda_verify(const kda_params* p, int32_t T, void* stream) {
+  bool bulk = false;
+  kda_status s = check_params(p, T, &bulk);
+  if (s != KDA_OK) return s;
+  if (p->B == 0) return ok();
+  cudaError_t e = kda::launch_step(*p, T, pick_tile(p, T), bulk, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params* r, void* stream) {
+  bool bulk = false;
+  kda_status s = check_params(p, T, &bulk);
+  if (s != KDA_OK) return s;
+  if (r == nullptr) return fail(KDA_EINVAL, "ring params is NULL");
+  if (r->W < 1 || r->W > 64) return fail(KDA_EUNSUPPORTED, "W = %d outside 1..64", r->W);
+  if (T > r->W) return fail(KDA_EINVAL, "T = %d exceeds the ring width W = %d", T, r->W);
+  if (r->flush_min < 1 || (r->flush_min - 1) + T > r->W)
+    return fail(KDA_EINVAL, "flush_min = %d: need flush_min >= 1 and flush_min - 1 + T <= W (T = %d, W = %d)",
+                r->flush_min, T, r->W);
+  if (p->N > 0) {
+    if (r->k_cache == nullptr || r->u_cache == nullptr || r->g_cache == nullptr || r->hist_len == nullptr)
+      return fail(KDA_EINVAL, "a ring buffer is NULL");
+    if (!aligned(r->k_cache, 16) || !aligned(r->u_cache, 16) || !aligned(r->g_cache, 16))
+      return fail(KDA_EINVAL, "k_cache, u_cache and g_cache must be 16-byte aligned");
+    if (!aligned(r->hist_len, 4)) return fail(KDA_EINVAL, "hist_len is not 4-byte aligned");
+    const int64_t ring = (int64_t)p->H * r->W * 128;
+    if (p->N > 1 && (r->k_slot_stride < ring || r->u_slot_stride < ring || r->g_slot_stride < ring))
+      return fail(KDA_EINVAL, "a ring slot stride is below H*W*128 = %lld", (long long)ring);
+    if (r->k_slot_stride % 8 || r->u_slot_stride % 8 || r->g_slot_stride % 4)
+      return fail(KDA_EINVAL, "ring slot strides must keep slots 16-byte aligned");
+  }
+  if (p->B == 0) return ok();
+  cudaError_t e = kda::launch_ring(*p, T, *r, pick_tile(p, T), bulk, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify_ring launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+}  // extern "C"

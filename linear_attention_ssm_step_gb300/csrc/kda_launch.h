@@ -1,0 +1,32 @@
+// kda_launch.h - internal launchers behind the C ABI (not part of the public header).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "kda.h"
+
+namespace kda {
+
+// Raise a kernel's dynamic shared-memory limit on the first launch only, so
+// that later calls (including calls made during CUDA-graph capture) make no
+// attribute call. A failed attempt is retried on the next launch.
+template <typename Kernel>
+cudaError_t set_smem_limit_once(Kernel kern, size_t bytes) {
+  static std::atomic<bool> done{false};
+  if (done.load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done.store(true, std::memory_order_release);
+  return e;
+}
+
+// T-token step (T = 1 is decode). tile_v in {8, 16, 32, 64, 128}; bulk selects
+// the bulk-copy staging of the state (16-byte aligned pool) over plain loads.
+cudaError_t launch_step(const kda_params& p, int T, int tile_v, bool bulk, cudaStream_t s);
+
+// Ring-cache verify with replay and fold.
+cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, int tile_v, bool bulk,
+                        cudaStream_t s);
+
+}  // namespace kda

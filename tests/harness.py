@@ -1,0 +1,108 @@
+"""Shared test helpers: run the oracle and the CUDA library on the same workload,
+and the tolerances the comparisons use.
+
+Tolerances:
+  * outputs: |o - o_ref| <= 2e-2 + 2e-2 |o_ref| element-wise;
+  * state:   |s - s_ref| <= 2 bf16 ulps, the ulp taken at max(|s_ref|, 2^-12 M)
+    where M is the largest |s_ref| of that (slot, head). The floor comes from
+    the fp32 arithmetic of the kernels: the gate's exp/sigmoid chain carries a
+    relative error of up to about 2^-20 into the decay, so an element whose
+    new value cancels to far below the size of the terms it was summed from
+    (|d s| and |k u|, both of order M) carries an absolute error of order
+    2^-20 M. Measured at 2^-12 M, 2 ulps are 2^-18 M, four times that.
+"""
+
+import numpy as np
+import torch
+
+import oracle
+
+OUT_ATOL = 2e-2
+OUT_RTOL = 2e-2
+STATE_ULPS = 2.0
+STATE_FLOOR = 2.0 ** -12
+
+
+def f64(t):
+    """bf16 / fp32 / int tensor -> numpy (fp64 for floating types; exact)."""
+    t = t.detach().cpu()
+    if t.dtype in (torch.bfloat16, torch.float16, torch.float32, torch.float64):
+        return t.double().numpy()
+    return t.numpy()
+
+
+def bf16_ulp(mag):
+    mag = np.maximum(np.asarray(mag, dtype=np.float64), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(mag)).astype(np.int64) - 7)
+
+
+def output_excess(got, ref):
+    """max over elements of |got - ref| / (atol + rtol |ref|); <= 1 passes."""
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    if got.size == 0:
+        return 0.0
+    return float(np.max(np.abs(got - ref) / (OUT_ATOL + OUT_RTOL * np.abs(ref))))
+
+
+def assert_output_close(got, ref, what="output"):
+    e = output_excess(got, ref)
+    assert e <= 1.0, f"{what}: error reaches {e:.3f} x the tolerance 2e-2 + 2e-2|ref|"
+
+
+def state_ulps(got, ref):
+    """Per-element error in bf16 ulps (see module docstring); got/ref [..., V, K]."""
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    if got.size == 0:
+        return np.zeros(got.shape)
+    M = np.max(np.abs(ref), axis=(-1, -2), keepdims=True)
+    mag = np.maximum(np.abs(ref), STATE_FLOOR * M)
+    return np.abs(got - ref) / bf16_ulp(mag)
+
+
+def assert_state_close(got, ref, what="state", max_ulps=STATE_ULPS):
+    u = state_ulps(got, ref)
+    worst = float(u.max()) if u.size else 0.0
+    assert worst <= max_ulps, f"{what}: error reaches {worst:.2f} bf16 ulps (limit {max_ulps})"
+
+
+# ------------------------------------------------------------------ runners
+
+def oracle_decode(w, scale=1.0, lower_bound=-5.0):
+    return oracle.kda_decode(f64(w.state), f64(w.state_indices), f64(w.q), f64(w.k), f64(w.v),
+                             f64(w.g_raw), f64(w.beta_logit), f64(w.A_log), f64(w.dt_bias),
+                             lower_bound=lower_bound, scale=scale)
+
+
+def oracle_verify(w, scale=1.0, lower_bound=-5.0):
+    return oracle.kda_verify(f64(w.state), f64(w.state_indices), f64(w.q), f64(w.k), f64(w.v),
+                             f64(w.g_raw), f64(w.beta_logit), f64(w.A_log), f64(w.dt_bias),
+                             lower_bound=lower_bound, scale=scale)
+
+
+def oracle_ring(w, restart=True, scale=1.0, lower_bound=-5.0):
+    r = w.ring
+    return oracle.kda_verify_ring(f64(w.state), f64(w.state_indices), f64(w.q), f64(w.k), f64(w.v),
+                                  f64(w.g_raw), f64(w.beta_logit), f64(w.A_log), f64(w.dt_bias),
+                                  f64(r["k_cache"]), f64(r["u_cache"]), f64(r["g_cache"]),
+                                  f64(r["hist_len"]), r["flush_min"], restart_hist_on_flush=restart,
+                                  lower_bound=lower_bound, scale=scale)
+
+
+def gpu_decode(wd, **kw):
+    from linear_attention_ssm_step_gb300 import kda
+    return kda.kda_decode(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
+                          wd.A_log, wd.dt_bias, **kw)
+
+
+def gpu_verify(wd, **kw):
+    from linear_attention_ssm_step_gb300 import kda
+    return kda.kda_verify(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
+                          wd.A_log, wd.dt_bias, **kw)
+
+
+def gpu_ring(wd, restart=True, **kw):
+    from linear_attention_ssm_step_gb300 import kda
+    r = wd.ring
+    return kda.kda_verify_ring(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
+                               wd.A_log, wd.dt_bias, r["k_cache"], r["u_cache"], r["g_cache"],
+                               r["hist_len"], r["flush_min"], restart_hist_on_flush=restart, **kw)

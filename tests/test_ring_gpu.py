@@ -1,0 +1,176 @@
+"""kda_verify_ring on the GPU against the oracle: replay of the live history,
+fold into the checkpoint, appended ring entries, hist_len bookkeeping, the
+inactive and invalid-history rules, and replay consistency on the GPU."""
+
+import numpy as np
+import pytest
+import torch
+
+from harness import assert_output_close, assert_state_close, f64, gpu_ring, oracle_ring, state_ulps
+from linear_attention_ssm_step_gb300 import kda, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def ring_ulps(got, ref):
+    """bf16 ulps of ring rows [..., W, D], the floor taken per (slot, head, entry) row."""
+    got, ref = np.asarray(got), np.asarray(ref)
+    return state_ulps(got[..., None, :], ref[..., None, :])
+
+
+def check_ring(w, dev, rows=None, restart=True, **kw):
+    wd = w.to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = gpu_ring(wd, restart=restart, error_word=err, **kw)
+    torch.cuda.synchronize()
+    sub = w if rows is None else w.select_rows(rows)
+    ref = oracle_ring(sub, restart=restart)
+    got_out = f64(out) if rows is None else f64(out)[rows]
+    idx = sub.state_indices.numpy().astype(np.int64)
+    hist0 = w.ring["hist_len"].numpy()
+    active = (idx >= 0) & (idx < w.N)
+    assert (got_out[~active] == 0).all()
+    assert_output_close(got_out, ref["out"])
+    slots = idx[active]
+    T = w.T
+    assert_state_close(f64(wd.state)[slots], ref["state"][slots])
+    for n in slots:
+        folded = hist0[n] >= w.ring["flush_min"]
+        if not folded:  # the checkpoint is written only by a fold
+            assert np.array_equal(f64(wd.state)[n], f64(w.state)[n])
+    assert np.array_equal(f64(wd.ring["hist_len"])[slots], ref["hist_len"][slots])
+    kc, uc, gc = f64(wd.ring["k_cache"]), f64(wd.ring["u_cache"]), f64(wd.ring["g_cache"])
+    for n in slots:
+        base = 0 if hist0[n] >= w.ring["flush_min"] else hist0[n]
+        new = slice(base, base + T)
+        assert float(ring_ulps(kc[n][:, new], ref["k_cache"][n][:, new]).max()) <= 1.0
+        assert float(ring_ulps(uc[n][:, new], ref["u_cache"][n][:, new]).max()) <= 2.0
+        G, Gr = gc[n][:, new], ref["g_cache"][n][:, new]
+        assert np.all(np.abs(G - Gr) <= 1e-5 * (1.0 + np.abs(Gr))), "G differs"
+        # everything else in the ring is untouched, NaN sentinels included
+        keep = np.ones(w.ring["W"], dtype=bool)
+        keep[new] = False
+        for name, got in (("k_cache", kc), ("u_cache", uc), ("g_cache", gc)):
+            assert np.array_equal(got[n][:, keep], f64(w.ring[name])[n][:, keep], equal_nan=True), name
+    assert int(err.item()) == ref["error_word"]
+    return wd, out, ref
+
+
+@pytest.mark.parametrize("fold", [0.0, 0.5, 1.0])
+@pytest.mark.parametrize("B", [1, 6, 32])
+def test_ring_matches_oracle(dev, B, fold):
+    w = workloads.ring_inputs(B, B + 64, T=8, W=32, flush_min=9, fold_frac=fold, seed=500 + B,
+                              inactive_frac=0.2 if B == 6 else 0.0)
+    check_ring(w, dev)
+
+
+def test_ring_serving_batch_512_sampled(dev):
+    """T = 8, W = 32, flush_min = 9, B = 512, half the rows folding: all rows run,
+    20 compared with the oracle."""
+    w = workloads.ring_inputs(512, 576, T=8, W=32, flush_min=9, fold_frac=0.5, seed=4)
+    rows = np.sort(np.random.default_rng(2).choice(512, 20, replace=False))
+    check_ring(w, dev, rows=rows)
+
+
+@pytest.mark.parametrize("config", [0, 1, 2, 3])
+def test_ring_every_tile_gives_the_same_bits(dev, config):
+    w = workloads.ring_inputs(5, 12, T=8, W=32, flush_min=9, fold_frac=0.5, seed=7)
+    a, b = w.to(dev), w.to(dev)
+    oa = gpu_ring(a, config_override=config)
+    ob = gpu_ring(b, config_override=3)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    for name in ("k_cache", "u_cache", "g_cache", "hist_len"):
+        x, y = a.ring[name], b.ring[name]
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32)), name
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+
+
+def test_ring_w16_t4(dev):
+    """The other mode of the pages: ring width 16, T = 4, flush_min = 13."""
+    w = workloads.ring_inputs(6, 20, T=4, W=16, flush_min=13, fold_frac=0.5, seed=8)
+    check_ring(w, dev)
+
+
+def test_ring_without_restart_keeps_hist_len(dev):
+    w = workloads.ring_inputs(4, 10, T=8, W=32, flush_min=9, fold_frac=1.0, seed=9)
+    wd, _, _ = check_ring(w, dev, restart=False)
+    idx = w.state_indices.long()
+    assert torch.equal(wd.ring["hist_len"].cpu()[idx], w.ring["hist_len"][idx])
+
+
+def test_ring_invalid_history_sets_error_and_touches_nothing(dev):
+    w = workloads.ring_inputs(4, 8, T=8, W=32, flush_min=9, seed=10)
+    idx = w.state_indices.long()
+    w.ring["hist_len"][idx[0]] = -1
+    w.ring["hist_len"][idx[1]] = 33
+    wd, out, ref = check_ring(w, dev)
+    assert ref["error_word"] == kda.KDA_ERR_HIST_LEN
+    for b in (0, 1):
+        n = int(idx[b])
+        assert (out[b].float() == 0).all()
+        assert torch.equal(wd.state[n].cpu().view(torch.int16), w.state[n].view(torch.int16))
+
+
+def test_ring_single_token_calls_chain_bitwise(dev):
+    """Without a fold, T single-token calls (hist_len advanced by the caller
+    between them) give the same bits as one T-token call: the replay of the
+    ring reproduces the in-call state exactly."""
+    T = 6
+    w = workloads.ring_inputs(5, 12, T=T, W=32, flush_min=20, fold_frac=0.0, seed=11)
+    hl = w.ring["hist_len"]
+    hl.copy_(torch.minimum(hl, torch.full_like(hl, 10)))  # no slot reaches flush_min within the T calls
+    a = w.to(dev)
+    out_all = gpu_ring(a)
+    c = w.to(dev)
+    idx = c.state_indices.long()
+    outs = []
+    from dataclasses import replace
+    for t in range(T):
+        wt = replace(c, T=1, g_raw=c.g_raw[:, t:t + 1], beta_logit=c.beta_logit[:, t:t + 1],
+                     q_sep=c.q_sep[:, t:t + 1], k_sep=c.k_sep[:, t:t + 1], v_sep=c.v_sep[:, t:t + 1])
+        outs.append(gpu_ring(wt))
+        c.ring["hist_len"][idx] += 1
+    torch.cuda.synchronize()
+    assert torch.equal(out_all.view(torch.int16), torch.cat(outs, dim=1).view(torch.int16))
+    for name in ("k_cache", "u_cache"):
+        assert torch.equal(a.ring[name].view(torch.int16), c.ring[name].view(torch.int16)), name
+    assert torch.equal(a.ring["g_cache"].view(torch.int32), c.ring["g_cache"].view(torch.int32))
+
+
+def test_ring_cuda_graph_bitwise(dev):
+    w = workloads.ring_inputs(6, 12, T=8, W=32, flush_min=9, fold_frac=0.5, seed=12)
+    wd = w.to(dev)
+    snap = {k: v.clone() for k, v in wd.ring.items() if isinstance(v, torch.Tensor)}
+    st0 = wd.state.clone()
+
+    def reset():
+        wd.state.copy_(st0)
+        for k, v in snap.items():
+            wd.ring[k].copy_(v)
+
+    gpu_ring(wd)
+    torch.cuda.synchronize()
+    reset()
+    out = torch.empty((6, 8, 12, 128), dtype=torch.bfloat16, device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gpu_ring(wd, out=out)
+    res = []
+    for _ in range(2):
+        reset()
+        graph.replay()
+        torch.cuda.synchronize()
+        res.append([out.clone(), wd.state.clone()] + [wd.ring[k].clone() for k in snap])
+    for x, y in zip(res[0], res[1]):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))

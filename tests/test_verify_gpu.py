@@ -1,0 +1,114 @@
+"""kda_verify (T tokens) on the GPU: against the oracle, and bit for bit
+against T chained kda_decode calls."""
+
+import numpy as np
+import pytest
+import torch
+
+from harness import assert_output_close, assert_state_close, f64, gpu_decode, gpu_verify, oracle_verify
+from linear_attention_ssm_step_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def check_verify(w, dev, rows=None, **kw):
+    wd = w.to(dev)
+    out = gpu_verify(wd, **kw)
+    torch.cuda.synchronize()
+    sub = w if rows is None else w.select_rows(rows)
+    ref_state, ref_out = oracle_verify(sub)
+    got_out = f64(out) if rows is None else f64(out)[rows]
+    idx = sub.state_indices.numpy().astype(np.int64)
+    active = (idx >= 0) & (idx < w.N)
+    assert (got_out[~active] == 0).all()
+    assert_output_close(got_out, ref_out)
+    assert_state_close(f64(wd.state)[idx[active]], ref_state[idx[active]])
+    return wd, out
+
+
+@pytest.mark.parametrize("T", [1, 2, 8, 16])
+@pytest.mark.parametrize("B", [1, 5, 32])
+def test_verify_matches_oracle(dev, B, T):
+    if B == 32 and T == 16:
+        pytest.skip("covered by the T=8 case; keeps the oracle time short")
+    w = workloads.decode_inputs(B, B + 64, seed=300 + 17 * B + T, T=T, inactive_frac=0.2 if B == 5 else 0.0)
+    check_verify(w, dev)
+
+
+@pytest.mark.parametrize("T", [2, 8])
+@pytest.mark.parametrize("config", [None, 0, 2, 3, 4])
+def test_verify_equals_chained_decodes_bitwise(dev, T, config):
+    kw = {} if config is None else {"config_override": config}
+    w = workloads.decode_inputs(7, 20, seed=400 + T, T=T, inactive_frac=0.15, layout="packed")
+    wd = w.to(dev)
+    out_v = gpu_verify(wd, **kw)
+    wc = w.to(dev)
+    outs = []
+    for t in range(T):
+        outs.append(gpu_decode(_token(wc, t), **kw))
+    torch.cuda.synchronize()
+    assert torch.equal(wd.state.view(torch.int16), wc.state.view(torch.int16))
+    assert torch.equal(out_v.view(torch.int16), torch.stack(outs, dim=1).view(torch.int16))
+
+
+def _token(w, t):
+    """Token t of a T-token workload as a decode workload sharing the pool."""
+    from dataclasses import replace
+    return replace(w, T=None, g_raw=w.g_raw[:, t], beta_logit=w.beta_logit[:, t],
+                   qkv=None if w.qkv is None else w.qkv[:, t],
+                   q_sep=None if w.q_sep is None else w.q_sep[:, t],
+                   k_sep=None if w.k_sep is None else w.k_sep[:, t],
+                   v_sep=None if w.v_sep is None else w.v_sep[:, t])
+
+
+def test_verify_serving_batch_512_sampled(dev):
+    """T = 8, B = 512, pool of 576: all rows run, 24 compared with the oracle."""
+    w = workloads.decode_inputs(512, 576, seed=3, T=8)
+    rows = np.sort(np.random.default_rng(1).choice(512, 24, replace=False))
+    check_verify(w, dev, rows=rows)
+
+
+def test_verify_misaligned_state_same_bits(dev):
+    w = workloads.decode_inputs(4, 6, seed=5, T=4)
+    wd = w.to(dev)
+    flat = torch.empty(6 * 12 * 128 * 128 + 8, dtype=torch.bfloat16, device=dev)
+    mis = flat[3:3 + 6 * 12 * 128 * 128].view(6, 12, 128, 128)
+    mis.copy_(wd.state)
+    out_a = gpu_verify(wd)
+    wd.state = mis
+    out_b = gpu_verify(wd)
+    ref = w.to(dev)
+    gpu_verify(ref)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(mis.view(torch.int16), ref.state.view(torch.int16))
+
+
+def test_verify_cuda_graph_bitwise(dev):
+    w = workloads.decode_inputs(6, 10, seed=6, T=8)
+    wd = w.to(dev)
+    init = wd.state.clone()
+    gpu_verify(wd)
+    torch.cuda.synchronize()
+    out = torch.empty((6, 8, 12, 128), dtype=torch.bfloat16, device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gpu_verify(wd, out=out)
+    res = []
+    for _ in range(3):
+        wd.state.copy_(init)
+        graph.replay()
+        torch.cuda.synchronize()
+        res.append((out.clone(), wd.state.clone()))
+    for o, s in res[1:]:
+        assert torch.equal(o.view(torch.int16), res[0][0].view(torch.int16))
+        assert torch.equal(s.view(torch.int16), res[0][1].view(torch.int16))
