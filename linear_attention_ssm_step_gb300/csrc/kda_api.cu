@@ -67,6 +67,8 @@ kda_status check_params(const kda_params* p, int T, bool* bulk) {
     return fail(KDA_EINVAL, "lower_bound is not finite");
   if (!(p->scale == p->scale) || p->scale > 3.0e38f || p->scale < -3.0e38f)
     return fail(KDA_EINVAL, "scale is not finite");
+  *bulk = false;
+  if (p->B == 0) return KDA_OK;  // nothing is read or written
   kda_status s;
   if ((s = check_view("q", p->q, 128)) != KDA_OK) return s;
   if ((s = check_view("k", p->k, 128)) != KDA_OK) return s;
@@ -163,7 +165,7 @@ kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params
   if (r->flush_min < 1 || (r->flush_min - 1) + T > r->W)
     return fail(KDA_EINVAL, "flush_min = %d: need flush_min >= 1 and flush_min - 1 + T <= W (T = %d, W = %d)",
                 r->flush_min, T, r->W);
-  if (p->N > 0) {
+  if (p->N > 0 && p->B > 0) {
     if (r->k_cache == nullptr || r->u_cache == nullptr || r->g_cache == nullptr || r->hist_len == nullptr)
       return fail(KDA_EINVAL, "a ring buffer is NULL");
     if (!aligned(r->k_cache, 16) || !aligned(r->u_cache, 16) || !aligned(r->g_cache, 16))

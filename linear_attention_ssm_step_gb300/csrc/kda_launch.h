@@ -9,12 +9,12 @@
 
 namespace kda {
 
-// Raise a kernel's dynamic shared-memory limit on the first launch only, so
+// Raise a kernel's dynamic shared-memory limit on its first launch only, so
 // that later calls (including calls made during CUDA-graph capture) make no
-// attribute call. A failed attempt is retried on the next launch.
+// attribute call. `done` must be a flag owned by that one kernel (a static
+// local of the per-kernel launcher). A failed attempt is retried next launch.
 template <typename Kernel>
-cudaError_t set_smem_limit_once(Kernel kern, size_t bytes) {
-  static std::atomic<bool> done{false};
+cudaError_t set_smem_limit_once(Kernel kern, size_t bytes, std::atomic<bool>& done) {
   if (done.load(std::memory_order_acquire)) return cudaSuccess;
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess) done.store(true, std::memory_order_release);

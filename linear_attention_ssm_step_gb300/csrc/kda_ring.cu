@@ -334,7 +334,8 @@ __global__ void __launch_bounds__(NTHREADS)
 template <int TV, bool BULK>
 static cudaError_t launch_ring_one(const kda_params& p, int T, const kda_ring_params& r, cudaStream_t s) {
   auto kern = kda_ring_kernel<TV, BULK>;
-  cudaError_t e = set_smem_limit_once(kern, ring_smem_bytes(TV, KDA_MAX_T));
+  static std::atomic<bool> smem_set{false};  // one flag per instantiation
+  cudaError_t e = set_smem_limit_once(kern, ring_smem_bytes(TV, KDA_MAX_T), smem_set);
   if (e != cudaSuccess) return e;
   const int tiles = KD / TV;
   const long long blocks = (long long)p.B * p.H * tiles;

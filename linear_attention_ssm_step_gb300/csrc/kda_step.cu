@@ -161,7 +161,8 @@ __global__ void __launch_bounds__(NTHREADS) kda_step_kernel(const kda_params p, 
 template <int TV, bool BULK, bool MULTI>
 static cudaError_t launch_one(const kda_params& p, int T, cudaStream_t stream) {
   auto kern = kda_step_kernel<TV, BULK, MULTI>;
-  cudaError_t e = set_smem_limit_once(kern, step_smem_bytes(TV, KDA_MAX_T));
+  static std::atomic<bool> smem_set{false};  // one flag per instantiation
+  cudaError_t e = set_smem_limit_once(kern, step_smem_bytes(TV, KDA_MAX_T), smem_set);
   if (e != cudaSuccess) return e;
   const int tiles = KD / TV;
   const long long blocks = (long long)p.B * p.H * tiles;

@@ -3,13 +3,25 @@ and the tolerances the comparisons use.
 
 Tolerances:
   * outputs: |o - o_ref| <= 2e-2 + 2e-2 |o_ref| element-wise;
-  * state:   |s - s_ref| <= 2 bf16 ulps, the ulp taken at max(|s_ref|, 2^-12 M)
-    where M is the largest |s_ref| of that (slot, head). The floor comes from
-    the fp32 arithmetic of the kernels: the gate's exp/sigmoid chain carries a
-    relative error of up to about 2^-20 into the decay, so an element whose
-    new value cancels to far below the size of the terms it was summed from
-    (|d s| and |k u|, both of order M) carries an absolute error of order
-    2^-20 M. Measured at 2^-12 M, 2 ulps are 2^-18 M, four times that.
+  * state after one step: |s - s_ref| <= 2 bf16 ulps, the ulp taken at
+    max(|s_ref|, 2^-12 M) where M is the largest |s_ref| of that (slot, head).
+    The floor comes from the fp32 arithmetic of the kernels: the gate's
+    exp/sigmoid chain carries a relative error of up to about 2^-20 into the
+    decay, so an element whose new value cancels to far below the size of the
+    terms it was summed from (|d s| and |k u|, both of order M) carries an
+    absolute error of order 2^-20 M. Measured at 2^-12 M, 2 ulps are 2^-18 M,
+    four times that.
+  * state after t > 1 rounded steps (verify, chained decodes): 2 bf16 ulps at
+    the head's scale M. Each step rounds the state to bf16; where the GPU and
+    the oracle round one element to neighbouring bf16 values (a 1-ulp
+    difference at that element's size, at most ulp(M)), the difference is
+    carried into the next steps in absolute terms: the step map
+    S -> (I - beta k k^T) diag(d) S is non-expansive, so it does not grow, but
+    the element itself may shrink, which makes the same difference many ulps
+    of its new, smaller value. The GPU and the oracle each run their own chain
+    (no oracle input ever comes from the GPU), so this is the bound that holds.
+    Single steps are held to the per-element bound above, and the GPU verify
+    equals the GPU's chained decodes bit for bit.
 """
 
 import numpy as np
@@ -49,20 +61,23 @@ def assert_output_close(got, ref, what="output"):
     assert e <= 1.0, f"{what}: error reaches {e:.3f} x the tolerance 2e-2 + 2e-2|ref|"
 
 
-def state_ulps(got, ref):
-    """Per-element error in bf16 ulps (see module docstring); got/ref [..., V, K]."""
+def state_ulps(got, ref, floor=STATE_FLOOR):
+    """Per-element error in bf16 ulps, the ulp taken at max(|ref|, floor * M),
+    M the largest |ref| over the last two axes; got/ref [..., V, K]."""
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
     if got.size == 0:
         return np.zeros(got.shape)
     M = np.max(np.abs(ref), axis=(-1, -2), keepdims=True)
-    mag = np.maximum(np.abs(ref), STATE_FLOOR * M)
+    mag = np.maximum(np.abs(ref), floor * M)
     return np.abs(got - ref) / bf16_ulp(mag)
 
 
-def assert_state_close(got, ref, what="state", max_ulps=STATE_ULPS):
-    u = state_ulps(got, ref)
+def assert_state_close(got, ref, what="state", steps=1, max_ulps=STATE_ULPS):
+    """The state tolerance of the module docstring for one step (steps = 1) or
+    for `steps` > 1 rounded steps."""
+    u = state_ulps(got, ref, STATE_FLOOR if steps == 1 else 1.0)
     worst = float(u.max()) if u.size else 0.0
-    assert worst <= max_ulps, f"{what}: error reaches {worst:.2f} bf16 ulps (limit {max_ulps})"
+    assert worst <= max_ulps, f"{what}: error reaches {worst:.2f} bf16 ulps (limit {max_ulps}, {steps} step(s))"
 
 
 # ------------------------------------------------------------------ runners

@@ -79,7 +79,7 @@ def test_single_row_sixteen_steps(dev):
         out = gpu_decode(wd)
         ref, ref_out = oracle_decode(w)
         assert_output_close(f64(out), ref_out, f"step {step} output")
-        assert_state_close(f64(gstate)[2:3], ref[2:3], f"step {step} state")
+        assert_state_close(f64(gstate)[2:3], ref[2:3], f"step {step} state", steps=step + 1)
         assert np.array_equal(f64(gstate)[[0, 1, 3]], f64(state)[[0, 1, 3]])
 
 
@@ -98,9 +98,9 @@ def test_thirtytwo_rows_sixty_four_chained_steps(dev):
         out = gpu_decode(wd)
         ref, ref_out = oracle_decode(w)
         worst_out = max(worst_out, output_excess(f64(out), ref_out))
-        worst_ulps = max(worst_ulps, float(state_ulps(f64(gstate), ref).max()))
+        worst_ulps = max(worst_ulps, float(state_ulps(f64(gstate), ref, floor=1.0).max()))
     assert worst_out <= 1.0, f"output error reached {worst_out:.3f} x tolerance over 64 steps"
-    assert worst_ulps <= 2.0, f"state drifted to {worst_ulps:.2f} bf16 ulps over 64 steps"
+    assert worst_ulps <= 2.0, f"state drifted to {worst_ulps:.2f} bf16 ulps of the head scale over 64 steps"
 
 
 def test_serving_batch_512_sampled(dev):
@@ -274,7 +274,7 @@ def test_cuda_graph_replay_is_deterministic_and_tracks_inputs(dev):
     assert torch.equal(results[0][1].view(torch.int16), results[1][1].view(torch.int16))
     # new inputs and new indices copied into the captured buffers
     w2 = workloads.decode_inputs(8, 12, seed=14, layout="packed", inactive_frac=0.25)
-    w2.state = w.state
+    w2.state, w2.A_log, w2.dt_bias = w.state, w.A_log, w.dt_bias  # not re-copied into the graph
     for name in ("qkv", "g_raw", "beta_logit", "state_indices"):
         getattr(wd, name).copy_(getattr(w2, name).to(dev))
     wd.state.copy_(init)

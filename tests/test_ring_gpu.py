@@ -38,9 +38,15 @@ def check_ring(w, dev, rows=None, restart=True, **kw):
     idx = sub.state_indices.numpy().astype(np.int64)
     hist0 = w.ring["hist_len"].numpy()
     active = (idx >= 0) & (idx < w.N)
-    assert (got_out[~active] == 0).all()
+    valid = active.copy()
+    valid[active] = (hist0[idx[active]] >= 0) & (hist0[idx[active]] <= w.ring["W"])
+    assert (got_out[~valid] == 0).all()
     assert_output_close(got_out, ref["out"])
-    slots = idx[active]
+    for n in idx[active & ~valid]:  # skipped for an invalid history: nothing touched
+        assert np.array_equal(f64(wd.state)[n], f64(w.state)[n])
+        for name in ("k_cache", "u_cache", "g_cache", "hist_len"):
+            assert np.array_equal(f64(wd.ring[name])[n], f64(w.ring[name])[n], equal_nan=True), name
+    slots = idx[valid]
     T = w.T
     assert_state_close(f64(wd.state)[slots], ref["state"][slots])
     for n in slots:

@@ -31,7 +31,7 @@ def check_verify(w, dev, rows=None, **kw):
     active = (idx >= 0) & (idx < w.N)
     assert (got_out[~active] == 0).all()
     assert_output_close(got_out, ref_out)
-    assert_state_close(f64(wd.state)[idx[active]], ref_state[idx[active]])
+    assert_state_close(f64(wd.state)[idx[active]], ref_state[idx[active]], steps=w.T)
     return wd, out
 
 
