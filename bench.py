@@ -5,8 +5,10 @@ Headline step: one kda_decode call (T = 1) over a 512-row serving batch:
 H = 12, K = V = 128, bf16 state pool of 640 slots, q/k/v strided views of a
 fused [512, 4672] bf16 projection buffer, about 5% of the rows inactive.
 value = algorithmic state GB/s (bytes the method must move / kernel time),
-measured with CUDA events around each call on the launching stream, with L2
-flushed (a 2 x L2 write) between calls. The same line carries:
+measured with CUDA events on the launching stream around each call, the call
+replayed from a CUDA graph (so host-side argument marshalling stays out of the
+device timing), with L2 flushed (a 2 x L2 write) between calls. The same line
+carries:
   e2e          the same metric through the public binding with this step's
                inputs copied from pinned host memory and the output copied
                back inside the timed region (the pool stays resident);
@@ -188,6 +190,19 @@ class L2Flush:
         self.buf.fill_(1)
 
 
+def graphed(fn):
+    """fn captured once in a CUDA graph; returns the replay. The library makes
+    no host-side decisions that depend on device data, so a replay repeats the
+    call exactly (on whatever the captured buffers hold at replay time)."""
+    fn()  # first call outside capture: one-time kernel attribute setup
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g.replay
+
+
 def time_calls(fn, steps, warmup, before=None, world=1):
     """Per-call device time (ms) of fn() with CUDA events on the current stream;
     before() runs outside the event pair ahead of every call."""
@@ -228,8 +243,9 @@ def headline(dev, steps, warmup, world, rank):
     flush = L2Flush(dev)
     act = n_active(w)
     nbytes = traffic.decode_bytes(act, B_HEAD - act)
+    replay = graphed(decode_call(wd, out))
     with ClockSampler(dev) as clk:
-        times = time_calls(decode_call(wd, out), steps, warmup, before=flush, world=world)
+        times = time_calls(replay, steps, warmup, before=flush, world=world)
     total_ms = max_over_ranks(sum(times), world, dev)
     return dict(w=w, wd=wd, out=out, times=times, total_ms=total_ms, nbytes=nbytes, clocks=clk.summary(),
                 active=act, flush=flush)
@@ -262,10 +278,12 @@ def sweep(dev, steps=20, warmup=3):
         w = workloads.decode_inputs(B, B + 128, seed=10 + B, layout="fused")
         wd = w.to(dev)
         out = torch.empty((B, 12, 128), dtype=torch.bfloat16, device=dev)
-        t = statistics.median(time_calls(decode_call(wd, out), steps, warmup, before=flush))
+        fn = decode_call(wd, out)
+        t = statistics.median(time_calls(graphed(fn), steps, warmup, before=flush))
+        td = statistics.median(time_calls(fn, steps, warmup, before=flush))
         nb = traffic.decode_bytes(B)
         res["t1_decode"].append({"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1),
-                                 "config": kda.kda_select_config(B, 1)})
+                                 "us_direct": round(td * 1e3, 2), "config": kda.kda_select_config(B, 1)})
         del w, wd
     for B in (1, 32, 512):
         w = workloads.decode_inputs(B, B + 64, seed=20 + B, T=8)
@@ -273,7 +291,7 @@ def sweep(dev, steps=20, warmup=3):
         out = torch.empty((B, 8, 12, 128), dtype=torch.bfloat16, device=dev)
         fn = lambda: kda.kda_verify(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
                                     wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
-        t = statistics.median(time_calls(fn, steps, warmup, before=flush))
+        t = statistics.median(time_calls(graphed(fn), steps, warmup, before=flush))
         nb = traffic.verify_bytes(B, 8)
         res["t8_verify"].append({"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1)})
         del w, wd
@@ -295,7 +313,7 @@ def sweep(dev, steps=20, warmup=3):
             fn = lambda: kda.kda_verify_ring(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
                                              wd.beta_logit, wd.A_log, wd.dt_bias, r["k_cache"], r["u_cache"],
                                              r["g_cache"], r["hist_len"], 9, out=out)
-            t = statistics.median(time_calls(fn, steps, warmup, before=restore))
+            t = statistics.median(time_calls(graphed(fn), steps, warmup, before=restore))
             idx = w.state_indices.to(torch.int64)
             hists = [int(w.ring["hist_len"][n]) for n in idx]
             nb = traffic.ring_bytes(hists, 8, 9)
@@ -365,6 +383,7 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "B": B_HEAD, "T": 1, "H": 12, "K": 128, "V": 128, "pool": N_HEAD,
                    "active_rows": h["active"], "bytes_per_step": h["nbytes"],
                    "l2": f"flushed between steps ({h['flush'].nbytes >> 20} MiB write, outside the timed calls)",
+                   "launch": "each timed call is one CUDA-graph replay of kda_decode",
                    "parallelism": f"{world} GPU(s), one independent batch and pool per GPU, no collective on the data path"},
         "e2e": {"value": round(h["nbytes"] * world * args.steps / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
                 "us_per_step": round(e2e_ms / args.steps * 1e3, 2),

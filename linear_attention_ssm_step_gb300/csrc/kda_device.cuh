@@ -154,42 +154,71 @@ __device__ __forceinline__ float load_bf16(const kda_view& vw, int b, int t, int
   return bf16_bits_to_float(p[(int64_t)b * vw.b_stride + (int64_t)t * vw.t_stride + (int64_t)h * vw.h_stride + c]);
 }
 
+// Raw per-token inputs of thread c (key channel c) for a chunk of PC tokens,
+// loaded into registers together so that their global-memory latencies
+// overlap instead of adding up token after token.
+constexpr int PC = 4;
+struct TokenLoads {
+  float q[PC], k[PC], g[PC], v[PC], bl[PC];
+};
+
+__device__ __forceinline__ void prologue_issue(const kda_params& p, int b, int h, int t0, int T, int v0, int TV,
+                                               TokenLoads& L) {
+  const int c = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < PC; ++i) {
+    const int t = t0 + i;
+    L.q[i] = L.k[i] = L.g[i] = L.v[i] = L.bl[i] = 0.0f;
+    if (t < T) {
+      L.q[i] = load_bf16(p.q, b, t, h, c);
+      L.k[i] = load_bf16(p.k, b, t, h, c);
+      L.g[i] = load_bf16(p.g_raw, b, t, h, c);
+      if (c < TV) L.v[i] = load_bf16(p.v, b, t, h, v0 + c);
+      if (c == 0)
+        L.bl[i] = bf16_bits_to_float(static_cast<const uint16_t*>(
+            p.beta_logit.ptr)[(int64_t)b * p.beta_logit.b_stride + (int64_t)t * p.beta_logit.t_stride +
+                              (int64_t)h * p.beta_logit.h_stride]);
+    }
+  }
+}
+
 // The per-token prologue of (row b, head h): L2 norms, k_hat . q_hat, the gate
-// and beta. Thread c of the CTA handles key channel c. Ends with a CTA barrier.
-// Every CTA of the same (b, h) computes the same bits: fixed reduction order.
+// and beta. Thread c of the CTA handles key channel c; `first` holds the
+// already-issued loads of tokens 0..PC-1. Ends with a CTA barrier. Every CTA of
+// the same (b, h) computes the same bits: fixed reduction order.
 __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h, int T, int v0, int TV,
-                                               const TokenSmem& ts) {
+                                               const TokenSmem& ts, const TokenLoads& first) {
   const int c = threadIdx.x;
   const int warp = c >> 5, lane = c & 31;
   const float a_h = expf(p.A_log[h]);
   const float dtb = p.dt_bias[(int64_t)h * KD + c];
-  for (int t = 0; t < T; ++t) {
-    const float qc = load_bf16(p.q, b, t, h, c);
-    const float kc = load_bf16(p.k, b, t, h, c);
-    const float gr = load_bf16(p.g_raw, b, t, h, c);
-    const float sq = warp_sum(__fmul_rn(qc, qc));
-    const float sk = warp_sum(__fmul_rn(kc, kc));
-    const float sqk = warp_sum(__fmul_rn(qc, kc));
-    if (lane == 0) {
-      float* r = ts.red + (t * NWARPS + warp) * 3;
-      r[0] = sq;
-      r[1] = sk;
-      r[2] = sqk;
-    }
-    // g = lower_bound * sigmoid(exp(A_log) * (g_raw + dt_bias)), decay exp(g)
-    const float z = __fmul_rn(a_h, __fadd_rn(gr, dtb));
-    const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-z)));
-    const float g = __fmul_rn(p.lower_bound, sig);
-    ts.gg[t * KD + c] = g;
-    ts.dd[t * KD + c] = expf(g);
-    ts.qh[t * KD + c] = qc;
-    ts.kh[t * KD + c] = kc;
-    if (c < TV) ts.vrow[t * TV + c] = load_bf16(p.v, b, t, h, v0 + c);
-    if (c == 0) {
-      const float bl = bf16_bits_to_float(static_cast<const uint16_t*>(
-          p.beta_logit.ptr)[(int64_t)b * p.beta_logit.b_stride + (int64_t)t * p.beta_logit.t_stride +
-                            (int64_t)h * p.beta_logit.h_stride]);
-      ts.beta[t] = __frcp_rn(__fadd_rn(1.0f, expf(-bl)));
+  TokenLoads L = first;
+  for (int t0 = 0; t0 < T; t0 += PC) {
+    if (t0 > 0) prologue_issue(p, b, h, t0, T, v0, TV, L);
+#pragma unroll
+    for (int i = 0; i < PC; ++i) {
+      const int t = t0 + i;
+      if (t >= T) break;
+      const float qc = L.q[i], kc = L.k[i];
+      const float sq = warp_sum(__fmul_rn(qc, qc));
+      const float sk = warp_sum(__fmul_rn(kc, kc));
+      const float sqk = warp_sum(__fmul_rn(qc, kc));
+      if (lane == 0) {
+        float* r = ts.red + (t * NWARPS + warp) * 3;
+        r[0] = sq;
+        r[1] = sk;
+        r[2] = sqk;
+      }
+      // g = lower_bound * sigmoid(exp(A_log) * (g_raw + dt_bias)), decay exp(g)
+      const float z = __fmul_rn(a_h, __fadd_rn(L.g[i], dtb));
+      const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-z)));
+      const float g = __fmul_rn(p.lower_bound, sig);
+      ts.gg[t * KD + c] = g;
+      ts.dd[t * KD + c] = expf(g);
+      ts.qh[t * KD + c] = qc;
+      ts.kh[t * KD + c] = kc;
+      if (c < TV) ts.vrow[t * TV + c] = L.v[i];
+      if (c == 0) ts.beta[t] = __frcp_rn(__fadd_rn(1.0f, expf(-L.bl[i])));
     }
   }
   __syncthreads();

@@ -83,25 +83,18 @@ __global__ void __launch_bounds__(NTHREADS)
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
 
   const int n = p.state_indices[b];
-  int hist = 0;
-  bool active = n >= 0 && n < p.N;
-  if (active) {
-    hist = rp.hist_len[n];
-    if (hist < 0 || hist > rp.W) {
-      active = false;
-      if (tid == 0 && tile == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_HIST_LEN);
-    }
-  }
-  if (!active) {
+  TokenLoads first;  // issued alongside the index load; unused by an inactive row
+  prologue_issue(p, b, h, 0, T, v0, TV, first);
+  if (n < 0 || n >= p.N) {
     for (int i = tid; i < T * TV; i += NTHREADS) {
       const int t = i / TV, r = i - t * TV;
       outp[out_base + (int64_t)t * p.out_t_stride + r] = 0;
     }
     return;
   }
-  const bool fold = hist >= rp.flush_min;
-  const int base = fold ? 0 : hist;
 
+  // The checkpoint copy starts before hist_len is known: reading it is harmless
+  // even when the history turns out to be invalid.
   uint16_t* gst = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride +
                   ((int64_t)h * KD + v0 + warp * RW) * KD;
   uint16_t* sst = st + warp * RW * KD;
@@ -112,16 +105,33 @@ __global__ void __launch_bounds__(NTHREADS)
       mbar_expect_tx(&mbar[warp], CHUNK_BYTES);
       bulk_g2s(sst, gst, CHUNK_BYTES, &mbar[warp]);
     }
-  } else {
+  }
+  const int hist = rp.hist_len[n];
+  if (hist < 0 || hist > rp.W) {
+    if (tid == 0 && tile == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_HIST_LEN);
+    if constexpr (BULK) {
+      __syncwarp();
+      if (!mbar_wait_bounded(&mbar[warp], 0) && lane == 0 && p.error_word != nullptr)
+        atomicOr(p.error_word, KDA_ERR_TIMEOUT);  // the copy must land before the CTA leaves
+    }
+    for (int i = tid; i < T * TV; i += NTHREADS) {
+      const int t = i / TV, r = i - t * TV;
+      outp[out_base + (int64_t)t * p.out_t_stride + r] = 0;
+    }
+    return;
+  }
+  if constexpr (!BULK) {
     for (int i = lane; i < RW * KD; i += 32) sst[i] = gst[i];
   }
+  const bool fold = hist >= rp.flush_min;
+  const int base = fold ? 0 : hist;
 
   // Ring slices of this (slot, head).
   uint16_t* kc = static_cast<uint16_t*>(rp.k_cache) + (int64_t)n * rp.k_slot_stride + (int64_t)h * rp.W * KD;
   uint16_t* uc = static_cast<uint16_t*>(rp.u_cache) + (int64_t)n * rp.u_slot_stride + (int64_t)h * rp.W * KD;
   float* gc = static_cast<float*>(rp.g_cache) + (int64_t)n * rp.g_slot_stride + (int64_t)h * rp.W * KD;
 
-  token_prologue(p, b, h, T, v0, TV, ts);  // ends with a CTA barrier
+  token_prologue(p, b, h, T, v0, TV, ts, first);  // ends with a CTA barrier
 
   // Per channel: k~, G, the decay exp(G_P - G_{P-1}) and the partial sums of k~ . q_hat.
   {

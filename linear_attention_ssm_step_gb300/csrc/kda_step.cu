@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(NTHREADS) kda_step_kernel(const kda_params p, 
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
 
   const int n = p.state_indices[b];
+  TokenLoads first;  // issued alongside the index load; unused by an inactive row
+  prologue_issue(p, b, h, 0, T, v0, TV, first);
   if (n < 0 || n >= p.N) {
     for (int i = tid; i < T * TV; i += NTHREADS) {
       const int t = i / TV, r = i - t * TV;
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(NTHREADS) kda_step_kernel(const kda_params p, 
     for (int i = lane; i < RW * KD; i += 32) sst[i] = gst[i];
   }
 
-  token_prologue(p, b, h, T, v0, TV, ts);
+  token_prologue(p, b, h, T, v0, TV, ts, first);
 
   bool ok = true;
   if constexpr (BULK) {

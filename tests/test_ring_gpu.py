@@ -21,10 +21,12 @@ def dev():
     return torch.device("cuda:0")
 
 
-def ring_ulps(got, ref):
+def ring_ulps(got, ref, floor=None):
     """bf16 ulps of ring rows [..., W, D], the floor taken per (slot, head, entry) row."""
     got, ref = np.asarray(got), np.asarray(ref)
-    return state_ulps(got[..., None, :], ref[..., None, :])
+    if floor is None:
+        return state_ulps(got[..., None, :], ref[..., None, :])
+    return state_ulps(got[..., None, :], ref[..., None, :], floor=floor)
 
 
 def check_ring(w, dev, rows=None, restart=True, **kw):
@@ -59,7 +61,9 @@ def check_ring(w, dev, rows=None, restart=True, **kw):
         base = 0 if hist0[n] >= w.ring["flush_min"] else hist0[n]
         new = slice(base, base + T)
         assert float(ring_ulps(kc[n][:, new], ref["k_cache"][n][:, new]).max()) <= 1.0
-        assert float(ring_ulps(uc[n][:, new], ref["u_cache"][n][:, new]).max()) <= 2.0
+        # u~ of token t depends on rounded values computed before it (the folded
+        # checkpoint, the u~ of earlier tokens): the multi-step bound applies
+        assert float(ring_ulps(uc[n][:, new], ref["u_cache"][n][:, new], floor=1.0).max()) <= 2.0
         G, Gr = gc[n][:, new], ref["g_cache"][n][:, new]
         assert np.all(np.abs(G - Gr) <= 1e-5 * (1.0 + np.abs(Gr))), "G differs"
         # everything else in the ring is untouched, NaN sentinels included
