@@ -240,9 +240,50 @@ __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h
   __syncthreads();
 }
 
-// A lane's 8 keys of one token's vectors, in registers.
+// ---------------------------------------------------------------- packed fp32 pairs
+
+// Two fp32 values in one 64-bit register pair, for the sm_100+ packed
+// instructions mul.rn.f32x2 / fma.rn.f32x2: one issue slot for two IEEE
+// operations, each rounded exactly as its scalar counterpart.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void upk2(f32x2 r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// bf16x2 word -> fp32 pair (exact).
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) {
+  return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// fp32 pair -> bf16x2 word, round to nearest even.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(f32x2 v) {
+  float lo, hi;
+  upk2(v, lo, hi);
+  return pack_bf16x2(lo, hi);
+}
+
+// A lane's 8 keys of one token's vectors, in registers, as 4 pairs each.
 struct LaneVecs {
-  float kh[8], qh[8], dd[8];
+  f32x2 kh[4], qh[4], dd[4];
 };
 
 __device__ __forceinline__ void load_lane_vecs(const TokenSmem& ts, int t, int j, LaneVecs& lv) {
@@ -252,10 +293,38 @@ __device__ __forceinline__ void load_lane_vecs(const TokenSmem& ts, int t, int j
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const float4 a = k4[i], q = q4[i], d = d4[i];
-    lv.kh[4 * i + 0] = a.x; lv.kh[4 * i + 1] = a.y; lv.kh[4 * i + 2] = a.z; lv.kh[4 * i + 3] = a.w;
-    lv.qh[4 * i + 0] = q.x; lv.qh[4 * i + 1] = q.y; lv.qh[4 * i + 2] = q.z; lv.qh[4 * i + 3] = q.w;
-    lv.dd[4 * i + 0] = d.x; lv.dd[4 * i + 1] = d.y; lv.dd[4 * i + 2] = d.z; lv.dd[4 * i + 3] = d.w;
+    lv.kh[2 * i] = pk2(a.x, a.y);
+    lv.kh[2 * i + 1] = pk2(a.z, a.w);
+    lv.qh[2 * i] = pk2(q.x, q.y);
+    lv.qh[2 * i + 1] = pk2(q.z, q.w);
+    lv.dd[2 * i] = pk2(d.x, d.y);
+    lv.dd[2 * i + 1] = pk2(d.z, d.w);
   }
+}
+
+// The two dot products of a row, reduced over the row's 16 lanes (lane j of
+// the row, j = lane & 15), and the row's u. Transposed butterfly: at the
+// first level the lanes with j < 8 keep the x half and the others the y half,
+// so each later level reduces one value instead of two; a last exchange hands
+// u (computed where x is complete) and y to every lane. 5 shuffles instead of
+// 8, and every lane of the row ends with the same u and y: each level adds the
+// same two values, in either order, in both lanes.
+__device__ __forceinline__ void row_reduce(f32x2 xp, f32x2 yp, int j, float beta, float vv, float& u, float& y) {
+  float x0, x1, y0, y1;
+  upk2(xp, x0, x1);
+  upk2(yp, y0, y1);
+  const float x = __fadd_rn(x0, x1), yy = __fadd_rn(y0, y1);
+  const bool upper = (j & 8) != 0;
+  float keep = upper ? yy : x;
+  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, upper ? x : yy, 8));
+  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, keep, 4));
+  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, keep, 2));
+  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, keep, 1));
+  // lanes j < 8 hold x, lanes j >= 8 hold y
+  const float mine = upper ? keep : __fmul_rn(beta, __fsub_rn(vv, keep));
+  const float got = __shfl_xor_sync(0xffffffffu, mine, 8);
+  u = upper ? got : mine;
+  y = upper ? keep : got;
 }
 
 // One gated delta-rule step on one state row, shared by 16 lanes (lane j holds
@@ -263,35 +332,27 @@ __device__ __forceinline__ void load_lane_vecs(const TokenSmem& ts, int t, int j
 //   a = d * s;  x = a . k_hat;  y = a . q_hat        (reduced over the 16 lanes)
 //   u = beta (v - x);  s <- bf16(a + k_hat u);  o = scale (y + u kappa)
 // The output uses the fused form o = (D s) . q_hat + u (k_hat . q_hat), which
-// equals s_new . q_hat before rounding. Every lane of the row gets the same u
-// and o: each butterfly level adds the same two values in both lanes.
-__device__ __forceinline__ float row_step(uint4& s, const LaneVecs& lv, float beta, float kappa, float vv,
+// equals s_new . q_hat before rounding.
+__device__ __forceinline__ float row_step(uint4& s, const LaneVecs& lv, int j, float beta, float kappa, float vv,
                                           float scale) {
-  float a[8];
-  unpack_bf16x2(s.x, a[0], a[1]);
-  unpack_bf16x2(s.y, a[2], a[3]);
-  unpack_bf16x2(s.z, a[4], a[5]);
-  unpack_bf16x2(s.w, a[6], a[7]);
+  f32x2 a[4];
+  a[0] = mul2(lv.dd[0], bf16x2_to_f32x2(s.x));
+  a[1] = mul2(lv.dd[1], bf16x2_to_f32x2(s.y));
+  a[2] = mul2(lv.dd[2], bf16x2_to_f32x2(s.z));
+  a[3] = mul2(lv.dd[3], bf16x2_to_f32x2(s.w));
+  f32x2 xp = mul2(lv.kh[0], a[0]), yp = mul2(lv.qh[0], a[0]);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = __fmul_rn(lv.dd[i], a[i]);
-  float x = 0.0f, y = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x = __fmaf_rn(lv.kh[i], a[i], x);
-    y = __fmaf_rn(lv.qh[i], a[i], y);
+  for (int i = 1; i < 4; ++i) {
+    xp = fma2(lv.kh[i], a[i], xp);
+    yp = fma2(lv.qh[i], a[i], yp);
   }
-#pragma unroll
-  for (int off = 8; off >= 1; off >>= 1) {
-    x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
-    y = __fadd_rn(y, __shfl_xor_sync(0xffffffffu, y, off));
-  }
-  const float u = __fmul_rn(beta, __fsub_rn(vv, x));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = __fmaf_rn(lv.kh[i], u, a[i]);
-  s.x = pack_bf16x2(a[0], a[1]);
-  s.y = pack_bf16x2(a[2], a[3]);
-  s.z = pack_bf16x2(a[4], a[5]);
-  s.w = pack_bf16x2(a[6], a[7]);
+  float u, y;
+  row_reduce(xp, yp, j, beta, vv, u, y);
+  const f32x2 uu = pk2(u, u);
+  s.x = f32x2_to_bf16x2(fma2(lv.kh[0], uu, a[0]));
+  s.y = f32x2_to_bf16x2(fma2(lv.kh[1], uu, a[1]));
+  s.z = f32x2_to_bf16x2(fma2(lv.kh[2], uu, a[2]));
+  s.w = f32x2_to_bf16x2(fma2(lv.kh[3], uu, a[3]));
   return __fmul_rn(scale, __fmaf_rn(u, kappa, y));
 }
 

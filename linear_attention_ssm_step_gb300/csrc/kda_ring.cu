@@ -170,17 +170,17 @@ __global__ void __launch_bounds__(NTHREADS)
   ok = __syncthreads_and(ok) != 0;
 
   const int r = lane >> 4, j = lane & 15;
-  float s[RP][8];
+  f32x2 s[RP][4];  // the lane's 8 keys of each of its rows, fp32
 #pragma unroll
   for (int pp = 0; pp < RP; ++pp) {
     const uint4 w = *reinterpret_cast<const uint4*>(st + (warp * RW + 2 * pp + r) * KD + j * 8);
-    unpack_bf16x2(w.x, s[pp][0], s[pp][1]);
-    unpack_bf16x2(w.y, s[pp][2], s[pp][3]);
-    unpack_bf16x2(w.z, s[pp][4], s[pp][5]);
-    unpack_bf16x2(w.w, s[pp][6], s[pp][7]);
+    s[pp][0] = bf16x2_to_f32x2(w.x);
+    s[pp][1] = bf16x2_to_f32x2(w.y);
+    s[pp][2] = bf16x2_to_f32x2(w.z);
+    s[pp][3] = bf16x2_to_f32x2(w.w);
   }
 
-  // Replay the live history in chunks.
+  // Replay the live history in chunks: s <- exp(G_j - G_{j-1}) s + k_j u_j[v].
   for (int j0 = 0; j0 < hist; j0 += HC) {
     const int nj = min(HC, hist - j0);
     __syncthreads();  // previous chunk consumed
@@ -197,17 +197,17 @@ __global__ void __launch_bounds__(NTHREADS)
     }
     __syncthreads();
     for (int jj = 0; jj < nj; ++jj) {
-      float kr[8], dr[8];
       const float4* k4 = reinterpret_cast<const float4*>(hk + jj * KD + j * 8);
       const float4* d4 = reinterpret_cast<const float4*>(hd + jj * KD + j * 8);
       const float4 ka = k4[0], kb = k4[1], da = d4[0], db = d4[1];
-      kr[0] = ka.x; kr[1] = ka.y; kr[2] = ka.z; kr[3] = ka.w; kr[4] = kb.x; kr[5] = kb.y; kr[6] = kb.z; kr[7] = kb.w;
-      dr[0] = da.x; dr[1] = da.y; dr[2] = da.z; dr[3] = da.w; dr[4] = db.x; dr[5] = db.y; dr[6] = db.z; dr[7] = db.w;
+      const f32x2 kr[4] = {pk2(ka.x, ka.y), pk2(ka.z, ka.w), pk2(kb.x, kb.y), pk2(kb.z, kb.w)};
+      const f32x2 dr[4] = {pk2(da.x, da.y), pk2(da.z, da.w), pk2(db.x, db.y), pk2(db.z, db.w)};
 #pragma unroll
       for (int pp = 0; pp < RP; ++pp) {
         const float uv = hu[jj * TV + warp * RW + 2 * pp + r];
+        const f32x2 uu = pk2(uv, uv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s[pp][i] = __fmaf_rn(kr[i], uv, __fmul_rn(dr[i], s[pp][i]));
+        for (int i = 0; i < 4; ++i) s[pp][i] = fma2(kr[i], uu, mul2(dr[i], s[pp][i]));
       }
     }
   }
@@ -216,15 +216,15 @@ __global__ void __launch_bounds__(NTHREADS)
 #pragma unroll
     for (int pp = 0; pp < RP; ++pp) {
       uint4 w;
-      w.x = pack_bf16x2(s[pp][0], s[pp][1]);
-      w.y = pack_bf16x2(s[pp][2], s[pp][3]);
-      w.z = pack_bf16x2(s[pp][4], s[pp][5]);
-      w.w = pack_bf16x2(s[pp][6], s[pp][7]);
+      w.x = f32x2_to_bf16x2(s[pp][0]);
+      w.y = f32x2_to_bf16x2(s[pp][1]);
+      w.z = f32x2_to_bf16x2(s[pp][2]);
+      w.w = f32x2_to_bf16x2(s[pp][3]);
       *reinterpret_cast<uint4*>(st + (warp * RW + 2 * pp + r) * KD + j * 8) = w;
-      unpack_bf16x2(w.x, s[pp][0], s[pp][1]);
-      unpack_bf16x2(w.y, s[pp][2], s[pp][3]);
-      unpack_bf16x2(w.z, s[pp][4], s[pp][5]);
-      unpack_bf16x2(w.w, s[pp][6], s[pp][7]);
+      s[pp][0] = bf16x2_to_f32x2(w.x);
+      s[pp][1] = bf16x2_to_f32x2(w.y);
+      s[pp][2] = bf16x2_to_f32x2(w.z);
+      s[pp][3] = bf16x2_to_f32x2(w.w);
     }
     if constexpr (BULK) {
       fence_proxy_async_smem();
@@ -238,6 +238,9 @@ __global__ void __launch_bounds__(NTHREADS)
       for (int i = lane; i < RW * KD; i += 32) gst[i] = sst[i];
     }
   }
+
+  // The new tokens, state kept in fp32: a = D s; u~ = bf16(beta (v - a . k~));
+  // s <- a + k~ u~; o = scale (a . q_hat + u~ (k~ . q_hat)).
   for (int t = 0; t < T; ++t) {
     LaneVecs lv;
     load_lane_vecs(ts, t, j, lv);
@@ -245,23 +248,21 @@ __global__ void __launch_bounds__(NTHREADS)
 #pragma unroll
     for (int pp = 0; pp < RP; ++pp) {
       const int row = warp * RW + 2 * pp + r;
-      float a[8];
+      f32x2 a[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = __fmul_rn(lv.dd[i], s[pp][i]);
-      float x = 0.0f, y = 0.0f;
+      for (int i = 0; i < 4; ++i) a[i] = mul2(lv.dd[i], s[pp][i]);
+      f32x2 xp = mul2(lv.kh[0], a[0]), yp = mul2(lv.qh[0], a[0]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x = __fmaf_rn(lv.kh[i], a[i], x);
-        y = __fmaf_rn(lv.qh[i], a[i], y);
+      for (int i = 1; i < 4; ++i) {
+        xp = fma2(lv.kh[i], a[i], xp);
+        yp = fma2(lv.qh[i], a[i], yp);
       }
+      float u, y;
+      row_reduce(xp, yp, j, beta, ts.vrow[t * TV + row], u, y);
+      u = round_bf16(u);
+      const f32x2 uu = pk2(u, u);
 #pragma unroll
-      for (int off = 8; off >= 1; off >>= 1) {
-        x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
-        y = __fadd_rn(y, __shfl_xor_sync(0xffffffffu, y, off));
-      }
-      const float u = round_bf16(__fmul_rn(beta, __fsub_rn(ts.vrow[t * TV + row], x)));
-#pragma unroll
-      for (int i = 0; i < 8; ++i) s[pp][i] = __fmaf_rn(lv.kh[i], u, a[i]);
+      for (int i = 0; i < 4; ++i) s[pp][i] = fma2(lv.kh[i], uu, a[i]);
       if (j == 0) {
         urow[t * TV + row] = u;
         orow[t * TV + row] = ok ? __fmul_rn(p.scale, __fmaf_rn(u, kappa, y)) : 0.0f;

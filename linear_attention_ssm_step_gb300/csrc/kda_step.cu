@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(NTHREADS) kda_step_kernel(const kda_params p, 
         const int row = warp * RW + 2 * pp + r;
         uint4* sp = reinterpret_cast<uint4*>(st + row * KD + j * 8);
         uint4 s = *sp;
-        const float o = row_step(s, lv, beta, kappa, ts.vrow[row], p.scale);
+        const float o = row_step(s, lv, j, beta, kappa, ts.vrow[row], p.scale);
         *sp = s;
         if (j == 0) orow[row] = o;
       }
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(NTHREADS) kda_step_kernel(const kda_params p, 
 #pragma unroll
         for (int pp = 0; pp < RP; ++pp) {
           const int row = warp * RW + 2 * pp + r;
-          const float o = row_step(s[pp], lv, beta, kappa, ts.vrow[t * TV + row], p.scale);
+          const float o = row_step(s[pp], lv, j, beta, kappa, ts.vrow[t * TV + row], p.scale);
           if (j == 0) orow[t * TV + row] = o;
         }
       }

@@ -1,0 +1,51 @@
+"""Run one library call on a standard synthetic workload a few times, for
+profilers (Nsight Compute) that need a short, clean stream of launches.
+
+  python -m linear_attention_ssm_step_gb300.profile_case decode 512
+  python -m linear_attention_ssm_step_gb300.profile_case verify 512 --T 8
+  python -m linear_attention_ssm_step_gb300.profile_case ring 512 --T 8 --fold 0.5
+
+Each call is launched --reps times (default 3) on the same inputs, with a
+device synchronize after each; nothing is timed here.
+"""
+
+import argparse
+
+import torch
+
+from . import kda, workloads
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("call", choices=["decode", "verify", "ring"])
+    ap.add_argument("B", type=int)
+    ap.add_argument("--T", type=int, default=8)
+    ap.add_argument("--fold", type=float, default=0.0)
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--config", type=int, default=-1)
+    a = ap.parse_args()
+    dev = torch.device("cuda:0")
+    kda.load_library()
+    if a.call == "decode":
+        w = workloads.decode_inputs(a.B, a.B + 128, seed=2, layout="fused", inactive_frac=0.05).to(dev)
+        fn = lambda: kda.kda_decode(w.state, w.state_indices, w.q, w.k, w.v, w.g_raw, w.beta_logit,  # noqa: E731
+                                    w.A_log, w.dt_bias, config_override=a.config)
+    elif a.call == "verify":
+        w = workloads.decode_inputs(a.B, a.B + 64, seed=3, T=a.T).to(dev)
+        fn = lambda: kda.kda_verify(w.state, w.state_indices, w.q, w.k, w.v, w.g_raw, w.beta_logit,  # noqa: E731
+                                    w.A_log, w.dt_bias, config_override=a.config)
+    else:
+        w = workloads.ring_inputs(a.B, a.B + 64, T=a.T, W=32, flush_min=9, fold_frac=a.fold, seed=4).to(dev)
+        r = w.ring
+        fn = lambda: kda.kda_verify_ring(w.state, w.state_indices, w.q, w.k, w.v, w.g_raw,  # noqa: E731
+                                         w.beta_logit, w.A_log, w.dt_bias, r["k_cache"], r["u_cache"],
+                                         r["g_cache"], r["hist_len"], r["flush_min"], config_override=a.config)
+    for _ in range(a.reps):
+        fn()
+        torch.cuda.synchronize()
+    print(f"{a.call} B={a.B} ran {a.reps} times")
+
+
+if __name__ == "__main__":
+    main()
