@@ -163,11 +163,15 @@ typedef struct {
  */
 kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params* r, void* stream);
 
-/* Launch configurations: index -> rows of V per CTA (tile) for kda_decode/kda_verify. */
+/* Launch configurations: index -> rows of V per CTA (tile). kda_params.config_override
+   takes an index; kda_verify_ring caps the tile at 64 rows. */
 int32_t kda_num_configs(void);
 int32_t kda_config_tile_v(int32_t config);
-/* The configuration the library picks for B rows and T tokens (-1 if B < 0 or T out of range). */
+/* The configuration kda_decode (T = 1) and kda_verify (T > 1) pick for B rows
+   (-1 if B < 0 or T is outside 1..KDA_MAX_T). */
 int32_t kda_select_config(int32_t B, int32_t T);
+/* The configuration kda_verify_ring picks for B rows and T tokens (-1 as above). */
+int32_t kda_select_ring_config(int32_t B, int32_t T);
 
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 const char* kda_last_error(void);

@@ -27,7 +27,7 @@ kda_status ok() {
 }
 
 // Rows of V per CTA, by configuration index.
-constexpr int kTileV[] = {8, 16, 32, 64, 128};
+constexpr int kTileV[] = {16, 32, 64, 128};
 constexpr int kNumConfigs = sizeof(kTileV) / sizeof(kTileV[0]);
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -109,6 +109,11 @@ int pick_tile(const kda_params* p, int T) {
   return kTileV[cfg];
 }
 
+int pick_ring_tile(const kda_params* p, int T) {
+  const int cfg = p->config_override >= 0 ? p->config_override : kda_select_ring_config(p->B, T);
+  return kTileV[cfg] > 64 ? 64 : kTileV[cfg];
+}
+
 }  // namespace
 
 extern "C" {
@@ -120,17 +125,30 @@ int32_t kda_config_tile_v(int32_t config) {
   return kTileV[config];
 }
 
-// Smaller tiles for small batches, so that B * H * (128 / TV) CTAs still cover
-// the 152 SMs of a GB300 several times over; whole-head tiles once a batch
-// fills the machine on its own.
+// Launch-configuration policy, measured on GB300 with L2 cold between calls
+// (CUDA-graph replays): small batches take smaller tiles, so that
+// B * H * (128 / TV) CTAs still cover the 152 SMs, and whole-head tiles
+// once a batch fills the machine on its own. T = 1 and T > 1 differ because
+// a verify CTA does T times the work per byte of state.
 int32_t kda_select_config(int32_t B, int32_t T) {
   if (B < 0 || T < 1 || T > KDA_MAX_T) return -1;
-  const long long heads = (long long)B * 12;
-  if (heads <= 12) return 0;    // 8 rows
-  if (heads <= 96) return 1;    // 16 rows
-  if (heads <= 384) return 2;   // 32 rows
-  if (heads <= 1536) return 3;  // 64 rows
-  return 4;                     // 128 rows
+  if (T == 1) {
+    if (B <= 16) return 1;  // 32 rows
+    if (B <= 32) return 2;  // 64 rows
+    return 3;               // 128 rows
+  }
+  if (B <= 2) return 0;  // 16 rows
+  if (B <= 8) return 1;  // 32 rows
+  return 3;              // 128 rows
+}
+
+// The ring kernel keeps each row in fp32 across the call and caps its tile at
+// 64 rows; its own policy, same measurements.
+int32_t kda_select_ring_config(int32_t B, int32_t T) {
+  if (B < 0 || T < 1 || T > KDA_MAX_T) return -1;
+  if (B <= 2) return 0;   // 16 rows
+  if (B <= 64) return 1;  // 32 rows
+  return 2;               // 64 rows
 }
 
 const char* kda_last_error(void) { return g_err; }
@@ -178,7 +196,7 @@ kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params
       return fail(KDA_EINVAL, "ring slot strides must keep slots 16-byte aligned");
   }
   if (p->B == 0) return ok();
-  cudaError_t e = kda::launch_ring(*p, T, *r, pick_tile(p, T), bulk, static_cast<cudaStream_t>(stream));
+  cudaError_t e = kda::launch_ring(*p, T, *r, pick_ring_tile(p, T), bulk, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify_ring launch: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -4,9 +4,11 @@
 // 256 bytes per row, 32 KB per head. A CTA of 128 threads owns one
 // (batch row, head, tile of TV value rows). Each warp stages its TV/4 rows in
 // shared memory with one bulk asynchronous copy (cp.async.bulk, completion on
-// an mbarrier), and writes them back with one bulk store. Inside a warp, 16
-// lanes share a row: lane j holds keys 8j..8j+7 (16 bytes, one bf16x8
-// vector), so a warp works on two rows at a time and reduces across 16 lanes.
+// an mbarrier), and writes them back with one bulk store. Inside a warp, 8
+// lanes share a row and a warp works on 4 rows at a time: lane j (= lane & 7)
+// of a row holds keys 8j..8j+7 and 64+8j..64+8j+7 (two bf16x8 vectors), so
+// that the 8 lanes of a row read 128 consecutive bytes per shared-memory
+// access (no bank conflicts), and the row's dot products reduce over 8 lanes.
 //
 // Sources: "feat(kda): add packed-input CuTe decode kernel" (PR #4417),
 // "Kernel design" (fused output o = (d*h).q + u*(k.q), packed bf16 state with
@@ -281,79 +283,142 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(f32x2 v) {
   return pack_bf16x2(lo, hi);
 }
 
-// A lane's 8 keys of one token's vectors, in registers, as 4 pairs each.
+// Lane layout of a row: LPR lanes per row, ROWS_PER_WARP rows per warp access.
+constexpr int LPR = 8;
+constexpr int ROWS_PER_WARP = 32 / LPR;
+
+// Element offset of lane j's first and second 8-key chunk within a row.
+__device__ __forceinline__ int chunk0(int j) { return 8 * j; }
+__device__ __forceinline__ int chunk1(int j) { return 64 + 8 * j; }
+
+// A lane's 16 keys of one token's vectors, in registers, as 8 pairs each:
+// pairs 0..3 are keys 8j..8j+7, pairs 4..7 are keys 64+8j..64+8j+7.
 struct LaneVecs {
-  f32x2 kh[4], qh[4], dd[4];
+  f32x2 kh[8], qh[8], dd[8];
 };
 
-__device__ __forceinline__ void load_lane_vecs(const TokenSmem& ts, int t, int j, LaneVecs& lv) {
-  const float4* k4 = reinterpret_cast<const float4*>(ts.kh + t * KD + j * 8);
-  const float4* q4 = reinterpret_cast<const float4*>(ts.qh + t * KD + j * 8);
-  const float4* d4 = reinterpret_cast<const float4*>(ts.dd + t * KD + j * 8);
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float4 a = k4[i], q = q4[i], d = d4[i];
-    lv.kh[2 * i] = pk2(a.x, a.y);
-    lv.kh[2 * i + 1] = pk2(a.z, a.w);
-    lv.qh[2 * i] = pk2(q.x, q.y);
-    lv.qh[2 * i + 1] = pk2(q.z, q.w);
-    lv.dd[2 * i] = pk2(d.x, d.y);
-    lv.dd[2 * i + 1] = pk2(d.z, d.w);
-  }
+__device__ __forceinline__ void load_pairs8(const float* v, int j, f32x2 (&out)[8]) {
+  const float4* a = reinterpret_cast<const float4*>(v + chunk0(j));
+  const float4* b = reinterpret_cast<const float4*>(v + chunk1(j));
+  const float4 a0 = a[0], a1 = a[1], b0 = b[0], b1 = b[1];
+  out[0] = pk2(a0.x, a0.y);
+  out[1] = pk2(a0.z, a0.w);
+  out[2] = pk2(a1.x, a1.y);
+  out[3] = pk2(a1.z, a1.w);
+  out[4] = pk2(b0.x, b0.y);
+  out[5] = pk2(b0.z, b0.w);
+  out[6] = pk2(b1.x, b1.y);
+  out[7] = pk2(b1.z, b1.w);
 }
 
-// The two dot products of a row, reduced over the row's 16 lanes (lane j of
-// the row, j = lane & 15), and the row's u. Transposed butterfly: at the
-// first level the lanes with j < 8 keep the x half and the others the y half,
-// so each later level reduces one value instead of two; a last exchange hands
-// u (computed where x is complete) and y to every lane. 5 shuffles instead of
-// 8, and every lane of the row ends with the same u and y: each level adds the
-// same two values, in either order, in both lanes.
-__device__ __forceinline__ void row_reduce(f32x2 xp, f32x2 yp, int j, float beta, float vv, float& u, float& y) {
-  float x0, x1, y0, y1;
-  upk2(xp, x0, x1);
-  upk2(yp, y0, y1);
-  const float x = __fadd_rn(x0, x1), yy = __fadd_rn(y0, y1);
-  const bool upper = (j & 8) != 0;
-  float keep = upper ? yy : x;
-  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, upper ? x : yy, 8));
-  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, keep, 4));
+__device__ __forceinline__ void load_lane_vecs(const TokenSmem& ts, int t, int j, LaneVecs& lv) {
+  load_pairs8(ts.kh + t * KD, j, lv.kh);
+  load_pairs8(ts.qh + t * KD, j, lv.qh);
+  load_pairs8(ts.dd + t * KD, j, lv.dd);
+}
+
+// A row's 16 keys of lane j, as two bf16x8 vectors.
+struct RowBf16 {
+  uint4 a, b;
+};
+
+__device__ __forceinline__ RowBf16 load_row_bf16(const uint16_t* row, int j) {
+  RowBf16 r;
+  r.a = *reinterpret_cast<const uint4*>(row + chunk0(j));
+  r.b = *reinterpret_cast<const uint4*>(row + chunk1(j));
+  return r;
+}
+
+__device__ __forceinline__ void store_row_bf16(uint16_t* row, int j, const RowBf16& r) {
+  *reinterpret_cast<uint4*>(row + chunk0(j)) = r.a;
+  *reinterpret_cast<uint4*>(row + chunk1(j)) = r.b;
+}
+
+__device__ __forceinline__ void row_to_f32(const RowBf16& r, f32x2 (&s)[8]) {
+  s[0] = bf16x2_to_f32x2(r.a.x);
+  s[1] = bf16x2_to_f32x2(r.a.y);
+  s[2] = bf16x2_to_f32x2(r.a.z);
+  s[3] = bf16x2_to_f32x2(r.a.w);
+  s[4] = bf16x2_to_f32x2(r.b.x);
+  s[5] = bf16x2_to_f32x2(r.b.y);
+  s[6] = bf16x2_to_f32x2(r.b.z);
+  s[7] = bf16x2_to_f32x2(r.b.w);
+}
+
+__device__ __forceinline__ RowBf16 row_to_bf16(const f32x2 (&s)[8]) {
+  RowBf16 r;
+  r.a.x = f32x2_to_bf16x2(s[0]);
+  r.a.y = f32x2_to_bf16x2(s[1]);
+  r.a.z = f32x2_to_bf16x2(s[2]);
+  r.a.w = f32x2_to_bf16x2(s[3]);
+  r.b.x = f32x2_to_bf16x2(s[4]);
+  r.b.y = f32x2_to_bf16x2(s[5]);
+  r.b.z = f32x2_to_bf16x2(s[6]);
+  r.b.w = f32x2_to_bf16x2(s[7]);
+  return r;
+}
+
+// Lane j's partial dot products x = a . k_hat and y = a . q_hat over its 16
+// keys (two accumulator chains each, summed in a fixed order).
+__device__ __forceinline__ void partial_dots(const f32x2 (&a)[8], const LaneVecs& lv, float& x, float& y) {
+  f32x2 xa = mul2(lv.kh[0], a[0]), xb = mul2(lv.kh[1], a[1]);
+  f32x2 ya = mul2(lv.qh[0], a[0]), yb = mul2(lv.qh[1], a[1]);
+#pragma unroll
+  for (int i = 2; i < 8; i += 2) {
+    xa = fma2(lv.kh[i], a[i], xa);
+    xb = fma2(lv.kh[i + 1], a[i + 1], xb);
+    ya = fma2(lv.qh[i], a[i], ya);
+    yb = fma2(lv.qh[i + 1], a[i + 1], yb);
+  }
+  float x0, x1, x2, x3, y0, y1, y2, y3;
+  upk2(xa, x0, x1);
+  upk2(xb, x2, x3);
+  upk2(ya, y0, y1);
+  upk2(yb, y2, y3);
+  x = __fadd_rn(__fadd_rn(x0, x2), __fadd_rn(x1, x3));
+  y = __fadd_rn(__fadd_rn(y0, y2), __fadd_rn(y1, y3));
+}
+
+// The row's x and y reduced over its 8 lanes, and its u = beta (v - x).
+// Transposed butterfly: at the first level lanes j < 4 keep the x half and
+// lanes j >= 4 the y half, so the next two levels reduce one value each; a
+// last exchange hands u (computed where x is complete) and y to every lane.
+// 4 shuffles for the 4 rows of a warp access. Every lane of the row ends with
+// the same u and y: each level adds the same two values, in either order, in
+// both lanes.
+__device__ __forceinline__ void row_reduce(float x, float y, int j, float beta, float vv, float& u, float& y_out) {
+  const bool upper = (j & 4) != 0;
+  float keep = upper ? y : x;
+  keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, upper ? x : y, 4));
   keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, keep, 2));
   keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, keep, 1));
-  // lanes j < 8 hold x, lanes j >= 8 hold y
+  // lanes j < 4 hold x, lanes j >= 4 hold y
   const float mine = upper ? keep : __fmul_rn(beta, __fsub_rn(vv, keep));
-  const float got = __shfl_xor_sync(0xffffffffu, mine, 8);
+  const float got = __shfl_xor_sync(0xffffffffu, mine, 4);
   u = upper ? got : mine;
-  y = upper ? keep : got;
+  y_out = upper ? keep : got;
 }
 
-// One gated delta-rule step on one state row, shared by 16 lanes (lane j holds
-// keys 8j..8j+7 as four bf16x2 words). For the row's value index v:
-//   a = d * s;  x = a . k_hat;  y = a . q_hat        (reduced over the 16 lanes)
+// One gated delta-rule step on one bf16 state row, shared by its 8 lanes. For
+// the row's value index v:
+//   a = d * s;  x = a . k_hat;  y = a . q_hat        (reduced over the 8 lanes)
 //   u = beta (v - x);  s <- bf16(a + k_hat u);  o = scale (y + u kappa)
 // The output uses the fused form o = (D s) . q_hat + u (k_hat . q_hat), which
 // equals s_new . q_hat before rounding.
-__device__ __forceinline__ float row_step(uint4& s, const LaneVecs& lv, int j, float beta, float kappa, float vv,
-                                          float scale) {
-  f32x2 a[4];
-  a[0] = mul2(lv.dd[0], bf16x2_to_f32x2(s.x));
-  a[1] = mul2(lv.dd[1], bf16x2_to_f32x2(s.y));
-  a[2] = mul2(lv.dd[2], bf16x2_to_f32x2(s.z));
-  a[3] = mul2(lv.dd[3], bf16x2_to_f32x2(s.w));
-  f32x2 xp = mul2(lv.kh[0], a[0]), yp = mul2(lv.qh[0], a[0]);
+__device__ __forceinline__ float row_step(RowBf16& row, const LaneVecs& lv, int j, float beta, float kappa,
+                                          float vv, float scale) {
+  f32x2 a[8];
+  row_to_f32(row, a);
 #pragma unroll
-  for (int i = 1; i < 4; ++i) {
-    xp = fma2(lv.kh[i], a[i], xp);
-    yp = fma2(lv.qh[i], a[i], yp);
-  }
-  float u, y;
-  row_reduce(xp, yp, j, beta, vv, u, y);
+  for (int i = 0; i < 8; ++i) a[i] = mul2(lv.dd[i], a[i]);
+  float x, y, u, yr;
+  partial_dots(a, lv, x, y);
+  row_reduce(x, y, j, beta, vv, u, yr);
   const f32x2 uu = pk2(u, u);
-  s.x = f32x2_to_bf16x2(fma2(lv.kh[0], uu, a[0]));
-  s.y = f32x2_to_bf16x2(fma2(lv.kh[1], uu, a[1]));
-  s.z = f32x2_to_bf16x2(fma2(lv.kh[2], uu, a[2]));
-  s.w = f32x2_to_bf16x2(fma2(lv.kh[3], uu, a[3]));
-  return __fmul_rn(scale, __fmaf_rn(u, kappa, y));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = fma2(lv.kh[i], uu, a[i]);
+  row = row_to_bf16(a);
+  return __fmul_rn(scale, __fmaf_rn(u, kappa, yr));
 }
 
 }  // namespace kda

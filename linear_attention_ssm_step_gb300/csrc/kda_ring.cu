@@ -7,7 +7,7 @@
 // exp(G_P - G_j), and fold the ring into the checkpoint once hist_len reaches
 // flush_min.
 //
-// One CTA (128 threads) per (batch row, head, tile of TV <= 64 value rows):
+// One CTA (128 threads) per (batch row, head, tile of TV = 16, 32 or 64 value rows):
 //   1. slot lookup, hist_len check (outside [0, W]: error bit, skip);
 //   2. bulk copy of the checkpoint rows into shared memory (per warp);
 //   3. per-token prologue, then per channel: k~ = bf16(k_hat),
@@ -49,9 +49,9 @@ __device__ __forceinline__ float round_bf16(float x) { return bf16_bits_to_float
 template <int TV, bool BULK>
 __global__ void __launch_bounds__(NTHREADS)
     kda_ring_kernel(const kda_params p, const kda_ring_params rp, const int T, const int tiles) {
-  static_assert(TV % 8 == 0 && TV >= 8 && TV <= 64, "ring tile must be 8..64 rows");
-  constexpr int RW = TV / NWARPS;
-  constexpr int RP = RW / 2;
+  static_assert(TV % 16 == 0 && TV >= 16 && TV <= 64, "ring tile must be 16, 32 or 64 rows");
+  constexpr int RW = TV / NWARPS;         // rows per warp
+  constexpr int RQ = RW / ROWS_PER_WARP;  // 4-row groups per warp
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -169,16 +169,10 @@ __global__ void __launch_bounds__(NTHREADS)
   // also publishes kappa.
   ok = __syncthreads_and(ok) != 0;
 
-  const int r = lane >> 4, j = lane & 15;
-  f32x2 s[RP][4];  // the lane's 8 keys of each of its rows, fp32
+  const int r = lane / LPR, j = lane % LPR;  // row within a 4-row group, lane within the row
+  f32x2 s[RQ][8];  // the lane's 16 keys of each of its rows, fp32
 #pragma unroll
-  for (int pp = 0; pp < RP; ++pp) {
-    const uint4 w = *reinterpret_cast<const uint4*>(st + (warp * RW + 2 * pp + r) * KD + j * 8);
-    s[pp][0] = bf16x2_to_f32x2(w.x);
-    s[pp][1] = bf16x2_to_f32x2(w.y);
-    s[pp][2] = bf16x2_to_f32x2(w.z);
-    s[pp][3] = bf16x2_to_f32x2(w.w);
-  }
+  for (int q = 0; q < RQ; ++q) row_to_f32(load_row_bf16(st + (warp * RW + ROWS_PER_WARP * q + r) * KD, j), s[q]);
 
   // Replay the live history in chunks: s <- exp(G_j - G_{j-1}) s + k_j u_j[v].
   for (int j0 = 0; j0 < hist; j0 += HC) {
@@ -197,34 +191,25 @@ __global__ void __launch_bounds__(NTHREADS)
     }
     __syncthreads();
     for (int jj = 0; jj < nj; ++jj) {
-      const float4* k4 = reinterpret_cast<const float4*>(hk + jj * KD + j * 8);
-      const float4* d4 = reinterpret_cast<const float4*>(hd + jj * KD + j * 8);
-      const float4 ka = k4[0], kb = k4[1], da = d4[0], db = d4[1];
-      const f32x2 kr[4] = {pk2(ka.x, ka.y), pk2(ka.z, ka.w), pk2(kb.x, kb.y), pk2(kb.z, kb.w)};
-      const f32x2 dr[4] = {pk2(da.x, da.y), pk2(da.z, da.w), pk2(db.x, db.y), pk2(db.z, db.w)};
+      f32x2 kr[8], dr[8];
+      load_pairs8(hk + jj * KD, j, kr);
+      load_pairs8(hd + jj * KD, j, dr);
 #pragma unroll
-      for (int pp = 0; pp < RP; ++pp) {
-        const float uv = hu[jj * TV + warp * RW + 2 * pp + r];
+      for (int q = 0; q < RQ; ++q) {
+        const float uv = hu[jj * TV + warp * RW + ROWS_PER_WARP * q + r];
         const f32x2 uu = pk2(uv, uv);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s[pp][i] = fma2(kr[i], uu, mul2(dr[i], s[pp][i]));
+        for (int i = 0; i < 8; ++i) s[q][i] = fma2(kr[i], uu, mul2(dr[i], s[q][i]));
       }
     }
   }
 
   if (fold && ok) {
 #pragma unroll
-    for (int pp = 0; pp < RP; ++pp) {
-      uint4 w;
-      w.x = f32x2_to_bf16x2(s[pp][0]);
-      w.y = f32x2_to_bf16x2(s[pp][1]);
-      w.z = f32x2_to_bf16x2(s[pp][2]);
-      w.w = f32x2_to_bf16x2(s[pp][3]);
-      *reinterpret_cast<uint4*>(st + (warp * RW + 2 * pp + r) * KD + j * 8) = w;
-      s[pp][0] = bf16x2_to_f32x2(w.x);
-      s[pp][1] = bf16x2_to_f32x2(w.y);
-      s[pp][2] = bf16x2_to_f32x2(w.z);
-      s[pp][3] = bf16x2_to_f32x2(w.w);
+    for (int q = 0; q < RQ; ++q) {
+      const RowBf16 w = row_to_bf16(s[q]);
+      store_row_bf16(st + (warp * RW + ROWS_PER_WARP * q + r) * KD, j, w);
+      row_to_f32(w, s[q]);
     }
     if constexpr (BULK) {
       fence_proxy_async_smem();
@@ -246,26 +231,21 @@ __global__ void __launch_bounds__(NTHREADS)
     load_lane_vecs(ts, t, j, lv);
     const float beta = ts.beta[t], kappa = ts.kappa[t];
 #pragma unroll
-    for (int pp = 0; pp < RP; ++pp) {
-      const int row = warp * RW + 2 * pp + r;
-      f32x2 a[4];
+    for (int q = 0; q < RQ; ++q) {
+      const int row = warp * RW + ROWS_PER_WARP * q + r;
+      f32x2 a[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = mul2(lv.dd[i], s[pp][i]);
-      f32x2 xp = mul2(lv.kh[0], a[0]), yp = mul2(lv.qh[0], a[0]);
-#pragma unroll
-      for (int i = 1; i < 4; ++i) {
-        xp = fma2(lv.kh[i], a[i], xp);
-        yp = fma2(lv.qh[i], a[i], yp);
-      }
-      float u, y;
-      row_reduce(xp, yp, j, beta, ts.vrow[t * TV + row], u, y);
+      for (int i = 0; i < 8; ++i) a[i] = mul2(lv.dd[i], s[q][i]);
+      float x, y, u, yr;
+      partial_dots(a, lv, x, y);
+      row_reduce(x, y, j, beta, ts.vrow[t * TV + row], u, yr);
       u = round_bf16(u);
       const f32x2 uu = pk2(u, u);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) s[pp][i] = fma2(lv.kh[i], uu, a[i]);
+      for (int i = 0; i < 8; ++i) s[q][i] = fma2(lv.kh[i], uu, a[i]);
       if (j == 0) {
         urow[t * TV + row] = u;
-        orow[t * TV + row] = ok ? __fmul_rn(p.scale, __fmaf_rn(u, kappa, y)) : 0.0f;
+        orow[t * TV + row] = ok ? __fmul_rn(p.scale, __fmaf_rn(u, kappa, yr)) : 0.0f;
       }
     }
   }
@@ -361,7 +341,6 @@ cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, in
                         cudaStream_t s) {
   if (tile_v > 64) tile_v = 64;
   switch (tile_v) {
-    case 8: return bulk ? launch_ring_one<8, true>(p, T, r, s) : launch_ring_one<8, false>(p, T, r, s);
     case 16: return bulk ? launch_ring_one<16, true>(p, T, r, s) : launch_ring_one<16, false>(p, T, r, s);
     case 32: return bulk ? launch_ring_one<32, true>(p, T, r, s) : launch_ring_one<32, false>(p, T, r, s);
     case 64: return bulk ? launch_ring_one<64, true>(p, T, r, s) : launch_ring_one<64, false>(p, T, r, s);

@@ -10,8 +10,9 @@
 //      the prologue.
 //   3. The CTA computes every token's prologue (q/k L2 norms, k.q, gate
 //      decay, beta) into shared memory, thread c owning key channel c.
-//   4. Each warp waits for its rows, applies the T steps (rows streamed from
-//      shared memory when T = 1; held in registers across tokens otherwise,
+//   4. Each warp waits for its rows, applies the T steps (8 lanes per row, 4
+//      rows per warp access; rows streamed from shared memory when T = 1,
+//      held in registers across tokens otherwise,
 //      rounded to bf16 after every token so that T tokens equal T decode
 //      calls bit for bit), writes the rows back to shared memory and starts
 //      one bulk store of them to HBM.
@@ -32,11 +33,14 @@ __host__ __device__ constexpr size_t step_smem_bytes(int TV, int T) {
          + (size_t)KDA_MAX_T * NWARPS * 3 * 4;  // reduction partials
 }
 
+// T = 1 kernels are capped at 85 registers so that six 128-thread CTAs (the
+// shared-memory limit of the 128-row tile) fit on an SM.
 template <int TV, bool BULK, bool MULTI>
-__global__ void __launch_bounds__(NTHREADS) kda_step_kernel(const kda_params p, const int T, const int tiles) {
-  static_assert(TV % 8 == 0 && TV >= 8 && TV <= KD, "tile must be a multiple of 8 rows");
-  constexpr int RW = TV / NWARPS;  // rows per warp
-  constexpr int RP = RW / 2;       // row pairs per warp
+__global__ void __launch_bounds__(NTHREADS, MULTI ? 1 : 6)
+    kda_step_kernel(const kda_params p, const int T, const int tiles) {
+  static_assert(TV % 16 == 0 && TV >= 16 && TV <= KD, "tile must be a multiple of 16 rows");
+  constexpr int RW = TV / NWARPS;        // rows per warp
+  constexpr int RQ = RW / ROWS_PER_WARP;  // 4-row groups per warp
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -98,41 +102,38 @@ __global__ void __launch_bounds__(NTHREADS) kda_step_kernel(const kda_params p, 
   } else {
     __syncwarp();
   }
-  const int r = lane >> 4, j = lane & 15;
+  const int r = lane / LPR, j = lane % LPR;  // row within a 4-row group, lane within the row
 
   if (ok) {
     if constexpr (!MULTI) {
       LaneVecs lv;
       load_lane_vecs(ts, 0, j, lv);
       const float beta = ts.beta[0], kappa = ts.kappa[0];
-#pragma unroll 4
-      for (int pp = 0; pp < RP; ++pp) {
-        const int row = warp * RW + 2 * pp + r;
-        uint4* sp = reinterpret_cast<uint4*>(st + row * KD + j * 8);
-        uint4 s = *sp;
+#pragma unroll 2
+      for (int q = 0; q < RQ; ++q) {
+        const int row = warp * RW + ROWS_PER_WARP * q + r;
+        RowBf16 s = load_row_bf16(st + row * KD, j);
         const float o = row_step(s, lv, j, beta, kappa, ts.vrow[row], p.scale);
-        *sp = s;
+        store_row_bf16(st + row * KD, j, s);
         if (j == 0) orow[row] = o;
       }
     } else {
-      uint4 s[RP];
+      RowBf16 s[RQ];
 #pragma unroll
-      for (int pp = 0; pp < RP; ++pp)
-        s[pp] = *reinterpret_cast<const uint4*>(st + (warp * RW + 2 * pp + r) * KD + j * 8);
+      for (int q = 0; q < RQ; ++q) s[q] = load_row_bf16(st + (warp * RW + ROWS_PER_WARP * q + r) * KD, j);
       for (int t = 0; t < T; ++t) {
         LaneVecs lv;
         load_lane_vecs(ts, t, j, lv);
         const float beta = ts.beta[t], kappa = ts.kappa[t];
 #pragma unroll
-        for (int pp = 0; pp < RP; ++pp) {
-          const int row = warp * RW + 2 * pp + r;
-          const float o = row_step(s[pp], lv, j, beta, kappa, ts.vrow[t * TV + row], p.scale);
+        for (int q = 0; q < RQ; ++q) {
+          const int row = warp * RW + ROWS_PER_WARP * q + r;
+          const float o = row_step(s[q], lv, j, beta, kappa, ts.vrow[t * TV + row], p.scale);
           if (j == 0) orow[t * TV + row] = o;
         }
       }
 #pragma unroll
-      for (int pp = 0; pp < RP; ++pp)
-        *reinterpret_cast<uint4*>(st + (warp * RW + 2 * pp + r) * KD + j * 8) = s[pp];
+      for (int q = 0; q < RQ; ++q) store_row_bf16(st + (warp * RW + ROWS_PER_WARP * q + r) * KD, j, s[q]);
     }
     if constexpr (BULK) {
       fence_proxy_async_smem();
@@ -180,7 +181,6 @@ static cudaError_t launch_tv(const kda_params& p, int T, bool bulk, cudaStream_t
 
 cudaError_t launch_step(const kda_params& p, int T, int tile_v, bool bulk, cudaStream_t s) {
   switch (tile_v) {
-    case 8: return launch_tv<8>(p, T, bulk, s);
     case 16: return launch_tv<16>(p, T, bulk, s);
     case 32: return launch_tv<32>(p, T, bulk, s);
     case 64: return launch_tv<64>(p, T, bulk, s);

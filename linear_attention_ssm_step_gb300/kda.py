@@ -65,6 +65,7 @@ EXPORTS = {
     "kda_num_configs": ([], ctypes.c_int32),
     "kda_config_tile_v": ([ctypes.c_int32], ctypes.c_int32),
     "kda_select_config": ([ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
+    "kda_select_ring_config": ([ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
     "kda_last_error": ([], ctypes.c_char_p),
 }
 
@@ -233,6 +234,10 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
 
 def kda_select_config(B, T=1):
     return load_library().kda_select_config(B, T)
+
+
+def kda_select_ring_config(B, T=8):
+    return load_library().kda_select_ring_config(B, T)
 
 
 def kda_num_configs():

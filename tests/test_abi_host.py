@@ -198,7 +198,7 @@ def test_ring_null_and_empty(lib):
 def test_config_table_and_selector(lib):
     n = kda.kda_num_configs()
     tiles = [kda.kda_config_tile_v(i) for i in range(n)]
-    assert tiles == sorted(tiles) and all(128 % t == 0 and t % 8 == 0 for t in tiles)
+    assert tiles == sorted(tiles) and all(128 % t == 0 and t % 16 == 0 for t in tiles)
     assert kda.kda_config_tile_v(-1) == -1 and kda.kda_config_tile_v(n) == -1
     assert kda.kda_select_config(-1, 1) == -1 and kda.kda_select_config(4, 0) == -1
     assert kda.kda_select_config(4, 17) == -1
@@ -208,6 +208,12 @@ def test_config_table_and_selector(lib):
         assert 0 <= c < n and c >= prev  # tiles never shrink as the batch grows
         prev = c
     assert kda.kda_config_tile_v(kda.kda_select_config(512, 1)) == 128
+    prev = 0
+    for B in (1, 2, 8, 16, 32, 64, 128, 512, 4096):
+        c = kda.kda_select_ring_config(B, 8)
+        assert 0 <= c < n and c >= prev and kda.kda_config_tile_v(c) <= 64
+        prev = c
+    assert kda.kda_select_ring_config(-1, 8) == -1 and kda.kda_select_ring_config(4, 17) == -1
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

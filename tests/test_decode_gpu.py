@@ -52,13 +52,13 @@ def test_decode_matches_oracle(dev, B, layout):
     run_and_check(w, dev)
 
 
-@pytest.mark.parametrize("config", range(5))
+@pytest.mark.parametrize("config", range(4))
 def test_every_config_gives_the_same_bits(dev, config):
     w = workloads.decode_inputs(9, 16, seed=7, layout="packed", inactive_frac=0.2)
     wd = w.to(dev)
     out = gpu_decode(wd, config_override=config)
     wd0 = w.to(dev)
-    out0 = gpu_decode(wd0, config_override=4)
+    out0 = gpu_decode(wd0, config_override=3)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
     assert torch.equal(wd.state.view(torch.int16), wd0.state.view(torch.int16))
