@@ -133,22 +133,21 @@ int32_t kda_config_tile_v(int32_t config) {
 int32_t kda_select_config(int32_t B, int32_t T) {
   if (B < 0 || T < 1 || T > KDA_MAX_T) return -1;
   if (T == 1) {
-    if (B <= 16) return 1;  // 32 rows
+    if (B <= 2) return 0;   // 16 rows
     if (B <= 32) return 2;  // 64 rows
     return 3;               // 128 rows
   }
-  if (B <= 2) return 0;  // 16 rows
-  if (B <= 8) return 1;  // 32 rows
-  return 3;              // 128 rows
+  if (B <= 2) return 0;   // 16 rows
+  if (B <= 16) return 1;  // 32 rows
+  return 3;               // 128 rows
 }
 
 // The ring kernel keeps each row in fp32 across the call and caps its tile at
 // 64 rows; its own policy, same measurements.
 int32_t kda_select_ring_config(int32_t B, int32_t T) {
   if (B < 0 || T < 1 || T > KDA_MAX_T) return -1;
-  if (B <= 2) return 0;   // 16 rows
-  if (B <= 64) return 1;  // 32 rows
-  return 2;               // 64 rows
+  if (B <= 2) return 0;  // 16 rows
+  return 2;              // 64 rows
 }
 
 const char* kda_last_error(void) { return g_err; }
