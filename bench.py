@@ -57,13 +57,17 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ------------------------------------------------------------------ helpers
 
+DECODE_SOURCES = ("include/kda.h", "linear_attention_ssm_step_gb300/csrc/kda_device.cuh",
+                  "linear_attention_ssm_step_gb300/csrc/kda_launch.h",
+                  "linear_attention_ssm_step_gb300/csrc/kda_step.cu")
+
+
 def kernel_source_hash():
-    """Hash of the CUDA sources; a profile summary taken from other sources is stale."""
+    """Hash of the sources the decode kernel is compiled from; a profile summary
+    taken from other sources is stale."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "linear_attention_ssm_step_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for rel in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
     return h.hexdigest()[:16]
 
 
