@@ -7,20 +7,35 @@
 // exp(G_P - G_j), and fold the ring into the checkpoint once hist_len reaches
 // flush_min.
 //
-// One CTA (128 threads) per (batch row, head, tile of TV = 16, 32 or 64 value rows):
-//   1. slot lookup, hist_len check (outside [0, W]: error bit, skip);
-//   2. bulk copy of the checkpoint rows into shared memory (per warp);
-//   3. per-token prologue, then per channel: k~ = bf16(k_hat),
-//      G_P = fp32(G_{P-1} + g), decay exp(G_P - G_{P-1}), k~ . q_hat;
-//   4. rows go to registers as fp32 and are replayed through the history in
-//      chunks of HC entries staged in shared memory:
-//      s <- exp(G_j - G_{j-1}) s + k_j u_j[v];
-//   5. fold (hist_len >= flush_min): rows are rounded to bf16, bulk-stored to
-//      the checkpoint and continue from the rounded values;
-//   6. the T tokens: a = D s; x = a . k~; y = a . q_hat; u~ = bf16(beta (v - x));
-//      s <- a + k~ u~; o = scale (y + u~ (k~ . q_hat)); outputs and this
-//      tile's rows of u~ written (rows no other CTA reads).
-// A second, stream-ordered kernel (one CTA per batch row) appends k~ and G_P
+// The step it computes, per (row, head): with base state S_b and token decays
+// d_t = exp(G_t - G_{t-1}),
+//   u~_t = bf16(beta_t (v_t - (D_t S_{t-1})^T k~_t)),  S_t = D_t S_{t-1} + k~_t u~_t^T,
+//   o_t  = scale S_t^T q_hat_t.
+// Unrolled over the tokens (the WY form of these pages' replay), with
+// P_t = d_0 * ... * d_t and w_tj = P_t / P_j = d_{j+1} * ... * d_t:
+//   (D_t S_{t-1})^T k~_t = S_b^T (P_t k~_t) + sum_{j<t}  u~_j (w_tj k~_j) . k~_t
+//   S_t^T q_hat_t        = S_b^T (P_t q_hat_t) + sum_{j<=t} u~_j (w_tj k~_j) . q_hat_t
+// so each state row is read once for 2T dot products, and the token-to-token
+// dependence shrinks to a T-step scalar recurrence per row over the T x T
+// coefficients cc[t][j] = (w_tj k~_j) . k~_t and ec[t][j] = (w_tj k~_j) . q_hat_t.
+// The base state is the checkpoint replayed through the h live entries, in
+// closed form with the pages' replay weights:
+//   S_h = diag(exp(G_{h-1})) S_0 + sum_{j<h} (exp(G_{h-1} - G_j) k~_j) u~_j^T;
+// a fold (h >= flush_min) rounds S_h to bf16, stores it as the new checkpoint
+// and uses the rounded state as the base (G restarts at 0); otherwise S_h
+// stays in fp32 and G continues from G_{h-1}.
+//
+// One CTA (128 threads) per (batch row, head, tile of TV = 16, 32 or 64 rows):
+//   1. slot lookup, checkpoint bulk copy, hist_len check (outside [0, W]:
+//      error bit, skip);
+//   2. per-token prologue; per channel: k~, G, d_t, P_t, the query vectors
+//      P_t k~_t and P_t q_hat_t, exp(G_{h-1}), the history keys;
+//   3. the coefficient matrices, one warp per column j;
+//   4. per 4-row group pair: base rows (replay, fold), the 2T dot products,
+//      a reduce-scatter that leaves token t's two sums on lane t % 8 of the
+//      row, and the T-step recurrence for u~_t and o_t;
+//   5. outputs and this tile's rows of u~ (rows no other CTA reads).
+// A second, stream-ordered kernel (one CTA per batch row) appends k~ and G
 // and resets hist_len after a fold. Both are shared by every tile and head of
 // a slot: after a fold the new entries overwrite ring positions 0..T-1 that
 // other CTAs of the first kernel may still be replaying, and a reset
@@ -31,27 +46,70 @@
 
 namespace kda {
 
-constexpr int HC = 8;  // history entries staged per chunk
-
-__host__ __device__ constexpr size_t ring_smem_bytes(int TV, int T) {
-  return (size_t)TV * KD * 2                   // checkpoint tile (bf16)
-         + 64                                    // mbarriers
-         + (size_t)T * KD * 4 * 4                // kh (k~), qh, dd (decay), gg (g)
-         + (size_t)T * TV * 4 * 3                // vrow, orow, urow
-         + (size_t)KDA_MAX_T * 4 * 2             // beta, kappa
-         + (size_t)KDA_MAX_T * NWARPS * 3 * 4    // reduction partials
-         + (size_t)HC * KD * 4 * 2               // history k, decay
-         + (size_t)HC * TV * 4;                  // history u rows
+__host__ __device__ constexpr size_t ring_smem_bytes(int TV, int T, int W) {
+  return (size_t)TV * KD * 2                        // checkpoint tile (bf16)
+         + 64                                         // mbarriers
+         + (size_t)T * KD * 4 * 4                     // kh (k~), qh, dd (d_t), gg (g)
+         + (size_t)T * KD * 4 * 2                     // qk = P_t k~_t, qq = P_t q_hat_t
+         + (size_t)T * TV * 4 * 3                     // vrow, orow, urow
+         + (size_t)KDA_MAX_T * 4 * 2                  // beta, kappa
+         + (size_t)KDA_MAX_T * NWARPS * 3 * 4         // reduction partials
+         + (size_t)KDA_MAX_T * KDA_MAX_T * 4 * 2      // cc, ec
+         + (size_t)KD * 4                             // exp(G_{h-1})
+         + (size_t)W * KD * 4                         // history keys
+         + (size_t)W * TV * 4;                        // history u rows
 }
 
 __device__ __forceinline__ float round_bf16(float x) { return bf16_bits_to_float(float_to_bf16_bits(x)); }
 
-template <int TV, bool BULK>
+// Dot product of a lane's 16 keys of a row with the lane's 16 keys of a vector.
+__device__ __forceinline__ float dot16(const f32x2 (&vec)[8], const f32x2 (&row)[8]) {
+  f32x2 xa = mul2(vec[0], row[0]), xb = mul2(vec[1], row[1]);
+#pragma unroll
+  for (int i = 2; i < 8; i += 2) {
+    xa = fma2(vec[i], row[i], xa);
+    xb = fma2(vec[i + 1], row[i + 1], xb);
+  }
+  float x0, x1, x2, x3;
+  upk2(xa, x0, x1);
+  upk2(xb, x2, x3);
+  return __fadd_rn(__fadd_rn(x0, x2), __fadd_rn(x1, x3));
+}
+
+// Slot of token t's sum ("which" = 0: with k~, 1: with q_hat) among the 2 TT
+// values a lane holds before the reduce-scatter; after it, lane j of the row
+// holds slots [j * 2TT/8, (j + 1) * 2TT/8), that is tokens j and j + 8.
+template <int TT>
+__device__ __forceinline__ constexpr int wy_slot(int t, int which) {
+  return TT == 8 ? 2 * t + which : 4 * (t & 7) + 2 * (t >> 3) + which;
+}
+
+// Reduce-scatter of NV per-lane values over the 8 lanes of a row: at the
+// level with lane mask m, a lane keeps the half of its current values picked
+// by bit m of its row lane and sends the other half to lane ^ m, who keeps it.
+template <int NV>
+__device__ __forceinline__ void reduce_scatter8(float (&v)[NV], int j) {
+#pragma unroll
+  for (int m = 4, c = NV; m >= 1; m >>= 1, c >>= 1) {
+    const bool hi = (j & m) != 0;
+#pragma unroll
+    for (int i = 0; i < c / 2; ++i) {
+      const float keep = hi ? v[c / 2 + i] : v[i];
+      const float send = hi ? v[i] : v[c / 2 + i];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, m));
+    }
+  }
+}
+
+template <int TV, bool BULK, int TT>
 __global__ void __launch_bounds__(NTHREADS)
     kda_ring_kernel(const kda_params p, const kda_ring_params rp, const int T, const int tiles) {
   static_assert(TV % 16 == 0 && TV >= 16 && TV <= 64, "ring tile must be 16, 32 or 64 rows");
+  static_assert(TT == 8 || TT == 16, "token slots");
   constexpr int RW = TV / NWARPS;         // rows per warp
   constexpr int RQ = RW / ROWS_PER_WARP;  // 4-row groups per warp
+  constexpr int RG = RQ < 2 ? RQ : 2;     // groups processed together
+  constexpr int NV = 2 * TT;              // sums per row before the reduce-scatter
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -69,15 +127,19 @@ __global__ void __launch_bounds__(NTHREADS)
   ts.qh = ts.kh + T * KD;
   ts.dd = ts.qh + T * KD;
   ts.gg = ts.dd + T * KD;
-  ts.vrow = ts.gg + T * KD;
+  float* qk = ts.gg + T * KD;
+  float* qq = qk + T * KD;
+  ts.vrow = qq + T * KD;
   float* orow = ts.vrow + T * TV;
   float* urow = orow + T * TV;
   ts.beta = urow + T * TV;
   ts.kappa = ts.beta + KDA_MAX_T;
   ts.red = ts.kappa + KDA_MAX_T;
-  float* hk = ts.red + KDA_MAX_T * NWARPS * 3;  // [HC][128]
-  float* hd = hk + HC * KD;                     // [HC][128]
-  float* hu = hd + HC * KD;                     // [HC][TV]
+  float* cc = ts.red + KDA_MAX_T * NWARPS * 3;  // [t][j], j < t
+  float* ec = cc + KDA_MAX_T * KDA_MAX_T;       // [t][j], j <= t
+  float* cdec = ec + KDA_MAX_T * KDA_MAX_T;     // [128] exp(G_{h-1})
+  float* hk = cdec + KD;                        // [W][128] exp(G_{h-1} - G_j) k~_j
+  float* hu = hk + rp.W * KD;                   // [W][TV] u~_j of this tile's rows
 
   uint16_t* outp = static_cast<uint16_t*>(p.out);
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
@@ -133,31 +195,58 @@ __global__ void __launch_bounds__(NTHREADS)
 
   token_prologue(p, b, h, T, v0, TV, ts, first);  // ends with a CTA barrier
 
-  // Per channel: k~, G, the decay exp(G_P - G_{P-1}) and the partial sums of k~ . q_hat.
+  // Channel pass, thread c = key channel c.
   {
     const int c = tid;
-    float G_prev = (!fold && hist > 0) ? gc[(int64_t)(hist - 1) * KD + c] : 0.0f;
-    float kq[KDA_MAX_T];
+    const float Gl = hist > 0 ? gc[(int64_t)(hist - 1) * KD + c] : 0.0f;  // G_{h-1}
+    cdec[c] = hist > 0 ? expf(Gl) : 1.0f;
+    for (int jx = 0; jx < hist; ++jx) {
+      const float kj = bf16_bits_to_float(kc[(int64_t)jx * KD + c]);
+      hk[jx * KD + c] = __fmul_rn(expf(__fsub_rn(Gl, gc[(int64_t)jx * KD + c])), kj);
+      if (c < TV) hu[jx * TV + c] = bf16_bits_to_float(uc[(int64_t)jx * KD + v0 + c]);
+    }
+    float G_prev = fold ? 0.0f : Gl;
+    float P = 1.0f;
     for (int t = 0; t < T; ++t) {
       const float kt = round_bf16(ts.kh[t * KD + c]);
       const float G = __fadd_rn(G_prev, ts.gg[t * KD + c]);
-      ts.dd[t * KD + c] = expf(__fsub_rn(G, G_prev));
+      const float d = expf(__fsub_rn(G, G_prev));
+      P = __fmul_rn(P, d);
       ts.kh[t * KD + c] = kt;
-      kq[t] = __fmul_rn(kt, ts.qh[t * KD + c]);
+      ts.dd[t * KD + c] = d;
+      qk[t * KD + c] = __fmul_rn(P, kt);
+      qq[t * KD + c] = __fmul_rn(P, ts.qh[t * KD + c]);
       G_prev = G;
-    }
-    for (int t = 0; t < T; ++t) {
-      const float s = warp_sum(kq[t]);
-      if (lane == 0) ts.red[(t * NWARPS + warp) * 3] = s;
     }
   }
   __syncthreads();
-  if (tid < T) {
-    const float* r = ts.red + tid * NWARPS * 3;
-    float s = r[0];
+
+  // Coefficients, warp w for columns j = w, w + 4, ...; lane l sums channels
+  // l + 32 i; w_tj is a running product of the token decays.
+  for (int j = warp; j < T; j += NWARPS) {
+    float wgt[4], kj[4];
 #pragma unroll
-    for (int w = 1; w < NWARPS; ++w) s = __fadd_rn(s, r[w * 3]);
-    ts.kappa[tid] = s;
+    for (int i = 0; i < 4; ++i) {
+      wgt[i] = 1.0f;
+      kj[i] = ts.kh[j * KD + lane + 32 * i];
+    }
+    for (int t = j; t < T; ++t) {
+      float sc = 0.0f, se = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = lane + 32 * i;
+        if (t > j) wgt[i] = __fmul_rn(wgt[i], ts.dd[t * KD + c]);
+        const float pj = __fmul_rn(wgt[i], kj[i]);
+        sc = __fmaf_rn(pj, ts.kh[t * KD + c], sc);
+        se = __fmaf_rn(pj, ts.qh[t * KD + c], se);
+      }
+      sc = warp_sum(sc);
+      se = warp_sum(se);
+      if (lane == 0) {
+        if (t > j) cc[t * KDA_MAX_T + j] = sc;
+        ec[t * KDA_MAX_T + j] = se;
+      }
+    }
   }
 
   bool ok = true;
@@ -166,90 +255,116 @@ __global__ void __launch_bounds__(NTHREADS)
   if (!ok && lane == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
   // The tile is written only if every warp's copy arrived; a CTA that gave up
   // writes zero output and leaves the checkpoint and ring alone. The barrier
-  // also publishes kappa.
+  // also publishes the coefficients.
   ok = __syncthreads_and(ok) != 0;
 
   const int r = lane / LPR, j = lane % LPR;  // row within a 4-row group, lane within the row
-  f32x2 s[RQ][8];  // the lane's 16 keys of each of its rows, fp32
+  for (int g = 0; g < RQ; g += RG) {
+    f32x2 s[RG][8];
+    int rows[RG];
 #pragma unroll
-  for (int q = 0; q < RQ; ++q) row_to_f32(load_row_bf16(st + (warp * RW + ROWS_PER_WARP * q + r) * KD, j), s[q]);
-
-  // Replay the live history in chunks: s <- exp(G_j - G_{j-1}) s + k_j u_j[v].
-  for (int j0 = 0; j0 < hist; j0 += HC) {
-    const int nj = min(HC, hist - j0);
-    __syncthreads();  // previous chunk consumed
-    {
-      const int c = tid;
-      for (int jj = 0; jj < nj; ++jj) {
-        const int jx = j0 + jj;
-        hk[jj * KD + c] = bf16_bits_to_float(kc[(int64_t)jx * KD + c]);
-        const float Gj = gc[(int64_t)jx * KD + c];
-        const float Gm = jx > 0 ? gc[(int64_t)(jx - 1) * KD + c] : 0.0f;
-        hd[jj * KD + c] = expf(__fsub_rn(Gj, Gm));
-        if (c < TV) hu[jj * TV + c] = bf16_bits_to_float(uc[(int64_t)jx * KD + v0 + c]);
+    for (int q = 0; q < RG; ++q) {
+      rows[q] = warp * RW + ROWS_PER_WARP * (g + q) + r;
+      row_to_f32(load_row_bf16(st + rows[q] * KD, j), s[q]);
+    }
+    // base = exp(G_{h-1}) S_0 + sum_j (exp(G_{h-1} - G_j) k~_j) u~_j[row]
+    if (hist > 0) {
+      f32x2 cv[8];
+      load_pairs8(cdec, j, cv);
+#pragma unroll
+      for (int q = 0; q < RG; ++q)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s[q][i] = mul2(cv[i], s[q][i]);
+      for (int jx = 0; jx < hist; ++jx) {
+        f32x2 kr[8];
+        load_pairs8(hk + jx * KD, j, kr);
+#pragma unroll
+        for (int q = 0; q < RG; ++q) {
+          const float uv = hu[jx * TV + rows[q]];
+          const f32x2 uu = pk2(uv, uv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s[q][i] = fma2(kr[i], uu, s[q][i]);
+        }
       }
     }
-    __syncthreads();
-    for (int jj = 0; jj < nj; ++jj) {
-      f32x2 kr[8], dr[8];
-      load_pairs8(hk + jj * KD, j, kr);
-      load_pairs8(hd + jj * KD, j, dr);
+    if (fold) {
 #pragma unroll
-      for (int q = 0; q < RQ; ++q) {
-        const float uv = hu[jj * TV + warp * RW + ROWS_PER_WARP * q + r];
-        const f32x2 uu = pk2(uv, uv);
+      for (int q = 0; q < RG; ++q) {
+        const RowBf16 w = row_to_bf16(s[q]);
+        if (ok) store_row_bf16(st + rows[q] * KD, j, w);
+        row_to_f32(w, s[q]);
+      }
+    }
+    // 2T dot products of each base row: S_b^T (P_t k~_t) and S_b^T (P_t q_hat_t).
+    float acc[RG][NV];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s[q][i] = fma2(kr[i], uu, mul2(dr[i], s[q][i]));
+    for (int q = 0; q < RG; ++q)
+#pragma unroll
+      for (int i = 0; i < NV; ++i) acc[q][i] = 0.0f;
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      if (t < T) {
+        f32x2 vk[8], vq[8];
+        load_pairs8(qk + t * KD, j, vk);
+        load_pairs8(qq + t * KD, j, vq);
+#pragma unroll
+        for (int q = 0; q < RG; ++q) {
+          acc[q][wy_slot<TT>(t, 0)] = dot16(vk, s[q]);
+          acc[q][wy_slot<TT>(t, 1)] = dot16(vq, s[q]);
+        }
+      }
+    }
+    // The T-step recurrence; lane j of the row owns tokens j and j + 8.
+#pragma unroll
+    for (int q = 0; q < RG; ++q) {
+      reduce_scatter8<NV>(acc[q], j);
+      const int row = rows[q];
+      float cu[2] = {0.0f, 0.0f}, co[2] = {0.0f, 0.0f}, uo[2] = {0.0f, 0.0f};
+      for (int sx = 0; sx < T; ++sx) {
+        const int half = sx >> 3;
+        float mine = 0.0f;
+        if (j == (sx & 7)) {
+          // token sx's sum with k~ sits in slot 0 (first token) or 2 (second) of its owner lane
+          const float A = half ? acc[q][TT == 16 ? 2 : 0] : acc[q][0];
+          const float cuh = half ? cu[1] : cu[0];
+          mine = round_bf16(__fmul_rn(ts.beta[sx], __fsub_rn(ts.vrow[sx * TV + row], __fadd_rn(A, cuh))));
+        }
+        const float us = __shfl_sync(0xffffffffu, mine, (lane & ~(LPR - 1)) | (sx & 7));
+#pragma unroll
+        for (int hh = 0; hh < TT / 8; ++hh) {
+          const int tok = j + 8 * hh;
+          if (tok < T) {
+            if (tok > sx) cu[hh] = __fmaf_rn(cc[tok * KDA_MAX_T + sx], us, cu[hh]);
+            if (tok >= sx) co[hh] = __fmaf_rn(ec[tok * KDA_MAX_T + sx], us, co[hh]);
+            if (tok == sx) uo[hh] = us;
+          }
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < TT / 8; ++hh) {
+        const int tok = j + 8 * hh;
+        if (tok < T) {
+          urow[tok * TV + row] = uo[hh];
+          orow[tok * TV + row] = ok ? __fmul_rn(p.scale, __fadd_rn(acc[q][2 * hh + 1], co[hh])) : 0.0f;
+        }
       }
     }
   }
 
   if (fold && ok) {
-#pragma unroll
-    for (int q = 0; q < RQ; ++q) {
-      const RowBf16 w = row_to_bf16(s[q]);
-      store_row_bf16(st + (warp * RW + ROWS_PER_WARP * q + r) * KD, j, w);
-      row_to_f32(w, s[q]);
-    }
     if constexpr (BULK) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         bulk_s2g(gst, sst, CHUNK_BYTES);
         bulk_commit();
+        bulk_wait_read_all();
       }
     } else {
       __syncwarp();
       for (int i = lane; i < RW * KD; i += 32) gst[i] = sst[i];
     }
   }
-
-  // The new tokens, state kept in fp32: a = D s; u~ = bf16(beta (v - a . k~));
-  // s <- a + k~ u~; o = scale (a . q_hat + u~ (k~ . q_hat)).
-  for (int t = 0; t < T; ++t) {
-    LaneVecs lv;
-    load_lane_vecs(ts, t, j, lv);
-    const float beta = ts.beta[t], kappa = ts.kappa[t];
-#pragma unroll
-    for (int q = 0; q < RQ; ++q) {
-      const int row = warp * RW + ROWS_PER_WARP * q + r;
-      f32x2 a[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = mul2(lv.dd[i], s[q][i]);
-      float x, y, u, yr;
-      partial_dots(a, lv, x, y);
-      row_reduce(x, y, j, beta, ts.vrow[t * TV + row], u, yr);
-      u = round_bf16(u);
-      const f32x2 uu = pk2(u, u);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) s[q][i] = fma2(lv.kh[i], uu, a[i]);
-      if (j == 0) {
-        urow[t * TV + row] = u;
-        orow[t * TV + row] = ok ? __fmul_rn(p.scale, __fmaf_rn(u, kappa, yr)) : 0.0f;
-      }
-    }
-  }
-  if (fold && ok && BULK && lane == 0) bulk_wait_read_all();
   __syncthreads();
   for (int i = tid; i < T * TV; i += NTHREADS) {
     const int t = i / TV, rr = i - t * TV;
@@ -322,28 +437,34 @@ __global__ void __launch_bounds__(NTHREADS)
   }
 }
 
-template <int TV, bool BULK>
+template <int TV, bool BULK, int TT>
 static cudaError_t launch_ring_one(const kda_params& p, int T, const kda_ring_params& r, cudaStream_t s) {
-  auto kern = kda_ring_kernel<TV, BULK>;
+  auto kern = kda_ring_kernel<TV, BULK, TT>;
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
-  cudaError_t e = set_smem_limit_once(kern, ring_smem_bytes(TV, KDA_MAX_T), smem_set);
+  cudaError_t e = set_smem_limit_once(kern, ring_smem_bytes(TV, KDA_MAX_T, 64), smem_set);
   if (e != cudaSuccess) return e;
   const int tiles = KD / TV;
   const long long blocks = (long long)p.B * p.H * tiles;
-  kern<<<(unsigned)blocks, NTHREADS, ring_smem_bytes(TV, T), s>>>(p, r, T, tiles);
+  kern<<<(unsigned)blocks, NTHREADS, ring_smem_bytes(TV, T, r.W), s>>>(p, r, T, tiles);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   kda_ring_append_kernel<<<(unsigned)p.B, NTHREADS, 0, s>>>(p, r, T);
   return cudaGetLastError();
 }
 
+template <int TV>
+static cudaError_t launch_ring_tv(const kda_params& p, int T, const kda_ring_params& r, bool bulk, cudaStream_t s) {
+  if (T <= 8) return bulk ? launch_ring_one<TV, true, 8>(p, T, r, s) : launch_ring_one<TV, false, 8>(p, T, r, s);
+  return bulk ? launch_ring_one<TV, true, 16>(p, T, r, s) : launch_ring_one<TV, false, 16>(p, T, r, s);
+}
+
 cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, int tile_v, bool bulk,
                         cudaStream_t s) {
   if (tile_v > 64) tile_v = 64;
   switch (tile_v) {
-    case 16: return bulk ? launch_ring_one<16, true>(p, T, r, s) : launch_ring_one<16, false>(p, T, r, s);
-    case 32: return bulk ? launch_ring_one<32, true>(p, T, r, s) : launch_ring_one<32, false>(p, T, r, s);
-    case 64: return bulk ? launch_ring_one<64, true>(p, T, r, s) : launch_ring_one<64, false>(p, T, r, s);
+    case 16: return launch_ring_tv<16>(p, T, r, bulk, s);
+    case 32: return launch_ring_tv<32>(p, T, r, bulk, s);
+    case 64: return launch_ring_tv<64>(p, T, r, bulk, s);
     default: return cudaErrorInvalidValue;
   }
 }

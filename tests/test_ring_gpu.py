@@ -132,10 +132,12 @@ def test_ring_invalid_history_sets_error_and_touches_nothing(dev):
         assert torch.equal(wd.state[n].cpu().view(torch.int16), w.state[n].view(torch.int16))
 
 
-def test_ring_single_token_calls_chain_bitwise(dev):
+def test_ring_single_token_calls_chain(dev):
     """Without a fold, T single-token calls (hist_len advanced by the caller
-    between them) give the same bits as one T-token call: the replay of the
-    ring reproduces the in-call state exactly."""
+    between them) compute what one T-token call computes: the later calls
+    replay what the earlier ones appended. k~ and G are the same bits; u~ and
+    the outputs agree to fp32 rounding (the one-call kernel sums the same terms
+    in another order)."""
     T = 6
     w = workloads.ring_inputs(5, 12, T=T, W=32, flush_min=20, fold_frac=0.0, seed=11)
     hl = w.ring["hist_len"]
@@ -152,9 +154,11 @@ def test_ring_single_token_calls_chain_bitwise(dev):
         outs.append(gpu_ring(wt))
         c.ring["hist_len"][idx] += 1
     torch.cuda.synchronize()
-    assert torch.equal(out_all.view(torch.int16), torch.cat(outs, dim=1).view(torch.int16))
-    for name in ("k_cache", "u_cache"):
-        assert torch.equal(a.ring[name].view(torch.int16), c.ring[name].view(torch.int16)), name
+    assert_output_close(f64(torch.cat(outs, dim=1)), f64(out_all))
+    ug, ur = f64(c.ring["u_cache"]), f64(a.ring["u_cache"])
+    assert np.array_equal(np.isnan(ug), np.isnan(ur))  # the same positions written, sentinels kept
+    assert float(ring_ulps(np.nan_to_num(ug), np.nan_to_num(ur), floor=1.0).max()) <= 2.0
+    assert torch.equal(a.ring["k_cache"].view(torch.int16), c.ring["k_cache"].view(torch.int16))
     assert torch.equal(a.ring["g_cache"].view(torch.int32), c.ring["g_cache"].view(torch.int32))
 
 
