@@ -159,13 +159,14 @@ __device__ __forceinline__ float load_bf16(const kda_view& vw, int b, int t, int
 // Raw per-token inputs of thread c (key channel c) for a chunk of PC tokens,
 // loaded into registers together so that their global-memory latencies
 // overlap instead of adding up token after token.
-constexpr int PC = 4;
+template <int PC>
 struct TokenLoads {
   float q[PC], k[PC], g[PC], v[PC], bl[PC];
 };
 
+template <int PC>
 __device__ __forceinline__ void prologue_issue(const kda_params& p, int b, int h, int t0, int T, int v0, int TV,
-                                               TokenLoads& L) {
+                                               TokenLoads<PC>& L) {
   const int c = threadIdx.x;
 #pragma unroll
   for (int i = 0; i < PC; ++i) {
@@ -188,13 +189,14 @@ __device__ __forceinline__ void prologue_issue(const kda_params& p, int b, int h
 // and beta. Thread c of the CTA handles key channel c; `first` holds the
 // already-issued loads of tokens 0..PC-1. Ends with a CTA barrier. Every CTA of
 // the same (b, h) computes the same bits: fixed reduction order.
+template <int PC>
 __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h, int T, int v0, int TV,
-                                               const TokenSmem& ts, const TokenLoads& first) {
+                                               const TokenSmem& ts, const TokenLoads<PC>& first) {
   const int c = threadIdx.x;
   const int warp = c >> 5, lane = c & 31;
   const float a_h = expf(p.A_log[h]);
   const float dtb = p.dt_bias[(int64_t)h * KD + c];
-  TokenLoads L = first;
+  TokenLoads<PC> L = first;
   for (int t0 = 0; t0 < T; t0 += PC) {
     if (t0 > 0) prologue_issue(p, b, h, t0, T, v0, TV, L);
 #pragma unroll

@@ -56,8 +56,10 @@ __host__ __device__ constexpr size_t ring_smem_bytes(int TV, int T, int W) {
          + (size_t)KDA_MAX_T * NWARPS * 3 * 4         // reduction partials
          + (size_t)KDA_MAX_T * KDA_MAX_T * 4 * 2      // cc, ec
          + (size_t)KD * 4                             // exp(G_{h-1})
-         + (size_t)W * KD * 4                         // history keys
-         + (size_t)W * TV * 4;                        // history u rows
+         + (size_t)W * KD * 4                         // history G, then history keys (in place)
+         + (size_t)W * KD * 2                         // history k~ (bf16, as stored)
+         + (size_t)W * TV * 2                         // history u~ of this tile's rows (bf16)
+         + 16;                                        // history mbarrier
 }
 
 __device__ __forceinline__ float round_bf16(float x) { return bf16_bits_to_float(float_to_bf16_bits(x)); }
@@ -138,14 +140,16 @@ __global__ void __launch_bounds__(NTHREADS)
   float* cc = ts.red + KDA_MAX_T * NWARPS * 3;  // [t][j], j < t
   float* ec = cc + KDA_MAX_T * KDA_MAX_T;       // [t][j], j <= t
   float* cdec = ec + KDA_MAX_T * KDA_MAX_T;     // [128] exp(G_{h-1})
-  float* hk = cdec + KD;                        // [W][128] exp(G_{h-1} - G_j) k~_j
-  float* hu = hk + rp.W * KD;                   // [W][TV] u~_j of this tile's rows
+  float* hk = cdec + KD;                        // [W][128] G_j as copied, then exp(G_{h-1} - G_j) k~_j
+  uint16_t* hkb = reinterpret_cast<uint16_t*>(hk + rp.W * KD);  // [W][128] k~_j (bf16)
+  uint16_t* hub = hkb + rp.W * KD;                               // [W][TV] u~_j[v0..v0+TV) (bf16)
+  uint64_t* hbar = reinterpret_cast<uint64_t*>(hub + rp.W * TV);  // history copies
 
   uint16_t* outp = static_cast<uint16_t*>(p.out);
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
 
   const int n = p.state_indices[b];
-  TokenLoads first;  // issued alongside the index load; unused by an inactive row
+  TokenLoads<8> first;  // issued alongside the index load; unused by an inactive row
   prologue_issue(p, b, h, 0, T, v0, TV, first);
   if (n < 0 || n >= p.N) {
     for (int i = tid; i < T * TV; i += NTHREADS) {
@@ -182,9 +186,6 @@ __global__ void __launch_bounds__(NTHREADS)
     }
     return;
   }
-  if constexpr (!BULK) {
-    for (int i = lane; i < RW * KD; i += 32) sst[i] = gst[i];
-  }
   const bool fold = hist >= rp.flush_min;
   const int base = fold ? 0 : hist;
 
@@ -193,17 +194,35 @@ __global__ void __launch_bounds__(NTHREADS)
   uint16_t* uc = static_cast<uint16_t*>(rp.u_cache) + (int64_t)n * rp.u_slot_stride + (int64_t)h * rp.W * KD;
   float* gc = static_cast<float*>(rp.g_cache) + (int64_t)n * rp.g_slot_stride + (int64_t)h * rp.W * KD;
 
-  token_prologue(p, b, h, T, v0, TV, ts, first);  // ends with a CTA barrier
+  // The live history arrives by bulk copies started now, so that its latency
+  // overlaps the prologue: k~ and G of entries 0..hist-1 are contiguous, this
+  // tile's u~ rows are one short copy per entry. The ring pointers and slot
+  // strides are 16-byte aligned (checked on the host), v0 is a multiple of 16.
+  if (hist > 0 && tid == 0) {
+    mbar_init(hbar, 1);
+    mbar_expect_tx(hbar, (uint32_t)hist * (KD * 2 + KD * 4 + TV * 2));
+    bulk_g2s(hkb, kc, (uint32_t)hist * KD * 2, hbar);
+    bulk_g2s(hk, gc, (uint32_t)hist * KD * 4, hbar);
+    for (int jx = 0; jx < hist; ++jx) bulk_g2s(hub + jx * TV, uc + (int64_t)jx * KD + v0, TV * 2, hbar);
+  }
+  if constexpr (!BULK) {
+    for (int i = lane; i < RW * KD; i += 32) sst[i] = gst[i];
+  }
+
+  token_prologue(p, b, h, T, v0, TV, ts, first);  // ends with a CTA barrier (publishes hbar's init)
+
+  bool hist_ok = true;
+  if (hist > 0) hist_ok = mbar_wait_bounded(hbar, 0);
+  if (!hist_ok && tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
 
   // Channel pass, thread c = key channel c.
   {
     const int c = tid;
-    const float Gl = hist > 0 ? gc[(int64_t)(hist - 1) * KD + c] : 0.0f;  // G_{h-1}
+    const float Gl = hist > 0 ? hk[(hist - 1) * KD + c] : 0.0f;  // G_{h-1}
     cdec[c] = hist > 0 ? expf(Gl) : 1.0f;
-    for (int jx = 0; jx < hist; ++jx) {
-      const float kj = bf16_bits_to_float(kc[(int64_t)jx * KD + c]);
-      hk[jx * KD + c] = __fmul_rn(expf(__fsub_rn(Gl, gc[(int64_t)jx * KD + c])), kj);
-      if (c < TV) hu[jx * TV + c] = bf16_bits_to_float(uc[(int64_t)jx * KD + v0 + c]);
+    for (int jx = 0; jx < hist; ++jx) {  // in place: G_j -> exp(G_{h-1} - G_j) k~_j
+      const float kj = bf16_bits_to_float(hkb[jx * KD + c]);
+      hk[jx * KD + c] = __fmul_rn(expf(__fsub_rn(Gl, hk[jx * KD + c])), kj);
     }
     float G_prev = fold ? 0.0f : Gl;
     float P = 1.0f;
@@ -256,7 +275,7 @@ __global__ void __launch_bounds__(NTHREADS)
   // The tile is written only if every warp's copy arrived; a CTA that gave up
   // writes zero output and leaves the checkpoint and ring alone. The barrier
   // also publishes the coefficients.
-  ok = __syncthreads_and(ok) != 0;
+  ok = __syncthreads_and(ok && hist_ok) != 0;
 
   const int r = lane / LPR, j = lane % LPR;  // row within a 4-row group, lane within the row
   for (int g = 0; g < RQ; g += RG) {
@@ -280,7 +299,7 @@ __global__ void __launch_bounds__(NTHREADS)
         load_pairs8(hk + jx * KD, j, kr);
 #pragma unroll
         for (int q = 0; q < RG; ++q) {
-          const float uv = hu[jx * TV + rows[q]];
+          const float uv = bf16_bits_to_float(hub[jx * TV + rows[q]]);
           const f32x2 uu = pk2(uv, uv);
 #pragma unroll
           for (int i = 0; i < 8; ++i) s[q][i] = fma2(kr[i], uu, s[q][i]);

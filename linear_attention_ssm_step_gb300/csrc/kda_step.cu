@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(NTHREADS, MULTI ? 1 : 6)
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
 
   const int n = p.state_indices[b];
-  TokenLoads first;  // issued alongside the index load; unused by an inactive row
+  constexpr int PCN = MULTI ? 8 : 1;  // tokens whose inputs are loaded in one batch
+  TokenLoads<PCN> first;              // issued alongside the index load; unused by an inactive row
   prologue_issue(p, b, h, 0, T, v0, TV, first);
   if (n < 0 || n >= p.N) {
     for (int i = tid; i < T * TV; i += NTHREADS) {
