@@ -49,8 +49,8 @@ namespace kda {
 __host__ __device__ constexpr size_t ring_smem_bytes(int TV, int T, int W) {
   return (size_t)TV * KD * 2                        // checkpoint tile (bf16)
          + 64                                         // mbarriers
-         + (size_t)T * KD * 4 * 4                     // kh (k~), qh, dd (d_t), gg (g)
-         + (size_t)T * KD * 4 * 2                     // qk = P_t k~_t, qq = P_t q_hat_t
+         + (size_t)T * KD * 4 * 4                     // kh (k~), qh, dd (d_t), gg (g, then P_t k~_t)
+         + (size_t)T * KD * 4                         // qq = P_t q_hat_t
          + (size_t)T * TV * 4 * 3                     // vrow, orow, urow
          + (size_t)KDA_MAX_T * 4 * 2                  // beta, kappa
          + (size_t)KDA_MAX_T * NWARPS * 3 * 4         // reduction partials
@@ -129,8 +129,8 @@ __global__ void __launch_bounds__(NTHREADS)
   ts.qh = ts.kh + T * KD;
   ts.dd = ts.qh + T * KD;
   ts.gg = ts.dd + T * KD;
-  float* qk = ts.gg + T * KD;
-  float* qq = qk + T * KD;
+  float* qk = ts.gg;  // each thread overwrites its channel's g_t with P_t k~_t in the channel pass
+  float* qq = ts.gg + T * KD;
   ts.vrow = qq + T * KD;
   float* orow = ts.vrow + T * TV;
   float* urow = orow + T * TV;
@@ -404,10 +404,15 @@ __device__ __forceinline__ float sum128_like_cta(const float (&x)[4]) {
 
 // After the ring kernel, one CTA per batch row: append k~ and G_P at ring
 // positions base..base+T-1 for every head, then reset hist_len[n] after a
-// fold when restart_hist_on_flush. Warp w handles heads w, w+4, ...; lane l
-// handles channels l + 32 i. The arithmetic of k~ and G repeats
-// token_prologue and the ring kernel's channel pass operation for operation.
-__global__ void __launch_bounds__(NTHREADS)
+// fold when restart_hist_on_flush. One warp per head (the CTA has
+// APPEND_WARPS warps and loops when H is larger); lane l handles channels
+// l + 32 i, and each head's inputs for up to 8 tokens are loaded in one
+// batch, so the CTA waits for memory a few times rather than once per token.
+// The arithmetic of k~ and G repeats token_prologue and the ring kernel's
+// channel pass operation for operation.
+constexpr int APPEND_WARPS = 16;
+
+__global__ void __launch_bounds__(32 * APPEND_WARPS)
     kda_ring_append_kernel(const kda_params p, const kda_ring_params rp, const int T) {
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -417,7 +422,7 @@ __global__ void __launch_bounds__(NTHREADS)
   if (hist < 0 || hist > rp.W) return;
   const bool fold = hist >= rp.flush_min;
   const int base = fold ? 0 : hist;
-  for (int h = warp; h < p.H; h += NWARPS) {
+  for (int h = warp; h < p.H; h += blockDim.x >> 5) {
     uint16_t* kc = static_cast<uint16_t*>(rp.k_cache) + (int64_t)n * rp.k_slot_stride + (int64_t)h * rp.W * KD;
     float* gc = static_cast<float*>(rp.g_cache) + (int64_t)n * rp.g_slot_stride + (int64_t)h * rp.W * KD;
     const float a_h = expf(p.A_log[h]);
@@ -428,30 +433,43 @@ __global__ void __launch_bounds__(NTHREADS)
       dtb[i] = p.dt_bias[(int64_t)h * KD + c];
       G_prev[i] = (!fold && hist > 0) ? gc[(int64_t)(hist - 1) * KD + c] : 0.0f;
     }
-    for (int t = 0; t < T; ++t) {
-      float kc4[4], sq[4];
+    for (int t0 = 0; t0 < T; t0 += 8) {
+      float kv[8][4], gv[8][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        kc4[i] = load_bf16(p.k, b, t, h, lane + 32 * i);
-        sq[i] = __fmul_rn(kc4[i], kc4[i]);
+      for (int tt = 0; tt < 8; ++tt) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          kv[tt][i] = gv[tt][i] = 0.0f;
+          if (t0 + tt < T) {
+            kv[tt][i] = load_bf16(p.k, b, t0 + tt, h, lane + 32 * i);
+            gv[tt][i] = load_bf16(p.g_raw, b, t0 + tt, h, lane + 32 * i);
+          }
+        }
       }
-      const float rk = __frcp_rn(__fsqrt_rn(__fadd_rn(sum128_like_cta(sq), L2_EPS)));
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = lane + 32 * i;
-        const float gr = load_bf16(p.g_raw, b, t, h, c);
-        const float z = __fmul_rn(a_h, __fadd_rn(gr, dtb[i]));
-        const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-z)));
-        const float g = __fmul_rn(p.lower_bound, sig);
-        const float G = __fadd_rn(G_prev[i], g);
-        kc[(int64_t)(base + t) * KD + c] = float_to_bf16_bits(__fmul_rn(kc4[i], rk));
-        gc[(int64_t)(base + t) * KD + c] = G;
-        G_prev[i] = G;
+      for (int tt = 0; tt < 8; ++tt) {
+        const int t = t0 + tt;
+        if (t >= T) break;
+        float sq[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sq[i] = __fmul_rn(kv[tt][i], kv[tt][i]);
+        const float rk = __frcp_rn(__fsqrt_rn(__fadd_rn(sum128_like_cta(sq), L2_EPS)));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = lane + 32 * i;
+          const float z = __fmul_rn(a_h, __fadd_rn(gv[tt][i], dtb[i]));
+          const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-z)));
+          const float g = __fmul_rn(p.lower_bound, sig);
+          const float G = __fadd_rn(G_prev[i], g);
+          kc[(int64_t)(base + t) * KD + c] = float_to_bf16_bits(__fmul_rn(kv[tt][i], rk));
+          gc[(int64_t)(base + t) * KD + c] = G;
+          G_prev[i] = G;
+        }
       }
     }
   }
   if (fold && rp.restart_hist_on_flush) {
-    __syncthreads();
+    __syncthreads();  // every warp has read hist_len
     if (threadIdx.x == 0) rp.hist_len[n] = 0;
   }
 }
@@ -467,7 +485,8 @@ static cudaError_t launch_ring_one(const kda_params& p, int T, const kda_ring_pa
   kern<<<(unsigned)blocks, NTHREADS, ring_smem_bytes(TV, T, r.W), s>>>(p, r, T, tiles);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kda_ring_append_kernel<<<(unsigned)p.B, NTHREADS, 0, s>>>(p, r, T);
+  const int append_warps = p.H < APPEND_WARPS ? p.H : APPEND_WARPS;
+  kda_ring_append_kernel<<<(unsigned)p.B, 32 * append_warps, 0, s>>>(p, r, T);
   return cudaGetLastError();
 }
 
