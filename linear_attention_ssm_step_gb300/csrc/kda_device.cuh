@@ -148,7 +148,6 @@ struct TokenSmem {
   float* vrow;   // [T][TV] v for this CTA's value rows
   float* beta;   // [KDA_MAX_T]
   float* kappa;  // [KDA_MAX_T] k_hat . q_hat
-  float* red;    // [KDA_MAX_T][NWARPS][3] reduction partials
 };
 
 __device__ __forceinline__ float load_bf16(const kda_view& vw, int b, int t, int h, int c) {
@@ -156,90 +155,99 @@ __device__ __forceinline__ float load_bf16(const kda_view& vw, int b, int t, int
   return bf16_bits_to_float(p[(int64_t)b * vw.b_stride + (int64_t)t * vw.t_stride + (int64_t)h * vw.h_stride + c]);
 }
 
-// Raw per-token inputs of thread c (key channel c) for a chunk of PC tokens,
-// loaded into registers together so that their global-memory latencies
-// overlap instead of adding up token after token.
-template <int PC>
+// The per-token prologue of (row b, head h): L2 norms, k_hat . q_hat, the gate
+// and beta, for every token into shared memory. Warp w handles tokens
+// w, w + 4, ...; lane l handles key channels l + 32 i (i < 4). A warp's
+// token inputs (up to PT tokens) are loaded into registers together, so that
+// their latencies overlap; prologue_issue starts those loads (callers issue
+// them next to the slot-index load), token_prologue finishes.
+//
+// Sums over the 128 channels: each lane adds its 4 channels in order, then a
+// butterfly over the warp. The order is fixed, so every CTA of a (row, head)
+// and every kernel that repeats it (the ring's append kernel) gets the same
+// bits.
+template <int PT>
 struct TokenLoads {
-  float q[PC], k[PC], g[PC], v[PC], bl[PC];
+  float q[PT][4], k[PT][4], g[PT][4], v[PT][4], bl[PT];
 };
 
-template <int PC>
-__device__ __forceinline__ void prologue_issue(const kda_params& p, int b, int h, int t0, int T, int v0, int TV,
-                                               TokenLoads<PC>& L) {
-  const int c = threadIdx.x;
+template <int PT>
+__device__ __forceinline__ void prologue_issue(const kda_params& p, int b, int h, int T, int v0, int TV,
+                                               TokenLoads<PT>& L) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-  for (int i = 0; i < PC; ++i) {
-    const int t = t0 + i;
-    L.q[i] = L.k[i] = L.g[i] = L.v[i] = L.bl[i] = 0.0f;
-    if (t < T) {
-      L.q[i] = load_bf16(p.q, b, t, h, c);
-      L.k[i] = load_bf16(p.k, b, t, h, c);
-      L.g[i] = load_bf16(p.g_raw, b, t, h, c);
-      if (c < TV) L.v[i] = load_bf16(p.v, b, t, h, v0 + c);
-      if (c == 0)
-        L.bl[i] = bf16_bits_to_float(static_cast<const uint16_t*>(
-            p.beta_logit.ptr)[(int64_t)b * p.beta_logit.b_stride + (int64_t)t * p.beta_logit.t_stride +
-                              (int64_t)h * p.beta_logit.h_stride]);
+  for (int s = 0; s < PT; ++s) {
+    const int t = warp + NWARPS * s;
+    L.bl[s] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      L.q[s][i] = L.k[s][i] = L.g[s][i] = L.v[s][i] = 0.0f;
+      if (t < T) {
+        const int c = lane + 32 * i;
+        L.q[s][i] = load_bf16(p.q, b, t, h, c);
+        L.k[s][i] = load_bf16(p.k, b, t, h, c);
+        L.g[s][i] = load_bf16(p.g_raw, b, t, h, c);
+        if (c < TV) L.v[s][i] = load_bf16(p.v, b, t, h, v0 + c);
+      }
     }
+    if (t < T && lane == 0)
+      L.bl[s] = bf16_bits_to_float(static_cast<const uint16_t*>(
+          p.beta_logit.ptr)[(int64_t)b * p.beta_logit.b_stride + (int64_t)t * p.beta_logit.t_stride +
+                            (int64_t)h * p.beta_logit.h_stride]);
   }
 }
 
-// The per-token prologue of (row b, head h): L2 norms, k_hat . q_hat, the gate
-// and beta. Thread c of the CTA handles key channel c; `first` holds the
-// already-issued loads of tokens 0..PC-1. Ends with a CTA barrier. Every CTA of
-// the same (b, h) computes the same bits: fixed reduction order.
-template <int PC>
+// Sum of a lane's 4 channel values, then over the warp (the fixed order above).
+__device__ __forceinline__ float sum_channels(float x0, float x1, float x2, float x3) {
+  return warp_sum(__fadd_rn(__fadd_rn(__fadd_rn(x0, x1), x2), x3));
+}
+
+// 1 / sqrt(sum + eps) for the L2 norm.
+__device__ __forceinline__ float inv_norm(float sum_sq) { return __frcp_rn(__fsqrt_rn(__fadd_rn(sum_sq, L2_EPS))); }
+
+// g = lower_bound * sigmoid(exp(A_log) * (g_raw + dt_bias)), given a_h = exp(A_log[h]).
+__device__ __forceinline__ float gate_log_decay(float a_h, float g_raw, float dt_bias, float lower_bound) {
+  const float z = __fmul_rn(a_h, __fadd_rn(g_raw, dt_bias));
+  return __fmul_rn(lower_bound, __frcp_rn(__fadd_rn(1.0f, expf(-z))));
+}
+
+template <int PT>
 __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h, int T, int v0, int TV,
-                                               const TokenSmem& ts, const TokenLoads<PC>& first) {
-  const int c = threadIdx.x;
-  const int warp = c >> 5, lane = c & 31;
+                                               const TokenSmem& ts, const TokenLoads<PT>& L) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float a_h = expf(p.A_log[h]);
-  const float dtb = p.dt_bias[(int64_t)h * KD + c];
-  TokenLoads<PC> L = first;
-  for (int t0 = 0; t0 < T; t0 += PC) {
-    if (t0 > 0) prologue_issue(p, b, h, t0, T, v0, TV, L);
+  float dtb[4];
 #pragma unroll
-    for (int i = 0; i < PC; ++i) {
-      const int t = t0 + i;
-      if (t >= T) break;
-      const float qc = L.q[i], kc = L.k[i];
-      const float sq = warp_sum(__fmul_rn(qc, qc));
-      const float sk = warp_sum(__fmul_rn(kc, kc));
-      const float sqk = warp_sum(__fmul_rn(qc, kc));
-      if (lane == 0) {
-        float* r = ts.red + (t * NWARPS + warp) * 3;
-        r[0] = sq;
-        r[1] = sk;
-        r[2] = sqk;
+  for (int i = 0; i < 4; ++i) dtb[i] = p.dt_bias[(int64_t)h * KD + lane + 32 * i];
+#pragma unroll
+  for (int s = 0; s < PT; ++s) {
+    const int t = warp + NWARPS * s;
+    if (t < T) {
+      float qq[4], kk[4], qk[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        qq[i] = __fmul_rn(L.q[s][i], L.q[s][i]);
+        kk[i] = __fmul_rn(L.k[s][i], L.k[s][i]);
+        qk[i] = __fmul_rn(L.q[s][i], L.k[s][i]);
       }
-      // g = lower_bound * sigmoid(exp(A_log) * (g_raw + dt_bias)), decay exp(g)
-      const float z = __fmul_rn(a_h, __fadd_rn(L.g[i], dtb));
-      const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-z)));
-      const float g = __fmul_rn(p.lower_bound, sig);
-      ts.gg[t * KD + c] = g;
-      ts.dd[t * KD + c] = expf(g);
-      ts.qh[t * KD + c] = qc;
-      ts.kh[t * KD + c] = kc;
-      if (c < TV) ts.vrow[t * TV + c] = L.v[i];
-      if (c == 0) ts.beta[t] = __frcp_rn(__fadd_rn(1.0f, expf(-L.bl[i])));
-    }
-  }
-  __syncthreads();
-  for (int t = 0; t < T; ++t) {
-    const float* r = ts.red + t * NWARPS * 3;
-    float sq = r[0], sk = r[1], sqk = r[2];
+      const float rq = inv_norm(sum_channels(qq[0], qq[1], qq[2], qq[3]));
+      const float rk = inv_norm(sum_channels(kk[0], kk[1], kk[2], kk[3]));
+      const float sqk = sum_channels(qk[0], qk[1], qk[2], qk[3]);
 #pragma unroll
-    for (int w = 1; w < NWARPS; ++w) {
-      sq = __fadd_rn(sq, r[w * 3 + 0]);
-      sk = __fadd_rn(sk, r[w * 3 + 1]);
-      sqk = __fadd_rn(sqk, r[w * 3 + 2]);
+      for (int i = 0; i < 4; ++i) {
+        const int c = lane + 32 * i;
+        const float g = gate_log_decay(a_h, L.g[s][i], dtb[i], p.lower_bound);
+        ts.gg[t * KD + c] = g;
+        ts.dd[t * KD + c] = expf(g);
+        ts.qh[t * KD + c] = __fmul_rn(L.q[s][i], rq);
+        ts.kh[t * KD + c] = __fmul_rn(L.k[s][i], rk);
+        if (c < TV) ts.vrow[t * TV + c] = L.v[s][i];
+      }
+      if (lane == 0) {
+        ts.kappa[t] = __fmul_rn(__fmul_rn(sqk, rq), rk);
+        ts.beta[t] = __frcp_rn(__fadd_rn(1.0f, expf(-L.bl[s])));
+      }
     }
-    const float rq = __frcp_rn(__fsqrt_rn(__fadd_rn(sq, L2_EPS)));
-    const float rk = __frcp_rn(__fsqrt_rn(__fadd_rn(sk, L2_EPS)));
-    ts.qh[t * KD + c] = __fmul_rn(ts.qh[t * KD + c], rq);
-    ts.kh[t * KD + c] = __fmul_rn(ts.kh[t * KD + c], rk);
-    if (c == 0) ts.kappa[t] = __fmul_rn(__fmul_rn(sqk, rq), rk);
   }
   __syncthreads();
 }

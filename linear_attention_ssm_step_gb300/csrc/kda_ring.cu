@@ -53,7 +53,6 @@ __host__ __device__ constexpr size_t ring_smem_bytes(int TV, int T, int W) {
          + (size_t)T * KD * 4                         // qq = P_t q_hat_t
          + (size_t)T * TV * 4 * 3                     // vrow, orow, urow
          + (size_t)KDA_MAX_T * 4 * 2                  // beta, kappa
-         + (size_t)KDA_MAX_T * NWARPS * 3 * 4         // reduction partials
          + (size_t)KDA_MAX_T * KDA_MAX_T * 4 * 2      // cc, ec
          + (size_t)KD * 4                             // exp(G_{h-1})
          + (size_t)W * KD * 4                         // history G, then history keys (in place)
@@ -103,6 +102,33 @@ __device__ __forceinline__ void reduce_scatter8(float (&v)[NV], int j) {
   }
 }
 
+// Reduce-scatter of NV (16 or 32) per-lane values over a whole warp: halving
+// levels (as in reduce_scatter8) while a lane holds more than one value, then
+// plain butterfly levels. Afterwards v[0] holds the warp-wide sum of value
+// lane >> (5 - log2 NV); each value is summed in one fixed order.
+template <int NV>
+__device__ __forceinline__ void reduce_scatter32(float (&v)[NV], int lane) {
+  static_assert(NV == 16 || NV == 32, "16 or 32 values");
+  int c = NV;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    if (c > 1) {
+      const bool hi = (lane & m) != 0;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        if (i < c / 2) {
+          const float keep = hi ? v[c / 2 + i] : v[i];
+          const float send = hi ? v[i] : v[c / 2 + i];
+          v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, m));
+        }
+      }
+      c >>= 1;
+    } else {
+      v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], m));
+    }
+  }
+}
+
 template <int TV, bool BULK, int TT>
 __global__ void __launch_bounds__(NTHREADS)
     kda_ring_kernel(const kda_params p, const kda_ring_params rp, const int T, const int tiles) {
@@ -136,8 +162,7 @@ __global__ void __launch_bounds__(NTHREADS)
   float* urow = orow + T * TV;
   ts.beta = urow + T * TV;
   ts.kappa = ts.beta + KDA_MAX_T;
-  ts.red = ts.kappa + KDA_MAX_T;
-  float* cc = ts.red + KDA_MAX_T * NWARPS * 3;  // [t][j], j < t
+  float* cc = ts.kappa + KDA_MAX_T;             // [t][j], j < t
   float* ec = cc + KDA_MAX_T * KDA_MAX_T;       // [t][j], j <= t
   float* cdec = ec + KDA_MAX_T * KDA_MAX_T;     // [128] exp(G_{h-1})
   float* hk = cdec + KD;                        // [W][128] G_j as copied, then exp(G_{h-1} - G_j) k~_j
@@ -149,8 +174,9 @@ __global__ void __launch_bounds__(NTHREADS)
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
 
   const int n = p.state_indices[b];
-  TokenLoads<8> first;  // issued alongside the index load; unused by an inactive row
-  prologue_issue(p, b, h, 0, T, v0, TV, first);
+  constexpr int PT = TT / NWARPS;  // tokens per warp in the prologue
+  TokenLoads<PT> first;            // issued alongside the index load; unused by an inactive row
+  prologue_issue(p, b, h, T, v0, TV, first);
   if (n < 0 || n >= p.N) {
     for (int i = tid; i < T * TV; i += NTHREADS) {
       const int t = i / TV, r = i - t * TV;
@@ -241,29 +267,42 @@ __global__ void __launch_bounds__(NTHREADS)
   __syncthreads();
 
   // Coefficients, warp w for columns j = w, w + 4, ...; lane l sums channels
-  // l + 32 i; w_tj is a running product of the token decays.
+  // l + 32 i; w_tj is a running product of the token decays. A column's 2 TT
+  // partial sums (cc and ec for every t) are reduced together, see
+  // reduce_scatter32.
   for (int j = warp; j < T; j += NWARPS) {
-    float wgt[4], kj[4];
+    float kj[4], wgt[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      wgt[i] = 1.0f;
       kj[i] = ts.kh[j * KD + lane + 32 * i];
+      wgt[i] = 1.0f;
     }
-    for (int t = j; t < T; ++t) {
-      float sc = 0.0f, se = 0.0f;
+    float vals[2 * TT];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = lane + 32 * i;
-        if (t > j) wgt[i] = __fmul_rn(wgt[i], ts.dd[t * KD + c]);
-        const float pj = __fmul_rn(wgt[i], kj[i]);
-        sc = __fmaf_rn(pj, ts.kh[t * KD + c], sc);
-        se = __fmaf_rn(pj, ts.qh[t * KD + c], se);
+    for (int t = 0; t < TT; ++t) {
+      float sc = 0.0f, se = 0.0f;
+      if (t >= j && t < T) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = lane + 32 * i;
+          if (t > j) wgt[i] = __fmul_rn(wgt[i], ts.dd[t * KD + c]);
+          const float pj = __fmul_rn(wgt[i], kj[i]);
+          sc = __fmaf_rn(pj, ts.kh[t * KD + c], sc);
+          se = __fmaf_rn(pj, ts.qh[t * KD + c], se);
+        }
       }
-      sc = warp_sum(sc);
-      se = warp_sum(se);
-      if (lane == 0) {
-        if (t > j) cc[t * KDA_MAX_T + j] = sc;
-        ec[t * KDA_MAX_T + j] = se;
+      vals[2 * t] = sc;
+      vals[2 * t + 1] = se;
+    }
+    reduce_scatter32<2 * TT>(vals, lane);
+    constexpr int SHIFT = (2 * TT == 16) ? 1 : 0;  // lanes per result
+    if ((lane & ((1 << SHIFT) - 1)) == 0) {
+      const int idx = lane >> SHIFT, t = idx >> 1;
+      if (t >= j && t < T) {
+        if (idx & 1)
+          ec[t * KDA_MAX_T + j] = vals[0];
+        else if (t > j)
+          cc[t * KDA_MAX_T + j] = vals[0];
       }
     }
   }
@@ -392,24 +431,14 @@ __global__ void __launch_bounds__(NTHREADS)
   }
 }
 
-// Sum over the 128 key channels in the order token_prologue uses (thread c =
-// 32 w + l sums within its warp by butterfly, then warps 0..3 in order). Lane
-// l holds channels l, 32 + l, 64 + l, 96 + l.
-__device__ __forceinline__ float sum128_like_cta(const float (&x)[4]) {
-  float s = warp_sum(x[0]);
-#pragma unroll
-  for (int w = 1; w < 4; ++w) s = __fadd_rn(s, warp_sum(x[w]));
-  return s;
-}
-
 // After the ring kernel, one CTA per batch row: append k~ and G_P at ring
 // positions base..base+T-1 for every head, then reset hist_len[n] after a
 // fold when restart_hist_on_flush. One warp per head (the CTA has
 // APPEND_WARPS warps and loops when H is larger); lane l handles channels
 // l + 32 i, and each head's inputs for up to 8 tokens are loaded in one
 // batch, so the CTA waits for memory a few times rather than once per token.
-// The arithmetic of k~ and G repeats token_prologue and the ring kernel's
-// channel pass operation for operation.
+// k~ and G come from the same helpers and summation order as token_prologue
+// and the ring kernel's channel pass, so the bits match.
 constexpr int APPEND_WARPS = 16;
 
 __global__ void __launch_bounds__(32 * APPEND_WARPS)
@@ -453,13 +482,11 @@ __global__ void __launch_bounds__(32 * APPEND_WARPS)
         float sq[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) sq[i] = __fmul_rn(kv[tt][i], kv[tt][i]);
-        const float rk = __frcp_rn(__fsqrt_rn(__fadd_rn(sum128_like_cta(sq), L2_EPS)));
+        const float rk = inv_norm(sum_channels(sq[0], sq[1], sq[2], sq[3]));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = lane + 32 * i;
-          const float z = __fmul_rn(a_h, __fadd_rn(gv[tt][i], dtb[i]));
-          const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-z)));
-          const float g = __fmul_rn(p.lower_bound, sig);
+          const float g = gate_log_decay(a_h, gv[tt][i], dtb[i], p.lower_bound);
           const float G = __fadd_rn(G_prev[i], g);
           kc[(int64_t)(base + t) * KD + c] = float_to_bf16_bits(__fmul_rn(kv[tt][i], rk));
           gc[(int64_t)(base + t) * KD + c] = G;
