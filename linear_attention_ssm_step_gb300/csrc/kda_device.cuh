@@ -148,6 +148,7 @@ struct TokenSmem {
   float* vrow;   // [T][TV] v for this CTA's value rows
   float* beta;   // [KDA_MAX_T]
   float* kappa;  // [KDA_MAX_T] k_hat . q_hat
+  float* red;    // [3][128] per-channel products (single-token prologue only)
 };
 
 __device__ __forceinline__ float load_bf16(const kda_view& vw, int b, int t, int h, int c) {
@@ -248,6 +249,52 @@ __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h
         ts.beta[t] = __frcp_rn(__fadd_rn(1.0f, expf(-L.bl[s])));
       }
     }
+  }
+  __syncthreads();
+}
+
+// The same prologue for a single token, with all 128 threads busy (thread c =
+// channel c), for the T = 1 decode. Each thread's channel products go through
+// shared memory so that every lane can add channels l, l + 32, l + 64, l + 96
+// in the order sum_channels uses before the same butterfly: the results are
+// bit-identical to token_prologue's for that token.
+struct TokenLoads1 {
+  float q, k, g, v, bl;
+};
+
+__device__ __forceinline__ void prologue_issue1(const kda_params& p, int b, int h, int v0, int TV, TokenLoads1& L) {
+  const int c = threadIdx.x;
+  L.q = load_bf16(p.q, b, 0, h, c);
+  L.k = load_bf16(p.k, b, 0, h, c);
+  L.g = load_bf16(p.g_raw, b, 0, h, c);
+  L.v = c < TV ? load_bf16(p.v, b, 0, h, v0 + c) : 0.0f;
+  L.bl = c == 0 ? bf16_bits_to_float(static_cast<const uint16_t*>(
+                      p.beta_logit.ptr)[(int64_t)b * p.beta_logit.b_stride + (int64_t)h * p.beta_logit.h_stride])
+                : 0.0f;
+}
+
+__device__ __forceinline__ void token_prologue1(const kda_params& p, int h, int TV, const TokenSmem& ts,
+                                                const TokenLoads1& L) {
+  const int c = threadIdx.x, lane = c & 31;
+  ts.red[c] = __fmul_rn(L.q, L.q);
+  ts.red[KD + c] = __fmul_rn(L.k, L.k);
+  ts.red[2 * KD + c] = __fmul_rn(L.q, L.k);
+  const float g = gate_log_decay(expf(p.A_log[h]), L.g, p.dt_bias[(int64_t)h * KD + c], p.lower_bound);
+  ts.gg[c] = g;
+  ts.dd[c] = expf(g);
+  if (c < TV) ts.vrow[c] = L.v;
+  __syncthreads();
+  const float* r = ts.red;
+  const float rq = inv_norm(sum_channels(r[lane], r[lane + 32], r[lane + 64], r[lane + 96]));
+  const float rk = inv_norm(sum_channels(r[KD + lane], r[KD + lane + 32], r[KD + lane + 64], r[KD + lane + 96]));
+  // every lane of every warp takes part in the butterflies; thread 0 stores
+  const float sqk =
+      sum_channels(r[2 * KD + lane], r[2 * KD + lane + 32], r[2 * KD + lane + 64], r[2 * KD + lane + 96]);
+  ts.qh[c] = __fmul_rn(L.q, rq);
+  ts.kh[c] = __fmul_rn(L.k, rk);
+  if (c == 0) {
+    ts.kappa[0] = __fmul_rn(__fmul_rn(sqk, rq), rk);
+    ts.beta[0] = __frcp_rn(__fadd_rn(1.0f, expf(-L.bl)));
   }
   __syncthreads();
 }

@@ -29,7 +29,8 @@ __host__ __device__ constexpr size_t step_smem_bytes(int TV, int T) {
          + 64                           // 4 mbarriers (padded)
          + (size_t)T * KD * 4 * 4       // kh, qh, dd, gg
          + (size_t)T * TV * 4 * 2       // vrow, orow
-         + (size_t)KDA_MAX_T * 4 * 2;   // beta, kappa
+         + (size_t)KDA_MAX_T * 4 * 2    // beta, kappa
+         + (size_t)3 * KD * 4;          // single-token reduction products
 }
 
 // T = 1 kernels are capped at 85 registers so that six 128-thread CTAs (the
@@ -61,14 +62,21 @@ __global__ void __launch_bounds__(NTHREADS, MULTI ? 1 : 6)
   float* orow = ts.vrow + T * TV;
   ts.beta = orow + T * TV;
   ts.kappa = ts.beta + KDA_MAX_T;
+  ts.red = ts.kappa + KDA_MAX_T;
 
   uint16_t* outp = static_cast<uint16_t*>(p.out);
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
 
   const int n = p.state_indices[b];
-  constexpr int PT = MULTI ? (KDA_MAX_T + NWARPS - 1) / NWARPS : 1;  // tokens per warp in the prologue
-  TokenLoads<PT> first;  // issued alongside the index load; unused by an inactive row
-  prologue_issue(p, b, h, T, v0, TV, first);
+  // Token inputs, issued alongside the index load (unused by an inactive row):
+  // one token over all threads for T = 1, else up to PT tokens per warp.
+  constexpr int PT = (KDA_MAX_T + NWARPS - 1) / NWARPS;
+  TokenLoads<MULTI ? PT : 1> first;
+  TokenLoads1 first1;
+  if constexpr (MULTI)
+    prologue_issue(p, b, h, T, v0, TV, first);
+  else
+    prologue_issue1(p, b, h, v0, TV, first1);
   if (n < 0 || n >= p.N) {
     for (int i = tid; i < T * TV; i += NTHREADS) {
       const int t = i / TV, r = i - t * TV;
@@ -92,7 +100,10 @@ __global__ void __launch_bounds__(NTHREADS, MULTI ? 1 : 6)
     for (int i = lane; i < RW * KD; i += 32) sst[i] = gst[i];
   }
 
-  token_prologue(p, b, h, T, v0, TV, ts, first);
+  if constexpr (MULTI)
+    token_prologue(p, b, h, T, v0, TV, ts, first);
+  else
+    token_prologue1(p, h, TV, ts, first1);
 
   bool ok = true;
   if constexpr (BULK) {
