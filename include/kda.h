@@ -164,7 +164,7 @@ typedef struct {
 kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params* r, void* stream);
 
 /* Launch configurations: index -> rows of V per CTA (tile). kda_params.config_override
-   takes an index; kda_verify_ring caps the tile at 64 rows. */
+   takes an index. */
 int32_t kda_num_configs(void);
 int32_t kda_config_tile_v(int32_t config);
 /* The configuration kda_decode (T = 1) and kda_verify (T > 1) pick for B rows

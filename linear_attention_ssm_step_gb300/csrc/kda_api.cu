@@ -111,7 +111,7 @@ int pick_tile(const kda_params* p, int T) {
 
 int pick_ring_tile(const kda_params* p, int T) {
   const int cfg = p->config_override >= 0 ? p->config_override : kda_select_ring_config(p->B, T);
-  return kTileV[cfg] > 64 ? 64 : kTileV[cfg];
+  return kTileV[cfg];
 }
 
 }  // namespace
@@ -142,12 +142,13 @@ int32_t kda_select_config(int32_t B, int32_t T) {
   return 3;               // 128 rows
 }
 
-// The ring kernel keeps each row in fp32 across the call and caps its tile at
-// 64 rows; its own policy, same measurements.
+// The ring kernel's own policy (its per-head work is larger: whole heads,
+// with 8 warps, once a batch fills the machine).
 int32_t kda_select_ring_config(int32_t B, int32_t T) {
   if (B < 0 || T < 1 || T > KDA_MAX_T) return -1;
-  if (B <= 2) return 0;  // 16 rows
-  return 2;              // 64 rows
+  if (B <= 2) return 0;   // 16 rows
+  if (B <= 64) return 2;  // 64 rows
+  return 3;               // 128 rows, 8 warps
 }
 
 const char* kda_last_error(void) { return g_err; }

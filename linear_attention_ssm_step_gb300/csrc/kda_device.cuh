@@ -157,8 +157,8 @@ __device__ __forceinline__ float load_bf16(const kda_view& vw, int b, int t, int
 }
 
 // The per-token prologue of (row b, head h): L2 norms, k_hat . q_hat, the gate
-// and beta, for every token into shared memory. Warp w handles tokens
-// w, w + 4, ...; lane l handles key channels l + 32 i (i < 4). A warp's
+// and beta, for every token into shared memory. Warp w of NW handles tokens
+// w, w + NW, ...; lane l handles key channels l + 32 i (i < 4). A warp's
 // token inputs (up to PT tokens) are loaded into registers together, so that
 // their latencies overlap; prologue_issue starts those loads (callers issue
 // them next to the slot-index load), token_prologue finishes.
@@ -172,13 +172,13 @@ struct TokenLoads {
   float q[PT][4], k[PT][4], g[PT][4], v[PT][4], bl[PT];
 };
 
-template <int PT>
+template <int PT, int NW = NWARPS>
 __device__ __forceinline__ void prologue_issue(const kda_params& p, int b, int h, int T, int v0, int TV,
                                                TokenLoads<PT>& L) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int s = 0; s < PT; ++s) {
-    const int t = warp + NWARPS * s;
+    const int t = warp + NW * s;
     L.bl[s] = 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -212,7 +212,7 @@ __device__ __forceinline__ float gate_log_decay(float a_h, float g_raw, float dt
   return __fmul_rn(lower_bound, __frcp_rn(__fadd_rn(1.0f, expf(-z))));
 }
 
-template <int PT>
+template <int PT, int NW = NWARPS>
 __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h, int T, int v0, int TV,
                                                const TokenSmem& ts, const TokenLoads<PT>& L) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -222,7 +222,7 @@ __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h
   for (int i = 0; i < 4; ++i) dtb[i] = p.dt_bias[(int64_t)h * KD + lane + 32 * i];
 #pragma unroll
   for (int s = 0; s < PT; ++s) {
-    const int t = warp + NWARPS * s;
+    const int t = warp + NW * s;
     if (t < T) {
       float qq[4], kk[4], qk[4];
 #pragma unroll

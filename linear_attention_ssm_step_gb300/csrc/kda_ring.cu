@@ -25,7 +25,8 @@
 // and uses the rounded state as the base (G restarts at 0); otherwise S_h
 // stays in fp32 and G continues from G_{h-1}.
 //
-// One CTA (128 threads) per (batch row, head, tile of TV = 16, 32 or 64 rows):
+// One CTA per (batch row, head, tile of TV = 16, 32, 64 or 128 rows), 4 warps
+// (8 for the whole-head tile):
 //   1. slot lookup, checkpoint bulk copy, hist_len check (outside [0, W]:
 //      error bit, skip);
 //   2. per-token prologue; per channel: k~, G, d_t, P_t, the query vectors
@@ -129,12 +130,15 @@ __device__ __forceinline__ void reduce_scatter32(float (&v)[NV], int lane) {
   }
 }
 
-template <int TV, bool BULK, int TT>
-__global__ void __launch_bounds__(NTHREADS)
+template <int TV, bool BULK, int TT, int NW>
+__global__ void __launch_bounds__(32 * NW)
     kda_ring_kernel(const kda_params p, const kda_ring_params rp, const int T, const int tiles) {
-  static_assert(TV % 16 == 0 && TV >= 16 && TV <= 64, "ring tile must be 16, 32 or 64 rows");
+  static_assert(TV % 16 == 0 && TV >= 16 && TV <= 128, "ring tile must be 16, 32, 64 or 128 rows");
   static_assert(TT == 8 || TT == 16, "token slots");
-  constexpr int RW = TV / NWARPS;         // rows per warp
+  static_assert(NW == 4 || NW == 8, "4 or 8 warps");
+  static_assert(TV % (4 * NW) == 0, "every warp owns whole 4-row groups");
+  constexpr int NT = 32 * NW;             // threads
+  constexpr int RW = TV / NW;             // rows per warp
   constexpr int RQ = RW / ROWS_PER_WARP;  // 4-row groups per warp
   constexpr int RG = RQ < 2 ? RQ : 2;     // groups processed together
   constexpr int NV = 2 * TT;              // sums per row before the reduce-scatter
@@ -174,11 +178,11 @@ __global__ void __launch_bounds__(NTHREADS)
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
 
   const int n = p.state_indices[b];
-  constexpr int PT = TT / NWARPS;  // tokens per warp in the prologue
-  TokenLoads<PT> first;            // issued alongside the index load; unused by an inactive row
-  prologue_issue(p, b, h, T, v0, TV, first);
+  constexpr int PT = TT / NW;  // tokens per warp in the prologue
+  TokenLoads<PT> first;        // issued alongside the index load; unused by an inactive row
+  prologue_issue<PT, NW>(p, b, h, T, v0, TV, first);
   if (n < 0 || n >= p.N) {
-    for (int i = tid; i < T * TV; i += NTHREADS) {
+    for (int i = tid; i < T * TV; i += NT) {
       const int t = i / TV, r = i - t * TV;
       outp[out_base + (int64_t)t * p.out_t_stride + r] = 0;
     }
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(NTHREADS)
       if (!mbar_wait_bounded(&mbar[warp], 0) && lane == 0 && p.error_word != nullptr)
         atomicOr(p.error_word, KDA_ERR_TIMEOUT);  // the copy must land before the CTA leaves
     }
-    for (int i = tid; i < T * TV; i += NTHREADS) {
+    for (int i = tid; i < T * TV; i += NT) {
       const int t = i / TV, r = i - t * TV;
       outp[out_base + (int64_t)t * p.out_t_stride + r] = 0;
     }
@@ -235,24 +239,25 @@ __global__ void __launch_bounds__(NTHREADS)
     for (int i = lane; i < RW * KD; i += 32) sst[i] = gst[i];
   }
 
-  token_prologue(p, b, h, T, v0, TV, ts, first);  // ends with a CTA barrier (publishes hbar's init)
+  token_prologue<PT, NW>(p, b, h, T, v0, TV, ts, first);  // ends with a CTA barrier (publishes hbar's init)
 
   bool hist_ok = true;
   if (hist > 0) hist_ok = mbar_wait_bounded(hbar, 0);
   if (!hist_ok && tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
 
-  // Channel pass, thread c = key channel c.
+  // Channel pass, thread c (and c + 128 with 8 warps) = key channel c.
   {
-    const int c = tid;
+    const int c = tid & (KD - 1), part = tid / KD;
     const float Gl = hist > 0 ? hk[(hist - 1) * KD + c] : 0.0f;  // G_{h-1}
-    cdec[c] = hist > 0 ? expf(Gl) : 1.0f;
-    for (int jx = 0; jx < hist; ++jx) {  // in place: G_j -> exp(G_{h-1} - G_j) k~_j
+    if (part == 0) cdec[c] = hist > 0 ? expf(Gl) : 1.0f;
+    if (NT > KD) __syncthreads();  // every thread has read G_{h-1} before entry h-1 is overwritten
+    for (int jx = part; jx < hist; jx += NT / KD) {  // in place: G_j -> exp(G_{h-1} - G_j) k~_j
       const float kj = bf16_bits_to_float(hkb[jx * KD + c]);
       hk[jx * KD + c] = __fmul_rn(expf(__fsub_rn(Gl, hk[jx * KD + c])), kj);
     }
     float G_prev = fold ? 0.0f : Gl;
     float P = 1.0f;
-    for (int t = 0; t < T; ++t) {
+    for (int t = 0; t < (part == 0 ? T : 0); ++t) {
       const float kt = round_bf16(ts.kh[t * KD + c]);
       const float G = __fadd_rn(G_prev, ts.gg[t * KD + c]);
       const float d = expf(__fsub_rn(G, G_prev));
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(NTHREADS)
   // l + 32 i; w_tj is a running product of the token decays. A column's 2 TT
   // partial sums (cc and ec for every t) are reduced together, see
   // reduce_scatter32.
-  for (int j = warp; j < T; j += NWARPS) {
+  for (int j = warp; j < T; j += NW) {
     float kj[4], wgt[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(NTHREADS)
     }
   }
   __syncthreads();
-  for (int i = tid; i < T * TV; i += NTHREADS) {
+  for (int i = tid; i < T * TV; i += NT) {
     const int t = i / TV, rr = i - t * TV;
     outp[out_base + (int64_t)t * p.out_t_stride + rr] = float_to_bf16_bits(orow[i]);
     if (ok) uc[(int64_t)(base + t) * KD + v0 + rr] = float_to_bf16_bits(urow[i]);
@@ -503,13 +508,14 @@ __global__ void __launch_bounds__(32 * APPEND_WARPS)
 
 template <int TV, bool BULK, int TT>
 static cudaError_t launch_ring_one(const kda_params& p, int T, const kda_ring_params& r, cudaStream_t s) {
-  auto kern = kda_ring_kernel<TV, BULK, TT>;
+  constexpr int NW = TV == 128 ? 8 : 4;  // a whole-head tile gets 8 warps
+  auto kern = kda_ring_kernel<TV, BULK, TT, NW>;
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
   cudaError_t e = set_smem_limit_once(kern, ring_smem_bytes(TV, KDA_MAX_T, 64), smem_set);
   if (e != cudaSuccess) return e;
   const int tiles = KD / TV;
   const long long blocks = (long long)p.B * p.H * tiles;
-  kern<<<(unsigned)blocks, NTHREADS, ring_smem_bytes(TV, T, r.W), s>>>(p, r, T, tiles);
+  kern<<<(unsigned)blocks, 32 * NW, ring_smem_bytes(TV, T, r.W), s>>>(p, r, T, tiles);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int append_warps = p.H < APPEND_WARPS ? p.H : APPEND_WARPS;
@@ -525,11 +531,11 @@ static cudaError_t launch_ring_tv(const kda_params& p, int T, const kda_ring_par
 
 cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, int tile_v, bool bulk,
                         cudaStream_t s) {
-  if (tile_v > 64) tile_v = 64;
   switch (tile_v) {
     case 16: return launch_ring_tv<16>(p, T, r, bulk, s);
     case 32: return launch_ring_tv<32>(p, T, r, bulk, s);
     case 64: return launch_ring_tv<64>(p, T, r, bulk, s);
+    case 128: return launch_ring_tv<128>(p, T, r, bulk, s);
     default: return cudaErrorInvalidValue;
   }
 }
