@@ -29,4 +29,6 @@ from .kda_oracle import (  # noqa: F401
     kda_verify_ring,
     RING_ERR_HIST_LEN,
     L2_EPS,
+    GATE_RAW,
+    GATE_PRECOMPUTED,
 )

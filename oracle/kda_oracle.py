@@ -117,15 +117,29 @@ def beta_from_logit(beta_logit):
     return _sigmoid(np.asarray(beta_logit, dtype=np.float64))
 
 
-def prologue(q, k, g_raw, beta_logit, A_log, dt_bias, lower_bound):
+GATE_RAW = 0
+GATE_PRECOMPUTED = 1
+
+
+def prologue(q, k, g_raw, beta_logit, A_log, dt_bias, lower_bound, gate_mode=GATE_RAW):
     """The per-(row, head) quantities the state update needs.
 
+    gate_mode GATE_RAW: g from the raw gate (gate_log_decay), beta =
+    sigmoid(beta_logit). GATE_PRECOMPUTED ([decode] section "T=1 fast path
+    inside recurrent_kda": the API-default form with log-space g and
+    pre-sigmoided beta, decay exp(g)): g_raw already holds g and beta_logit
+    holds beta; A_log, dt_bias and lower_bound are not used.
     Returns (q_hat, k_hat, g, d, beta) with d = exp(g).
     """
     q_hat = l2_normalize(q)
     k_hat = l2_normalize(k)
-    g = gate_log_decay(g_raw, A_log, dt_bias, lower_bound)
-    return q_hat, k_hat, g, np.exp(g), beta_from_logit(beta_logit)
+    if gate_mode == GATE_PRECOMPUTED:
+        g = np.asarray(g_raw, dtype=np.float64)
+        beta = np.asarray(beta_logit, dtype=np.float64)
+    else:
+        g = gate_log_decay(g_raw, A_log, dt_bias, lower_bound)
+        beta = beta_from_logit(beta_logit)
+    return q_hat, k_hat, g, np.exp(g), beta
 
 
 def decode_step_math(S, q_hat, k_hat, v, d, beta, scale=1.0):
@@ -148,7 +162,7 @@ def _active_mask(state_indices, N):
 
 
 def kda_decode(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
-               lower_bound=-5.0, scale=1.0):
+               lower_bound=-5.0, scale=1.0, gate_mode=GATE_RAW):
     """T=1 decode ([decode] opening paragraph).
 
     state: [N, H, V, K] fp64 holding bf16 values (memory layout, K contiguous).
@@ -174,7 +188,7 @@ def kda_decode(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
     q_hat, k_hat, _, d, beta = prologue(
         np.asarray(q, np.float64)[rows], np.asarray(k, np.float64)[rows],
         np.asarray(g_raw, np.float64)[rows], np.asarray(beta_logit, np.float64)[rows],
-        A_log, dt_bias, lower_bound)
+        A_log, dt_bias, lower_bound, gate_mode)
     S = np.swapaxes(state[slots], -1, -2)  # [nA, H, K, V]
     S_new, o, _ = decode_step_math(S, q_hat, k_hat, np.asarray(v, np.float64)[rows],
                                    d, beta, scale)
@@ -184,7 +198,7 @@ def kda_decode(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
 
 
 def kda_verify(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
-               lower_bound=-5.0, scale=1.0):
+               lower_bound=-5.0, scale=1.0, gate_mode=GATE_RAW):
     """T-token speculative verify: T single decode steps on the same slots.
 
     q, k, g_raw: [B, T, H, K]; v: [B, T, H, V]; beta_logit: [B, T, H].
@@ -199,7 +213,7 @@ def kda_verify(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
         state, out[:, t] = kda_decode(state, state_indices, q[:, t], np.asarray(k)[:, t],
                                       np.asarray(v)[:, t], np.asarray(g_raw)[:, t],
                                       np.asarray(beta_logit)[:, t], A_log, dt_bias,
-                                      lower_bound, scale)
+                                      lower_bound, scale, gate_mode)
     return state, out
 
 
@@ -239,7 +253,7 @@ def ring_fold_closed_form(S0, k_hist, u_hist, G_hist):
 
 def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
                     k_cache, u_cache, g_cache, hist_len, flush_min,
-                    restart_hist_on_flush=True, lower_bound=-5.0, scale=1.0):
+                    restart_hist_on_flush=True, lower_bound=-5.0, scale=1.0, gate_mode=GATE_RAW):
     """Ring-cache verify with replay and fold ([ring] "What it does", "API", "Caching").
 
     state (checkpoint): [N, H, V, K]; k_cache: [N, H, W, K] bf16 k_hat;
@@ -296,7 +310,7 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
             new["error_word"] |= RING_ERR_HIST_LEN
             continue
         q_hat, k_hat, g, _, beta = prologue(q[b], k[b], g_raw[b], beta_logit[b],
-                                            A_log, dt_bias, lower_bound)
+                                            A_log, dt_bias, lower_bound, gate_mode)
         S0 = np.swapaxes(state[n], -1, -2)  # [H, K, V]
         S = ring_replay(S0, k_cache[n, :, :h], u_cache[n, :, :h], g_cache[n, :, :h])
         if h >= flush_min:

@@ -362,6 +362,25 @@ def pin_verify_is_stepwise(m):
     assert (out[1] == 0).all()
 
 
+def pin_precomputed_gate_convention(m):
+    """Log-space g and beta given directly: decay exp(g) per key channel, beta as
+    given; fed the raw form's own g and beta it reproduces the raw form exactly."""
+    rng = np.random.default_rng(19)
+    p = small_problem(rng, B=3, H=2, K=8, V=8, N=4)
+    idx = np.array([3, -1, 1])
+    raw_state, raw_out = _decode(m, p, idx)
+    g = m.gate_log_decay(p["g_raw"], p["A_log"], p["dt_bias"], LB)
+    beta = m.beta_from_logit(p["beta_logit"])
+    pre_state, pre_out = m.kda_decode(p["state"], idx, p["q"], p["k"], p["v"], g, beta, None, None,
+                                      gate_mode=m.GATE_PRECOMPUTED)
+    assert np.array_equal(pre_state, raw_state) and np.array_equal(pre_out, raw_out)
+    # closed form: S = 0 row, g = log(1/2) everywhere, beta = 1/4
+    q_hat, k_hat, gg, d, bb = m.prologue(p["q"][0], p["k"][0], np.full((2, 8), math.log(0.5)),
+                                         np.full(2, 0.25), None, None, LB, m.GATE_PRECOMPUTED)
+    assert np.allclose(d, 0.5, rtol=1e-15) and (bb == 0.25).all()
+    assert np.array_equal(gg, np.full((2, 8), math.log(0.5)))
+
+
 # ---------------------------------------------------------------- ring
 
 def ring_problem(rng, B=3, H=2, K=8, V=8, N=5, T=3, W=12, hist=None):

@@ -56,6 +56,10 @@ MUTATIONS = [
     ("hist_len kept on fold", 'new["hist_len"][n] = 0', 'new["hist_len"][n] = h'),
     ("bad hist_len accepted", "if h < 0 or h > W:", "if h < 0 or h > W + 1:"),
     ("ring decay from g, not G", "D = np.exp(G_P - G_prev)", "D = np.exp(g[t])"),
+    ("precomputed beta sigmoided again", "beta = np.asarray(beta_logit, dtype=np.float64)\n",
+     "beta = beta_from_logit(beta_logit)\n"),
+    ("precomputed g used as the decay", "g = np.asarray(g_raw, dtype=np.float64)\n",
+     "g = np.log(np.asarray(g_raw, dtype=np.float64) + 6.0)\n"),
     ("ring u from undecayed state", '(v[b, t] - np.einsum("hkv,hk->hv", S1, k_t))',
      '(v[b, t] - np.einsum("hkv,hk->hv", S, k_t))'),
 ]
