@@ -14,7 +14,8 @@ carries:
                back inside the timed region (the pool stays resident);
   roofline     the decode kernel's achieved GB/s against the measured HBM peak;
   cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload;
-  sweep        T=1 decode at B = 1..512, T=8 verify and T=8 ring verify at
+  sweep        T=1 decode at B = 1..512 (and with the pre-computed gate
+               convention at B = 8, 512), T=8 verify and T=8 ring verify at
                B = 1, 32, 512 (0/50/100% of rows folding), all L2-cold.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-sweep]
@@ -277,7 +278,7 @@ def e2e(dev, h, steps, warmup, world):
 
 def sweep(dev, steps=20, warmup=3):
     flush = L2Flush(dev)
-    res = {"t1_decode": [], "t8_verify": [], "t8_ring_w32": []}
+    res = {"t1_decode": [], "t8_verify": [], "t8_ring_w32": []}  # more keys added below
     for B in (1, 8, 16, 32, 64, 128, 256, 512):
         w = workloads.decode_inputs(B, B + 128, seed=10 + B, layout="fused")
         wd = w.to(dev)
@@ -288,6 +289,17 @@ def sweep(dev, steps=20, warmup=3):
         nb = traffic.decode_bytes(B)
         res["t1_decode"].append({"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1),
                                  "us_direct": round(td * 1e3, 2), "config": kda.kda_select_config(B, 1)})
+        del w, wd
+    res["t1_decode_precomputed_gate"] = []
+    for B in (8, 512):
+        w = workloads.decode_inputs(B, B + 128, seed=40 + B, layout="fused", gate_mode=1)
+        wd = w.to(dev)
+        out = torch.empty((B, 12, 128), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_decode(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
+                                    wd.beta_logit, None, None, out=out, gate_mode=kda.KDA_GATE_PRECOMPUTED)
+        t = statistics.median(time_calls(graphed(fn), steps, warmup, before=flush))
+        res["t1_decode_precomputed_gate"].append({"B": B, "us": round(t * 1e3, 2),
+                                                  "GB/s": round(traffic.decode_bytes(B) / t / 1e6, 1)})
         del w, wd
     for B in (1, 32, 512):
         w = workloads.decode_inputs(B, B + 64, seed=20 + B, T=8)

@@ -69,6 +69,12 @@ typedef enum {
 #define KDA_ERR_HIST_LEN 1u /* a ring slot's hist_len was outside [0, W]; that slot was skipped */
 #define KDA_ERR_TIMEOUT 2u  /* a bounded wait for an async copy gave up; that tile was skipped */
 
+/* kda_params.gate_mode: how g_raw and beta_logit are read (source: PR #4417, "T=1 fast path
+   inside recurrent_kda", which covers both recurrent_kda calling conventions). */
+#define KDA_GATE_RAW 0         /* g = lower_bound * sigmoid(exp(A_log) * (g_raw + dt_bias)), beta = sigmoid(beta_logit) */
+#define KDA_GATE_PRECOMPUTED 1 /* g_raw holds the log-space decay g, beta_logit holds beta; A_log, dt_bias,
+                                  lower_bound unused (A_log and dt_bias may be NULL) */
+
 /* Largest number of tokens kda_verify and kda_verify_ring accept. */
 #define KDA_MAX_T 16
 
@@ -95,8 +101,9 @@ typedef struct {
   int32_t V; /* value dimension; must be 128 */
   int32_t N; /* slots in the state pool, >= 0; N == 0 makes every row inactive */
 
-  kda_view q, k, v, g_raw; /* bf16 [B][T][H][128] */
-  kda_view beta_logit;     /* bf16 [B][T][H]; h_stride steps heads (D = 1) */
+  kda_view q, k, v, g_raw; /* bf16 [B][T][H][128]; g_raw is g itself under KDA_GATE_PRECOMPUTED */
+  kda_view beta_logit;     /* bf16 [B][T][H]; h_stride steps heads (D = 1); beta itself under
+                              KDA_GATE_PRECOMPUTED */
   const float* A_log;      /* fp32 [H] */
   const float* dt_bias;    /* fp32 [H][K] */
   float lower_bound;       /* gate lower bound, the pages use -5 */
@@ -111,6 +118,7 @@ typedef struct {
 
   uint32_t* error_word;    /* optional device word (NULL = none); KDA_ERR_* bits are ORed in */
   int32_t config_override; /* -1: kda_select_config decides; else an index < kda_num_configs() */
+  int32_t gate_mode;       /* KDA_GATE_RAW (0) or KDA_GATE_PRECOMPUTED (1) */
 } kda_params;
 
 /*

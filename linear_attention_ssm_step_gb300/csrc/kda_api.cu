@@ -61,6 +61,8 @@ kda_status check_params(const kda_params* p, int T, bool* bulk) {
   if (T < 1 || T > KDA_MAX_T) return fail(KDA_EUNSUPPORTED, "T = %d outside 1..%d", T, KDA_MAX_T);
   if ((long long)p->B * p->H * 128 > 0x7fffffffLL)
     return fail(KDA_EUNSUPPORTED, "B * H = %lld is too large for one launch", (long long)p->B * p->H);
+  if (p->gate_mode != KDA_GATE_RAW && p->gate_mode != KDA_GATE_PRECOMPUTED)
+    return fail(KDA_EINVAL, "gate_mode = %d is neither KDA_GATE_RAW nor KDA_GATE_PRECOMPUTED", p->gate_mode);
   if (p->config_override < -1 || p->config_override >= kNumConfigs)
     return fail(KDA_EINVAL, "config_override = %d outside -1..%d", p->config_override, kNumConfigs - 1);
   if (!(p->lower_bound == p->lower_bound) || p->lower_bound > 3.0e38f || p->lower_bound < -3.0e38f)
@@ -75,9 +77,12 @@ kda_status check_params(const kda_params* p, int T, bool* bulk) {
   if ((s = check_view("v", p->v, 128)) != KDA_OK) return s;
   if ((s = check_view("g_raw", p->g_raw, 128)) != KDA_OK) return s;
   if ((s = check_view("beta_logit", p->beta_logit, 1)) != KDA_OK) return s;
-  if (p->A_log == nullptr || !aligned(p->A_log, 4)) return fail(KDA_EINVAL, "A_log is NULL or not 4-byte aligned");
-  if (p->dt_bias == nullptr || !aligned(p->dt_bias, 4))
-    return fail(KDA_EINVAL, "dt_bias is NULL or not 4-byte aligned");
+  if (p->gate_mode == KDA_GATE_RAW) {
+    if (p->A_log == nullptr || !aligned(p->A_log, 4))
+      return fail(KDA_EINVAL, "A_log is NULL or not 4-byte aligned");
+    if (p->dt_bias == nullptr || !aligned(p->dt_bias, 4))
+      return fail(KDA_EINVAL, "dt_bias is NULL or not 4-byte aligned");
+  }
   if (p->state_indices == nullptr || !aligned(p->state_indices, 4))
     return fail(KDA_EINVAL, "state_indices is NULL or not 4-byte aligned");
   if (p->out == nullptr || !aligned(p->out, 2)) return fail(KDA_EINVAL, "out is NULL or not 2-byte aligned");

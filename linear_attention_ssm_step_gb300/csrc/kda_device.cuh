@@ -212,14 +212,32 @@ __device__ __forceinline__ float gate_log_decay(float a_h, float g_raw, float dt
   return __fmul_rn(lower_bound, __frcp_rn(__fadd_rn(1.0f, expf(-z))));
 }
 
+__device__ __forceinline__ float sigmoid(float x) { return __frcp_rn(__fadd_rn(1.0f, expf(-x))); }
+
+// The gate of the call's convention (KDA_GATE_RAW or KDA_GATE_PRECOMPUTED):
+// log-decay g of one channel, and beta from its input.
+struct Gate {
+  bool raw;
+  float a_h, lower_bound;
+  __device__ __forceinline__ Gate(const kda_params& p, int h)
+      : raw(p.gate_mode == KDA_GATE_RAW), a_h(raw ? expf(p.A_log[h]) : 0.0f), lower_bound(p.lower_bound) {}
+  __device__ __forceinline__ float dt_bias(const kda_params& p, int h, int c) const {
+    return raw ? p.dt_bias[(int64_t)h * KD + c] : 0.0f;
+  }
+  __device__ __forceinline__ float g(float g_in, float dtb) const {
+    return raw ? gate_log_decay(a_h, g_in, dtb, lower_bound) : g_in;
+  }
+  __device__ __forceinline__ float beta(float b_in) const { return raw ? sigmoid(b_in) : b_in; }
+};
+
 template <int PT, int NW = NWARPS>
 __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h, int T, int v0, int TV,
                                                const TokenSmem& ts, const TokenLoads<PT>& L) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float a_h = expf(p.A_log[h]);
+  const Gate gate(p, h);
   float dtb[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) dtb[i] = p.dt_bias[(int64_t)h * KD + lane + 32 * i];
+  for (int i = 0; i < 4; ++i) dtb[i] = gate.dt_bias(p, h, lane + 32 * i);
 #pragma unroll
   for (int s = 0; s < PT; ++s) {
     const int t = warp + NW * s;
@@ -237,7 +255,7 @@ __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int c = lane + 32 * i;
-        const float g = gate_log_decay(a_h, L.g[s][i], dtb[i], p.lower_bound);
+        const float g = gate.g(L.g[s][i], dtb[i]);
         ts.gg[t * KD + c] = g;
         ts.dd[t * KD + c] = expf(g);
         ts.qh[t * KD + c] = __fmul_rn(L.q[s][i], rq);
@@ -246,7 +264,7 @@ __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h
       }
       if (lane == 0) {
         ts.kappa[t] = __fmul_rn(__fmul_rn(sqk, rq), rk);
-        ts.beta[t] = __frcp_rn(__fadd_rn(1.0f, expf(-L.bl[s])));
+        ts.beta[t] = gate.beta(L.bl[s]);
       }
     }
   }
@@ -279,7 +297,8 @@ __device__ __forceinline__ void token_prologue1(const kda_params& p, int h, int 
   ts.red[c] = __fmul_rn(L.q, L.q);
   ts.red[KD + c] = __fmul_rn(L.k, L.k);
   ts.red[2 * KD + c] = __fmul_rn(L.q, L.k);
-  const float g = gate_log_decay(expf(p.A_log[h]), L.g, p.dt_bias[(int64_t)h * KD + c], p.lower_bound);
+  const Gate gate(p, h);
+  const float g = gate.g(L.g, gate.dt_bias(p, h, c));
   ts.gg[c] = g;
   ts.dd[c] = expf(g);
   if (c < TV) ts.vrow[c] = L.v;
@@ -294,7 +313,7 @@ __device__ __forceinline__ void token_prologue1(const kda_params& p, int h, int 
   ts.kh[c] = __fmul_rn(L.k, rk);
   if (c == 0) {
     ts.kappa[0] = __fmul_rn(__fmul_rn(sqk, rq), rk);
-    ts.beta[0] = __frcp_rn(__fadd_rn(1.0f, expf(-L.bl)));
+    ts.beta[0] = gate.beta(L.bl);
   }
   __syncthreads();
 }

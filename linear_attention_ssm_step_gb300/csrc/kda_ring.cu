@@ -459,12 +459,12 @@ __global__ void __launch_bounds__(32 * APPEND_WARPS)
   for (int h = warp; h < p.H; h += blockDim.x >> 5) {
     uint16_t* kc = static_cast<uint16_t*>(rp.k_cache) + (int64_t)n * rp.k_slot_stride + (int64_t)h * rp.W * KD;
     float* gc = static_cast<float*>(rp.g_cache) + (int64_t)n * rp.g_slot_stride + (int64_t)h * rp.W * KD;
-    const float a_h = expf(p.A_log[h]);
+    const Gate gate(p, h);
     float G_prev[4], dtb[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int c = lane + 32 * i;
-      dtb[i] = p.dt_bias[(int64_t)h * KD + c];
+      dtb[i] = gate.dt_bias(p, h, c);
       G_prev[i] = (!fold && hist > 0) ? gc[(int64_t)(hist - 1) * KD + c] : 0.0f;
     }
     for (int t0 = 0; t0 < T; t0 += 8) {
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(32 * APPEND_WARPS)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = lane + 32 * i;
-          const float g = gate_log_decay(a_h, gv[tt][i], dtb[i], p.lower_bound);
+          const float g = gate.g(gv[tt][i], dtb[i]);
           const float G = __fadd_rn(G_prev[i], g);
           kc[(int64_t)(base + t) * KD + c] = float_to_bf16_bits(__fmul_rn(kv[tt][i], rk));
           gc[(int64_t)(base + t) * KD + c] = G;

@@ -17,6 +17,7 @@ KDA_OK, KDA_EINVAL, KDA_EUNSUPPORTED, KDA_ELAUNCH = 0, 1, 2, 3
 KDA_ERR_HIST_LEN = 1
 KDA_ERR_TIMEOUT = 2
 KDA_MAX_T = 16
+KDA_GATE_RAW, KDA_GATE_PRECOMPUTED = 0, 1
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_EINVAL", 2: "KDA_EUNSUPPORTED", 3: "KDA_ELAUNCH"}
 
 
@@ -44,6 +45,7 @@ class KdaParams(ctypes.Structure):
         ("out", ctypes.c_void_p), ("out_b_stride", ctypes.c_int64),
         ("out_t_stride", ctypes.c_int64), ("out_h_stride", ctypes.c_int64),
         ("error_word", ctypes.c_void_p), ("config_override", ctypes.c_int32),
+        ("gate_mode", ctypes.c_int32),
     ]
 
 
@@ -127,7 +129,7 @@ def _stream_handle(stream, device):
 
 
 def _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
-            lower_bound, scale, error_word, config_override):
+            lower_bound, scale, error_word, config_override, gate_mode):
     has_T = T is not None
     B = q.shape[0]
     H = q.shape[-2]
@@ -139,12 +141,14 @@ def _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, ou
     _need(state_indices, "state_indices", torch.int32)
     if state_indices.shape != (B,) or (B > 0 and state_indices.stride(0) != 1):
         raise ValueError("state_indices must be a contiguous [B] tensor")
-    _need(A_log, "A_log", torch.float32)
-    _need(dt_bias, "dt_bias", torch.float32)
-    if A_log.numel() != H or not A_log.is_contiguous():
-        raise ValueError("A_log must be a contiguous [H] tensor")
-    if dt_bias.numel() != H * 128 or not dt_bias.is_contiguous():
-        raise ValueError("dt_bias must be a contiguous [H, 128] tensor")
+    if gate_mode == KDA_GATE_RAW or A_log is not None:
+        _need(A_log, "A_log", torch.float32)
+        if A_log.numel() != H or not A_log.is_contiguous():
+            raise ValueError("A_log must be a contiguous [H] tensor")
+    if gate_mode == KDA_GATE_RAW or dt_bias is not None:
+        _need(dt_bias, "dt_bias", torch.float32)
+        if dt_bias.numel() != H * 128 or not dt_bias.is_contiguous():
+            raise ValueError("dt_bias must be a contiguous [H, 128] tensor")
     _need(out, "out", torch.bfloat16)
     if out.stride(-1) != 1:
         raise ValueError("out must have a contiguous last dim")
@@ -156,8 +160,8 @@ def _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, ou
     p.v = _view(v, "v", has_T, 128)
     p.g_raw = _view(g_raw, "g_raw", has_T, 128)
     p.beta_logit = _view(beta_logit, "beta_logit", has_T, 1)
-    p.A_log = A_log.data_ptr()
-    p.dt_bias = dt_bias.data_ptr()
+    p.A_log = None if A_log is None else A_log.data_ptr()
+    p.dt_bias = None if dt_bias is None else dt_bias.data_ptr()
     p.lower_bound = lower_bound
     p.scale = scale
     p.state = state.data_ptr()
@@ -172,31 +176,35 @@ def _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, ou
         _need(error_word, "error_word", torch.int32)
         p.error_word = error_word.data_ptr()
     p.config_override = config_override
+    p.gate_mode = gate_mode
     return p
 
 
 def kda_decode(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
-               lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, stream=None):
+               lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
+               stream=None):
     """T=1 decode. q, k, v, g_raw: bf16 [B, H, 128] views (any row and head stride);
     beta_logit: bf16 [B, H]; state: bf16 [N, H, 128, 128] pool updated in place;
-    returns out bf16 [B, H, 128]."""
+    returns out bf16 [B, H, 128]. With gate_mode=KDA_GATE_PRECOMPUTED, g_raw holds
+    log-space g, beta_logit holds beta, and A_log / dt_bias may be None."""
     if out is None:
         out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
     p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
-                lower_bound, scale, error_word, config_override)
+                lower_bound, scale, error_word, config_override, gate_mode)
     _check(load_library().kda_decode(ctypes.byref(p), _stream_handle(stream, q.device)))
     return out
 
 
 def kda_verify(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
-               lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, stream=None):
+               lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
+               stream=None):
     """T-token verify. q, k, v, g_raw: bf16 [B, T, H, 128]; beta_logit: bf16 [B, T, H];
     returns out bf16 [B, T, H, 128]."""
     B, T, H = q.shape[0], q.shape[1], q.shape[2]
     if out is None:
         out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=q.device)
     p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
-                lower_bound, scale, error_word, config_override)
+                lower_bound, scale, error_word, config_override, gate_mode)
     _check(load_library().kda_verify(ctypes.byref(p), T, _stream_handle(stream, q.device)))
     return out
 
@@ -204,14 +212,14 @@ def kda_verify(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
 def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
                     k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush=True,
                     out=None, lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1,
-                    stream=None):
+                    gate_mode=KDA_GATE_RAW, stream=None):
     """Ring-cache verify with replay and fold. k_cache, u_cache: bf16 [N, H, W, 128];
     g_cache: fp32 [N, H, W, 128]; hist_len: int32 [N]. Returns out bf16 [B, T, H, 128]."""
     B, T, H = q.shape[0], q.shape[1], q.shape[2]
     if out is None:
         out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=q.device)
     p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
-                lower_bound, scale, error_word, config_override)
+                lower_bound, scale, error_word, config_override, gate_mode)
     _need(k_cache, "k_cache", torch.bfloat16)
     _need(u_cache, "u_cache", torch.bfloat16)
     _need(g_cache, "g_cache", torch.float32)

@@ -5,7 +5,8 @@ CUDA library and the CPU oracle. This module draws random numbers and lays
 them out; it holds none of the method's arithmetic.
 
 Distributions (the serving workloads these stand in for; no dataset exists):
-  state ~ N(0, 0.02^2) bf16; q, k, v, g_raw, beta_logit ~ N(0, 1) bf16;
+  state ~ N(0, 0.02^2) bf16; q, k, v, g_raw, beta_logit ~ N(0, 1) bf16 (pre-computed
+  gate convention: g = -5 U[0, 1) and beta = U[0, 1), bf16);
   A_log = log U[1, 16] fp32 [H]; dt_bias ~ N(0, 0.5^2) fp32 [H, 128];
   ring: k_cache = unit vectors (normalised Gaussians) in bf16,
   u_cache ~ N(0, 0.5^2) bf16, g_cache = fp32 running sums over ring
@@ -47,6 +48,7 @@ class Workload:
     k_sep: torch.Tensor = None
     v_sep: torch.Tensor = None
     ring: dict = field(default_factory=dict)  # k_cache, u_cache, g_cache, hist_len, W, flush_min
+    gate_mode: int = 0           # 0: raw gate and beta logits; 1: log-space g and beta given
 
     @property
     def B(self):
@@ -121,7 +123,7 @@ def slot_indices(g, B, N, inactive_frac=0.0):
 
 
 def decode_inputs(B, N, seed=0, T=None, layout="separate", inactive_frac=0.0, H=H_DEFAULT,
-                  state_std=0.02, indices=None):
+                  state_std=0.02, indices=None, gate_mode=0):
     """Inputs of kda_decode (T None) or kda_verify (T tokens).
 
     layout "packed": one bf16 row [3][H][128] per (b, t), as a serving stack's
@@ -145,21 +147,26 @@ def decode_inputs(B, N, seed=0, T=None, layout="separate", inactive_frac=0.0, H=
         kw.update(qkv=_randn(g, (B,) + tok + (3 * hk + 64,)))
     else:
         raise ValueError(layout)
+    if gate_mode == 1:  # pre-computed convention: log-space g in [-5, 0), beta in [0, 1)
+        g_in = (-5.0 * torch.rand((B,) + tok + (H, D), generator=g)).to(torch.bfloat16)
+        b_in = torch.rand((B,) + tok + (H,), generator=g).to(torch.bfloat16)
+    else:
+        g_in, b_in = _randn(g, (B,) + tok + (H, D)), _randn(g, (B,) + tok + (H,))
     return Workload(
         state=state, state_indices=torch.as_tensor(indices, dtype=torch.int32),
-        g_raw=_randn(g, (B,) + tok + (H, D)), beta_logit=_randn(g, (B,) + tok + (H,)),
+        g_raw=g_in, beta_logit=b_in, gate_mode=gate_mode,
         A_log=torch.log(torch.rand((H,), generator=g, dtype=torch.float32) * 15.0 + 1.0),
         dt_bias=torch.randn((H, D), generator=g, dtype=torch.float32) * 0.5,
         T=T, layout=layout, **kw)
 
 
 def ring_inputs(B, N, T, W=32, flush_min=9, fold_frac=0.0, seed=0, H=H_DEFAULT, layout="separate",
-                inactive_frac=0.0, sentinels=True):
+                inactive_frac=0.0, sentinels=True, gate_mode=0):
     """Inputs of kda_verify_ring. Active rows fold with probability given by
     fold_frac (exactly round(fold_frac * active) of them): their hist_len is
     drawn from [flush_min, flush_min + T - 1], the others' from [0, flush_min - 1].
     Ring positions at or past hist_len hold NaN, so a stray read shows up."""
-    w = decode_inputs(B, N, seed=seed, T=T, layout=layout, inactive_frac=inactive_frac, H=H)
+    w = decode_inputs(B, N, seed=seed, T=T, layout=layout, inactive_frac=inactive_frac, H=H, gate_mode=gate_mode)
     g = _gen(seed + 7919)
     x = torch.randn((N, H, W, D), generator=g, dtype=torch.float64)
     k_cache = (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)

@@ -36,7 +36,9 @@ STATE_FLOOR = 2.0 ** -12
 
 
 def f64(t):
-    """bf16 / fp32 / int tensor -> numpy (fp64 for floating types; exact)."""
+    """bf16 / fp32 / int tensor -> numpy (fp64 for floating types; exact); None passes."""
+    if t is None:
+        return None
     t = t.detach().cpu()
     if t.dtype in (torch.bfloat16, torch.float16, torch.float32, torch.float64):
         return t.double().numpy()
@@ -85,13 +87,13 @@ def assert_state_close(got, ref, what="state", steps=1, max_ulps=STATE_ULPS):
 def oracle_decode(w, scale=1.0, lower_bound=-5.0):
     return oracle.kda_decode(f64(w.state), f64(w.state_indices), f64(w.q), f64(w.k), f64(w.v),
                              f64(w.g_raw), f64(w.beta_logit), f64(w.A_log), f64(w.dt_bias),
-                             lower_bound=lower_bound, scale=scale)
+                             lower_bound=lower_bound, scale=scale, gate_mode=w.gate_mode)
 
 
 def oracle_verify(w, scale=1.0, lower_bound=-5.0):
     return oracle.kda_verify(f64(w.state), f64(w.state_indices), f64(w.q), f64(w.k), f64(w.v),
                              f64(w.g_raw), f64(w.beta_logit), f64(w.A_log), f64(w.dt_bias),
-                             lower_bound=lower_bound, scale=scale)
+                             lower_bound=lower_bound, scale=scale, gate_mode=w.gate_mode)
 
 
 def oracle_ring(w, restart=True, scale=1.0, lower_bound=-5.0):
@@ -100,17 +102,19 @@ def oracle_ring(w, restart=True, scale=1.0, lower_bound=-5.0):
                                   f64(w.g_raw), f64(w.beta_logit), f64(w.A_log), f64(w.dt_bias),
                                   f64(r["k_cache"]), f64(r["u_cache"]), f64(r["g_cache"]),
                                   f64(r["hist_len"]), r["flush_min"], restart_hist_on_flush=restart,
-                                  lower_bound=lower_bound, scale=scale)
+                                  lower_bound=lower_bound, scale=scale, gate_mode=w.gate_mode)
 
 
 def gpu_decode(wd, **kw):
     from linear_attention_ssm_step_gb300 import kda
+    kw.setdefault("gate_mode", wd.gate_mode)
     return kda.kda_decode(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
                           wd.A_log, wd.dt_bias, **kw)
 
 
 def gpu_verify(wd, **kw):
     from linear_attention_ssm_step_gb300 import kda
+    kw.setdefault("gate_mode", wd.gate_mode)
     return kda.kda_verify(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
                           wd.A_log, wd.dt_bias, **kw)
 
@@ -118,6 +122,7 @@ def gpu_verify(wd, **kw):
 def gpu_ring(wd, restart=True, **kw):
     from linear_attention_ssm_step_gb300 import kda
     r = wd.ring
+    kw.setdefault("gate_mode", wd.gate_mode)
     return kda.kda_verify_ring(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
                                wd.A_log, wd.dt_bias, r["k_cache"], r["u_cache"], r["g_cache"],
                                r["hist_len"], r["flush_min"], restart_hist_on_flush=restart, **kw)

@@ -56,7 +56,7 @@ int main(void) {
          sizeof(kda_view), sizeof(kda_params), sizeof(kda_ring_params));
   P(kda_params, q); P(kda_params, beta_logit); P(kda_params, A_log); P(kda_params, lower_bound);
   P(kda_params, state); P(kda_params, state_indices); P(kda_params, out); P(kda_params, out_h_stride);
-  P(kda_params, error_word); P(kda_params, config_override);
+  P(kda_params, error_word); P(kda_params, config_override); P(kda_params, gate_mode);
   P(kda_ring_params, g_slot_stride); P(kda_ring_params, hist_len); P(kda_ring_params, W);
   P(kda_ring_params, restart_hist_on_flush);
   return 0;
@@ -143,6 +143,10 @@ def test_empty_batch_is_ok_without_launch(lib):
     (lambda p: setattr(p, "scale", float("inf")), kda.KDA_EINVAL, "scale"),
     (lambda p: setattr(p, "out", p.state + 4096), kda.KDA_EINVAL, "overlaps"),
     (lambda p: setattr(p, "error_word", (1 << 32) + 2), kda.KDA_EINVAL, "error_word"),
+    (lambda p: setattr(p, "gate_mode", 2), kda.KDA_EINVAL, "gate_mode"),
+    # A_log and dt_bias are not needed in the pre-computed convention: the next check fires instead
+    (lambda p: (setattr(p, "gate_mode", 1), setattr(p, "A_log", None), setattr(p, "dt_bias", None),
+                setattr(p, "state_indices", None)), kda.KDA_EINVAL, "state_indices"),
 ])
 def test_decode_rejects(lib, mutate, expect, msg):
     p = fake_params()

@@ -307,3 +307,12 @@ def test_error_word_stays_clear(dev):
     gpu_decode(wd, error_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("B", [3, 32])
+def test_precomputed_gate_convention(dev, B):
+    """Log-space g and beta given directly (the API-default convention of the
+    pages' recurrent_kda); A_log and dt_bias are not passed."""
+    w = workloads.decode_inputs(B, B + 4, seed=40 + B, layout="packed", inactive_frac=0.2, gate_mode=1)
+    w.A_log = w.dt_bias = None
+    run_and_check(w, dev)

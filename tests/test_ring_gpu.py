@@ -188,3 +188,9 @@ def test_ring_cuda_graph_bitwise(dev):
         res.append([out.clone(), wd.state.clone()] + [wd.ring[k].clone() for k in snap])
     for x, y in zip(res[0], res[1]):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+def test_ring_precomputed_gate_convention(dev):
+    w = workloads.ring_inputs(6, 12, T=8, W=32, flush_min=9, fold_frac=0.5, seed=13, gate_mode=1)
+    w.A_log = w.dt_bias = None
+    check_ring(w, dev)

@@ -112,3 +112,9 @@ def test_verify_cuda_graph_bitwise(dev):
     for o, s in res[1:]:
         assert torch.equal(o.view(torch.int16), res[0][0].view(torch.int16))
         assert torch.equal(s.view(torch.int16), res[0][1].view(torch.int16))
+
+
+def test_verify_precomputed_gate_convention(dev):
+    w = workloads.decode_inputs(5, 12, seed=7, T=8, inactive_frac=0.2, gate_mode=1)
+    w.A_log = w.dt_bias = None
+    check_verify(w, dev)
