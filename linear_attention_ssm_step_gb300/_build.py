@@ -17,7 +17,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libkda_gb300.so")
 
 SOURCES = ["kda_api.cu", "kda_step.cu", "kda_ring.cu"]
-HEADERS = ["kda_device.cuh", "kda_launch.h"]
+HEADERS = ["kda_device.cuh", "kda_launch.h", "kda_tc.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # --fmad=false: no implicit mul+add contraction anywhere, so every fused

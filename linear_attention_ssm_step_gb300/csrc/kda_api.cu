@@ -114,10 +114,8 @@ int pick_tile(const kda_params* p, int T) {
   return kTileV[cfg];
 }
 
-int pick_ring_tile(const kda_params* p, int T) {
-  const int cfg = p->config_override >= 0 ? p->config_override : kda_select_ring_config(p->B, T);
-  return kTileV[cfg];
-}
+// The ring kernel works on whole heads: the one configuration it runs.
+constexpr int kRingConfig = 3;
 
 }  // namespace
 
@@ -147,13 +145,11 @@ int32_t kda_select_config(int32_t B, int32_t T) {
   return 3;               // 128 rows
 }
 
-// The ring kernel's own policy (its per-head work is larger: whole heads,
-// with 8 warps, once a batch fills the machine).
+// The ring kernel runs one CTA per (row, head): its state rows enter one
+// 128-row tensor-core product, so it has a single configuration.
 int32_t kda_select_ring_config(int32_t B, int32_t T) {
   if (B < 0 || T < 1 || T > KDA_MAX_T) return -1;
-  if (B <= 2) return 0;   // 16 rows
-  if (B <= 64) return 2;  // 64 rows
-  return 3;               // 128 rows, 8 warps
+  return kRingConfig;  // 128 rows
 }
 
 const char* kda_last_error(void) { return g_err; }
@@ -200,8 +196,11 @@ kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params
     if (r->k_slot_stride % 8 || r->u_slot_stride % 8 || r->g_slot_stride % 4)
       return fail(KDA_EINVAL, "ring slot strides must keep slots 16-byte aligned");
   }
+  if (p->config_override >= 0 && p->config_override != kRingConfig)
+    return fail(KDA_EUNSUPPORTED, "config_override = %d: kda_verify_ring runs whole-head tiles only (configuration %d)",
+                p->config_override, kRingConfig);
   if (p->B == 0) return ok();
-  cudaError_t e = kda::launch_ring(*p, T, *r, pick_ring_tile(p, T), bulk, static_cast<cudaStream_t>(stream));
+  cudaError_t e = kda::launch_ring(*p, T, *r, bulk, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify_ring launch: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -25,8 +25,9 @@ cudaError_t set_smem_limit_once(Kernel kern, size_t bytes, std::atomic<bool>& do
 // the bulk-copy staging of the state (16-byte aligned pool) over plain loads.
 cudaError_t launch_step(const kda_params& p, int T, int tile_v, bool bulk, cudaStream_t s);
 
-// Ring-cache verify with replay and fold. tile_v in {16, 32, 64, 128}.
-cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, int tile_v, bool bulk,
-                        cudaStream_t s);
+// Ring-cache verify with replay and fold, one CTA per (row, head). bulk
+// selects tensor-map copies of the checkpoint (16-byte aligned pool) over
+// plain loads and stores.
+cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, bool bulk, cudaStream_t s);
 
 }  // namespace kda

@@ -12,103 +12,125 @@
 //   u~_t = bf16(beta_t (v_t - (D_t S_{t-1})^T k~_t)),  S_t = D_t S_{t-1} + k~_t u~_t^T,
 //   o_t  = scale S_t^T q_hat_t.
 // Unrolled over the tokens (the WY form of these pages' replay), with
-// P_t = d_0 * ... * d_t and w_tj = P_t / P_j = d_{j+1} * ... * d_t:
+// P_t = d_0 * ... * d_t and w_tj = d_{j+1} * ... * d_t:
 //   (D_t S_{t-1})^T k~_t = S_b^T (P_t k~_t) + sum_{j<t}  u~_j (w_tj k~_j) . k~_t
 //   S_t^T q_hat_t        = S_b^T (P_t q_hat_t) + sum_{j<=t} u~_j (w_tj k~_j) . q_hat_t
-// so each state row is read once for 2T dot products, and the token-to-token
-// dependence shrinks to a T-step scalar recurrence per row over the T x T
-// coefficients cc[t][j] = (w_tj k~_j) . k~_t and ec[t][j] = (w_tj k~_j) . q_hat_t.
-// The base state is the checkpoint replayed through the h live entries, in
-// closed form with the pages' replay weights:
-//   S_h = diag(exp(G_{h-1})) S_0 + sum_{j<h} (exp(G_{h-1} - G_j) k~_j) u~_j^T;
-// a fold (h >= flush_min) rounds S_h to bf16, stores it as the new checkpoint
-// and uses the rounded state as the base (G restarts at 0); otherwise S_h
-// stays in fp32 and G continues from G_{h-1}.
+// so the token-to-token dependence shrinks to a T-step scalar recurrence per
+// value row over the T x T coefficients cc[t][j] = (w_tj k~_j) . k~_t and
+// ec[t][j] = (w_tj k~_j) . q_hat_t, and the state enters only through the 2T
+// dot products S_b^T x of every row: one [128 x 128] x [128 x 2T] product.
 //
-// One CTA per (batch row, head, tile of TV = 16, 32, 64 or 128 rows), 4 warps
-// (8 for the whole-head tile):
-//   1. slot lookup, checkpoint bulk copy, hist_len check (outside [0, W]:
-//      error bit, skip);
-//   2. per-token prologue; per channel: k~, G, d_t, P_t, the query vectors
-//      P_t k~_t and P_t q_hat_t, exp(G_{h-1}), the history keys;
-//   3. the coefficient matrices, one warp per column j;
-//   4. per 4-row group pair: base rows (replay, fold), the 2T dot products,
-//      a reduce-scatter that leaves token t's two sums on lane t % 8 of the
-//      row, and the T-step recurrence for u~_t and o_t;
-//   5. outputs and this tile's rows of u~ (rows no other CTA reads).
-// A second, stream-ordered kernel (one CTA per batch row) appends k~ and G
-// and resets hist_len after a fold. Both are shared by every tile and head of
-// a slot: after a fold the new entries overwrite ring positions 0..T-1 that
-// other CTAs of the first kernel may still be replaying, and a reset
-// hist_len must not be seen by a CTA that has not read it yet. The second
-// kernel recomputes k~ and G with the same arithmetic, so the bits match.
+// The base state is the checkpoint S_0 replayed through the h live entries, in
+// closed form with the pages' replay weights:
+//   S_b = diag(exp(G_{h-1})) S_0 + sum_{j<h} (exp(G_{h-1} - G_j) k~_j) u~_j^T.
+// Without a fold it is never formed: for every query vector x,
+//   S_b^T x = S_0^T (exp(G_{h-1}) x) + sum_{j<h} u~_j ((exp(G_{h-1} - G_j) k~_j) . x),
+// so the product runs on the bf16 checkpoint as stored, and the history adds
+// h x 2T coefficients. A fold (h >= flush_min) forms S_b row by row, rounds it
+// to bf16, stores it as the new checkpoint and uses it as S_0 with G
+// restarting at 0 and no history.
+//
+// One CTA of 128 threads per (batch row, head); thread i is key channel i in
+// the per-channel work and value row i in the per-row work:
+//   1. slot index, hist_len, the first history entries; the checkpoint
+//      arrives by two tensor-map loads (128-byte swizzle, the tensor core's
+//      operand layout);
+//   2. per channel: the token inputs, L2 norms (block sums), gate, G, P_t and
+//      the query vectors, written as bf16 hi + lo pairs into the B operand;
+//      the coefficients and, without a fold, the history coefficients as
+//      per-channel products, summed over the block;
+//   3. fold: a first tensor-core product forms sum_j u~_j[row] hkey_j for all
+//      rows and keys (A = the u~ history, B = the history keys as three bf16
+//      parts, 128 fp32 tensor-memory columns); each row thread adds
+//      exp(G_{h-1}) s_0, rounds and writes its row back in place; the
+//      checkpoint leaves by two tensor-map stores;
+//   4. one thread issues 16 tcgen05.mma (M = 128 rows, N = 2T, K = 128; hi
+//      and lo halves accumulate into the same fp32 tensor-memory columns);
+//   5. each row thread reads its 2T sums from tensor memory, adds the
+//      history terms, runs the recurrence and writes o_t and u~_t; each
+//      channel thread writes k~_t and G_t.
+// Every ring column of a (slot, head) is read and written by one thread of
+// one CTA, so appending in place is safe. hist_len is shared by the heads of
+// a slot: a second, stream-ordered kernel resets it after a fold.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+
 #include "kda_device.cuh"
 #include "kda_launch.h"
+#include "kda_tc.cuh"
 
 namespace kda {
 
-__host__ __device__ constexpr size_t ring_smem_bytes(int TV, int T, int W) {
-  return (size_t)TV * KD * 2                        // checkpoint tile (bf16)
-         + 64                                         // mbarriers
-         + (size_t)T * KD * 4 * 4                     // kh (k~), qh, dd (d_t), gg (g, then P_t k~_t)
-         + (size_t)T * KD * 4                         // qq = P_t q_hat_t
-         + (size_t)T * TV * 4 * 3                     // vrow, orow, urow
-         + (size_t)KDA_MAX_T * 4 * 2                  // beta, kappa
-         + (size_t)KDA_MAX_T * KDA_MAX_T * 4 * 2      // cc, ec
-         + (size_t)KD * 4                             // exp(G_{h-1})
-         + (size_t)W * KD * 4                         // history G, then history keys (in place)
-         + (size_t)W * KD * 2                         // history k~ (bf16, as stored)
-         + (size_t)W * TV * 2                         // history u~ of this tile's rows (bf16)
-         + 16;                                        // history mbarrier
+constexpr int RING_THREADS = 128;
+constexpr uint32_t RING_TMEM_COLS = 128;  // the fold's 128 x 128 fp32 sums, later the 2T dot products
+
+// Shared-memory carve-up (bytes from a 1024-aligned base) for TT token slots,
+// ring width W and fold threshold flush_min. The union region holds either
+// the fold's operands (u~ history and three parts of the history keys, K in
+// steps of 16 entries, 32-byte swizzle) or, without a fold, the history
+// coefficients and the u~ history; the B operand (query vectors) sits at its
+// start and is written after the fold's product has read its operands.
+struct RingLayout {
+  uint32_t a, u, fa, fk, b, hred, hfin, hu, red, rn, fin, fint, sdec, beta, bar, tslot, total;
+};
+
+__host__ __device__ inline RingLayout ring_layout(int TT, int W, int flush_min) {
+  RingLayout L{};
+  const uint32_t NB = 2u * TT;
+  const uint32_t ks = ((uint32_t)W + 15u) / 16u;                        // fold K steps
+  const uint32_t hmax = flush_min > 1 ? (uint32_t)flush_min - 1 : 0u;  // history of a call that does not fold
+  const uint32_t cpe = TT == 8 ? 2u : 1u;                               // history entries per chunk
+  const uint32_t nhc = (hmax + 7u) / 8u * (8u / cpe);                   // chunks, in blocks of 8 entries
+  uint32_t o = 0;
+  L.a = o;
+  o += 128u * 256u;  // checkpoint, 128 rows x 128 keys bf16
+  L.u = o;
+  L.fa = o;               // fold: u~ history [ks][128 x 32 B]
+  L.fk = o + ks * 4096u;  // fold: history keys, 3 parts x [ks][128 x 32 B]
+  const uint32_t fold_bytes = ks * 4096u * 4u;
+  L.b = o;                        // query vectors: 2 NB rows (high halves, then low) x 256 B
+  L.hred = L.b + NB * 512u;       // no fold: history partial sums [nhc][4][32]
+  L.hfin = L.hred + nhc * 512u;   // no fold: history coefficients [nhc][32]
+  L.hu = L.hfin + nhc * 128u;     // no fold: u~ history [hmax][128] bf16
+  const uint32_t nofold_bytes = L.hu + hmax * 256u - o;
+  o += fold_bytes > nofold_bytes ? fold_bytes : nofold_bytes;
+  L.red = o;
+  o += (1u + (TT * TT) / 32u) * 512u;  // per-warp partial sums: norms, then coefficients
+  L.rn = o;
+  o += 32u * 4u;  // inverse norms
+  L.fin = o;
+  o += TT * TT * 4u;  // coefficient sums
+  L.fint = o;
+  o += TT * TT * 4u;  // the same, transposed
+  L.sdec = o;
+  o += 128u * 4u;  // fold: exp(G_{h-1})
+  L.beta = o;
+  o += KDA_MAX_T * 4u;
+  L.bar = o;
+  o += 32u;
+  L.tslot = o;
+  o += 16u;
+  L.total = o;
+  return L;
+}
+
+__host__ __device__ inline size_t ring_smem_bytes(int TT, int W, int flush_min) {
+  return (size_t)ring_layout(TT, W, flush_min).total + 1024;  // + alignment slack
 }
 
 __device__ __forceinline__ float round_bf16(float x) { return bf16_bits_to_float(float_to_bf16_bits(x)); }
 
-// Dot product of a lane's 16 keys of a row with the lane's 16 keys of a vector.
-__device__ __forceinline__ float dot16(const f32x2 (&vec)[8], const f32x2 (&row)[8]) {
-  f32x2 xa = mul2(vec[0], row[0]), xb = mul2(vec[1], row[1]);
-#pragma unroll
-  for (int i = 2; i < 8; i += 2) {
-    xa = fma2(vec[i], row[i], xa);
-    xb = fma2(vec[i + 1], row[i + 1], xb);
-  }
-  float x0, x1, x2, x3;
-  upk2(xa, x0, x1);
-  upk2(xb, x2, x3);
-  return __fadd_rn(__fadd_rn(x0, x2), __fadd_rn(x1, x3));
-}
-
-// Slot of token t's sum ("which" = 0: with k~, 1: with q_hat) among the 2 TT
-// values a lane holds before the reduce-scatter; after it, lane j of the row
-// holds slots [j * 2TT/8, (j + 1) * 2TT/8), that is tokens j and j + 8.
-template <int TT>
-__device__ __forceinline__ constexpr int wy_slot(int t, int which) {
-  return TT == 8 ? 2 * t + which : 4 * (t & 7) + 2 * (t >> 3) + which;
-}
-
-// Reduce-scatter of NV per-lane values over the 8 lanes of a row: at the
-// level with lane mask m, a lane keeps the half of its current values picked
-// by bit m of its row lane and sends the other half to lane ^ m, who keeps it.
+// Reduce-scatter of NV (16 or 32) per-lane values over a warp: at the level
+// with lane mask m, a lane keeps the half of its current values picked by bit
+// m of its lane and sends the other half to lane ^ m, who keeps it; once a
+// lane holds one value, plain butterfly levels follow. Afterwards v[0] of
+// lane l holds the warp-wide sum of value l >> (5 - log2 NV). Every value is
+// summed over the same butterfly tree, so its bits do not depend on where it
+// sits.
 template <int NV>
-__device__ __forceinline__ void reduce_scatter8(float (&v)[NV], int j) {
-#pragma unroll
-  for (int m = 4, c = NV; m >= 1; m >>= 1, c >>= 1) {
-    const bool hi = (j & m) != 0;
-#pragma unroll
-    for (int i = 0; i < c / 2; ++i) {
-      const float keep = hi ? v[c / 2 + i] : v[i];
-      const float send = hi ? v[i] : v[c / 2 + i];
-      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, m));
-    }
-  }
-}
-
-// Reduce-scatter of NV (16 or 32) per-lane values over a whole warp: halving
-// levels (as in reduce_scatter8) while a lane holds more than one value, then
-// plain butterfly levels. Afterwards v[0] holds the warp-wide sum of value
-// lane >> (5 - log2 NV); each value is summed in one fixed order.
-template <int NV>
-__device__ __forceinline__ void reduce_scatter32(float (&v)[NV], int lane) {
+__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane) {
   static_assert(NV == 16 || NV == 32, "16 or 32 values");
   int c = NV;
 #pragma unroll
@@ -130,414 +152,754 @@ __device__ __forceinline__ void reduce_scatter32(float (&v)[NV], int lane) {
   }
 }
 
-template <int TV, bool BULK, int TT, int NW>
-__global__ void __launch_bounds__(32 * NW)
-    kda_ring_kernel(const kda_params p, const kda_ring_params rp, const int T, const int tiles) {
-  static_assert(TV % 16 == 0 && TV >= 16 && TV <= 128, "ring tile must be 16, 32, 64 or 128 rows");
-  static_assert(TT == 8 || TT == 16, "token slots");
-  static_assert(NW == 4 || NW == 8, "4 or 8 warps");
-  static_assert(TV % (4 * NW) == 0, "every warp owns whole 4-row groups");
-  constexpr int NT = 32 * NW;             // threads
-  constexpr int RW = TV / NW;             // rows per warp
-  constexpr int RQ = RW / ROWS_PER_WARP;  // 4-row groups per warp
-  constexpr int RG = RQ < 2 ? RQ : 2;     // groups processed together
-  constexpr int NV = 2 * TT;              // sums per row before the reduce-scatter
-  extern __shared__ __align__(128) unsigned char smem[];
+// The block sum of value l of a 32-value chunk: its four warp partials in warp order.
+__device__ __forceinline__ float block_sum(const float* part, int chunk, int l) {
+  const float* q = part + chunk * 128 + l;
+  return __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[32]), q[64]), q[96]);
+}
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x % tiles;
-  const int bh = blockIdx.x / tiles;
-  const int h = bh % p.H;
-  const int b = bh / p.H;
-  const int v0 = tile * TV;
+// x as bf16 hi + lo (hi = bf16(x), lo = bf16(x - hi); |x - hi - lo| <= 2^-17 |x|)
+// at element (row, k) of the two B-operand halves.
+template <int NB>
+__device__ __forceinline__ void store_split(unsigned char* hi, unsigned char* lo, int row, int k, float x) {
+  const uint16_t xh = float_to_bf16_bits(x);
+  const uint16_t xl = float_to_bf16_bits(__fsub_rn(x, bf16_bits_to_float(xh)));
+  const uint32_t off = sw128_offset(NB, row, k);
+  *reinterpret_cast<uint16_t*>(hi + off) = xh;
+  *reinterpret_cast<uint16_t*>(lo + off) = xl;
+}
 
-  uint16_t* st = reinterpret_cast<uint16_t*>(smem);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + TV * KD * 2);
-  float* fbase = reinterpret_cast<float*>(smem + TV * KD * 2 + 64);
-  TokenSmem ts;
-  ts.kh = fbase;
-  ts.qh = ts.kh + T * KD;
-  ts.dd = ts.qh + T * KD;
-  ts.gg = ts.dd + T * KD;
-  float* qk = ts.gg;  // each thread overwrites its channel's g_t with P_t k~_t in the channel pass
-  float* qq = ts.gg + T * KD;
-  ts.vrow = qq + T * KD;
-  float* orow = ts.vrow + T * TV;
-  float* urow = orow + T * TV;
-  ts.beta = urow + T * TV;
-  ts.kappa = ts.beta + KDA_MAX_T;
-  float* cc = ts.kappa + KDA_MAX_T;             // [t][j], j < t
-  float* ec = cc + KDA_MAX_T * KDA_MAX_T;       // [t][j], j <= t
-  float* cdec = ec + KDA_MAX_T * KDA_MAX_T;     // [128] exp(G_{h-1})
-  float* hk = cdec + KD;                        // [W][128] G_j as copied, then exp(G_{h-1} - G_j) k~_j
-  uint16_t* hkb = reinterpret_cast<uint16_t*>(hk + rp.W * KD);  // [W][128] k~_j (bf16)
-  uint16_t* hub = hkb + rp.W * KD;                               // [W][TV] u~_j[v0..v0+TV) (bf16)
-  uint64_t* hbar = reinterpret_cast<uint64_t*>(hub + rp.W * TV);  // history copies
+// x as three bf16 parts (exact to 2^-25 |x|) at element (row, j) of three
+// 32-byte-swizzled operands `part` bytes apart.
+__device__ __forceinline__ void store_split3(unsigned char* base, uint32_t part, int row, int j, float x) {
+  const uint16_t x0 = float_to_bf16_bits(x);
+  const float r1 = __fsub_rn(x, bf16_bits_to_float(x0));
+  const uint16_t x1 = float_to_bf16_bits(r1);
+  const uint16_t x2 = float_to_bf16_bits(__fsub_rn(r1, bf16_bits_to_float(x1)));
+  const uint32_t off = sw32_offset(128, row, j);
+  *reinterpret_cast<uint16_t*>(base + off) = x0;
+  *reinterpret_cast<uint16_t*>(base + part + off) = x1;
+  *reinterpret_cast<uint16_t*>(base + 2 * part + off) = x2;
+}
 
-  uint16_t* outp = static_cast<uint16_t*>(p.out);
-  const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
+// Token inputs of one item in registers, as loaded (bf16 bits, converted
+// where they are used, so that the loads all fly together): q, k, g of key
+// channel tid and v of value row tid, for every token slot (zero past T).
+template <int TT>
+struct TokenRegs {
+  uint16_t qv[TT], kv[TT], gv[TT], vv[TT];
+  uint16_t blogit;
+  float alog, dtb;  // A_log[h] and dt_bias[h][tid] (raw gate)
+};
 
-  const int n = p.state_indices[b];
-  constexpr int PT = TT / NW;  // tokens per warp in the prologue
-  TokenLoads<PT> first;        // issued alongside the index load; unused by an inactive row
-  prologue_issue<PT, NW>(p, b, h, T, v0, TV, first);
-  if (n < 0 || n >= p.N) {
-    for (int i = tid; i < T * TV; i += NT) {
-      const int t = i / TV, r = i - t * TV;
-      outp[out_base + (int64_t)t * p.out_t_stride + r] = 0;
-    }
-    return;
-  }
+__device__ __forceinline__ uint16_t load_bits(const kda_view& vw, int b, int t, int h, int c) {
+  const uint16_t* ptr = static_cast<const uint16_t*>(vw.ptr);
+  return ptr[(int64_t)b * vw.b_stride + (int64_t)t * vw.t_stride + (int64_t)h * vw.h_stride + c];
+}
 
-  // The checkpoint copy starts before hist_len is known: reading it is harmless
-  // even when the history turns out to be invalid.
-  uint16_t* gst = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride +
-                  ((int64_t)h * KD + v0 + warp * RW) * KD;
-  uint16_t* sst = st + warp * RW * KD;
-  constexpr uint32_t CHUNK_BYTES = RW * KD * 2;
-  if constexpr (BULK) {
-    if (lane == 0) {
-      mbar_init(&mbar[warp], 1);
-      mbar_expect_tx(&mbar[warp], CHUNK_BYTES);
-      bulk_g2s(sst, gst, CHUNK_BYTES, &mbar[warp]);
+// Slots t >= T are never loaded and keep the zeros set once by zero_tokens.
+template <int TT>
+__device__ __forceinline__ void zero_tokens(TokenRegs<TT>& L) {
+#pragma unroll
+  for (int t = 0; t < TT; ++t) L.qv[t] = L.kv[t] = L.gv[t] = L.vv[t] = 0;
+  L.blogit = 0;
+  L.alog = L.dtb = 0.0f;
+}
+
+template <int TT>
+__device__ __forceinline__ void load_tokens(const kda_params& p, int b, int h, int T, TokenRegs<TT>& L) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    if (t < T) {
+      L.qv[t] = load_bits(p.q, b, t, h, tid);
+      L.kv[t] = load_bits(p.k, b, t, h, tid);
+      L.gv[t] = load_bits(p.g_raw, b, t, h, tid);
+      L.vv[t] = load_bits(p.v, b, t, h, tid);
     }
   }
-  const int hist = rp.hist_len[n];
-  if (hist < 0 || hist > rp.W) {
-    if (tid == 0 && tile == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_HIST_LEN);
-    if constexpr (BULK) {
-      __syncwarp();
-      if (!mbar_wait_bounded(&mbar[warp], 0) && lane == 0 && p.error_word != nullptr)
-        atomicOr(p.error_word, KDA_ERR_TIMEOUT);  // the copy must land before the CTA leaves
-    }
-    for (int i = tid; i < T * TV; i += NT) {
-      const int t = i / TV, r = i - t * TV;
-      outp[out_base + (int64_t)t * p.out_t_stride + r] = 0;
-    }
-    return;
-  }
-  const bool fold = hist >= rp.flush_min;
-  const int base = fold ? 0 : hist;
-
-  // Ring slices of this (slot, head).
-  uint16_t* kc = static_cast<uint16_t*>(rp.k_cache) + (int64_t)n * rp.k_slot_stride + (int64_t)h * rp.W * KD;
-  uint16_t* uc = static_cast<uint16_t*>(rp.u_cache) + (int64_t)n * rp.u_slot_stride + (int64_t)h * rp.W * KD;
-  float* gc = static_cast<float*>(rp.g_cache) + (int64_t)n * rp.g_slot_stride + (int64_t)h * rp.W * KD;
-
-  // The live history arrives by bulk copies started now, so that its latency
-  // overlaps the prologue: k~ and G of entries 0..hist-1 are contiguous, this
-  // tile's u~ rows are one short copy per entry. The ring pointers and slot
-  // strides are 16-byte aligned (checked on the host), v0 is a multiple of 16.
-  if (hist > 0 && tid == 0) {
-    mbar_init(hbar, 1);
-    mbar_expect_tx(hbar, (uint32_t)hist * (KD * 2 + KD * 4 + TV * 2));
-    bulk_g2s(hkb, kc, (uint32_t)hist * KD * 2, hbar);
-    bulk_g2s(hk, gc, (uint32_t)hist * KD * 4, hbar);
-    for (int jx = 0; jx < hist; ++jx) bulk_g2s(hub + jx * TV, uc + (int64_t)jx * KD + v0, TV * 2, hbar);
-  }
-  if constexpr (!BULK) {
-    for (int i = lane; i < RW * KD; i += 32) sst[i] = gst[i];
-  }
-
-  token_prologue<PT, NW>(p, b, h, T, v0, TV, ts, first);  // ends with a CTA barrier (publishes hbar's init)
-
-  bool hist_ok = true;
-  if (hist > 0) hist_ok = mbar_wait_bounded(hbar, 0);
-  if (!hist_ok && tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
-
-  // Channel pass, thread c (and c + 128 with 8 warps) = key channel c.
-  {
-    const int c = tid & (KD - 1), part = tid / KD;
-    const float Gl = hist > 0 ? hk[(hist - 1) * KD + c] : 0.0f;  // G_{h-1}
-    if (part == 0) cdec[c] = hist > 0 ? expf(Gl) : 1.0f;
-    if (NT > KD) __syncthreads();  // every thread has read G_{h-1} before entry h-1 is overwritten
-    for (int jx = part; jx < hist; jx += NT / KD) {  // in place: G_j -> exp(G_{h-1} - G_j) k~_j
-      const float kj = bf16_bits_to_float(hkb[jx * KD + c]);
-      hk[jx * KD + c] = __fmul_rn(expf(__fsub_rn(Gl, hk[jx * KD + c])), kj);
-    }
-    float G_prev = fold ? 0.0f : Gl;
-    float P = 1.0f;
-    for (int t = 0; t < (part == 0 ? T : 0); ++t) {
-      const float kt = round_bf16(ts.kh[t * KD + c]);
-      const float G = __fadd_rn(G_prev, ts.gg[t * KD + c]);
-      const float d = expf(__fsub_rn(G, G_prev));
-      P = __fmul_rn(P, d);
-      ts.kh[t * KD + c] = kt;
-      ts.dd[t * KD + c] = d;
-      qk[t * KD + c] = __fmul_rn(P, kt);
-      qq[t * KD + c] = __fmul_rn(P, ts.qh[t * KD + c]);
-      G_prev = G;
-    }
-  }
-  __syncthreads();
-
-  // Coefficients, warp w for columns j = w, w + 4, ...; lane l sums channels
-  // l + 32 i; w_tj is a running product of the token decays. A column's 2 TT
-  // partial sums (cc and ec for every t) are reduced together, see
-  // reduce_scatter32.
-  for (int j = warp; j < T; j += NW) {
-    float kj[4], wgt[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      kj[i] = ts.kh[j * KD + lane + 32 * i];
-      wgt[i] = 1.0f;
-    }
-    float vals[2 * TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      float sc = 0.0f, se = 0.0f;
-      if (t >= j && t < T) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = lane + 32 * i;
-          if (t > j) wgt[i] = __fmul_rn(wgt[i], ts.dd[t * KD + c]);
-          const float pj = __fmul_rn(wgt[i], kj[i]);
-          sc = __fmaf_rn(pj, ts.kh[t * KD + c], sc);
-          se = __fmaf_rn(pj, ts.qh[t * KD + c], se);
-        }
-      }
-      vals[2 * t] = sc;
-      vals[2 * t + 1] = se;
-    }
-    reduce_scatter32<2 * TT>(vals, lane);
-    constexpr int SHIFT = (2 * TT == 16) ? 1 : 0;  // lanes per result
-    if ((lane & ((1 << SHIFT) - 1)) == 0) {
-      const int idx = lane >> SHIFT, t = idx >> 1;
-      if (t >= j && t < T) {
-        if (idx & 1)
-          ec[t * KDA_MAX_T + j] = vals[0];
-        else if (t > j)
-          cc[t * KDA_MAX_T + j] = vals[0];
-      }
-    }
-  }
-
-  bool ok = true;
-  __syncwarp();
-  if constexpr (BULK) ok = mbar_wait_bounded(&mbar[warp], 0);
-  if (!ok && lane == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
-  // The tile is written only if every warp's copy arrived; a CTA that gave up
-  // writes zero output and leaves the checkpoint and ring alone. The barrier
-  // also publishes the coefficients.
-  ok = __syncthreads_and(ok && hist_ok) != 0;
-
-  const int r = lane / LPR, j = lane % LPR;  // row within a 4-row group, lane within the row
-  for (int g = 0; g < RQ; g += RG) {
-    f32x2 s[RG][8];
-    int rows[RG];
-#pragma unroll
-    for (int q = 0; q < RG; ++q) {
-      rows[q] = warp * RW + ROWS_PER_WARP * (g + q) + r;
-      row_to_f32(load_row_bf16(st + rows[q] * KD, j), s[q]);
-    }
-    // base = exp(G_{h-1}) S_0 + sum_j (exp(G_{h-1} - G_j) k~_j) u~_j[row]
-    if (hist > 0) {
-      f32x2 cv[8];
-      load_pairs8(cdec, j, cv);
-#pragma unroll
-      for (int q = 0; q < RG; ++q)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s[q][i] = mul2(cv[i], s[q][i]);
-      for (int jx = 0; jx < hist; ++jx) {
-        f32x2 kr[8];
-        load_pairs8(hk + jx * KD, j, kr);
-#pragma unroll
-        for (int q = 0; q < RG; ++q) {
-          const float uv = bf16_bits_to_float(hub[jx * TV + rows[q]]);
-          const f32x2 uu = pk2(uv, uv);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) s[q][i] = fma2(kr[i], uu, s[q][i]);
-        }
-      }
-    }
-    if (fold) {
-#pragma unroll
-      for (int q = 0; q < RG; ++q) {
-        const RowBf16 w = row_to_bf16(s[q]);
-        if (ok) store_row_bf16(st + rows[q] * KD, j, w);
-        row_to_f32(w, s[q]);
-      }
-    }
-    // 2T dot products of each base row: S_b^T (P_t k~_t) and S_b^T (P_t q_hat_t).
-    float acc[RG][NV];
-#pragma unroll
-    for (int q = 0; q < RG; ++q)
-#pragma unroll
-      for (int i = 0; i < NV; ++i) acc[q][i] = 0.0f;
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      if (t < T) {
-        f32x2 vk[8], vq[8];
-        load_pairs8(qk + t * KD, j, vk);
-        load_pairs8(qq + t * KD, j, vq);
-#pragma unroll
-        for (int q = 0; q < RG; ++q) {
-          acc[q][wy_slot<TT>(t, 0)] = dot16(vk, s[q]);
-          acc[q][wy_slot<TT>(t, 1)] = dot16(vq, s[q]);
-        }
-      }
-    }
-    // The T-step recurrence; lane j of the row owns tokens j and j + 8.
-#pragma unroll
-    for (int q = 0; q < RG; ++q) {
-      reduce_scatter8<NV>(acc[q], j);
-      const int row = rows[q];
-      float cu[2] = {0.0f, 0.0f}, co[2] = {0.0f, 0.0f}, uo[2] = {0.0f, 0.0f};
-      for (int sx = 0; sx < T; ++sx) {
-        const int half = sx >> 3;
-        float mine = 0.0f;
-        if (j == (sx & 7)) {
-          // token sx's sum with k~ sits in slot 0 (first token) or 2 (second) of its owner lane
-          const float A = half ? acc[q][TT == 16 ? 2 : 0] : acc[q][0];
-          const float cuh = half ? cu[1] : cu[0];
-          mine = round_bf16(__fmul_rn(ts.beta[sx], __fsub_rn(ts.vrow[sx * TV + row], __fadd_rn(A, cuh))));
-        }
-        const float us = __shfl_sync(0xffffffffu, mine, (lane & ~(LPR - 1)) | (sx & 7));
-#pragma unroll
-        for (int hh = 0; hh < TT / 8; ++hh) {
-          const int tok = j + 8 * hh;
-          if (tok < T) {
-            if (tok > sx) cu[hh] = __fmaf_rn(cc[tok * KDA_MAX_T + sx], us, cu[hh]);
-            if (tok >= sx) co[hh] = __fmaf_rn(ec[tok * KDA_MAX_T + sx], us, co[hh]);
-            if (tok == sx) uo[hh] = us;
-          }
-        }
-      }
-#pragma unroll
-      for (int hh = 0; hh < TT / 8; ++hh) {
-        const int tok = j + 8 * hh;
-        if (tok < T) {
-          urow[tok * TV + row] = uo[hh];
-          orow[tok * TV + row] = ok ? __fmul_rn(p.scale, __fadd_rn(acc[q][2 * hh + 1], co[hh])) : 0.0f;
-        }
-      }
-    }
-  }
-
-  if (fold && ok) {
-    if constexpr (BULK) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        bulk_s2g(gst, sst, CHUNK_BYTES);
-        bulk_commit();
-        bulk_wait_read_all();
-      }
-    } else {
-      __syncwarp();
-      for (int i = lane; i < RW * KD; i += 32) gst[i] = sst[i];
-    }
-  }
-  __syncthreads();
-  for (int i = tid; i < T * TV; i += NT) {
-    const int t = i / TV, rr = i - t * TV;
-    outp[out_base + (int64_t)t * p.out_t_stride + rr] = float_to_bf16_bits(orow[i]);
-    if (ok) uc[(int64_t)(base + t) * KD + v0 + rr] = float_to_bf16_bits(urow[i]);
+  if (tid < T) L.blogit = load_bits(p.beta_logit, b, tid, h, 0);
+  if (p.gate_mode == KDA_GATE_RAW) {
+    L.alog = p.A_log[h];
+    L.dtb = p.dt_bias[(int64_t)h * KD + tid];
   }
 }
 
-// After the ring kernel, one CTA per batch row: append k~ and G_P at ring
-// positions base..base+T-1 for every head, then reset hist_len[n] after a
-// fold when restart_hist_on_flush. One warp per head (the CTA has
-// APPEND_WARPS warps and loops when H is larger); lane l handles channels
-// l + 32 i, and each head's inputs for up to 8 tokens are loaded in one
-// batch, so the CTA waits for memory a few times rather than once per token.
-// k~ and G come from the same helpers and summation order as token_prologue
-// and the ring kernel's channel pass, so the bits match.
-constexpr int APPEND_WARPS = 16;
+// The gate of the ring kernel: the formulas of Gate with the fast exponential
+// (__expf) and the approximate reciprocal. Their relative errors, a few 1e-7,
+// stay far below the tolerances of G, the decays and u~; the history weights
+// and the fold keep the IEEE exponential.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
-__global__ void __launch_bounds__(32 * APPEND_WARPS)
-    kda_ring_append_kernel(const kda_params p, const kda_ring_params rp, const int T) {
-  const int b = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+struct RingGate {
+  bool raw;
+  float a_h, lower_bound;
+  __device__ __forceinline__ RingGate(const kda_params& p, float alog) {
+    raw = p.gate_mode == KDA_GATE_RAW;
+    a_h = raw ? __expf(alog) : 0.0f;
+    lower_bound = p.lower_bound;
+  }
+  __device__ __forceinline__ float g(float g_in, float dtb) const {
+    if (!raw) return g_in;
+    const float z = __fmul_rn(a_h, __fadd_rn(g_in, dtb));
+    return __fmul_rn(lower_bound, rcp_approx(__fadd_rn(1.0f, __expf(-z))));
+  }
+  __device__ __forceinline__ float beta(float b_in) const {
+    return raw ? rcp_approx(__fadd_rn(1.0f, __expf(-b_in))) : b_in;
+  }
+};
+
+// Persistent: CTA c works on items (b, h) = c, c + gridDim.x, ... (item = b H + h).
+// While item i computes, the slot index and hist_len of item i+1 are read;
+// once item i's product has read the checkpoint buffer, the copy of item
+// i+1's checkpoint and its token loads are issued, and land while item i runs
+// its recurrence and item i+1 starts. Padded token slots (t >= T) carry
+// zero inputs through the same arithmetic, so no loop branches on T.
+template <bool TMA, int TT>
+__global__ void __launch_bounds__(RING_THREADS, 3)
+    kda_ring_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p, const kda_ring_params rp,
+                    const int T) {
+  static_assert(TT == 8 || TT == 16, "token slots");
+  constexpr int NB = 2 * TT;            // dot products per row: TT with P_t k~_t, then TT with P_t q_hat_t
+  constexpr int NB2 = 2 * NB;           // B operand rows: NB high halves, then NB low halves
+  constexpr int CPE = TT == 8 ? 2 : 1;  // history entries per reduction chunk
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int total = p.B * p.H;
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const RingLayout SL = ring_layout(TT, rp.W, rp.flush_min);
+  unsigned char* sA = sm + SL.a;
+  unsigned char* sFA = sm + SL.fa;
+  unsigned char* sFK = sm + SL.fk;
+  unsigned char* sB = sm + SL.b;
+  float* hred = reinterpret_cast<float*>(sm + SL.hred);
+  float* hfin = reinterpret_cast<float*>(sm + SL.hfin);
+  uint16_t* hu = reinterpret_cast<uint16_t*>(sm + SL.hu);
+  float* red = reinterpret_cast<float*>(sm + SL.red);
+  float* rn = reinterpret_cast<float*>(sm + SL.rn);
+  float* fin = reinterpret_cast<float*>(sm + SL.fin);    // M[a][b], see the coefficients below
+  float* fint = reinterpret_cast<float*>(sm + SL.fint);  // M transposed
+  float* sdec = reinterpret_cast<float*>(sm + SL.sdec);
+  float* sbeta = reinterpret_cast<float*>(sm + SL.beta);
+  uint64_t* barA = reinterpret_cast<uint64_t*>(sm + SL.bar);  // checkpoint copy
+  uint64_t* barF = barA + 1;                                   // fold product
+  uint64_t* barD = barA + 2;                                   // dot products
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL.tslot);
+  const uint32_t fk_part = (uint32_t)((rp.W + 15) / 16) * 4096u;  // bytes between the key parts
+  uint16_t* outp = static_cast<uint16_t*>(p.out);
+
+  if (tid == 0) {
+    mbar_init(barA, 1);
+    mbar_init(barF, 1);
+    mbar_init(barD, 1);
+  }
+  if (warp == 0) tmem_alloc(tslot, RING_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t row_tmem = tmem + ((uint32_t)(warp * 32) << 16);
+  uint32_t phA = 0, phF = 0, phD = 0;                // mbarrier phases
+  bool pendA = false, pendF = false, pendD = false;  // a copy or a product is in flight
+  bool broken = false;                               // a bounded wait gave up: nothing more is issued
+
+  // The first item's slot, checkpoint copy and token inputs.
+  int it = blockIdx.x;
+  int b = it / p.H, h = it % p.H;
+  TokenRegs<TT> L;
+  zero_tokens(L);
+  load_tokens(p, b, h, T, L);
+  int n = p.state_indices[b];
+  bool active = n >= 0 && n < p.N;
+  if (TMA && active) {
+    if (tid == 0) {
+      mbar_expect_tx(barA, KD * KD * 2);
+      tma_load_3d(sA, &smap, 0, h * KD, n, barA);
+      tma_load_3d(sA + KD * 128, &smap, 64, h * KD, n, barA);
+    }
+    pendA = true;
+  }
+  int hist = active ? rp.hist_len[n] : 0;
+
+  for (; it < total; it += gridDim.x) {
+    const int itn = it + gridDim.x;
+    const bool has_next = itn < total;
+    const int bn = has_next ? itn / p.H : 0, hn = has_next ? itn % p.H : 0;
+    const int n_next = has_next ? p.state_indices[bn] : -1;
+    const bool active_next = n_next >= 0 && n_next < p.N;
+    const bool valid = active && hist >= 0 && hist <= rp.W;
+    const int64_t obase = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + tid;
+    if (active && !valid && tid == 0 && h == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_HIST_LEN);
+
+    const bool fold = valid && hist >= rp.flush_min;
+    const int base = fold ? 0 : hist;
+    uint16_t* kc = static_cast<uint16_t*>(rp.k_cache) + (int64_t)n * rp.k_slot_stride + (int64_t)h * rp.W * KD;
+    uint16_t* uc = static_cast<uint16_t*>(rp.u_cache) + (int64_t)n * rp.u_slot_stride + (int64_t)h * rp.W * KD;
+    float* gc = static_cast<float*>(rp.g_cache) + (int64_t)n * rp.g_slot_stride + (int64_t)h * rp.W * KD;
+    uint16_t* gstate = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride + (int64_t)h * KD * KD;
+
+    bool ok = valid && !broken;
+    uint16_t vcur[TT];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) vcur[t] = L.vv[t];
+    float X[NB];
+#pragma unroll
+    for (int i = 0; i < NB; ++i) X[i] = 0.0f;
+    int hist_next = 0;
+    const int fks = (hist + 15) / 16;  // fold K steps
+
+    if (ok) {
+      // History reads, used after the per-channel work below: G_{h-1} and the
+      // first 8 entries' G_j and k~_j of channel tid, u~_j of value row tid.
+      const float Gl = hist > 0 ? gc[(int64_t)(hist - 1) * KD + tid] : 0.0f;
+      float Gj0[8];
+      uint16_t kj0[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        Gj0[e] = e < hist ? gc[(int64_t)e * KD + tid] : 0.0f;
+        kj0[e] = e < hist ? kc[(int64_t)e * KD + tid] : (uint16_t)0;
+      }
+      uint16_t uh[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) uh[j] = j < hist ? uc[(int64_t)j * KD + tid] : (uint16_t)0;
+
+      if constexpr (!TMA) {  // plain loads into the same swizzled layout
+        for (int r = 0; r < KD; ++r)
+          *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, tid)) = gstate[(int64_t)r * KD + tid];
+      }
+      const RingGate gate(p, L.alog);
+      if (tid < TT) sbeta[tid] = tid < T ? gate.beta(bf16_bits_to_float(L.blogit)) : 0.0f;
+
+      // L2 norms: block sums of q_t^2 (value t) and k_t^2 (value TT + t), then
+      // one inverse norm per value.
+      {
+        float vals[NB];
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const float q = bf16_bits_to_float(L.qv[t]), k = bf16_bits_to_float(L.kv[t]);
+          vals[t] = __fmul_rn(q, q);
+          vals[TT + t] = __fmul_rn(k, k);
+        }
+        reduce_scatter<NB>(vals, lane);
+        if (NB == 32 || (lane & 1) == 0) red[warp * 32 + (NB == 32 ? lane : lane >> 1)] = vals[0];
+      }
+      __syncthreads();
+      if (tid < NB) rn[tid] = inv_norm(block_sum(red, 0, tid));
+      __syncthreads();
+
+      float qh[TT], kt[TT];
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        qh[t] = __fmul_rn(bf16_bits_to_float(L.qv[t]), rn[t]);
+        kt[t] = round_bf16(__fmul_rn(bf16_bits_to_float(L.kv[t]), rn[TT + t]));
+      }
+
+      // Per channel: gate, G, decays, P_t and the query vectors of the
+      // product. The gates are independent; only G and P are running.
+      // Without a fold the checkpoint enters as S_0^T (exp(G_{h-1}) x).
+      const float e_last = hist > 0 ? expf(Gl) : 1.0f;
+      if (fold) sdec[tid] = e_last;
+      const float dtb = L.dtb;
+      float dd[TT], Gt[TT], pk[TT], pq[TT];
+      {
+        float gg[TT];
+#pragma unroll
+        for (int t = 0; t < TT; ++t) gg[t] = gate.g(bf16_bits_to_float(L.gv[t]), dtb);
+        float G = fold ? 0.0f : Gl;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          Gt[t] = __fadd_rn(G, gg[t]);
+          dd[t] = __expf(__fsub_rn(Gt[t], G));
+          G = Gt[t];
+        }
+        float P = 1.0f;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          P = __fmul_rn(P, dd[t]);
+          pk[t] = __fmul_rn(P, kt[t]);  // zero past T: k~_t is zero there
+          pq[t] = __fmul_rn(P, qh[t]);
+        }
+      }
+      if (!fold) {
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          store_split<NB2>(sB, sB + NB * 128, t, tid, __fmul_rn(e_last, pk[t]));
+          store_split<NB2>(sB, sB + NB * 128, TT + t, tid, __fmul_rn(e_last, pq[t]));
+        }
+      }
+
+      // Coefficients, as the TT x TT matrix M (flat index a TT + b): a > b
+      // holds cc[a][b] = (w_ab k~_b) . k~_a, a <= b holds
+      // ec[b][a] = (w_ba k~_a) . q_hat_b, with w a running product of the
+      // token decays; 32 entries per chunk. Rows and columns past T are zero.
+#pragma unroll
+      for (int a0 = 0; a0 < TT; a0 += 32 / TT) {
+        float vals[32];
+#pragma unroll
+        for (int r = 0; r < 32 / TT; ++r) {
+          const int a = a0 + r;
+#pragma unroll
+          for (int b2 = 0; b2 < TT; ++b2) vals[r * TT + b2] = 0.0f;
+          float w = 1.0f;  // w_{a,b} for b = a-1, a-2, ...: d_a d_{a-1} ... d_{b+1}
+#pragma unroll
+          for (int b2 = TT - 1; b2 >= 0; --b2) {
+            if (b2 < a) {
+              w = __fmul_rn(w, dd[b2 + 1]);
+              vals[r * TT + b2] = __fmul_rn(__fmul_rn(w, kt[b2]), kt[a]);
+            }
+          }
+          float w2 = 1.0f;  // w_{b,a} for b = a, a+1, ...: d_{a+1} ... d_b
+#pragma unroll
+          for (int b2 = 0; b2 < TT; ++b2) {
+            if (b2 >= a) {
+              if (b2 > a) w2 = __fmul_rn(w2, dd[b2]);
+              vals[r * TT + b2] = __fmul_rn(__fmul_rn(w2, kt[a]), qh[b2]);
+            }
+          }
+        }
+        reduce_scatter<32>(vals, lane);
+        red[((1 + a0 * TT / 32) * 4 + warp) * 32 + lane] = vals[0];
+      }
+
+      // hist_len of the next item (its slot index has arrived by now).
+      if (has_next && active_next) hist_next = rp.hist_len[n_next];
+
+      // u~ of row tid into shared memory: the fold's A operand (zero past
+      // hist) or the history buffer.
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (fold) {
+          if (j < fks * 16) *reinterpret_cast<uint16_t*>(sFA + sw32_offset(128, tid, j)) = uh[j];
+        } else if (j < hist) {
+          hu[j * KD + tid] = uh[j];
+        }
+      }
+      for (int j = 16; j < (fold ? fks * 16 : hist); ++j) {
+        const uint16_t u = j < hist ? uc[(int64_t)j * KD + tid] : (uint16_t)0;
+        if (fold)
+          *reinterpret_cast<uint16_t*>(sFA + sw32_offset(128, tid, j)) = u;
+        else
+          hu[j * KD + tid] = u;
+      }
+
+      // History, in blocks of 8 entries: the keys exp(G_{h-1} - G_j) k~_j of
+      // channel tid (zero past hist). With a fold they go, in three bf16
+      // parts, into the fold's B operand (row tid, column j); otherwise their
+      // products with the query vectors are summed over the block (chunk
+      // j / CPE, value (j % CPE) NB + 2t with P_t k~_t, + 1 with P_t q_hat_t).
+      for (int j0 = 0; j0 < (fold ? fks * 16 : hist); j0 += 8) {
+        float Gj[8];
+        uint16_t kj[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const bool in = j0 + e < hist;
+          if (j0 == 0) {
+            Gj[e] = Gj0[e];
+            kj[e] = kj0[e];
+          } else {
+            Gj[e] = in ? gc[(int64_t)(j0 + e) * KD + tid] : 0.0f;
+            kj[e] = in ? kc[(int64_t)(j0 + e) * KD + tid] : (uint16_t)0;
+          }
+        }
+        float kw[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          kw[e] = j0 + e < hist ? __fmul_rn(expf(__fsub_rn(Gl, Gj[e])), bf16_bits_to_float(kj[e])) : 0.0f;
+        if (fold) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) store_split3(sFK, fk_part, tid, j0 + e, kw[e]);
+        } else {
+#pragma unroll
+          for (int e0 = 0; e0 < 8; e0 += CPE) {
+            float vals[32];
+#pragma unroll
+            for (int e = 0; e < CPE; ++e)
+#pragma unroll
+              for (int t = 0; t < TT; ++t) {
+                vals[e * NB + 2 * t] = __fmul_rn(kw[e0 + e], pk[t]);
+                vals[e * NB + 2 * t + 1] = __fmul_rn(kw[e0 + e], pq[t]);
+              }
+            reduce_scatter<32>(vals, lane);
+            hred[(((j0 + e0) / CPE) * 4 + warp) * 32 + lane] = vals[0];
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the operands are read by the tensor core
+
+      // The checkpoint has arrived in every thread's view, or the CTA stops.
+      bool a_ok = true;
+      if constexpr (TMA) a_ok = mbar_wait_bounded(barA, phA);
+      ok = __syncthreads_and(a_ok) != 0;  // also publishes the operands and the partial sums
+      if (TMA) {
+        if (ok) {
+          phA ^= 1u;
+          pendA = false;
+        } else {
+          broken = true;
+          if (tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+        }
+      }
+
+      if (ok) {  // the new ring entries of channel tid (its history reads are done)
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+          if (t < T) {
+            kc[(int64_t)(base + t) * KD + tid] = float_to_bf16_bits(kt[t]);
+            gc[(int64_t)(base + t) * KD + tid] = Gt[t];
+          }
+      }
+
+      if (fold && ok) {
+        if (tid == 0) {  // D[row][key] = sum_j u~_j[row] hkey_j[key], K in steps of 16 entries
+          tc_fence_after();
+          constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+          const uint32_t a0 = smem_addr(sFA), k0 = smem_addr(sFK);
+          for (int part = 0; part < 3; ++part)
+            for (int ks = 0; ks < fks; ++ks)
+              tc_mma_bf16(tmem, sw32_desc(a0 + ks * 4096), sw32_desc(k0 + part * fk_part + ks * 4096), idesc,
+                          (part | ks) != 0 ? 1u : 0u);
+          tc_commit(barF);
+        }
+        pendF = true;
+      }
+
+      // Block sums of the coefficients (M and its transpose) and the history
+      // coefficients, while the fold's product runs.
+      for (int i = tid; i < TT * TT; i += RING_THREADS) {
+        const float v = block_sum(red, 1 + (i >> 5), i & 31);
+        fin[i] = v;
+        fint[(i % TT) * TT + i / TT] = v;
+      }
+      const int nhc = fold ? 0 : (hist + 7) / 8 * (8 / CPE);
+      for (int i = tid; i < nhc * 32; i += RING_THREADS) hfin[i] = block_sum(hred, i >> 5, i & 31);
+
+      if (pendF) {
+        const bool f_ok = __syncthreads_and(mbar_wait_bounded(barF, phF)) != 0;
+        if (f_ok) {
+          phF ^= 1u;
+          pendF = false;
+          // Row tid of the folded state: exp(G_{h-1}) s_0 + D, rounded in place.
+          tc_fence_after();
+#pragma unroll 1
+          for (int cb = 0; cb < KD / 16; ++cb) {
+            float dsum[16];
+            tmem_ld16(row_tmem + cb * 16, dsum);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int k = cb * 16 + half * 8;
+              uint4* cell = reinterpret_cast<uint4*>(sA + sw128_offset(KD, tid, k));
+              uint4 raw = *cell;
+              const float4 d0 = *reinterpret_cast<const float4*>(sdec + k);
+              const float4 d1 = *reinterpret_cast<const float4*>(sdec + k + 4);
+              const float* ds = dsum + half * 8;
+              const f32x2 s0 = fma2(pk2(d0.x, d0.y), bf16x2_to_f32x2(raw.x), pk2(ds[0], ds[1]));
+              const f32x2 s1 = fma2(pk2(d0.z, d0.w), bf16x2_to_f32x2(raw.y), pk2(ds[2], ds[3]));
+              const f32x2 s2 = fma2(pk2(d1.x, d1.y), bf16x2_to_f32x2(raw.z), pk2(ds[4], ds[5]));
+              const f32x2 s3 = fma2(pk2(d1.z, d1.w), bf16x2_to_f32x2(raw.w), pk2(ds[6], ds[7]));
+              raw.x = f32x2_to_bf16x2(s0);
+              raw.y = f32x2_to_bf16x2(s1);
+              raw.z = f32x2_to_bf16x2(s2);
+              raw.w = f32x2_to_bf16x2(s3);
+              *cell = raw;
+            }
+          }
+          // The B operand overwrites the fold's operands, which its product has read.
+#pragma unroll
+          for (int t = 0; t < TT; ++t) {
+            store_split<NB2>(sB, sB + NB * 128, t, tid, pk[t]);
+            store_split<NB2>(sB, sB + NB * 128, TT + t, tid, pq[t]);
+          }
+          fence_proxy_async_smem();
+        } else {
+          ok = false;
+          broken = true;
+          if (tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+        }
+        tc_fence_before();
+      }
+      __syncthreads();  // the folded rows, the B operand and the coefficient sums
+
+      // The product: D[row][col] = sum_k A[row][k] B[col][k], K in 8 steps of
+      // 16; columns NB.. hold the low halves' share.
+      if (ok) {
+        if (tid == 0) {
+          tc_fence_after();
+          constexpr uint32_t idesc = idesc_bf16_f32(128, NB2);
+          const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_bf16(tmem, sw128_desc(a0 + (kk >> 2) * (KD * 128) + (kk & 3) * 32),
+                        sw128_desc(b0 + (kk >> 2) * (NB2 * 128) + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
+          tc_commit(barD);
+          if (TMA && fold) {
+            tma_store_3d(&smap, 0, h * KD, n, sA);
+            tma_store_3d(&smap, 64, h * KD, n, sA + KD * 128);
+            bulk_commit();
+          }
+        }
+        pendD = true;
+        if (!TMA && fold) {
+          for (int r = 0; r < KD; ++r)
+            gstate[(int64_t)r * KD + tid] = *reinterpret_cast<const uint16_t*>(sA + sw128_offset(KD, r, tid));
+        }
+        fence_proxy_async_smem();  // generic reads of the buffer before the next copy into it
+        const bool d_ok = __syncthreads_and(mbar_wait_bounded(barD, phD)) != 0;
+        if (d_ok) {
+          phD ^= 1u;
+          pendD = false;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < NB; c0 += 16) {
+            float xh[16], xl[16];
+            tmem_ld16(row_tmem + c0, xh);
+            tmem_ld16(row_tmem + NB + c0, xl);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) X[c0 + i] = __fadd_rn(xh[i], xl[i]);
+          }
+        } else {
+          ok = false;
+          broken = true;
+          if (tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+        }
+      }
+    } else if (has_next && active_next) {
+      hist_next = rp.hist_len[n_next];
+    }
+
+    // The checkpoint buffer is free: start the next item's copy and token loads.
+    if (tid == 0) {
+      if (TMA && fold && ok) bulk_wait_read_all();  // the fold's store has read the buffer
+      if (TMA && pendA && !valid && !broken) {       // a skipped item's copy must land first
+        if (!mbar_wait_bounded(barA, phA)) {
+          broken = true;
+          if (p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+        }
+      }
+    }
+    if (TMA && pendA && !valid) {
+      broken = __syncthreads_or(broken) != 0;
+      if (!broken) {
+        phA ^= 1u;
+        pendA = false;
+      }
+    }
+    if (TMA && has_next && active_next && !broken) {
+      if (tid == 0) {
+        mbar_expect_tx(barA, KD * KD * 2);
+        tma_load_3d(sA, &smap, 0, hn * KD, n_next, barA);
+        tma_load_3d(sA + KD * 128, &smap, 64, hn * KD, n_next, barA);
+      }
+      pendA = true;
+    }
+    if (has_next) load_tokens(p, bn, hn, T, L);
+
+    // Row tid: history terms, then the recurrence over the tokens (padded
+    // slots compute zeros and write nothing).
+    if (ok && !fold) {
+      for (int j = 0; j < hist; ++j) {
+        const float u = bf16_bits_to_float(hu[j * KD + tid]);
+        const float4* cj = reinterpret_cast<const float4*>(hfin + (j / CPE) * 32 + (j % CPE) * NB);
+#pragma unroll
+        for (int t2 = 0; t2 < TT / 2; ++t2) {
+          const float4 c = cj[t2];  // (k, q) of tokens 2 t2 and 2 t2 + 1
+          X[2 * t2] = __fmaf_rn(u, c.x, X[2 * t2]);
+          X[TT + 2 * t2] = __fmaf_rn(u, c.y, X[TT + 2 * t2]);
+          X[2 * t2 + 1] = __fmaf_rn(u, c.z, X[2 * t2 + 1]);
+          X[TT + 2 * t2 + 1] = __fmaf_rn(u, c.w, X[TT + 2 * t2 + 1]);
+        }
+      }
+    }
+    if (active) {
+      float ut[TT];
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        float cct[TT], ect[TT];  // cc[t][s] (s < t) and ec[t][s] (s <= t)
+#pragma unroll
+        for (int s4 = 0; s4 < TT / 4; ++s4) {
+          const float4 c = reinterpret_cast<const float4*>(fin + t * TT)[s4];
+          const float4 e = reinterpret_cast<const float4*>(fint + t * TT)[s4];
+          cct[4 * s4] = c.x;
+          cct[4 * s4 + 1] = c.y;
+          cct[4 * s4 + 2] = c.z;
+          cct[4 * s4 + 3] = c.w;
+          ect[4 * s4] = e.x;
+          ect[4 * s4 + 1] = e.y;
+          ect[4 * s4 + 2] = e.z;
+          ect[4 * s4 + 3] = e.w;
+        }
+        float acc = 0.0f;
+#pragma unroll
+        for (int s2 = 0; s2 < t; ++s2) acc = __fmaf_rn(cct[s2], ut[s2], acc);
+        ut[t] = round_bf16(__fmul_rn(sbeta[t], __fsub_rn(bf16_bits_to_float(vcur[t]), __fadd_rn(X[t], acc))));
+        float acco = 0.0f;
+#pragma unroll
+        for (int s2 = 0; s2 <= t; ++s2) acco = __fmaf_rn(ect[s2], ut[s2], acco);
+        const float o = __fmul_rn(p.scale, __fadd_rn(X[TT + t], acco));
+        if (t < T) {
+          outp[obase + (int64_t)t * p.out_t_stride] = ok ? float_to_bf16_bits(o) : (uint16_t)0;
+          if (ok) uc[(int64_t)(base + t) * KD + tid] = float_to_bf16_bits(ut[t]);
+        }
+      }
+    } else {
+      for (int t = 0; t < T; ++t) outp[obase + (int64_t)t * p.out_t_stride] = 0;
+    }
+
+    tc_fence_before();
+    __syncthreads();  // this item's shared-memory and tensor-memory reads are done
+    tc_fence_after();
+    b = bn;
+    h = hn;
+    n = n_next;
+    active = active_next;
+    hist = hist_next;
+  }
+
+  // Anything still in flight after a wait that gave up gets one more bounded
+  // wait before the tensor memory is released and the CTA leaves.
+  if (tid == 0) {
+    if (pendA) mbar_wait_bounded(barA, phA);
+    if (pendF) mbar_wait_bounded(barF, phF);
+    if (pendD) mbar_wait_bounded(barD, phD);
+    if (TMA) bulk_wait_read_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, RING_TMEM_COLS);
+  }
+}
+
+// After the ring kernel, one thread per batch row: a fold resets hist_len[n]
+// to 0 (restart_hist_on_flush). hist_len is shared by every head of the slot,
+// so this waits until every head's CTA has read it.
+__global__ void kda_ring_reset_kernel(const kda_params p, const kda_ring_params rp) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.B) return;
   const int n = p.state_indices[b];
   if (n < 0 || n >= p.N) return;
   const int hist = rp.hist_len[n];
-  if (hist < 0 || hist > rp.W) return;
-  const bool fold = hist >= rp.flush_min;
-  const int base = fold ? 0 : hist;
-  for (int h = warp; h < p.H; h += blockDim.x >> 5) {
-    uint16_t* kc = static_cast<uint16_t*>(rp.k_cache) + (int64_t)n * rp.k_slot_stride + (int64_t)h * rp.W * KD;
-    float* gc = static_cast<float*>(rp.g_cache) + (int64_t)n * rp.g_slot_stride + (int64_t)h * rp.W * KD;
-    const Gate gate(p, h);
-    float G_prev[4], dtb[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = lane + 32 * i;
-      dtb[i] = gate.dt_bias(p, h, c);
-      G_prev[i] = (!fold && hist > 0) ? gc[(int64_t)(hist - 1) * KD + c] : 0.0f;
-    }
-    for (int t0 = 0; t0 < T; t0 += 8) {
-      float kv[8][4], gv[8][4];
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          kv[tt][i] = gv[tt][i] = 0.0f;
-          if (t0 + tt < T) {
-            kv[tt][i] = load_bf16(p.k, b, t0 + tt, h, lane + 32 * i);
-            gv[tt][i] = load_bf16(p.g_raw, b, t0 + tt, h, lane + 32 * i);
-          }
-        }
-      }
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        const int t = t0 + tt;
-        if (t >= T) break;
-        float sq[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sq[i] = __fmul_rn(kv[tt][i], kv[tt][i]);
-        const float rk = inv_norm(sum_channels(sq[0], sq[1], sq[2], sq[3]));
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = lane + 32 * i;
-          const float g = gate.g(gv[tt][i], dtb[i]);
-          const float G = __fadd_rn(G_prev[i], g);
-          kc[(int64_t)(base + t) * KD + c] = float_to_bf16_bits(__fmul_rn(kv[tt][i], rk));
-          gc[(int64_t)(base + t) * KD + c] = G;
-          G_prev[i] = G;
-        }
-      }
-    }
-  }
-  if (fold && rp.restart_hist_on_flush) {
-    __syncthreads();  // every warp has read hist_len
-    if (threadIdx.x == 0) rp.hist_len[n] = 0;
-  }
+  if (hist >= rp.flush_min && hist <= rp.W) rp.hist_len[n] = 0;
 }
 
-template <int TV, bool BULK, int TT>
-static cudaError_t launch_ring_one(const kda_params& p, int T, const kda_ring_params& r, cudaStream_t s) {
-  constexpr int NW = TV == 128 ? 8 : 4;  // a whole-head tile gets 8 warps
-  auto kern = kda_ring_kernel<TV, BULK, TT, NW>;
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// The state pool as a 3-D bf16 tensor {128 keys, H * 128 value rows, N slots}
+// read and written in {64, 128, 1} boxes with the 128-byte swizzle. The last
+// map is kept per host thread, keyed by pool address and shape.
+static cudaError_t state_tensor_map(const kda_params& p, CUtensorMap* out) {
+  struct Cached {
+    const void* ptr = nullptr;
+    int N = 0, H = 0;
+    int64_t stride = 0;
+    CUtensorMap map;
+  };
+  thread_local Cached cache;
+  const int64_t slot = p.N > 1 ? p.state_slot_stride : (int64_t)p.H * KD * KD;
+  if (cache.ptr == p.state && cache.N == p.N && cache.H == p.H && cache.stride == slot) {
+    *out = cache.map;
+    return cudaSuccess;
+  }
+  const EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)KD, (cuuint64_t)p.H * KD, (cuuint64_t)p.N};
+  const cuuint64_t strides[2] = {(cuuint64_t)KD * 2, (cuuint64_t)slot * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMap map;
+  const CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.state, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  cache.ptr = p.state;
+  cache.N = p.N;
+  cache.H = p.H;
+  cache.stride = slot;
+  cache.map = map;
+  *out = map;
+  return cudaSuccess;
+}
+
+template <bool TMA, int TT>
+static cudaError_t launch_ring_one(const CUtensorMap& map, const kda_params& p, int T, const kda_ring_params& r,
+                                   cudaStream_t s) {
+  auto kern = kda_ring_kernel<TMA, TT>;
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
-  cudaError_t e = set_smem_limit_once(kern, ring_smem_bytes(TV, KDA_MAX_T, 64), smem_set);
+  cudaError_t e = set_smem_limit_once(kern, ring_smem_bytes(TT, 64, 64), smem_set);
   if (e != cudaSuccess) return e;
-  const int tiles = KD / TV;
-  const long long blocks = (long long)p.B * p.H * tiles;
-  kern<<<(unsigned)blocks, 32 * NW, ring_smem_bytes(TV, T, r.W), s>>>(p, r, T, tiles);
+  static std::atomic<bool> carveout_set{false};  // all of L1 as shared memory: several CTAs per SM
+  if (!carveout_set.load(std::memory_order_acquire)) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+    carveout_set.store(true, std::memory_order_release);
+  }
+  // Persistent grid: as many CTAs as fit on the device at once (shared
+  // memory, registers, and tensor-memory columns: 512 per SM), at most one
+  // per item. The occupancy calculator is not used: it reports one CTA per
+  // SM for any kernel that allocates tensor memory.
+  const size_t smem = ring_smem_bytes(TT, r.W, r.flush_min);
+  int dev = 0, sms = 0, smem_sm = 0, reserved = 0, regs_sm = 0, blocks_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&blocks_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev)) != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+  const int warp_regs = (fa.numRegs * 32 + 255) / 256 * 256;
+  int per_sm = smem_sm / (int)(smem + reserved);
+  per_sm = std::min(per_sm, regs_sm / (warp_regs * (RING_THREADS / 32)));
+  per_sm = std::min(per_sm, 512 / (int)RING_TMEM_COLS);
+  per_sm = std::min(per_sm, blocks_sm);
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const long long items = (long long)p.B * p.H;
+  const long long grid = std::min(items, (long long)sms * per_sm);
+  kern<<<(unsigned)grid, RING_THREADS, smem, s>>>(map, p, r, T);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int append_warps = p.H < APPEND_WARPS ? p.H : APPEND_WARPS;
-  kda_ring_append_kernel<<<(unsigned)p.B, 32 * append_warps, 0, s>>>(p, r, T);
+  if (e != cudaSuccess || !r.restart_hist_on_flush) return e;
+  kda_ring_reset_kernel<<<(unsigned)((p.B + 127) / 128), 128, 0, s>>>(p, r);
   return cudaGetLastError();
 }
 
-template <int TV>
-static cudaError_t launch_ring_tv(const kda_params& p, int T, const kda_ring_params& r, bool bulk, cudaStream_t s) {
-  if (T <= 8) return bulk ? launch_ring_one<TV, true, 8>(p, T, r, s) : launch_ring_one<TV, false, 8>(p, T, r, s);
-  return bulk ? launch_ring_one<TV, true, 16>(p, T, r, s) : launch_ring_one<TV, false, 16>(p, T, r, s);
+template <bool TMA>
+static cudaError_t launch_ring_tma(const CUtensorMap& map, const kda_params& p, int T, const kda_ring_params& r,
+                                   cudaStream_t s) {
+  return T <= 8 ? launch_ring_one<TMA, 8>(map, p, T, r, s) : launch_ring_one<TMA, 16>(map, p, T, r, s);
 }
 
-cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, int tile_v, bool bulk,
-                        cudaStream_t s) {
-  switch (tile_v) {
-    case 16: return launch_ring_tv<16>(p, T, r, bulk, s);
-    case 32: return launch_ring_tv<32>(p, T, r, bulk, s);
-    case 64: return launch_ring_tv<64>(p, T, r, bulk, s);
-    case 128: return launch_ring_tv<128>(p, T, r, bulk, s);
-    default: return cudaErrorInvalidValue;
+cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, bool bulk, cudaStream_t s) {
+  CUtensorMap map;
+  memset(&map, 0, sizeof(map));
+  if (bulk) {
+    const cudaError_t e = state_tensor_map(p, &map);
+    if (e != cudaSuccess) return e;
+    return launch_ring_tma<true>(map, p, T, r, s);
   }
+  return launch_ring_tma<false>(map, p, T, r, s);
 }
 
 }  // namespace kda

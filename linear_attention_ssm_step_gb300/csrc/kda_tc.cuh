@@ -1,0 +1,138 @@
+// kda_tc.cuh - fifth-generation tensor cores (tcgen05, accumulators in tensor
+// memory) and tensor-map bulk copies (cp.async.bulk.tensor) for sm_103a.
+//
+// Operand layout used throughout: a K-major bf16 matrix of R rows (R a
+// multiple of 8) and 128 columns, stored as two regions of R rows x 128 bytes
+// (columns 0..63, then 64..127), each region 1024-byte aligned, with the
+// 128-byte swizzle: the 16-byte chunk c of row r sits at chunk c ^ (r % 8).
+// That is the layout a tensor-map load with CU_TENSOR_MAP_SWIZZLE_128B and a
+// 64-column box writes, and the canonical K-major, 128-byte-swizzled layout
+// the tensor core reads through a shared-memory matrix descriptor (8-row
+// groups 1024 bytes apart).
+#pragma once
+
+#include <cuda.h>
+
+#include "kda_device.cuh"
+
+namespace kda {
+
+// ---------------------------------------------------------------- tensor-map copies
+
+// 3-D tiled load into shared memory, completing its bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 3-D tiled store from shared memory in the current bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, const void* src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+               : "memory");
+}
+
+// ---------------------------------------------------------------- operand layout
+
+// Byte offset of bf16 element (r, k) of a K-major, 128-byte-swizzled operand of R rows.
+__host__ __device__ constexpr uint32_t sw128_offset(int R, int r, int k) {
+  return (uint32_t)(k >> 6) * (uint32_t)R * 128u + (uint32_t)r * 128u +
+         ((uint32_t)(((k & 63) >> 3) ^ (r & 7)) << 4) + ((uint32_t)(k & 7) << 1);
+}
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
+// starting at shared address `saddr`: start address (bits 0-13, in 16-byte
+// units), leading byte offset 16 (unused by this layout), stride byte offset
+// 1024 between 8-row groups (bits 32-45), descriptor version 1 (bit 46),
+// base offset 0 (the swizzle atoms are 1024-byte aligned), swizzle mode 2 =
+// 128-byte (bits 61-63). Stepping K by 16 elements inside a region adds 32
+// bytes to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
+         ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
+// Byte offset of bf16 element (r, k) of a K-major operand of R rows with the
+// 32-byte swizzle: K in regions of 16 columns (R rows x 32 bytes each); the
+// 16-byte chunk c (0 or 1) of row r sits at chunk c ^ ((r / 4) % 2).
+__host__ __device__ constexpr uint32_t sw32_offset(int R, int r, int k) {
+  return (uint32_t)(k >> 4) * (uint32_t)R * 32u + (uint32_t)r * 32u +
+         ((uint32_t)(((k & 15) >> 3) ^ ((r >> 2) & 1)) << 4) + ((uint32_t)(k & 7) << 1);
+}
+
+// Descriptor of a K-major operand with the 32-byte swizzle: 8-row groups 256
+// bytes apart, swizzle mode 6 = 32-byte; one region holds one K step of 16.
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1u << 16) | ((uint64_t)(256u >> 4) << 32) |
+         ((uint64_t)1u << 46) | ((uint64_t)6u << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B (both
+// K-major), fp32 accumulation, M x N: D format F32 (bits 4-5 = 1), A and B
+// format BF16 (bits 7-9 and 10-12 = 1), N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- tensor memory
+
+// Allocate `ncols` (a power of two >= 32) tensor-memory columns; the whole
+// warp executes this and the base address lands in *dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Order tcgen05 operations around a thread barrier.
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (tensor memory) = A B^T (+ D if accumulate), issued by one thread.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One arrival on `bar` once every tcgen05.mma this thread issued has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane (warp w
+// reads lanes 32 (w % 4) .. 32 (w % 4) + 31). The wait names the registers,
+// so no use of them moves above it.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&out)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) out[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace kda

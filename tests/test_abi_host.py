@@ -192,6 +192,15 @@ def test_ring_rejects(lib, T, mut, expect, msg):
 
 
 @no_gpu
+@pytest.mark.parametrize("config", [0, 1, 2])
+def test_ring_rejects_partial_head_tiles(lib, config):
+    p = fake_params()
+    p.config_override = config
+    assert status(lib, p, T=8, ring=ring()) == kda.KDA_EUNSUPPORTED
+    assert "whole-head" in kda.kda_last_error()
+
+
+@no_gpu
 def test_ring_null_and_empty(lib):
     p = fake_params()
     assert lib.kda_verify_ring(ctypes.byref(p), 8, None, None) == kda.KDA_EINVAL
@@ -212,11 +221,9 @@ def test_config_table_and_selector(lib):
         assert 0 <= c < n and c >= prev  # tiles never shrink as the batch grows
         prev = c
     assert kda.kda_config_tile_v(kda.kda_select_config(512, 1)) == 128
-    prev = 0
-    for B in (1, 2, 8, 16, 32, 64, 128, 512, 4096):
-        c = kda.kda_select_ring_config(B, 8)
-        assert 0 <= c < n and c >= prev
-        prev = c
+    for B in (0, 1, 2, 8, 16, 32, 64, 128, 512, 4096):  # the ring kernel always takes whole heads
+        for T in (1, 4, 8, 16):
+            assert kda.kda_config_tile_v(kda.kda_select_ring_config(B, T)) == 128
     assert kda.kda_select_ring_config(-1, 8) == -1 and kda.kda_select_ring_config(4, 17) == -1
 
 

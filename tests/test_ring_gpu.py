@@ -91,12 +91,11 @@ def test_ring_serving_batch_512_sampled(dev):
     check_ring(w, dev, rows=rows)
 
 
-@pytest.mark.parametrize("config", [0, 1, 2, 3])
-def test_ring_every_tile_gives_the_same_bits(dev, config):
+def test_ring_whole_head_config_is_the_default(dev):
     w = workloads.ring_inputs(5, 12, T=8, W=32, flush_min=9, fold_frac=0.5, seed=7)
     a, b = w.to(dev), w.to(dev)
-    oa = gpu_ring(a, config_override=config)
-    ob = gpu_ring(b, config_override=2)
+    oa = gpu_ring(a, config_override=3)
+    ob = gpu_ring(b)
     torch.cuda.synchronize()
     assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
     for name in ("k_cache", "u_cache", "g_cache", "hist_len"):
@@ -110,6 +109,33 @@ def test_ring_w16_t4(dev):
     """The other mode of the pages: ring width 16, T = 4, flush_min = 13."""
     w = workloads.ring_inputs(6, 20, T=4, W=16, flush_min=13, fold_frac=0.5, seed=8)
     check_ring(w, dev)
+
+
+@pytest.mark.parametrize("T,W,flush_min", [(16, 32, 17), (1, 16, 16), (8, 64, 40), (16, 64, 49)])
+def test_ring_other_widths_and_token_counts(dev, T, W, flush_min):
+    """T = 16 and T = 1 token slots, and a 64-wide ring whose histories run to
+    flush_min - 1 + T entries."""
+    w = workloads.ring_inputs(6, 16, T=T, W=W, flush_min=flush_min, fold_frac=0.5, seed=40 + T + W)
+    check_ring(w, dev)
+
+
+def test_ring_misaligned_pool_uses_plain_copies_with_same_bits(dev):
+    w = workloads.ring_inputs(6, 12, T=8, W=32, flush_min=9, fold_frac=0.5, seed=14, inactive_frac=0.2)
+    a, b = w.to(dev), w.to(dev)
+    flat = torch.empty(b.state.numel() + 8, dtype=torch.bfloat16, device=dev)
+    mis = flat[1:1 + b.state.numel()].view(b.state.shape)  # 2-byte aligned only
+    mis.copy_(b.state)
+    assert mis.data_ptr() % 16 == 2
+    b.state = mis
+    oa = gpu_ring(a)
+    ob = gpu_ring(b)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+    for name in ("k_cache", "u_cache", "g_cache", "hist_len"):
+        x, y = a.ring[name], b.ring[name]
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32)), name
 
 
 def test_ring_without_restart_keeps_hist_len(dev):
