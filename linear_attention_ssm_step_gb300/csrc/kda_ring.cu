@@ -79,7 +79,6 @@ struct RingLayout {
 __host__ __device__ inline RingLayout ring_layout(int TT, int W, int flush_min) {
   RingLayout L{};
   const uint32_t NB = 2u * TT;
-  const uint32_t ks = ((uint32_t)W + 15u) / 16u;                        // fold K steps
   const uint32_t hmax = flush_min > 1 ? (uint32_t)flush_min - 1 : 0u;  // history of a call that does not fold
   const uint32_t cpe = TT == 8 ? 2u : 1u;                               // history entries per chunk
   const uint32_t nhc = (hmax + 7u) / 8u * (8u / cpe);                   // chunks, in blocks of 8 entries
@@ -87,9 +86,9 @@ __host__ __device__ inline RingLayout ring_layout(int TT, int W, int flush_min) 
   L.a = o;
   o += 128u * 256u;  // checkpoint, 128 rows x 128 keys bf16
   L.u = o;
-  L.fa = o;               // fold: u~ history [ks][128 x 32 B]
-  L.fk = o + ks * 4096u;  // fold: history keys, 3 parts x [ks][128 x 32 B]
-  const uint32_t fold_bytes = ks * 4096u * 4u;
+  L.fa = o;           // fold: u~ history, one K step [128 x 32 B]
+  L.fk = o + 4096u;   // fold: history keys, 3 parts x [128 x 32 B]
+  const uint32_t fold_bytes = 4u * 4096u;
   L.b = o;                        // query vectors: 2 NB rows (high halves, then low) x 256 B
   L.hred = L.b + NB * 512u;       // no fold: history partial sums [nhc][4][32]
   L.hfin = L.hred + nhc * 512u;   // no fold: history coefficients [nhc][32]
@@ -290,7 +289,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
   uint64_t* barF = barA + 1;                                   // fold product
   uint64_t* barD = barA + 2;                                   // dot products
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL.tslot);
-  const uint32_t fk_part = (uint32_t)((rp.W + 15) / 16) * 4096u;  // bytes between the key parts
+  constexpr uint32_t fk_part = 4096u;  // bytes between the key parts
   uint16_t* outp = static_cast<uint16_t*>(p.out);
 
   if (tid == 0) {
@@ -469,30 +468,26 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       // hist_len of the next item (its slot index has arrived by now).
       if (has_next && active_next) hist_next = rp.hist_len[n_next];
 
-      // u~ of row tid into shared memory: the fold's A operand (zero past
-      // hist) or the history buffer.
+      // u~ of row tid into shared memory: the fold's A operand for its first
+      // K step of 16 entries (zero past hist) or the history buffer.
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         if (fold) {
-          if (j < fks * 16) *reinterpret_cast<uint16_t*>(sFA + sw32_offset(128, tid, j)) = uh[j];
+          *reinterpret_cast<uint16_t*>(sFA + sw32_offset(128, tid, j)) = uh[j];
         } else if (j < hist) {
           hu[j * KD + tid] = uh[j];
         }
       }
-      for (int j = 16; j < (fold ? fks * 16 : hist); ++j) {
-        const uint16_t u = j < hist ? uc[(int64_t)j * KD + tid] : (uint16_t)0;
-        if (fold)
-          *reinterpret_cast<uint16_t*>(sFA + sw32_offset(128, tid, j)) = u;
-        else
-          hu[j * KD + tid] = u;
-      }
+      if (!fold)
+        for (int j = 16; j < hist; ++j) hu[j * KD + tid] = uc[(int64_t)j * KD + tid];
 
       // History, in blocks of 8 entries: the keys exp(G_{h-1} - G_j) k~_j of
-      // channel tid (zero past hist). With a fold they go, in three bf16
-      // parts, into the fold's B operand (row tid, column j); otherwise their
-      // products with the query vectors are summed over the block (chunk
-      // j / CPE, value (j % CPE) NB + 2t with P_t k~_t, + 1 with P_t q_hat_t).
-      for (int j0 = 0; j0 < (fold ? fks * 16 : hist); j0 += 8) {
+      // channel tid (zero past hist). With a fold, the first 16 go, in three
+      // bf16 parts, into the fold's B operand (row tid, column j); otherwise
+      // their products with the query vectors are summed over the block
+      // (chunk j / CPE, value (j % CPE) NB + 2t with P_t k~_t, + 1 with
+      // P_t q_hat_t).
+      for (int j0 = 0; j0 < (fold ? 16 : hist); j0 += 8) {
         float Gj[8];
         uint16_t kj[8];
 #pragma unroll
@@ -560,9 +555,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
           constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
           const uint32_t a0 = smem_addr(sFA), k0 = smem_addr(sFK);
           for (int part = 0; part < 3; ++part)
-            for (int ks = 0; ks < fks; ++ks)
-              tc_mma_bf16(tmem, sw32_desc(a0 + ks * 4096), sw32_desc(k0 + part * fk_part + ks * 4096), idesc,
-                          (part | ks) != 0 ? 1u : 0u);
+            tc_mma_bf16(tmem, sw32_desc(a0), sw32_desc(k0 + part * fk_part), idesc, part != 0 ? 1u : 0u);
           tc_commit(barF);
         }
         pendF = true;
@@ -579,10 +572,42 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       for (int i = tid; i < nhc * 32; i += RING_THREADS) hfin[i] = block_sum(hred, i >> 5, i & 31);
 
       if (pendF) {
-        const bool f_ok = __syncthreads_and(mbar_wait_bounded(barF, phF)) != 0;
+        bool f_ok = __syncthreads_and(mbar_wait_bounded(barF, phF)) != 0;
         if (f_ok) {
           phF ^= 1u;
           pendF = false;
+        }
+        // Histories longer than 16 entries: the further K steps, one at a
+        // time through the same operand buffer.
+        for (int ks = 1; ks < fks && f_ok; ++ks) {
+#pragma unroll 4
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = 16 * ks + jj;
+            const bool in = j < hist;
+            *reinterpret_cast<uint16_t*>(sFA + sw32_offset(128, tid, jj)) =
+                in ? uc[(int64_t)j * KD + tid] : (uint16_t)0;
+            const float kw = in ? __fmul_rn(expf(__fsub_rn(Gl, gc[(int64_t)j * KD + tid])),
+                                            bf16_bits_to_float(kc[(int64_t)j * KD + tid]))
+                                : 0.0f;
+            store_split3(sFK, fk_part, tid, jj, kw);
+          }
+          fence_proxy_async_smem();
+          __syncthreads();
+          if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+            for (int part = 0; part < 3; ++part)
+              tc_mma_bf16(tmem, sw32_desc(smem_addr(sFA)), sw32_desc(smem_addr(sFK) + part * fk_part), idesc, 1u);
+            tc_commit(barF);
+          }
+          pendF = true;
+          f_ok = __syncthreads_and(mbar_wait_bounded(barF, phF)) != 0;
+          if (f_ok) {
+            phF ^= 1u;
+            pendF = false;
+          }
+        }
+        if (f_ok) {
           // Row tid of the folded state: exp(G_{h-1}) s_0 + D, rounded in place.
           tc_fence_after();
 #pragma unroll 1
