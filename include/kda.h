@@ -168,6 +168,12 @@ typedef struct {
  *     written at position P.
  * The checkpoint is written only by a fold. hist_len is otherwise left to
  * the caller, who adds the number of accepted draft tokens afterwards.
+ * The ring kernel works on whole heads: p->config_override must be -1 or the
+ * 128-row configuration (3), anything else returns KDA_EUNSUPPORTED. Its
+ * 2T dot products per state row, and a fold's replay, run on the tensor
+ * cores with fp32 accumulation (operands split into bf16 parts, exact to
+ * 2^-17 relative for the query vectors and 2^-25 for the fold's history
+ * keys).
  */
 kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params* r, void* stream);
 
@@ -178,7 +184,7 @@ int32_t kda_config_tile_v(int32_t config);
 /* The configuration kda_decode (T = 1) and kda_verify (T > 1) pick for B rows
    (-1 if B < 0 or T is outside 1..KDA_MAX_T). */
 int32_t kda_select_config(int32_t B, int32_t T);
-/* The configuration kda_verify_ring picks for B rows and T tokens (-1 as above). */
+/* The configuration kda_verify_ring picks for B rows and T tokens: always 3, whole heads (-1 as above). */
 int32_t kda_select_ring_config(int32_t B, int32_t T);
 
 /* Message for the last non-OK status returned on this host thread ("" if none). */
