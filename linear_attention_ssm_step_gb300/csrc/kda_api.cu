@@ -140,9 +140,9 @@ int32_t kda_select_config(int32_t B, int32_t T) {
     if (B <= 32) return 2;  // 64 rows
     return 3;               // 128 rows
   }
-  if (B <= 2) return 0;   // 16 rows
-  if (B <= 16) return 1;  // 32 rows
-  return 3;               // 128 rows
+  if (B <= 2) return 0;  // 16 rows
+  if (B <= 8) return 2;  // 64 rows, 8 warps
+  return 3;              // 128 rows, 8 warps
 }
 
 // The ring kernel runs one CTA per (row, head): its state rows enter one

@@ -1,6 +1,7 @@
 // kda_step.cu - T=1 decode and T-token verify kernels for sm_103a.
 //
-// One CTA (128 threads) per (batch row b, head h, tile of TV value rows).
+// One CTA (128 threads; 256 for verify tiles of 64 or 128 rows) per (batch
+// row b, head h, tile of TV value rows).
 //   1. All threads read state_indices[b]; an inactive row writes zero output
 //      and touches nothing else ("feat(kda): add packed-input CuTe decode
 //      kernel" (PR #4417), opening paragraph).
@@ -33,14 +34,19 @@ __host__ __device__ constexpr size_t step_smem_bytes(int TV, int T) {
          + (size_t)3 * KD * 4;          // single-token reduction products
 }
 
-// T = 1 kernels are capped at 85 registers so that six 128-thread CTAs (the
-// shared-memory limit of the 128-row tile) fit on an SM.
-template <int TV, bool BULK, bool MULTI>
-__global__ void __launch_bounds__(NTHREADS, MULTI ? 1 : 6)
+// NW warps per CTA; TT token slots of the prologue (T <= TT). T = 1 kernels
+// (4 warps) are capped at 85 registers so that six 128-thread CTAs (the
+// shared-memory limit of the 128-row tile) fit on an SM; 8-warp verify
+// kernels at 128 registers, two CTAs (16 warps) per SM.
+template <int TV, bool BULK, bool MULTI, int NW, int TT>
+__global__ void __launch_bounds__(32 * NW, MULTI ? (NW == 8 ? 2 : 1) : 6)
     kda_step_kernel(const kda_params p, const int T, const int tiles) {
   static_assert(TV % 16 == 0 && TV >= 16 && TV <= KD, "tile must be a multiple of 16 rows");
-  constexpr int RW = TV / NWARPS;        // rows per warp
+  constexpr int NT = 32 * NW;             // threads
+  constexpr int RW = TV / NW;             // rows per warp
   constexpr int RQ = RW / ROWS_PER_WARP;  // 4-row groups per warp
+  static_assert(RQ >= 1 && RW % ROWS_PER_WARP == 0, "every warp owns whole 4-row groups");
+  static_assert(MULTI || NW == NWARPS, "the single-token prologue uses 128 threads");
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -70,15 +76,15 @@ __global__ void __launch_bounds__(NTHREADS, MULTI ? 1 : 6)
   const int n = p.state_indices[b];
   // Token inputs, issued alongside the index load (unused by an inactive row):
   // one token over all threads for T = 1, else up to PT tokens per warp.
-  constexpr int PT = (KDA_MAX_T + NWARPS - 1) / NWARPS;
+  constexpr int PT = (TT + NW - 1) / NW;
   TokenLoads<MULTI ? PT : 1> first;
   TokenLoads1 first1;
   if constexpr (MULTI)
-    prologue_issue(p, b, h, T, v0, TV, first);
+    prologue_issue<PT, NW>(p, b, h, T, v0, TV, first);
   else
     prologue_issue1(p, b, h, v0, TV, first1);
   if (n < 0 || n >= p.N) {
-    for (int i = tid; i < T * TV; i += NTHREADS) {
+    for (int i = tid; i < T * TV; i += NT) {
       const int t = i / TV, r = i - t * TV;
       outp[out_base + (int64_t)t * p.out_t_stride + r] = 0;
     }
@@ -101,7 +107,7 @@ __global__ void __launch_bounds__(NTHREADS, MULTI ? 1 : 6)
   }
 
   if constexpr (MULTI)
-    token_prologue(p, b, h, T, v0, TV, ts, first);
+    token_prologue<PT, NW>(p, b, h, T, v0, TV, ts, first);
   else
     token_prologue1(p, h, TV, ts, first1);
 
@@ -165,28 +171,37 @@ __global__ void __launch_bounds__(NTHREADS, MULTI ? 1 : 6)
     }
   }
   __syncthreads();
-  for (int i = tid; i < T * TV; i += NTHREADS) {
+  for (int i = tid; i < T * TV; i += NT) {
     const int t = i / TV, rr = i - t * TV;
     outp[out_base + (int64_t)t * p.out_t_stride + rr] = float_to_bf16_bits(orow[i]);
   }
 }
 
-template <int TV, bool BULK, bool MULTI>
+template <int TV, bool BULK, bool MULTI, int NW, int TT>
 static cudaError_t launch_one(const kda_params& p, int T, cudaStream_t stream) {
-  auto kern = kda_step_kernel<TV, BULK, MULTI>;
+  auto kern = kda_step_kernel<TV, BULK, MULTI, NW, TT>;
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
   cudaError_t e = set_smem_limit_once(kern, step_smem_bytes(TV, KDA_MAX_T), smem_set);
   if (e != cudaSuccess) return e;
   const int tiles = KD / TV;
   const long long blocks = (long long)p.B * p.H * tiles;
-  kern<<<(unsigned)blocks, NTHREADS, step_smem_bytes(TV, T), stream>>>(p, T, tiles);
+  kern<<<(unsigned)blocks, 32 * NW, step_smem_bytes(TV, T), stream>>>(p, T, tiles);
   return cudaGetLastError();
+}
+
+// Verify tiles of 64 or 128 rows run 8 warps (16 warps per SM at two CTAs);
+// smaller tiles keep 4.
+template <int TV, bool BULK>
+static cudaError_t launch_verify(const kda_params& p, int T, cudaStream_t s) {
+  constexpr int NW = TV >= 64 ? 8 : 4;
+  return T <= 8 ? launch_one<TV, BULK, true, NW, 8>(p, T, s) : launch_one<TV, BULK, true, NW, 16>(p, T, s);
 }
 
 template <int TV>
 static cudaError_t launch_tv(const kda_params& p, int T, bool bulk, cudaStream_t s) {
-  if (T == 1) return bulk ? launch_one<TV, true, false>(p, T, s) : launch_one<TV, false, false>(p, T, s);
-  return bulk ? launch_one<TV, true, true>(p, T, s) : launch_one<TV, false, true>(p, T, s);
+  if (T == 1)
+    return bulk ? launch_one<TV, true, false, NWARPS, 1>(p, T, s) : launch_one<TV, false, false, NWARPS, 1>(p, T, s);
+  return bulk ? launch_verify<TV, true>(p, T, s) : launch_verify<TV, false>(p, T, s);
 }
 
 cudaError_t launch_step(const kda_params& p, int T, int tile_v, bool bulk, cudaStream_t s) {
