@@ -28,6 +28,7 @@ from .kda_oracle import (  # noqa: F401
     ring_fold_closed_form,
     kda_verify_ring,
     RING_ERR_HIST_LEN,
+    RING_ERR_CACHE_BASE,
     L2_EPS,
     GATE_RAW,
     GATE_PRECOMPUTED,

@@ -51,6 +51,7 @@ L2_EPS = 1e-6
 # Bit set in the ring call's error word when a slot's hist_len lies outside
 # [0, W]. The slot is then treated as inactive.
 RING_ERR_HIST_LEN = 1
+RING_ERR_CACHE_BASE = 4
 
 # bf16: 8 significant bits (7 stored), exponent range of fp32.
 _BF16_SIG_BITS = 8
@@ -253,15 +254,23 @@ def ring_fold_closed_form(S0, k_hist, u_hist, G_hist):
 
 def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
                     k_cache, u_cache, g_cache, hist_len, flush_min,
-                    restart_hist_on_flush=True, lower_bound=-5.0, scale=1.0, gate_mode=GATE_RAW):
+                    restart_hist_on_flush=True, lower_bound=-5.0, scale=1.0, gate_mode=GATE_RAW,
+                    cache_base=None):
     """Ring-cache verify with replay and fold ([ring] "What it does", "API", "Caching").
 
     state (checkpoint): [N, H, V, K]; k_cache: [N, H, W, K] bf16 k_hat;
     u_cache: [N, H, W, V] bf16 u; g_cache: [N, H, W, K] fp32 cumulative
-    log-decay; hist_len: [N] live entries per slot. Token inputs as kda_verify.
+    log-decay; hist_len: [N] live entries per slot; cache_base: [N] ring start
+    per slot (None: 0). Token inputs as kda_verify.
+
+    Ring position P of slot n is the stored entry (cache_base[n] + P) mod W: the
+    ring page names a cache_base argument and says nothing more about it, and
+    a per-slot start of a circular ring is the plainest reading. cache_base is
+    read, never written.
 
     Per active row (slot n, history length h):
-      * h outside [0, W]: the slot is inactive and RING_ERR_HIST_LEN is set.
+      * h outside [0, W]: the slot is inactive and RING_ERR_HIST_LEN is set;
+        cache_base outside [0, W): likewise with RING_ERR_CACHE_BASE.
       * the current state is the checkpoint replayed through the h entries;
       * if h >= flush_min it is folded first: the checkpoint becomes its bf16
         rounding, the new tokens start at ring position 0 with G restarting
@@ -285,6 +294,8 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
     u_cache = np.asarray(u_cache, dtype=np.float64)
     g_cache = np.asarray(g_cache, dtype=np.float64)
     hist_len = np.asarray(hist_len, dtype=np.int64)
+    cache_base = (np.zeros(k_cache.shape[0], dtype=np.int64) if cache_base is None
+                  else np.asarray(cache_base, dtype=np.int64))
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
@@ -309,10 +320,15 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
         if h < 0 or h > W:
             new["error_word"] |= RING_ERR_HIST_LEN
             continue
+        cb = int(cache_base[n])
+        if cb < 0 or cb >= W:
+            new["error_word"] |= RING_ERR_CACHE_BASE
+            continue
+        live = [(cb + j) % W for j in range(h)]  # stored entries of positions 0 .. h-1
         q_hat, k_hat, g, _, beta = prologue(q[b], k[b], g_raw[b], beta_logit[b],
                                             A_log, dt_bias, lower_bound, gate_mode)
         S0 = np.swapaxes(state[n], -1, -2)  # [H, K, V]
-        S = ring_replay(S0, k_cache[n, :, :h], u_cache[n, :, :h], g_cache[n, :, :h])
+        S = ring_replay(S0, k_cache[n][:, live], u_cache[n][:, live], g_cache[n][:, live])
         if h >= flush_min:
             S = round_to_bf16(S)
             new["state"][n] = np.swapaxes(S, -1, -2)
@@ -322,9 +338,9 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
             G_prev = np.zeros((H, S.shape[-2]), dtype=np.float64)
         else:
             base = h
-            G_prev = g_cache[n, :, h - 1] if h > 0 else np.zeros((H, S.shape[-2]))
+            G_prev = g_cache[n, :, live[-1]] if h > 0 else np.zeros((H, S.shape[-2]))
         for t in range(T):
-            P = base + t
+            P = (cb + base + t) % W  # stored entry of ring position base + t
             G_P = round_to_fp32(G_prev + g[t])
             D = np.exp(G_P - G_prev)
             k_t = round_to_bf16(k_hat[t])

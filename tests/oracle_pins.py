@@ -407,11 +407,11 @@ def m_free_unit_keys(rng, shape):
     return bits.view(np.float32).astype(np.float64)
 
 
-def _ring(m, p, idx, flush_min, restart=True, scale=1.0):
+def _ring(m, p, idx, flush_min, restart=True, scale=1.0, cache_base=None):
     return m.kda_verify_ring(p["state"], idx, p["q"], p["k"], p["v"], p["g_raw"], p["beta_logit"],
                              p["A_log"], p["dt_bias"], p["k_cache"], p["u_cache"], p["g_cache"],
                              p["hist_len"], flush_min, restart_hist_on_flush=restart,
-                             lower_bound=LB, scale=scale)
+                             lower_bound=LB, scale=scale, cache_base=cache_base)
 
 
 def pin_ring_replay_closed_form(m):
@@ -562,6 +562,44 @@ def pin_ring_single_token_is_decode_with_stored_values(m):
     assert np.array_equal(r["out"][0, 0], o)
     assert np.array_equal(r["u_cache"][0, :, 0], u)
     assert np.array_equal(r["g_cache"][0, :, 0], G0)
+
+
+def pin_ring_cache_base_is_a_rotation(m):
+    """A ring stored from entry cache_base on (circularly) computes what the same ring stored from
+    entry 0 computes: same outputs, checkpoint and hist_len, and the written ring rotated alike.
+    Slots fold and not, and some live histories and appended tokens wrap past the last entry."""
+    rng = np.random.default_rng(19)
+    W, T, fm = 8, 3, 5
+    p = ring_problem(rng, B=4, N=5, T=T, W=W, hist=[2, 6, 4, 0, 5])
+    idx = np.array([0, 1, 2, 4])
+    cb = np.array([7, 5, 3, 1, 6])
+    r0 = _ring(m, p, idx, flush_min=fm)
+    q = dict(p)
+    for key in ("k_cache", "u_cache", "g_cache"):
+        q[key] = np.stack([np.roll(p[key][n], cb[n], axis=1) for n in range(5)])
+    r1 = _ring(m, q, idx, flush_min=fm, cache_base=cb)
+    for key in ("out", "state", "hist_len"):
+        assert np.array_equal(r1[key], r0[key]), key
+    for key in ("k_cache", "u_cache", "g_cache"):
+        back = np.stack([np.roll(r1[key][n], -cb[n], axis=1) for n in range(5)])
+        assert np.array_equal(back, r0[key], equal_nan=True), key
+    assert r1["error_word"] == 0
+    # the wrap is exercised: slot 1 (cb 5, six live entries) stores positions 0..2 at entries 5..7
+    # and positions 3..5 at entries 0..2
+    assert np.array_equal(r1["k_cache"][1][:, 0], p["k_cache"][1][:, 3])
+
+
+def pin_ring_bad_cache_base(m):
+    """cache_base outside [0, W) skips the slot (zero output, nothing touched) and sets its error bit."""
+    rng = np.random.default_rng(20)
+    p = ring_problem(rng, B=2, N=3, T=2, W=8, hist=[3, 2, 1])
+    r = _ring(m, p, np.array([0, 1]), flush_min=5, cache_base=np.array([8, -1, 0]))
+    assert (r["out"] == 0).all()
+    for key in ("state", "k_cache", "u_cache", "g_cache", "hist_len"):
+        assert np.array_equal(r[key], np.asarray(p[key], dtype=r[key].dtype), equal_nan=True), key
+    assert r["error_word"] == m.RING_ERR_CACHE_BASE
+    r = _ring(m, p, np.array([2, -1]), flush_min=5, cache_base=np.array([8, -1, 7]))
+    assert r["error_word"] == 0
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

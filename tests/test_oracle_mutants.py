@@ -14,6 +14,10 @@ import oracle
 import oracle_pins
 
 MUTATIONS = [
+    ("cache_base ignored on writes", "P = (cb + base + t) % W", "P = (base + t) % W"),
+    ("cache_base ignored on reads", "live = [(cb + j) % W for j in range(h)]", "live = [j for j in range(h)]"),
+    ("cache_base subtracted", "live = [(cb + j) % W for j in range(h)]", "live = [(j - cb) % W for j in range(h)]"),
+    ("cache_base not validated", "if cb < 0 or cb >= W:", "if cb < 0 or cb > W:"),
     ("l2 eps dropped", "keepdims=True) + L2_EPS)", "keepdims=True))"),
     ("l2 without sqrt", "return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + L2_EPS)",
      "return x / (np.sum(x * x, axis=-1, keepdims=True) + L2_EPS)"),
@@ -50,8 +54,8 @@ MUTATIONS = [
     ("G kept in fp64", "G_P = round_to_fp32(G_prev + g[t])", "G_P = G_prev + g[t]"),
     ("ring key not rounded", "k_t = round_to_bf16(k_hat[t])", "k_t = k_hat[t]"),
     ("ring u not rounded", "u_t = round_to_bf16(u)", "u_t = u"),
-    ("ring position off by one", "P = base + t\n", "P = base + t + 1\n"),
-    ("G restarts without fold", "G_prev = g_cache[n, :, h - 1] if h > 0",
+    ("ring position off by one", "P = (cb + base + t) % W", "P = (cb + base + t + 1) % W"),
+    ("G restarts without fold", "G_prev = g_cache[n, :, live[-1]] if h > 0",
      "G_prev = 0.0 * g_cache[n, :, 0] if h > 0"),
     ("hist_len kept on fold", 'new["hist_len"][n] = 0', 'new["hist_len"][n] = h'),
     ("bad hist_len accepted", "if h < 0 or h > W:", "if h < 0 or h > W + 1:"),
