@@ -68,6 +68,7 @@ typedef enum {
 /* Bits a kernel ORs into the optional device error word (kda_params.error_word). */
 #define KDA_ERR_HIST_LEN 1u /* a ring slot's hist_len was outside [0, W]; that slot was skipped */
 #define KDA_ERR_TIMEOUT 2u  /* a bounded wait for an async copy gave up; that tile was skipped */
+#define KDA_ERR_CACHE_BASE 4u /* a ring slot's cache_base was outside [0, W); that slot was skipped */
 
 /* kda_params.gate_mode: how g_raw and beta_logit are read (source: PR #4417, "T=1 fast path
    inside recurrent_kda", which covers both recurrent_kda calling conventions). */
@@ -148,6 +149,8 @@ typedef struct {
   int32_t W;         /* ring width (entries per slot and head), 1..64; the pages use 16 and 32 */
   int32_t flush_min; /* fold when hist_len >= flush_min; needs flush_min >= 1 and flush_min-1+T <= W */
   int32_t restart_hist_on_flush; /* nonzero: a fold writes hist_len = 0 */
+  const int32_t* cache_base; /* optional int32 [N]: ring position P of slot n is entry (cache_base[n] + P) mod W;
+                                NULL means 0 for every slot. Read, never written. */
 } kda_ring_params;
 
 /*
@@ -155,7 +158,11 @@ typedef struct {
  * "API", "Caching"). For each active row b, slot n = state_indices[b],
  * h = hist_len[n]:
  *   - h outside [0, W]: KDA_ERR_HIST_LEN is ORed into p->error_word and the
- *     row is skipped (zero output, nothing touched);
+ *     row is skipped (zero output, nothing touched); likewise a cache_base
+ *     outside [0, W) with KDA_ERR_CACHE_BASE;
+ *   - ring positions are circular from cache_base[n] (the page names this
+ *     argument without defining it; a per-slot ring start is its plainest
+ *     reading): position P is stored at entry (cache_base[n] + P) mod W;
  *   - the current state is the checkpoint p->state[n] replayed through ring
  *     entries j < h: S <- diag(exp(G_j - G_{j-1})) S + k_j u_j^T, G_{-1} = 0;
  *   - if h >= flush_min the state is folded first: the checkpoint becomes

@@ -190,6 +190,8 @@ kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params
     if (!aligned(r->k_cache, 16) || !aligned(r->u_cache, 16) || !aligned(r->g_cache, 16))
       return fail(KDA_EINVAL, "k_cache, u_cache and g_cache must be 16-byte aligned");
     if (!aligned(r->hist_len, 4)) return fail(KDA_EINVAL, "hist_len is not 4-byte aligned");
+    if (r->cache_base != nullptr && !aligned(r->cache_base, 4))
+      return fail(KDA_EINVAL, "cache_base is not 4-byte aligned");
     const int64_t ring = (int64_t)p->H * r->W * 128;
     if (p->N > 1 && (r->k_slot_stride < ring || r->u_slot_stride < ring || r->g_slot_stride < ring))
       return fail(KDA_EINVAL, "a ring slot stride is below H*W*128 = %lld", (long long)ring);

@@ -121,6 +121,13 @@ __host__ __device__ inline size_t ring_smem_bytes(int TT, int W, int flush_min) 
 
 __device__ __forceinline__ float round_bf16(float x) { return bf16_bits_to_float(float_to_bf16_bits(x)); }
 
+// Element offset (a multiple of 128) of ring position pos of a slot whose ring
+// starts at entry cb: the entry (cb + pos) mod W, for 0 <= pos, cb < W.
+__device__ __forceinline__ int64_t ring_row(int cb, int pos, int W) {
+  const int r = cb + pos;
+  return (int64_t)(r >= W ? r - W : r) * KD;
+}
+
 // Reduce-scatter of NV (16 or 32) per-lane values over a warp: at the level
 // with lane mask m, a lane keeps the half of its current values picked by bit
 // m of its lane and sends the other half to lane ^ m, who keeps it; once a
@@ -324,6 +331,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
     pendA = true;
   }
   int hist = active ? rp.hist_len[n] : 0;
+  int cb = active && rp.cache_base != nullptr ? rp.cache_base[n] : 0;
 
   for (; it < total; it += gridDim.x) {
     const int itn = it + gridDim.x;
@@ -331,9 +339,11 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
     const int bn = has_next ? itn / p.H : 0, hn = has_next ? itn % p.H : 0;
     const int n_next = has_next ? p.state_indices[bn] : -1;
     const bool active_next = n_next >= 0 && n_next < p.N;
-    const bool valid = active && hist >= 0 && hist <= rp.W;
+    const bool hist_ok = hist >= 0 && hist <= rp.W, cb_ok = cb >= 0 && cb < rp.W;
+    const bool valid = active && hist_ok && cb_ok;
     const int64_t obase = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + tid;
-    if (active && !valid && tid == 0 && h == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_HIST_LEN);
+    if (active && !valid && tid == 0 && h == 0 && p.error_word != nullptr)
+      atomicOr(p.error_word, hist_ok ? KDA_ERR_CACHE_BASE : KDA_ERR_HIST_LEN);
 
     const bool fold = valid && hist >= rp.flush_min;
     const int base = fold ? 0 : hist;
@@ -349,23 +359,24 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
     float X[NB];
 #pragma unroll
     for (int i = 0; i < NB; ++i) X[i] = 0.0f;
-    int hist_next = 0;
+    int hist_next = 0, cb_next = 0;
     const int fks = (hist + 15) / 16;  // fold K steps
 
     if (ok) {
       // History reads, used after the per-channel work below: G_{h-1} and the
       // first 8 entries' G_j and k~_j of channel tid, u~_j of value row tid.
-      const float Gl = hist > 0 ? gc[(int64_t)(hist - 1) * KD + tid] : 0.0f;
+      const int W = rp.W;
+      const float Gl = hist > 0 ? gc[ring_row(cb, hist - 1, W) + tid] : 0.0f;
       float Gj0[8];
       uint16_t kj0[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        Gj0[e] = e < hist ? gc[(int64_t)e * KD + tid] : 0.0f;
-        kj0[e] = e < hist ? kc[(int64_t)e * KD + tid] : (uint16_t)0;
+        Gj0[e] = e < hist ? gc[ring_row(cb, e, W) + tid] : 0.0f;
+        kj0[e] = e < hist ? kc[ring_row(cb, e, W) + tid] : (uint16_t)0;
       }
       uint16_t uh[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) uh[j] = j < hist ? uc[(int64_t)j * KD + tid] : (uint16_t)0;
+      for (int j = 0; j < 16; ++j) uh[j] = j < hist ? uc[ring_row(cb, j, W) + tid] : (uint16_t)0;
 
       if constexpr (!TMA) {  // plain loads into the same swizzled layout
         for (int r = 0; r < KD; ++r)
@@ -466,7 +477,10 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       }
 
       // hist_len of the next item (its slot index has arrived by now).
-      if (has_next && active_next) hist_next = rp.hist_len[n_next];
+      if (has_next && active_next) {
+        hist_next = rp.hist_len[n_next];
+        if (rp.cache_base != nullptr) cb_next = rp.cache_base[n_next];
+      }
 
       // u~ of row tid into shared memory: the fold's A operand for its first
       // K step of 16 entries (zero past hist) or the history buffer.
@@ -479,7 +493,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
         }
       }
       if (!fold)
-        for (int j = 16; j < hist; ++j) hu[j * KD + tid] = uc[(int64_t)j * KD + tid];
+        for (int j = 16; j < hist; ++j) hu[j * KD + tid] = uc[ring_row(cb, j, W) + tid];
 
       // History, in blocks of 8 entries: the keys exp(G_{h-1} - G_j) k~_j of
       // channel tid (zero past hist). With a fold, the first 16 go, in three
@@ -497,8 +511,8 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
             Gj[e] = Gj0[e];
             kj[e] = kj0[e];
           } else {
-            Gj[e] = in ? gc[(int64_t)(j0 + e) * KD + tid] : 0.0f;
-            kj[e] = in ? kc[(int64_t)(j0 + e) * KD + tid] : (uint16_t)0;
+            Gj[e] = in ? gc[ring_row(cb, j0 + e, W) + tid] : 0.0f;
+            kj[e] = in ? kc[ring_row(cb, j0 + e, W) + tid] : (uint16_t)0;
           }
         }
         float kw[8];
@@ -544,8 +558,8 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
 #pragma unroll
         for (int t = 0; t < TT; ++t)
           if (t < T) {
-            kc[(int64_t)(base + t) * KD + tid] = float_to_bf16_bits(kt[t]);
-            gc[(int64_t)(base + t) * KD + tid] = Gt[t];
+            kc[ring_row(cb, base + t, W) + tid] = float_to_bf16_bits(kt[t]);
+            gc[ring_row(cb, base + t, W) + tid] = Gt[t];
           }
       }
 
@@ -585,9 +599,9 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
             const int j = 16 * ks + jj;
             const bool in = j < hist;
             *reinterpret_cast<uint16_t*>(sFA + sw32_offset(128, tid, jj)) =
-                in ? uc[(int64_t)j * KD + tid] : (uint16_t)0;
-            const float kw = in ? __fmul_rn(expf(__fsub_rn(Gl, gc[(int64_t)j * KD + tid])),
-                                            bf16_bits_to_float(kc[(int64_t)j * KD + tid]))
+                in ? uc[ring_row(cb, j, W) + tid] : (uint16_t)0;
+            const float kw = in ? __fmul_rn(expf(__fsub_rn(Gl, gc[ring_row(cb, j, W) + tid])),
+                                            bf16_bits_to_float(kc[ring_row(cb, j, W) + tid]))
                                 : 0.0f;
             store_split3(sFK, fk_part, tid, jj, kw);
           }
@@ -694,6 +708,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       }
     } else if (has_next && active_next) {
       hist_next = rp.hist_len[n_next];
+      if (rp.cache_base != nullptr) cb_next = rp.cache_base[n_next];
     }
 
     // The checkpoint buffer is free: start the next item's copy and token loads.
@@ -767,7 +782,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
         const float o = __fmul_rn(p.scale, __fadd_rn(X[TT + t], acco));
         if (t < T) {
           outp[obase + (int64_t)t * p.out_t_stride] = ok ? float_to_bf16_bits(o) : (uint16_t)0;
-          if (ok) uc[(int64_t)(base + t) * KD + tid] = float_to_bf16_bits(ut[t]);
+          if (ok) uc[ring_row(cb, base + t, rp.W) + tid] = float_to_bf16_bits(ut[t]);
         }
       }
     } else {
@@ -782,6 +797,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
     n = n_next;
     active = active_next;
     hist = hist_next;
+    cb = cb_next;
   }
 
   // Anything still in flight after a wait that gave up gets one more bounded
@@ -809,7 +825,8 @@ __global__ void kda_ring_reset_kernel(const kda_params p, const kda_ring_params 
   const int n = p.state_indices[b];
   if (n < 0 || n >= p.N) return;
   const int hist = rp.hist_len[n];
-  if (hist >= rp.flush_min && hist <= rp.W) rp.hist_len[n] = 0;
+  const int cb = rp.cache_base != nullptr ? rp.cache_base[n] : 0;
+  if (hist >= rp.flush_min && hist <= rp.W && cb >= 0 && cb < rp.W) rp.hist_len[n] = 0;
 }
 
 // ---------------------------------------------------------------- host side

@@ -16,6 +16,7 @@ from . import _build
 KDA_OK, KDA_EINVAL, KDA_EUNSUPPORTED, KDA_ELAUNCH = 0, 1, 2, 3
 KDA_ERR_HIST_LEN = 1
 KDA_ERR_TIMEOUT = 2
+KDA_ERR_CACHE_BASE = 4
 KDA_MAX_T = 16
 KDA_GATE_RAW, KDA_GATE_PRECOMPUTED = 0, 1
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_EINVAL", 2: "KDA_EUNSUPPORTED", 3: "KDA_ELAUNCH"}
@@ -55,7 +56,7 @@ class KdaRingParams(ctypes.Structure):
         ("k_slot_stride", ctypes.c_int64), ("u_slot_stride", ctypes.c_int64),
         ("g_slot_stride", ctypes.c_int64),
         ("hist_len", ctypes.c_void_p), ("W", ctypes.c_int32), ("flush_min", ctypes.c_int32),
-        ("restart_hist_on_flush", ctypes.c_int32),
+        ("restart_hist_on_flush", ctypes.c_int32), ("cache_base", ctypes.c_void_p),
     ]
 
 
@@ -212,9 +213,11 @@ def kda_verify(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
 def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
                     k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush=True,
                     out=None, lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1,
-                    gate_mode=KDA_GATE_RAW, stream=None):
+                    gate_mode=KDA_GATE_RAW, stream=None, cache_base=None):
     """Ring-cache verify with replay and fold. k_cache, u_cache: bf16 [N, H, W, 128];
-    g_cache: fp32 [N, H, W, 128]; hist_len: int32 [N]. Returns out bf16 [B, T, H, 128]."""
+    g_cache: fp32 [N, H, W, 128]; hist_len: int32 [N]; cache_base: optional int32 [N]
+    (ring position P of slot n is entry (cache_base[n] + P) mod W). Returns out
+    bf16 [B, T, H, 128]."""
     B, T, H = q.shape[0], q.shape[1], q.shape[2]
     if out is None:
         out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=q.device)
@@ -230,11 +233,16 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
             raise ValueError(f"{name} must be [N, {H}, {W}, 128] with contiguous slots")
     if hist_len.shape != (state.shape[0],) or not hist_len.is_contiguous():
         raise ValueError("hist_len must be a contiguous [N] tensor")
+    if cache_base is not None:
+        _need(cache_base, "cache_base", torch.int32)
+        if cache_base.shape != (state.shape[0],) or not cache_base.is_contiguous():
+            raise ValueError("cache_base must be a contiguous [N] tensor")
     r = KdaRingParams()
     r.k_cache, r.u_cache, r.g_cache = k_cache.data_ptr(), u_cache.data_ptr(), g_cache.data_ptr()
     r.k_slot_stride, r.u_slot_stride, r.g_slot_stride = k_cache.stride(0), u_cache.stride(0), g_cache.stride(0)
     r.hist_len = hist_len.data_ptr()
     r.W, r.flush_min, r.restart_hist_on_flush = W, flush_min, int(bool(restart_hist_on_flush))
+    r.cache_base = None if cache_base is None else cache_base.data_ptr()
     _check(load_library().kda_verify_ring(ctypes.byref(p), T, ctypes.byref(r),
                                           _stream_handle(stream, q.device)))
     return out

@@ -161,11 +161,13 @@ def decode_inputs(B, N, seed=0, T=None, layout="separate", inactive_frac=0.0, H=
 
 
 def ring_inputs(B, N, T, W=32, flush_min=9, fold_frac=0.0, seed=0, H=H_DEFAULT, layout="separate",
-                inactive_frac=0.0, sentinels=True, gate_mode=0):
+                inactive_frac=0.0, sentinels=True, gate_mode=0, circular=False):
     """Inputs of kda_verify_ring. Active rows fold with probability given by
     fold_frac (exactly round(fold_frac * active) of them): their hist_len is
     drawn from [flush_min, flush_min + T - 1], the others' from [0, flush_min - 1].
-    Ring positions at or past hist_len hold NaN, so a stray read shows up."""
+    Ring positions at or past hist_len hold NaN, so a stray read shows up.
+    circular: every slot gets a random ring start cache_base in [0, W), and its
+    ring is stored rotated by it (position P at entry (cache_base + P) mod W)."""
     w = decode_inputs(B, N, seed=seed, T=T, layout=layout, inactive_frac=inactive_frac, H=H, gate_mode=gate_mode)
     g = _gen(seed + 7919)
     x = torch.randn((N, H, W, D), generator=g, dtype=torch.float64)
@@ -190,6 +192,13 @@ def ring_inputs(B, N, T, W=32, flush_min=9, fold_frac=0.0, seed=0, H=H_DEFAULT, 
         k_cache = k_cache.masked_fill(dead, float("nan"))
         u_cache = u_cache.masked_fill(dead, float("nan"))
         g_cache = g_cache.masked_fill(dead, float("nan"))
+    cache_base = None
+    if circular:
+        cache_base = torch.randint(0, W, (N,), generator=g, dtype=torch.int32)
+        shifts = [int(c) for c in cache_base]
+        k_cache = torch.stack([torch.roll(k_cache[n], shifts[n], dims=1) for n in range(N)])
+        u_cache = torch.stack([torch.roll(u_cache[n], shifts[n], dims=1) for n in range(N)])
+        g_cache = torch.stack([torch.roll(g_cache[n], shifts[n], dims=1) for n in range(N)])
     w.ring = dict(k_cache=k_cache, u_cache=u_cache, g_cache=g_cache, hist_len=hist, W=W,
-                  flush_min=flush_min)
+                  flush_min=flush_min, cache_base=cache_base)
     return w

@@ -102,7 +102,8 @@ def oracle_ring(w, restart=True, scale=1.0, lower_bound=-5.0):
                                   f64(w.g_raw), f64(w.beta_logit), f64(w.A_log), f64(w.dt_bias),
                                   f64(r["k_cache"]), f64(r["u_cache"]), f64(r["g_cache"]),
                                   f64(r["hist_len"]), r["flush_min"], restart_hist_on_flush=restart,
-                                  lower_bound=lower_bound, scale=scale, gate_mode=w.gate_mode)
+                                  lower_bound=lower_bound, scale=scale, gate_mode=w.gate_mode,
+                                  cache_base=None if r.get("cache_base") is None else f64(r["cache_base"]))
 
 
 def gpu_decode(wd, **kw):
@@ -123,6 +124,8 @@ def gpu_ring(wd, restart=True, **kw):
     from linear_attention_ssm_step_gb300 import kda
     r = wd.ring
     kw.setdefault("gate_mode", wd.gate_mode)
+    if r.get("cache_base") is not None:
+        kw.setdefault("cache_base", r["cache_base"])
     return kda.kda_verify_ring(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
                                wd.A_log, wd.dt_bias, r["k_cache"], r["u_cache"], r["g_cache"],
                                r["hist_len"], r["flush_min"], restart_hist_on_flush=restart, **kw)

@@ -44,6 +44,15 @@ def test_every_declared_function_is_exported(lib):
     assert set(names) == set(kda.EXPORTS), "binding and header disagree"
 
 
+def test_header_constants_match_binding():
+    text = open(HEADER).read()
+    for name in ("KDA_ERR_HIST_LEN", "KDA_ERR_TIMEOUT", "KDA_ERR_CACHE_BASE", "KDA_GATE_RAW",
+                 "KDA_GATE_PRECOMPUTED", "KDA_MAX_T"):
+        m = re.search(r"#define\s+" + name + r"\s+(\d+)u?", text)
+        assert m, name
+        assert int(m.group(1)) == getattr(kda, name), name
+
+
 def test_struct_layout_matches_header(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text(r"""
@@ -58,7 +67,7 @@ int main(void) {
   P(kda_params, state); P(kda_params, state_indices); P(kda_params, out); P(kda_params, out_h_stride);
   P(kda_params, error_word); P(kda_params, config_override); P(kda_params, gate_mode);
   P(kda_ring_params, g_slot_stride); P(kda_ring_params, hist_len); P(kda_ring_params, W);
-  P(kda_ring_params, restart_hist_on_flush);
+  P(kda_ring_params, restart_hist_on_flush); P(kda_ring_params, cache_base);
   return 0;
 }
 """)
@@ -182,6 +191,7 @@ def ring(W=32, flush_min=9, N=8, H=12):
     (8, lambda r: setattr(r, "k_cache", None), kda.KDA_EINVAL, "NULL"),
     (8, lambda r: setattr(r, "g_cache", (1 << 36) + 8), kda.KDA_EINVAL, "16-byte"),
     (8, lambda r: setattr(r, "u_slot_stride", 12), kda.KDA_EINVAL, "stride"),
+    (8, lambda r: setattr(r, "cache_base", (1 << 36) + 2), kda.KDA_EINVAL, "cache_base"),
 ])
 def test_ring_rejects(lib, T, mut, expect, msg):
     p = fake_params()

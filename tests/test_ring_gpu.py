@@ -39,9 +39,13 @@ def check_ring(w, dev, rows=None, restart=True, **kw):
     got_out = f64(out) if rows is None else f64(out)[rows]
     idx = sub.state_indices.numpy().astype(np.int64)
     hist0 = w.ring["hist_len"].numpy()
+    W = w.ring["W"]
+    cb0 = (np.zeros(w.N, dtype=np.int64) if w.ring.get("cache_base") is None
+           else w.ring["cache_base"].numpy().astype(np.int64))
     active = (idx >= 0) & (idx < w.N)
     valid = active.copy()
-    valid[active] = (hist0[idx[active]] >= 0) & (hist0[idx[active]] <= w.ring["W"])
+    valid[active] = ((hist0[idx[active]] >= 0) & (hist0[idx[active]] <= W)
+                     & (cb0[idx[active]] >= 0) & (cb0[idx[active]] < W))
     assert (got_out[~valid] == 0).all()
     assert_output_close(got_out, ref["out"])
     for n in idx[active & ~valid]:  # skipped for an invalid history: nothing touched
@@ -59,7 +63,7 @@ def check_ring(w, dev, rows=None, restart=True, **kw):
     kc, uc, gc = f64(wd.ring["k_cache"]), f64(wd.ring["u_cache"]), f64(wd.ring["g_cache"])
     for n in slots:
         base = 0 if hist0[n] >= w.ring["flush_min"] else hist0[n]
-        new = slice(base, base + T)
+        new = [(cb0[n] + base + t) % W for t in range(T)]  # stored entries of the new positions
         assert float(ring_ulps(kc[n][:, new], ref["k_cache"][n][:, new]).max()) <= 1.0
         # u~ of token t depends on rounded values computed before it (the folded
         # checkpoint, the u~ of earlier tokens): the multi-step bound applies
@@ -67,7 +71,7 @@ def check_ring(w, dev, rows=None, restart=True, **kw):
         G, Gr = gc[n][:, new], ref["g_cache"][n][:, new]
         assert np.all(np.abs(G - Gr) <= 1e-5 * (1.0 + np.abs(Gr))), "G differs"
         # everything else in the ring is untouched, NaN sentinels included
-        keep = np.ones(w.ring["W"], dtype=bool)
+        keep = np.ones(W, dtype=bool)
         keep[new] = False
         for name, got in (("k_cache", kc), ("u_cache", uc), ("g_cache", gc)):
             assert np.array_equal(got[n][:, keep], f64(w.ring[name])[n][:, keep], equal_nan=True), name
@@ -117,6 +121,48 @@ def test_ring_other_widths_and_token_counts(dev, T, W, flush_min):
     flush_min - 1 + T entries."""
     w = workloads.ring_inputs(6, 16, T=T, W=W, flush_min=flush_min, fold_frac=0.5, seed=40 + T + W)
     check_ring(w, dev)
+
+
+@pytest.mark.parametrize("fold", [0.0, 0.5, 1.0])
+def test_ring_circular_cache_base(dev, fold):
+    """Rings stored from a random entry per slot (cache_base), histories and
+    appends wrapping past the last entry."""
+    w = workloads.ring_inputs(12, 20, T=8, W=32, flush_min=9, fold_frac=fold, seed=60, circular=True)
+    assert w.ring["cache_base"] is not None
+    check_ring(w, dev)
+
+
+def test_ring_circular_matches_rotated_plain_ring(dev):
+    """A circular ring computes what the same ring stored from entry 0 computes, bit for bit."""
+    w = workloads.ring_inputs(6, 12, T=8, W=32, flush_min=9, fold_frac=0.5, seed=61, circular=True)
+    a = w.to(dev)
+    b = w.to(dev)
+    cb = [int(c) for c in w.ring["cache_base"]]
+    for name in ("k_cache", "u_cache", "g_cache"):
+        b.ring[name] = torch.stack([torch.roll(b.ring[name][n], -cb[n], dims=1) for n in range(12)]).contiguous()
+    b.ring["cache_base"] = None
+    oa, ob = gpu_ring(a), gpu_ring(b)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+    assert torch.equal(a.ring["hist_len"], b.ring["hist_len"])
+    for name in ("k_cache", "u_cache", "g_cache"):
+        back = torch.stack([torch.roll(a.ring[name][n], -cb[n], dims=1) for n in range(12)])
+        x, y = back, b.ring[name]
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32)), name
+
+
+def test_ring_invalid_cache_base_sets_error_and_touches_nothing(dev):
+    w = workloads.ring_inputs(4, 8, T=8, W=32, flush_min=9, fold_frac=0.5, seed=62, circular=True)
+    idx = w.state_indices.long()
+    w.ring["cache_base"][idx[0]] = 32
+    w.ring["cache_base"][idx[1]] = -1
+    wd, out, ref = check_ring(w, dev)
+    assert ref["error_word"] == kda.KDA_ERR_CACHE_BASE
+    for b in (0, 1):
+        n = int(idx[b])
+        assert (out[b].float() == 0).all()
 
 
 def test_ring_misaligned_pool_uses_plain_copies_with_same_bits(dev):
