@@ -123,7 +123,9 @@ __device__ __forceinline__ float round_bf16(float x) { return bf16_bits_to_float
 
 // Element offset (a multiple of 128) of ring position pos of a slot whose ring
 // starts at entry cb: the entry (cb + pos) mod W, for 0 <= pos, cb < W.
+template <bool CIRC>
 __device__ __forceinline__ int64_t ring_row(int cb, int pos, int W) {
+  if (!CIRC) return (int64_t)pos * KD;
   const int r = cb + pos;
   return (int64_t)(r >= W ? r - W : r) * KD;
 }
@@ -265,7 +267,7 @@ struct RingGate {
 // i+1's checkpoint and its token loads are issued, and land while item i runs
 // its recurrence and item i+1 starts. Padded token slots (t >= T) carry
 // zero inputs through the same arithmetic, so no loop branches on T.
-template <bool TMA, int TT>
+template <bool TMA, int TT, bool CIRC>
 __global__ void __launch_bounds__(RING_THREADS, 3)
     kda_ring_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p, const kda_ring_params rp,
                     const int T) {
@@ -331,7 +333,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
     pendA = true;
   }
   int hist = active ? rp.hist_len[n] : 0;
-  int cb = active && rp.cache_base != nullptr ? rp.cache_base[n] : 0;
+  int cb = CIRC && active ? rp.cache_base[n] : 0;  // ring start (0 without cache_base)
 
   for (; it < total; it += gridDim.x) {
     const int itn = it + gridDim.x;
@@ -366,17 +368,17 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       // History reads, used after the per-channel work below: G_{h-1} and the
       // first 8 entries' G_j and k~_j of channel tid, u~_j of value row tid.
       const int W = rp.W;
-      const float Gl = hist > 0 ? gc[ring_row(cb, hist - 1, W) + tid] : 0.0f;
+      const float Gl = hist > 0 ? gc[ring_row<CIRC>(cb, hist - 1, W) + tid] : 0.0f;
       float Gj0[8];
       uint16_t kj0[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        Gj0[e] = e < hist ? gc[ring_row(cb, e, W) + tid] : 0.0f;
-        kj0[e] = e < hist ? kc[ring_row(cb, e, W) + tid] : (uint16_t)0;
+        Gj0[e] = e < hist ? gc[ring_row<CIRC>(cb, e, W) + tid] : 0.0f;
+        kj0[e] = e < hist ? kc[ring_row<CIRC>(cb, e, W) + tid] : (uint16_t)0;
       }
       uint16_t uh[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) uh[j] = j < hist ? uc[ring_row(cb, j, W) + tid] : (uint16_t)0;
+      for (int j = 0; j < 16; ++j) uh[j] = j < hist ? uc[ring_row<CIRC>(cb, j, W) + tid] : (uint16_t)0;
 
       if constexpr (!TMA) {  // plain loads into the same swizzled layout
         for (int r = 0; r < KD; ++r)
@@ -479,7 +481,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       // hist_len of the next item (its slot index has arrived by now).
       if (has_next && active_next) {
         hist_next = rp.hist_len[n_next];
-        if (rp.cache_base != nullptr) cb_next = rp.cache_base[n_next];
+        if (CIRC) cb_next = rp.cache_base[n_next];
       }
 
       // u~ of row tid into shared memory: the fold's A operand for its first
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
         }
       }
       if (!fold)
-        for (int j = 16; j < hist; ++j) hu[j * KD + tid] = uc[ring_row(cb, j, W) + tid];
+        for (int j = 16; j < hist; ++j) hu[j * KD + tid] = uc[ring_row<CIRC>(cb, j, W) + tid];
 
       // History, in blocks of 8 entries: the keys exp(G_{h-1} - G_j) k~_j of
       // channel tid (zero past hist). With a fold, the first 16 go, in three
@@ -511,8 +513,8 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
             Gj[e] = Gj0[e];
             kj[e] = kj0[e];
           } else {
-            Gj[e] = in ? gc[ring_row(cb, j0 + e, W) + tid] : 0.0f;
-            kj[e] = in ? kc[ring_row(cb, j0 + e, W) + tid] : (uint16_t)0;
+            Gj[e] = in ? gc[ring_row<CIRC>(cb, j0 + e, W) + tid] : 0.0f;
+            kj[e] = in ? kc[ring_row<CIRC>(cb, j0 + e, W) + tid] : (uint16_t)0;
           }
         }
         float kw[8];
@@ -558,8 +560,8 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
 #pragma unroll
         for (int t = 0; t < TT; ++t)
           if (t < T) {
-            kc[ring_row(cb, base + t, W) + tid] = float_to_bf16_bits(kt[t]);
-            gc[ring_row(cb, base + t, W) + tid] = Gt[t];
+            kc[ring_row<CIRC>(cb, base + t, W) + tid] = float_to_bf16_bits(kt[t]);
+            gc[ring_row<CIRC>(cb, base + t, W) + tid] = Gt[t];
           }
       }
 
@@ -599,9 +601,9 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
             const int j = 16 * ks + jj;
             const bool in = j < hist;
             *reinterpret_cast<uint16_t*>(sFA + sw32_offset(128, tid, jj)) =
-                in ? uc[ring_row(cb, j, W) + tid] : (uint16_t)0;
-            const float kw = in ? __fmul_rn(expf(__fsub_rn(Gl, gc[ring_row(cb, j, W) + tid])),
-                                            bf16_bits_to_float(kc[ring_row(cb, j, W) + tid]))
+                in ? uc[ring_row<CIRC>(cb, j, W) + tid] : (uint16_t)0;
+            const float kw = in ? __fmul_rn(expf(__fsub_rn(Gl, gc[ring_row<CIRC>(cb, j, W) + tid])),
+                                            bf16_bits_to_float(kc[ring_row<CIRC>(cb, j, W) + tid]))
                                 : 0.0f;
             store_split3(sFK, fk_part, tid, jj, kw);
           }
@@ -708,7 +710,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       }
     } else if (has_next && active_next) {
       hist_next = rp.hist_len[n_next];
-      if (rp.cache_base != nullptr) cb_next = rp.cache_base[n_next];
+      if (CIRC) cb_next = rp.cache_base[n_next];
     }
 
     // The checkpoint buffer is free: start the next item's copy and token loads.
@@ -782,7 +784,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
         const float o = __fmul_rn(p.scale, __fadd_rn(X[TT + t], acco));
         if (t < T) {
           outp[obase + (int64_t)t * p.out_t_stride] = ok ? float_to_bf16_bits(o) : (uint16_t)0;
-          if (ok) uc[ring_row(cb, base + t, rp.W) + tid] = float_to_bf16_bits(ut[t]);
+          if (ok) uc[ring_row<CIRC>(cb, base + t, rp.W) + tid] = float_to_bf16_bits(ut[t]);
         }
       }
     } else {
@@ -884,10 +886,10 @@ static cudaError_t state_tensor_map(const kda_params& p, CUtensorMap* out) {
   return cudaSuccess;
 }
 
-template <bool TMA, int TT>
+template <bool TMA, int TT, bool CIRC>
 static cudaError_t launch_ring_one(const CUtensorMap& map, const kda_params& p, int T, const kda_ring_params& r,
                                    cudaStream_t s) {
-  auto kern = kda_ring_kernel<TMA, TT>;
+  auto kern = kda_ring_kernel<TMA, TT, CIRC>;
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
   cudaError_t e = set_smem_limit_once(kern, ring_smem_bytes(TT, 64, 64), smem_set);
   if (e != cudaSuccess) return e;
@@ -930,7 +932,9 @@ static cudaError_t launch_ring_one(const CUtensorMap& map, const kda_params& p, 
 template <bool TMA>
 static cudaError_t launch_ring_tma(const CUtensorMap& map, const kda_params& p, int T, const kda_ring_params& r,
                                    cudaStream_t s) {
-  return T <= 8 ? launch_ring_one<TMA, 8>(map, p, T, r, s) : launch_ring_one<TMA, 16>(map, p, T, r, s);
+  if (r.cache_base != nullptr)
+    return T <= 8 ? launch_ring_one<TMA, 8, true>(map, p, T, r, s) : launch_ring_one<TMA, 16, true>(map, p, T, r, s);
+  return T <= 8 ? launch_ring_one<TMA, 8, false>(map, p, T, r, s) : launch_ring_one<TMA, 16, false>(map, p, T, r, s);
 }
 
 cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, bool bulk, cudaStream_t s) {
