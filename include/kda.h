@@ -44,8 +44,10 @@
  *     otherwise a plain-load variant of the same kernel runs (same results,
  *     bit for bit). Neither case is an error.
  *   - `out` must not overlap the state pool or any input.
- *   - The calls are deterministic: the same inputs give the same bits,
- *     whatever the launch configuration and across CUDA-graph replays.
+ *   - The calls are deterministic: the same inputs give the same bits across
+ *     CUDA-graph replays, and whatever the CUDA-core launch configuration
+ *     (0-3); the tensor-core verify configuration (4) sums the dot products
+ *     in another order and agrees with them to rounding.
  *   - Arithmetic is fp32 with fp32 CUDA math functions; the state and the
  *     outputs are rounded to bf16 (round to nearest even) when stored.
  */
@@ -132,10 +134,13 @@ kda_status kda_decode(const kda_params* p, void* stream);
 
 /*
  * T-token speculative verify (source: PR #4864, "API": T is the draft length
- * inferred from q's shape, 8 and 4 in the pages). Equal, bit for bit, to T
- * consecutive kda_decode calls on the same slots: the state is rounded to
- * bf16 after every token, kept on chip between tokens, and written back once.
- * Writes out[b][t][h][:] for t < T. 1 <= T <= KDA_MAX_T.
+ * inferred from q's shape, 8 and 4 in the pages). Equal to T consecutive
+ * kda_decode calls on the same slots: the state is rounded to bf16 after
+ * every token, kept on chip between tokens, and written back once. The
+ * CUDA-core configurations (0-3) are equal bit for bit; configuration 4
+ * computes each token's two dot products of every state row on the tensor
+ * cores (the query vectors in three bf16 parts, fp32 accumulation) and is
+ * equal to rounding. Writes out[b][t][h][:] for t < T. 1 <= T <= KDA_MAX_T.
  */
 kda_status kda_verify(const kda_params* p, int32_t T, void* stream);
 
@@ -185,7 +190,8 @@ typedef struct {
 kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params* r, void* stream);
 
 /* Launch configurations: index -> rows of V per CTA (tile). kda_params.config_override
-   takes an index. */
+   takes an index. 0-3: CUDA-core tiles of 16, 32, 64 and 128 rows; 4: whole heads with the
+   dot products on the tensor cores, kda_verify with T > 1 only (KDA_EUNSUPPORTED otherwise). */
 int32_t kda_num_configs(void);
 int32_t kda_config_tile_v(int32_t config);
 /* The configuration kda_decode (T = 1) and kda_verify (T > 1) pick for B rows

@@ -26,8 +26,10 @@ kda_status ok() {
   return KDA_OK;
 }
 
-// Rows of V per CTA, by configuration index.
-constexpr int kTileV[] = {16, 32, 64, 128};
+// Rows of V per CTA, by configuration index. Configuration 4 runs whole heads
+// with the dot products on the tensor cores (T > 1 only).
+constexpr int kTileV[] = {16, 32, 64, 128, 128};
+constexpr int kTensorCoreConfig = 4;
 constexpr int kNumConfigs = sizeof(kTileV) / sizeof(kTileV[0]);
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -109,9 +111,8 @@ kda_status check_params(const kda_params* p, int T, bool* bulk) {
   return KDA_OK;
 }
 
-int pick_tile(const kda_params* p, int T) {
-  const int cfg = p->config_override >= 0 ? p->config_override : kda_select_config(p->B, T);
-  return kTileV[cfg];
+int pick_config(const kda_params* p, int T) {
+  return p->config_override >= 0 ? p->config_override : kda_select_config(p->B, T);
 }
 
 // The ring kernel works on whole heads: the one configuration it runs.
@@ -140,9 +141,10 @@ int32_t kda_select_config(int32_t B, int32_t T) {
     if (B <= 32) return 2;  // 64 rows
     return 3;               // 128 rows
   }
-  if (B <= 2) return 0;  // 16 rows
-  if (B <= 8) return 2;  // 64 rows, 8 warps
-  return 3;              // 128 rows, 8 warps
+  if (B <= 2) return 0;   // 16 rows
+  if (B <= 8) return 2;   // 64 rows, 8 warps
+  if (B <= 32) return 3;  // 128 rows, 8 warps
+  return 4;               // 128 rows, dot products on the tensor cores
 }
 
 // The ring kernel runs one CTA per (row, head): its state rows enter one
@@ -158,8 +160,10 @@ kda_status kda_decode(const kda_params* p, void* stream) {
   bool bulk = false;
   kda_status s = check_params(p, 1, &bulk);
   if (s != KDA_OK) return s;
+  if (p->config_override == kTensorCoreConfig)
+    return fail(KDA_EUNSUPPORTED, "config_override = %d (tensor-core verify) needs T > 1", kTensorCoreConfig);
   if (p->B == 0) return ok();
-  cudaError_t e = kda::launch_step(*p, 1, pick_tile(p, 1), bulk, static_cast<cudaStream_t>(stream));
+  cudaError_t e = kda::launch_step(*p, 1, kTileV[pick_config(p, 1)], bulk, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_decode launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -168,8 +172,13 @@ kda_status kda_verify(const kda_params* p, int32_t T, void* stream) {
   bool bulk = false;
   kda_status s = check_params(p, T, &bulk);
   if (s != KDA_OK) return s;
+  if (T == 1 && p->config_override == kTensorCoreConfig)
+    return fail(KDA_EUNSUPPORTED, "config_override = %d (tensor-core verify) needs T > 1", kTensorCoreConfig);
   if (p->B == 0) return ok();
-  cudaError_t e = kda::launch_step(*p, T, pick_tile(p, T), bulk, static_cast<cudaStream_t>(stream));
+  const int cfg = pick_config(p, T);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cfg == kTensorCoreConfig ? kda::launch_verify_tc(*p, T, bulk, st)
+                                           : kda::launch_step(*p, T, kTileV[cfg], bulk, st);
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify launch: %s", cudaGetErrorString(e));
   return ok();
 }

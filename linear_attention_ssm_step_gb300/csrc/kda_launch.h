@@ -1,6 +1,7 @@
 // kda_launch.h - internal launchers behind the C ABI (not part of the public header).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -24,6 +25,15 @@ cudaError_t set_smem_limit_once(Kernel kern, size_t bytes, std::atomic<bool>& do
 // T-token step (T = 1 is decode). tile_v in {16, 32, 64, 128}; bulk selects
 // the bulk-copy staging of the state (16-byte aligned pool) over plain loads.
 cudaError_t launch_step(const kda_params& p, int T, int tile_v, bool bulk, cudaStream_t s);
+
+// The state pool as a 3-D bf16 tensor map {128 keys, H * 128 value rows, N
+// slots}, {64, 128, 1} boxes, 128-byte swizzle (the tensor core's K-major
+// operand layout); needs a 16-byte aligned pool and slot stride.
+cudaError_t state_tensor_map(const kda_params& p, CUtensorMap* out);
+
+// T-token verify with the two dot products of every state row per token on
+// the tensor cores; one CTA per (row, head). bulk as above.
+cudaError_t launch_verify_tc(const kda_params& p, int T, bool bulk, cudaStream_t s);
 
 // Ring-cache verify with replay and fold, one CTA per (row, head). bulk
 // selects tensor-map copies of the checkpoint (16-byte aligned pool) over

@@ -135,4 +135,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&out)[16]) {
   for (int i = 0; i < 16; ++i) out[i] = __uint_as_float(r[i]);
 }
 
+// 8 consecutive fp32 columns of this thread's tensor-memory lane (as tmem_ld16).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&out)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out[i] = __uint_as_float(r[i]);
+}
+
 }  // namespace kda

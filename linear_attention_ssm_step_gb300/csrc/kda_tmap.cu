@@ -1,0 +1,65 @@
+// kda_tmap.cu - tensor maps of the state pool, for tensor-map (TMA) copies.
+// Host code: the encoder comes from the driver through the runtime's entry
+// point query, so the library links no driver library of its own.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kda_device.cuh"
+#include "kda_launch.h"
+
+namespace kda {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// The state pool as a 3-D bf16 tensor {128 keys, H * 128 value rows, N slots}
+// read and written in {64, 128, 1} boxes with the 128-byte swizzle. The last
+// map is kept per host thread, keyed by pool address and shape.
+cudaError_t state_tensor_map(const kda_params& p, CUtensorMap* out) {
+  struct Cached {
+    const void* ptr = nullptr;
+    int N = 0, H = 0;
+    int64_t stride = 0;
+    CUtensorMap map;
+  };
+  thread_local Cached cache;
+  const int64_t slot = p.N > 1 ? p.state_slot_stride : (int64_t)p.H * KD * KD;
+  if (cache.ptr == p.state && cache.N == p.N && cache.H == p.H && cache.stride == slot) {
+    *out = cache.map;
+    return cudaSuccess;
+  }
+  const EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)KD, (cuuint64_t)p.H * KD, (cuuint64_t)p.N};
+  const cuuint64_t strides[2] = {(cuuint64_t)KD * 2, (cuuint64_t)slot * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMap map;
+  const CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.state, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  cache.ptr = p.state;
+  cache.N = p.N;
+  cache.H = p.H;
+  cache.stride = slot;
+  cache.map = map;
+  *out = map;
+  return cudaSuccess;
+}
+
+}  // namespace kda

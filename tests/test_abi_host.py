@@ -165,6 +165,17 @@ def test_decode_rejects(lib, mutate, expect, msg):
 
 
 @no_gpu
+def test_tensor_core_configuration_is_verify_only(lib):
+    p = fake_params()
+    p.config_override = 4
+    assert status(lib, p) == kda.KDA_EUNSUPPORTED  # decode
+    assert "T > 1" in kda.kda_last_error()
+    assert status(lib, p, T=1) == kda.KDA_EUNSUPPORTED
+    assert status(lib, p, T=8, ring=ring()) == kda.KDA_EUNSUPPORTED  # the ring takes whole-head tiles only
+    assert kda.kda_config_tile_v(4) == 128
+
+
+@no_gpu
 def test_verify_token_range(lib):
     for T in (0, -1, 17):
         assert status(lib, fake_params(), T=T) == kda.KDA_EUNSUPPORTED

@@ -1,12 +1,17 @@
 """kda_verify (T tokens) on the GPU: against the oracle, and bit for bit
-against T chained kda_decode calls."""
+against T chained kda_decode calls (the CUDA-core configurations 0-3). The
+tensor-core configuration (4) sums the dot products in another order: it
+matches the oracle and chained decodes within the multi-step tolerances, and
+is bitwise deterministic on its own."""
 
 import numpy as np
 import pytest
 import torch
 
 from harness import assert_output_close, assert_state_close, f64, gpu_decode, gpu_verify, oracle_verify
-from linear_attention_ssm_step_gb300 import workloads
+from linear_attention_ssm_step_gb300 import kda, workloads
+
+TC = 4  # the tensor-core configuration
 
 pytestmark = pytest.mark.gpu
 
@@ -44,8 +49,90 @@ def test_verify_matches_oracle(dev, B, T):
     check_verify(w, dev)
 
 
+@pytest.mark.parametrize("T", [2, 8, 16])
+@pytest.mark.parametrize("B", [1, 5, 32])
+def test_verify_tensor_cores_match_oracle(dev, B, T):
+    if B == 32 and T == 16:
+        pytest.skip("covered by the T=8 case; keeps the oracle time short")
+    w = workloads.decode_inputs(B, B + 64, seed=310 + 17 * B + T, T=T, inactive_frac=0.2 if B == 5 else 0.0)
+    check_verify(w, dev, config_override=TC)
+
+
+def test_verify_tensor_cores_match_chained_decodes(dev):
+    T = 8
+    w = workloads.decode_inputs(7, 20, seed=408, T=T, inactive_frac=0.15, layout="packed")
+    wd = w.to(dev)
+    out_v = gpu_verify(wd, config_override=TC)
+    wc = w.to(dev)
+    outs = [gpu_decode(_token(wc, t)) for t in range(T)]
+    torch.cuda.synchronize()
+    idx = w.state_indices.numpy().astype(np.int64)
+    act = idx[(idx >= 0) & (idx < w.N)]
+    assert_state_close(f64(wd.state)[act], f64(wc.state)[act], steps=T)
+    assert_output_close(f64(out_v), f64(torch.stack(outs, dim=1)))
+
+
+def test_verify_tensor_cores_serving_batch_512_sampled(dev):
+    w = workloads.decode_inputs(512, 576, seed=3, T=8)
+    rows = np.sort(np.random.default_rng(2).choice(512, 24, replace=False))
+    check_verify(w, dev, rows=rows, config_override=TC)
+
+
+def test_verify_tensor_cores_misaligned_state_same_bits(dev):
+    w = workloads.decode_inputs(4, 6, seed=5, T=4)
+    wd = w.to(dev)
+    flat = torch.empty(6 * 12 * 128 * 128 + 8, dtype=torch.bfloat16, device=dev)
+    mis = flat[3:3 + 6 * 12 * 128 * 128].view(6, 12, 128, 128)
+    mis.copy_(wd.state)
+    out_a = gpu_verify(wd, config_override=TC)
+    wd.state = mis
+    out_b = gpu_verify(wd, config_override=TC)
+    ref = w.to(dev)
+    gpu_verify(ref, config_override=TC)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(mis.view(torch.int16), ref.state.view(torch.int16))
+
+
+def test_verify_tensor_cores_cuda_graph_bitwise(dev):
+    w = workloads.decode_inputs(6, 10, seed=6, T=8)
+    wd = w.to(dev)
+    init = wd.state.clone()
+    gpu_verify(wd, config_override=TC)
+    torch.cuda.synchronize()
+    out = torch.empty((6, 8, 12, 128), dtype=torch.bfloat16, device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gpu_verify(wd, out=out, config_override=TC)
+    res = []
+    for _ in range(3):
+        wd.state.copy_(init)
+        graph.replay()
+        torch.cuda.synchronize()
+        res.append((out.clone(), wd.state.clone()))
+    for o, s in res[1:]:
+        assert torch.equal(o.view(torch.int16), res[0][0].view(torch.int16))
+        assert torch.equal(s.view(torch.int16), res[0][1].view(torch.int16))
+
+
+def test_verify_tensor_cores_precomputed_gate_convention(dev):
+    w = workloads.decode_inputs(5, 12, seed=8, T=8, inactive_frac=0.2, gate_mode=1)
+    w.A_log = w.dt_bias = None
+    check_verify(w, dev, config_override=TC)
+
+
+def test_tensor_core_configuration_needs_several_tokens(dev):
+    w = workloads.decode_inputs(3, 6, seed=9, T=1)
+    wd = w.to(dev)
+    with pytest.raises(kda.KdaError):
+        gpu_verify(wd, config_override=TC)
+    w1 = workloads.decode_inputs(3, 6, seed=9)
+    with pytest.raises(kda.KdaError):
+        gpu_decode(w1.to(dev), config_override=TC)
+
+
 @pytest.mark.parametrize("T", [2, 8])
-@pytest.mark.parametrize("config", [None, 0, 1, 2, 3])
+@pytest.mark.parametrize("config", [0, 1, 2, 3])
 def test_verify_equals_chained_decodes_bitwise(dev, T, config):
     kw = {} if config is None else {"config_override": config}
     w = workloads.decode_inputs(7, 20, seed=400 + T, T=T, inactive_frac=0.15, layout="packed")
