@@ -221,6 +221,9 @@ struct Gate {
   float a_h, lower_bound;
   __device__ __forceinline__ Gate(const kda_params& p, int h)
       : raw(p.gate_mode == KDA_GATE_RAW), a_h(raw ? expf(p.A_log[h]) : 0.0f), lower_bound(p.lower_bound) {}
+  // The same, from A_log[h] loaded ahead of time.
+  __device__ __forceinline__ Gate(const kda_params& p, float alog, bool)
+      : raw(p.gate_mode == KDA_GATE_RAW), a_h(raw ? expf(alog) : 0.0f), lower_bound(p.lower_bound) {}
   __device__ __forceinline__ float dt_bias(const kda_params& p, int h, int c) const {
     return raw ? p.dt_bias[(int64_t)h * KD + c] : 0.0f;
   }
@@ -278,10 +281,14 @@ __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h
 // bit-identical to token_prologue's for that token.
 struct TokenLoads1 {
   float q, k, g, v, bl;
+  float alog, dtb;  // A_log[h] and dt_bias[h][c] (raw gate)
 };
 
 __device__ __forceinline__ void prologue_issue1(const kda_params& p, int b, int h, int v0, int TV, TokenLoads1& L) {
   const int c = threadIdx.x;
+  const bool raw = p.gate_mode == KDA_GATE_RAW;
+  L.alog = raw ? p.A_log[h] : 0.0f;
+  L.dtb = raw ? p.dt_bias[(int64_t)h * KD + c] : 0.0f;
   L.q = load_bf16(p.q, b, 0, h, c);
   L.k = load_bf16(p.k, b, 0, h, c);
   L.g = load_bf16(p.g_raw, b, 0, h, c);
@@ -297,8 +304,8 @@ __device__ __forceinline__ void token_prologue1(const kda_params& p, int h, int 
   ts.red[c] = __fmul_rn(L.q, L.q);
   ts.red[KD + c] = __fmul_rn(L.k, L.k);
   ts.red[2 * KD + c] = __fmul_rn(L.q, L.k);
-  const Gate gate(p, h);
-  const float g = gate.g(L.g, gate.dt_bias(p, h, c));
+  const Gate gate(p, L.alog, true);
+  const float g = gate.g(L.g, L.dtb);
   ts.gg[c] = g;
   ts.dd[c] = expf(g);
   if (c < TV) ts.vrow[c] = L.v;
