@@ -52,6 +52,31 @@ def test_decode_matches_oracle(dev, B, layout):
     run_and_check(w, dev)
 
 
+@pytest.mark.parametrize("H", [1, 3, 64])
+@pytest.mark.parametrize("config", [0, 3])
+def test_decode_other_head_counts(dev, H, config):
+    """H from 1 to the largest the boundary accepts, on the smallest and the whole-head tile."""
+    w = workloads.decode_inputs(3, 5, seed=120 + H, H=H, inactive_frac=0.0)
+    run_and_check(w, dev, config_override=config)
+
+
+def test_decode_large_batch_sampled(dev):
+    """B = 2048 (24576 CTAs of the whole-head tile); 16 rows compared with the oracle, the
+    inactive rule checked on every row."""
+    w = workloads.decode_inputs(2048, 2112, seed=121, inactive_frac=0.05)
+    wd = w.to(dev)
+    out = gpu_decode(wd)
+    torch.cuda.synchronize()
+    idx = w.state_indices.numpy().astype(np.int64)
+    active = (idx >= 0) & (idx < w.N)
+    assert (f64(out)[~active] == 0).all()
+    rows = np.sort(np.random.default_rng(5).choice(np.nonzero(active)[0], 16, replace=False))
+    sub = w.select_rows(rows)
+    ref_state, ref_out = oracle_decode(sub)
+    assert_output_close(f64(out)[rows], ref_out)
+    assert_state_close(f64(wd.state)[idx[rows]], ref_state[idx[rows]])
+
+
 @pytest.mark.parametrize("config", range(4))
 def test_every_config_gives_the_same_bits(dev, config):
     w = workloads.decode_inputs(9, 16, seed=7, layout="packed", inactive_frac=0.2)

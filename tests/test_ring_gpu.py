@@ -165,6 +165,20 @@ def test_ring_invalid_cache_base_sets_error_and_touches_nothing(dev):
         assert (out[b].float() == 0).all()
 
 
+@pytest.mark.parametrize("H", [1, 3, 64])
+def test_ring_other_head_counts(dev, H):
+    w = workloads.ring_inputs(3, 6, T=8, W=32, flush_min=9, fold_frac=0.5, seed=70 + H, H=H)
+    check_ring(w, dev)
+
+
+def test_ring_large_batch_sampled(dev):
+    """B = 2048, half the rows folding: about 54 (row, head) items per persistent CTA; 12 rows
+    compared with the oracle, the written ring and hist_len checked on those rows."""
+    w = workloads.ring_inputs(2048, 2112, T=8, W=32, flush_min=9, fold_frac=0.5, seed=71)
+    rows = np.sort(np.random.default_rng(7).choice(2048, 12, replace=False))
+    check_ring(w, dev, rows=rows)
+
+
 def test_ring_misaligned_pool_uses_plain_copies_with_same_bits(dev):
     w = workloads.ring_inputs(6, 12, T=8, W=32, flush_min=9, fold_frac=0.5, seed=14, inactive_frac=0.2)
     a, b = w.to(dev), w.to(dev)

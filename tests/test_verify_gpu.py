@@ -58,6 +58,22 @@ def test_verify_tensor_cores_match_oracle(dev, B, T):
     check_verify(w, dev, config_override=TC)
 
 
+@pytest.mark.parametrize("H", [1, 3, 64])
+@pytest.mark.parametrize("config", [3, TC])
+def test_verify_other_head_counts(dev, H, config):
+    w = workloads.decode_inputs(2, 4, seed=320 + H, T=4, H=H)
+    check_verify(w, dev, config_override=config)
+
+
+def test_verify_large_batch_sampled(dev):
+    """T = 8, B = 2048 on the default (tensor-core) configuration; 12 rows compared with the oracle."""
+    w = workloads.decode_inputs(2048, 2112, seed=321, T=8, inactive_frac=0.05)
+    idx = w.state_indices.numpy().astype(np.int64)
+    active = np.nonzero((idx >= 0) & (idx < w.N))[0]
+    rows = np.sort(np.random.default_rng(6).choice(active, 12, replace=False))
+    check_verify(w, dev, rows=rows)
+
+
 def test_verify_tensor_cores_match_chained_decodes(dev):
     T = 8
     w = workloads.decode_inputs(7, 20, seed=408, T=T, inactive_frac=0.15, layout="packed")
