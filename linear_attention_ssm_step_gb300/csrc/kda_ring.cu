@@ -66,6 +66,12 @@ namespace kda {
 constexpr int RING_THREADS = 128;
 constexpr uint32_t RING_TMEM_COLS = 128;  // the fold's 128 x 128 fp32 sums, later the 2T dot products
 
+// Per-warp tile for summing 32 values over the warp's 32 lanes: row l holds
+// lane l's values, rows 36 floats apart (16-byte aligned, and the 32 lanes'
+// column reads fall in 32 different banks).
+constexpr int XPOSE_LD = 36;
+constexpr uint32_t XPOSE_WARP_BYTES = 32u * XPOSE_LD * 4u;
+
 // Shared-memory carve-up (bytes from a 1024-aligned base) for TT token slots,
 // ring width W and fold threshold flush_min. The union region holds either
 // the fold's operands (u~ history and three parts of the history keys, K in
@@ -73,7 +79,7 @@ constexpr uint32_t RING_TMEM_COLS = 128;  // the fold's 128 x 128 fp32 sums, lat
 // coefficients and the u~ history; the B operand (query vectors) sits at its
 // start and is written after the fold's product has read its operands.
 struct RingLayout {
-  uint32_t a, u, fa, fk, b, hred, hfin, hu, red, rn, fin, fint, sdec, beta, bar, tslot, total;
+  uint32_t a, u, fa, fk, b, hred, hfin, hu, red, rn, fin, fint, sdec, beta, xpose, bar, tslot, total;
 };
 
 __host__ __device__ inline RingLayout ring_layout(int TT, int W, int flush_min) {
@@ -107,6 +113,8 @@ __host__ __device__ inline RingLayout ring_layout(int TT, int W, int flush_min) 
   o += 128u * 4u;  // fold: exp(G_{h-1})
   L.beta = o;
   o += KDA_MAX_T * 4u;
+  L.xpose = o;
+  o += 4u * XPOSE_WARP_BYTES;  // per-warp transpose tiles of the block sums
   L.bar = o;
   o += 32u;
   L.tslot = o;
@@ -158,6 +166,21 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane) {
       v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], m));
     }
   }
+}
+
+// The warp sum of each of 32 per-lane values, through a shared-memory tile:
+// lane l writes its values as row l, then sums column l over the 32 rows in
+// row order. Returns the sum of value `lane`.
+__device__ __forceinline__ float warp_sum_transpose(const float (&v)[32], float* tile, int lane) {
+  float4* row = reinterpret_cast<float4*>(tile + lane * XPOSE_LD);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) row[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  __syncwarp();
+  float sum = tile[lane];
+#pragma unroll
+  for (int r = 1; r < 32; ++r) sum = __fadd_rn(sum, tile[r * XPOSE_LD + lane]);
+  __syncwarp();  // the tile is free again
+  return sum;
 }
 
 // The block sum of value l of a 32-value chunk: its four warp partials in warp order.
@@ -298,6 +321,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
   uint64_t* barF = barA + 1;                                   // fold product
   uint64_t* barD = barA + 2;                                   // dot products
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL.tslot);
+  float* xtile = reinterpret_cast<float*>(sm + SL.xpose + warp * XPOSE_WARP_BYTES);
   constexpr uint32_t fk_part = 4096u;  // bytes between the key parts
   uint16_t* outp = static_cast<uint16_t*>(p.out);
 
@@ -474,8 +498,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
             }
           }
         }
-        reduce_scatter<32>(vals, lane);
-        red[((1 + a0 * TT / 32) * 4 + warp) * 32 + lane] = vals[0];
+        red[((1 + a0 * TT / 32) * 4 + warp) * 32 + lane] = warp_sum_transpose(vals, xtile, lane);
       }
 
       // hist_len of the next item (its slot index has arrived by now).
@@ -535,8 +558,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
                 vals[e * NB + 2 * t] = __fmul_rn(kw[e0 + e], pk[t]);
                 vals[e * NB + 2 * t + 1] = __fmul_rn(kw[e0 + e], pq[t]);
               }
-            reduce_scatter<32>(vals, lane);
-            hred[(((j0 + e0) / CPE) * 4 + warp) * 32 + lane] = vals[0];
+            hred[(((j0 + e0) / CPE) * 4 + warp) * 32 + lane] = warp_sum_transpose(vals, xtile, lane);
           }
         }
       }
