@@ -66,9 +66,10 @@ namespace kda {
 constexpr int RING_THREADS = 128;
 constexpr uint32_t RING_TMEM_COLS = 128;  // the fold's 128 x 128 fp32 sums, later the 2T dot products
 
-// Per-warp tile for summing 32 values over the warp's 32 lanes: row l holds
-// lane l's values, rows 36 floats apart (16-byte aligned, and the 32 lanes'
-// column reads fall in 32 different banks).
+// Per-warp tile for summing 32 values over the warp's 32 lanes: row i holds
+// value i of every lane, rows 36 floats apart (16-byte aligned, and each
+// group of 8 lanes reading 16 bytes of 8 different rows hits 32 different
+// banks).
 constexpr int XPOSE_LD = 36;
 constexpr uint32_t XPOSE_WARP_BYTES = 32u * XPOSE_LD * 4u;
 
@@ -79,7 +80,7 @@ constexpr uint32_t XPOSE_WARP_BYTES = 32u * XPOSE_LD * 4u;
 // coefficients and the u~ history; the B operand (query vectors) sits at its
 // start and is written after the fold's product has read its operands.
 struct RingLayout {
-  uint32_t a, u, fa, fk, b, hred, hfin, hu, red, rn, fin, fint, sdec, beta, xpose, bar, tslot, total;
+  uint32_t a, u, fa, fk, b, hred, hfin, hu, red, rn, fcp, sdec, beta, xpose, bar, tslot, total;
 };
 
 __host__ __device__ inline RingLayout ring_layout(int TT, int W, int flush_min) {
@@ -105,10 +106,8 @@ __host__ __device__ inline RingLayout ring_layout(int TT, int W, int flush_min) 
   o += (1u + (TT * TT) / 32u) * 512u;  // per-warp partial sums: norms, then coefficients
   L.rn = o;
   o += 32u * 4u;  // inverse norms
-  L.fin = o;
-  o += TT * TT * 4u;  // coefficient sums
-  L.fint = o;
-  o += TT * TT * 4u;  // the same, transposed
+  L.fcp = o;
+  o += TT * TT * 8u;  // coefficient sums, as pairs (M[a][b], M[b][a])
   L.sdec = o;
   o += 128u * 4u;  // fold: exp(G_{h-1})
   L.beta = o;
@@ -138,49 +137,62 @@ __device__ __forceinline__ int64_t ring_row(int cb, int pos, int W) {
   return (int64_t)(r >= W ? r - W : r) * KD;
 }
 
-// Reduce-scatter of NV (16 or 32) per-lane values over a warp: at the level
-// with lane mask m, a lane keeps the half of its current values picked by bit
-// m of its lane and sends the other half to lane ^ m, who keeps it; once a
-// lane holds one value, plain butterfly levels follow. Afterwards v[0] of
-// lane l holds the warp-wide sum of value l >> (5 - log2 NV). Every value is
-// summed over the same butterfly tree, so its bits do not depend on where it
-// sits.
-template <int NV>
-__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane) {
-  static_assert(NV == 16 || NV == 32, "16 or 32 values");
-  int c = NV;
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
-    if (c > 1) {
-      const bool hi = (lane & m) != 0;
-#pragma unroll
-      for (int i = 0; i < NV / 2; ++i) {
-        if (i < c / 2) {
-          const float keep = hi ? v[c / 2 + i] : v[i];
-          const float send = hi ? v[i] : v[c / 2 + i];
-          v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, m));
-        }
-      }
-      c >>= 1;
-    } else {
-      v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], m));
-    }
-  }
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
-// The warp sum of each of 32 per-lane values, through a shared-memory tile:
-// lane l writes its values as row l, then sums column l over the 32 rows in
-// row order. Returns the sum of value `lane`.
-__device__ __forceinline__ float warp_sum_transpose(const float (&v)[32], float* tile, int lane) {
-  float4* row = reinterpret_cast<float4*>(tile + lane * XPOSE_LD);
+// Warp sums of per-lane values through a per-warp shared-memory tile: lane r
+// puts its value i at row i, column r (the 32 lanes' stores of one value are
+// one contiguous row), then lane l sums row l over the 32 lanes as a fixed
+// pairwise tree on packed pairs. tile_put_* write the values; tile_row_sum
+// (after a __syncwarp) returns the sum of value `row`.
+__device__ __forceinline__ void tile_put(float* tile, int lane, int i, float x) { tile[i * XPOSE_LD + lane] = x; }
+
+__device__ __forceinline__ void tile_put2(float* tile, int lane, int i, f32x2 x) {
+  float lo, hi;
+  upk2(x, lo, hi);
+  tile[2 * i * XPOSE_LD + lane] = lo;
+  tile[(2 * i + 1) * XPOSE_LD + lane] = hi;
+}
+
+__device__ __forceinline__ float tile_row_sum(const float* tile, int row) {
+  const float4* r = reinterpret_cast<const float4*>(tile + row * XPOSE_LD);
+  f32x2 s[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) row[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  for (int q = 0; q < 8; ++q) {
+    const float4 f = r[q];
+    s[2 * q] = pk2(f.x, f.y);
+    s[2 * q + 1] = pk2(f.z, f.w);
+  }
+#pragma unroll
+  for (int w = 1; w < 16; w <<= 1)
+#pragma unroll
+    for (int m = 0; m < 16; m += 2 * w) s[m] = add2(s[m], s[m + w]);
+  float lo, hi;
+  upk2(s[0], lo, hi);
+  return __fadd_rn(lo, hi);
+}
+
+// The warp sum of value `lane` of 32 per-lane values.
+__device__ __forceinline__ float warp_sum32(const float (&v)[32], float* tile, int lane) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) tile_put(tile, lane, i, v[i]);
   __syncwarp();
-  float sum = tile[lane];
-#pragma unroll
-  for (int r = 1; r < 32; ++r) sum = __fadd_rn(sum, tile[r * XPOSE_LD + lane]);
+  const float s = tile_row_sum(tile, lane);
   __syncwarp();  // the tile is free again
-  return sum;
+  return s;
+}
+
+// The same for 32 values held as 16 packed pairs (value 2i low, 2i + 1 high).
+__device__ __forceinline__ float warp_sum32(const f32x2 (&v)[16], float* tile, int lane) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) tile_put2(tile, lane, i, v[i]);
+  __syncwarp();
+  const float s = tile_row_sum(tile, lane);
+  __syncwarp();
+  return s;
 }
 
 // The block sum of value l of a 32-value chunk: its four warp partials in warp order.
@@ -313,8 +325,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
   uint16_t* hu = reinterpret_cast<uint16_t*>(sm + SL.hu);
   float* red = reinterpret_cast<float*>(sm + SL.red);
   float* rn = reinterpret_cast<float*>(sm + SL.rn);
-  float* fin = reinterpret_cast<float*>(sm + SL.fin);    // M[a][b], see the coefficients below
-  float* fint = reinterpret_cast<float*>(sm + SL.fint);  // M transposed
+  float* fcp = reinterpret_cast<float*>(sm + SL.fcp);  // pairs (M[a][b], M[b][a]), see the coefficients below
   float* sdec = reinterpret_cast<float*>(sm + SL.sdec);
   float* sbeta = reinterpret_cast<float*>(sm + SL.beta);
   uint64_t* barA = reinterpret_cast<uint64_t*>(sm + SL.bar);  // checkpoint copy
@@ -382,9 +393,9 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
     uint16_t vcur[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) vcur[t] = L.vv[t];
-    float X[NB];
+    f32x2 X[TT];  // (S_b^T (P_t k~_t), S_b^T (P_t q_hat_t)) of row tid, per token t
 #pragma unroll
-    for (int i = 0; i < NB; ++i) X[i] = 0.0f;
+    for (int t = 0; t < TT; ++t) X[t] = pk2(0.0f, 0.0f);
     int hist_next = 0, cb_next = 0;
     const int fks = (hist + 15) / 16;  // fold K steps
 
@@ -414,15 +425,16 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       // L2 norms: block sums of q_t^2 (value t) and k_t^2 (value TT + t), then
       // one inverse norm per value.
       {
-        float vals[NB];
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
           const float q = bf16_bits_to_float(L.qv[t]), k = bf16_bits_to_float(L.kv[t]);
-          vals[t] = __fmul_rn(q, q);
-          vals[TT + t] = __fmul_rn(k, k);
+          tile_put(xtile, lane, t, __fmul_rn(q, q));
+          tile_put(xtile, lane, TT + t, __fmul_rn(k, k));
         }
-        reduce_scatter<NB>(vals, lane);
-        if (NB == 32 || (lane & 1) == 0) red[warp * 32 + (NB == 32 ? lane : lane >> 1)] = vals[0];
+        __syncwarp();
+        const float s = tile_row_sum(xtile, lane & (NB - 1));
+        __syncwarp();
+        if (lane < NB) red[warp * 32 + lane] = s;
       }
       __syncthreads();
       if (tid < NB) rn[tid] = inv_norm(block_sum(red, 0, tid));
@@ -441,7 +453,8 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       const float e_last = hist > 0 ? expf(Gl) : 1.0f;
       if (fold) sdec[tid] = e_last;
       const float dtb = L.dtb;
-      float dd[TT], Gt[TT], pk[TT], pq[TT];
+      float dd[TT], Gt[TT];
+      f32x2 pkq[TT];  // (P_t k~_t, P_t q_hat_t)
       {
         float gg[TT];
 #pragma unroll
@@ -457,15 +470,16 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
           P = __fmul_rn(P, dd[t]);
-          pk[t] = __fmul_rn(P, kt[t]);  // zero past T: k~_t is zero there
-          pq[t] = __fmul_rn(P, qh[t]);
+          pkq[t] = mul2(pk2(P, P), pk2(kt[t], qh[t]));  // zero k part past T: k~_t is zero there
         }
       }
-      if (!fold) {
+      if (!fold) {  // B rows 2t and 2t + 1: the pair of token t
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
-          store_split<NB2>(sB, sB + NB * 128, t, tid, __fmul_rn(e_last, pk[t]));
-          store_split<NB2>(sB, sB + NB * 128, TT + t, tid, __fmul_rn(e_last, pq[t]));
+          float xk, xq;
+          upk2(mul2(pk2(e_last, e_last), pkq[t]), xk, xq);
+          store_split<NB2>(sB, sB + NB * 128, 2 * t, tid, xk);
+          store_split<NB2>(sB, sB + NB * 128, 2 * t + 1, tid, xq);
         }
       }
 
@@ -498,7 +512,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
             }
           }
         }
-        red[((1 + a0 * TT / 32) * 4 + warp) * 32 + lane] = warp_sum_transpose(vals, xtile, lane);
+        red[((1 + a0 * TT / 32) * 4 + warp) * 32 + lane] = warp_sum32(vals, xtile, lane);
       }
 
       // hist_len of the next item (its slot index has arrived by now).
@@ -525,7 +539,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       // bf16 parts, into the fold's B operand (row tid, column j); otherwise
       // their products with the query vectors are summed over the block
       // (chunk j / CPE, value (j % CPE) NB + 2t with P_t k~_t, + 1 with
-      // P_t q_hat_t).
+      // P_t q_hat_t, one packed product per pair).
       for (int j0 = 0; j0 < (fold ? 16 : hist); j0 += 8) {
         float Gj[8];
         uint16_t kj[8];
@@ -550,15 +564,12 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
         } else {
 #pragma unroll
           for (int e0 = 0; e0 < 8; e0 += CPE) {
-            float vals[32];
+            f32x2 vals[16];
 #pragma unroll
             for (int e = 0; e < CPE; ++e)
 #pragma unroll
-              for (int t = 0; t < TT; ++t) {
-                vals[e * NB + 2 * t] = __fmul_rn(kw[e0 + e], pk[t]);
-                vals[e * NB + 2 * t + 1] = __fmul_rn(kw[e0 + e], pq[t]);
-              }
-            hred[(((j0 + e0) / CPE) * 4 + warp) * 32 + lane] = warp_sum_transpose(vals, xtile, lane);
+              for (int t = 0; t < TT; ++t) vals[e * TT + t] = mul2(pk2(kw[e0 + e], kw[e0 + e]), pkq[t]);
+            hred[(((j0 + e0) / CPE) * 4 + warp) * 32 + lane] = warp_sum32(vals, xtile, lane);
           }
         }
       }
@@ -599,12 +610,13 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
         pendF = true;
       }
 
-      // Block sums of the coefficients (M and its transpose) and the history
-      // coefficients, while the fold's product runs.
+      // Block sums of the coefficients (each M[a][b] goes to pair a TT + b,
+      // low, and to pair b TT + a, high) and the history coefficients, while
+      // the fold's product runs.
       for (int i = tid; i < TT * TT; i += RING_THREADS) {
         const float v = block_sum(red, 1 + (i >> 5), i & 31);
-        fin[i] = v;
-        fint[(i % TT) * TT + i / TT] = v;
+        fcp[2 * i] = v;
+        fcp[2 * ((i % TT) * TT + i / TT) + 1] = v;
       }
       const int nhc = fold ? 0 : (hist + 7) / 8 * (8 / CPE);
       for (int i = tid; i < nhc * 32; i += RING_THREADS) hfin[i] = block_sum(hred, i >> 5, i & 31);
@@ -674,8 +686,10 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
           // The B operand overwrites the fold's operands, which its product has read.
 #pragma unroll
           for (int t = 0; t < TT; ++t) {
-            store_split<NB2>(sB, sB + NB * 128, t, tid, pk[t]);
-            store_split<NB2>(sB, sB + NB * 128, TT + t, tid, pq[t]);
+            float xk, xq;
+            upk2(pkq[t], xk, xq);
+            store_split<NB2>(sB, sB + NB * 128, 2 * t, tid, xk);
+            store_split<NB2>(sB, sB + NB * 128, 2 * t + 1, tid, xq);
           }
           fence_proxy_async_smem();
         } else {
@@ -722,7 +736,8 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
             tmem_ld16(row_tmem + c0, xh);
             tmem_ld16(row_tmem + NB + c0, xl);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) X[c0 + i] = __fadd_rn(xh[i], xl[i]);
+            for (int i = 0; i < 8; ++i)
+              X[c0 / 2 + i] = add2(pk2(xh[2 * i], xh[2 * i + 1]), pk2(xl[2 * i], xl[2 * i + 1]));
           }
         } else {
           ok = false;
@@ -767,46 +782,44 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
     if (ok && !fold) {
       for (int j = 0; j < hist; ++j) {
         const float u = bf16_bits_to_float(hu[j * KD + tid]);
+        const f32x2 uu = pk2(u, u);
         const float4* cj = reinterpret_cast<const float4*>(hfin + (j / CPE) * 32 + (j % CPE) * NB);
 #pragma unroll
         for (int t2 = 0; t2 < TT / 2; ++t2) {
           const float4 c = cj[t2];  // (k, q) of tokens 2 t2 and 2 t2 + 1
-          X[2 * t2] = __fmaf_rn(u, c.x, X[2 * t2]);
-          X[TT + 2 * t2] = __fmaf_rn(u, c.y, X[TT + 2 * t2]);
-          X[2 * t2 + 1] = __fmaf_rn(u, c.z, X[2 * t2 + 1]);
-          X[TT + 2 * t2 + 1] = __fmaf_rn(u, c.w, X[TT + 2 * t2 + 1]);
+          X[2 * t2] = fma2(uu, pk2(c.x, c.y), X[2 * t2]);
+          X[2 * t2 + 1] = fma2(uu, pk2(c.z, c.w), X[2 * t2 + 1]);
         }
       }
     }
     if (active) {
-      float ut[TT];
+      f32x2 uu[TT];  // (u~_s, u~_s)
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
-        float cct[TT], ect[TT];  // cc[t][s] (s < t) and ec[t][s] (s <= t)
+        f32x2 ce[TT];  // (cc[t][s], ec[t][s]): cc for s < t, ec for s <= t
 #pragma unroll
-        for (int s4 = 0; s4 < TT / 4; ++s4) {
-          const float4 c = reinterpret_cast<const float4*>(fin + t * TT)[s4];
-          const float4 e = reinterpret_cast<const float4*>(fint + t * TT)[s4];
-          cct[4 * s4] = c.x;
-          cct[4 * s4 + 1] = c.y;
-          cct[4 * s4 + 2] = c.z;
-          cct[4 * s4 + 3] = c.w;
-          ect[4 * s4] = e.x;
-          ect[4 * s4 + 1] = e.y;
-          ect[4 * s4 + 2] = e.z;
-          ect[4 * s4 + 3] = e.w;
+        for (int s2 = 0; s2 < TT / 2; ++s2) {
+          const float4 c = reinterpret_cast<const float4*>(fcp + 2 * t * TT)[s2];
+          ce[2 * s2] = pk2(c.x, c.y);
+          ce[2 * s2 + 1] = pk2(c.z, c.w);
         }
-        float acc = 0.0f;
+        // Both sums over s < t in one packed chain, in the order of s; the
+        // output's sum then takes its s = t term.
+        f32x2 acc2 = pk2(0.0f, 0.0f);
 #pragma unroll
-        for (int s2 = 0; s2 < t; ++s2) acc = __fmaf_rn(cct[s2], ut[s2], acc);
-        ut[t] = round_bf16(__fmul_rn(sbeta[t], __fsub_rn(bf16_bits_to_float(vcur[t]), __fadd_rn(X[t], acc))));
-        float acco = 0.0f;
-#pragma unroll
-        for (int s2 = 0; s2 <= t; ++s2) acco = __fmaf_rn(ect[s2], ut[s2], acco);
-        const float o = __fmul_rn(p.scale, __fadd_rn(X[TT + t], acco));
+        for (int s2 = 0; s2 < t; ++s2) acc2 = fma2(ce[s2], uu[s2], acc2);
+        float acc, acco, xk, xq, ctt, ect;  // ctt = cc[t][t] is not a coefficient
+        upk2(acc2, acc, acco);
+        upk2(X[t], xk, xq);
+        upk2(ce[t], ctt, ect);
+        (void)ctt;
+        const float ut = round_bf16(__fmul_rn(sbeta[t], __fsub_rn(bf16_bits_to_float(vcur[t]), __fadd_rn(xk, acc))));
+        uu[t] = pk2(ut, ut);
+        acco = __fmaf_rn(ect, ut, acco);
+        const float o = __fmul_rn(p.scale, __fadd_rn(xq, acco));
         if (t < T) {
           outp[obase + (int64_t)t * p.out_t_stride] = ok ? float_to_bf16_bits(o) : (uint16_t)0;
-          if (ok) uc[ring_row<CIRC>(cb, base + t, rp.W) + tid] = float_to_bf16_bits(ut[t]);
+          if (ok) uc[ring_row<CIRC>(cb, base + t, rp.W) + tid] = float_to_bf16_bits(ut);
         }
       }
     } else {
