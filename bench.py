@@ -287,8 +287,16 @@ def sweep(dev, steps=20, warmup=3):
         t = statistics.median(time_calls(graphed(fn), steps, warmup, before=flush))
         td = statistics.median(time_calls(fn, steps, warmup, before=flush))
         nb = traffic.decode_bytes(B)
-        res["t1_decode"].append({"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1),
-                                 "us_direct": round(td * 1e3, 2), "config": kda.kda_select_config(B, 1)})
+        row = {"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1),
+               "us_direct": round(td * 1e3, 2), "config": kda.kda_select_config(B, 1)}
+        # WARM L2, marked as such: a decode loop of 16 consecutive steps on the same
+        # slots (the state chained in place) captured as one graph, per step. Up to
+        # B = 128 the state stays in L2 between steps, as it does when serving; at
+        # larger B most of it does not.
+        loop = graphed(lambda: [fn() for _ in range(16)])
+        tw = statistics.median(time_calls(loop, steps, warmup)) / 16
+        row["us_warm_16step_graph"] = round(tw * 1e3, 2)
+        res["t1_decode"].append(row)
         del w, wd
     res["t1_decode_precomputed_gate"] = []
     for B in (8, 512):
@@ -339,8 +347,67 @@ def sweep(dev, steps=20, warmup=3):
     return res
 
 
+def _oracle_chunk_worker(path, n_iter, q):
+    """One forked worker of the all-cores oracle timing: n_iter oracle decode
+    calls on the chunk saved at `path`; puts the elapsed seconds on q."""
+    import oracle
+
+    a = np.load(path)
+    args = tuple(a[k] for k in ("state", "idx", "q", "k", "v", "g_raw", "beta_logit", "A_log", "dt_bias"))
+    oracle.kda_decode(*args)
+    t0 = time.perf_counter()
+    for _ in range(n_iter):
+        oracle.kda_decode(*args)
+    q.put(time.perf_counter() - t0)
+
+
+def oracle_all_cores(path, n_iter):
+    """Run in a fresh process that has made no CUDA call (so forking is safe):
+    one oracle worker per host core, each on its own copy of the chunk; prints
+    the core count and the slowest worker's time as one JSON line."""
+    import multiprocessing
+
+    cores = len(os.sched_getaffinity(0))
+    ctx = multiprocessing.get_context("fork")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_chunk_worker, args=(path, n_iter, q)) for _ in range(cores)]
+    for pr in procs:
+        pr.start()
+    times = [q.get() for _ in procs]
+    for pr in procs:
+        pr.join()
+    print(json.dumps({"cores": cores, "max_s": max(times), "n_iter": n_iter}), flush=True)
+
+
+def cpu_baseline_all_cores(sub, rows, per_call, seconds=10.0):
+    """The oracle on every host core at once: each core runs the same 16-row call
+    (its own copy, a compact pool of those rows' slots) in a separate process."""
+    import tempfile
+
+    idx = sub.state_indices.to(torch.int64)
+    f = lambda t: t.double().numpy()  # noqa: E731
+    chunk = {"state": f(sub.state[idx]), "idx": np.arange(len(rows), dtype=np.int32), "q": f(sub.q),
+             "k": f(sub.k), "v": f(sub.v), "g_raw": f(sub.g_raw), "beta_logit": f(sub.beta_logit),
+             "A_log": f(sub.A_log), "dt_bias": f(sub.dt_bias)}
+    n_iter = max(3, int(seconds / per_call))
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "chunk.npz")
+        np.savez(path, **chunk)
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-all-cores", path, str(n_iter)],
+                           capture_output=True, text=True, timeout=30 * seconds + 120)
+    if r.returncode != 0:
+        return {"unavailable": (r.stderr.strip().splitlines() or ["worker failed"])[-1][:200]}
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    cores, el = res["cores"], res["max_s"]
+    gbs = cores * traffic.decode_bytes(len(rows)) * n_iter / el / 1e9
+    return {"value": round(gbs, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes, each {n_iter} calls on its own copy of {len(rows)} active rows of the "
+                      f"B=512 workload; slowest {el:.1f} s; numpy fp64, one thread each"}
+
+
 def cpu_baseline(seconds=10.0):
-    """The fp64 oracle, as it stands, on 16 active rows of the headline workload."""
+    """The fp64 oracle, as it stands, on 16 active rows of the headline workload
+    (one thread), plus the same on every host core."""
     import oracle
 
     w = workloads.decode_inputs(B_HEAD, N_HEAD, seed=SEED_HEAD, layout="fused", inactive_frac=0.05)
@@ -362,7 +429,8 @@ def cpu_baseline(seconds=10.0):
     return {"value": round(traffic.decode_bytes(len(rows)) / per_call / 1e9, 6), "unit": "GB/s", "cores": 1,
             "kind": "oracle",
             "sample": f"{len(rows)} active rows of the B=512 workload per call, {n} calls in {el:.1f} s "
-                      f"({per_call * 1e3:.1f} ms per call), numpy fp64, one thread"}
+                      f"({per_call * 1e3:.1f} ms per call), numpy fp64, one thread",
+            "all_cores": cpu_baseline_all_cores(sub, rows, per_call, seconds)}
 
 
 def run_gpu(args):
@@ -459,7 +527,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-sweep", action="store_true", help="skip the B / T / fold sweep")
+    ap.add_argument("--oracle-all-cores", nargs=2, metavar=("CHUNK", "N_ITER"), help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_all_cores:
+        oracle_all_cores(args.oracle_all_cores[0], int(args.oracle_all_cores[1]))
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     if args.impl == "reference":

@@ -129,15 +129,17 @@ int32_t kda_config_tile_v(int32_t config) {
   return kTileV[config];
 }
 
-// Launch-configuration policy, measured on GB300 with L2 cold between calls
-// (CUDA-graph replays): small batches take smaller tiles, so that
-// B * H * (128 / TV) CTAs still cover the 152 SMs, and whole-head tiles
-// once a batch fills the machine on its own. T = 1 and T > 1 differ because
-// a verify CTA does T times the work per byte of state.
+// Launch-configuration policy, measured on GB300 both with L2 cold between
+// calls (CUDA-graph replays) and in warm 16-step decode loops: small batches
+// take smaller tiles, so that B * H * (128 / TV) CTAs still cover the 152
+// SMs, and whole-head tiles once a batch fills the machine on its own. T = 1
+// and T > 1 differ because a verify CTA does T times the work per byte of
+// state.
 int32_t kda_select_config(int32_t B, int32_t T) {
   if (B < 0 || T < 1 || T > KDA_MAX_T) return -1;
   if (T == 1) {
-    if (B <= 2) return 0;   // 16 rows
+    if (B <= 4) return 0;   // 16 rows
+    if (B <= 8) return 1;   // 32 rows
     if (B <= 32) return 2;  // 64 rows
     return 3;               // 128 rows
   }
