@@ -10,6 +10,7 @@ ring's cumulative log-decay) exactly where the method stores values, with a
 direct fp64 -> bf16 round-to-nearest-even that never passes through fp32.
 
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
+(the fp8 state pool in ``tests/test_oracle_pins_fp8.py``)
 against closed forms, invariants, brute force at K=V=4 and library rounding
 routines. No function is "parity unpinned".
 """
@@ -32,4 +33,12 @@ from .kda_oracle import (  # noqa: F401
     L2_EPS,
     GATE_RAW,
     GATE_PRECOMPUTED,
+)
+from .kda_fp8_oracle import (  # noqa: F401,E402
+    e4m3_decode,
+    e4m3_encode,
+    row_exponent,
+    requantize_rows,
+    dequantize,
+    kda_decode_fp8,
 )
