@@ -298,6 +298,24 @@ def sweep(dev, steps=20, warmup=3):
         row["us_warm_16step_graph"] = round(tw * 1e3, 2)
         res["t1_decode"].append(row)
         del w, wd
+    # T=1 decode on an fp8 (E4M3) pool with per-row power-of-two scales: the
+    # same activations, half the state bytes (all rows active, pool B+128)
+    res["t1_decode_fp8_state"] = []
+    for B in (1, 8, 32, 128, 512):
+        w = workloads.decode_inputs(B, B + 128, seed=50 + B, layout="fused")
+        codes, scales = workloads.fp8_pool(B + 128, seed=60 + B)
+        wd = w.to(dev)
+        c_d, s_d = codes.to(dev), scales.to(dev)
+        out = torch.empty((B, 12, 128), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_decode_fp8(c_d, s_d, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
+                                        wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
+        t = statistics.median(time_calls(graphed(fn), steps, warmup, before=flush))
+        loop = graphed(lambda: [fn() for _ in range(16)])
+        tw = statistics.median(time_calls(loop, steps, warmup)) / 16
+        nb = traffic.decode_fp8_bytes(B)
+        res["t1_decode_fp8_state"].append({"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1),
+                                           "us_warm_16step_graph": round(tw * 1e3, 2)})
+        del w, wd, c_d, s_d
     res["t1_decode_precomputed_gate"] = []
     for B in (8, 512):
         w = workloads.decode_inputs(B, B + 128, seed=40 + B, layout="fused", gate_mode=1)

@@ -7,7 +7,13 @@
 #include <stdio.h>
 
 #include "kda.h"
+#include "kda_fp8.h"
 #include "kda_launch.h"
+
+namespace kda {
+// T=1 decode on an fp8 pool (kda_fp8.cu); tile_v and bulk as launch_step's.
+cudaError_t launch_decode_fp8(const kda_params& p, const kda_fp8_pool& f, int tile_v, bool bulk, cudaStream_t s);
+}  // namespace kda
 
 namespace {
 
@@ -215,6 +221,48 @@ kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params
   if (p->B == 0) return ok();
   cudaError_t e = kda::launch_ring(*p, T, *r, bulk, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify_ring launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+kda_status kda_decode_fp8(const kda_params* p, const kda_fp8_pool* f, void* stream) {
+  if (p == nullptr) return fail(KDA_EINVAL, "params is NULL");
+  // The shared checks without the bf16 pool's (N = 0 there); the fp8 pool's follow.
+  kda_params common = *p;
+  common.N = 0;
+  bool unused = false;
+  kda_status s = check_params(&common, 1, &unused);
+  if (s != KDA_OK) return s;
+  if (p->config_override == kTensorCoreConfig)
+    return fail(KDA_EUNSUPPORTED, "config_override = %d (tensor-core verify) needs T > 1", kTensorCoreConfig);
+  if (f == nullptr) return fail(KDA_EINVAL, "fp8 pool is NULL");
+  const int64_t slot = (int64_t)p->H * 128 * 128, sslot = (int64_t)p->H * 128;
+  bool bulk = false;
+  if (p->N > 0) {
+    if (p->state == nullptr) return fail(KDA_EINVAL, "state is NULL with N = %d", p->N);
+    if (f->scale == nullptr || !aligned(f->scale, 4))
+      return fail(KDA_EINVAL, "scale is NULL or not 4-byte aligned with N = %d", p->N);
+    if (p->N > 1 && p->state_slot_stride < slot)
+      return fail(KDA_EINVAL, "state_slot_stride = %lld < H*V*K = %lld", (long long)p->state_slot_stride,
+                  (long long)slot);
+    if (p->N > 1 && f->scale_slot_stride < sslot)
+      return fail(KDA_EINVAL, "scale_slot_stride = %lld < H*V = %lld", (long long)f->scale_slot_stride,
+                  (long long)sslot);
+    bulk = aligned(p->state, 16) && aligned(f->scale, 16) &&
+           (p->N == 1 || (p->state_slot_stride % 16 == 0 && f->scale_slot_stride % 4 == 0));
+    if (p->B > 0) {
+      uintptr_t o0, o1;
+      view_extent(p->out, p->B, 1, p->H, 128, p->out_b_stride, p->out_t_stride, p->out_h_stride, o0, o1);
+      const uintptr_t c0 = reinterpret_cast<uintptr_t>(p->state);
+      const uintptr_t c1 = c0 + (uintptr_t)((int64_t)(p->N - 1) * p->state_slot_stride + slot);
+      const uintptr_t s0 = reinterpret_cast<uintptr_t>(f->scale);
+      const uintptr_t s1 = s0 + (uintptr_t)((int64_t)(p->N - 1) * f->scale_slot_stride + sslot) * 4;
+      if (overlaps(o0, o1, c0, c1)) return fail(KDA_EINVAL, "out overlaps the fp8 codes");
+      if (overlaps(o0, o1, s0, s1)) return fail(KDA_EINVAL, "out overlaps the fp8 scales");
+    }
+  }
+  if (p->B == 0) return ok();
+  cudaError_t e = kda::launch_decode_fp8(*p, *f, kTileV[pick_config(p, 1)], bulk, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_decode_fp8 launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -1,0 +1,303 @@
+// kda_fp8.cu - T=1 decode on an fp8 (E4M3) state pool for sm_103a.
+//
+// Source: "feat(kda): add packed-input CuTe decode kernel" (PR #4417),
+// section "Nsight Compute": the bf16 decode already runs at the machine's
+// ceiling for its access pattern, so the remaining headroom is fewer bytes
+// per state element, for example an fp8 state. The format is this library's
+// reading (include/kda_fp8.h): E4M3 codes, one power-of-two fp32 scale per
+// state row, kda_decode's arithmetic on the exact values code * 2^e, and
+// requantization decided in fp32 - m = max |s'| over the row's 128 keys, e =
+// the smallest integer with m 2^-e <= 448, codes = round-to-nearest-even of
+// s' 2^-e.
+//
+// One CTA of 128 threads per (batch row, head, tile of TV value rows), as in
+// the bf16 decode:
+//   1. all threads read state_indices[b]; an inactive row writes zero output
+//      and touches nothing else;
+//   2. lane 0 of each warp starts two bulk copies on one mbarrier: the warp's
+//      TV/4 rows of codes (TV/4 * 128 bytes, contiguous) and their TV/4
+//      scales; the single-token prologue runs meanwhile (the bf16 decode's,
+//      the same bits);
+//   3. 8 lanes share a row, 4 rows per warp access; lane j holds keys
+//      16j..16j+15 (16 code bytes), so a row's 8 lanes read its 128 bytes at
+//      once. Codes become fp32 through the hardware conversions
+//      cvt.rn.f16x2.e4m3x2 (exact) and f16 -> f32; the new row's maximum
+//      goes over the row's 8 lanes; cvt.rn.satfinite.e4m3x2.f32 rounds the
+//      scaled values;
+//   4. the warp writes its rows and scales back with two bulk stores, the CTA
+//      writes the outputs.
+#include <cuda_fp16.h>
+
+#include "kda_device.cuh"
+#include "kda_fp8.h"
+
+namespace kda {
+
+constexpr int F8_ROW_BYTES = KD;  // 128 codes per state row
+
+// Token vectors of one head (kh, qh, dd, gg), its v rows and outputs, beta and kappa.
+__host__ __device__ constexpr size_t fp8_head_floats(int TV) { return 4 * KD + 2 * TV + 2 * KDA_MAX_T; }
+
+__host__ __device__ constexpr size_t fp8_smem_bytes(int TV, int HP) {
+  return (size_t)HP * TV * F8_ROW_BYTES        // codes
+         + (size_t)HP * TV * 4                  // row scales
+         + 64                                   // 4 mbarriers (padded)
+         + (size_t)HP * fp8_head_floats(TV) * 4 // per-head token vectors
+         + (size_t)3 * KD * 4;                  // single-token reduction products
+}
+
+// Two E4M3 codes (low byte first) -> their exact values as an fp32 pair.
+__device__ __forceinline__ f32x2 e4m3x2_to_f32x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two & 0xffffu)));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return pk2(f.x, f.y);
+}
+
+// An fp32 pair -> two E4M3 codes (low byte = low value), round to nearest
+// even, saturating at 448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(f32x2 v) {
+  float lo, hi;
+  upk2(v, lo, hi);
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 2^e as an fp32 value, exactly, for -149 <= e <= 127.
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
+}
+
+// The smallest integer e with m 2^-e <= 448 for m >= 0 (fp32 bits): with
+// m = M 2^E, 1 <= M < 2 and 448 = 1.75 2^8, e = E - 8 when M <= 1.75 (the
+// fraction field at most 0x600000), else E - 7; 0 for m = 0 and -134 below
+// the normal range.
+__device__ __forceinline__ int row_exponent(float m) {
+  const uint32_t bits = __float_as_uint(m);
+  if (bits == 0u) return 0;
+  const int biased = (int)(bits >> 23);
+  if (biased == 0) return -134;
+  return biased - 127 - 8 + ((bits & 0x7fffffu) > 0x600000u ? 1 : 0);
+}
+
+// A lane's 16 consecutive keys 16j..16j+15 of one token's vectors, as 8 pairs.
+__device__ __forceinline__ void load_pairs16(const float* v, int j, f32x2 (&out)[8]) {
+  const float4* a = reinterpret_cast<const float4*>(v + 16 * j);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = a[i];
+    out[2 * i] = pk2(f.x, f.y);
+    out[2 * i + 1] = pk2(f.z, f.w);
+  }
+}
+
+// One step on one fp8 state row, shared by its 8 lanes (see row_step for the
+// arithmetic): dequantize, decay, the two dot products over the 8 lanes,
+// update; then the row's new exponent and codes. codes and rscale are updated
+// in place; returns the output of the row.
+__device__ __forceinline__ float row_step_fp8(uint4& codes, float& rscale, const LaneVecs& lv, int j, float beta,
+                                              float kappa, float vv, float oscale) {
+  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+  const f32x2 sc = pk2(rscale, rscale);
+  f32x2 a[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a[2 * i] = e4m3x2_to_f32x2(w[i]);
+    a[2 * i + 1] = e4m3x2_to_f32x2(w[i] >> 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = mul2(lv.dd[i], mul2(a[i], sc));  // d * (code * 2^e)
+  float x, y, u, yr;
+  partial_dots(a, lv, x, y);
+  row_reduce(x, y, j, beta, vv, u, yr);
+  const f32x2 uu = pk2(u, u);
+  float mx = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    a[i] = fma2(lv.kh[i], uu, a[i]);
+    float lo, hi;
+    upk2(a[i], lo, hi);
+    mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+  const int e = row_exponent(mx);
+  uint32_t c[4];
+  if (__all_sync(0xffffffffu, e >= -127)) {  // 2^-e is one fp32 value (every row of the warp access)
+    const f32x2 ia = pk2(pow2f(-e), pow2f(-e));
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      c[i] = f32x2_to_e4m3x2(mul2(a[2 * i], ia)) | (f32x2_to_e4m3x2(mul2(a[2 * i + 1], ia)) << 16);
+  } else {  // rows below the normal range (e down to -134): 2^-e in two exact factors
+    const int ea = min(-e, 127);
+    const f32x2 ia = pk2(pow2f(ea), pow2f(ea)), ib = pk2(pow2f(-e - ea), pow2f(-e - ea));
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      c[i] = f32x2_to_e4m3x2(mul2(mul2(a[2 * i], ia), ib)) |
+             (f32x2_to_e4m3x2(mul2(mul2(a[2 * i + 1], ia), ib)) << 16);
+  }
+  codes = make_uint4(c[0], c[1], c[2], c[3]);
+  rscale = pow2f(e);
+  return __fmul_rn(oscale, __fmaf_rn(u, kappa, yr));
+}
+
+// Five CTAs per SM: 102 registers, no spills (six would cap them at 80 and spill).
+// A CTA covers HP heads of TV rows each: with whole-head tiles, two heads (the
+// rows of heads h and h + 1 are contiguous in a slot), so that each warp has
+// 64 rows (8 KB) in flight, as many bytes as the bf16 decode's 32 rows.
+template <int TV, int HP, bool BULK>
+__global__ void __launch_bounds__(NTHREADS, 5)
+    kda_decode_fp8_kernel(const kda_params p, const kda_fp8_pool f, const int tiles) {
+  static_assert(TV % 16 == 0 && TV >= 16 && TV <= KD, "tile must be a multiple of 16 rows");
+  static_assert(HP == 1 || (HP == 2 && TV == KD), "two heads per CTA only with whole-head tiles");
+  constexpr int ROWS = HP * TV;            // rows per CTA
+  constexpr int RW = ROWS / NWARPS;        // rows per warp, all of one head
+  constexpr int RQ = RW / ROWS_PER_WARP;   // 4-row groups per warp
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int groups = p.H / HP;
+  const int tile = blockIdx.x % tiles;
+  const int hb = blockIdx.x / tiles;
+  const int h0 = (hb % groups) * HP;
+  const int b = hb / groups;
+  const int v0 = tile * TV;
+
+  uint8_t* st = smem;
+  float* ssc = reinterpret_cast<float*>(smem + ROWS * F8_ROW_BYTES);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + ROWS * F8_ROW_BYTES + ROWS * 4);
+  float* fbase = reinterpret_cast<float*>(smem + ROWS * F8_ROW_BYTES + ROWS * 4 + 64);
+  float* red = fbase + HP * fp8_head_floats(TV);
+  auto head_smem = [&](int hh, float*& orow) {
+    TokenSmem t;
+    t.kh = fbase + hh * fp8_head_floats(TV);
+    t.qh = t.kh + KD;
+    t.dd = t.qh + KD;
+    t.gg = t.dd + KD;
+    t.vrow = t.gg + KD;
+    orow = t.vrow + TV;
+    t.beta = orow + TV;
+    t.kappa = t.beta + KDA_MAX_T;
+    t.red = red;
+    return t;
+  };
+  float* orow0;
+  float* orow1;
+  const TokenSmem ts0 = head_smem(0, orow0);
+  const TokenSmem ts1 = head_smem(HP - 1, orow1);
+
+  uint16_t* outp = static_cast<uint16_t*>(p.out);
+  const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h0 * p.out_h_stride + v0;
+
+  const int n = p.state_indices[b];
+  TokenLoads1 first0, first1;  // issued alongside the index load
+  prologue_issue1(p, b, h0, v0, TV, first0);
+  if (HP == 2) prologue_issue1(p, b, h0 + 1, v0, TV, first1);
+  if (n < 0 || n >= p.N) {
+    for (int i = tid; i < ROWS; i += NTHREADS) outp[out_base + (int64_t)(i / TV) * p.out_h_stride + i % TV] = 0;
+    return;
+  }
+
+  const int64_t row0 = (int64_t)h0 * KD + v0 + warp * RW;  // first state row of this warp in the slot
+  uint8_t* gst = static_cast<uint8_t*>(p.state) + (int64_t)n * p.state_slot_stride + row0 * F8_ROW_BYTES;
+  float* gsc = f.scale + (int64_t)n * f.scale_slot_stride + row0;
+  uint8_t* sst = st + warp * RW * F8_ROW_BYTES;
+  float* ssw = ssc + warp * RW;
+  constexpr uint32_t CODE_BYTES = RW * F8_ROW_BYTES, SCALE_BYTES = RW * 4;
+
+  if constexpr (BULK) {
+    if (lane == 0) {
+      mbar_init(&mbar[warp], 1);
+      mbar_expect_tx(&mbar[warp], CODE_BYTES + SCALE_BYTES);
+      bulk_g2s(sst, gst, CODE_BYTES, &mbar[warp]);
+      bulk_g2s(ssw, gsc, SCALE_BYTES, &mbar[warp]);
+    }
+  } else {
+    for (int i = lane; i < (int)CODE_BYTES; i += 32) sst[i] = gst[i];
+    for (int i = lane; i < RW; i += 32) ssw[i] = gsc[i];
+  }
+
+  token_prologue1(p, h0, TV, ts0, first0);
+  if (HP == 2) token_prologue1(p, h0 + 1, TV, ts1, first1);
+
+  bool ok = true;
+  __syncwarp();
+  if constexpr (BULK) ok = mbar_wait_bounded(&mbar[warp], 0);
+  const int r = lane / LPR, j = lane % LPR;  // row within a 4-row group, lane within the row
+  const int hw = (warp * RW) / TV;           // this warp's head within the CTA
+  const TokenSmem& ts = hw ? ts1 : ts0;
+  float* orow = hw ? orow1 : orow0;
+  const int hrow0 = warp * RW - hw * TV;     // the warp's first row within its head's tile
+
+  if (ok) {
+    LaneVecs lv;
+    load_pairs16(ts.kh, j, lv.kh);
+    load_pairs16(ts.qh, j, lv.qh);
+    load_pairs16(ts.dd, j, lv.dd);
+    const float beta = ts.beta[0], kappa = ts.kappa[0];
+#pragma unroll 2
+    for (int q = 0; q < RQ; ++q) {
+      const int row = ROWS_PER_WARP * q + r;  // within the warp's rows
+      uint4* cell = reinterpret_cast<uint4*>(sst + row * F8_ROW_BYTES + 16 * j);
+      uint4 c = *cell;
+      float rs = ssw[row];
+      const float o = row_step_fp8(c, rs, lv, j, beta, kappa, ts.vrow[hrow0 + row], p.scale);
+      *cell = c;
+      if (j == 0) {
+        ssw[row] = rs;
+        orow[hrow0 + row] = o;
+      }
+    }
+    if constexpr (BULK) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_s2g(gst, sst, CODE_BYTES);
+        bulk_s2g(gsc, ssw, SCALE_BYTES);
+        bulk_commit();
+        bulk_wait_read_all();
+      }
+    } else {
+      __syncwarp();
+      for (int i = lane; i < (int)CODE_BYTES; i += 32) gst[i] = sst[i];
+      for (int i = lane; i < RW; i += 32) gsc[i] = ssw[i];
+    }
+  } else {
+    if (lane == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+    for (int i = lane; i < RW; i += 32) orow[hrow0 + i] = 0.0f;
+  }
+  __syncthreads();
+  for (int i = tid; i < ROWS; i += NTHREADS) {
+    const float o = i < TV ? orow0[i] : orow1[i - TV];
+    outp[out_base + (int64_t)(i / TV) * p.out_h_stride + i % TV] = float_to_bf16_bits(o);
+  }
+}
+
+template <int TV, int HP, bool BULK>
+static cudaError_t launch_f8(const kda_params& p, const kda_fp8_pool& f, cudaStream_t s) {
+  const int tiles = KD / TV;
+  const long long blocks = (long long)p.B * (p.H / HP) * tiles;
+  kda_decode_fp8_kernel<TV, HP, BULK><<<(unsigned)blocks, NTHREADS, fp8_smem_bytes(TV, HP), s>>>(p, f, tiles);
+  return cudaGetLastError();
+}
+
+template <int TV>
+static cudaError_t launch_f8_tv(const kda_params& p, const kda_fp8_pool& f, bool bulk, cudaStream_t s) {
+  return bulk ? launch_f8<TV, 1, true>(p, f, s) : launch_f8<TV, 1, false>(p, f, s);
+}
+
+cudaError_t launch_decode_fp8(const kda_params& p, const kda_fp8_pool& f, int tile_v, bool bulk, cudaStream_t s) {
+  switch (tile_v) {
+    case 16: return launch_f8_tv<16>(p, f, bulk, s);
+    case 32: return launch_f8_tv<32>(p, f, bulk, s);
+    case 64: return launch_f8_tv<64>(p, f, bulk, s);
+    case 128:
+      if (p.H % 2 == 0) return bulk ? launch_f8<128, 2, true>(p, f, s) : launch_f8<128, 2, false>(p, f, s);
+      return launch_f8_tv<128>(p, f, bulk, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kda

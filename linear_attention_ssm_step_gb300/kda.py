@@ -60,8 +60,15 @@ class KdaRingParams(ctypes.Structure):
     ]
 
 
+class KdaFp8Pool(ctypes.Structure):
+    """kda_fp8_pool of include/kda_fp8.h."""
+
+    _fields_ = [("scale", ctypes.c_void_p), ("scale_slot_stride", ctypes.c_int64)]
+
+
 EXPORTS = {
     "kda_decode": ([ctypes.POINTER(KdaParams), ctypes.c_void_p], ctypes.c_int),
+    "kda_decode_fp8": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaFp8Pool), ctypes.c_void_p], ctypes.c_int),
     "kda_verify": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "kda_verify_ring": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.POINTER(KdaRingParams),
                          ctypes.c_void_p], ctypes.c_int),
@@ -130,11 +137,11 @@ def _stream_handle(stream, device):
 
 
 def _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
-            lower_bound, scale, error_word, config_override, gate_mode):
+            lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.bfloat16):
     has_T = T is not None
     B = q.shape[0]
     H = q.shape[-2]
-    _need(state, "state", torch.bfloat16)
+    _need(state, "state", state_dtype)
     if state.dim() != 4 or state.shape[1:] != (H, 128, 128):
         raise ValueError(f"state must be [N, {H}, 128, 128], got {tuple(state.shape)}")
     if state.stride()[1:] != (128 * 128, 128, 1):
@@ -193,6 +200,24 @@ def kda_decode(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
     p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
                 lower_bound, scale, error_word, config_override, gate_mode)
     _check(load_library().kda_decode(ctypes.byref(p), _stream_handle(stream, q.device)))
+    return out
+
+
+def kda_decode_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
+                   lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
+                   stream=None):
+    """T=1 decode on an fp8 state pool (include/kda_fp8.h): codes uint8
+    [N, H, 128, 128] (E4M3) and scales fp32 [N, H, 128] (powers of two), both
+    updated in place for active rows; other arguments as kda_decode."""
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
+    p = _params(codes, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
+                lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.uint8)
+    _need(scales, "scales", torch.float32)
+    if scales.dim() != 3 or scales.shape != codes.shape[:3] or scales.stride()[1:] != (128, 1):
+        raise ValueError(f"scales must be [N, H, 128] with contiguous slots, got {tuple(scales.shape)}")
+    f = KdaFp8Pool(scales.data_ptr(), scales.stride(0))
+    _check(load_library().kda_decode_fp8(ctypes.byref(p), ctypes.byref(f), _stream_handle(stream, q.device)))
     return out
 
 

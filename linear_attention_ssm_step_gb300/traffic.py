@@ -15,6 +15,9 @@ activations. The same count is used here, per row:
                            + T x (activations + outputs) + index + hist_len
                            + f x checkpoint write
   per call:                A_log H*4 + dt_bias H*128*4
+  T=1 decode on an fp8 pool (kda_fp8.h), active row:
+                           codes read + write 2*H*V*K + row scales 2*H*V*4
+                           + the same activations, output and index
 """
 
 H, K, V = 12, 128, 128
@@ -24,6 +27,7 @@ TOKEN_IO_BYTES = 4 * H * K * 2 + H * 2 + H * V * 2  # q, k, v, g_raw, beta, out:
 RING_ENTRY_BYTES = H * (K * 2 + V * 2 + K * 4)      # k~, u~, G for all heads: 12,288
 INDEX_BYTES = 4
 PER_CALL_BYTES = H * 4 + H * K * 4           # A_log, dt_bias: 6,192
+FP8_STATE_BYTES = H * V * K + H * V * 4      # codes and row scales, one direction: 202,752
 
 
 def decode_bytes(n_active, n_inactive=0):
@@ -45,3 +49,8 @@ def ring_bytes(hists, T, flush_min, n_inactive=0):
     """hists: hist_len of each active row before the call."""
     return (sum(ring_row_bytes(h, T, h >= flush_min) for h in hists)
             + n_inactive * (INDEX_BYTES + T * H * V * 2) + PER_CALL_BYTES)
+
+
+def decode_fp8_bytes(n_active, n_inactive=0):
+    return (n_active * (2 * FP8_STATE_BYTES + TOKEN_IO_BYTES + INDEX_BYTES)
+            + n_inactive * (INDEX_BYTES + H * V * 2) + PER_CALL_BYTES)

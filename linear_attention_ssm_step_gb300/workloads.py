@@ -11,6 +11,10 @@ Distributions (the serving workloads these stand in for; no dataset exists):
   ring: k_cache = unit vectors (normalised Gaussians) in bf16,
   u_cache ~ N(0, 0.5^2) bf16, g_cache = fp32 running sums over ring
   positions of increments drawn from U[-5, 0], hist_len per slot.
+  fp8 state pool: E4M3 codes drawn field by field - sign uniform, exponent
+  field round(N(11, 2^2)) clipped to 1..15, mantissa uniform (at most 6 when
+  the exponent field is 15, so never NaN) - and per-row scales 2^e with e
+  uniform in -14..-8 (row values up to 448 * 2^-8 = 1.75, typically ~0.01).
 Standard deviations are given as the second argument of N(mean, sd^2).
 """
 
@@ -202,3 +206,18 @@ def ring_inputs(B, N, T, W=32, flush_min=9, fold_frac=0.0, seed=0, H=H_DEFAULT, 
     w.ring = dict(k_cache=k_cache, u_cache=u_cache, g_cache=g_cache, hist_len=hist, W=W,
                   flush_min=flush_min, cache_base=cache_base)
     return w
+
+
+def fp8_pool(N, H=H_DEFAULT, seed=0):
+    """An fp8 (E4M3) state pool: codes uint8 [N, H, 128, 128] and fp32 row
+    scales [N, H, 128] (powers of two), drawn as in the module docstring."""
+    g = _gen(seed)
+    shape = (N, H, D, D)
+    sign = torch.randint(0, 2, shape, generator=g, dtype=torch.int64)
+    ef = torch.clamp(torch.round(torch.randn(shape, generator=g) * 2.0 + 11.0), 1, 15).to(torch.int64)
+    mant = torch.randint(0, 8, shape, generator=g, dtype=torch.int64)
+    mant = torch.where(ef == 15, torch.clamp(mant, max=6), mant)
+    codes = ((sign << 7) | (ef << 3) | mant).to(torch.uint8)
+    e = torch.randint(-14, -7, (N, H, D), generator=g, dtype=torch.int64)
+    scales = torch.pow(2.0, e.to(torch.float64)).to(torch.float32)
+    return codes, scales

@@ -1,5 +1,5 @@
 """The C ABI on the host, without a GPU: the library loads, exports every
-function include/kda.h declares, lays out its structs as the binding does,
+function include/kda.h and include/kda_fp8.h declare, lays out its structs as the binding does,
 and rejects malformed arguments before touching CUDA. No call here passes
 validation with a non-zero batch, so nothing is ever launched."""
 
@@ -16,6 +16,8 @@ from linear_attention_ssm_step_gb300 import _build, kda
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "kda.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 # The checks that call the entry points pass fake host addresses, which
@@ -31,16 +33,19 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", text)))
+    names = set()
+    for path in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names |= set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_every_declared_function_is_exported(lib):
     names = declared_functions()
-    assert {"kda_decode", "kda_verify", "kda_verify_ring", "kda_select_config", "kda_last_error"} <= set(names)
+    assert {"kda_decode", "kda_verify", "kda_verify_ring", "kda_select_config", "kda_last_error",
+            "kda_decode_fp8"} <= set(names)
     for name in names:
-        assert hasattr(lib, name), f"{name} declared in kda.h but not exported"
+        assert hasattr(lib, name), f"{name} declared in a header but not exported"
     assert set(names) == set(kda.EXPORTS), "binding and header disagree"
 
 
@@ -59,10 +64,12 @@ def test_struct_layout_matches_header(tmp_path):
 #include <stddef.h>
 #include <stdio.h>
 #include "kda.h"
+#include "kda_fp8.h"
 #define P(s, f) printf(#s "." #f " %zu\n", offsetof(s, f))
 int main(void) {
-  printf("kda_view %zu\nkda_params %zu\nkda_ring_params %zu\n",
-         sizeof(kda_view), sizeof(kda_params), sizeof(kda_ring_params));
+  printf("kda_view %zu\nkda_params %zu\nkda_ring_params %zu\nkda_fp8_pool %zu\n",
+         sizeof(kda_view), sizeof(kda_params), sizeof(kda_ring_params), sizeof(kda_fp8_pool));
+  P(kda_fp8_pool, scale); P(kda_fp8_pool, scale_slot_stride);
   P(kda_params, q); P(kda_params, beta_logit); P(kda_params, A_log); P(kda_params, lower_bound);
   P(kda_params, state); P(kda_params, state_indices); P(kda_params, out); P(kda_params, out_h_stride);
   P(kda_params, error_word); P(kda_params, config_override); P(kda_params, gate_mode);
@@ -77,10 +84,12 @@ int main(void) {
     assert int(got["kda_view"]) == ctypes.sizeof(kda.KdaView)
     assert int(got["kda_params"]) == ctypes.sizeof(kda.KdaParams)
     assert int(got["kda_ring_params"]) == ctypes.sizeof(kda.KdaRingParams)
+    assert int(got["kda_fp8_pool"]) == ctypes.sizeof(kda.KdaFp8Pool)
     for key, val in got.items():
         if "." in key:
             s, f = key.split(".")
-            cls = {"kda_params": kda.KdaParams, "kda_ring_params": kda.KdaRingParams}[s]
+            cls = {"kda_params": kda.KdaParams, "kda_ring_params": kda.KdaRingParams,
+                   "kda_fp8_pool": kda.KdaFp8Pool}[s]
             assert getattr(cls, f).offset == int(val), key
 
 
@@ -253,3 +262,23 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(kda, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         kda.load_library()
+
+
+@no_gpu
+def test_fp8_decode_validation(lib):
+    """kda_decode_fp8 rejects a missing pool or scale array, short scale slot
+    strides, the tensor-core configuration and out overlapping the scales."""
+    p = fake_params()
+    call = lambda f: lib.kda_decode_fp8(ctypes.byref(p), None if f is None else ctypes.byref(f), None)  # noqa: E731
+    assert call(None) == kda.KDA_EINVAL and "fp8 pool" in kda.kda_last_error()
+    assert call(kda.KdaFp8Pool(None, 12 * 128)) == kda.KDA_EINVAL and "scale" in kda.kda_last_error()
+    assert call(kda.KdaFp8Pool(p.state + (1 << 26) + 2, 12 * 128)) == kda.KDA_EINVAL  # 2-byte aligned
+    assert call(kda.KdaFp8Pool(p.state + (1 << 26), 12 * 128 - 1)) == kda.KDA_EINVAL
+    assert "scale_slot_stride" in kda.kda_last_error()
+    f = kda.KdaFp8Pool(p.out, 12 * 128)  # the scales where the output goes
+    assert call(f) == kda.KDA_EINVAL and "overlaps" in kda.kda_last_error()
+    p.config_override = 4
+    assert call(kda.KdaFp8Pool(p.state + (1 << 26), 12 * 128)) == kda.KDA_EUNSUPPORTED
+    p.config_override = -1
+    p.B = 0
+    assert call(kda.KdaFp8Pool(p.state + (1 << 26), 12 * 128)) == kda.KDA_OK
