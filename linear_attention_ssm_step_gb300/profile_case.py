@@ -4,6 +4,7 @@ profilers (Nsight Compute) that need a short, clean stream of launches.
   python -m linear_attention_ssm_step_gb300.profile_case decode 512
   python -m linear_attention_ssm_step_gb300.profile_case verify 512 --T 8
   python -m linear_attention_ssm_step_gb300.profile_case ring 512 --T 8 --fold 0.5
+  python -m linear_attention_ssm_step_gb300.profile_case decode_fp8 512
 
 Each call is launched --reps times (default 3) on the same inputs, with a
 device synchronize after each; nothing is timed here.
@@ -18,7 +19,7 @@ from . import kda, workloads
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("call", choices=["decode", "verify", "ring"])
+    ap.add_argument("call", choices=["decode", "verify", "ring", "decode_fp8"])
     ap.add_argument("B", type=int)
     ap.add_argument("--T", type=int, default=8)
     ap.add_argument("--fold", type=float, default=0.0)
@@ -31,6 +32,11 @@ def main():
         w = workloads.decode_inputs(a.B, a.B + 128, seed=2, layout="fused", inactive_frac=0.05).to(dev)
         fn = lambda: kda.kda_decode(w.state, w.state_indices, w.q, w.k, w.v, w.g_raw, w.beta_logit,  # noqa: E731
                                     w.A_log, w.dt_bias, config_override=a.config)
+    elif a.call == "decode_fp8":
+        w = workloads.decode_inputs(a.B, a.B + 128, seed=2, layout="fused", inactive_frac=0.05).to(dev)
+        codes, scales = (t.to(dev) for t in workloads.fp8_pool(a.B + 128, seed=5))
+        fn = lambda: kda.kda_decode_fp8(codes, scales, w.state_indices, w.q, w.k, w.v, w.g_raw,  # noqa: E731
+                                        w.beta_logit, w.A_log, w.dt_bias, config_override=a.config)
     elif a.call == "verify":
         w = workloads.decode_inputs(a.B, a.B + 64, seed=3, T=a.T).to(dev)
         fn = lambda: kda.kda_verify(w.state, w.state_indices, w.q, w.k, w.v, w.g_raw, w.beta_logit,  # noqa: E731
