@@ -215,3 +215,35 @@ def test_fp8_rejects_bad_arguments(dev):
                            wd.dt_bias, out=s_d.view(-1).view(torch.bfloat16)[:2 * 12 * 128].view(2, 12, 128))
     assert e.value.status == kda.KDA_EINVAL
     del out_bad
+
+
+def test_fp8_precomputed_gate_and_empty_cases(dev):
+    """The pre-computed gate convention, an empty pool (every row inactive) and
+    an empty batch."""
+    w = workloads.decode_inputs(4, 6, seed=480, gate_mode=1)
+    codes, scales = workloads.fp8_pool(6, seed=481)
+    wd = w.to(dev)
+    c_d, s_d = codes.to(dev), scales.to(dev)
+    out = kda.kda_decode_fp8(c_d, s_d, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit, None, None,
+                             gate_mode=kda.KDA_GATE_PRECOMPUTED)
+    torch.cuda.synchronize()
+    ref_c, ref_s, ref_out, info = oracle.kda_decode_fp8(
+        codes.numpy(), scales.double().numpy(), w.state_indices.numpy(), f64(w.q), f64(w.k), f64(w.v),
+        f64(w.g_raw), f64(w.beta_logit), None, None, LB, 1.0, oracle.GATE_PRECOMPUTED)
+    assert_output_close(f64(out), ref_out)
+    slots = w.state_indices.numpy().astype(np.int64)
+    check_state(c_d.cpu().numpy()[slots], s_d.cpu().double().numpy()[slots], ref_c[slots], ref_s[slots],
+                info["S_new"])
+    # N = 0: every row inactive, zero output
+    empty_c, empty_s = c_d[:0], s_d[:0]
+    out = torch.full((4, 12, 128), 7.0, dtype=torch.bfloat16, device=dev)
+    kda.kda_decode_fp8(empty_c, empty_s, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit, None, None,
+                       out=out, gate_mode=kda.KDA_GATE_PRECOMPUTED)
+    torch.cuda.synchronize()
+    assert not out.any()
+    # B = 0: nothing happens
+    before = c_d.clone()
+    kda.kda_decode_fp8(c_d, s_d, wd.state_indices[:0], wd.q[:0], wd.k[:0], wd.v[:0], wd.g_raw[:0],
+                       wd.beta_logit[:0], None, None, gate_mode=kda.KDA_GATE_PRECOMPUTED)
+    torch.cuda.synchronize()
+    assert torch.equal(before, c_d)
