@@ -276,6 +276,12 @@ def e2e(dev, h, steps, warmup, world):
     return total_ms, h2d, d2h
 
 
+def spread(ts):
+    """Median, 10th and 90th percentile of per-call times (ms), in µs."""
+    q = statistics.quantiles(ts, n=10, method="inclusive")
+    return round(statistics.median(ts) * 1e3, 2), round(q[0] * 1e3, 2), round(q[-1] * 1e3, 2)
+
+
 def sweep(dev, steps=20, warmup=3):
     flush = L2Flush(dev)
     res = {"t1_decode": [], "t8_verify": [], "t8_ring_w32": []}  # more keys added below
@@ -284,10 +290,10 @@ def sweep(dev, steps=20, warmup=3):
         wd = w.to(dev)
         out = torch.empty((B, 12, 128), dtype=torch.bfloat16, device=dev)
         fn = decode_call(wd, out)
-        t = statistics.median(time_calls(graphed(fn), steps, warmup, before=flush))
+        us, p10, p90 = spread(time_calls(graphed(fn), steps, warmup, before=flush))
         td = statistics.median(time_calls(fn, steps, warmup, before=flush))
         nb = traffic.decode_bytes(B)
-        row = {"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1),
+        row = {"B": B, "us": us, "us_p10": p10, "us_p90": p90, "GB/s": round(nb / us / 1e3, 1),
                "us_direct": round(td * 1e3, 2), "config": kda.kda_select_config(B, 1)}
         # WARM L2, marked as such: a decode loop of 16 consecutive steps on the same
         # slots (the state chained in place) captured as one graph, per step. Up to
@@ -309,11 +315,12 @@ def sweep(dev, steps=20, warmup=3):
         out = torch.empty((B, 12, 128), dtype=torch.bfloat16, device=dev)
         fn = lambda: kda.kda_decode_fp8(c_d, s_d, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
                                         wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
-        t = statistics.median(time_calls(graphed(fn), steps, warmup, before=flush))
+        us, p10, p90 = spread(time_calls(graphed(fn), steps, warmup, before=flush))
         loop = graphed(lambda: [fn() for _ in range(16)])
         tw = statistics.median(time_calls(loop, steps, warmup)) / 16
         nb = traffic.decode_fp8_bytes(B)
-        res["t1_decode_fp8_state"].append({"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1),
+        res["t1_decode_fp8_state"].append({"B": B, "us": us, "us_p10": p10, "us_p90": p90,
+                                           "GB/s": round(nb / us / 1e3, 1),
                                            "us_warm_16step_graph": round(tw * 1e3, 2)})
         del w, wd, c_d, s_d
     res["t1_decode_precomputed_gate"] = []
@@ -333,9 +340,9 @@ def sweep(dev, steps=20, warmup=3):
         out = torch.empty((B, 8, 12, 128), dtype=torch.bfloat16, device=dev)
         fn = lambda: kda.kda_verify(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
                                     wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
-        t = statistics.median(time_calls(graphed(fn), steps, warmup, before=flush))
+        us, p10, p90 = spread(time_calls(graphed(fn), steps, warmup, before=flush))
         nb = traffic.verify_bytes(B, 8)
-        res["t8_verify"].append({"B": B, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1)})
+        res["t8_verify"].append({"B": B, "us": us, "us_p10": p10, "us_p90": p90, "GB/s": round(nb / us / 1e3, 1)})
         del w, wd
     for B in (1, 32, 512):
         for fold in (0.0, 0.5, 1.0):
@@ -355,12 +362,12 @@ def sweep(dev, steps=20, warmup=3):
             fn = lambda: kda.kda_verify_ring(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
                                              wd.beta_logit, wd.A_log, wd.dt_bias, r["k_cache"], r["u_cache"],
                                              r["g_cache"], r["hist_len"], 9, out=out)
-            t = statistics.median(time_calls(graphed(fn), steps, warmup, before=restore))
+            us, p10, p90 = spread(time_calls(graphed(fn), steps, warmup, before=restore))
             idx = w.state_indices.to(torch.int64)
             hists = [int(w.ring["hist_len"][n]) for n in idx]
             nb = traffic.ring_bytes(hists, 8, 9)
-            res["t8_ring_w32"].append({"B": B, "fold": fold, "us": round(t * 1e3, 2),
-                                       "GB/s": round(nb / t / 1e6, 1)})
+            res["t8_ring_w32"].append({"B": B, "fold": fold, "us": us, "us_p10": p10, "us_p90": p90,
+                                       "GB/s": round(nb / us / 1e3, 1)})
             del w, wd, saved, st0
     return res
 
