@@ -203,6 +203,36 @@ def kda_decode(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
     return out
 
 
+class PreparedCall:
+    """A library call bound to fixed tensors: argument checks and the C parameter
+    struct are done once, and each call() launches the kernel on the tensors'
+    current contents, on the stream given (or current) at preparation. The bound
+    tensors must stay alive and keep their storage; `out` is the output tensor.
+    For serving loops that refill the same input buffers every step."""
+
+    def __init__(self, fn, params, stream, out, keep):
+        self._fn, self._params, self._stream = fn, params, stream
+        self._ref = ctypes.byref(params)
+        self.out = out
+        self._keep = keep  # the bound tensors, kept alive with the call
+
+    def __call__(self):
+        _check(self._fn(self._ref, self._stream))
+        return self.out
+
+
+def prepare_decode(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
+                   lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
+                   stream=None):
+    """kda_decode bound to these tensors (see PreparedCall); same arguments."""
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
+    p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
+                lower_bound, scale, error_word, config_override, gate_mode)
+    keep = (state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, error_word)
+    return PreparedCall(load_library().kda_decode, p, _stream_handle(stream, q.device), out, keep)
+
+
 def kda_decode_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
                    lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
                    stream=None):

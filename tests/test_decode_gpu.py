@@ -341,3 +341,23 @@ def test_precomputed_gate_convention(dev, B):
     w = workloads.decode_inputs(B, B + 4, seed=40 + B, layout="packed", inactive_frac=0.2, gate_mode=1)
     w.A_log = w.dt_bias = None
     run_and_check(w, dev)
+
+
+def test_prepared_decode_equals_direct_call(dev):
+    """kda.prepare_decode binds the tensors once; each call runs on their
+    current contents and gives the bits of a direct kda_decode."""
+    w = workloads.decode_inputs(8, 12, seed=130, layout="fused", inactive_frac=0.25)
+    wa, wb = w.to(dev), w.to(dev)
+    call = kda.prepare_decode(wa.state, wa.state_indices, wa.q, wa.k, wa.v, wa.g_raw, wa.beta_logit, wa.A_log,
+                              wa.dt_bias)
+    w2 = workloads.decode_inputs(8, 12, seed=131, layout="fused", inactive_frac=0.25)
+    for step in range(3):  # refill the bound inputs between calls, as a serving loop does
+        src = (w if step % 2 == 0 else w2).to(dev)
+        for name in ("qkv", "g_raw", "beta_logit"):
+            getattr(wa, name).copy_(getattr(src, name))
+            getattr(wb, name).copy_(getattr(src, name))
+        out_a = call()
+        out_b = kda.kda_decode(wb.state, wb.state_indices, wb.q, wb.k, wb.v, wb.g_raw, wb.beta_logit, wb.A_log,
+                               wb.dt_bias)
+        torch.cuda.synchronize()
+        assert torch.equal(out_a, out_b) and torch.equal(wa.state, wb.state)
