@@ -9,14 +9,18 @@ measured with CUDA events on the launching stream around each call, the call
 replayed from a CUDA graph (so host-side argument marshalling stays out of the
 device timing), with L2 flushed (a 2 x L2 write) between calls. The same line
 carries:
-  e2e          the same metric through the public binding with this step's
-               inputs copied from pinned host memory and the output copied
-               back inside the timed region (the pool stays resident);
+  e2e          the same metric through the public binding as a serving loop
+               runs it: every step's inputs copied in from pinned host memory
+               and its output copied back, all inside one timed region,
+               pipelined over two buffer sets (the pool stays resident);
   roofline     the decode kernel's achieved GB/s against the measured HBM peak;
-  cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload;
-  sweep        T=1 decode at B = 1..512 (and with the pre-computed gate
+  cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload,
+               on one core and on all host cores;
+  sweep        T=1 decode at B = 1..512, L2-cold per call and warm in 16-step
+               loops (also on an fp8 pool, and with the pre-computed gate
                convention at B = 8, 512), T=8 verify and T=8 ring verify at
-               B = 1, 32, 512 (0/50/100% of rows folding), all L2-cold.
+               B = 1, 32, 512 (0/50/100% of rows folding), L2-cold, each with
+               its median and 10th/90th percentiles.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-sweep]
 
