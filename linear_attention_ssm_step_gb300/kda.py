@@ -210,14 +210,13 @@ class PreparedCall:
     tensors must stay alive and keep their storage; `out` is the output tensor.
     For serving loops that refill the same input buffers every step."""
 
-    def __init__(self, fn, params, stream, out, keep):
-        self._fn, self._params, self._stream = fn, params, stream
-        self._ref = ctypes.byref(params)
+    def __init__(self, fn, args, out, keep):
+        self._fn, self._args = fn, args  # ctypes arguments, structs passed by reference
         self.out = out
-        self._keep = keep  # the bound tensors, kept alive with the call
+        self._keep = keep  # the structs and bound tensors, kept alive with the call
 
     def __call__(self):
-        _check(self._fn(self._ref, self._stream))
+        _check(self._fn(*self._args))
         return self.out
 
 
@@ -229,8 +228,8 @@ def prepare_decode(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_b
         out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
     p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
                 lower_bound, scale, error_word, config_override, gate_mode)
-    keep = (state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, error_word)
-    return PreparedCall(load_library().kda_decode, p, _stream_handle(stream, q.device), out, keep)
+    keep = (p, state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, error_word)
+    return PreparedCall(load_library().kda_decode, (ctypes.byref(p), _stream_handle(stream, q.device)), out, keep)
 
 
 def kda_decode_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
@@ -243,12 +242,30 @@ def kda_decode_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_l
         out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
     p = _params(codes, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
                 lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.uint8)
+    f = _fp8_pool(codes, scales)
+    _check(load_library().kda_decode_fp8(ctypes.byref(p), ctypes.byref(f), _stream_handle(stream, q.device)))
+    return out
+
+
+def _fp8_pool(codes, scales):
     _need(scales, "scales", torch.float32)
     if scales.dim() != 3 or scales.shape != codes.shape[:3] or scales.stride()[1:] != (128, 1):
         raise ValueError(f"scales must be [N, H, 128] with contiguous slots, got {tuple(scales.shape)}")
-    f = KdaFp8Pool(scales.data_ptr(), scales.stride(0))
-    _check(load_library().kda_decode_fp8(ctypes.byref(p), ctypes.byref(f), _stream_handle(stream, q.device)))
-    return out
+    return KdaFp8Pool(scales.data_ptr(), scales.stride(0))
+
+
+def prepare_decode_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
+                       lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
+                       stream=None):
+    """kda_decode_fp8 bound to these tensors (see PreparedCall); same arguments."""
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
+    p = _params(codes, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
+                lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.uint8)
+    f = _fp8_pool(codes, scales)
+    keep = (p, f, codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, error_word)
+    args = (ctypes.byref(p), ctypes.byref(f), _stream_handle(stream, q.device))
+    return PreparedCall(load_library().kda_decode_fp8, args, out, keep)
 
 
 def kda_verify(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
@@ -265,6 +282,20 @@ def kda_verify(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
     return out
 
 
+def prepare_verify(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
+                   lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
+                   stream=None):
+    """kda_verify bound to these tensors (see PreparedCall); same arguments."""
+    B, T, H = q.shape[0], q.shape[1], q.shape[2]
+    if out is None:
+        out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=q.device)
+    p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
+                lower_bound, scale, error_word, config_override, gate_mode)
+    keep = (p, state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, error_word)
+    return PreparedCall(load_library().kda_verify, (ctypes.byref(p), T, _stream_handle(stream, q.device)), out,
+                        keep)
+
+
 def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
                     k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush=True,
                     out=None, lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1,
@@ -278,6 +309,30 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
         out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=q.device)
     p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
                 lower_bound, scale, error_word, config_override, gate_mode)
+    r = _ring_params(state, H, k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush, cache_base)
+    _check(load_library().kda_verify_ring(ctypes.byref(p), T, ctypes.byref(r),
+                                          _stream_handle(stream, q.device)))
+    return out
+
+
+def prepare_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
+                        k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush=True,
+                        out=None, lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1,
+                        gate_mode=KDA_GATE_RAW, stream=None, cache_base=None):
+    """kda_verify_ring bound to these tensors (see PreparedCall); same arguments."""
+    B, T, H = q.shape[0], q.shape[1], q.shape[2]
+    if out is None:
+        out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=q.device)
+    p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
+                lower_bound, scale, error_word, config_override, gate_mode)
+    r = _ring_params(state, H, k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush, cache_base)
+    keep = (p, r, state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, k_cache, u_cache, g_cache,
+            hist_len, cache_base, error_word)
+    args = (ctypes.byref(p), T, ctypes.byref(r), _stream_handle(stream, q.device))
+    return PreparedCall(load_library().kda_verify_ring, args, out, keep)
+
+
+def _ring_params(state, H, k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush, cache_base):
     _need(k_cache, "k_cache", torch.bfloat16)
     _need(u_cache, "u_cache", torch.bfloat16)
     _need(g_cache, "g_cache", torch.float32)
@@ -298,9 +353,7 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
     r.hist_len = hist_len.data_ptr()
     r.W, r.flush_min, r.restart_hist_on_flush = W, flush_min, int(bool(restart_hist_on_flush))
     r.cache_base = None if cache_base is None else cache_base.data_ptr()
-    _check(load_library().kda_verify_ring(ctypes.byref(p), T, ctypes.byref(r),
-                                          _stream_handle(stream, q.device)))
-    return out
+    return r
 
 
 def kda_select_config(B, T=1):
