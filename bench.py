@@ -331,7 +331,9 @@ def spread(ts):
     return round(statistics.median(ts) * 1e3, 2), round(q[0] * 1e3, 2), round(q[-1] * 1e3, 2)
 
 
-def sweep(dev, steps=20, warmup=3):
+def sweep(dev, steps=100, warmup=100):
+    """Each point: the median (and 10th/90th percentiles) of `steps` timed calls
+    after `warmup` untimed ones (100 and 100: the pages' protocol)."""
     flush = L2Flush(dev)
     res = {"t1_decode": [], "t8_verify": [], "t8_ring_w32": []}  # more keys added below
     for B in (1, 8, 16, 32, 64, 128, 256, 512):
