@@ -63,7 +63,7 @@ extern "C" {
 typedef enum {
   KDA_OK = 0,
   KDA_EINVAL = 1,        /* an argument is malformed (null, misaligned, negative, overlapping) */
-  KDA_EUNSUPPORTED = 2,  /* well-formed but outside this build (K or V != 128, H > 64, T > 16) */
+  KDA_EUNSUPPORTED = 2,  /* well-formed but outside what the library supports (K or V != 128, H > 64, T > 16) */
   KDA_ELAUNCH = 3        /* the CUDA launch was rejected (no sm_103a device, bad stream, ...) */
 } kda_status;
 
