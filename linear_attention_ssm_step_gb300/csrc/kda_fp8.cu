@@ -191,6 +191,9 @@ __global__ void __launch_bounds__(NTHREADS, 5)
   uint16_t* outp = static_cast<uint16_t*>(p.out);
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h0 * p.out_h_stride + v0;
 
+  // Programmatic dependent launch, as the bf16 decode: wait for the kernel
+  // ahead on the stream before the first read of global memory.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n = p.state_indices[b];
   TokenLoads1 first0, first1;  // issued alongside the index load
   prologue_issue1(p, b, h0, v0, TV, first0);
@@ -273,14 +276,24 @@ __global__ void __launch_bounds__(NTHREADS, 5)
     const float o = i < TV ? orow0[i] : orow1[i - TV];
     outp[out_base + (int64_t)(i / TV) * p.out_h_stride + i % TV] = float_to_bf16_bits(o);
   }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <int TV, int HP, bool BULK>
 static cudaError_t launch_f8(const kda_params& p, const kda_fp8_pool& f, cudaStream_t s) {
   const int tiles = KD / TV;
   const long long blocks = (long long)p.B * (p.H / HP) * tiles;
-  kda_decode_fp8_kernel<TV, HP, BULK><<<(unsigned)blocks, NTHREADS, fp8_smem_bytes(TV, HP), s>>>(p, f, tiles);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = fp8_smem_bytes(TV, HP);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kda_decode_fp8_kernel<TV, HP, BULK>, p, f, tiles);
 }
 
 template <int TV>

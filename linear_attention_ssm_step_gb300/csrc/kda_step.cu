@@ -73,6 +73,10 @@ __global__ void __launch_bounds__(32 * NW, MULTI ? (NW == 8 ? 2 : 1) : 6)
   uint16_t* outp = static_cast<uint16_t*>(p.out);
   const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
 
+  // Launched with programmatic dependent launch allowed: wait here, before the
+  // first read of global memory, until the kernel ahead on the stream has
+  // completed and its writes are visible (a no-op without one).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n = p.state_indices[b];
   // Token inputs, issued alongside the index load (unused by an inactive row):
   // one token over all threads for T = 1, else up to PT tokens per warp.
@@ -175,6 +179,8 @@ __global__ void __launch_bounds__(32 * NW, MULTI ? (NW == 8 ? 2 : 1) : 6)
     const int t = i / TV, rr = i - t * TV;
     outp[out_base + (int64_t)t * p.out_t_stride + rr] = float_to_bf16_bits(orow[i]);
   }
+  // This CTA's writes are issued: the next kernel on the stream may start launching.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <int TV, bool BULK, bool MULTI, int NW, int TT>
@@ -185,8 +191,19 @@ static cudaError_t launch_one(const kda_params& p, int T, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int tiles = KD / TV;
   const long long blocks = (long long)p.B * p.H * tiles;
-  kern<<<(unsigned)blocks, 32 * NW, step_smem_bytes(TV, T), stream>>>(p, T, tiles);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the grid may be scheduled while the kernel
+  // ahead on the stream finishes (its CTAs wait at griddepcontrol.wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(32 * NW);
+  cfg.dynamicSmemBytes = step_smem_bytes(TV, T);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, T, tiles);
 }
 
 // Verify tiles of 64 or 128 rows run 8 warps (16 warps per SM at two CTAs);
