@@ -10,14 +10,14 @@
 // the smallest integer with m 2^-e <= 448, codes = round-to-nearest-even of
 // s' 2^-e.
 //
-// One CTA of 128 threads per (batch row, head, tile of TV value rows), as in
-// the bf16 decode:
+// One CTA of 128 threads per (batch row, HP heads, tile of TV value rows), as
+// in the bf16 decode (whole-head tiles take two heads, HP = 2):
 //   1. all threads read state_indices[b]; an inactive row writes zero output
 //      and touches nothing else;
 //   2. lane 0 of each warp starts two bulk copies on one mbarrier: the warp's
-//      TV/4 rows of codes (TV/4 * 128 bytes, contiguous) and their TV/4
-//      scales; the single-token prologue runs meanwhile (the bf16 decode's,
-//      the same bits);
+//      HP TV/4 rows of codes (128 bytes each, contiguous) and their scales;
+//      the single-token prologue of each head runs meanwhile (the bf16
+//      decode's, the same bits);
 //   3. 8 lanes share a row, 4 rows per warp access; lane j holds keys
 //      16j..16j+15 (16 code bytes), so a row's 8 lanes read its 128 bytes at
 //      once. Codes become fp32 through the hardware conversions
