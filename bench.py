@@ -547,7 +547,10 @@ def run_gpu(args):
                    "parallelism": f"{world} GPU(s), one independent batch and pool per GPU, no collective on the data path"},
         "e2e": {"value": round(h["nbytes"] * world * args.steps / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s",
                 "us_per_step": round(e2e_ms / args.steps * 1e3, 2),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "prepared kda_decode call; each step's inputs copied in from pinned host memory and its "
+                       "output copied back inside one timed region over all steps, pipelined over two buffer "
+                       "sets on three streams; no L2 flush (the state pool is larger than L2)"},
         "roofline": {"kernel": "kda_step_kernel<128,bulk,T=1>", "bound": "hbm",
                      "achieved": round(per_launch_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(per_launch_gbs / peak, 4), "peak_kind": f"{peak_kind} HBM copy bandwidth",
