@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from harness import assert_output_close, assert_state_close, f64, gpu_ring, oracle_ring, state_ulps
 from linear_attention_ssm_step_gb300 import kda, workloads
 
@@ -280,3 +281,51 @@ def test_ring_precomputed_gate_convention(dev):
     w = workloads.ring_inputs(6, 12, T=8, W=32, flush_min=9, fold_frac=0.5, seed=13, gate_mode=1)
     w.A_log = w.dt_bias = None
     check_ring(w, dev)
+
+
+def test_ring_serving_loop(dev):
+    """Six consecutive T = 8 calls on the same slots, as a speculative-decoding
+    loop runs them: between calls the caller advances hist_len by the tokens it
+    accepted (8, 5, 8, 3, 8, 8), and a call folds whenever the history has
+    reached flush_min = 9. GPU and oracle each run their own chain; every
+    call's outputs within tolerance, hist_len equal, the checkpoints within the
+    chained-state bound and the live ring entries within their bounds."""
+    B, N, T, W, FM = 4, 8, 8, 32, 9
+    w0 = workloads.ring_inputs(B, N, T=T, W=W, flush_min=FM, fold_frac=0.0, seed=40)
+    w0.ring["hist_len"].zero_()
+    idx_t = w0.state_indices
+    idx = idx_t.numpy().astype(np.int64)
+    g_state = w0.state.to(dev)
+    g_ring = {k: w0.ring[k].to(dev) for k in ("k_cache", "u_cache", "g_cache", "hist_len")}
+    r_state = f64(w0.state)
+    r_ring = {k: f64(w0.ring[k]) for k in ("k_cache", "u_cache", "g_cache", "hist_len")}
+    folds = 0
+    for call, accepted in enumerate((8, 5, 8, 3, 8, 8)):
+        w = workloads.decode_inputs(B, N, seed=50 + call, T=T, indices=idx_t)
+        wd = w.to(dev)
+        folds += int((r_ring["hist_len"][idx] >= FM).any())
+        out = kda.kda_verify_ring(g_state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit, wd.A_log,
+                                  wd.dt_bias, g_ring["k_cache"], g_ring["u_cache"], g_ring["g_cache"],
+                                  g_ring["hist_len"], FM)
+        ref = oracle.kda_verify_ring(r_state, idx, f64(w.q), f64(w.k), f64(w.v), f64(w.g_raw), f64(w.beta_logit),
+                                     f64(w.A_log), f64(w.dt_bias), r_ring["k_cache"], r_ring["u_cache"],
+                                     r_ring["g_cache"], r_ring["hist_len"], FM)
+        torch.cuda.synchronize()
+        assert_output_close(f64(out), ref["out"], f"call {call} output")
+        assert np.array_equal(f64(g_ring["hist_len"]), ref["hist_len"]), f"call {call} hist_len"
+        assert_state_close(f64(g_state)[idx], ref["state"][idx], f"call {call} checkpoint", steps=max(folds, 1) + 1)
+        live = [int(h) for h in ref["hist_len"][idx]]
+        kc, uc, gc = f64(g_ring["k_cache"]), f64(g_ring["u_cache"]), f64(g_ring["g_cache"])
+        for n, h in zip(idx, live):  # the entries this call wrote, from the (possibly reset) history on
+            pos = list(range(h, h + T))
+            assert float(ring_ulps(kc[n][:, pos], ref["k_cache"][n][:, pos]).max()) <= 1.0
+            assert float(ring_ulps(uc[n][:, pos], ref["u_cache"][n][:, pos], floor=1.0).max()) <= 2.0
+            G, Gr = gc[n][:, pos], ref["g_cache"][n][:, pos]
+            assert np.all(np.abs(G - Gr) <= 1e-5 * (1.0 + np.abs(Gr)))
+        r_state = ref["state"]
+        r_ring = {k: ref[k] for k in ("k_cache", "u_cache", "g_cache")}
+        r_ring["hist_len"] = ref["hist_len"].copy()
+        # the caller accepts `accepted` of the T draft tokens
+        r_ring["hist_len"][idx] += accepted
+        g_ring["hist_len"][idx_t.long().to(dev)] += accepted
+    assert folds >= 2
