@@ -395,9 +395,10 @@ def sweep(dev, steps=100, warmup=100):
         nb = traffic.verify_bytes(B, 8)
         res["t8_verify"].append({"B": B, "us": us, "us_p10": p10, "us_p90": p90, "GB/s": round(nb / us / 1e3, 1)})
         del w, wd
-    for B in (1, 32, 512):
+    res["t8_ring_w16"] = []  # the pages' own ring width for T = 8, at the serving batch
+    for B, W in [(1, 32), (32, 32), (512, 32), (512, 16)]:
         for fold in (0.0, 0.5, 1.0):
-            w = workloads.ring_inputs(B, B + 64, T=8, W=32, flush_min=9, fold_frac=fold, seed=30 + B)
+            w = workloads.ring_inputs(B, B + 64, T=8, W=W, flush_min=9, fold_frac=fold, seed=30 + B)
             wd = w.to(dev)
             saved = {k: v.clone() for k, v in wd.ring.items() if isinstance(v, torch.Tensor)}
             st0 = wd.state.clone()
@@ -417,8 +418,8 @@ def sweep(dev, steps=100, warmup=100):
             idx = w.state_indices.to(torch.int64)
             hists = [int(w.ring["hist_len"][n]) for n in idx]
             nb = traffic.ring_bytes(hists, 8, 9)
-            res["t8_ring_w32"].append({"B": B, "fold": fold, "us": us, "us_p10": p10, "us_p90": p90,
-                                       "GB/s": round(nb / us / 1e3, 1)})
+            res["t8_ring_w%d" % W].append({"B": B, "fold": fold, "us": us, "us_p10": p10, "us_p90": p90,
+                                            "GB/s": round(nb / us / 1e3, 1)})
             del w, wd, saved, st0
     return res
 
