@@ -18,6 +18,12 @@ activations. The same count is used here, per row:
   T=1 decode on an fp8 pool (kda_fp8.h), active row:
                            codes read + write 2*H*V*K + row scales 2*H*V*4
                            + the same activations, output and index
+  varlen prefill (kda_prefill.h), an active sequence of n tokens:
+                           its slot once each way + n x (activations + outputs)
+                           + index + two cu_seqlens entries. The prefill is
+                           bound by arithmetic, not bytes: per token and head
+                           the step does 7 flops per state element (decay 1,
+                           two dot products 4, update 2), 7*K*V in all.
 """
 
 H, K, V = 12, 128, 128
@@ -54,3 +60,14 @@ def ring_bytes(hists, T, flush_min, n_inactive=0):
 def decode_fp8_bytes(n_active, n_inactive=0):
     return (n_active * (2 * FP8_STATE_BYTES + TOKEN_IO_BYTES + INDEX_BYTES)
             + n_inactive * (INDEX_BYTES + H * V * 2) + PER_CALL_BYTES)
+
+
+def prefill_bytes(lengths, n_inactive_tokens=0):
+    """Active sequences of the given lengths, plus inactive tokens (zero outputs)."""
+    return (sum(2 * STATE_BYTES + n * TOKEN_IO_BYTES + INDEX_BYTES + 8 for n in lengths)
+            + n_inactive_tokens * H * V * 2 + PER_CALL_BYTES)
+
+
+def prefill_flops(tokens, heads=H):
+    """Arithmetic of the recurrence over `tokens` active tokens of `heads` heads."""
+    return tokens * heads * 7 * K * V

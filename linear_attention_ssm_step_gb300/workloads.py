@@ -11,6 +11,9 @@ Distributions (the serving workloads these stand in for; no dataset exists):
   ring: k_cache = unit vectors (normalised Gaussians) in bf16,
   u_cache ~ N(0, 0.5^2) bf16, g_cache = fp32 running sums over ring
   positions of increments drawn from U[-5, 0], hist_len per slot.
+  prefill: packed sequences of given lengths, one token per activation row
+  (the decode distributions), cu_seqlens their running offsets, one distinct
+  slot per sequence (a fraction of them inactive, as for decode rows).
   fp8 state pool: E4M3 codes drawn field by field - sign uniform, exponent
   field round(N(11, 2^2)) clipped to 1..15, mantissa uniform (at most 6 when
   the exponent field is 15, so never NaN) - and per-row scales 2^e with e
@@ -53,6 +56,7 @@ class Workload:
     v_sep: torch.Tensor = None
     ring: dict = field(default_factory=dict)  # k_cache, u_cache, g_cache, hist_len, W, flush_min
     gate_mode: int = 0           # 0: raw gate and beta logits; 1: log-space g and beta given
+    cu_seqlens: torch.Tensor = None  # prefill: int32 [S + 1] row offsets of the sequences
 
     @property
     def B(self):
@@ -98,7 +102,7 @@ class Workload:
         return replace(self, state=mv(self.state), state_indices=mv(self.state_indices),
                        g_raw=mv(self.g_raw), beta_logit=mv(self.beta_logit), A_log=mv(self.A_log),
                        dt_bias=mv(self.dt_bias), qkv=mv(self.qkv), q_sep=mv(self.q_sep),
-                       k_sep=mv(self.k_sep), v_sep=mv(self.v_sep), ring=ring)
+                       k_sep=mv(self.k_sep), v_sep=mv(self.v_sep), ring=ring, cu_seqlens=mv(self.cu_seqlens))
 
     def clone(self):
         c = lambda t: None if t is None else t.clone()  # noqa: E731
@@ -106,7 +110,7 @@ class Workload:
         return replace(self, state=c(self.state), state_indices=c(self.state_indices),
                        g_raw=c(self.g_raw), beta_logit=c(self.beta_logit), A_log=c(self.A_log),
                        dt_bias=c(self.dt_bias), qkv=c(self.qkv), q_sep=c(self.q_sep),
-                       k_sep=c(self.k_sep), v_sep=c(self.v_sep), ring=ring)
+                       k_sep=c(self.k_sep), v_sep=c(self.v_sep), ring=ring, cu_seqlens=c(self.cu_seqlens))
 
 
 def slot_indices(g, B, N, inactive_frac=0.0):
@@ -205,6 +209,21 @@ def ring_inputs(B, N, T, W=32, flush_min=9, fold_frac=0.0, seed=0, H=H_DEFAULT, 
         g_cache = torch.stack([torch.roll(g_cache[n], shifts[n], dims=1) for n in range(N)])
     w.ring = dict(k_cache=k_cache, u_cache=u_cache, g_cache=g_cache, hist_len=hist, W=W,
                   flush_min=flush_min, cache_base=cache_base)
+    return w
+
+
+def prefill_inputs(lengths, N, seed=0, layout="separate", inactive_frac=0.0, H=H_DEFAULT, state_std=0.02,
+                   gate_mode=0):
+    """Inputs of kda_prefill: len(lengths) sequences packed row after row
+    (L = sum(lengths) activation rows, drawn as decode rows), cu_seqlens their
+    offsets, state_indices one slot per sequence (some inactive)."""
+    L = int(sum(lengths))
+    g = _gen(seed + 104729)
+    idx = slot_indices(g, len(lengths), N, inactive_frac)
+    w = decode_inputs(L, N, seed=seed, layout=layout, H=H, state_std=state_std, gate_mode=gate_mode,
+                      indices=torch.zeros(L, dtype=torch.int32))
+    w.state_indices = idx
+    w.cu_seqlens = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
     return w
 
 

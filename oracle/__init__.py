@@ -10,7 +10,8 @@ ring's cumulative log-decay) exactly where the method stores values, with a
 direct fp64 -> bf16 round-to-nearest-even that never passes through fp32.
 
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
-(the fp8 state pool in ``tests/test_oracle_pins_fp8.py``)
+(the fp8 state pool in ``tests/test_oracle_pins_fp8.py``, the varlen prefill in
+``tests/test_oracle_pins_prefill.py``)
 against closed forms, invariants, brute force at K=V=4 and library rounding
 routines. No function is "parity unpinned".
 """
@@ -41,4 +42,8 @@ from .kda_fp8_oracle import (  # noqa: F401,E402
     requantize_rows,
     dequantize,
     kda_decode_fp8,
+)
+from .kda_prefill_oracle import (  # noqa: F401,E402
+    kda_prefill,
+    PREFILL_ERR_SEQLENS,
 )
