@@ -20,8 +20,11 @@ carries:
   sweep        T=1 decode at B = 1..2048, L2-cold per call and warm in 16-step
                loops (also on an fp8 pool, and with the pre-computed gate
                convention at B = 8, 512), T=8 verify and T=8 ring verify at
-               B = 1, 32, 512 (0/50/100% of rows folding), L2-cold, each with
-               its median and 10th/90th percentiles.
+               B = 1, 32, 512 (0/50/100% of rows folding), L2-cold, and the
+               varlen prefill at 1 x 4096, 8 x 2048, 64 x 256 and 512 x 16
+               tokens (H = 12) and two shapes of the prefill page (H = 16,
+               1 x 16384; H = 4, lengths 1..15), each with its median and
+               10th/90th percentiles.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-sweep]
 
@@ -405,6 +408,33 @@ def sweep(dev, steps=100, warmup=100):
         nb = traffic.verify_bytes(B, 8)
         res["t8_verify"].append({"B": B, "us": us, "us_p10": p10, "us_p90": p90, "GB/s": round(nb / us / 1e3, 1)})
         del w, wd
+    # varlen prefill (kda_prefill): S sequences of equal length packed row after
+    # row, each filling its own slot; L2 flushed before each call
+    # (the last two are shapes of the prefill page's portfolio: H16 with one
+    # 16384-token sequence, and H4 with sequences of 1..15 tokens)
+    res["prefill"] = []
+    for name, lens, Hh in (("1x4096", [4096], 12), ("8x2048", [2048] * 8, 12), ("64x256", [256] * 64, 12),
+                           ("512x16", [16] * 512, 12), ("h16_1x16384", [16384], 16),
+                           ("h4_seq1_to_15", list(range(1, 16)), 4)):
+        S, toks = len(lens), sum(lens)
+        w = workloads.prefill_inputs(lens, S + 8, seed=90 + S, layout="fused", H=Hh)
+        wd = w.to(dev)
+        st0 = wd.state.clone()
+        out = torch.empty((toks, Hh, 128), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_prefill(wd.state, wd.state_indices, wd.cu_seqlens, wd.q, wd.k, wd.v,  # noqa: E731
+                                     wd.g_raw, wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
+
+        def reset():
+            wd.state.copy_(st0)
+            flush()
+
+        n = max(10, steps // 4)
+        us, p10, p90 = spread(time_calls(graphed(fn), n, max(3, warmup // 4), before=reset))
+        flops = traffic.prefill_flops(toks, Hh)
+        res["prefill"].append({"case": name, "H": Hh, "seqs": S, "tokens": toks, "us": us, "us_p10": p10,
+                               "us_p90": p90, "Mtokens/s": round(toks / us, 3),
+                               "TFLOP/s": round(flops / us / 1e6, 2), "config": kda.kda_select_prefill_config(S, Hh)})
+        del w, wd, st0, out
     res["t8_ring_w16"] = []  # the pages' own ring width for T = 8, at the serving batch
     for B, W in [(1, 32), (32, 32), (512, 32), (512, 16)]:
         for fold in (0.0, 0.5, 1.0):

@@ -16,7 +16,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libkda_gb300.so")
 
-SOURCES = ["kda_api.cu", "kda_step.cu", "kda_ring.cu", "kda_tmap.cu", "kda_verify_tc.cu", "kda_fp8.cu"]
+SOURCES = ["kda_api.cu", "kda_step.cu", "kda_ring.cu", "kda_tmap.cu", "kda_verify_tc.cu", "kda_fp8.cu",
+           "kda_prefill.cu"]
 HEADERS = ["kda_device.cuh", "kda_launch.h", "kda_tc.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -35,7 +36,7 @@ def _nvcc():
 
 
 def _inputs():
-    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, h) for h in ("kda.h", "kda_fp8.h")]
+    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, h) for h in ("kda.h", "kda_fp8.h", "kda_prefill.h")]
     files.append(os.path.abspath(__file__))
     return files
 

@@ -17,6 +17,7 @@ KDA_OK, KDA_EINVAL, KDA_EUNSUPPORTED, KDA_ELAUNCH = 0, 1, 2, 3
 KDA_ERR_HIST_LEN = 1
 KDA_ERR_TIMEOUT = 2
 KDA_ERR_CACHE_BASE = 4
+KDA_ERR_SEQLENS = 8
 KDA_MAX_T = 16
 KDA_GATE_RAW, KDA_GATE_PRECOMPUTED = 0, 1
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_EINVAL", 2: "KDA_EUNSUPPORTED", 3: "KDA_ELAUNCH"}
@@ -66,10 +67,18 @@ class KdaFp8Pool(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_void_p), ("scale_slot_stride", ctypes.c_int64)]
 
 
+class KdaSeqs(ctypes.Structure):
+    """kda_seqs of include/kda_prefill.h."""
+
+    _fields_ = [("cu_seqlens", ctypes.c_void_p), ("num_seqs", ctypes.c_int32)]
+
+
 EXPORTS = {
     "kda_decode": ([ctypes.POINTER(KdaParams), ctypes.c_void_p], ctypes.c_int),
     "kda_decode_fp8": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaFp8Pool), ctypes.c_void_p], ctypes.c_int),
     "kda_verify": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
+    "kda_prefill": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaSeqs), ctypes.c_void_p], ctypes.c_int),
+    "kda_select_prefill_config": ([ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
     "kda_verify_ring": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.POINTER(KdaRingParams),
                          ctypes.c_void_p], ctypes.c_int),
     "kda_num_configs": ([], ctypes.c_int32),
@@ -137,9 +146,11 @@ def _stream_handle(stream, device):
 
 
 def _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
-            lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.bfloat16):
+            lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.bfloat16,
+            n_indices=None):
     has_T = T is not None
     B = q.shape[0]
+    n_idx = B if n_indices is None else n_indices
     H = q.shape[-2]
     _need(state, "state", state_dtype)
     if state.dim() != 4 or state.shape[1:] != (H, 128, 128):
@@ -147,8 +158,8 @@ def _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, ou
     if state.stride()[1:] != (128 * 128, 128, 1):
         raise ValueError("each state slot must be contiguous [H][V][K]")
     _need(state_indices, "state_indices", torch.int32)
-    if state_indices.shape != (B,) or (B > 0 and state_indices.stride(0) != 1):
-        raise ValueError("state_indices must be a contiguous [B] tensor")
+    if state_indices.shape != (n_idx,) or (n_idx > 0 and state_indices.stride(0) != 1):
+        raise ValueError(f"state_indices must be a contiguous [{n_idx}] tensor")
     if gate_mode == KDA_GATE_RAW or A_log is not None:
         _need(A_log, "A_log", torch.float32)
         if A_log.numel() != H or not A_log.is_contiguous():
@@ -354,6 +365,33 @@ def _ring_params(state, H, k_cache, u_cache, g_cache, hist_len, flush_min, resta
     r.W, r.flush_min, r.restart_hist_on_flush = W, flush_min, int(bool(restart_hist_on_flush))
     r.cache_base = None if cache_base is None else cache_base.data_ptr()
     return r
+
+
+def kda_prefill(state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
+                lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
+                stream=None):
+    """Varlen prefill (include/kda_prefill.h). q, k, v, g_raw: bf16 [L, H, 128]
+    views with one row per token (any row and head stride); beta_logit: bf16
+    [L, H]; cu_seqlens: int32 [S + 1] on the device, sequence i owning rows
+    cu_seqlens[i] .. cu_seqlens[i+1]-1; state_indices: int32 [S], one slot per
+    sequence; state: bf16 [N, H, 128, 128] pool, read as each sequence's
+    initial state and overwritten with its final state. Returns out bf16
+    [L, H, 128] (rows no sequence covers are left as they were)."""
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    if cu_seqlens.dim() != 1 or cu_seqlens.shape[0] < 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous [S + 1] tensor")
+    S = cu_seqlens.shape[0] - 1
+    p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
+                lower_bound, scale, error_word, config_override, gate_mode, n_indices=S)
+    sq = KdaSeqs(cu_seqlens.data_ptr(), S)
+    _check(load_library().kda_prefill(ctypes.byref(p), ctypes.byref(sq), _stream_handle(stream, q.device)))
+    return out
+
+
+def kda_select_prefill_config(num_seqs, H=12):
+    return int(load_library().kda_select_prefill_config(num_seqs, H))
 
 
 def kda_select_config(B, T=1):

@@ -1,0 +1,228 @@
+"""kda_prefill (varlen prefill on the bf16 pool) on the GPU against the fp64
+prefill oracle, through the C ABI.
+
+What is compared:
+  * outputs: the decode's tolerance, 2e-2 + 2e-2 |o_ref|;
+  * final states: one-token sequences are one decode step, held to the
+    single-step bound (2 bf16 ulps at max(|s_ref|, 2^-12 M)); longer ones to
+    2 bf16 ulps at the head's scale M. The kernel carries the state in fp32
+    across the tokens and the oracle in fp64: their difference grows by at
+    most a few 2^-24 M per token (the step map is non-expansive), far below
+    ulp(M) for the lengths here, and the final rounding to bf16 can fall on
+    either side of a boundary;
+  * rows of inactive sequences: exactly zero; rows no valid sequence covers
+    and slots no active sequence owns: bit for bit unchanged;
+  * one-token sequences against kda_decode on the same rows: bit for bit.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from harness import assert_output_close, assert_state_close, f64
+from linear_attention_ssm_step_gb300 import kda, workloads
+
+pytestmark = pytest.mark.gpu
+
+LB = -5.0
+SENTINEL = 7.0  # written into out before a call: rows the call must not touch keep it
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def gpu_prefill(wd, out=None, **kw):
+    kw.setdefault("gate_mode", wd.gate_mode)
+    if out is None:
+        out = torch.full((wd.q.shape[0], wd.H, 128), SENTINEL, dtype=torch.bfloat16, device=wd.q.device)
+    return kda.kda_prefill(wd.state, wd.state_indices, wd.cu_seqlens, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
+                           wd.A_log, wd.dt_bias, out=out, lower_bound=LB, **kw)
+
+
+def oracle_prefill(w, scale=1.0):
+    return oracle.kda_prefill(f64(w.state), f64(w.state_indices), f64(w.cu_seqlens), f64(w.q), f64(w.k), f64(w.v),
+                              f64(w.g_raw), f64(w.beta_logit), f64(w.A_log), f64(w.dt_bias),
+                              lower_bound=LB, scale=scale, gate_mode=w.gate_mode)
+
+
+def check_prefill(w, wd, out, scale=1.0, err_expected=0):
+    new_ref, out_ref, written, err = oracle_prefill(w, scale)
+    assert err == err_expected
+    got = f64(out)
+    assert_output_close(got[written], out_ref[written], "outputs")
+    assert np.all(got[~written] == SENTINEL), "rows no sequence covers must keep their contents"
+    st = f64(wd.state)
+    st0 = f64(w.state)
+    idx = w.state_indices.tolist()
+    cu = w.cu_seqlens.tolist()
+    owned = set()
+    for i, n in enumerate(idx):
+        t0, t1 = cu[i], cu[i + 1]
+        if not (0 <= n < w.N) or not (0 <= t0 <= t1 <= w.q.shape[0]) or t0 == t1:
+            continue
+        owned.add(n)
+        assert_state_close(st[n], new_ref[n], f"final state of sequence {i} ({t1 - t0} tokens)", steps=t1 - t0)
+    for i, n in enumerate(idx):
+        t0, t1 = cu[i], cu[i + 1]
+        if not (0 <= n < w.N) and 0 <= t0 <= t1 <= w.q.shape[0]:
+            assert np.all(got[t0:t1] == 0.0), f"inactive sequence {i} must write zeros"
+    rest = [n for n in range(w.N) if n not in owned]
+    assert np.array_equal(st[rest], st0[rest]), "slots no active sequence owns must be untouched"
+
+
+LENGTHS = [1, 17, 0, 40, 5, 16, 33, 2]
+
+
+@pytest.mark.parametrize("config", [-1, 0, 1, 2, 3])
+def test_prefill_matches_oracle(dev, config):
+    w = workloads.prefill_inputs(LENGTHS, 12, seed=70 + config, inactive_frac=0.25, layout="fused")
+    wd = w.to(dev)
+    out = gpu_prefill(wd, config_override=config)
+    torch.cuda.synchronize()
+    check_prefill(w, wd, out)
+
+
+def test_prefill_precomputed_gate_and_scale(dev):
+    w = workloads.prefill_inputs([7, 20, 1], 5, seed=71, gate_mode=1)
+    wd = w.to(dev)
+    out = gpu_prefill(wd, scale=0.5)
+    torch.cuda.synchronize()
+    check_prefill(w, wd, out, scale=0.5)
+
+
+def test_prefill_three_heads_packed(dev):
+    w = workloads.prefill_inputs([9, 3, 25], 6, seed=72, H=3, layout="packed")
+    wd = w.to(dev)
+    out = gpu_prefill(wd)
+    torch.cuda.synchronize()
+    check_prefill(w, wd, out)
+
+
+def test_prefill_long_sequence(dev):
+    """One 1000-token sequence and two short ones; every output and both states."""
+    w = workloads.prefill_inputs([1000, 3, 12], 4, seed=73)
+    wd = w.to(dev)
+    out = gpu_prefill(wd)
+    torch.cuda.synchronize()
+    check_prefill(w, wd, out)
+
+
+def test_single_token_sequences_equal_decode_bit_for_bit(dev):
+    """A prefill of one-token sequences is one decode step per slot."""
+    B = 37
+    w = workloads.prefill_inputs([1] * B, B + 20, seed=74, inactive_frac=0.1, layout="fused")
+    a, b = w.to(dev), w.to(dev)
+    out_p = gpu_prefill(a)
+    out_d = kda.kda_decode(b.state, b.state_indices, b.q, b.k, b.v, b.g_raw, b.beta_logit, b.A_log, b.dt_bias,
+                           lower_bound=LB)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p.view(torch.int16), out_d.view(torch.int16))
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+
+
+def test_prefill_configs_agree_bit_for_bit(dev):
+    """The tile size changes only which CTA runs a row, not its arithmetic."""
+    w = workloads.prefill_inputs([5, 30, 18], 5, seed=75)
+    res = []
+    for config in (0, 1, 2, 3):
+        wd = w.to(dev)
+        out = gpu_prefill(wd, config_override=config)
+        torch.cuda.synchronize()
+        res.append((out.view(torch.int16).clone(), wd.state.view(torch.int16).clone()))
+    for o, s in res[1:]:
+        assert torch.equal(o, res[0][0]) and torch.equal(s, res[0][1])
+
+
+def test_prefill_misaligned_pool_same_bits(dev):
+    w = workloads.prefill_inputs([6, 21], 4, seed=76)
+    a, b = w.to(dev), w.to(dev)
+    flat = torch.empty(b.state.numel() + 8, dtype=torch.bfloat16, device=dev)
+    mis = flat[1:1 + b.state.numel()].view(b.state.shape)
+    mis.copy_(b.state)
+    assert mis.data_ptr() % 16 == 2
+    b.state = mis
+    oa, ob = gpu_prefill(a), gpu_prefill(b)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+
+
+def test_prefill_bad_bounds_set_the_error_bit(dev):
+    w = workloads.prefill_inputs([5, 4, 6], 6, seed=77)
+    w.cu_seqlens = torch.tensor([0, 5, 9, 3], dtype=torch.int32)  # sequence 2 runs backwards
+    wd = w.to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = gpu_prefill(wd, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == kda.KDA_ERR_SEQLENS
+    check_prefill(w, wd, out, err_expected=oracle.PREFILL_ERR_SEQLENS)
+    w.cu_seqlens = torch.tensor([0, 5, 9, 16], dtype=torch.int32)  # sequence 2 ends past the last row
+    wd = w.to(dev)
+    err.zero_()
+    out = gpu_prefill(wd, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == kda.KDA_ERR_SEQLENS
+    check_prefill(w, wd, out, err_expected=oracle.PREFILL_ERR_SEQLENS)
+
+
+def test_prefill_graph_replays_are_identical(dev):
+    w = workloads.prefill_inputs([12, 1, 30], 5, seed=78)
+    wd = w.to(dev)
+    st0 = wd.state.clone()
+    out = torch.empty((wd.q.shape[0], 12, 128), dtype=torch.bfloat16, device=dev)
+    fn = lambda: gpu_prefill(wd, out=out)  # noqa: E731
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    res = []
+    for _ in range(3):
+        wd.state.copy_(st0)
+        g.replay()
+        torch.cuda.synchronize()
+        res.append((out.view(torch.int16).clone(), wd.state.view(torch.int16).clone()))
+    for o, s in res[1:]:
+        assert torch.equal(o, res[0][0]) and torch.equal(s, res[0][1])
+
+
+def test_prefill_empty_calls(dev):
+    w = workloads.prefill_inputs([0, 0, 0], 4, seed=79)
+    wd = w.to(dev)
+    st0 = wd.state.clone()
+    out = torch.full((1, 12, 128), SENTINEL, dtype=torch.bfloat16, device=dev)
+    q = torch.zeros((0, 12, 128), dtype=torch.bfloat16, device=dev)
+    b = torch.zeros((0, 12), dtype=torch.bfloat16, device=dev)
+    kda.kda_prefill(wd.state, wd.state_indices, wd.cu_seqlens, q, q, q, q, b, wd.A_log, wd.dt_bias, out=out[:0])
+    w2 = workloads.prefill_inputs([4, 0, 2], 4, seed=80)
+    wd2 = w2.to(dev)
+    cu0 = torch.zeros(1, dtype=torch.int32, device=dev)
+    idx0 = torch.zeros(0, dtype=torch.int32, device=dev)
+    o2 = torch.full((6, 12, 128), SENTINEL, dtype=torch.bfloat16, device=dev)
+    kda.kda_prefill(wd2.state, idx0, cu0, wd2.q, wd2.k, wd2.v, wd2.g_raw, wd2.beta_logit, wd2.A_log, wd2.dt_bias,
+                    out=o2)
+    torch.cuda.synchronize()
+    assert torch.equal(wd.state, st0)
+    assert torch.all(o2.float() == SENTINEL), "no sequence: nothing written"
+    assert torch.equal(wd2.state, w2.state.to(dev))
+
+
+def test_prefill_rejects_bad_arguments(dev):
+    w = workloads.prefill_inputs([3, 2], 4, seed=81)
+    wd = w.to(dev)
+    with pytest.raises(kda.KdaError) as e:
+        gpu_prefill(wd, config_override=4)
+    assert e.value.status == kda.KDA_EUNSUPPORTED
+    with pytest.raises(TypeError):
+        kda.kda_prefill(wd.state, wd.state_indices, wd.cu_seqlens.long(), wd.q, wd.k, wd.v, wd.g_raw,
+                        wd.beta_logit, wd.A_log, wd.dt_bias)
+    with pytest.raises(ValueError):
+        kda.kda_prefill(wd.state, wd.state_indices[:1], wd.cu_seqlens, wd.q, wd.k, wd.v, wd.g_raw,
+                        wd.beta_logit, wd.A_log, wd.dt_bias)
