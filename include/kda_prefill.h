@@ -66,7 +66,7 @@ typedef struct {
 kda_status kda_prefill(const kda_params* p, const kda_seqs* s, void* stream);
 
 /* The configuration kda_prefill picks for num_seqs sequences of H heads
-   (an index for kda_config_tile_v: 0..3). */
+   (an index for kda_config_tile_v: 0..3); -1 for negative num_seqs or H < 1. */
 int32_t kda_select_prefill_config(int32_t num_seqs, int32_t H);
 
 #ifdef __cplusplus

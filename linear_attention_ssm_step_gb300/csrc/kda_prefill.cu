@@ -9,13 +9,13 @@
 // value rows of a head are independent given the per-token vectors, so a
 // sequence's head is split over 128 / TV CTAs, each repeating the per-token
 // prologue for its rows.
-//   1. Thread 0 reads cu_seqlens[i], cu_seqlens[i+1] and the slot; invalid
+//   1. Every thread reads cu_seqlens[i], cu_seqlens[i+1] and the slot; invalid
 //      bounds set KDA_ERR_SEQLENS, an inactive slot zeroes the out rows.
 //   2. Each warp starts one bulk copy of its TV/NW state rows (plain loads for
 //      a misaligned pool), which flies under the first chunk's prologue.
 //   3. Tokens go in chunks of 16: the chunk's prologue (q/k L2 norms, k.q,
 //      gate, beta: the verify kernel's warp-per-token prologue, the same bits)
-//      into shared memory; then every token in order on the rows, held in
+//      into shared memory, lane-major; then every token in order on the rows, held in
 //      fp32 registers for the whole sequence (8 lanes per row, 4 rows per
 //      warp access, the decode step's arithmetic without its rounding); the
 //      chunk's outputs leave as bf16 rows.
@@ -31,9 +31,73 @@ constexpr int PF_CHUNK = KDA_MAX_T;  // tokens per prologue chunk
 __host__ __device__ constexpr size_t prefill_smem_bytes(int TV) {
   return (size_t)TV * KD * 2                 // state tile
          + 128                               // mbarriers (up to 16 warps)
-         + (size_t)PF_CHUNK * KD * 4 * 4     // kh, qh, dd, gg
+         + (size_t)PF_CHUNK * KD * 4 * 3     // kh, qh, dd (lane-major)
          + (size_t)PF_CHUNK * TV * 4 * 2     // vrow, orow
          + (size_t)PF_CHUNK * 4 * 2;         // beta, kappa
+}
+
+// The token vectors (k_hat, q_hat, d) are stored lane-major: lane j's 16 keys
+// (8j..8j+7 and 64+8j..64+8j+7, four float4) sit in float4 slots j, 8+j, 16+j,
+// 24+j, so each of a lane's four 16-byte loads covers 128 contiguous bytes
+// across the 8 lanes of a row (no bank conflicts; the 4 rows of a warp access
+// read the same bytes). Position of key channel c:
+__device__ __forceinline__ int lane_major(int c) {
+  return ((2 * (c >> 6) + ((c & 7) >> 2)) * 8 + ((c >> 3) & 7)) * 4 + (c & 3);
+}
+
+// load_pairs8 (kda_device.cuh) from a lane-major vector: the same pairs.
+__device__ __forceinline__ void load_pairs8_lm(const float* v, int j, f32x2 (&out)[8]) {
+  const float4* a = reinterpret_cast<const float4*>(v);
+  const float4 a0 = a[j], a1 = a[8 + j], b0 = a[16 + j], b1 = a[24 + j];
+  out[0] = pk2(a0.x, a0.y);
+  out[1] = pk2(a0.z, a0.w);
+  out[2] = pk2(a1.x, a1.y);
+  out[3] = pk2(a1.z, a1.w);
+  out[4] = pk2(b0.x, b0.y);
+  out[5] = pk2(b0.z, b0.w);
+  out[6] = pk2(b1.x, b1.y);
+  out[7] = pk2(b1.z, b1.w);
+}
+
+// token_prologue (kda_device.cuh) with the same arithmetic, writing k_hat,
+// q_hat and d lane-major and no g (the prefill keeps no ring).
+template <int PT, int NW>
+__device__ __forceinline__ void token_prologue_lm(const kda_params& p, int h, int T, int TV, const TokenSmem& ts,
+                                                  const TokenLoads<PT>& L) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Gate gate(p, h);
+  float dtb[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dtb[i] = gate.dt_bias(p, h, lane + 32 * i);
+#pragma unroll
+  for (int s = 0; s < PT; ++s) {
+    const int t = warp + NW * s;
+    if (t < T) {
+      float qq[4], kk[4], qk[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        qq[i] = __fmul_rn(L.q[s][i], L.q[s][i]);
+        kk[i] = __fmul_rn(L.k[s][i], L.k[s][i]);
+        qk[i] = __fmul_rn(L.q[s][i], L.k[s][i]);
+      }
+      const float rq = inv_norm(sum_channels(qq[0], qq[1], qq[2], qq[3]));
+      const float rk = inv_norm(sum_channels(kk[0], kk[1], kk[2], kk[3]));
+      const float sqk = sum_channels(qk[0], qk[1], qk[2], qk[3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = lane + 32 * i, pos = t * KD + lane_major(c);
+        ts.dd[pos] = expf(gate.g(L.g[s][i], dtb[i]));
+        ts.qh[pos] = __fmul_rn(L.q[s][i], rq);
+        ts.kh[pos] = __fmul_rn(L.k[s][i], rk);
+        if (c < TV) ts.vrow[t * TV + c] = L.v[s][i];
+      }
+      if (lane == 0) {
+        ts.kappa[t] = __fmul_rn(__fmul_rn(sqk, rq), rk);
+        ts.beta[t] = gate.beta(L.bl[s]);
+      }
+    }
+  }
+  __syncthreads();
 }
 
 // The decode step (row_step in kda_device.cuh) on a row held in fp32: the same
@@ -78,8 +142,8 @@ __global__ void __launch_bounds__(32 * NW) kda_prefill_kernel(const kda_params p
   ts.kh = fbase;
   ts.qh = ts.kh + PF_CHUNK * KD;
   ts.dd = ts.qh + PF_CHUNK * KD;
-  ts.gg = ts.dd + PF_CHUNK * KD;
-  ts.vrow = ts.gg + PF_CHUNK * KD;
+  ts.gg = nullptr;  // no ring
+  ts.vrow = ts.dd + PF_CHUNK * KD;
   float* orow = ts.vrow + PF_CHUNK * TV;
   ts.beta = orow + PF_CHUNK * TV;
   ts.kappa = ts.beta + PF_CHUNK;
@@ -124,7 +188,7 @@ __global__ void __launch_bounds__(32 * NW) kda_prefill_kernel(const kda_params p
     const int T = min(PF_CHUNK, t1 - c0);
     TokenLoads<PT> L;
     prologue_issue<PT, NW>(p, c0, h, T, v0, TV, L);
-    token_prologue<PT, NW>(p, c0, h, T, v0, TV, ts, L);  // ends with __syncthreads
+    token_prologue_lm<PT, NW>(p, h, T, TV, ts, L);  // ends with __syncthreads
     if (c0 == t0) {  // the state rows, once: bf16 -> fp32 registers
       __syncwarp();
       if constexpr (BULK) ok = mbar_wait_bounded(&mbar[warp], 0);
@@ -136,9 +200,12 @@ __global__ void __launch_bounds__(32 * NW) kda_prefill_kernel(const kda_params p
       }
     }
     if (ok) {
+#pragma unroll 2
       for (int t = 0; t < T; ++t) {
         LaneVecs lv;
-        load_lane_vecs(ts, t, j, lv);
+        load_pairs8_lm(ts.kh + t * KD, j, lv.kh);
+        load_pairs8_lm(ts.qh + t * KD, j, lv.qh);
+        load_pairs8_lm(ts.dd + t * KD, j, lv.dd);
         const float beta = ts.beta[t], kappa = ts.kappa[t];
 #pragma unroll
         for (int q = 0; q < RQ; ++q) {

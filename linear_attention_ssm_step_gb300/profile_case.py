@@ -5,6 +5,9 @@ profilers (Nsight Compute) that need a short, clean stream of launches.
   python -m linear_attention_ssm_step_gb300.profile_case verify 512 --T 8
   python -m linear_attention_ssm_step_gb300.profile_case ring 512 --T 8 --fold 0.5
   python -m linear_attention_ssm_step_gb300.profile_case decode_fp8 512
+  python -m linear_attention_ssm_step_gb300.profile_case prefill 8 --len 2048
+
+For prefill, B is the number of sequences, each of --len tokens.
 
 Each call is launched --reps times (default 3) on the same inputs, with a
 device synchronize after each; nothing is timed here.
@@ -19,12 +22,14 @@ from . import kda, workloads
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("call", choices=["decode", "verify", "ring", "decode_fp8"])
+    ap.add_argument("call", choices=["decode", "verify", "ring", "decode_fp8", "prefill"])
     ap.add_argument("B", type=int)
     ap.add_argument("--T", type=int, default=8)
     ap.add_argument("--fold", type=float, default=0.0)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--config", type=int, default=-1)
+    ap.add_argument("--len", type=int, default=16, help="prefill: tokens per sequence")
+    ap.add_argument("--H", type=int, default=12, help="prefill: heads")
     a = ap.parse_args()
     dev = torch.device("cuda:0")
     kda.load_library()
@@ -37,6 +42,10 @@ def main():
         codes, scales = (t.to(dev) for t in workloads.fp8_pool(a.B + 128, seed=5))
         fn = lambda: kda.kda_decode_fp8(codes, scales, w.state_indices, w.q, w.k, w.v, w.g_raw,  # noqa: E731
                                         w.beta_logit, w.A_log, w.dt_bias, config_override=a.config)
+    elif a.call == "prefill":
+        w = workloads.prefill_inputs([a.len] * a.B, a.B + 8, seed=90 + a.B, layout="fused", H=a.H).to(dev)
+        fn = lambda: kda.kda_prefill(w.state, w.state_indices, w.cu_seqlens, w.q, w.k, w.v, w.g_raw,  # noqa: E731
+                                     w.beta_logit, w.A_log, w.dt_bias, config_override=a.config)
     elif a.call == "verify":
         w = workloads.decode_inputs(a.B, a.B + 64, seed=3, T=a.T).to(dev)
         fn = lambda: kda.kda_verify(w.state, w.state_indices, w.q, w.k, w.v, w.g_raw, w.beta_logit,  # noqa: E731
