@@ -56,6 +56,9 @@ def test_header_constants_match_binding():
         m = re.search(r"#define\s+" + name + r"\s+(\d+)u?", text)
         assert m, name
         assert int(m.group(1)) == getattr(kda, name), name
+    text = open(os.path.join(ROOT, "include", "kda_prefill.h")).read()
+    m = re.search(r"#define\s+KDA_ERR_SEQLENS\s+(\d+)u?", text)
+    assert m and int(m.group(1)) == kda.KDA_ERR_SEQLENS
 
 
 def test_struct_layout_matches_header(tmp_path):
@@ -65,11 +68,14 @@ def test_struct_layout_matches_header(tmp_path):
 #include <stdio.h>
 #include "kda.h"
 #include "kda_fp8.h"
+#include "kda_prefill.h"
 #define P(s, f) printf(#s "." #f " %zu\n", offsetof(s, f))
 int main(void) {
-  printf("kda_view %zu\nkda_params %zu\nkda_ring_params %zu\nkda_fp8_pool %zu\n",
-         sizeof(kda_view), sizeof(kda_params), sizeof(kda_ring_params), sizeof(kda_fp8_pool));
+  printf("kda_view %zu\nkda_params %zu\nkda_ring_params %zu\nkda_fp8_pool %zu\nkda_seqs %zu\n",
+         sizeof(kda_view), sizeof(kda_params), sizeof(kda_ring_params), sizeof(kda_fp8_pool),
+         sizeof(kda_seqs));
   P(kda_fp8_pool, scale); P(kda_fp8_pool, scale_slot_stride);
+  P(kda_seqs, cu_seqlens); P(kda_seqs, num_seqs);
   P(kda_params, q); P(kda_params, beta_logit); P(kda_params, A_log); P(kda_params, lower_bound);
   P(kda_params, state); P(kda_params, state_indices); P(kda_params, out); P(kda_params, out_h_stride);
   P(kda_params, error_word); P(kda_params, config_override); P(kda_params, gate_mode);
@@ -85,11 +91,12 @@ int main(void) {
     assert int(got["kda_params"]) == ctypes.sizeof(kda.KdaParams)
     assert int(got["kda_ring_params"]) == ctypes.sizeof(kda.KdaRingParams)
     assert int(got["kda_fp8_pool"]) == ctypes.sizeof(kda.KdaFp8Pool)
+    assert int(got["kda_seqs"]) == ctypes.sizeof(kda.KdaSeqs)
     for key, val in got.items():
         if "." in key:
             s, f = key.split(".")
             cls = {"kda_params": kda.KdaParams, "kda_ring_params": kda.KdaRingParams,
-                   "kda_fp8_pool": kda.KdaFp8Pool}[s]
+                   "kda_fp8_pool": kda.KdaFp8Pool, "kda_seqs": kda.KdaSeqs}[s]
             assert getattr(cls, f).offset == int(val), key
 
 
@@ -282,3 +289,29 @@ def test_fp8_decode_validation(lib):
     p.config_override = -1
     p.B = 0
     assert call(kda.KdaFp8Pool(p.state + (1 << 26), 12 * 128)) == kda.KDA_OK
+
+
+@no_gpu
+def test_prefill_validation(lib):
+    """kda_prefill rejects missing arguments, a negative sequence count, the
+    tensor-core configuration and an unaligned cu_seqlens; an empty call
+    launches nothing."""
+    p = fake_params()
+    call = lambda sq: lib.kda_prefill(ctypes.byref(p), None if sq is None else ctypes.byref(sq), None)  # noqa: E731
+    cu = (1 << 32) + 10 * (1 << 24)
+    assert lib.kda_prefill(None, ctypes.byref(kda.KdaSeqs(cu, 1)), None) == kda.KDA_EINVAL
+    assert call(None) == kda.KDA_EINVAL and "seqs" in kda.kda_last_error()
+    assert call(kda.KdaSeqs(cu, -1)) == kda.KDA_EINVAL and "num_seqs" in kda.kda_last_error()
+    assert call(kda.KdaSeqs(None, 2)) == kda.KDA_EINVAL and "cu_seqlens" in kda.kda_last_error()
+    assert call(kda.KdaSeqs(cu + 2, 2)) == kda.KDA_EINVAL and "cu_seqlens" in kda.kda_last_error()
+    p.config_override = 4
+    assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_EUNSUPPORTED
+    p.config_override = -1
+    p.K = 64
+    assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_EUNSUPPORTED
+    p.K = 128
+    assert call(kda.KdaSeqs(None, 0)) == kda.KDA_OK  # no sequence: nothing to do
+    p.B = 0
+    assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_OK  # no token rows: nothing launched
+    assert [lib.kda_select_prefill_config(s, 12) for s in (1, 8, 512)] == [2, 2, 2]
+    assert lib.kda_select_prefill_config(-1, 12) == -1 and lib.kda_select_prefill_config(1, 0) == -1

@@ -226,3 +226,31 @@ def test_prefill_rejects_bad_arguments(dev):
     with pytest.raises(ValueError):
         kda.kda_prefill(wd.state, wd.state_indices[:1], wd.cu_seqlens, wd.q, wd.k, wd.v, wd.g_raw,
                         wd.beta_logit, wd.A_log, wd.dt_bias)
+
+
+@pytest.mark.parametrize("S,L", [(512, 16), (64, 256)])
+def test_prefill_bench_shapes_sampled(dev, S, L):
+    """The bench's workloads in its launch configuration: 12 sampled sequences
+    against the oracle (outputs and final states), every other slot untouched
+    and every row written."""
+    w = workloads.prefill_inputs([L] * S, S + 8, seed=90 + S, layout="fused")
+    wd = w.to(dev)
+    out = gpu_prefill(wd)
+    torch.cuda.synchronize()
+    got_out, got_state = f64(out), f64(wd.state)
+    assert np.all(got_out != SENTINEL), "every row belongs to a sequence"
+    rng = np.random.default_rng(S)
+    picks = rng.choice(S, size=12, replace=False)
+    for i in picks:
+        rows = slice(i * L, (i + 1) * L)
+        n = int(w.state_indices[i])
+        ref_state, ref_out, _, err = oracle.kda_prefill(
+            f64(w.state[n:n + 1]), np.array([0]), np.array([0, L]), f64(w.q[rows]), f64(w.k[rows]),
+            f64(w.v[rows]), f64(w.g_raw[rows]), f64(w.beta_logit[rows]), f64(w.A_log), f64(w.dt_bias),
+            lower_bound=LB)
+        assert err == 0
+        assert_output_close(got_out[rows], ref_out, f"outputs of sequence {i}")
+        assert_state_close(got_state[n], ref_state[0], f"final state of sequence {i}", steps=L)
+    owned = set(int(x) for x in w.state_indices)
+    rest = [n for n in range(w.N) if n not in owned]
+    assert np.array_equal(got_state[rest], f64(w.state)[rest])
