@@ -1,4 +1,4 @@
-"""Algorithmic HBM bytes of the three calls: what the method must move, no more.
+"""Algorithmic HBM bytes of the calls: what the method must move, no more.
 
 "feat(kda): add packed-input CuTe decode kernel" (PR #4417), section "DRAM
 utilization": per step the decode reads and rewrites the whole bf16 state of
