@@ -254,3 +254,26 @@ def test_prefill_bench_shapes_sampled(dev, S, L):
     owned = set(int(x) for x in w.state_indices)
     rest = [n for n in range(w.N) if n not in owned]
     assert np.array_equal(got_state[rest], f64(w.state)[rest])
+
+
+def test_prefill_sixty_four_heads(dev):
+    """The largest head count the library takes."""
+    w = workloads.prefill_inputs([3, 18], 3, seed=82, H=64)
+    wd = w.to(dev)
+    out = gpu_prefill(wd)
+    torch.cuda.synchronize()
+    check_prefill(w, wd, out)
+
+
+def test_prefill_on_a_side_stream_same_bits(dev):
+    """Launched on a caller's stream: the same bits as on the current stream."""
+    w = workloads.prefill_inputs([11, 4, 27], 5, seed=83)
+    a, b = w.to(dev), w.to(dev)
+    oa = gpu_prefill(a)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        ob = gpu_prefill(b, stream=side)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
