@@ -277,3 +277,15 @@ def test_prefill_on_a_side_stream_same_bits(dev):
     torch.cuda.synchronize()
     assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
     assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+
+
+def test_prefill_empty_pool_writes_zeros(dev):
+    """N = 0: every sequence is inactive, its rows are zero, nothing else is read."""
+    w = workloads.prefill_inputs([4, 9], 2, seed=84)
+    wd = w.to(dev)
+    empty = torch.empty((0, 12, 128, 128), dtype=torch.bfloat16, device=dev)
+    out = torch.full((13, 12, 128), SENTINEL, dtype=torch.bfloat16, device=dev)
+    kda.kda_prefill(empty, wd.state_indices, wd.cu_seqlens, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit,
+                    wd.A_log, wd.dt_bias, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(out.float() == 0.0)
