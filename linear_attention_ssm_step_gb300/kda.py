@@ -390,6 +390,25 @@ def kda_prefill(state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_
     return out
 
 
+def prepare_prefill(state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
+                    lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
+                    stream=None):
+    """kda_prefill bound to these tensors (see PreparedCall); same arguments. The
+    sequence count is fixed by cu_seqlens' length; its contents may change."""
+    if out is None:
+        out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    if cu_seqlens.dim() != 1 or cu_seqlens.shape[0] < 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous [S + 1] tensor")
+    S = cu_seqlens.shape[0] - 1
+    p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
+                lower_bound, scale, error_word, config_override, gate_mode, n_indices=S)
+    sq = KdaSeqs(cu_seqlens.data_ptr(), S)
+    keep = (p, sq, state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias, error_word)
+    return PreparedCall(load_library().kda_prefill, (ctypes.byref(p), ctypes.byref(sq),
+                                                     _stream_handle(stream, q.device)), out, keep)
+
+
 def kda_select_prefill_config(num_seqs, H=12):
     return int(load_library().kda_select_prefill_config(num_seqs, H))
 

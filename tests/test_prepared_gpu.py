@@ -58,3 +58,24 @@ def test_prepared_decode_fp8(dev):
                                    a.dt_bias)
         torch.cuda.synchronize()
         assert torch.equal(out_a, out_b) and torch.equal(ca, cb) and torch.equal(sa, sb)
+
+
+def test_prepared_prefill(dev):
+    """Bound once; refilling the bound input buffers between calls (new tokens of
+    the same sequence lengths) gives the direct call's bits."""
+    w = workloads.prefill_inputs([7, 0, 19], 5, seed=703, inactive_frac=0.3)
+    w2 = workloads.prefill_inputs([7, 0, 19], 5, seed=704)
+    a, b = w.to(dev), w.to(dev)
+    call = kda.prepare_prefill(a.state, a.state_indices, a.cu_seqlens, a.q_sep, a.k_sep, a.v_sep, a.g_raw,
+                               a.beta_logit, a.A_log, a.dt_bias)
+    for step in range(2):
+        if step == 1:  # the next step's token inputs, into the bound buffers
+            for name in ("q_sep", "k_sep", "v_sep", "g_raw", "beta_logit"):
+                getattr(a, name).copy_(getattr(w2, name))
+                getattr(b, name).copy_(getattr(w2, name))
+        out_a = call()
+        out_b = kda.kda_prefill(b.state, b.state_indices, b.cu_seqlens, b.q, b.k, b.v, b.g_raw, b.beta_logit,
+                                b.A_log, b.dt_bias)
+        torch.cuda.synchronize()
+        assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+        assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
