@@ -25,6 +25,8 @@ carries:
                tokens (H = 12) and two shapes of the prefill page (H = 16,
                1 x 16384; H = 4, lengths 1..15), each with its median and
                10th/90th percentiles.
+               streaming_reference: a plain PyTorch in-place multiply over the
+               headline state's bytes, the same flush (context for the roofline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-sweep]
 
@@ -368,6 +370,15 @@ def sweep(dev, steps=100, warmup=100):
         row["us_warm_16step_graph"] = round(tw * 1e3, 2)
         res["t1_decode"].append(row)
         del w, wd
+    # Context for the decode's roofline: a plain streaming kernel (PyTorch's
+    # in-place elementwise multiply) over the bytes of the headline's state
+    # (486 active rows: read and written once), behind the same flush.
+    x = torch.ones(486 * traffic.STATE_BYTES // 2, dtype=torch.bfloat16, device=dev)
+    t = statistics.median(time_calls(graphed(lambda: x.mul_(1.0)), steps, warmup, before=flush))
+    nb = 2 * x.numel() * 2
+    res["streaming_reference"] = {"what": "torch in-place bf16 multiply, read + write once, graph replay",
+                                  "bytes": nb, "us": round(t * 1e3, 2), "GB/s": round(nb / t / 1e6, 1)}
+    del x
     # T=1 decode on an fp8 (E4M3) pool with per-row power-of-two scales: the
     # same activations, half the state bytes (all rows active, pool B+128)
     res["t1_decode_fp8_state"] = []
