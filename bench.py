@@ -15,6 +15,10 @@ carries:
                and its output copied back, all inside one timed region,
                pipelined over two buffer sets (the pool stays resident);
   roofline     the decode kernel's achieved GB/s against the measured HBM peak;
+  warm         the headline call in a steady decode loop (16 chained calls in
+               one graph, no flush), per call, with its fraction of the peak;
+  t8           the metric's T = 8 half at B = 512: verify and ring (W = 32,
+               0/50/100% folding), us, GB/s and fraction of the peak;
   cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload,
                on one core and on all host cores;
   sweep        T=1 decode at B = 1..2048, L2-cold per call and warm in 16-step
@@ -24,7 +28,8 @@ carries:
                varlen prefill at 1 x 4096, 8 x 2048, 64 x 256 and 512 x 16
                tokens (H = 12) and two shapes of the prefill page (H = 16,
                1 x 16384; H = 4, lengths 1..15), each with its median and
-               10th/90th percentiles.
+               10th/90th percentiles, and (state GB/s points) the fraction
+               of the measured HBM peak.
                streaming_reference: a plain PyTorch in-place multiply over the
                headline state's bytes, the same flush (context for the roofline).
 
@@ -272,8 +277,12 @@ def headline(dev, steps, warmup, world, rank):
     with ClockSampler(dev) as clk:
         times = time_calls(replay, steps, warmup, before=flush, world=world)
     total_ms = max_over_ranks(sum(times), world, dev)
+    # Steady state beside the cold figure: 16 consecutive calls on the same batch
+    # (the state chained in place) in one CUDA graph, no flush between them.
+    loop = graphed(lambda: [decode_call(wd, out)() for _ in range(16)])
+    warm_ms = statistics.median(time_calls(loop, max(10, steps // 4), warmup)) / 16
     return dict(w=w, wd=wd, out=out, times=times, total_ms=total_ms, nbytes=nbytes, clocks=clk.summary(),
-                active=act, flush=flush)
+                active=act, flush=flush, warm_ms=warm_ms)
 
 
 def e2e(dev, h, steps, warmup, world):
@@ -350,7 +359,7 @@ def sweep(dev, steps=100, warmup=100):
     """Each point: the median (and 10th/90th percentiles) of `steps` timed calls
     after `warmup` untimed ones (100 and 100: the pages' protocol)."""
     flush = L2Flush(dev)
-    res = {"t1_decode": [], "t8_verify": [], "t8_ring_w32": []}  # more keys added below
+    res = {"t1_decode": []}  # more keys added below
     for B in (1, 8, 16, 32, 64, 128, 256, 512, 1024, 2048):
         w = workloads.decode_inputs(B, B + 128, seed=10 + B, layout="fused")
         wd = w.to(dev)
@@ -409,16 +418,7 @@ def sweep(dev, steps=100, warmup=100):
         res["t1_decode_precomputed_gate"].append({"B": B, "us": round(t * 1e3, 2),
                                                   "GB/s": round(traffic.decode_bytes(B) / t / 1e6, 1)})
         del w, wd
-    for B in (1, 32, 512):
-        w = workloads.decode_inputs(B, B + 64, seed=20 + B, T=8)
-        wd = w.to(dev)
-        out = torch.empty((B, 8, 12, 128), dtype=torch.bfloat16, device=dev)
-        fn = lambda: kda.kda_verify(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
-                                    wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
-        us, p10, p90 = spread(time_calls(graphed(fn), steps, warmup, before=flush))
-        nb = traffic.verify_bytes(B, 8)
-        res["t8_verify"].append({"B": B, "us": us, "us_p10": p10, "us_p90": p90, "GB/s": round(nb / us / 1e3, 1)})
-        del w, wd
+    res["t8_verify"] = t8_verify_points(dev, (1, 32, 512), steps, warmup, flush)
     # varlen prefill (kda_prefill): S sequences of equal length packed row after
     # row, each filling its own slot; L2 flushed before each call
     # (the last two are shapes of the prefill page's portfolio: H16 with one
@@ -446,8 +446,35 @@ def sweep(dev, steps=100, warmup=100):
                                "us_p90": p90, "Mtokens/s": round(toks / us, 3),
                                "TFLOP/s": round(flops / us / 1e6, 2), "config": kda.kda_select_prefill_config(S, Hh)})
         del w, wd, st0, out
-    res["t8_ring_w16"] = []  # the pages' own ring width for T = 8, at the serving batch
-    for B, W in [(1, 32), (32, 32), (512, 32), (512, 16)]:
+    res["t8_ring_w32"] = t8_ring_points(dev, [(1, 32), (32, 32), (512, 32)], steps, warmup, flush)
+    # the pages' own ring width for T = 8, at the serving batch
+    res["t8_ring_w16"] = t8_ring_points(dev, [(512, 16)], steps, warmup, flush)
+    add_fractions(res)
+    return res
+
+
+def t8_verify_points(dev, Bs, steps, warmup, flush):
+    """T = 8 kda_verify at each B (pool B + 64, all rows active), L2 emptied before every call."""
+    pts = []
+    for B in Bs:
+        w = workloads.decode_inputs(B, B + 64, seed=20 + B, T=8)
+        wd = w.to(dev)
+        out = torch.empty((B, 8, 12, 128), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_verify(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
+                                    wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
+        us, p10, p90 = spread(time_calls(graphed(fn), steps, warmup, before=flush))
+        nb = traffic.verify_bytes(B, 8)
+        pts.append({"B": B, "us": us, "us_p10": p10, "us_p90": p90, "GB/s": round(nb / us / 1e3, 1),
+                    "config": kda.kda_select_config(B, 8)})
+        del w, wd
+    return pts
+
+
+def t8_ring_points(dev, cases, steps, warmup, flush):
+    """T = 8 kda_verify_ring, flush_min = 9, for each (B, W) at 0 / 50 / 100 % of rows
+    folding; the pool, the ring and hist_len restored and L2 emptied before every call."""
+    pts = []
+    for B, W in cases:
         for fold in (0.0, 0.5, 1.0):
             w = workloads.ring_inputs(B, B + 64, T=8, W=W, flush_min=9, fold_frac=fold, seed=30 + B)
             wd = w.to(dev)
@@ -469,10 +496,40 @@ def sweep(dev, steps=100, warmup=100):
             idx = w.state_indices.to(torch.int64)
             hists = [int(w.ring["hist_len"][n]) for n in idx]
             nb = traffic.ring_bytes(hists, 8, 9)
-            res["t8_ring_w%d" % W].append({"B": B, "fold": fold, "us": us, "us_p10": p10, "us_p90": p90,
-                                            "GB/s": round(nb / us / 1e3, 1)})
+            pts.append({"B": B, "W": W, "fold": fold, "us": us, "us_p10": p10, "us_p90": p90,
+                        "GB/s": round(nb / us / 1e3, 1)})
             del w, wd, saved, st0
-    return res
+    return pts
+
+
+def add_fractions(res):
+    """Every sweep point with a state GB/s also gets its fraction of the measured HBM peak."""
+    peak, _ = measured_peak()
+    for key, pts in res.items():
+        if not isinstance(pts, list):
+            continue
+        for pt in pts:
+            if "GB/s" in pt and key != "prefill":
+                pt["frac"] = round(pt["GB/s"] / peak, 4)
+
+
+def t8_summary(dev, sweep_res, steps=100, warmup=100):
+    """The metric's T = 8 half at the serving batch: verify and the ring (W = 32) at
+    B = 512, 0 / 50 / 100 % folding, with their fractions of the measured HBM peak.
+    Taken from the sweep when it ran, else measured here."""
+    peak, kind = measured_peak()
+    if sweep_res is not None:
+        ver = [p for p in sweep_res["t8_verify"] if p["B"] == 512]
+        ring = [p for p in sweep_res["t8_ring_w32"] if p["B"] == 512]
+    else:
+        flush = L2Flush(dev)
+        ver = t8_verify_points(dev, (512,), steps, warmup, flush)
+        ring = t8_ring_points(dev, [(512, 32)], steps, warmup, flush)
+    keep = lambda p: {k: p[k] for k in ("B", "fold", "us", "GB/s") if k in p}  # noqa: E731
+    return {"verify": [dict(keep(p), frac=round(p["GB/s"] / peak, 4)) for p in ver],
+            "ring_w32": [dict(keep(p), frac=round(p["GB/s"] / peak, 4)) for p in ring],
+            "peak": peak, "peak_kind": f"{kind} HBM copy bandwidth",
+            "how": "one CUDA-graph replay per call, L2 emptied (and the ring restored) before each, median of 100"}
 
 
 def _oracle_chunk_worker(path, n_iter, q):
@@ -608,13 +665,20 @@ def run_gpu(args):
                      "achieved": round(per_launch_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(per_launch_gbs / peak, 4), "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "traffic": profiled_traffic(), "algorithmic_bytes": h["nbytes"]},
+        "warm": {"us_per_step": round(h["warm_ms"] * 1e3, 2),
+                 "GB/s": round(h["nbytes"] / h["warm_ms"] / 1e6, 1),
+                 "frac": round(h["nbytes"] / h["warm_ms"] / 1e6 / peak, 4),
+                 "how": "16 consecutive kda_decode calls on the headline batch, state chained in place, captured "
+                        "as one CUDA graph, no L2 flush; median over replays, per call"},
         "gpu_launches": args.steps,
         "clocks": h["clocks"],
         "context_b200_pages": {"B512_direct_us": 63.82, "B512_effective_TBps": 6.43,
                                "note": "B200 numbers from the pages, no inactive rows; context only"},
     }
-    if not args.no_sweep:
-        line["sweep"] = sweep(dev)
+    sw = None if args.no_sweep else sweep(dev)
+    line["t8"] = t8_summary(dev, sw)
+    if sw is not None:
+        line["sweep"] = sw
     line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
 

@@ -69,7 +69,9 @@ typedef enum {
 
 /* Bits a kernel ORs into the optional device error word (kda_params.error_word). */
 #define KDA_ERR_HIST_LEN 1u /* a ring slot's hist_len was outside [0, W]; that slot was skipped */
-#define KDA_ERR_TIMEOUT 2u  /* a bounded wait for an async copy gave up; that tile was skipped */
+#define KDA_ERR_TIMEOUT 2u  /* a bounded wait (1 s) for an async copy gave up; that tile was skipped: zero
+                               output, its state (and ring entries) untouched; a ring call still resets
+                               hist_len of rows that reached flush_min (stream-ordered, unaware of the skip) */
 #define KDA_ERR_CACHE_BASE 4u /* a ring slot's cache_base was outside [0, W); that slot was skipped */
 
 /* kda_params.gate_mode: how g_raw and beta_logit are read (source: PR #4417, "T=1 fast path
@@ -189,18 +191,36 @@ typedef struct {
  */
 kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params* r, void* stream);
 
-/* Launch configurations: index -> rows of V per CTA (tile). kda_params.config_override
-   takes an index. 0-3: CUDA-core tiles of 16, 32, 64 and 128 rows; 4: whole heads with the
-   dot products on the tensor cores, kda_verify with T > 1 only (KDA_EUNSUPPORTED otherwise). */
+/*
+ * Launch configurations and the per-batch selector (source: PR #4417,
+ * "Kernel design", the per-batch policy bullet: the decode picks its kernel
+ * shape and value-row tile from the batch size, smaller tiles for small
+ * batches and whole-head tiles once the batch fills the GPU, and a tile_v
+ * override forces one for sweeps; the thresholds here are this library's own,
+ * measured on GB300). kda_params.config_override takes an index. 0-3:
+ * CUDA-core tiles of 16, 32, 64 and 128 value rows per CTA; 4: whole heads with
+ * the dot products on the tensor cores, kda_verify with T > 1 only
+ * (KDA_EUNSUPPORTED otherwise).
+ *   kda_num_configs:   the number of configurations (5).
+ *   kda_config_tile_v: rows of V per CTA of a configuration; -1 outside 0..4.
+ * Pure host functions: no device, no CUDA call.
+ */
 int32_t kda_num_configs(void);
 int32_t kda_config_tile_v(int32_t config);
 /* The configuration kda_decode (T = 1) and kda_verify (T > 1) pick for B rows
-   (-1 if B < 0 or T is outside 1..KDA_MAX_T). */
+   (same source; -1 if B < 0 or T is outside 1..KDA_MAX_T). */
 int32_t kda_select_config(int32_t B, int32_t T);
-/* The configuration kda_verify_ring picks for B rows and T tokens: always 3, whole heads (-1 as above). */
+/* The configuration kda_verify_ring picks for B rows and T tokens (same source):
+   always 3, whole heads, because the ring kernel's product takes all 128 state
+   rows of a head at once (-1 as above). */
 int32_t kda_select_ring_config(int32_t B, int32_t T);
 
-/* Message for the last non-OK status returned on this host thread ("" if none). */
+/* Message for the last non-OK status returned on this host thread ("" if none),
+   the error convention every call above follows: a kda_status return value for
+   host-side validation and launch, and this thread-local text beside it (source:
+   PR #4417, review comments asking that tile overrides and arguments be checked
+   before launch and rejected with a clear configuration error rather than reach
+   the kernel). The pointer stays valid until the next call on the same thread. */
 const char* kda_last_error(void);
 
 #ifdef __cplusplus

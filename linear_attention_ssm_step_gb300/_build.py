@@ -41,25 +41,46 @@ def _inputs():
     return files
 
 
-def is_stale():
-    if not os.path.exists(LIB_PATH):
+# Builds of the same sources for tests only, by name: their own library file
+# and object folder, extra compiler definitions. "waittest" is the
+# failure-detection build: every asynchronous global -> shared copy is left
+# unissued and the bounded waits give up after 2 ms, so each kernel's timeout
+# path runs without a fault (kda_device.cuh, KDA_WITHHOLD_LOADS).
+VARIANTS = {
+    "waittest": ["-DKDA_WITHHOLD_LOADS", "-DKDA_WAIT_LIMIT_NS=2000000ull"],
+}
+
+
+def lib_path(variant=None):
+    if variant is None:
+        return LIB_PATH
+    return os.path.join(PKG_DIR, f"libkda_gb300_{variant}.so")
+
+
+def is_stale(variant=None):
+    path = lib_path(variant)
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force=False, verbose=False):
-    """Compile and link libkda_gb300.so; returns its path."""
-    if not force and not is_stale():
-        return LIB_PATH
+def build(force=False, verbose=False, variant=None):
+    """Compile and link libkda_gb300.so (or a test variant of it); returns its path."""
+    path = lib_path(variant)
+    if not force and not is_stale(variant):
+        return path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    bdir = BUILD_DIR if variant is None else os.path.join(BUILD_DIR, variant)
+    extra = [] if variant is None else VARIANTS[variant]
+    os.makedirs(bdir, exist_ok=True)
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [nvcc] + CFLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = ([nvcc] + CFLAGS + extra + (["-Xptxas", "-v"] if verbose else []) +
+               ["-c", os.path.join(CSRC, src), "-o", obj])
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
     failed = []
     for src, p in procs:
@@ -70,13 +91,13 @@ def build(force=False, verbose=False):
             failed.append((src, out))
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(f"--- {s}\n{o}" for s, o in failed))
-    tmp = LIB_PATH + ".tmp"
+    tmp = path + ".tmp"
     link = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path
 
 
 if __name__ == "__main__":

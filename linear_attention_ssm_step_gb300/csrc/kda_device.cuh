@@ -31,9 +31,26 @@ constexpr int NWARPS = NTHREADS / 32;
 constexpr float L2_EPS = 1e-6f;
 
 // Bounded waits: a wait that has not finished after this long gives up, sets
-// KDA_ERR_TIMEOUT and skips its tile instead of hanging the GPU.
-constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // 1 s
+// KDA_ERR_TIMEOUT and skips its tile instead of hanging the GPU. The library
+// uses 1 s; the failure-detection test build (KDA_WITHHOLD_LOADS below) sets a
+// few milliseconds.
+#ifndef KDA_WAIT_LIMIT_NS
+#define KDA_WAIT_LIMIT_NS 1000000000ull
+#endif
+constexpr unsigned long long WAIT_LIMIT_NS = KDA_WAIT_LIMIT_NS;
 constexpr unsigned WAIT_LIMIT_ITERS = 1u << 28;
+
+// KDA_WITHHOLD_LOADS is defined only in the failure-detection test build of
+// the library: there every asynchronous global -> shared copy (bulk and
+// tensor-map loads) is left unissued while its mbarrier still expects the
+// bytes, so the kernel's wait on it runs out as on a copy that never lands,
+// with nothing in flight, and the timeout path (error bit, skipped tile,
+// zero output, state untouched) runs.
+#ifdef KDA_WITHHOLD_LOADS
+constexpr bool kWithholdLoads = true;
+#else
+constexpr bool kWithholdLoads = false;
+#endif
 
 // ---------------------------------------------------------------- PTX wrappers
 
@@ -80,9 +97,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// After a bounded wait gave up: one more bounded wait on the same phase, so
+// that a copy still in flight lands before the CTA leaves and its shared
+// memory goes to another CTA.
+__device__ __forceinline__ void mbar_drain_bounded(uint64_t* bar, uint32_t parity) {
+  (void)mbar_wait_bounded(bar, parity);
+}
+
 // Bulk copy global -> shared, completing `bytes` of transaction count on `bar`.
 // src and dst 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {
+  if constexpr (kWithholdLoads) return;
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_addr(dst_smem)),

@@ -268,7 +268,10 @@ __global__ void __launch_bounds__(NTHREADS, 5)
       for (int i = lane; i < RW; i += 32) gsc[i] = ssw[i];
     }
   } else {
-    if (lane == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+    if (lane == 0) {
+      if (p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+      if constexpr (BULK) mbar_drain_bounded(&mbar[warp], 0);
+    }
     for (int i = lane; i < RW; i += 32) orow[hrow0 + i] = 0.0f;
   }
   __syncthreads();

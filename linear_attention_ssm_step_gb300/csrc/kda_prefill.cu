@@ -195,8 +195,9 @@ __global__ void __launch_bounds__(32 * NW) kda_prefill_kernel(const kda_params p
       if (ok) {
 #pragma unroll
         for (int q = 0; q < RQ; ++q) row_to_f32(load_row_bf16(sst + (ROWS_PER_WARP * q + r) * KD, j), a[q]);
-      } else if (lane == 0 && p.error_word != nullptr) {
-        atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+      } else if (lane == 0) {
+        if (p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+        if constexpr (BULK) mbar_drain_bounded(&mbar[warp], 0);
       }
     }
     if (ok) {

@@ -168,7 +168,10 @@ __global__ void __launch_bounds__(32 * NW, MULTI ? (NW == 8 ? 2 : 1) : 6)
       for (int i = lane; i < RW * KD; i += 32) gst[i] = sst[i];
     }
   } else {
-    if (lane == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+    if (lane == 0) {
+      if (p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+      if constexpr (BULK) mbar_drain_bounded(&mbar[warp], 0);
+    }
     for (int i = lane; i < T * RW; i += 32) {
       const int t = i / RW, rr = i - t * RW;
       orow[t * TV + warp * RW + rr] = 0.0f;

@@ -21,6 +21,7 @@ namespace kda {
 
 // 3-D tiled load into shared memory, completing its bytes on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  if constexpr (kWithholdLoads) return;  // failure-detection test build (kda_device.cuh)
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
           "r"(smem_addr(dst)),

@@ -95,19 +95,23 @@ def lib_path():
     return _build.LIB_PATH
 
 
+def bind_library(path):
+    """Open a build of the library at `path` with the C signatures of EXPORTS set."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in EXPORTS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
 def load_library():
     """Load libkda_gb300.so (built by __graft_entry__.build()); raise if it is absent."""
     global _lib
     if _lib is None:
-        path = lib_path()
-        if not os.path.exists(path):
-            raise RuntimeError(f"{path} is not built; run __graft_entry__.build() first")
-        lib = ctypes.CDLL(path)
-        for name, (args, res) in EXPORTS.items():
-            fn = getattr(lib, name)
-            fn.argtypes = args
-            fn.restype = res
-        _lib = lib
+        _lib = bind_library(lib_path())
     return _lib
 
 

@@ -1,14 +1,18 @@
-"""kda_verify (T tokens) on the GPU: against the oracle, and bit for bit
-against T chained kda_decode calls (the CUDA-core configurations 0-3). The
-tensor-core configuration (4) sums the dot products in another order: it
-matches the oracle and chained decodes within the multi-step tolerances, and
-is bitwise deterministic on its own."""
+"""kda_verify (T tokens) on the GPU: against the oracle token by token, and
+bit for bit against T chained kda_decode calls (the CUDA-core configurations
+0-3). Every state comparison is per element at the single-step bound: the
+oracle step for token t starts from the GPU's own state after t tokens
+(harness.verify_teacher_forced). The tensor-core configuration (4) sums the
+dot products in another order than the CUDA-core ones: each of its tokens is
+held to that bound against the oracle, and against one GPU decode step from
+its own previous state; it is bitwise deterministic on its own."""
 
 import numpy as np
 import pytest
 import torch
 
-from harness import assert_output_close, assert_state_close, f64, gpu_decode, gpu_verify, oracle_verify
+from harness import (assert_output_close, assert_state_close, decode_token, f64, gpu_decode, gpu_verify,
+                     identity_tokens, token_slice, verify_teacher_forced)
 from linear_attention_ssm_step_gb300 import kda, workloads
 
 TC = 4  # the tensor-core configuration
@@ -26,17 +30,13 @@ def dev():
 
 
 def check_verify(w, dev, rows=None, **kw):
-    wd = w.to(dev)
-    out = gpu_verify(wd, **kw)
+    wd, out, _ = verify_teacher_forced(w, dev, rows=rows, **kw)
     torch.cuda.synchronize()
-    sub = w if rows is None else w.select_rows(rows)
-    ref_state, ref_out = oracle_verify(sub)
-    got_out = f64(out) if rows is None else f64(out)[rows]
-    idx = sub.state_indices.numpy().astype(np.int64)
-    active = (idx >= 0) & (idx < w.N)
-    assert (got_out[~active] == 0).all()
-    assert_output_close(got_out, ref_out)
-    assert_state_close(f64(wd.state)[idx[active]], ref_state[idx[active]], steps=w.T)
+    if rows is None:  # slots no active row owns are untouched
+        idx = w.state_indices.numpy().astype(np.int64)
+        owned = set(idx[(idx >= 0) & (idx < w.N)].tolist())
+        rest = [n for n in range(w.N) if n not in owned]
+        assert torch.equal(wd.state.cpu()[rest].view(torch.int16), w.state[rest].view(torch.int16))
     return wd, out
 
 
@@ -74,18 +74,46 @@ def test_verify_large_batch_sampled(dev):
     check_verify(w, dev, rows=rows)
 
 
-def test_verify_tensor_cores_match_chained_decodes(dev):
+def test_verify_tensor_cores_match_decode_steps(dev):
+    """Configuration 4 token by token against the GPU's own T = 1 decode: the
+    state after t + 1 tokens of a tensor-core verify equals one kda_decode step
+    from its state after t tokens to the single-step bound, and so do the
+    outputs to theirs. (The two sum the dot products in different orders.)"""
     T = 8
     w = workloads.decode_inputs(7, 20, seed=408, T=T, inactive_frac=0.15, layout="packed")
-    wd = w.to(dev)
-    out_v = gpu_verify(wd, config_override=TC)
-    wc = w.to(dev)
-    outs = [gpu_decode(_token(wc, t)) for t in range(T)]
-    torch.cuda.synchronize()
     idx = w.state_indices.numpy().astype(np.int64)
     act = idx[(idx >= 0) & (idx < w.N)]
-    assert_state_close(f64(wd.state)[act], f64(wc.state)[act], steps=T)
-    assert_output_close(f64(out_v), f64(torch.stack(outs, dim=1)))
+    wd = w.to(dev)
+    out_v = gpu_verify(wd, config_override=TC)
+    for t in range(T):
+        if t == 0:
+            pre = w.to(dev)
+        else:
+            pre = (identity_tokens(token_slice(w, 0, 2), 1) if t == 1 else token_slice(w, 0, t)).to(dev)
+            gpu_verify(pre, config_override=TC)
+        nxt = wd if t == T - 1 else (identity_tokens(token_slice(w, 0, 2), 1) if t == 0 else
+                                      token_slice(w, 0, t + 1)).to(dev)
+        if t < T - 1:
+            gpu_verify(nxt, config_override=TC)
+        step = decode_token(w, t).to(dev)
+        step.state = pre.state
+        out_d = gpu_decode(step)
+        torch.cuda.synchronize()
+        assert_state_close(f64(nxt.state)[act], f64(pre.state)[act], f"token {t}: verify against a decode step")
+        assert_output_close(f64(out_v)[:, t], f64(out_d), f"token {t} output")
+
+
+def test_identity_token_leaves_the_tensor_core_state_unchanged(dev):
+    """The one-token prefix of the teacher-forced checks pads configuration 4 with
+    an identity token: a trailing identity token changes no state bit."""
+    w = workloads.decode_inputs(5, 12, seed=409, T=3, inactive_frac=0.2)
+    a = identity_tokens(w, 2).to(dev)
+    b = token_slice(w, 0, 2).to(dev)
+    oa = gpu_verify(a, config_override=TC)
+    ob = gpu_verify(b, config_override=TC)
+    torch.cuda.synchronize()
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+    assert torch.equal(oa[:, :2].view(torch.int16), ob.view(torch.int16))
 
 
 def test_verify_tensor_cores_serving_batch_512_sampled(dev):
