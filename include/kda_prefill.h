@@ -15,7 +15,7 @@
  *   (rounded to bf16) to out row t, and keeps S in fp32 for the next token.
  *   After the last token, S is rounded to bf16 (round to nearest even) once
  *   and stored in the slot. A one-token sequence is exactly one kda_decode
- *   step, bit for bit.
+ *   step: bit for bit in configurations 0-3, to rounding in configuration 4.
  *
  * The activations are kda_decode's T = 1 views with one row per token:
  * q, k, v, g_raw bf16 [B][H][128] and beta_logit bf16 [B][H], B = the total
@@ -26,8 +26,16 @@
  *     outside [0, N) makes the sequence inactive: its out rows are zero and
  *     the pool is not touched;
  *   - B == 0 or num_seqs == 0 launches nothing;
- *   - config_override is -1 (the library chooses) or 0..3, the value-row tile
- *     of kda_config_tile_v(); configuration 4 is not a prefill configuration.
+ *   - config_override is -1 (the library chooses: 4), 0..3 (the recurrence
+ *     token by token on the CUDA cores, value-row tiles of kda_config_tile_v())
+ *     or 4 (chunks of 16 tokens with the chunk math on the tensor cores, the
+ *     page's BT16 chunked form: per chunk, every value row's dot products with
+ *     the chunk's decayed keys and queries as one product, a 16-step scalar
+ *     recurrence per row, and the state update as a second product onto the
+ *     fp32 state held in tensor memory; its products take the fp32 operands
+ *     as bf16 parts: the state and the vectors to about 2^-17 relative in the
+ *     dot products, u and the decayed keys to about 2^-24 in the update).
+ *     Both compute the reading above; they round differently within fp32.
  *
  * cu_seqlens is a DEVICE int32 array [num_seqs + 1], read only by the kernel
  * (the host never reads device memory). Sequence i is skipped, and
@@ -58,15 +66,16 @@ typedef struct {
 
 /*
  * Varlen prefill: every sequence of s, in place on its slot (the reading
- * above). Host-side validation: p and s non-NULL, num_seqs >= 0 and
- * config_override != 4; with num_seqs > 0, kda_decode's checks with T = 1 and
+ * above). Host-side validation: p and s non-NULL, num_seqs >= 0; with
+ * num_seqs > 0, kda_decode's checks with T = 1 (config_override -1..4) and
  * cu_seqlens non-NULL and 4-byte aligned (KDA_EINVAL or KDA_EUNSUPPORTED
  * otherwise).
  */
 kda_status kda_prefill(const kda_params* p, const kda_seqs* s, void* stream);
 
-/* The configuration kda_prefill picks for num_seqs sequences of H heads
-   (an index for kda_config_tile_v: 0..3); -1 for negative num_seqs or H < 1. */
+/* The configuration kda_prefill picks for num_seqs sequences of H heads: 4, the
+   chunked tensor-core kernel (source: PR #4605, Description: the BT16 chunked
+   backend); -1 for negative num_seqs or H < 1. */
 int32_t kda_select_prefill_config(int32_t num_seqs, int32_t H);
 
 #ifdef __cplusplus

@@ -14,9 +14,11 @@
 namespace kda {
 // T=1 decode on an fp8 pool (kda_fp8.cu); tile_v and bulk as launch_step's.
 cudaError_t launch_decode_fp8(const kda_params& p, const kda_fp8_pool& f, int tile_v, bool bulk, cudaStream_t s);
-// Varlen prefill (kda_prefill.cu): num_seqs * H * (128 / tile_v) CTAs.
+// Varlen prefill token by token on the CUDA cores (kda_prefill.cu): num_seqs * H * (128 / tile_v) CTAs.
 cudaError_t launch_prefill(const kda_params& p, const int32_t* cu, int num_seqs, int tile_v, bool bulk,
                            cudaStream_t s);
+// Varlen prefill in chunks of 16 tokens on the tensor cores (kda_prefill_tc.cu), persistent.
+cudaError_t launch_prefill_tc(const kda_params& p, const int32_t* cu, int num_seqs, bool bulk, cudaStream_t s);
 }  // namespace kda
 
 namespace {
@@ -166,15 +168,14 @@ int32_t kda_select_ring_config(int32_t B, int32_t T) {
   return kRingConfig;  // 128 rows
 }
 
-// Prefill: every (sequence, head) runs its tokens in order, so the grid is
-// num_seqs * H * (128 / TV) CTAs whatever the lengths. Measured on GB300
-// (H = 12: 1 x 4096, 8 x 2048, 16 x 1024, 64 x 256, 512 x 16 tokens; H = 4:
-// lengths 1..15; every configuration): 64-row tiles (8 warps, two 4-row groups
-// each, two tokens of each chunk's prologue per warp) were fastest or within
-// 4 % of it in every case, also where fewer CTAs than SMs run.
+// Prefill: the chunked kernel on the tensor cores (configuration 4) does the
+// per-token work of a 16-token chunk as two products and a 16-step scalar
+// recurrence per value row, instead of 16 passes over the state; the
+// token-by-token CUDA-core kernel (configurations 0-3, of which 64-row tiles
+// were the fastest on every shape measured) stays selectable.
 int32_t kda_select_prefill_config(int32_t num_seqs, int32_t H) {
   if (num_seqs < 0 || H < 1) return -1;
-  return 2;  // 64 rows
+  return kTensorCoreConfig;
 }
 
 const char* kda_last_error(void) { return g_err; }
@@ -243,8 +244,6 @@ kda_status kda_prefill(const kda_params* p, const kda_seqs* sq, void* stream) {
   if (p == nullptr) return fail(KDA_EINVAL, "params is NULL");
   if (sq == nullptr) return fail(KDA_EINVAL, "seqs is NULL");
   if (sq->num_seqs < 0) return fail(KDA_EINVAL, "num_seqs = %d is negative", sq->num_seqs);
-  if (p->config_override == kTensorCoreConfig)
-    return fail(KDA_EUNSUPPORTED, "config_override = %d is not a prefill configuration (0..3)", kTensorCoreConfig);
   if (sq->num_seqs == 0) return ok();  // nothing to read or write (state_indices may be empty)
   bool bulk = false;
   kda_status s = check_params(p, 1, &bulk);
@@ -256,8 +255,9 @@ kda_status kda_prefill(const kda_params* p, const kda_seqs* sq, void* stream) {
   if ((long long)sq->num_seqs * p->H * (128 / kTileV[cfg]) > 0x7fffffffLL)
     return fail(KDA_EUNSUPPORTED, "num_seqs * H = %lld is too large for one launch",
                 (long long)sq->num_seqs * p->H);
-  cudaError_t e = kda::launch_prefill(*p, sq->cu_seqlens, sq->num_seqs, kTileV[cfg], bulk,
-                                      static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cfg == kTensorCoreConfig ? kda::launch_prefill_tc(*p, sq->cu_seqlens, sq->num_seqs, bulk, st)
+                                           : kda::launch_prefill(*p, sq->cu_seqlens, sq->num_seqs, kTileV[cfg], bulk, st);
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_prefill launch: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -293,9 +293,9 @@ def test_fp8_decode_validation(lib):
 
 @no_gpu
 def test_prefill_validation(lib):
-    """kda_prefill rejects missing arguments, a negative sequence count, the
-    tensor-core configuration and an unaligned cu_seqlens; an empty call
-    launches nothing."""
+    """kda_prefill rejects missing arguments, a negative sequence count, a
+    configuration index past the last and an unaligned cu_seqlens; an empty
+    call launches nothing; the selector picks the chunked tensor-core kernel."""
     p = fake_params()
     call = lambda sq: lib.kda_prefill(ctypes.byref(p), None if sq is None else ctypes.byref(sq), None)  # noqa: E731
     cu = (1 << 32) + 10 * (1 << 24)
@@ -304,8 +304,8 @@ def test_prefill_validation(lib):
     assert call(kda.KdaSeqs(cu, -1)) == kda.KDA_EINVAL and "num_seqs" in kda.kda_last_error()
     assert call(kda.KdaSeqs(None, 2)) == kda.KDA_EINVAL and "cu_seqlens" in kda.kda_last_error()
     assert call(kda.KdaSeqs(cu + 2, 2)) == kda.KDA_EINVAL and "cu_seqlens" in kda.kda_last_error()
-    p.config_override = 4
-    assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_EUNSUPPORTED
+    p.config_override = 5
+    assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_EINVAL and "config_override" in kda.kda_last_error()
     p.config_override = -1
     p.K = 64
     assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_EUNSUPPORTED
@@ -313,5 +313,5 @@ def test_prefill_validation(lib):
     assert call(kda.KdaSeqs(None, 0)) == kda.KDA_OK  # no sequence: nothing to do
     p.B = 0
     assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_OK  # no token rows: nothing launched
-    assert [lib.kda_select_prefill_config(s, 12) for s in (1, 8, 512)] == [2, 2, 2]
+    assert [lib.kda_select_prefill_config(s, 12) for s in (1, 8, 512)] == [4, 4, 4]
     assert lib.kda_select_prefill_config(-1, 12) == -1 and lib.kda_select_prefill_config(1, 0) == -1

@@ -12,7 +12,12 @@ What is compared:
     side of a boundary (harness module docstring);
   * rows of inactive sequences: exactly zero; rows no valid sequence covers
     and slots no active sequence owns: bit for bit unchanged;
-  * one-token sequences against kda_decode on the same rows: bit for bit.
+  * one-token sequences against kda_decode on the same rows: bit for bit on
+    the CUDA cores (configurations 0-3), to the single-step bound in the
+    chunked tensor-core configuration (4, the default), whose products round
+    differently;
+  * the chunked kernel at chunk boundaries, against the token-by-token one,
+    and with more (sequence, head) items than its persistent grid has CTAs.
 """
 
 import numpy as np
@@ -80,7 +85,7 @@ def check_prefill(w, wd, out, scale=1.0, err_expected=0):
 LENGTHS = [1, 17, 0, 40, 5, 16, 33, 2]
 
 
-@pytest.mark.parametrize("config", [-1, 0, 1, 2, 3])
+@pytest.mark.parametrize("config", [-1, 0, 1, 2, 3, 4])
 def test_prefill_matches_oracle(dev, config):
     w = workloads.prefill_inputs(LENGTHS, 12, seed=70 + config, inactive_frac=0.25, layout="fused")
     wd = w.to(dev)
@@ -114,17 +119,76 @@ def test_prefill_long_sequence(dev):
     check_prefill(w, wd, out)
 
 
-def test_single_token_sequences_equal_decode_bit_for_bit(dev):
-    """A prefill of one-token sequences is one decode step per slot."""
+@pytest.mark.parametrize("config", [0, 2, 3])
+def test_single_token_sequences_equal_decode_bit_for_bit(dev, config):
+    """On the CUDA cores (configurations 0-3) a prefill of one-token sequences
+    is one decode step per slot, bit for bit."""
     B = 37
     w = workloads.prefill_inputs([1] * B, B + 20, seed=74, inactive_frac=0.1, layout="fused")
     a, b = w.to(dev), w.to(dev)
-    out_p = gpu_prefill(a)
+    out_p = gpu_prefill(a, config_override=config)
     out_d = kda.kda_decode(b.state, b.state_indices, b.q, b.k, b.v, b.g_raw, b.beta_logit, b.A_log, b.dt_bias,
                            lower_bound=LB)
     torch.cuda.synchronize()
     assert torch.equal(out_p.view(torch.int16), out_d.view(torch.int16))
     assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+
+
+def test_single_token_sequences_chunked_match_decode(dev):
+    """The chunked tensor-core kernel on one-token sequences: one decode step
+    per slot to the single-step bound (its products round differently), and
+    against the oracle."""
+    B = 37
+    w = workloads.prefill_inputs([1] * B, B + 20, seed=74, inactive_frac=0.1, layout="fused")
+    a, b = w.to(dev), w.to(dev)
+    out_p = gpu_prefill(a, config_override=4)
+    out_d = kda.kda_decode(b.state, b.state_indices, b.q, b.k, b.v, b.g_raw, b.beta_logit, b.A_log, b.dt_bias,
+                           lower_bound=LB)
+    torch.cuda.synchronize()
+    idx = w.state_indices.numpy().astype(np.int64)
+    act = idx[(idx >= 0) & (idx < w.N)]
+    assert_output_close(f64(out_p), f64(out_d))
+    assert_state_close(f64(a.state)[act], f64(b.state)[act], "chunked one-token prefill against a decode step")
+    check_prefill(w, a, out_p)
+
+
+@pytest.mark.parametrize("lengths", [[15, 16, 17], [31, 32, 33, 48], [47, 64, 1, 2]])
+def test_prefill_chunk_boundaries(dev, lengths):
+    """Sequences that end just before, on and just after a 16-token chunk
+    boundary, in the chunked kernel and in the token-by-token one."""
+    for config in (4, 2):
+        w = workloads.prefill_inputs(lengths, len(lengths) + 3, seed=85 + sum(lengths) + config)
+        wd = w.to(dev)
+        out = gpu_prefill(wd, config_override=config)
+        torch.cuda.synchronize()
+        check_prefill(w, wd, out)
+
+
+def test_prefill_chunked_against_token_by_token(dev):
+    """The two kernels compute the same reading with different fp32 rounding:
+    their outputs within the output tolerance of each other and their states
+    within the prefill bound."""
+    lens = [200, 7, 64, 129]
+    w = workloads.prefill_inputs(lens, 8, seed=86, layout="packed")
+    a, b = w.to(dev), w.to(dev)
+    oa = gpu_prefill(a, config_override=4)
+    ob = gpu_prefill(b, config_override=2)
+    torch.cuda.synchronize()
+    assert_output_close(f64(oa), f64(ob))
+    for i, n in enumerate(w.state_indices.tolist()):
+        assert_prefill_state_close(f64(a.state)[n], f64(b.state)[n], lens[i], f"sequence {i}")
+
+
+def test_prefill_many_sequences_per_cta(dev):
+    """More (sequence, head) items than the persistent grid has CTAs, with mixed
+    lengths and inactive sequences: 400 sequences of 0..40 tokens at H = 4."""
+    rng = np.random.default_rng(87)
+    lens = [int(x) for x in rng.integers(0, 41, 400)]
+    w = workloads.prefill_inputs(lens, 420, seed=87, H=4, inactive_frac=0.1)
+    wd = w.to(dev)
+    out = gpu_prefill(wd)
+    torch.cuda.synchronize()
+    check_prefill(w, wd, out)
 
 
 def test_prefill_configs_agree_bit_for_bit(dev):
@@ -140,7 +204,9 @@ def test_prefill_configs_agree_bit_for_bit(dev):
         assert torch.equal(o, res[0][0]) and torch.equal(s, res[0][1])
 
 
-def test_prefill_misaligned_pool_same_bits(dev):
+@pytest.mark.parametrize("config", [2, 4])
+def test_prefill_misaligned_pool_same_bits(dev, config):
+    """A 2-byte aligned pool takes plain loads and stores: the same bits."""
     w = workloads.prefill_inputs([6, 21], 4, seed=76)
     a, b = w.to(dev), w.to(dev)
     flat = torch.empty(b.state.numel() + 8, dtype=torch.bfloat16, device=dev)
@@ -148,7 +214,7 @@ def test_prefill_misaligned_pool_same_bits(dev):
     mis.copy_(b.state)
     assert mis.data_ptr() % 16 == 2
     b.state = mis
-    oa, ob = gpu_prefill(a), gpu_prefill(b)
+    oa, ob = gpu_prefill(a, config_override=config), gpu_prefill(b, config_override=config)
     torch.cuda.synchronize()
     assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
     assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
@@ -218,8 +284,8 @@ def test_prefill_rejects_bad_arguments(dev):
     w = workloads.prefill_inputs([3, 2], 4, seed=81)
     wd = w.to(dev)
     with pytest.raises(kda.KdaError) as e:
-        gpu_prefill(wd, config_override=4)
-    assert e.value.status == kda.KDA_EUNSUPPORTED
+        gpu_prefill(wd, config_override=5)
+    assert e.value.status == kda.KDA_EINVAL
     with pytest.raises(TypeError):
         kda.kda_prefill(wd.state, wd.state_indices, wd.cu_seqlens.long(), wd.q, wd.k, wd.v, wd.g_raw,
                         wd.beta_logit, wd.A_log, wd.dt_bias)
