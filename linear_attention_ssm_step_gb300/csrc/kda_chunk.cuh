@@ -151,4 +151,62 @@ __device__ __forceinline__ void load_tokens(const kda_params& p, int b, int h, i
   }
 }
 
+// The gate of the chunk kernels (ring verify, chunked prefill): the formulas
+// of Gate with the fast exponential (__expf) and the approximate reciprocal.
+// Their relative errors, a few 1e-7 (g to about 5 x 2^-22 absolute, so the
+// decay exp(g) to about 2^-20 relative), stay inside the tolerances of G, the
+// decays, u~ and the prefill state; the ring's history weights and fold keep
+// the IEEE exponential.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+struct FastGate {
+  bool raw;
+  float a_h, lower_bound;
+  __device__ __forceinline__ FastGate(const kda_params& p, float alog) {
+    raw = p.gate_mode == KDA_GATE_RAW;
+    a_h = raw ? __expf(alog) : 0.0f;
+    lower_bound = p.lower_bound;
+  }
+  __device__ __forceinline__ float g(float g_in, float dtb) const {
+    if (!raw) return g_in;
+    const float z = __fmul_rn(a_h, __fadd_rn(g_in, dtb));
+    return __fmul_rn(lower_bound, rcp_approx(__fadd_rn(1.0f, __expf(-z))));
+  }
+  __device__ __forceinline__ float beta(float b_in) const {
+    return raw ? rcp_approx(__fadd_rn(1.0f, __expf(-b_in))) : b_in;
+  }
+};
+
+// 16 fp32 values x[0..15] (K = 0..15) of row `row` of a K-major operand with
+// the 32-byte swizzle (sw32_offset, R = 128) as three bf16 parts `part` bytes
+// apart: x0 = bf16(x), x1 = bf16(x - x0), x2 = bf16(x - x0 - x1) as
+// store_split3 forms them, each part's row in two 16-byte stores.
+__device__ __forceinline__ void store_row_split3(unsigned char* base, uint32_t part, int row, const float (&x)[16]) {
+  uint32_t w0[8], w1[8], w2[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float a = x[2 * q], b = x[2 * q + 1];
+    w0[q] = pack_bf16x2(a, b);
+    float a0, b0;
+    unpack_bf16x2(w0[q], a0, b0);
+    const float ra = __fsub_rn(a, a0), rb = __fsub_rn(b, b0);
+    w1[q] = pack_bf16x2(ra, rb);
+    float a1, b1;
+    unpack_bf16x2(w1[q], a1, b1);
+    w2[q] = pack_bf16x2(__fsub_rn(ra, a1), __fsub_rn(rb, b1));
+  }
+  const uint32_t sw = ((uint32_t)row >> 2) & 1u;
+  const uint32_t o0 = (uint32_t)row * 32u + (sw << 4), o1 = (uint32_t)row * 32u + ((1u ^ sw) << 4);
+  *reinterpret_cast<uint4*>(base + o0) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+  *reinterpret_cast<uint4*>(base + o1) = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+  *reinterpret_cast<uint4*>(base + part + o0) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+  *reinterpret_cast<uint4*>(base + part + o1) = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+  *reinterpret_cast<uint4*>(base + 2 * part + o0) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+  *reinterpret_cast<uint4*>(base + 2 * part + o1) = make_uint4(w2[4], w2[5], w2[6], w2[7]);
+}
+
 }  // namespace kda

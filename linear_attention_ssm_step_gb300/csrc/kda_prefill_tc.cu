@@ -198,14 +198,14 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
 
       // Per channel tid: the normalised vectors, the gate (tokens past the
       // chunk's end: decay 1, beta 0, zero vectors), P_t and the B operand.
-      const Gate gate(p, L.alog, true);
+      const FastGate gate(p, L.alog);
       if (tid < PC) sbeta[tid] = tid < Tc ? gate.beta(bf16_bits_to_float(L.blogit)) : 0.0f;
       float qh[PC], kh[PC], dd[PC];
 #pragma unroll
       for (int t = 0; t < PC; ++t) {
         qh[t] = __fmul_rn(bf16_bits_to_float(L.qv[t]), rn[t]);
         kh[t] = __fmul_rn(bf16_bits_to_float(L.kv[t]), rn[PC + t]);
-        dd[t] = t < Tc ? expf(gate.g(bf16_bits_to_float(L.gv[t]), L.dtb)) : 1.0f;
+        dd[t] = t < Tc ? __expf(gate.g(bf16_bits_to_float(L.gv[t]), L.dtb)) : 1.0f;
       }
       {
         float P = 1.0f;
@@ -381,11 +381,16 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
             ce[2 * s2] = pk2(c.x, c.y);
             ce[2 * s2 + 1] = pk2(c.z, c.w);
           }
-          f32x2 acc2 = pk2(0.0f, 0.0f);
+          f32x2 acc_e = pk2(0.0f, 0.0f), acc_o = pk2(0.0f, 0.0f);  // two chains: half the latency
 #pragma unroll
-          for (int s2 = 0; s2 < t; ++s2) acc2 = fma2(ce[s2], uu[s2], acc2);
+          for (int s2 = 0; s2 < t; ++s2) {
+            if (s2 & 1)
+              acc_o = fma2(ce[s2], uu[s2], acc_o);
+            else
+              acc_e = fma2(ce[s2], uu[s2], acc_e);
+          }
           float acc, acco, xk, xq, ctt, ect;
-          upk2(acc2, acc, acco);
+          upk2(add2(acc_e, acc_o), acc, acco);
           upk2(X[t], xk, xq);
           upk2(ce[t], ctt, ect);
           (void)ctt;
@@ -400,11 +405,8 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
 
       // 5. U (row tid) and W (channel tid) as three bf16 parts; the update product
       // accumulates sum_j u_j W_j onto P_{C-1} S_0 in tensor memory.
-#pragma unroll
-      for (int j = 0; j < PC; ++j) {
-        store_split3(sU, PC_UW_PART, tid, j, uval[j]);
-        store_split3(sW, PC_UW_PART, tid, j, Wk[j]);
-      }
+      store_row_split3(sU, PC_UW_PART, tid, uval);
+      store_row_split3(sW, PC_UW_PART, tid, Wk);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncthreads();

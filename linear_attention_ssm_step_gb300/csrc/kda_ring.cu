@@ -129,34 +129,6 @@ __device__ __forceinline__ int64_t ring_row(int cb, int pos, int W) {
   return (int64_t)(r >= W ? r - W : r) * KD;
 }
 
-// The gate of the ring kernel: the formulas of Gate with the fast exponential
-// (__expf) and the approximate reciprocal. Their relative errors, a few 1e-7,
-// stay far below the tolerances of G, the decays and u~; the history weights
-// and the fold keep the IEEE exponential.
-__device__ __forceinline__ float rcp_approx(float x) {
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
-struct RingGate {
-  bool raw;
-  float a_h, lower_bound;
-  __device__ __forceinline__ RingGate(const kda_params& p, float alog) {
-    raw = p.gate_mode == KDA_GATE_RAW;
-    a_h = raw ? __expf(alog) : 0.0f;
-    lower_bound = p.lower_bound;
-  }
-  __device__ __forceinline__ float g(float g_in, float dtb) const {
-    if (!raw) return g_in;
-    const float z = __fmul_rn(a_h, __fadd_rn(g_in, dtb));
-    return __fmul_rn(lower_bound, rcp_approx(__fadd_rn(1.0f, __expf(-z))));
-  }
-  __device__ __forceinline__ float beta(float b_in) const {
-    return raw ? rcp_approx(__fadd_rn(1.0f, __expf(-b_in))) : b_in;
-  }
-};
-
 // Persistent: CTA c works on items (b, h) = c, c + gridDim.x, ... (item = b H + h).
 // While item i computes, the slot index and hist_len of item i+1 are read;
 // once item i's product has read the checkpoint buffer, the copy of item
@@ -280,7 +252,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
         for (int r = 0; r < KD; ++r)
           *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, tid)) = gstate[(int64_t)r * KD + tid];
       }
-      const RingGate gate(p, L.alog);
+      const FastGate gate(p, L.alog);
       if (tid < TT) sbeta[tid] = tid < T ? gate.beta(bf16_bits_to_float(L.blogit)) : 0.0f;
 
       // L2 norms: block sums of q_t^2 (value t) and k_t^2 (value TT + t), then
