@@ -14,14 +14,21 @@
 // tensor memory. The update and the rounding are the CUDA-core kernel's, per
 // element, so only the order of the dot products' sums differs from it.
 //
-// One CTA of 128 threads per (batch row, head): thread v owns value row v
-// (held in registers as bf16 pairs) and key channel v.
+// One CTA of 128 threads per (batch row, head). Thread v is key channel v in
+// the per-channel work and reads value row v's sums from tensor memory; in the
+// per-row work each thread owns a tile of 16 value rows x 8 keys of the state
+// (held in registers as bf16 pairs): lane l of warp w takes rows
+// 32 w + 16 (l / 16) .. + 15 and keys 8 (l % 16) .. + 7, so a warp holds
+// whole rows 32 w .. 32 w + 31, the rows whose sums it reads.
 //   1. slot index; the state arrives by two tensor-map loads into the
 //      K-major, 128-byte-swizzled layout of the A operand; the per-token
 //      prologue (the CUDA-core verify's, the same bits) runs meanwhile;
 //   2. per token: each thread writes its channel of the B operand; one thread
-//      issues 8 tcgen05.mma; each row thread reads its sums, computes u and
-//      o, updates its row in registers and writes it back to the A operand;
+//      issues 8 tcgen05.mma; each thread waits for the product itself, reads
+//      its row's sums and computes u and o for that row; u goes to its warp's
+//      shared-memory slot; each thread updates its tile with the u of its 16
+//      rows and the decay and key of its 8 channels, and writes the tile back
+//      to the A operand (one CTA barrier per token, before the product);
 //   3. the final rows leave by two tensor-map stores.
 #include <cuda.h>
 
@@ -39,7 +46,7 @@ constexpr uint32_t VT_TMEM_COLS = 32;
 
 // Shared-memory carve-up (bytes from a 1024-aligned base) for TT token slots.
 struct VerifyLayout {
-  uint32_t a, b, kh, qh, dd, vrow, beta, kappa, bar, tslot, total;
+  uint32_t a, b, kh, qh, dd, vrow, beta, kappa, su, bar, tslot, total;
 };
 
 __host__ __device__ inline VerifyLayout verify_layout(int TT) {
@@ -62,6 +69,8 @@ __host__ __device__ inline VerifyLayout verify_layout(int TT) {
   o += KDA_MAX_T * 4u;
   L.kappa = o;
   o += KDA_MAX_T * 4u;
+  L.su = o;  // per-warp slots of the rows' u
+  o += 128u * 4u;
   L.bar = o;
   o += 16u;
   L.tslot = o;
@@ -151,16 +160,19 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   ok = __syncthreads_and(ok) != 0;
   if (!ok && tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
 
-  // Row tid of the state, in registers: 16 chunks of 8 keys, 4 bf16 pairs each.
-  uint32_t rw[64];
+  // This thread's tile: rows r0 .. r0 + 15, keys 8 kg .. 8 kg + 7 (4 bf16 pairs per row).
+  const int lane = tid & 31, kg = lane & 15;
+  const int r0 = warp * 32 + (lane >> 4) * 16;
+  uint32_t rw[16][4];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const uint4 c = *reinterpret_cast<const uint4*>(sA + sw128_offset(KD, tid, 8 * i));
-    rw[4 * i] = c.x;
-    rw[4 * i + 1] = c.y;
-    rw[4 * i + 2] = c.z;
-    rw[4 * i + 3] = c.w;
+    const uint4 c = *reinterpret_cast<const uint4*>(sA + sw128_offset(KD, r0 + i, 8 * kg));
+    rw[i][0] = c.x;
+    rw[i][1] = c.y;
+    rw[i][2] = c.z;
+    rw[i][3] = c.w;
   }
+  float* su = reinterpret_cast<float*>(sm + SL.su) + warp * 32;  // u of rows 32 warp .. + 31
 
   bool pendD = false;  // a product is in flight, issued with parity pend_par
   uint32_t pend_par = 0;
@@ -170,10 +182,10 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
       const float d = ts.dd[t * KD + tid];
       store_split3_b(sB, 0, tid, __fmul_rn(d, ts.kh[t * KD + tid]));
       store_split3_b(sB, 1, tid, __fmul_rn(d, ts.qh[t * KD + tid]));
-      fence_proxy_async_smem();  // B and the rows written back are read by the tensor core
+      fence_proxy_async_smem();  // B and the tiles written back are read by the tensor core
     }
     tc_fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(ok) != 0;
     float o = 0.0f;
     if (ok) {
       if (tid == 0) {
@@ -188,47 +200,63 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
       }
       pendD = true;
       pend_par = (uint32_t)(t & 1);
-      ok = __syncthreads_and(mbar_wait_bounded(barD, pend_par)) != 0;
+      ok = mbar_wait_bounded(barD, pend_par);  // every thread waits for the product itself
       if (!ok) {
-        if (tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+        if (p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
       } else {
         pendD = false;
         tc_fence_after();
+        // Row tid's sums: x and y in three parts each, then u and o of the row.
         float c[8];
         tmem_ld8(row_tmem, c);
         const float x = __fadd_rn(__fadd_rn(c[0], c[2]), c[4]);
         const float y = __fadd_rn(__fadd_rn(c[1], c[3]), c[5]);
         const float u = __fmul_rn(ts.beta[t], __fsub_rn(ts.vrow[t * KD + tid], x));
         o = __fmul_rn(p.scale, __fmaf_rn(u, ts.kappa[t], y));
-        // s <- bf16(d * s + k_hat u), in registers and in the A operand.
-        const f32x2 uu = pk2(u, u);
-        const float* dv = ts.dd + t * KD;
-        const float* kv = ts.kh + t * KD;
+        su[lane] = u;
+      }
+    }
+    __syncwarp();
+    if (ok) {
+      // The tile: s <- bf16(d * s + k_hat u), in registers and in the A operand.
+      const float* dv = ts.dd + t * KD + 8 * kg;
+      const float* kv = ts.kh + t * KD + 8 * kg;
+      const float4 d0 = *reinterpret_cast<const float4*>(dv);
+      const float4 d1 = *reinterpret_cast<const float4*>(dv + 4);
+      const float4 k0 = *reinterpret_cast<const float4*>(kv);
+      const float4 k1 = *reinterpret_cast<const float4*>(kv + 4);
+      const f32x2 dp0 = pk2(d0.x, d0.y), dp1 = pk2(d0.z, d0.w), dp2 = pk2(d1.x, d1.y), dp3 = pk2(d1.z, d1.w);
+      const f32x2 kp0 = pk2(k0.x, k0.y), kp1 = pk2(k0.z, k0.w), kp2 = pk2(k1.x, k1.y), kp3 = pk2(k1.z, k1.w);
+      const float4* uq = reinterpret_cast<const float4*>(su + (lane & 16));
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float4 d0 = *reinterpret_cast<const float4*>(dv + 8 * i);
-          const float4 d1 = *reinterpret_cast<const float4*>(dv + 8 * i + 4);
-          const float4 k0 = *reinterpret_cast<const float4*>(kv + 8 * i);
-          const float4 k1 = *reinterpret_cast<const float4*>(kv + 8 * i + 4);
-          f32x2 a0 = mul2(pk2(d0.x, d0.y), bf16x2_to_f32x2(rw[4 * i]));
-          f32x2 a1 = mul2(pk2(d0.z, d0.w), bf16x2_to_f32x2(rw[4 * i + 1]));
-          f32x2 a2 = mul2(pk2(d1.x, d1.y), bf16x2_to_f32x2(rw[4 * i + 2]));
-          f32x2 a3 = mul2(pk2(d1.z, d1.w), bf16x2_to_f32x2(rw[4 * i + 3]));
-          a0 = fma2(pk2(k0.x, k0.y), uu, a0);
-          a1 = fma2(pk2(k0.z, k0.w), uu, a1);
-          a2 = fma2(pk2(k1.x, k1.y), uu, a2);
-          a3 = fma2(pk2(k1.z, k1.w), uu, a3);
-          rw[4 * i] = f32x2_to_bf16x2(a0);
-          rw[4 * i + 1] = f32x2_to_bf16x2(a1);
-          rw[4 * i + 2] = f32x2_to_bf16x2(a2);
-          rw[4 * i + 3] = f32x2_to_bf16x2(a3);
-          *reinterpret_cast<uint4*>(sA + sw128_offset(KD, tid, 8 * i)) =
-              make_uint4(rw[4 * i], rw[4 * i + 1], rw[4 * i + 2], rw[4 * i + 3]);
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 u4 = uq[i4];
+        const float ur[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+        for (int i1 = 0; i1 < 4; ++i1) {
+          const int i = 4 * i4 + i1;
+          const f32x2 uu = pk2(ur[i1], ur[i1]);
+          f32x2 a0 = mul2(dp0, bf16x2_to_f32x2(rw[i][0]));
+          f32x2 a1 = mul2(dp1, bf16x2_to_f32x2(rw[i][1]));
+          f32x2 a2 = mul2(dp2, bf16x2_to_f32x2(rw[i][2]));
+          f32x2 a3 = mul2(dp3, bf16x2_to_f32x2(rw[i][3]));
+          a0 = fma2(kp0, uu, a0);
+          a1 = fma2(kp1, uu, a1);
+          a2 = fma2(kp2, uu, a2);
+          a3 = fma2(kp3, uu, a3);
+          rw[i][0] = f32x2_to_bf16x2(a0);
+          rw[i][1] = f32x2_to_bf16x2(a1);
+          rw[i][2] = f32x2_to_bf16x2(a2);
+          rw[i][3] = f32x2_to_bf16x2(a3);
+          *reinterpret_cast<uint4*>(sA + sw128_offset(KD, r0 + i, 8 * kg)) =
+              make_uint4(rw[i][0], rw[i][1], rw[i][2], rw[i][3]);
         }
       }
     }
     outp[obase + (int64_t)t * p.out_t_stride] = ok ? float_to_bf16_bits(o) : (uint16_t)0;
   }
+  ok = __syncthreads_and(ok) != 0;
+  if (!ok && tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
 
   // The final rows: a tensor-map store of the A operand, or plain stores.
   if (ok) {
