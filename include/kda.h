@@ -46,8 +46,8 @@
  *   - `out` must not overlap the state pool or any input.
  *   - The calls are deterministic: the same inputs give the same bits across
  *     CUDA-graph replays, and whatever the CUDA-core launch configuration
- *     (0-3); the verify configurations 4 and 5 sum the dot products in other
- *     orders and agree with them to rounding.
+ *     (0-3); the tensor-core verify configuration (4) sums the dot products
+ *     in another order and agrees with them to rounding.
  *   - Arithmetic is fp32 with fp32 CUDA math functions; the state and the
  *     outputs are rounded to bf16 (round to nearest even) when stored.
  */
@@ -199,13 +199,10 @@ kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params
  * override forces one for sweeps; the thresholds here are this library's own,
  * measured on GB300). kda_params.config_override takes an index. 0-3:
  * CUDA-core tiles of 16, 32, 64 and 128 value rows per CTA; 4: whole heads with
- * the dot products on the tensor cores; 5: whole heads on the CUDA cores, each
- * token's two dot products computed in the previous token's update pass on
- * the rounded values (8-row x 8-key tiles per thread, the row sums reduced
- * within a warp). 4 and 5 are kda_verify configurations with T > 1 only
- * (KDA_EUNSUPPORTED otherwise; kda_prefill takes 4 for its chunked kernel).
- *   kda_num_configs:   the number of configurations (6).
- *   kda_config_tile_v: rows of V per CTA of a configuration; -1 outside 0..5.
+ * the dot products on the tensor cores, kda_verify with T > 1 only
+ * (KDA_EUNSUPPORTED otherwise).
+ *   kda_num_configs:   the number of configurations (5).
+ *   kda_config_tile_v: rows of V per CTA of a configuration; -1 outside 0..4.
  * Pure host functions: no device, no CUDA call.
  */
 int32_t kda_num_configs(void);

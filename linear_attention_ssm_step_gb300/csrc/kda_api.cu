@@ -17,8 +17,6 @@ cudaError_t launch_decode_fp8(const kda_params& p, const kda_fp8_pool& f, int ti
 // Varlen prefill token by token on the CUDA cores (kda_prefill.cu): num_seqs * H * (128 / tile_v) CTAs.
 cudaError_t launch_prefill(const kda_params& p, const int32_t* cu, int num_seqs, int tile_v, bool bulk,
                            cudaStream_t s);
-// T-token verify, dot products fused into the update pass (kda_verify_fused.cu).
-cudaError_t launch_verify_fused(const kda_params& p, int T, bool bulk, cudaStream_t s);
 // Varlen prefill in chunks of 16 tokens on the tensor cores (kda_prefill_tc.cu), persistent.
 cudaError_t launch_prefill_tc(const kda_params& p, const int32_t* cu, int num_seqs, bool bulk, cudaStream_t s);
 }  // namespace kda
@@ -41,12 +39,9 @@ kda_status ok() {
 }
 
 // Rows of V per CTA, by configuration index. Configuration 4 runs whole heads
-// with the dot products on the tensor cores (T > 1 only; the prefill's chunked
-// kernel); configuration 5 whole heads on the CUDA cores with each token's dot
-// products fused into the previous token's update (T > 1 only).
-constexpr int kTileV[] = {16, 32, 64, 128, 128, 128};
+// with the dot products on the tensor cores (T > 1 only).
+constexpr int kTileV[] = {16, 32, 64, 128, 128};
 constexpr int kTensorCoreConfig = 4;
-constexpr int kFusedConfig = 5;
 constexpr int kNumConfigs = sizeof(kTileV) / sizeof(kTileV[0]);
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -189,8 +184,8 @@ kda_status kda_decode(const kda_params* p, void* stream) {
   bool bulk = false;
   kda_status s = check_params(p, 1, &bulk);
   if (s != KDA_OK) return s;
-  if (p->config_override == kTensorCoreConfig || p->config_override == kFusedConfig)
-    return fail(KDA_EUNSUPPORTED, "config_override = %d (a verify configuration) needs T > 1", p->config_override);
+  if (p->config_override == kTensorCoreConfig)
+    return fail(KDA_EUNSUPPORTED, "config_override = %d (tensor-core verify) needs T > 1", kTensorCoreConfig);
   if (p->B == 0) return ok();
   cudaError_t e = kda::launch_step(*p, 1, kTileV[pick_config(p, 1)], bulk, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_decode launch: %s", cudaGetErrorString(e));
@@ -201,13 +196,12 @@ kda_status kda_verify(const kda_params* p, int32_t T, void* stream) {
   bool bulk = false;
   kda_status s = check_params(p, T, &bulk);
   if (s != KDA_OK) return s;
-  if (T == 1 && (p->config_override == kTensorCoreConfig || p->config_override == kFusedConfig))
-    return fail(KDA_EUNSUPPORTED, "config_override = %d (a verify configuration) needs T > 1", p->config_override);
+  if (T == 1 && p->config_override == kTensorCoreConfig)
+    return fail(KDA_EUNSUPPORTED, "config_override = %d (tensor-core verify) needs T > 1", kTensorCoreConfig);
   if (p->B == 0) return ok();
   const int cfg = pick_config(p, T);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cfg == kTensorCoreConfig ? kda::launch_verify_tc(*p, T, bulk, st)
-                  : cfg == kFusedConfig    ? kda::launch_verify_fused(*p, T, bulk, st)
                                            : kda::launch_step(*p, T, kTileV[cfg], bulk, st);
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify launch: %s", cudaGetErrorString(e));
   return ok();
@@ -250,8 +244,6 @@ kda_status kda_prefill(const kda_params* p, const kda_seqs* sq, void* stream) {
   if (p == nullptr) return fail(KDA_EINVAL, "params is NULL");
   if (sq == nullptr) return fail(KDA_EINVAL, "seqs is NULL");
   if (sq->num_seqs < 0) return fail(KDA_EINVAL, "num_seqs = %d is negative", sq->num_seqs);
-  if (p->config_override == kFusedConfig)
-    return fail(KDA_EUNSUPPORTED, "config_override = %d is not a prefill configuration (0..4)", kFusedConfig);
   if (sq->num_seqs == 0) return ok();  // nothing to read or write (state_indices may be empty)
   bool bulk = false;
   kda_status s = check_params(p, 1, &bulk);
@@ -278,8 +270,8 @@ kda_status kda_decode_fp8(const kda_params* p, const kda_fp8_pool* f, void* stre
   bool unused = false;
   kda_status s = check_params(&common, 1, &unused);
   if (s != KDA_OK) return s;
-  if (p->config_override == kTensorCoreConfig || p->config_override == kFusedConfig)
-    return fail(KDA_EUNSUPPORTED, "config_override = %d (a verify configuration) needs T > 1", p->config_override);
+  if (p->config_override == kTensorCoreConfig)
+    return fail(KDA_EUNSUPPORTED, "config_override = %d (tensor-core verify) needs T > 1", kTensorCoreConfig);
   if (f == nullptr) return fail(KDA_EINVAL, "fp8 pool is NULL");
   const int64_t slot = (int64_t)p->H * 128 * 128, sslot = (int64_t)p->H * 128;
   bool bulk = false;

@@ -181,15 +181,14 @@ def test_decode_rejects(lib, mutate, expect, msg):
 
 
 @no_gpu
-@pytest.mark.parametrize("config", [4, 5])
-def test_verify_configurations_need_several_tokens(lib, config):
+def test_tensor_core_configuration_is_verify_only(lib):
     p = fake_params()
-    p.config_override = config
+    p.config_override = 4
     assert status(lib, p) == kda.KDA_EUNSUPPORTED  # decode
     assert "T > 1" in kda.kda_last_error()
     assert status(lib, p, T=1) == kda.KDA_EUNSUPPORTED
     assert status(lib, p, T=8, ring=ring()) == kda.KDA_EUNSUPPORTED  # the ring takes whole-head tiles only
-    assert kda.kda_config_tile_v(config) == 128
+    assert kda.kda_config_tile_v(4) == 128
 
 
 @no_gpu
@@ -294,9 +293,8 @@ def test_fp8_decode_validation(lib):
 
 @no_gpu
 def test_prefill_validation(lib):
-    """kda_prefill rejects missing arguments, a negative sequence count, the
-    fused verify configuration, a configuration index past the last and an
-    unaligned cu_seqlens; an empty
+    """kda_prefill rejects missing arguments, a negative sequence count, a
+    configuration index past the last and an unaligned cu_seqlens; an empty
     call launches nothing; the selector picks the chunked tensor-core kernel."""
     p = fake_params()
     call = lambda sq: lib.kda_prefill(ctypes.byref(p), None if sq is None else ctypes.byref(sq), None)  # noqa: E731
@@ -306,9 +304,7 @@ def test_prefill_validation(lib):
     assert call(kda.KdaSeqs(cu, -1)) == kda.KDA_EINVAL and "num_seqs" in kda.kda_last_error()
     assert call(kda.KdaSeqs(None, 2)) == kda.KDA_EINVAL and "cu_seqlens" in kda.kda_last_error()
     assert call(kda.KdaSeqs(cu + 2, 2)) == kda.KDA_EINVAL and "cu_seqlens" in kda.kda_last_error()
-    p.config_override = 5  # the fused verify configuration
-    assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_EUNSUPPORTED and "prefill" in kda.kda_last_error()
-    p.config_override = 6
+    p.config_override = 5
     assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_EINVAL and "config_override" in kda.kda_last_error()
     p.config_override = -1
     p.K = 64

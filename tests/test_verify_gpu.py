@@ -16,7 +16,6 @@ from harness import (assert_output_close, assert_state_close, decode_token, f64,
 from linear_attention_ssm_step_gb300 import kda, workloads
 
 TC = 4  # the tensor-core configuration
-FUSED = 5  # the CUDA-core configuration with the dot products fused into the update pass
 
 pytestmark = pytest.mark.gpu
 
@@ -59,69 +58,8 @@ def test_verify_tensor_cores_match_oracle(dev, B, T):
     check_verify(w, dev, config_override=TC)
 
 
-@pytest.mark.parametrize("T", [2, 8, 16])
-@pytest.mark.parametrize("B", [1, 5, 32])
-def test_verify_fused_match_oracle(dev, B, T):
-    if B == 32 and T == 16:
-        pytest.skip("covered by the T=8 case; keeps the oracle time short")
-    w = workloads.decode_inputs(B, B + 64, seed=330 + 17 * B + T, T=T, inactive_frac=0.2 if B == 5 else 0.0,
-                                layout="fused")
-    check_verify(w, dev, config_override=FUSED)
-
-
-def test_verify_fused_serving_batch_512_sampled(dev):
-    w = workloads.decode_inputs(512, 576, seed=3, T=8)
-    rows = np.sort(np.random.default_rng(4).choice(512, 24, replace=False))
-    check_verify(w, dev, rows=rows, config_override=FUSED)
-
-
-@pytest.mark.parametrize("config", [TC, FUSED])
-def test_verify_fused_and_tensor_core_misaligned_state_same_bits(dev, config):
-    """A 2-byte aligned pool takes plain loads and stores: the same bits."""
-    w = workloads.decode_inputs(4, 6, seed=5, T=4)
-    wd = w.to(dev)
-    flat = torch.empty(6 * 12 * 128 * 128 + 8, dtype=torch.bfloat16, device=dev)
-    mis = flat[3:3 + 6 * 12 * 128 * 128].view(6, 12, 128, 128)
-    mis.copy_(wd.state)
-    out_a = gpu_verify(wd, config_override=config)
-    wd.state = mis
-    out_b = gpu_verify(wd, config_override=config)
-    ref = w.to(dev)
-    gpu_verify(ref, config_override=config)
-    torch.cuda.synchronize()
-    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
-    assert torch.equal(mis.view(torch.int16), ref.state.view(torch.int16))
-
-
-def test_verify_fused_cuda_graph_bitwise(dev):
-    w = workloads.decode_inputs(6, 10, seed=6, T=8)
-    wd = w.to(dev)
-    init = wd.state.clone()
-    gpu_verify(wd, config_override=FUSED)
-    torch.cuda.synchronize()
-    out = torch.empty((6, 8, 12, 128), dtype=torch.bfloat16, device=dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        gpu_verify(wd, out=out, config_override=FUSED)
-    res = []
-    for _ in range(3):
-        wd.state.copy_(init)
-        graph.replay()
-        torch.cuda.synchronize()
-        res.append((out.clone(), wd.state.clone()))
-    for o, s in res[1:]:
-        assert torch.equal(o.view(torch.int16), res[0][0].view(torch.int16))
-        assert torch.equal(s.view(torch.int16), res[0][1].view(torch.int16))
-
-
-def test_verify_fused_precomputed_gate_convention(dev):
-    w = workloads.decode_inputs(5, 12, seed=9, T=8, inactive_frac=0.2, gate_mode=1)
-    w.A_log = w.dt_bias = None
-    check_verify(w, dev, config_override=FUSED)
-
-
 @pytest.mark.parametrize("H", [1, 3, 64])
-@pytest.mark.parametrize("config", [3, TC, FUSED])
+@pytest.mark.parametrize("config", [3, TC])
 def test_verify_other_head_counts(dev, H, config):
     w = workloads.decode_inputs(2, 4, seed=320 + H, T=4, H=H)
     check_verify(w, dev, config_override=config)
@@ -227,15 +165,14 @@ def test_verify_tensor_cores_precomputed_gate_convention(dev):
     check_verify(w, dev, config_override=TC)
 
 
-@pytest.mark.parametrize("config", [TC, FUSED])
-def test_verify_configurations_need_several_tokens(dev, config):
+def test_tensor_core_configuration_needs_several_tokens(dev):
     w = workloads.decode_inputs(3, 6, seed=9, T=1)
     wd = w.to(dev)
     with pytest.raises(kda.KdaError):
-        gpu_verify(wd, config_override=config)
+        gpu_verify(wd, config_override=TC)
     w1 = workloads.decode_inputs(3, 6, seed=9)
     with pytest.raises(kda.KdaError):
-        gpu_decode(w1.to(dev), config_override=config)
+        gpu_decode(w1.to(dev), config_override=TC)
 
 
 @pytest.mark.parametrize("T", [2, 8])
