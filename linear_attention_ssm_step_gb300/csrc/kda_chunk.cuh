@@ -132,10 +132,9 @@ __device__ __forceinline__ void zero_tokens(TokenRegs<TT>& L) {
   L.alog = L.dtb = 0.0f;
 }
 
-// Token inputs of T tokens from batch row b for key channel / value row c.
 template <int TT>
-__device__ __forceinline__ void load_tokens_at(const kda_params& p, int b, int h, int T, TokenRegs<TT>& L, int c) {
-  const int tid = c;
+__device__ __forceinline__ void load_tokens(const kda_params& p, int b, int h, int T, TokenRegs<TT>& L) {
+  const int tid = threadIdx.x;
 #pragma unroll
   for (int t = 0; t < TT; ++t) {
     if (t < T) {
@@ -150,11 +149,6 @@ __device__ __forceinline__ void load_tokens_at(const kda_params& p, int b, int h
     L.alog = p.A_log[h];
     L.dtb = p.dt_bias[(int64_t)h * KD + tid];
   }
-}
-
-template <int TT>
-__device__ __forceinline__ void load_tokens(const kda_params& p, int b, int h, int T, TokenRegs<TT>& L) {
-  load_tokens_at(p, b, h, T, L, (int)threadIdx.x);
 }
 
 // The gate of the chunk kernels (ring verify, chunked prefill): the formulas

@@ -60,9 +60,7 @@ namespace kda {
 
 constexpr int PC = KDA_MAX_T;  // tokens per chunk
 constexpr int PC_NB = 2 * PC;  // dot products per row and chunk: P_t k_t (even columns), P_t q_t (odd)
-constexpr int PC_WG = 2;       // warp groups: each takes half of a chunk's tokens, state columns, coefficients
-constexpr int PC_TW = PC / PC_WG;  // tokens per warp group
-constexpr int PC_THREADS = 128 * PC_WG;
+constexpr int PC_THREADS = 128;
 constexpr uint32_t PC_TMEM_COLS = 256;     // S: columns 0..127; the X/Y sums: 128..191
 constexpr uint32_t PC_XY = 128;
 constexpr uint32_t PC_PART = 128u * 256u;  // one bf16 part of S as the A operand (128 rows x 128 keys)
@@ -70,7 +68,7 @@ constexpr uint32_t PC_UW_PART = 4096u;     // one bf16 part of U or W: 128 rows 
 
 // Shared-memory carve-up (bytes from a 1024-aligned base).
 struct PcLayout {
-  uint32_t a, b, red, fcp, rn, plast, beta, xkh, xqh, xdd, xv, su, xpose, bar, tslot, total;
+  uint32_t a, b, red, fcp, rn, plast, beta, xpose, bar, tslot, total;
 };
 
 __host__ __device__ inline PcLayout pc_layout() {
@@ -80,28 +78,18 @@ __host__ __device__ inline PcLayout pc_layout() {
   o += 2u * PC_PART;
   L.b = o;  // X/Y B operand: rows 0..31 high parts, 32..63 low parts, 128 keys, 128-byte swizzle
   o += 2u * PC_NB * 256u;
-  L.red = o;  // per-warp partial sums: each warp group's norms, then the coefficients
-  o += (PC_WG + PC * PC / 32u) * 512u;
+  L.red = o;  // per-warp partial sums: norms, then the coefficients
+  o += (1u + PC * PC / 32u) * 512u;
   L.fcp = o;  // coefficient sums, as pairs (M[a][b], M[b][a])
   o += PC * PC * 8u;
-  L.rn = o;  // inverse norms: q of token t at t, k at PC + t
+  L.rn = o;  // inverse norms
   o += PC_NB * 4u;
   L.plast = o;  // P_{C-1} per key channel
   o += 128u * 4u;
   L.beta = o;
   o += PC * 4u;
-  L.xkh = o;  // the chunk's k_hat, q_hat, decay and v, token-major [PC][128]: each warp group
-  o += PC * 512u;  // writes its tokens, both read all
-  L.xqh = o;
-  o += PC * 512u;
-  L.xdd = o;
-  o += PC * 512u;
-  L.xv = o;
-  o += PC * 512u;
-  L.su = o;  // the rows' u, token-major [PC][128], from the u chain to the outputs
-  o += PC * 512u;
   L.xpose = o;  // per-warp transpose tiles of the block sums
-  o += (PC_THREADS / 32u) * XPOSE_WARP_BYTES;
+  o += 4u * XPOSE_WARP_BYTES;
   L.bar = o;
   o += 32u;
   L.tslot = o;
@@ -114,20 +102,11 @@ __host__ __device__ inline size_t pc_smem_bytes() { return (size_t)pc_layout().t
 
 // p: the call's parameters with t_stride = b_stride in q, k, v, g_raw and
 // beta_logit, so that token t of a chunk starting at row c0 is (b = c0, t).
-//
-// Thread tid is warp group wg = tid / 128 and index c = tid % 128: key channel
-// c in the per-channel work, value row c in the per-row work (warps w and
-// w + 4 read the same tensor-memory lanes). Warp group wg takes tokens
-// 8 wg .. 8 wg + 7 of a chunk (inputs, norms, gates, B-operand rows), rows
-// 8 wg .. of the coefficient matrix, columns 64 wg .. 64 wg + 63 of the state
-// (its split and decay), entries 8 wg .. of the update's decayed keys; in the
-// recurrence warp group 0 runs the u chain and warp group 1 the outputs.
 template <bool TMA>
-__global__ void __launch_bounds__(PC_THREADS, 1)
+__global__ void __launch_bounds__(PC_THREADS, 2)
     kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p, const int32_t* __restrict__ cu,
                           const int num_seqs) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int wg = tid >> 7, c = tid & 127, wq = warp & 3;
   const int total = num_seqs * p.H;
 
   extern __shared__ unsigned char smem_raw[];
@@ -142,11 +121,6 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
   float* rn = reinterpret_cast<float*>(sm + SL.rn);
   float* splast = reinterpret_cast<float*>(sm + SL.plast);
   float* sbeta = reinterpret_cast<float*>(sm + SL.beta);
-  float* xkh = reinterpret_cast<float*>(sm + SL.xkh);
-  float* xqh = reinterpret_cast<float*>(sm + SL.xqh);
-  float* xdd = reinterpret_cast<float*>(sm + SL.xdd);
-  float* xv = reinterpret_cast<float*>(sm + SL.xv);
-  float* su = reinterpret_cast<float*>(sm + SL.su);
   float* xtile = reinterpret_cast<float*>(sm + SL.xpose + warp * XPOSE_WARP_BYTES);
   uint64_t* barA = reinterpret_cast<uint64_t*>(sm + SL.bar);  // the slot's state copy
   uint64_t* barD = barA + 1;                                   // X/Y product
@@ -164,9 +138,9 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t row_tmem = tmem + ((uint32_t)(wq * 32) << 16);  // lane c, column 0
-  uint32_t phA = 0, phD = 0, phU = 0;                              // mbarrier phases
-  bool pendA = false, pendD = false, pendU = false;                // a copy or a product is in flight
+  const uint32_t row_tmem = tmem + ((uint32_t)(warp * 32) << 16);  // lane tid, column 0
+  uint32_t phA = 0, phD = 0, phU = 0;                                // mbarrier phases
+  bool pendA = false, pendD = false, pendU = false;                  // a copy or a product is in flight
   bool broken = false;  // a bounded wait gave up: nothing more is issued
 
   for (int it = blockIdx.x; it < total; it += gridDim.x) {
@@ -177,9 +151,9 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
       if (tid == 0 && h == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_SEQLENS);
       continue;
     }
-    const int64_t ob = (int64_t)h * p.out_h_stride + c;  // output element of row c, + token row * out_b_stride
+    const int64_t ob = (int64_t)h * p.out_h_stride + tid;  // output element of row tid, + token row * out_b_stride
     if (n < 0 || n >= p.N || broken) {  // inactive (or skipped after a wait gave up): zero outputs
-      for (int t = t0 + wg; t < t1; t += PC_WG) outp[(int64_t)t * p.out_b_stride + ob] = 0;
+      for (int t = t0; t < t1; ++t) outp[(int64_t)t * p.out_b_stride + ob] = 0;
       continue;
     }
     if (t0 == t1) continue;
@@ -194,84 +168,62 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
       }
       pendA = true;
     } else {
-      for (int r = wg; r < KD; r += PC_WG)
-        *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, c)) = gstate[(int64_t)r * KD + c];
+      for (int r = 0; r < KD; ++r)
+        *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, tid)) = gstate[(int64_t)r * KD + tid];
     }
 
-    // This warp group's tokens of the first chunk.
-    TokenRegs<PC_TW> L;
+    TokenRegs<PC> L;
     zero_tokens(L);
-    load_tokens_at(p, t0 + wg * PC_TW, h, min(PC_TW, t1 - t0 - wg * PC_TW), L, c);
+    load_tokens(p, t0, h, min(PC, t1 - t0), L);
     bool first = true, ok = true;
     for (int c0 = t0; c0 < t1; c0 += PC) {
       const int Tc = min(PC, t1 - c0);
-      const int tb = wg * PC_TW;  // this warp group's first token
 
-      // 1. L2 norms of this warp group's tokens: block sums of q^2 (value i) and
-      // k^2 (value PC_TW + i) over the group's four warps.
+      // 1. L2 norms: block sums of q_t^2 (value t) and k_t^2 (value PC + t).
 #pragma unroll
-      for (int i = 0; i < PC_TW; ++i) {
-        const float q = bf16_bits_to_float(L.qv[i]), k = bf16_bits_to_float(L.kv[i]);
-        tile_put(xtile, lane, i, __fmul_rn(q, q));
-        tile_put(xtile, lane, PC_TW + i, __fmul_rn(k, k));
+      for (int t = 0; t < PC; ++t) {
+        const float q = bf16_bits_to_float(L.qv[t]), k = bf16_bits_to_float(L.kv[t]);
+        tile_put(xtile, lane, t, __fmul_rn(q, q));
+        tile_put(xtile, lane, PC + t, __fmul_rn(k, k));
       }
       __syncwarp();
       {
-        const float s = tile_row_sum(xtile, lane & (2 * PC_TW - 1));
+        const float s = tile_row_sum(xtile, lane);
         __syncwarp();
-        red[(wg * 4 + wq) * 32 + lane] = s;
+        red[warp * 32 + lane] = s;
       }
       __syncthreads();
-      if (c < 2 * PC_TW) {
-        const float inv = inv_norm(block_sum(red, wg, c));
-        rn[c < PC_TW ? tb + c : PC + tb + c - PC_TW] = inv;
-      }
+      if (tid < PC_NB) rn[tid] = inv_norm(block_sum(red, 0, tid));
       __syncthreads();
 
-      // 2. Per channel c, this group's tokens: the normalised vectors, the gate
-      // (tokens past the chunk's end: decay 1, beta 0, zero vectors), shared
-      // through shared memory with the other group; v of row c likewise.
-      {
-        const FastGate gate(p, L.alog);
-        if (c < PC_TW) sbeta[tb + c] = tb + c < Tc ? gate.beta(bf16_bits_to_float(L.blogit)) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < PC_TW; ++i) {
-          const int t = tb + i;
-          xqh[t * KD + c] = __fmul_rn(bf16_bits_to_float(L.qv[i]), rn[t]);
-          xkh[t * KD + c] = __fmul_rn(bf16_bits_to_float(L.kv[i]), rn[PC + t]);
-          xdd[t * KD + c] = t < Tc ? __expf(gate.g(bf16_bits_to_float(L.gv[i]), L.dtb)) : 1.0f;
-          xv[t * KD + c] = bf16_bits_to_float(L.vv[i]);
-        }
-      }
-      __syncthreads();
+      // Per channel tid: the normalised vectors, the gate (tokens past the
+      // chunk's end: decay 1, beta 0, zero vectors), P_t and the B operand.
+      const FastGate gate(p, L.alog);
+      if (tid < PC) sbeta[tid] = tid < Tc ? gate.beta(bf16_bits_to_float(L.blogit)) : 0.0f;
       float qh[PC], kh[PC], dd[PC];
 #pragma unroll
       for (int t = 0; t < PC; ++t) {
-        qh[t] = xqh[t * KD + c];
-        kh[t] = xkh[t * KD + c];
-        dd[t] = xdd[t * KD + c];
+        qh[t] = __fmul_rn(bf16_bits_to_float(L.qv[t]), rn[t]);
+        kh[t] = __fmul_rn(bf16_bits_to_float(L.kv[t]), rn[PC + t]);
+        dd[t] = t < Tc ? __expf(gate.g(bf16_bits_to_float(L.gv[t]), L.dtb)) : 1.0f;
       }
-      {  // P_t, and this group's rows of the B operand
+      {
         float P = 1.0f;
 #pragma unroll
         for (int t = 0; t < PC; ++t) {
           P = __fmul_rn(P, dd[t]);
-          if (t >= tb && t < tb + PC_TW) {
-            float xk, xq;
-            upk2(mul2(pk2(P, P), pk2(kh[t], qh[t])), xk, xq);
-            store_split<2 * PC_NB>(sB, sB + PC_NB * 128, 2 * t, c, xk);
-            store_split<2 * PC_NB>(sB, sB + PC_NB * 128, 2 * t + 1, c, xq);
-          }
+          float xk, xq;
+          upk2(mul2(pk2(P, P), pk2(kh[t], qh[t])), xk, xq);
+          store_split<2 * PC_NB>(sB, sB + PC_NB * 128, 2 * t, tid, xk);
+          store_split<2 * PC_NB>(sB, sB + PC_NB * 128, 2 * t + 1, tid, xq);
         }
-        if (wg == 0) splast[c] = P;
+        splast[tid] = P;
       }
 
-      // Coefficients M[a][b] (flat a PC + b) for this group's rows a: a > b holds
-      // cc[a][b] = (w_ab k_b) . k_a, a <= b holds ec[b][a] = (w_ba k_a) . q_b, w a
-      // running product of the decays.
+      // Coefficients M[a][b] (flat a PC + b): a > b holds cc[a][b] = (w_ab k_b) . k_a,
+      // a <= b holds ec[b][a] = (w_ba k_a) . q_b, w a running product of the decays.
 #pragma unroll
       for (int a0 = 0; a0 < PC; a0 += 32 / PC) {
-        if (a0 / PC_TW != wg) continue;  // rows of the other warp group (a uniform branch; a0 stays static)
         float vals[32];
 #pragma unroll
         for (int r = 0; r < 32 / PC; ++r) {
@@ -295,31 +247,26 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
             }
           }
         }
-        red[((PC_WG + a0 * PC / 32) * 4 + wq) * 32 + lane] = warp_sum32(vals, xtile, lane);
+        red[((1 + a0 * PC / 32) * 4 + warp) * 32 + lane] = warp_sum32(vals, xtile, lane);
       }
-      // The update's decayed keys of channel c for this group's entries:
-      // W_j = (d_{j+1} ... d_{PC-1}) k_j.
-      float Wk[PC_TW];
+      // The update's decayed keys of channel tid: W_j = (d_{j+1} ... d_{PC-1}) k_j.
+      float Wk[PC];
       {
-        float W16[PC];
         float wl = 1.0f;
 #pragma unroll
         for (int j = PC - 1; j >= 0; --j) {
-          W16[j] = __fmul_rn(wl, kh[j]);
+          Wk[j] = __fmul_rn(wl, kh[j]);
           wl = __fmul_rn(wl, dd[j]);
         }
-#pragma unroll
-        for (int j = 0; j < PC_TW; ++j) Wk[j] = wg == 0 ? W16[j] : W16[PC_TW + j];
       }
       __syncthreads();  // partial sums, the B operand, P_{C-1}, beta
-      {
-        const int i = tid;  // PC * PC = 256 coefficients, one per thread
-        const float v = block_sum(red, PC_WG + (i >> 5), i & 31);
+      for (int i = tid; i < PC * PC; i += PC_THREADS) {
+        const float v = block_sum(red, 1 + (i >> 5), i & 31);
         fcp[2 * i] = v;
         fcp[2 * ((i % PC) * PC + i / PC) + 1] = v;
       }
 
-      // 3. The previous update has finished with S and the A region; on the
+      // 2. The previous update has finished with S and the A region; on the
       // first chunk the slot's state has arrived.
       {
         bool w_ok = true;
@@ -337,45 +284,44 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
         pendA = false;
       }
       tc_fence_after();
-      // Row c, this group's 64 columns: S into the bf16 parts of the A operand,
-      // S <- P_{C-1} S in tensor memory.
+      // Row tid: S into the bf16 parts of the A operand, S <- P_{C-1} S in tensor memory.
 #pragma unroll 1
-      for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
+      for (int cb = 0; cb < 4; ++cb) {
         float s[32];
         if (first) {  // the slot's bf16 row, from the A operand
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(sA + sw128_offset(KD, c, cb * 32 + 8 * q));
-            unpack_bf16x2(raw.x, s[8 * q], s[8 * q + 1]);
-            unpack_bf16x2(raw.y, s[8 * q + 2], s[8 * q + 3]);
-            unpack_bf16x2(raw.z, s[8 * q + 4], s[8 * q + 5]);
-            unpack_bf16x2(raw.w, s[8 * q + 6], s[8 * q + 7]);
+          for (int c = 0; c < 4; ++c) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(sA + sw128_offset(KD, tid, cb * 32 + 8 * c));
+            unpack_bf16x2(raw.x, s[8 * c], s[8 * c + 1]);
+            unpack_bf16x2(raw.y, s[8 * c + 2], s[8 * c + 3]);
+            unpack_bf16x2(raw.z, s[8 * c + 4], s[8 * c + 5]);
+            unpack_bf16x2(raw.w, s[8 * c + 6], s[8 * c + 7]);
           }
         } else {
           tmem_ld32(row_tmem + cb * 32, s);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t hw[4], lw[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float s0 = s[8 * q + 2 * e], s1 = s[8 * q + 2 * e + 1];
-              hw[e] = pack_bf16x2(s0, s1);
+            for (int q = 0; q < 4; ++q) {
+              const float s0 = s[8 * c + 2 * q], s1 = s[8 * c + 2 * q + 1];
+              hw[q] = pack_bf16x2(s0, s1);
               float h0, h1;
-              unpack_bf16x2(hw[e], h0, h1);
-              lw[e] = pack_bf16x2(__fsub_rn(s0, h0), __fsub_rn(s1, h1));
+              unpack_bf16x2(hw[q], h0, h1);
+              lw[q] = pack_bf16x2(__fsub_rn(s0, h0), __fsub_rn(s1, h1));
             }
-            const uint32_t off = sw128_offset(KD, c, cb * 32 + 8 * q);
+            const uint32_t off = sw128_offset(KD, tid, cb * 32 + 8 * c);
             *reinterpret_cast<uint4*>(sA + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4*>(sA + PC_PART + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 pl = *reinterpret_cast<const float4*>(splast + cb * 32 + 4 * q);
-          f32x2 x0 = mul2(pk2(pl.x, pl.y), pk2(s[4 * q], s[4 * q + 1]));
-          f32x2 x1 = mul2(pk2(pl.z, pl.w), pk2(s[4 * q + 2], s[4 * q + 3]));
-          upk2(x0, s[4 * q], s[4 * q + 1]);
-          upk2(x1, s[4 * q + 2], s[4 * q + 3]);
+        for (int c = 0; c < 8; ++c) {
+          const float4 pl = *reinterpret_cast<const float4*>(splast + cb * 32 + 4 * c);
+          f32x2 a = mul2(pk2(pl.x, pl.y), pk2(s[4 * c], s[4 * c + 1]));
+          f32x2 b = mul2(pk2(pl.z, pl.w), pk2(s[4 * c + 2], s[4 * c + 3]));
+          upk2(a, s[4 * c], s[4 * c + 1]);
+          upk2(b, s[4 * c + 2], s[4 * c + 3]);
         }
         tmem_st32(row_tmem + cb * 32, s);
       }
@@ -384,7 +330,7 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
       tc_fence_before();
       __syncthreads();
 
-      // 4. The X/Y product: D[row][col] = sum_k S[row][k] B[col][k], K in 8 steps of
+      // 3. The X/Y product: D[row][col] = sum_k S[row][k] B[col][k], K in 8 steps of
       // 16, per part of S; columns 32.. hold the low parts' share.
       if (tid == 0) {
         tc_fence_after();
@@ -400,94 +346,67 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
         tc_commit(barD);
       }
       pendD = true;
+      uint16_t vcur[PC];
+#pragma unroll
+      for (int t = 0; t < PC; ++t) vcur[t] = L.vv[t];
       if (c0 + PC < t1) {  // the next chunk's token inputs fly while this chunk finishes
         zero_tokens(L);
-        const int nb = c0 + PC + tb;
-        load_tokens_at(p, nb, h, min(PC_TW, t1 - nb), L, c);
+        load_tokens(p, c0 + PC, h, min(PC, t1 - c0 - PC), L);
       }
       ok = __syncthreads_and(mbar_wait_bounded(barD, phD)) != 0;
       if (!ok) break;
       phD ^= 1u;
       pendD = false;
       tc_fence_after();
-      f32x2 X[PC];  // (S_0^T (P_t k_t), S_0^T (P_t q_t)) of row c
+      f32x2 X[PC];  // (S_0^T (P_t k_t), S_0^T (P_t q_t)) of row tid
 #pragma unroll
-      for (int q = 0; q < PC_NB; q += 16) {
+      for (int c = 0; c < PC_NB; c += 16) {
         float xh[16], xl[16];
-        tmem_ld16(row_tmem + PC_XY + q, xh);
-        tmem_ld16(row_tmem + PC_XY + PC_NB + q, xl);
+        tmem_ld16(row_tmem + PC_XY + c, xh);
+        tmem_ld16(row_tmem + PC_XY + PC_NB + c, xl);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) X[q / 2 + i] = add2(pk2(xh[2 * i], xh[2 * i + 1]), pk2(xl[2 * i], xl[2 * i + 1]));
+        for (int i = 0; i < 8; ++i) X[c / 2 + i] = add2(pk2(xh[2 * i], xh[2 * i + 1]), pk2(xl[2 * i], xl[2 * i + 1]));
       }
 
-      // 5. Row c: warp group 0 runs the u chain and shares u; warp group 1 then
-      // forms the outputs. U (group 0) and this group's W entries as bf16 parts.
-      if (wg == 0) {
-        float uval[PC];
+      // 4. Row tid: the recurrence over the chunk's tokens, and their outputs.
+      float uval[PC];
+      {
+        f32x2 uu[PC];
 #pragma unroll
         for (int t = 0; t < PC; ++t) {
-          float acc_e = 0.0f, acc_o = 0.0f;
+          f32x2 ce[PC];  // (cc[t][s], ec[t][s]): cc for s < t, ec for s <= t
+#pragma unroll
+          for (int s2 = 0; s2 < PC / 2; ++s2) {
+            const float4 c = reinterpret_cast<const float4*>(fcp + 2 * t * PC)[s2];
+            ce[2 * s2] = pk2(c.x, c.y);
+            ce[2 * s2 + 1] = pk2(c.z, c.w);
+          }
+          f32x2 acc_e = pk2(0.0f, 0.0f), acc_o = pk2(0.0f, 0.0f);  // two chains: half the latency
 #pragma unroll
           for (int s2 = 0; s2 < t; ++s2) {
-            const float cc = fcp[2 * (t * PC + s2)];
             if (s2 & 1)
-              acc_o = __fmaf_rn(cc, uval[s2], acc_o);
+              acc_o = fma2(ce[s2], uu[s2], acc_o);
             else
-              acc_e = __fmaf_rn(cc, uval[s2], acc_e);
+              acc_e = fma2(ce[s2], uu[s2], acc_e);
           }
-          float xk, xq;
+          float acc, acco, xk, xq, ctt, ect;
+          upk2(add2(acc_e, acc_o), acc, acco);
           upk2(X[t], xk, xq);
-          (void)xq;
-          uval[t] = __fmul_rn(sbeta[t], __fsub_rn(xv[t * KD + c], __fadd_rn(xk, __fadd_rn(acc_e, acc_o))));
-          su[t * KD + c] = uval[t];
-        }
-        store_row_split3(sU, PC_UW_PART, c, uval);
-      }
-      __syncthreads();  // u of every row
-      if (wg == 1) {
-        float uval[PC];
-#pragma unroll
-        for (int t = 0; t < PC; ++t) uval[t] = su[t * KD + c];
-#pragma unroll
-        for (int t = 0; t < PC; ++t) {
-          if (t < Tc) {
-            float xk, xq;
-            upk2(X[t], xk, xq);
-            (void)xk;
-            float acc_e = 0.0f, acc_o = 0.0f;
-#pragma unroll
-            for (int s2 = 0; s2 <= t; ++s2) {
-              const float ec = fcp[2 * (t * PC + s2) + 1];
-              if (s2 & 1)
-                acc_o = __fmaf_rn(ec, uval[s2], acc_o);
-              else
-                acc_e = __fmaf_rn(ec, uval[s2], acc_e);
-            }
-            const float o = __fmul_rn(p.scale, __fadd_rn(xq, __fadd_rn(acc_e, acc_o)));
-            outp[(int64_t)(c0 + t) * p.out_b_stride + ob] = float_to_bf16_bits(o);
-          }
+          upk2(ce[t], ctt, ect);
+          (void)ctt;
+          const float ut = __fmul_rn(sbeta[t], __fsub_rn(bf16_bits_to_float(vcur[t]), __fadd_rn(xk, acc)));
+          uu[t] = pk2(ut, ut);
+          uval[t] = ut;
+          acco = __fmaf_rn(ect, ut, acco);
+          const float o = __fmul_rn(p.scale, __fadd_rn(xq, acco));
+          if (t < Tc) outp[(int64_t)(c0 + t) * p.out_b_stride + ob] = float_to_bf16_bits(o);
         }
       }
-      // W entries 8 wg .. 8 wg + 7 of row (key) c: one 16-byte chunk per part.
-      {
-        uint32_t w0[4], w1[4], w2[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float a = Wk[2 * q], b = Wk[2 * q + 1];
-          w0[q] = pack_bf16x2(a, b);
-          float a0, b0;
-          unpack_bf16x2(w0[q], a0, b0);
-          const float ra = __fsub_rn(a, a0), rb = __fsub_rn(b, b0);
-          w1[q] = pack_bf16x2(ra, rb);
-          float a1, b1;
-          unpack_bf16x2(w1[q], a1, b1);
-          w2[q] = pack_bf16x2(__fsub_rn(ra, a1), __fsub_rn(rb, b1));
-        }
-        const uint32_t off = sw32_offset(128, c, 8 * wg);
-        *reinterpret_cast<uint4*>(sW + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-        *reinterpret_cast<uint4*>(sW + PC_UW_PART + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-        *reinterpret_cast<uint4*>(sW + 2 * PC_UW_PART + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-      }
+
+      // 5. U (row tid) and W (channel tid) as three bf16 parts; the update product
+      // accumulates sum_j u_j W_j onto P_{C-1} S_0 in tensor memory.
+      store_row_split3(sU, PC_UW_PART, tid, uval);
+      store_row_split3(sW, PC_UW_PART, tid, Wk);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncthreads();
@@ -508,15 +427,15 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
       first = false;
     }
 
-    if (ok) {  // the final state, rounded to bf16 once; row c, this group's columns, into the slot
+    if (ok) {  // the final state, rounded to bf16 once; row tid into the slot
       ok = __syncthreads_and(mbar_wait_bounded(barU, phU)) != 0;
       if (ok) {
         phU ^= 1u;
         pendU = false;
         tc_fence_after();
-        uint16_t* grow = gstate + (int64_t)c * KD;
+        uint16_t* grow = gstate + (int64_t)tid * KD;
 #pragma unroll 1
-        for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
+        for (int cb = 0; cb < 4; ++cb) {
           float s[32];
           tmem_ld32(row_tmem + cb * 32, s);
           uint32_t w[16];
@@ -525,7 +444,7 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
           if constexpr (TMA) {  // 16-byte aligned pool
             uint4* dst = reinterpret_cast<uint4*>(grow + cb * 32);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
           } else {
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
@@ -539,7 +458,7 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
     if (!ok) {  // a bounded wait gave up: the sequence is skipped, and every later one
       broken = true;
       if (tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
-      for (int t = t0 + wg; t < t1; t += PC_WG) outp[(int64_t)t * p.out_b_stride + ob] = 0;
+      for (int t = t0; t < t1; ++t) outp[(int64_t)t * p.out_b_stride + ob] = 0;
     }
     tc_fence_before();
     __syncthreads();  // this item's tensor-memory and shared-memory use is done
