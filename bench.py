@@ -379,6 +379,13 @@ def sweep(dev, steps=100, warmup=100):
         row["us_warm_16step_graph"] = round(tw * 1e3, 2)
         res["t1_decode"].append(row)
         del w, wd
+    # Context for the small-batch points: the same cold single-call timing of a
+    # graph holding one trivial kernel (a one-element fill), the launch and
+    # event floor every cold single-call figure above includes.
+    tiny = torch.zeros(1, dtype=torch.float32, device=dev)
+    t = statistics.median(time_calls(graphed(lambda: tiny.fill_(1.0)), steps, warmup, before=flush))
+    res["launch_floor"] = {"what": "one-element fill in a CUDA graph, the same cold single-call timing",
+                           "us": round(t * 1e3, 2)}
     # Context for the decode's roofline: a plain streaming kernel (PyTorch's
     # in-place elementwise multiply) over the bytes of the headline's state
     # (486 active rows: read and written once), behind the same flush.
