@@ -86,6 +86,30 @@ __device__ __forceinline__ float block_sum(const float* part, int chunk, int l) 
 
 // x as bf16 hi + lo (hi = bf16(x), lo = bf16(x - hi); |x - hi - lo| <= 2^-17 |x|)
 // at element (row, k) of the two B-operand halves.
+// Column k of a K-major, 128-byte-swizzled operand of R rows (sw128_offset):
+// the part of the offset that does not depend on the row, and the column's
+// 16-byte chunk within its 128-byte row, formed once per column.
+struct Sw128Col {
+  uint32_t base, chunk;
+};
+
+__device__ __forceinline__ Sw128Col sw128_col(int R, int k) {
+  return Sw128Col{(uint32_t)(k >> 6) * (uint32_t)R * 128u + ((uint32_t)(k & 7) << 1), (uint32_t)((k >> 3) & 7)};
+}
+
+// sw128_offset(R, r, k) for the column of `c`.
+__device__ __forceinline__ uint32_t sw128_at(const Sw128Col& c, int r) {
+  return c.base + (uint32_t)r * 128u + ((c.chunk ^ (uint32_t)(r & 7)) << 4);
+}
+
+// store_split at a precomputed offset.
+__device__ __forceinline__ void store_split_at(unsigned char* hi, unsigned char* lo, uint32_t off, float x) {
+  const uint16_t xh = float_to_bf16_bits(x);
+  const uint16_t xl = float_to_bf16_bits(__fsub_rn(x, bf16_bits_to_float(xh)));
+  *reinterpret_cast<uint16_t*>(hi + off) = xh;
+  *reinterpret_cast<uint16_t*>(lo + off) = xl;
+}
+
 template <int NB>
 __device__ __forceinline__ void store_split(unsigned char* hi, unsigned char* lo, int row, int k, float x) {
   const uint16_t xh = float_to_bf16_bits(x);
@@ -132,17 +156,28 @@ __device__ __forceinline__ void zero_tokens(TokenRegs<TT>& L) {
   L.alog = L.dtb = 0.0f;
 }
 
+// The addresses are formed once per tensor and stepped by t_stride, so that
+// each load costs one add.
 template <int TT>
 __device__ __forceinline__ void load_tokens(const kda_params& p, int b, int h, int T, TokenRegs<TT>& L) {
   const int tid = threadIdx.x;
+  const uint16_t* qb = static_cast<const uint16_t*>(p.q.ptr) + ((int64_t)b * p.q.b_stride + (int64_t)h * p.q.h_stride + tid);
+  const uint16_t* kb = static_cast<const uint16_t*>(p.k.ptr) + ((int64_t)b * p.k.b_stride + (int64_t)h * p.k.h_stride + tid);
+  const uint16_t* gb =
+      static_cast<const uint16_t*>(p.g_raw.ptr) + ((int64_t)b * p.g_raw.b_stride + (int64_t)h * p.g_raw.h_stride + tid);
+  const uint16_t* vb = static_cast<const uint16_t*>(p.v.ptr) + ((int64_t)b * p.v.b_stride + (int64_t)h * p.v.h_stride + tid);
 #pragma unroll
   for (int t = 0; t < TT; ++t) {
     if (t < T) {
-      L.qv[t] = load_bits(p.q, b, t, h, tid);
-      L.kv[t] = load_bits(p.k, b, t, h, tid);
-      L.gv[t] = load_bits(p.g_raw, b, t, h, tid);
-      L.vv[t] = load_bits(p.v, b, t, h, tid);
+      L.qv[t] = *qb;
+      L.kv[t] = *kb;
+      L.gv[t] = *gb;
+      L.vv[t] = *vb;
     }
+    qb += p.q.t_stride;
+    kb += p.k.t_stride;
+    gb += p.g_raw.t_stride;
+    vb += p.v.t_stride;
   }
   if (tid < T) L.blogit = load_bits(p.beta_logit, b, tid, h, 0);
   if (p.gate_mode == KDA_GATE_RAW) {

@@ -209,13 +209,14 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
       }
       {
         float P = 1.0f;
+        const Sw128Col col = sw128_col(2 * PC_NB, tid);
 #pragma unroll
         for (int t = 0; t < PC; ++t) {
           P = __fmul_rn(P, dd[t]);
           float xk, xq;
           upk2(mul2(pk2(P, P), pk2(kh[t], qh[t])), xk, xq);
-          store_split<2 * PC_NB>(sB, sB + PC_NB * 128, 2 * t, tid, xk);
-          store_split<2 * PC_NB>(sB, sB + PC_NB * 128, 2 * t + 1, tid, xq);
+          store_split_at(sB, sB + PC_NB * 128, sw128_at(col, 2 * t), xk);
+          store_split_at(sB, sB + PC_NB * 128, sw128_at(col, 2 * t + 1), xq);
         }
         splast[tid] = P;
       }
@@ -374,9 +375,9 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
         f32x2 uu[PC];
 #pragma unroll
         for (int t = 0; t < PC; ++t) {
-          f32x2 ce[PC];  // (cc[t][s], ec[t][s]): cc for s < t, ec for s <= t
+          f32x2 ce[PC];  // (cc[t][s], ec[t][s]): cc for s < t, ec for s <= t (only those are loaded)
 #pragma unroll
-          for (int s2 = 0; s2 < PC / 2; ++s2) {
+          for (int s2 = 0; s2 <= t / 2; ++s2) {
             const float4 c = reinterpret_cast<const float4*>(fcp + 2 * t * PC)[s2];
             ce[2 * s2] = pk2(c.x, c.y);
             ce[2 * s2 + 1] = pk2(c.z, c.w);

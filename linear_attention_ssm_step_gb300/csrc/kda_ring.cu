@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
   uint64_t* barD = barA + 2;                                   // dot products
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL.tslot);
   float* xtile = reinterpret_cast<float*>(sm + SL.xpose + warp * XPOSE_WARP_BYTES);
+  const Sw128Col bcol = sw128_col(NB2, tid);  // channel tid's column of the B operand
   constexpr uint32_t fk_part = 4096u;  // bytes between the key parts
   uint16_t* outp = static_cast<uint16_t*>(p.out);
 
@@ -311,8 +312,8 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
         for (int t = 0; t < TT; ++t) {
           float xk, xq;
           upk2(mul2(pk2(e_last, e_last), pkq[t]), xk, xq);
-          store_split<NB2>(sB, sB + NB * 128, 2 * t, tid, xk);
-          store_split<NB2>(sB, sB + NB * 128, 2 * t + 1, tid, xq);
+          store_split_at(sB, sB + NB * 128, sw128_at(bcol, 2 * t), xk);
+          store_split_at(sB, sB + NB * 128, sw128_at(bcol, 2 * t + 1), xq);
         }
       }
 
@@ -521,8 +522,8 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
           for (int t = 0; t < TT; ++t) {
             float xk, xq;
             upk2(pkq[t], xk, xq);
-            store_split<NB2>(sB, sB + NB * 128, 2 * t, tid, xk);
-            store_split<NB2>(sB, sB + NB * 128, 2 * t + 1, tid, xq);
+            store_split_at(sB, sB + NB * 128, sw128_at(bcol, 2 * t), xk);
+            store_split_at(sB, sB + NB * 128, sw128_at(bcol, 2 * t + 1), xq);
           }
           fence_proxy_async_smem();
         } else {
@@ -629,9 +630,9 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
       f32x2 uu[TT];  // (u~_s, u~_s)
 #pragma unroll
       for (int t = 0; t < TT; ++t) {
-        f32x2 ce[TT];  // (cc[t][s], ec[t][s]): cc for s < t, ec for s <= t
+        f32x2 ce[TT];  // (cc[t][s], ec[t][s]): cc for s < t, ec for s <= t (only those are loaded)
 #pragma unroll
-        for (int s2 = 0; s2 < TT / 2; ++s2) {
+        for (int s2 = 0; s2 <= t / 2; ++s2) {
           const float4 c = reinterpret_cast<const float4*>(fcp + 2 * t * TT)[s2];
           ce[2 * s2] = pk2(c.x, c.y);
           ce[2 * s2 + 1] = pk2(c.z, c.w);
