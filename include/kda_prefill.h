@@ -48,6 +48,8 @@
 #ifndef KDA_GB300_KDA_PREFILL_H
 #define KDA_GB300_KDA_PREFILL_H
 
+#include <stddef.h>
+
 #include "kda.h"
 
 #ifdef __cplusplus
@@ -77,6 +79,53 @@ kda_status kda_prefill(const kda_params* p, const kda_seqs* s, void* stream);
    chunked tensor-core kernel (source: PR #4605, Description: the BT16 chunked
    backend); -1 for negative num_seqs or H < 1. */
 int32_t kda_select_prefill_config(int32_t num_seqs, int32_t H);
+
+/*
+ * Two-stage prefill with a caller-owned workspace.
+ *
+ * Source: PR #4605, the embedded #4675 commit text (Description): the
+ * long-sequence prefill as a two-stage BT16 portfolio, a preparation stage
+ * and then a recurrence-chain stage; the review threads pass the stages'
+ * shared data through a caller-owned workspace (RecurrentKDAPrefillWorkspace).
+ *
+ * Configuration 5 of kda_prefill_ws computes the reading above in two
+ * kernels on the caller's stream. The first prepares every 16-token chunk of
+ * every (sequence, head) at once: norms, gates, the chunk's 16 x 16
+ * coefficients, and then by forward substitution the chunk's contribution to
+ * u and o in a form that no longer depends on the state. It writes these
+ * into the workspace. The second carries each (sequence, head) through its
+ * chunks in order, the fp32 state in tensor memory, with two tensor-core
+ * products per chunk: the state against the prepared vectors as two bf16
+ * parts (exact to about 2^-17), and the update from u and the decayed keys
+ * as three bf16 parts (exact to about 2^-24). Its results agree with
+ * configurations 0-4 to rounding, not bit for bit.
+ *
+ * workspace: device memory of at least kda_prefill_workspace_bytes(B,
+ * num_seqs, H) bytes, 16-byte aligned, owned by the caller, overlapping none
+ * of the call's inputs, outputs or the state pool. Its contents on entry do
+ * not matter and on return are unspecified; two calls in flight at once need
+ * two workspaces.
+ *
+ * config_override: -1 lets kda_select_prefill_ws_config choose; 0..4 run
+ * kda_prefill's configurations (the workspace is then not used and may be
+ * NULL); 5 runs the two-stage kernels. Validation as kda_prefill's, plus
+ * KDA_EINVAL for configuration 5 with a NULL, unaligned, too small or
+ * overlapping workspace. Errors found on the device (KDA_ERR_SEQLENS,
+ * KDA_ERR_TIMEOUT) are reported as kda_prefill reports them.
+ */
+kda_status kda_prefill_ws(const kda_params* p, const kda_seqs* s, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Workspace bytes kda_prefill_ws needs in configuration 5 for B token rows,
+   num_seqs sequences and H heads: (ceil(B / 16) + num_seqs) * H chunk images
+   of 45568 bytes; 0 when B <= 0, num_seqs <= 0 or H < 1. */
+size_t kda_prefill_workspace_bytes(int32_t B, int32_t num_seqs, int32_t H);
+
+/* The configuration kda_prefill_ws picks: 5 (two stages) when the sequences
+   average at least 512 tokens (B >= 512 num_seqs), else 4; -1 for negative B or
+   num_seqs or H < 1. Source: PR #4605, #4675 commit text (Description):
+   the preparation-and-chain schedules are selected from the input shape. */
+int32_t kda_select_prefill_ws_config(int32_t B, int32_t num_seqs, int32_t H);
 
 #ifdef __cplusplus
 }

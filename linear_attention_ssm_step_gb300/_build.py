@@ -17,7 +17,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libkda_gb300.so")
 
 SOURCES = ["kda_api.cu", "kda_step.cu", "kda_ring.cu", "kda_tmap.cu", "kda_verify_tc.cu", "kda_fp8.cu",
-           "kda_prefill.cu", "kda_prefill_tc.cu"]
+           "kda_prefill.cu", "kda_prefill_tc.cu", "kda_prefill_chain.cu"]
 HEADERS = ["kda_device.cuh", "kda_launch.h", "kda_tc.cuh", "kda_chunk.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

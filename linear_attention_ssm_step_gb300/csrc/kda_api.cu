@@ -43,6 +43,8 @@ kda_status ok() {
 constexpr int kTileV[] = {16, 32, 64, 128, 128};
 constexpr int kTensorCoreConfig = 4;
 constexpr int kNumConfigs = sizeof(kTileV) / sizeof(kTileV[0]);
+// Prefill only: the two-stage kernels, which need a caller's workspace (kda_prefill_ws).
+constexpr int kChainConfig = 5;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -178,6 +180,22 @@ int32_t kda_select_prefill_config(int32_t num_seqs, int32_t H) {
   return kTensorCoreConfig;
 }
 
+// Prefill with a workspace: the two-stage kernels (configuration 5) once the
+// sequences average 512 tokens (32 chunks) or more, where the chain's short
+// per-chunk step outweighs the workspace round trip and the second launch
+// (measured on GB300: 1 x 4096 and 8 x 2048 tokens faster in two stages,
+// 64 x 256 and 512 x 16 faster in one); the chunked single kernel below that.
+int32_t kda_select_prefill_ws_config(int32_t B, int32_t num_seqs, int32_t H) {
+  if (B < 0 || num_seqs < 0 || H < 1) return -1;
+  if (num_seqs > 0 && (long long)B >= 512LL * num_seqs) return kChainConfig;
+  return kTensorCoreConfig;
+}
+
+size_t kda_prefill_workspace_bytes(int32_t B, int32_t num_seqs, int32_t H) {
+  if (B <= 0 || num_seqs <= 0 || H < 1) return 0;
+  return (size_t)kda::prefill_chunk_images(B, num_seqs, H) * kda::kPrefillChunkImageBytes;
+}
+
 const char* kda_last_error(void) { return g_err; }
 
 kda_status kda_decode(const kda_params* p, void* stream) {
@@ -259,6 +277,67 @@ kda_status kda_prefill(const kda_params* p, const kda_seqs* sq, void* stream) {
   cudaError_t e = cfg == kTensorCoreConfig ? kda::launch_prefill_tc(*p, sq->cu_seqlens, sq->num_seqs, bulk, st)
                                            : kda::launch_prefill(*p, sq->cu_seqlens, sq->num_seqs, kTileV[cfg], bulk, st);
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_prefill launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+kda_status kda_prefill_ws(const kda_params* p, const kda_seqs* sq, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (p == nullptr) return fail(KDA_EINVAL, "params is NULL");
+  if (sq == nullptr) return fail(KDA_EINVAL, "seqs is NULL");
+  if (sq->num_seqs < 0) return fail(KDA_EINVAL, "num_seqs = %d is negative", sq->num_seqs);
+  const int cfg =
+      p->config_override >= 0 ? p->config_override : kda_select_prefill_ws_config(p->B, sq->num_seqs, p->H);
+  if (cfg != kChainConfig) {  // the single-kernel configurations; the workspace is not used
+    if (p->config_override < 0) {
+      kda_params q = *p;
+      q.config_override = cfg;
+      return kda_prefill(&q, sq, stream);
+    }
+    return kda_prefill(p, sq, stream);
+  }
+  if (sq->num_seqs == 0) return ok();
+  kda_params q = *p;
+  q.config_override = -1;  // configuration 5 is prefill-only; the shared checks see "library's choice"
+  bool bulk = false;
+  kda_status s = check_params(&q, 1, &bulk);
+  if (s != KDA_OK) return s;
+  if (p->B == 0) return ok();
+  if (sq->cu_seqlens == nullptr || !aligned(sq->cu_seqlens, 4))
+    return fail(KDA_EINVAL, "cu_seqlens is NULL or not 4-byte aligned");
+  if ((long long)sq->num_seqs * p->H > 0x7fffffffLL)
+    return fail(KDA_EUNSUPPORTED, "num_seqs * H = %lld is too large for one launch",
+                (long long)sq->num_seqs * p->H);
+  const size_t need = kda_prefill_workspace_bytes(p->B, sq->num_seqs, p->H);
+  if (workspace == nullptr || !aligned(workspace, 16))
+    return fail(KDA_EINVAL, "workspace is NULL or not 16-byte aligned (configuration %d)", kChainConfig);
+  if (workspace_bytes < need)
+    return fail(KDA_EINVAL, "workspace_bytes = %zu is below the %zu this call needs (kda_prefill_workspace_bytes)",
+                workspace_bytes, need);
+  {  // the workspace must not overlap anything the call reads or writes
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), w1 = w0 + need;
+    struct {
+      const char* name;
+      const kda_view* v;
+      int D;
+    } views[] = {{"q", &p->q, 128}, {"k", &p->k, 128}, {"v", &p->v, 128}, {"g_raw", &p->g_raw, 128},
+                 {"beta_logit", &p->beta_logit, 1}};
+    for (const auto& e : views) {
+      uintptr_t a0, a1;
+      view_extent(e.v->ptr, p->B, 1, p->H, e.D, e.v->b_stride, 0, e.v->h_stride, a0, a1);
+      if (overlaps(w0, w1, a0, a1)) return fail(KDA_EINVAL, "workspace overlaps %s", e.name);
+    }
+    uintptr_t o0, o1;
+    view_extent(p->out, p->B, 1, p->H, 128, p->out_b_stride, 0, p->out_h_stride, o0, o1);
+    if (overlaps(w0, w1, o0, o1)) return fail(KDA_EINVAL, "workspace overlaps out");
+    if (p->N > 0) {
+      const uintptr_t s0 = reinterpret_cast<uintptr_t>(p->state);
+      const uintptr_t s1 = s0 + (uintptr_t)((int64_t)(p->N - 1) * p->state_slot_stride + (int64_t)p->H * 128 * 128) * 2;
+      if (overlaps(w0, w1, s0, s1)) return fail(KDA_EINVAL, "workspace overlaps the state pool");
+    }
+  }
+  cudaError_t e =
+      kda::launch_prefill_chain(*p, sq->cu_seqlens, sq->num_seqs, workspace, bulk, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_prefill_ws launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -26,6 +26,12 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
   return d;
 }
 
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Warp sums of per-lane values through a per-warp shared-memory tile: lane r
 // puts its value i at row i, column r (the 32 lanes' stores of one value are
 // one contiguous row), then lane l sums row l over the 32 lanes as a fixed

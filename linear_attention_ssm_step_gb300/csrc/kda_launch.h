@@ -40,4 +40,18 @@ cudaError_t launch_verify_tc(const kda_params& p, int T, bool bulk, cudaStream_t
 // plain loads and stores.
 cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, bool bulk, cudaStream_t s);
 
+// Bytes of one chunk image of the two-stage prefill (kda_prefill_chain.cu):
+// the operands of one 16-token chunk of one head.
+constexpr uint32_t kPrefillChunkImageBytes = 45568u;
+
+// Chunk images a two-stage prefill of B token rows, num_seqs sequences and H
+// heads may write: (ceil(B / 16) + num_seqs) * H.
+long long prefill_chunk_images(int B, int num_seqs, int H);
+
+// Two-stage varlen prefill: the preparation kernel writes every chunk's image
+// into `ws` (prefill_chunk_images(...) images, 16-byte aligned), then the
+// chain kernel runs each (sequence, head) through its chunks. bulk as above.
+cudaError_t launch_prefill_chain(const kda_params& p, const int32_t* cu, int num_seqs, void* ws, bool bulk,
+                                 cudaStream_t s);
+
 }  // namespace kda

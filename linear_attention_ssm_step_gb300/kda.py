@@ -79,6 +79,10 @@ EXPORTS = {
     "kda_verify": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "kda_prefill": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaSeqs), ctypes.c_void_p], ctypes.c_int),
     "kda_select_prefill_config": ([ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
+    "kda_prefill_ws": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaSeqs), ctypes.c_void_p, ctypes.c_size_t,
+                        ctypes.c_void_p], ctypes.c_int),
+    "kda_prefill_workspace_bytes": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32], ctypes.c_size_t),
+    "kda_select_prefill_ws_config": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
     "kda_verify_ring": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.POINTER(KdaRingParams),
                          ctypes.c_void_p], ctypes.c_int),
     "kda_num_configs": ([], ctypes.c_int32),
@@ -373,16 +377,27 @@ def _ring_params(state, H, k_cache, u_cache, g_cache, hist_len, flush_min, resta
 
 def kda_prefill(state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
                 lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
-                stream=None):
+                stream=None, workspace=None):
     """Varlen prefill (include/kda_prefill.h). q, k, v, g_raw: bf16 [L, H, 128]
     views with one row per token (any row and head stride); beta_logit: bf16
     [L, H]; cu_seqlens: int32 [S + 1] on the device, sequence i owning rows
     cu_seqlens[i] .. cu_seqlens[i+1]-1; state_indices: int32 [S], one slot per
     sequence; state: bf16 [N, H, 128, 128] pool, read as each sequence's
     initial state and overwritten with its final state. Returns out bf16
-    [L, H, 128] (rows no sequence covers are left as they were)."""
+    [L, H, 128] (rows no sequence covers are left as they were).
+    workspace: None (kda_prefill, configurations 0-4) or a device byte tensor
+    of at least prefill_workspace_bytes(L, S, H) (kda_prefill_ws, which may
+    then choose the two-stage configuration 5)."""
     if out is None:
         out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
+    fn, args, _ = _prefill_call(state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias,
+                                out, lower_bound, scale, error_word, config_override, gate_mode, stream, workspace)
+    _check(fn(*args))
+    return out
+
+
+def _prefill_call(state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias, out,
+                  lower_bound, scale, error_word, config_override, gate_mode, stream, workspace):
     _need(cu_seqlens, "cu_seqlens", torch.int32)
     if cu_seqlens.dim() != 1 or cu_seqlens.shape[0] < 1 or not cu_seqlens.is_contiguous():
         raise ValueError("cu_seqlens must be a contiguous [S + 1] tensor")
@@ -390,27 +405,44 @@ def kda_prefill(state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_
     p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
                 lower_bound, scale, error_word, config_override, gate_mode, n_indices=S)
     sq = KdaSeqs(cu_seqlens.data_ptr(), S)
-    _check(load_library().kda_prefill(ctypes.byref(p), ctypes.byref(sq), _stream_handle(stream, q.device)))
-    return out
+    keep = (p, sq, state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias, error_word,
+            workspace)
+    lib = load_library()
+    handle = _stream_handle(stream, q.device)
+    if workspace is None:
+        return lib.kda_prefill, (ctypes.byref(p), ctypes.byref(sq), handle), keep
+    _need(workspace, "workspace", torch.uint8)
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous byte tensor")
+    return lib.kda_prefill_ws, (ctypes.byref(p), ctypes.byref(sq), workspace.data_ptr(), workspace.numel(),
+                                handle), keep
 
 
 def prepare_prefill(state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
                     lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
-                    stream=None):
+                    stream=None, workspace=None):
     """kda_prefill bound to these tensors (see PreparedCall); same arguments. The
     sequence count is fixed by cu_seqlens' length; its contents may change."""
     if out is None:
         out = torch.empty((q.shape[0], q.shape[1], 128), dtype=torch.bfloat16, device=q.device)
-    _need(cu_seqlens, "cu_seqlens", torch.int32)
-    if cu_seqlens.dim() != 1 or cu_seqlens.shape[0] < 1 or not cu_seqlens.is_contiguous():
-        raise ValueError("cu_seqlens must be a contiguous [S + 1] tensor")
-    S = cu_seqlens.shape[0] - 1
-    p = _params(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, None,
-                lower_bound, scale, error_word, config_override, gate_mode, n_indices=S)
-    sq = KdaSeqs(cu_seqlens.data_ptr(), S)
-    keep = (p, sq, state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias, error_word)
-    return PreparedCall(load_library().kda_prefill, (ctypes.byref(p), ctypes.byref(sq),
-                                                     _stream_handle(stream, q.device)), out, keep)
+    fn, args, keep = _prefill_call(state, state_indices, cu_seqlens, q, k, v, g_raw, beta_logit, A_log, dt_bias,
+                                   out, lower_bound, scale, error_word, config_override, gate_mode, stream,
+                                   workspace)
+    return PreparedCall(fn, args, out, keep)
+
+
+def prefill_workspace_bytes(B, num_seqs, H):
+    """Bytes of the workspace kda_prefill_ws needs (include/kda_prefill.h)."""
+    return int(load_library().kda_prefill_workspace_bytes(B, num_seqs, H))
+
+
+def prefill_workspace(B, num_seqs, H, device):
+    """A device workspace for prefill calls of up to B token rows and num_seqs sequences of H heads."""
+    return torch.empty(max(16, prefill_workspace_bytes(B, num_seqs, H)), dtype=torch.uint8, device=device)
+
+
+def kda_select_prefill_ws_config(B, num_seqs, H=12):
+    return int(load_library().kda_select_prefill_ws_config(B, num_seqs, H))
 
 
 def kda_select_prefill_config(num_seqs, H=12):

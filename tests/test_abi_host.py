@@ -315,3 +315,48 @@ def test_prefill_validation(lib):
     assert call(kda.KdaSeqs(cu, 2)) == kda.KDA_OK  # no token rows: nothing launched
     assert [lib.kda_select_prefill_config(s, 12) for s in (1, 8, 512)] == [4, 4, 4]
     assert lib.kda_select_prefill_config(-1, 12) == -1 and lib.kda_select_prefill_config(1, 0) == -1
+
+
+@no_gpu
+def test_prefill_ws_validation(lib):
+    """kda_prefill_ws: configuration 5 needs a workspace of the size
+    kda_prefill_workspace_bytes gives, 16-byte aligned and apart from the
+    call's other buffers; other configurations go to kda_prefill's checks; the
+    selector takes the two-stage kernels from an average of 512 tokens per
+    sequence."""
+    p = fake_params(B=40)
+    cu = (1 << 32) + 10 * (1 << 24)
+    sq = kda.KdaSeqs(cu, 2)
+    need = ((40 + 15) // 16 + 2) * 12 * 45568
+    assert lib.kda_prefill_workspace_bytes(40, 2, 12) == need
+    assert [lib.kda_prefill_workspace_bytes(*a) for a in ((0, 2, 12), (40, 0, 12), (40, 2, 0), (-1, 2, 12))] == [0] * 4
+    ws = (1 << 32) + 32 * (1 << 24)
+
+    def call(w, n, s=sq):
+        return lib.kda_prefill_ws(ctypes.byref(p), None if s is None else ctypes.byref(s), w, n, None)
+
+    p.config_override = 5
+    assert call(None, need) == kda.KDA_EINVAL and "workspace" in kda.kda_last_error()
+    assert call(ws + 8, need) == kda.KDA_EINVAL and "aligned" in kda.kda_last_error()
+    assert call(ws, need - 16) == kda.KDA_EINVAL and "workspace_bytes" in kda.kda_last_error()
+    assert call(p.out, need) == kda.KDA_EINVAL and "overlaps out" in kda.kda_last_error()
+    assert call(p.state, need) == kda.KDA_EINVAL and "state pool" in kda.kda_last_error()
+    assert call(p.q.ptr, need) == kda.KDA_EINVAL and "overlaps q" in kda.kda_last_error()
+    assert call(ws, need, None) == kda.KDA_EINVAL and "seqs" in kda.kda_last_error()
+    assert call(ws, need, kda.KdaSeqs(None, 2)) == kda.KDA_EINVAL and "cu_seqlens" in kda.kda_last_error()
+    assert call(ws, need, kda.KdaSeqs(cu, -1)) == kda.KDA_EINVAL
+    assert call(None, 0, kda.KdaSeqs(None, 0)) == kda.KDA_OK  # no sequence: nothing to do
+    p.K = 64
+    assert call(ws, need) == kda.KDA_EUNSUPPORTED
+    p.K = 128
+    p.config_override = 6
+    assert call(ws, need) == kda.KDA_EINVAL and "config_override" in kda.kda_last_error()
+    p.config_override = 4  # a single-kernel configuration: kda_prefill's checks, no workspace needed
+    assert call(None, 0, kda.KdaSeqs(cu + 2, 2)) == kda.KDA_EINVAL and "cu_seqlens" in kda.kda_last_error()
+    p.config_override = 5
+    p.B = 0
+    assert call(None, 0) == kda.KDA_OK  # no token rows: nothing launched
+    sel = lib.kda_select_prefill_ws_config
+    assert [sel(4096, 1, 12), sel(16384, 1, 16), sel(8 * 2048, 8, 12), sel(512 * 3, 3, 12)] == [5, 5, 5, 5]
+    assert [sel(64 * 256, 64, 12), sel(512 * 16, 512, 12), sel(511 * 10, 10, 12), sel(100, 0, 12)] == [4, 4, 4, 4]
+    assert sel(-1, 1, 12) == -1 and sel(16, -1, 12) == -1 and sel(16, 1, 0) == -1

@@ -124,6 +124,24 @@ def test_prefill_timeout_skips_and_reports(dev, wlib):
     assert torch.equal(wd.state.cpu().view(torch.int16), w.state.view(torch.int16))
 
 
+def test_prefill_two_stage_timeout_skips_and_reports(dev, wlib):
+    """Configuration 5: the chain kernel's waits for the state and for its
+    chunk images run out; the preparation kernel, which waits for nothing,
+    still fills the workspace."""
+    w = workloads.prefill_inputs([5, 19, 1, 70], 8, seed=735)
+    wd = w.to(dev)
+    L = w.q.shape[0]
+    out, err = _sentinel_out((L, 12, 128), dev), _err(dev)
+    p = _params(wd, out, err, n_indices=4)
+    p.config_override = 5
+    sq = kda.KdaSeqs(wd.cu_seqlens.data_ptr(), 4)
+    ws = torch.empty(int(wlib.kda_prefill_workspace_bytes(L, 4, 12)), dtype=torch.uint8, device=dev)
+    assert wlib.kda_prefill_ws(ctypes.byref(p), ctypes.byref(sq), ws.data_ptr(), ws.numel(),
+                               kda._stream_handle(None, dev)) == kda.KDA_OK
+    _expect_timeout(err, out)
+    assert torch.equal(wd.state.cpu().view(torch.int16), w.state.view(torch.int16))
+
+
 def test_fp8_decode_timeout_skips_and_reports(dev, wlib):
     w = workloads.decode_inputs(4, 6, seed=740)
     codes, scales = workloads.fp8_pool(6, seed=741)
