@@ -27,7 +27,9 @@ carries:
                B = 1, 32, 512 (0/50/100% of rows folding), L2-cold, and the
                varlen prefill at 1 x 4096, 8 x 2048, 64 x 256 and 512 x 16
                tokens (H = 12) and two shapes of the prefill page (H = 16,
-               1 x 16384; H = 4, lengths 1..15), each with its median and
+               1 x 16384; H = 4, lengths 1..15) with a caller's workspace
+               and the library's choice of configuration (two stages from
+               512 tokens per sequence), each with its median and
                10th/90th percentiles, and (state GB/s points) the fraction
                of the measured HBM peak.
                streaming_reference: a plain PyTorch in-place multiply over the
@@ -439,8 +441,9 @@ def sweep(dev, steps=100, warmup=100):
         wd = w.to(dev)
         st0 = wd.state.clone()
         out = torch.empty((toks, Hh, 128), dtype=torch.bfloat16, device=dev)
+        ws = kda.prefill_workspace(toks, S, Hh, dev)  # the caller-owned workspace, allocated once
         fn = lambda: kda.kda_prefill(wd.state, wd.state_indices, wd.cu_seqlens, wd.q, wd.k, wd.v,  # noqa: E731
-                                     wd.g_raw, wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
+                                     wd.g_raw, wd.beta_logit, wd.A_log, wd.dt_bias, out=out, workspace=ws)
 
         def reset():
             wd.state.copy_(st0)
@@ -451,8 +454,10 @@ def sweep(dev, steps=100, warmup=100):
         flops = traffic.prefill_flops(toks, Hh)
         res["prefill"].append({"case": name, "H": Hh, "seqs": S, "tokens": toks, "us": us, "us_p10": p10,
                                "us_p90": p90, "Mtokens/s": round(toks / us, 3),
-                               "TFLOP/s": round(flops / us / 1e6, 2), "config": kda.kda_select_prefill_config(S, Hh)})
-        del w, wd, st0, out
+                               "TFLOP/s": round(flops / us / 1e6, 2),
+                               "config": kda.kda_select_prefill_ws_config(toks, S, Hh),
+                               "workspace_MB": round(ws.numel() / 1e6, 1)})
+        del w, wd, st0, out, ws
     res["t8_ring_w32"] = t8_ring_points(dev, [(1, 32), (32, 32), (512, 32)], steps, warmup, flush)
     # the pages' own ring width for T = 8, at the serving batch
     res["t8_ring_w16"] = t8_ring_points(dev, [(512, 16)], steps, warmup, flush)
