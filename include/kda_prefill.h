@@ -127,6 +127,36 @@ size_t kda_prefill_workspace_bytes(int32_t B, int32_t num_seqs, int32_t H);
    the preparation-and-chain schedules are selected from the input shape. */
 int32_t kda_select_prefill_ws_config(int32_t B, int32_t num_seqs, int32_t H);
 
+/*
+ * Two-stage prefill that allocates nothing, with the workspace inside the
+ * library. The paper has no counterpart: this entry point exists for callers
+ * of this library that cannot call cudaMalloc when they run a prefill (a
+ * step captured into a CUDA graph in global capture mode, where allocation
+ * calls are not permitted; a plugin whose host framework owns all device
+ * memory and forbids allocation while it enqueues work; a server that
+ * reserved all device memory for its state pools at start-up).
+ *
+ * It runs configuration 5 of kda_prefill_ws with the workspace in a fixed
+ * array of KDA_PREFILL_STATIC_BYTES (64 MiB) compiled into the library:
+ * every GPU that loads the library holds those 64 MiB until the process
+ * exits. The caller passes inputs and outputs as for kda_prefill_ws.
+ *   - Limit: a call whose kda_prefill_workspace_bytes(B, num_seqs, H) exceeds
+ *     64 MiB (more than 1472 chunk images; e.g. one sequence of more than
+ *     1936 tokens at H = 12) is rejected with KDA_EUNSUPPORTED and a message
+ *     giving both sizes, before anything is launched; use kda_prefill_ws.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     with that device current; make that first call before any stream
+ *     capture. Later calls only launch.
+ *   - Sharing: every call uses the same array, which keeps the last call's
+ *     contents; nothing in it has to start at zero (a call reads only what it
+ *     wrote itself). Calls that overlap on the GPU (other streams, other host
+ *     threads) race on the array and give undefined results.
+ *   - config_override: -1 or 5 (both run configuration 5), else KDA_EINVAL;
+ *     everything else as kda_prefill_ws.
+ */
+#define KDA_PREFILL_STATIC_BYTES (64u * 1024u * 1024u)
+kda_status kda_prefill_static(const kda_params* p, const kda_seqs* s, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -341,6 +341,28 @@ kda_status kda_prefill_ws(const kda_params* p, const kda_seqs* sq, void* workspa
   return ok();
 }
 
+kda_status kda_prefill_static(const kda_params* p, const kda_seqs* sq, void* stream) {
+  if (p == nullptr) return fail(KDA_EINVAL, "params is NULL");
+  if (sq == nullptr) return fail(KDA_EINVAL, "seqs is NULL");
+  if (p->config_override != -1 && p->config_override != kChainConfig)
+    return fail(KDA_EINVAL, "config_override = %d: kda_prefill_static runs configuration %d only (or -1)",
+                p->config_override, kChainConfig);
+  kda_params q = *p;
+  q.config_override = kChainConfig;
+  if (sq->num_seqs <= 0 || p->B <= 0) return kda_prefill_ws(&q, sq, nullptr, 0, stream);  // nothing is launched
+  const size_t need = kda_prefill_workspace_bytes(p->B, sq->num_seqs, p->H);
+  if (need > (size_t)KDA_PREFILL_STATIC_BYTES)
+    return fail(KDA_EUNSUPPORTED,
+                "kda_prefill_static: B = %d, num_seqs = %d, H = %d need %zu bytes of workspace, above its fixed %zu; "
+                "use kda_prefill_ws",
+                p->B, sq->num_seqs, p->H, need, (size_t)KDA_PREFILL_STATIC_BYTES);
+  void* ws = nullptr;
+  const cudaError_t e = kda::prefill_static_workspace(&ws);
+  if (e != cudaSuccess)
+    return fail(KDA_ELAUNCH, "kda_prefill_static: the workspace's device address: %s", cudaGetErrorString(e));
+  return kda_prefill_ws(&q, sq, ws, KDA_PREFILL_STATIC_BYTES, stream);
+}
+
 kda_status kda_decode_fp8(const kda_params* p, const kda_fp8_pool* f, void* stream) {
   if (p == nullptr) return fail(KDA_EINVAL, "params is NULL");
   // The shared checks without the bf16 pool's (N = 0 there); the fp8 pool's follow.

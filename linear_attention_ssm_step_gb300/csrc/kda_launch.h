@@ -54,4 +54,8 @@ long long prefill_chunk_images(int B, int num_seqs, int H);
 cudaError_t launch_prefill_chain(const kda_params& p, const int32_t* cu, int num_seqs, void* ws, bool bulk,
                                  cudaStream_t s);
 
+// The device address of the fixed workspace of kda_prefill_static on the
+// current device (looked up on the first call per device).
+cudaError_t prefill_static_workspace(void** ptr);
+
 }  // namespace kda

@@ -46,6 +46,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "kda_chunk.cuh"
 #include "kda_device.cuh"
@@ -668,6 +669,30 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
+
+// The workspace of kda_prefill_static: one fixed array per device that loads
+// the library, for callers that cannot allocate. Host code must not pass the
+// array's name to a kernel (on the host it names a stand-in, not device
+// memory); prefill_static_workspace gives its device address.
+static __device__ __align__(256) unsigned char g_prefill_static_ws[KDA_PREFILL_STATIC_BYTES];
+
+cudaError_t prefill_static_workspace(void** ptr) {
+  constexpr int kMaxDevices = 256;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {  // once per device, with that device current
+    void* a = nullptr;
+    if ((e = cudaGetSymbolAddress(&a, g_prefill_static_ws)) != cudaSuccess) return e;
+    addr[dev] = a;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 long long prefill_chunk_images(int B, int num_seqs, int H) {
   return ((long long)(B + CH - 1) / CH + num_seqs) * (long long)H;

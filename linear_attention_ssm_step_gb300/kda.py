@@ -82,6 +82,7 @@ EXPORTS = {
     "kda_prefill_ws": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaSeqs), ctypes.c_void_p, ctypes.c_size_t,
                         ctypes.c_void_p], ctypes.c_int),
     "kda_prefill_workspace_bytes": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32], ctypes.c_size_t),
+    "kda_prefill_static": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaSeqs), ctypes.c_void_p], ctypes.c_int),
     "kda_select_prefill_ws_config": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
     "kda_verify_ring": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.POINTER(KdaRingParams),
                          ctypes.c_void_p], ctypes.c_int),
