@@ -331,16 +331,23 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
 
 // ---------------------------------------------------------------- chain
 
-// 256 threads: thread i is value row i % 128 of half i / 128. In the state's
-// conversion a half takes 64 of the 128 key columns; in the epilogue 8 of the
-// 16 tokens.
-constexpr int CN_THREADS = 256;
+// 288 threads. Threads 0..255 (warps 0-7) work on the state: thread i is
+// value row i % 128 of half i / 128; in the state's conversion a half takes
+// 64 of the 128 key columns, in the epilogue 8 of the 16 tokens. Warp 8
+// issues the tensor-core products and the chunk-image copies, so that the
+// conversion never waits for an issue: the state warps signal it through
+// named barriers (bar.arrive) and go on.
+constexpr int CN_WORKERS = 256;
+constexpr int CN_THREADS = CN_WORKERS + 32;
+constexpr int CN_MMA_WARP = CN_WORKERS / 32;
 constexpr uint32_t CN_TMEM_COLS = 512;
 constexpr uint32_t CN_D = 128;   // D of the first product: columns 128..159
 constexpr uint32_t CN_AS = 256;  // S as two bf16 parts, the first product's A operand: part p at 256 + 64 p
 constexpr uint32_t CN_AU = 384;  // u as three bf16 parts, the update's A operand: part p at 384 + 8 p
 constexpr int CN_NBUF = 3;       // chunk images in flight
 constexpr uint32_t CN_IMG_STRIDE = (kPrefillChunkImageBytes + 1023u) & ~1023u;
+// Named barriers between the state warps and the issuing warp.
+constexpr uint32_t CN_BAR_ROUND0 = 1, CN_BAR_ROUND1 = 2, CN_BAR_U = 3;
 
 struct CnLayout {
   uint32_t a, img, bar, tslot, scratch, total;
@@ -357,8 +364,8 @@ __host__ __device__ inline CnLayout cn_layout() {
   o += 64u;
   L.tslot = o;
   o += 16u;
-  L.scratch = o;
-  o += 32u;
+  L.scratch = o;  // one int per warp (chunk_base)
+  o += 64u;
   L.total = o;
   return L;
 }
@@ -371,7 +378,8 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
                              const int32_t* __restrict__ cu, const int num_seqs,
                              const unsigned char* __restrict__ ws, const long long ws_images) {
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int row = tid & (KD - 1), hf = tid >> 7;
+  const bool worker = tid < CN_WORKERS, issuer = warp == CN_MMA_WARP;
+  const int row = tid & (KD - 1), hf = tid >> 7;  // meaningful in the state warps
   const int total = num_seqs * p.H;
 
   extern __shared__ unsigned char smem_raw[];
@@ -417,14 +425,16 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
     }
     const int64_t ob = (int64_t)h * p.out_h_stride + row;  // output element of row `row`, + token row * out_b_stride
     if (n < 0 || n >= p.N || broken) {
-      for (int t = t0 + hf; t < t1; t += 2) outp[(int64_t)t * p.out_b_stride + ob] = 0;
+      if (worker)
+        for (int t = t0 + hf; t < t1; t += 2) outp[(int64_t)t * p.out_b_stride + ob] = 0;
       continue;
     }
     if (t0 == t1) continue;
     const int base = chunk_base(cu, seq, p.B, scratch);
     const int nch = (t1 - t0 + CH - 1) / CH;
     if ((long long)(base + nch) * p.H > ws_images) {  // only overlapping token ranges get here (undefined)
-      for (int t = t0 + hf; t < t1; t += 2) outp[(int64_t)t * p.out_b_stride + ob] = 0;
+      if (worker)
+        for (int t = t0 + hf; t < t1; t += 2) outp[(int64_t)t * p.out_b_stride + ob] = 0;
       continue;
     }
     uint16_t* gstate = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride + (int64_t)h * KD * KD;
@@ -439,7 +449,7 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
         tma_load_3d(sA + KD * 128, &smap, 64, h * KD, n, barA);
       }
       pendA = true;
-    } else {
+    } else if (worker) {
       for (int r = hf; r < KD; r += 2)
         *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, row)) = gstate[(int64_t)r * KD + row];
     }
@@ -479,7 +489,7 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
       pendI &= ~(1u << b);
       if (j >= 1 && j + 2 < nch) {  // chunk j + 2 into the buffer chunk j - 1 has released
         const int bn = (j + 2) % CN_NBUF;
-        if (tid == 0) {
+        if (tid == CN_WORKERS) {
           mbar_expect_tx(barI + bn, kPrefillChunkImageBytes);
           bulk_g2s(sImg + bn * CN_IMG_STRIDE, image(j + 2), kPrefillChunkImageBytes, barI + bn);
         }
@@ -487,64 +497,70 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
       }
       tc_fence_after();
 
-      // 2. In two rounds, each half converts one 32-column block of row `row`:
-      // S into its bf16 parts (tensor memory, the A operand) and S <- P_{C-1} S;
-      // after each round warp 0 issues the first product's K steps that
-      // the round completed (block cb holds K steps 2 cb and 2 cb + 1). D[row][t']
-      // = sum_k S[row][k] XB[t'][k]: the high parts of both, the low part of S
-      // with the high rows of XB, the high part of S with the low rows (the
-      // first chunk's S is exact in one part; its low part is written as zero).
-      const float* splast = reinterpret_cast<const float*>(im + IMG_PL);
-      const uint32_t x0 = smem_addr(im + IMG_XB);
+      // 2. In two rounds, each half of the state warps converts one 32-column
+      // block of row `row`: S into its bf16 parts (tensor memory, the A
+      // operand) and S <- P_{C-1} S; after each round the issuing warp issues
+      // the first product's K steps that the round completed (block cb holds
+      // K steps 2 cb and 2 cb + 1). D[row][t'] = sum_k S[row][k] XB[t'][k]:
+      // the high parts of both, the low part of S with the high rows of XB,
+      // the high part of S with the low rows (the first chunk's S is exact in
+      // one part; its low part is written as zero).
+      if (worker) {
+        const float* splast = reinterpret_cast<const float*>(im + IMG_PL);
 #pragma unroll
-      for (int rd = 0; rd < 2; ++rd) {
-        const int cb = 2 * hf + rd;
-        float s[32];
-        if (first) {  // the slot's bf16 row, exact: one part
-          uint32_t hw[16];
+        for (int rd = 0; rd < 2; ++rd) {
+          const int cb = 2 * hf + rd;
+          float s[32];
+          if (first) {  // the slot's bf16 row, exact: one part
+            uint32_t hw[16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(sA + sw128_offset(KD, row, cb * 32 + 8 * c));
-            hw[4 * c] = raw.x;
-            hw[4 * c + 1] = raw.y;
-            hw[4 * c + 2] = raw.z;
-            hw[4 * c + 3] = raw.w;
+            for (int c = 0; c < 4; ++c) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(sA + sw128_offset(KD, row, cb * 32 + 8 * c));
+              hw[4 * c] = raw.x;
+              hw[4 * c + 1] = raw.y;
+              hw[4 * c + 2] = raw.z;
+              hw[4 * c + 3] = raw.w;
+            }
+#pragma unroll
+            for (int q = 0; q < 16; ++q) unpack_bf16x2(hw[q], s[2 * q], s[2 * q + 1]);
+            tmem_st16(row_tmem + CN_AS + cb * 16, hw);
+            uint32_t zw[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) zw[q] = 0u;
+            tmem_st16(row_tmem + CN_AS + 64 + cb * 16, zw);  // the low part of an exact state is zero
+          } else {
+            tmem_ld32(row_tmem + cb * 32, s);
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float s0 = s[2 * q], s1 = s[2 * q + 1];
+              hw[q] = pack_bf16x2(s0, s1);
+              lw[q] = f32x2_to_bf16x2(sub2(pk2(s0, s1), bf16x2_to_f32x2(hw[q])));
+            }
+            tmem_st16(row_tmem + CN_AS + cb * 16, hw);
+            tmem_st16(row_tmem + CN_AS + 64 + cb * 16, lw);
           }
 #pragma unroll
-          for (int q = 0; q < 16; ++q) unpack_bf16x2(hw[q], s[2 * q], s[2 * q + 1]);
-          tmem_st16(row_tmem + CN_AS + cb * 16, hw);
-          uint32_t zw[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) zw[q] = 0u;
-          tmem_st16(row_tmem + CN_AS + 64 + cb * 16, zw);  // the low part of an exact state is zero
-        } else {
-          tmem_ld32(row_tmem + cb * 32, s);
-          uint32_t hw[16], lw[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float s0 = s[2 * q], s1 = s[2 * q + 1];
-            hw[q] = pack_bf16x2(s0, s1);
-            lw[q] = f32x2_to_bf16x2(sub2(pk2(s0, s1), bf16x2_to_f32x2(hw[q])));
+          for (int c = 0; c < 8; ++c) {
+            const float4 pl = *reinterpret_cast<const float4*>(splast + cb * 32 + 4 * c);
+            f32x2 a = mul2(pk2(pl.x, pl.y), pk2(s[4 * c], s[4 * c + 1]));
+            f32x2 bb = mul2(pk2(pl.z, pl.w), pk2(s[4 * c + 2], s[4 * c + 3]));
+            upk2(a, s[4 * c], s[4 * c + 1]);
+            upk2(bb, s[4 * c + 2], s[4 * c + 3]);
           }
-          tmem_st16(row_tmem + CN_AS + cb * 16, hw);
-          tmem_st16(row_tmem + CN_AS + 64 + cb * 16, lw);
+          tmem_st32(row_tmem + cb * 32, s);
+          tmem_st_wait();
+          tc_fence_before();
+          bar_arrive(rd == 0 ? CN_BAR_ROUND0 : CN_BAR_ROUND1, CN_THREADS);
         }
+      } else if (issuer) {
+        const uint32_t x0 = smem_addr(im + IMG_XB);
+        const uint32_t tb = __shfl_sync(0xffffffffu, tmem, 0), xb = __shfl_sync(0xffffffffu, x0, 0);
+        constexpr uint32_t idesc = idesc_bf16_f32(128, 2 * CH);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 pl = *reinterpret_cast<const float4*>(splast + cb * 32 + 4 * c);
-          f32x2 a = mul2(pk2(pl.x, pl.y), pk2(s[4 * c], s[4 * c + 1]));
-          f32x2 bb = mul2(pk2(pl.z, pl.w), pk2(s[4 * c + 2], s[4 * c + 3]));
-          upk2(a, s[4 * c], s[4 * c + 1]);
-          upk2(bb, s[4 * c + 2], s[4 * c + 3]);
-        }
-        tmem_st32(row_tmem + cb * 32, s);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) {
+        for (int rd = 0; rd < 2; ++rd) {
+          bar_sync(rd == 0 ? CN_BAR_ROUND0 : CN_BAR_ROUND1, CN_THREADS);
           tc_fence_after();
-          constexpr uint32_t idesc = idesc_bf16_f32(128, 2 * CH);
-          const uint32_t tb = __shfl_sync(0xffffffffu, tmem, 0), xb = __shfl_sync(0xffffffffu, x0, 0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {  // K steps of blocks rd and 2 + rd
             const int kk = (i < 2 ? 2 * rd : 4 + 2 * rd) + (i & 1);
@@ -554,8 +570,8 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
             tc_mma_bf16_ta_w(tb + CN_D, ak, sw128_desc(xk + IMG_XB_LO), idesc, 1u);
             tc_mma_bf16_ta_w(tb + CN_D, ak + 64, sw128_desc(xk), idesc, 1u);
           }
-          if (rd == 1) tc_commit_w(barD);
         }
+        tc_commit_w(barD);
       }
       pendD = true;
       ok = __syncthreads_and(mbar_wait_bounded(barD, phD)) != 0;
@@ -565,51 +581,54 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
       tc_fence_after();
 
       // 3. Tokens 8 hf .. 8 hf + 7 of row `row`: u_t = U_t + D_t as three bf16
-      // parts into tensor memory (the update's A operand).
-      float dx[8], dy[8];
-      tmem_ld8(row_tmem + CN_D + 8 * hf, dx);
-      tmem_ld8(row_tmem + CN_D + CH + 8 * hf, dy);
-      const float* gu = reinterpret_cast<const float*>(im + IMG_U) + (8 * hf) * KD + row;
-      {
-        uint32_t w0[4], w1[4], w2[4];
+      // parts into tensor memory (the update's A operand); 4. the issuing warp
+      // issues S += sum_t u_t K~_t (the products of order <= 2 of the three
+      // parts of each) while the state warps form the chunk's outputs.
+      if (worker) {
+        float dx[8], dy[8];
+        tmem_ld8(row_tmem + CN_D + 8 * hf, dx);
+        tmem_ld8(row_tmem + CN_D + CH + 8 * hf, dy);
+        const float* gu = reinterpret_cast<const float*>(im + IMG_U) + (8 * hf) * KD + row;
+        {
+          uint32_t w0[4], w1[4], w2[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const f32x2 u = add2(pk2(gu[(2 * q) * KD], gu[(2 * q + 1) * KD]), pk2(dx[2 * q], dx[2 * q + 1]));
-          w0[q] = f32x2_to_bf16x2(u);
-          const f32x2 r1 = sub2(u, bf16x2_to_f32x2(w0[q]));
-          w1[q] = f32x2_to_bf16x2(r1);
-          w2[q] = f32x2_to_bf16x2(sub2(r1, bf16x2_to_f32x2(w1[q])));
+          for (int q = 0; q < 4; ++q) {
+            const f32x2 u = add2(pk2(gu[(2 * q) * KD], gu[(2 * q + 1) * KD]), pk2(dx[2 * q], dx[2 * q + 1]));
+            w0[q] = f32x2_to_bf16x2(u);
+            const f32x2 r1 = sub2(u, bf16x2_to_f32x2(w0[q]));
+            w1[q] = f32x2_to_bf16x2(r1);
+            w2[q] = f32x2_to_bf16x2(sub2(r1, bf16x2_to_f32x2(w1[q])));
+          }
+          tmem_st4(row_tmem + CN_AU + 4 * hf, w0);
+          tmem_st4(row_tmem + CN_AU + 8 + 4 * hf, w1);
+          tmem_st4(row_tmem + CN_AU + 16 + 4 * hf, w2);
         }
-        tmem_st4(row_tmem + CN_AU + 4 * hf, w0);
-        tmem_st4(row_tmem + CN_AU + 8 + 4 * hf, w1);
-        tmem_st4(row_tmem + CN_AU + 16 + 4 * hf, w2);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncthreads();
-
-      // 4. S += sum_t u_t K~_t (products of order <= 2 of the three parts of
-      // each), while the chunk's outputs are formed.
-      if (warp == 0) {
+        tmem_st_wait();
+        tc_fence_before();
+        bar_arrive(CN_BAR_U, CN_THREADS);
+        const float* go = reinterpret_cast<const float*>(im + IMG_O) + (8 * hf) * KD + row;
+        uint16_t* orow = outp + (int64_t)(c0 + 8 * hf) * p.out_b_stride + ob;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float o = __fmul_rn(p.scale, __fadd_rn(dy[i], go[i * KD]));
+          if (8 * hf + i < Tc) *orow = float_to_bf16_bits(o);
+          orow += p.out_b_stride;
+        }
+      } else if (issuer) {
+        bar_sync(CN_BAR_U, CN_THREADS);
         tc_fence_after();
+        const uint32_t tb = __shfl_sync(0xffffffffu, tmem, 0);
+        const uint32_t w0 = __shfl_sync(0xffffffffu, smem_addr(im + IMG_KW), 0);
         constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
-        const uint32_t w0 = smem_addr(im + IMG_KW);
 #pragma unroll
         for (int q = 0; q < 6; ++q) {
           const uint32_t pa = q < 3 ? (uint32_t)q : (q == 4 ? 1u : 0u);
           const uint32_t pb = q < 3 ? 0u : (q == 5 ? 2u : 1u);
-          tc_mma_bf16_ta_w(tmem, tmem + CN_AU + 8 * pa, sw32_desc(w0 + pb * IMG_KW_PART), idesc, 1u);
+          tc_mma_bf16_ta_w(tb, tb + CN_AU + 8 * pa, sw32_desc(w0 + pb * IMG_KW_PART), idesc, 1u);
         }
         tc_commit_w(barU);
       }
       pendU = true;
-      const float* go = reinterpret_cast<const float*>(im + IMG_O) + (8 * hf) * KD + row;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int t = 8 * hf + i;
-        const float o = __fmul_rn(p.scale, __fadd_rn(dy[i], go[i * KD]));
-        if (t < Tc) outp[(int64_t)(c0 + t) * p.out_b_stride + ob] = float_to_bf16_bits(o);
-      }
       first = false;
     }
 
@@ -619,23 +638,25 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
         phU ^= 1u;
         pendU = false;
         tc_fence_after();
-        uint16_t* grow = gstate + (int64_t)row * KD;
+        if (worker) {
+          uint16_t* grow = gstate + (int64_t)row * KD;
 #pragma unroll 1
-        for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
-          float s[32];
-          tmem_ld32(row_tmem + cb * 32, s);
-          uint32_t w[16];
+          for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
+            float s[32];
+            tmem_ld32(row_tmem + cb * 32, s);
+            uint32_t w[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) w[q] = pack_bf16x2(s[2 * q], s[2 * q + 1]);
-          if constexpr (TMA) {  // 16-byte aligned pool
-            uint4* dst = reinterpret_cast<uint4*>(grow + cb * 32);
+            for (int q = 0; q < 16; ++q) w[q] = pack_bf16x2(s[2 * q], s[2 * q + 1]);
+            if constexpr (TMA) {  // 16-byte aligned pool
+              uint4* dst = reinterpret_cast<uint4*>(grow + cb * 32);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-          } else {
+              for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            } else {
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              grow[cb * 32 + 2 * q] = (uint16_t)(w[q] & 0xffffu);
-              grow[cb * 32 + 2 * q + 1] = (uint16_t)(w[q] >> 16);
+              for (int q = 0; q < 16; ++q) {
+                grow[cb * 32 + 2 * q] = (uint16_t)(w[q] & 0xffffu);
+                grow[cb * 32 + 2 * q + 1] = (uint16_t)(w[q] >> 16);
+              }
             }
           }
         }
@@ -644,7 +665,8 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
     if (!ok) {  // a bounded wait gave up: the sequence is skipped, and every later one
       broken = true;
       if (tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
-      for (int t = t0 + hf; t < t1; t += 2) outp[(int64_t)t * p.out_b_stride + ob] = 0;
+      if (worker)
+        for (int t = t0 + hf; t < t1; t += 2) outp[(int64_t)t * p.out_b_stride + ob] = 0;
     }
     tc_fence_before();
     __syncthreads();  // this item's tensor-memory and shared-memory use is done
