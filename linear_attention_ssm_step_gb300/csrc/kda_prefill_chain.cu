@@ -96,15 +96,21 @@ __device__ int chunk_base(const int32_t* __restrict__ cu, int seq, int B, int* s
 
 // ---------------------------------------------------------------- preparation
 
+// Token inputs staged in shared memory (16-byte aligned views): q, k, v and
+// g_raw of a chunk, [tensor][token][128 channels] bf16, two buffers.
+constexpr uint32_t PP_TOK_BYTES = 4u * CH * KD * 2u;
+
 struct PpLayout {
-  uint32_t stage, red, fcp, rn, beta, xpose, scratch, total;
+  uint32_t stage, tok, red, fcp, rn, beta, xpose, scratch, total;
 };
 
-__host__ __device__ inline PpLayout pp_layout() {
+__host__ __device__ inline PpLayout pp_layout(bool vec) {
   PpLayout L{};
   uint32_t o = 0;
   L.stage = o;  // XB and KW of the chunk being written
   o += IMG_STAGED;
+  L.tok = o;
+  if (vec) o += 2u * PP_TOK_BYTES;
   L.red = o;  // per-warp partial sums: norms, then the coefficients
   o += (1u + CH * CH / 32u) * 512u;
   L.fcp = o;  // (cc[t][s], ec[t][s]) at pair t * 16 + s
@@ -121,11 +127,37 @@ __host__ __device__ inline PpLayout pp_layout() {
   return L;
 }
 
-__host__ __device__ inline size_t pp_smem_bytes() { return (size_t)pp_layout().total + 1024; }
+__host__ __device__ inline size_t pp_smem_bytes(bool vec) { return (size_t)pp_layout(vec).total + 1024; }
+
+// 16 bytes global -> shared without registers (cp.async); src_bytes 0 fills zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// q, k, v and g_raw of the chunk of Tc tokens at row c0 (head h) into `buf`,
+// 16 bytes per copy, zeros past Tc: piece i = (tensor, token, 8 channels).
+__device__ __forceinline__ void issue_token_copies(const kda_params& p, int c0, int h, int Tc, unsigned char* buf) {
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int i = threadIdx.x + CH_THREADS * m;  // tensor m / 2, token (i / 16) % 16, channels 8 (i % 16) ..
+    const int t = (i >> 4) & (CH - 1), c8 = i & 15;
+    const kda_view& vw = m < 2 ? p.q : m < 4 ? p.k : m < 6 ? p.v : p.g_raw;
+    const int tt = t < Tc ? t : 0;
+    const uint16_t* src = static_cast<const uint16_t*>(vw.ptr) + (int64_t)(c0 + tt) * vw.b_stride +
+                          (int64_t)h * vw.h_stride + 8 * c8;
+    cp_async16(buf + (uint32_t)i * 16u, src, t < Tc ? 16u : 0u);
+  }
+}
 
 // CTA (sequence, head, z) prepares chunks z, z + Z, z + 2Z, ... of its
 // sequence. p: t_stride = b_stride in every activation view (token t of a
-// chunk starting at row c0 is (b = c0, t)).
+// chunk starting at row c0 is (b = c0, t)). VEC: q, k, v and g_raw rows are
+// 16-byte aligned, and the next chunk's token inputs are copied into shared
+// memory while this one is computed.
+template <bool VEC>
 __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const kda_params p,
                                                                          const int32_t* __restrict__ cu,
                                                                          const int num_seqs, const int Z,
@@ -137,8 +169,9 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  const PpLayout SL = pp_layout();
+  const PpLayout SL = pp_layout(VEC);
   unsigned char* stage = sm + SL.stage;
+  unsigned char* stok = sm + SL.tok;
   float* red = reinterpret_cast<float*>(sm + SL.red);
   float* fcp = reinterpret_cast<float*>(sm + SL.fcp);
   float* rn = reinterpret_cast<float*>(sm + SL.rn);
@@ -157,15 +190,49 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
   const int nch = (t1 - t0 + CH - 1) / CH;
   if (z >= nch) return;
   const int base = chunk_base(cu, seq, p.B, scratch);
+  float alog = 0.0f, dtb = 0.0f;  // A_log[h] and dt_bias[h][tid] (raw gate)
+  if (VEC && p.gate_mode == KDA_GATE_RAW) {
+    alog = p.A_log[h];
+    dtb = p.dt_bias[(int64_t)h * KD + tid];
+  }
+  uint16_t blogit_next = 0;
+  if (VEC) {
+    const int c0 = t0 + z * CH, Tc = min(CH, t1 - c0);
+    issue_token_copies(p, c0, h, Tc, stok);
+    cp_async_commit();
+    if (tid < Tc) blogit_next = load_bits(p.beta_logit, c0, tid, h, 0);
+  }
 
-  for (int j = z; j < nch; j += Z) {
+  for (int j = z, buf = 0; j < nch; j += Z, buf ^= 1) {
     const long long img = (long long)(base + j) * p.H + h;
     if (img >= ws_images) break;  // only overlapping token ranges get here (undefined)
     unsigned char* gimg = ws + img * kPrefillChunkImageBytes;
     const int c0 = t0 + j * CH, Tc = min(CH, t1 - c0);
     TokenRegs<CH> L;
-    zero_tokens(L);
-    load_tokens(p, c0, h, Tc, L);
+    if constexpr (VEC) {
+      L.blogit = blogit_next;
+      L.alog = alog;
+      L.dtb = dtb;
+      if (j + Z < nch) {  // the next chunk's inputs fly while this one is computed
+        const int cn = c0 + Z * CH, Tn = min(CH, t1 - cn);
+        issue_token_copies(p, cn, h, Tn, stok + (buf ^ 1) * PP_TOK_BYTES);
+        blogit_next = tid < Tn ? load_bits(p.beta_logit, cn, tid, h, 0) : (uint16_t)0;
+      }
+      cp_async_commit();
+      cp_async_wait_prev();  // this chunk's copies have landed (each thread's own)
+      __syncthreads();       // and everyone's
+      const uint16_t* tk = reinterpret_cast<const uint16_t*>(stok + buf * PP_TOK_BYTES) + tid;
+#pragma unroll
+      for (int t = 0; t < CH; ++t) {
+        L.qv[t] = tk[(0 * CH + t) * KD];
+        L.kv[t] = tk[(1 * CH + t) * KD];
+        L.vv[t] = tk[(2 * CH + t) * KD];
+        L.gv[t] = tk[(3 * CH + t) * KD];
+      }
+    } else {
+      zero_tokens(L);
+      load_tokens(p, c0, h, Tc, L);
+    }
 
     // L2 norms: block sums of q_t^2 (value t) and k_t^2 (value CH + t).
 #pragma unroll
@@ -327,6 +394,7 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
     }
   }
   if (tid == 0) bulk_wait_all();
+  if (VEC) asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- chain
@@ -554,9 +622,20 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
           bar_arrive(rd == 0 ? CN_BAR_ROUND0 : CN_BAR_ROUND1, CN_THREADS);
         }
       } else if (issuer) {
+        // Every operand is formed before the first barrier, so that the issue
+        // itself (while the state warps convert, on the same schedulers) is
+        // the products alone.
         const uint32_t x0 = smem_addr(im + IMG_XB);
         const uint32_t tb = __shfl_sync(0xffffffffu, tmem, 0), xb = __shfl_sync(0xffffffffu, x0, 0);
         constexpr uint32_t idesc = idesc_bf16_f32(128, 2 * CH);
+        uint64_t bh[8], bl[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t xk = xb + (kk >> 2) * (64 * 128) + (kk & 3) * 32;
+          bh[kk] = sw128_desc(xk);
+          bl[kk] = sw128_desc(xk + IMG_XB_LO);
+        }
+        const uint32_t dcol = tb + CN_D, acol = tb + CN_AS;
 #pragma unroll
         for (int rd = 0; rd < 2; ++rd) {
           bar_sync(rd == 0 ? CN_BAR_ROUND0 : CN_BAR_ROUND1, CN_THREADS);
@@ -564,11 +643,9 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {  // K steps of blocks rd and 2 + rd
             const int kk = (i < 2 ? 2 * rd : 4 + 2 * rd) + (i & 1);
-            const uint32_t ak = tb + CN_AS + kk * 8;
-            const uint32_t xk = xb + (kk >> 2) * (64 * 128) + (kk & 3) * 32;
-            tc_mma_bf16_ta_w(tb + CN_D, ak, sw128_desc(xk), idesc, (rd > 0 || i > 0) ? 1u : 0u);
-            tc_mma_bf16_ta_w(tb + CN_D, ak, sw128_desc(xk + IMG_XB_LO), idesc, 1u);
-            tc_mma_bf16_ta_w(tb + CN_D, ak + 64, sw128_desc(xk), idesc, 1u);
+            tc_mma_bf16_ta_w(dcol, acol + kk * 8, bh[kk], idesc, (rd > 0 || i > 0) ? 1u : 0u);
+            tc_mma_bf16_ta_w(dcol, acol + kk * 8, bl[kk], idesc, 1u);
+            tc_mma_bf16_ta_w(dcol, acol + 64 + kk * 8, bh[kk], idesc, 1u);
           }
         }
         tc_commit_w(barD);
@@ -761,10 +838,14 @@ cudaError_t launch_prefill_chain(const kda_params& p, const int32_t* cu, int num
   // Preparation: Z CTAs per (sequence, head), enough for about 8 CTAs per SM
   // when there are few sequences, never more than a sequence can have chunks.
   {
-    auto kern = kda_prefill_prepare_kernel;
-    const size_t smem = pp_smem_bytes();
-    static std::atomic<bool> smem_set{false};
-    if ((e = set_smem_limit_once(kern, smem, smem_set)) != cudaSuccess) return e;
+    auto aligned_rows = [](const kda_view& v) {
+      return (reinterpret_cast<uintptr_t>(v.ptr) & 15u) == 0 && v.b_stride % 8 == 0 && v.h_stride % 8 == 0;
+    };
+    const bool vec = aligned_rows(q.q) && aligned_rows(q.k) && aligned_rows(q.v) && aligned_rows(q.g_raw);
+    auto kern = vec ? kda_prefill_prepare_kernel<true> : kda_prefill_prepare_kernel<false>;
+    const size_t smem = pp_smem_bytes(vec);
+    static std::atomic<bool> smem_set_vec{false}, smem_set_plain{false};
+    if ((e = set_smem_limit_once(kern, smem, vec ? smem_set_vec : smem_set_plain)) != cudaSuccess) return e;
     const long long per = (long long)num_seqs * p.H;
     const long long want = 8LL * sms;
     long long Z = std::max(1LL, (want + per - 1) / per);
