@@ -88,8 +88,8 @@ int32_t kda_select_prefill_config(int32_t num_seqs, int32_t H);
  * and then a recurrence-chain stage; the review threads pass the stages'
  * shared data through a caller-owned workspace (RecurrentKDAPrefillWorkspace).
  *
- * Configuration 5 of kda_prefill_ws computes the reading above in two
- * kernels on the caller's stream. The first prepares every 16-token chunk of
+ * Configurations 5 and 6 of kda_prefill_ws compute the reading above in two
+ * stages on the caller's stream. The first prepares every 16-token chunk of
  * every (sequence, head) at once: norms, gates, the chunk's 16 x 16
  * coefficients, and then by forward substitution the chunk's contribution to
  * u and o in a form that no longer depends on the state. It writes these
@@ -99,6 +99,14 @@ int32_t kda_select_prefill_config(int32_t num_seqs, int32_t H);
  * parts (exact to about 2^-17), and the update from u and the decayed keys
  * as three bf16 parts (exact to about 2^-24). Its results agree with
  * configurations 0-4 to rounding, not bit for bit.
+ *   5: the stages as two launches, the chain after the whole preparation.
+ *   6: both stages in one cooperative launch of one CTA per SM: num_seqs * H
+ *      CTAs carry the chains while the others prepare the chunks in chunk
+ *      order (chunk 0 of every chain first), and each chain waits (bounded)
+ *      for a chunk's ready flag before reading it; bit for bit equal to 5.
+ *      Needs num_seqs <= 32, 2 * num_seqs * H <= the device's SM count and
+ *      the q, k, v and g_raw rows 16-byte aligned (pointer, b_stride and
+ *      h_stride); the call clears the flags (cudaMemsetAsync on the stream).
  *
  * workspace: device memory of at least kda_prefill_workspace_bytes(B,
  * num_seqs, H) bytes, 16-byte aligned, owned by the caller, overlapping none
@@ -106,25 +114,29 @@ int32_t kda_select_prefill_config(int32_t num_seqs, int32_t H);
  * not matter and on return are unspecified; two calls in flight at once need
  * two workspaces.
  *
- * config_override: -1 lets kda_select_prefill_ws_config choose; 0..4 run
- * kda_prefill's configurations (the workspace is then not used and may be
- * NULL); 5 runs the two-stage kernels. Validation as kda_prefill's, plus
- * KDA_EINVAL for configuration 5 with a NULL, unaligned, too small or
- * overlapping workspace. Errors found on the device (KDA_ERR_SEQLENS,
+ * config_override: -1 lets kda_select_prefill_ws_config choose (its choice of
+ * 6 becomes 5 when 6's conditions do not hold); 0..4 run kda_prefill's
+ * configurations (the workspace is then not used and may be NULL); 5 and 6
+ * the two stages. Validation as kda_prefill's, plus KDA_EINVAL for
+ * configuration 5 or 6 with a NULL, unaligned, too small or overlapping
+ * workspace, and KDA_EUNSUPPORTED for configuration 6 outside its conditions. Errors found on the device (KDA_ERR_SEQLENS,
  * KDA_ERR_TIMEOUT) are reported as kda_prefill reports them.
  */
 kda_status kda_prefill_ws(const kda_params* p, const kda_seqs* s, void* workspace, size_t workspace_bytes,
                           void* stream);
 
-/* Workspace bytes kda_prefill_ws needs in configuration 5 for B token rows,
-   num_seqs sequences and H heads: (ceil(B / 16) + num_seqs) * H chunk images
-   of 45568 bytes; 0 when B <= 0, num_seqs <= 0 or H < 1. */
+/* Workspace bytes kda_prefill_ws needs in configurations 5 and 6 for B token
+   rows, num_seqs sequences and H heads: n = (ceil(B / 16) + num_seqs) * H
+   chunk images of 45568 bytes, then n 4-byte ready flags padded to a multiple
+   of 16 bytes; 0 when B <= 0, num_seqs <= 0 or H < 1. */
 size_t kda_prefill_workspace_bytes(int32_t B, int32_t num_seqs, int32_t H);
 
-/* The configuration kda_prefill_ws picks: 5 (two stages) when the sequences
-   average at least 512 tokens (B >= 512 num_seqs), else 4; -1 for negative B or
-   num_seqs or H < 1. Source: PR #4605, #4675 commit text (Description):
-   the preparation-and-chain schedules are selected from the input shape. */
+/* The configuration kda_prefill_ws picks: two stages when the sequences
+   average at least 512 tokens (B >= 512 num_seqs) — 6 (one launch) for at
+   most 32 sequences and 64 (sequence, head) chains, else 5 —, otherwise 4;
+   -1 for negative B or num_seqs or H < 1. Source: PR #4605, #4675 commit text
+   (Description): the preparation-and-chain schedules are selected from the
+   physical device and the input shape. */
 int32_t kda_select_prefill_ws_config(int32_t B, int32_t num_seqs, int32_t H);
 
 /*
@@ -141,8 +153,8 @@ int32_t kda_select_prefill_ws_config(int32_t B, int32_t num_seqs, int32_t H);
  * every GPU that loads the library holds those 64 MiB until the process
  * exits. The caller passes inputs and outputs as for kda_prefill_ws.
  *   - Limit: a call whose kda_prefill_workspace_bytes(B, num_seqs, H) exceeds
- *     64 MiB (more than 1472 chunk images; e.g. one sequence of more than
- *     1936 tokens at H = 12) is rejected with KDA_EUNSUPPORTED and a message
+ *     64 MiB (more than 1472 chunk images with their flags; e.g. one sequence
+ *     of more than 1936 tokens at H = 12) is rejected with KDA_EUNSUPPORTED and a message
  *     giving both sizes, before anything is launched; use kda_prefill_ws.
  *   - Set-up: the first call on a device looks up the array's device address
  *     with that device current; make that first call before any stream

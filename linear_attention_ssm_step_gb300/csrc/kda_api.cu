@@ -43,8 +43,11 @@ kda_status ok() {
 constexpr int kTileV[] = {16, 32, 64, 128, 128};
 constexpr int kTensorCoreConfig = 4;
 constexpr int kNumConfigs = sizeof(kTileV) / sizeof(kTileV[0]);
-// Prefill only: the two-stage kernels, which need a caller's workspace (kda_prefill_ws).
+// Prefill only, with a caller's workspace (kda_prefill_ws): the two stages in
+// two launches (5) or in one cooperative launch (6).
 constexpr int kChainConfig = 5;
+constexpr int kFusedConfig = 6;
+constexpr int kFusedMaxSeqs = 32;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -180,20 +183,23 @@ int32_t kda_select_prefill_config(int32_t num_seqs, int32_t H) {
   return kTensorCoreConfig;
 }
 
-// Prefill with a workspace: the two-stage kernels (configuration 5) once the
-// sequences average 512 tokens (32 chunks) or more, where the chain's short
-// per-chunk step outweighs the workspace round trip and the second launch
-// (measured on GB300: 1 x 4096 and 8 x 2048 tokens faster in two stages,
-// 64 x 256 and 512 x 16 faster in one); the chunked single kernel below that.
+// Prefill with a workspace: the two stages once the sequences average 512
+// tokens (32 chunks) or more, where the chain's short per-chunk step outweighs
+// the workspace round trip (measured on GB300: 1 x 4096 and 8 x 2048 tokens
+// faster in two stages, 64 x 256 and 512 x 16 faster in the chunked single
+// kernel); in one launch (6) when there are few chains (at most 32 sequences
+// and 64 (sequence, head) chains), where the preparation then runs beside the
+// chains instead of before them; the chunked single kernel (4) below 512.
 int32_t kda_select_prefill_ws_config(int32_t B, int32_t num_seqs, int32_t H) {
   if (B < 0 || num_seqs < 0 || H < 1) return -1;
-  if (num_seqs > 0 && (long long)B >= 512LL * num_seqs) return kChainConfig;
+  if (num_seqs > 0 && (long long)B >= 512LL * num_seqs)
+    return (num_seqs <= kFusedMaxSeqs && (long long)num_seqs * H <= 64) ? kFusedConfig : kChainConfig;
   return kTensorCoreConfig;
 }
 
 size_t kda_prefill_workspace_bytes(int32_t B, int32_t num_seqs, int32_t H) {
   if (B <= 0 || num_seqs <= 0 || H < 1) return 0;
-  return (size_t)kda::prefill_chunk_images(B, num_seqs, H) * kda::kPrefillChunkImageBytes;
+  return kda::prefill_workspace_size(B, num_seqs, H);
 }
 
 const char* kda_last_error(void) { return g_err; }
@@ -285,9 +291,8 @@ kda_status kda_prefill_ws(const kda_params* p, const kda_seqs* sq, void* workspa
   if (p == nullptr) return fail(KDA_EINVAL, "params is NULL");
   if (sq == nullptr) return fail(KDA_EINVAL, "seqs is NULL");
   if (sq->num_seqs < 0) return fail(KDA_EINVAL, "num_seqs = %d is negative", sq->num_seqs);
-  const int cfg =
-      p->config_override >= 0 ? p->config_override : kda_select_prefill_ws_config(p->B, sq->num_seqs, p->H);
-  if (cfg != kChainConfig) {  // the single-kernel configurations; the workspace is not used
+  int cfg = p->config_override >= 0 ? p->config_override : kda_select_prefill_ws_config(p->B, sq->num_seqs, p->H);
+  if (cfg != kChainConfig && cfg != kFusedConfig) {  // the single-kernel configurations; the workspace is not used
     if (p->config_override < 0) {
       kda_params q = *p;
       q.config_override = cfg;
@@ -297,7 +302,7 @@ kda_status kda_prefill_ws(const kda_params* p, const kda_seqs* sq, void* workspa
   }
   if (sq->num_seqs == 0) return ok();
   kda_params q = *p;
-  q.config_override = -1;  // configuration 5 is prefill-only; the shared checks see "library's choice"
+  q.config_override = -1;  // configurations 5 and 6 are prefill-only; the shared checks see "library's choice"
   bool bulk = false;
   kda_status s = check_params(&q, 1, &bulk);
   if (s != KDA_OK) return s;
@@ -335,8 +340,24 @@ kda_status kda_prefill_ws(const kda_params* p, const kda_seqs* sq, void* workspa
       if (overlaps(w0, w1, s0, s1)) return fail(KDA_EINVAL, "workspace overlaps the state pool");
     }
   }
-  cudaError_t e =
-      kda::launch_prefill_chain(*p, sq->cu_seqlens, sq->num_seqs, workspace, bulk, static_cast<cudaStream_t>(stream));
+  if (cfg == kFusedConfig) {  // one cooperative launch: few chains, 16-byte aligned token rows
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return fail(KDA_ELAUNCH, "kda_prefill_ws: no current device");
+    const bool fits = sq->num_seqs <= kFusedMaxSeqs && 2LL * sq->num_seqs * p->H <= sms;
+    const bool aligned_rows = kda::prefill_rows_aligned16(*p);
+    if (!fits || !aligned_rows) {
+      if (p->config_override == kFusedConfig)
+        return fail(KDA_EUNSUPPORTED,
+                    "configuration %d needs num_seqs <= %d, 2 * num_seqs * H <= %d SMs and q, k, v, g_raw rows "
+                    "16-byte aligned (num_seqs = %d, H = %d)",
+                    kFusedConfig, kFusedMaxSeqs, sms, sq->num_seqs, p->H);
+      cfg = kChainConfig;  // the library's choice falls back to two launches
+    }
+  }
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cfg == kFusedConfig ? kda::launch_prefill_fused(*p, sq->cu_seqlens, sq->num_seqs, workspace, bulk, st)
+                                      : kda::launch_prefill_chain(*p, sq->cu_seqlens, sq->num_seqs, workspace, bulk, st);
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_prefill_ws launch: %s", cudaGetErrorString(e));
   return ok();
 }

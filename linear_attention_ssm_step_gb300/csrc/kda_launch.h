@@ -48,6 +48,19 @@ constexpr uint32_t kPrefillChunkImageBytes = 45568u;
 // heads may write: (ceil(B / 16) + num_seqs) * H.
 long long prefill_chunk_images(int B, int num_seqs, int H);
 
+// Workspace bytes of the two-stage prefill: the chunk images, then one ready
+// flag (4 bytes) per image for the single-launch schedule, padded to 16.
+size_t prefill_workspace_size(int B, int num_seqs, int H);
+
+// q, k, v and g_raw rows 16-byte aligned (the preparation's vector copies).
+bool prefill_rows_aligned16(const kda_params& p);
+
+// The single-launch two-stage prefill (configuration 6): a cooperative grid of
+// one CTA per SM, num_seqs * H chain CTAs (at most half the SMs, num_seqs <= 32)
+// and preparation CTAs beside them; needs prefill_rows_aligned16.
+cudaError_t launch_prefill_fused(const kda_params& p, const int32_t* cu, int num_seqs, void* ws, bool bulk,
+                                 cudaStream_t s);
+
 // Two-stage varlen prefill: the preparation kernel writes every chunk's image
 // into `ws` (prefill_chunk_images(...) images, 16-byte aligned), then the
 // chain kernel runs each (sequence, head) through its chunks. bulk as above.

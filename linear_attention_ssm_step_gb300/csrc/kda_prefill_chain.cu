@@ -128,6 +128,8 @@ __host__ __device__ inline PpLayout pp_layout(bool vec) {
 }
 
 __host__ __device__ inline size_t pp_smem_bytes(bool vec) { return (size_t)pp_layout(vec).total + 1024; }
+// One preparation group's shared memory inside the single-launch kernel (1024-byte multiple).
+constexpr uint32_t PP_GROUP_STRIDE = 90112u;
 
 // 16 bytes global -> shared without registers (cp.async); src_bytes 0 fills zeros and reads nothing.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
@@ -139,10 +141,12 @@ __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wa
 
 // q, k, v and g_raw of the chunk of Tc tokens at row c0 (head h) into `buf`,
 // 16 bytes per copy, zeros past Tc: piece i = (tensor, token, 8 channels).
-__device__ __forceinline__ void issue_token_copies(const kda_params& p, int c0, int h, int Tc, unsigned char* buf) {
+// gtid: the thread's index in its 128-thread group.
+__device__ __forceinline__ void issue_token_copies(const kda_params& p, int c0, int h, int Tc, unsigned char* buf,
+                                                   int gtid) {
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
-    const int i = threadIdx.x + CH_THREADS * m;  // tensor m / 2, token (i / 16) % 16, channels 8 (i % 16) ..
+    const int i = gtid + CH_THREADS * m;  // tensor m / 2, token (i / 16) % 16, channels 8 (i % 16) ..
     const int t = (i >> 4) & (CH - 1), c8 = i & 15;
     const kda_view& vw = m < 2 ? p.q : m < 4 ? p.k : m < 6 ? p.v : p.g_raw;
     const int tt = t < Tc ? t : 0;
@@ -152,23 +156,34 @@ __device__ __forceinline__ void issue_token_copies(const kda_params& p, int c0, 
   }
 }
 
-// CTA (sequence, head, z) prepares chunks z, z + Z, z + 2Z, ... of its
-// sequence. p: t_stride = b_stride in every activation view (token t of a
-// chunk starting at row c0 is (b = c0, t)). VEC: q, k, v and g_raw rows are
-// 16-byte aligned, and the next chunk's token inputs are copied into shared
-// memory while this one is computed.
-template <bool VEC>
-__global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const kda_params p,
-                                                                         const int32_t* __restrict__ cu,
-                                                                         const int num_seqs, const int Z,
-                                                                         unsigned char* __restrict__ ws,
-                                                                         const long long ws_images) {
-  // The chain kernel's CTAs may launch once every CTA of this grid has
-  // started; they wait for the whole grid before they read a chunk image.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+// A chunk to prepare: token rows c0 .. c0 + Tc - 1 of head h into chunk image `img`.
+struct PrepItem {
+  int c0, Tc, h;
+  long long img;
+  bool ok;  // false: no more items
+};
+
+// Chunk image `img` is complete and visible to every SM: the bulk stores of
+// this thread have completed (wait), the group's plain stores are ordered
+// before this thread by a group barrier, and the flag is set with release.
+__device__ __forceinline__ void publish_image(uint32_t* flags, long long img) {
+  bulk_wait_all();
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + img), "r"(1u) : "memory");
+}
+
+// One 128-thread group prepares next(0), next(1), ... in order, until an item
+// with ok == false: thread gtid is key channel gtid and value row gtid; `bar`
+// is the group's barrier (0 when the group is the whole CTA); `sm` its
+// 1024-aligned shared memory (pp_layout(VEC)). VEC: q, k, v and g_raw rows
+// are 16-byte aligned, and the next item's token inputs are copied into
+// shared memory while the current one is computed. flags: NULL, or one word
+// per chunk image, set once the image is complete (publish_image).
+template <bool VEC, class Next>
+__device__ void prepare_items(const kda_params& p, const int gtid, const uint32_t bar, unsigned char* sm,
+                              unsigned char* __restrict__ ws, uint32_t* flags, Next next) {
+  const int tid = gtid, warp = tid >> 5, lane = tid & 31;
   const PpLayout SL = pp_layout(VEC);
   unsigned char* stage = sm + SL.stage;
   unsigned char* stok = sm + SL.tok;
@@ -177,50 +192,37 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
   float* rn = reinterpret_cast<float*>(sm + SL.rn);
   float* sbeta = reinterpret_cast<float*>(sm + SL.beta);
   float* xtile = reinterpret_cast<float*>(sm + SL.xpose + warp * XPOSE_WARP_BYTES);
-  int* scratch = reinterpret_cast<int*>(sm + SL.scratch);
+  auto gsync = [&]() { bar_sync(bar, CH_THREADS); };
 
-  const int item = blockIdx.x;
-  const int z = item % Z, sh = item / Z;
-  const int seq = sh / p.H, h = sh - seq * p.H;
-  if (seq >= num_seqs) return;
-  const int t0 = cu[seq], t1 = cu[seq + 1];
-  if (t0 < 0 || t1 < t0 || t1 > p.B) return;  // the chain kernel reports it
-  const int n = p.state_indices[seq];
-  if (n < 0 || n >= p.N) return;  // inactive: the chain kernel writes zero outputs
-  const int nch = (t1 - t0 + CH - 1) / CH;
-  if (z >= nch) return;
-  const int base = chunk_base(cu, seq, p.B, scratch);
-  float alog = 0.0f, dtb = 0.0f;  // A_log[h] and dt_bias[h][tid] (raw gate)
-  if (VEC && p.gate_mode == KDA_GATE_RAW) {
-    alog = p.A_log[h];
-    dtb = p.dt_bias[(int64_t)h * KD + tid];
-  }
+  PrepItem cur = next(0);
   uint16_t blogit_next = 0;
-  if (VEC) {
-    const int c0 = t0 + z * CH, Tc = min(CH, t1 - c0);
-    issue_token_copies(p, c0, h, Tc, stok);
+  if (VEC && cur.ok) {
+    issue_token_copies(p, cur.c0, cur.h, cur.Tc, stok, tid);
     cp_async_commit();
-    if (tid < Tc) blogit_next = load_bits(p.beta_logit, c0, tid, h, 0);
+    if (tid < cur.Tc) blogit_next = load_bits(p.beta_logit, cur.c0, tid, cur.h, 0);
   }
+  long long last_img = -1;  // the image whose flag is still to be set
 
-  for (int j = z, buf = 0; j < nch; j += Z, buf ^= 1) {
-    const long long img = (long long)(base + j) * p.H + h;
-    if (img >= ws_images) break;  // only overlapping token ranges get here (undefined)
-    unsigned char* gimg = ws + img * kPrefillChunkImageBytes;
-    const int c0 = t0 + j * CH, Tc = min(CH, t1 - c0);
+  for (int k = 0, buf = 0; cur.ok; ++k, buf ^= 1) {
+    const PrepItem nxt = next(k + 1);
+    const int c0 = cur.c0, Tc = cur.Tc, h = cur.h;
+    unsigned char* gimg = ws + cur.img * kPrefillChunkImageBytes;
     TokenRegs<CH> L;
     if constexpr (VEC) {
       L.blogit = blogit_next;
-      L.alog = alog;
-      L.dtb = dtb;
-      if (j + Z < nch) {  // the next chunk's inputs fly while this one is computed
-        const int cn = c0 + Z * CH, Tn = min(CH, t1 - cn);
-        issue_token_copies(p, cn, h, Tn, stok + (buf ^ 1) * PP_TOK_BYTES);
-        blogit_next = tid < Tn ? load_bits(p.beta_logit, cn, tid, h, 0) : (uint16_t)0;
+      L.alog = 0.0f;
+      L.dtb = 0.0f;
+      if (p.gate_mode == KDA_GATE_RAW) {
+        L.alog = p.A_log[h];
+        L.dtb = p.dt_bias[(int64_t)h * KD + tid];
+      }
+      if (nxt.ok) {  // the next item's inputs fly while this one is computed
+        issue_token_copies(p, nxt.c0, nxt.h, nxt.Tc, stok + (buf ^ 1) * PP_TOK_BYTES, tid);
+        blogit_next = tid < nxt.Tc ? load_bits(p.beta_logit, nxt.c0, tid, nxt.h, 0) : (uint16_t)0;
       }
       cp_async_commit();
-      cp_async_wait_prev();  // this chunk's copies have landed (each thread's own)
-      __syncthreads();       // and everyone's
+      cp_async_wait_prev();  // this item's copies have landed (each thread's own)
+      gsync();               // and everyone's
       const uint16_t* tk = reinterpret_cast<const uint16_t*>(stok + buf * PP_TOK_BYTES) + tid;
 #pragma unroll
       for (int t = 0; t < CH; ++t) {
@@ -231,15 +233,15 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
       }
     } else {
       zero_tokens(L);
-      load_tokens(p, c0, h, Tc, L);
+      load_tokens(p, c0, h, Tc, L);  // thread index = threadIdx.x: the group is the whole CTA here
     }
 
     // L2 norms: block sums of q_t^2 (value t) and k_t^2 (value CH + t).
 #pragma unroll
     for (int t = 0; t < CH; ++t) {
-      const float q = bf16_bits_to_float(L.qv[t]), k = bf16_bits_to_float(L.kv[t]);
+      const float q = bf16_bits_to_float(L.qv[t]), kq = bf16_bits_to_float(L.kv[t]);
       tile_put(xtile, lane, t, __fmul_rn(q, q));
-      tile_put(xtile, lane, CH + t, __fmul_rn(k, k));
+      tile_put(xtile, lane, CH + t, __fmul_rn(kq, kq));
     }
     __syncwarp();
     {
@@ -247,9 +249,9 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
       __syncwarp();
       red[warp * 32 + lane] = s;
     }
-    __syncthreads();
+    gsync();
     if (tid < 2 * CH) rn[tid] = inv_norm(block_sum(red, 0, tid));
-    __syncthreads();
+    gsync();
 
     // Channel tid: the normalised vectors, the gate, P_t.
     const FastGate gate(p, L.alog);
@@ -309,13 +311,13 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
         wl = __fmul_rn(wl, dd[s]);
       }
     }
-    __syncthreads();  // partial sums, beta
+    gsync();  // partial sums, beta
     for (int i = tid; i < CH * CH; i += CH_THREADS) {
       const float v = block_sum(red, 1 + (i >> 5), i & 31);
       fcp[2 * i] = v;
       fcp[2 * ((i % CH) * CH + i / CH) + 1] = v;
     }
-    __syncthreads();
+    gsync();
 
     // Forward substitution, channel tid (W, Q) and value row tid (U, O) as
     // packed pairs: (W_t, U_t) = beta_t ((P_t k_t, v_t) - sum_{s<t} cc[t][s] (W_s, U_s)),
@@ -362,9 +364,17 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
       Ov[t] = eu;
     }
 
-    // The image: XB and KW staged, then one bulk store; U, O and P_{C-1} straight to global memory.
-    if (tid == 0) bulk_wait_read_all();  // the previous chunk's bulk store has read the stage
-    __syncthreads();
+    // The image: XB and KW staged, then one bulk store; U, O and P_{C-1}
+    // straight to global memory. Before the stage is rewritten the previous
+    // item's bulk store has read it (with flags: has completed, and that
+    // item's image is published).
+    if (tid == 0) {
+      if (flags != nullptr && last_img >= 0)
+        publish_image(flags, last_img);
+      else
+        bulk_wait_read_all();
+    }
+    gsync();
     {
       const Sw128Col col = sw128_col(64, tid);
 #pragma unroll
@@ -387,14 +397,62 @@ __global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const k
     }
     reinterpret_cast<float*>(gimg + IMG_PL)[tid] = P[CH - 1];
     fence_proxy_async_smem();
-    __syncthreads();
+    gsync();
     if (tid == 0) {
       bulk_s2g(gimg + IMG_XB, stage, IMG_STAGED);
       bulk_commit();
     }
+    last_img = cur.img;
+    cur = nxt;
   }
-  if (tid == 0) bulk_wait_all();
+  gsync();  // every thread's plain stores of the last image before its flag
+  if (tid == 0) {
+    if (flags != nullptr && last_img >= 0)
+      publish_image(flags, last_img);
+    else
+      bulk_wait_all();
+  }
   if (VEC) asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// CTA (sequence, head, z) prepares chunks z, z + Z, z + 2Z, ... of its
+// sequence (the two-launch schedule, configuration 5). p: t_stride = b_stride
+// in every activation view (token t of a chunk starting at row c0 is (b = c0, t)).
+template <bool VEC>
+__global__ void __launch_bounds__(CH_THREADS) kda_prefill_prepare_kernel(const kda_params p,
+                                                                         const int32_t* __restrict__ cu,
+                                                                         const int num_seqs, const int Z,
+                                                                         unsigned char* __restrict__ ws,
+                                                                         const long long ws_images) {
+  // The chain kernel's CTAs may launch once every CTA of this grid has
+  // started; they wait for the whole grid before they read a chunk image.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  int* scratch = reinterpret_cast<int*>(sm + pp_layout(VEC).scratch);
+
+  const int item = blockIdx.x;
+  const int z = item % Z, sh = item / Z;
+  const int seq = sh / p.H, h = sh - seq * p.H;
+  if (seq >= num_seqs) return;
+  const int t0 = cu[seq], t1 = cu[seq + 1];
+  if (t0 < 0 || t1 < t0 || t1 > p.B) return;  // the chain kernel reports it
+  const int n = p.state_indices[seq];
+  if (n < 0 || n >= p.N) return;  // inactive: the chain kernel writes zero outputs
+  const int nch = (t1 - t0 + CH - 1) / CH;
+  if (z >= nch) return;
+  const int base = chunk_base(cu, seq, p.B, scratch);
+  auto next = [&](int k) {
+    const int j = z + k * Z;
+    PrepItem it;
+    it.c0 = t0 + j * CH;
+    it.Tc = min(CH, t1 - it.c0);
+    it.h = h;
+    it.img = (long long)(base + j) * p.H + h;
+    it.ok = j < nch && it.img < ws_images;  // beyond ws_images only with overlapping token ranges (undefined)
+    return it;
+  };
+  prepare_items<VEC>(p, threadIdx.x, 0u, sm, ws, nullptr, next);
 }
 
 // ---------------------------------------------------------------- chain
@@ -440,18 +498,41 @@ __host__ __device__ inline CnLayout cn_layout() {
 
 __host__ __device__ inline size_t cn_smem_bytes() { return (size_t)cn_layout().total + 1024; }
 
+// Chunk image `img` has been published (publish_image); false if the bounded wait gave up.
+__device__ __forceinline__ bool wait_image_bounded(const uint32_t* flags, long long img) {
+  const uint32_t* f = flags + img;
+  auto ready = [&]() {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v != 0u;
+  };
+  bool ok = ready();
+  if (!ok) {
+    const unsigned long long t0 = global_timer_ns();
+    for (unsigned it = 1; it < WAIT_LIMIT_ITERS; ++it) {
+      __nanosleep(64);
+      if ((ok = ready())) break;
+      if ((it & 255u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) break;
+    }
+  }
+  if (ok) asm volatile("fence.proxy.async.global;" ::: "memory");  // the image is read by bulk copies
+  return ok;
+}
+
+// The chain over items it0, it0 + stride, ... (item = (sequence, head)) by
+// one 288-thread CTA with shared memory `sm` (cn_layout). flags: NULL when the
+// images are complete before the chain starts (two launches), else each
+// image's copy waits for its flag (one launch, preparation running beside).
 template <bool TMA>
-__global__ void __launch_bounds__(CN_THREADS, 1)
-    kda_prefill_chain_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p,
-                             const int32_t* __restrict__ cu, const int num_seqs,
-                             const unsigned char* __restrict__ ws, const long long ws_images) {
+__device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda_params& p, const int32_t* __restrict__ cu,
+                            const int num_seqs, const unsigned char* __restrict__ ws, const long long ws_images,
+                            const uint32_t* flags, const int it0, const int stride, unsigned char* sm) {
+  const CUtensorMap& smap = *smap_p;
   const int tid = threadIdx.x, warp = tid >> 5;
   const bool worker = tid < CN_WORKERS, issuer = warp == CN_MMA_WARP;
   const int row = tid & (KD - 1), hf = tid >> 7;  // meaningful in the state warps
   const int total = num_seqs * p.H;
 
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const CnLayout SL = cn_layout();
   unsigned char* sA = sm + SL.a;
   unsigned char* sImg = sm + SL.img;
@@ -475,15 +556,13 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t row_tmem = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // lane `row`, column 0
-  // The preparation grid has finished and its chunk images are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   uint32_t phA = 0, phD = 0, phU = 0;
   uint32_t phI = 0u, pendI = 0u;  // per image buffer b, bit b: its barrier's phase, a copy in flight
   bool pendA = false, pendD = false, pendU = false;
   bool broken = false;
 
-  for (int it = blockIdx.x; it < total; it += gridDim.x) {
+  for (int it = it0; it < total; it += stride) {
     const int seq = it / p.H, h = it - seq * p.H;
     const int t0 = cu[seq], t1 = cu[seq + 1];
     const int n = p.state_indices[seq];
@@ -506,8 +585,15 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
       continue;
     }
     uint16_t* gstate = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride + (int64_t)h * KD * KD;
-    auto image = [&](int j) {
-      return ws + ((long long)(base + j) * p.H + h) * (long long)kPrefillChunkImageBytes;
+    // Chunk j's image into buffer bb, once it is published (one launch);
+    // a wait that gives up issues nothing, and the chain's own bounded wait
+    // on the buffer then reports it.
+    auto issue_image = [&](int j, int bb) {
+      const long long img = (long long)(base + j) * p.H + h;
+      if (flags != nullptr && !wait_image_bounded(flags, img)) return;
+      mbar_expect_tx(barI + bb, kPrefillChunkImageBytes);
+      bulk_g2s(sImg + bb * CN_IMG_STRIDE, ws + img * (long long)kPrefillChunkImageBytes, kPrefillChunkImageBytes,
+               barI + bb);
     };
 
     if constexpr (TMA) {
@@ -522,10 +608,7 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
         *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, row)) = gstate[(int64_t)r * KD + row];
     }
     for (int j = 0; j < min(CN_NBUF, nch); ++j) {
-      if (tid == 0) {
-        mbar_expect_tx(barI + j, kPrefillChunkImageBytes);
-        bulk_g2s(sImg + j * CN_IMG_STRIDE, image(j), kPrefillChunkImageBytes, barI + j);
-      }
+      if (tid == 0) issue_image(j, j);
       pendI |= 1u << j;
     }
 
@@ -557,10 +640,7 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
       pendI &= ~(1u << b);
       if (j >= 1 && j + 2 < nch) {  // chunk j + 2 into the buffer chunk j - 1 has released
         const int bn = (j + 2) % CN_NBUF;
-        if (tid == CN_WORKERS) {
-          mbar_expect_tx(barI + bn, kPrefillChunkImageBytes);
-          bulk_g2s(sImg + bn * CN_IMG_STRIDE, image(j + 2), kPrefillChunkImageBytes, barI + bn);
-        }
+        if (tid == CN_WORKERS) issue_image(j + 2, bn);
         pendI |= 1u << bn;
       }
       tc_fence_after();
@@ -767,6 +847,94 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
   }
 }
 
+// The chain of the two-launch schedule (configuration 5): after the
+// preparation grid, persistent over (sequence, head) items.
+template <bool TMA>
+__global__ void __launch_bounds__(CN_THREADS, 1)
+    kda_prefill_chain_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p,
+                             const int32_t* __restrict__ cu, const int num_seqs,
+                             const unsigned char* __restrict__ ws, const long long ws_images) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  // The preparation grid has finished and its chunk images are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  chain_items<TMA>(&smap, p, cu, num_seqs, ws, ws_images, nullptr, blockIdx.x, gridDim.x, sm);
+}
+
+// ---------------------------------------------------------------- one launch
+
+// The single-launch schedule (configuration 6), a cooperative grid of one CTA
+// per SM: CTA c < num_seqs * H carries chain c; every other CTA runs two
+// preparation groups (warps 0-3 and 4-7) over the chunk images in chunk-major
+// order (chunk 0 of every chain, then chunk 1, ...), publishing each image with
+// a flag that the chains wait for. The preparation never waits for a chain,
+// and every CTA is resident (cooperative launch), so every wait ends.
+constexpr int FU_MAX_SEQS = 32;
+constexpr uint32_t FU_TABLE = 2 * PP_GROUP_STRIDE;  // the sequence table, after the two groups' regions
+static_assert(28672u + 2u * PP_TOK_BYTES + 9u * 512u + 2048u + 128u + 64u + 4u * XPOSE_WARP_BYTES + 16u <=
+                  PP_GROUP_STRIDE,
+              "a preparation group's shared memory");
+
+template <bool TMA>
+__global__ void __launch_bounds__(CN_THREADS, 1)
+    kda_prefill_fused_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p,
+                             const int32_t* __restrict__ cu, const int num_seqs, unsigned char* __restrict__ ws,
+                             const long long ws_images, uint32_t* flags) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int nchains = num_seqs * p.H;  // at most half the grid (host)
+  if ((int)blockIdx.x < nchains) {
+    chain_items<TMA>(&smap, p, cu, num_seqs, ws, ws_images, flags, blockIdx.x, nchains, sm);
+    return;
+  }
+  // Sequence table: first row, chunk count, first image, active.
+  int* st0 = reinterpret_cast<int*>(sm + FU_TABLE);
+  int* snch = st0 + FU_MAX_SEQS;
+  int* sbase = snch + FU_MAX_SEQS;
+  int* smax = sbase + FU_MAX_SEQS;
+  if (threadIdx.x == 0) {
+    int base = 0, mx = 0;
+    for (int s2 = 0; s2 < num_seqs; ++s2) {
+      const int a = cu[s2], b = cu[s2 + 1];
+      const bool wf = a >= 0 && b >= a && b <= p.B;  // well formed
+      const int nc = wf ? (b - a + CH - 1) / CH : 0;
+      const int n = p.state_indices[s2];
+      st0[s2] = a;
+      sbase[s2] = base;
+      snch[s2] = (wf && n >= 0 && n < p.N) ? nc : 0;  // chunks to prepare
+      base += nc;
+      mx = max(mx, snch[s2]);
+    }
+    smax[0] = mx;
+  }
+  __syncthreads();
+  if (threadIdx.x >= 2 * CH_THREADS) return;  // warp 8 has no preparation role
+  const int g = threadIdx.x / CH_THREADS, gtid = threadIdx.x % CH_THREADS;
+  const long long Q = 2LL * (gridDim.x - nchains);
+  const long long slots = (long long)smax[0] * nchains;
+  long long pos = 2LL * (blockIdx.x - nchains) + g - Q;  // advanced by Q before each use
+  const int t1_cap = p.B;
+  auto next = [=](int) mutable {
+    PrepItem it;
+    it.ok = false;
+    for (pos += Q; pos < slots; pos += Q) {
+      const int j = (int)(pos / nchains), c = (int)(pos % nchains);
+      const int s2 = c / p.H, h = c - s2 * p.H;
+      if (j >= snch[s2]) continue;
+      const long long img = (long long)(sbase[s2] + j) * p.H + h;
+      if (img >= ws_images) continue;  // only overlapping token ranges (undefined)
+      it.c0 = st0[s2] + j * CH;
+      it.Tc = min(CH, min(cu[s2 + 1], t1_cap) - it.c0);
+      it.h = h;
+      it.img = img;
+      it.ok = true;
+      break;
+    }
+    return it;
+  };
+  prepare_items<true>(p, gtid, 1u + (uint32_t)g, sm + g * PP_GROUP_STRIDE, ws, flags, next);
+}
+
 // ---------------------------------------------------------------- host side
 
 // The workspace of kda_prefill_static: one fixed array per device that loads
@@ -795,6 +963,68 @@ cudaError_t prefill_static_workspace(void** ptr) {
 
 long long prefill_chunk_images(int B, int num_seqs, int H) {
   return ((long long)(B + CH - 1) / CH + num_seqs) * (long long)H;
+}
+
+size_t prefill_workspace_size(int B, int num_seqs, int H) {
+  const long long images = prefill_chunk_images(B, num_seqs, H);
+  return (size_t)images * kPrefillChunkImageBytes + (((size_t)images * 4u + 15u) & ~(size_t)15u);
+}
+
+template <bool TMA>
+static cudaError_t launch_fused(const CUtensorMap& map, const kda_params& q, const int32_t* cu, int num_seqs,
+                                unsigned char* ws, long long images, uint32_t* flags, int sms, cudaStream_t s) {
+  auto kern = kda_prefill_fused_kernel<TMA>;
+  const size_t smem = std::max(cn_smem_bytes(), (size_t)FU_TABLE + 4u * FU_MAX_SEQS * 4u + 1024u);
+  static std::atomic<bool> smem_set{false};  // one flag per instantiation
+  cudaError_t e = set_smem_limit_once(kern, smem, smem_set);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CN_THREADS, smem)) != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sms);  // one CTA per SM, all resident
+  cfg.blockDim = dim3(CN_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, map, q, cu, num_seqs, ws, images, flags);
+}
+
+cudaError_t launch_prefill_fused(const kda_params& p, const int32_t* cu, int num_seqs, void* ws, bool bulk,
+                                 cudaStream_t s) {
+  const long long images = prefill_chunk_images(p.B, num_seqs, p.H);
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(w + images * kPrefillChunkImageBytes);
+  int dev = 0, sms = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if (num_seqs > FU_MAX_SEQS || 2LL * num_seqs * p.H > sms) return cudaErrorInvalidConfiguration;
+  if ((e = cudaMemsetAsync(flags, 0, (size_t)images * 4u, s)) != cudaSuccess) return e;
+  kda_params q = p;  // token t of a chunk is activation row c0 + t
+  q.q.t_stride = q.q.b_stride;
+  q.k.t_stride = q.k.b_stride;
+  q.v.t_stride = q.v.b_stride;
+  q.g_raw.t_stride = q.g_raw.b_stride;
+  q.beta_logit.t_stride = q.beta_logit.b_stride;
+  CUtensorMap map;
+  memset(&map, 0, sizeof(map));
+  if (bulk) {
+    if ((e = state_tensor_map(p, &map)) != cudaSuccess) return e;
+    return launch_fused<true>(map, q, cu, num_seqs, w, images, flags, sms, s);
+  }
+  return launch_fused<false>(map, q, cu, num_seqs, w, images, flags, sms, s);
+}
+
+bool prefill_rows_aligned16(const kda_params& p) {
+  auto ok = [](const kda_view& v) {
+    return (reinterpret_cast<uintptr_t>(v.ptr) & 15u) == 0 && v.b_stride % 8 == 0 && v.h_stride % 8 == 0;
+  };
+  return ok(p.q) && ok(p.k) && ok(p.v) && ok(p.g_raw);
 }
 
 template <bool TMA>
@@ -838,10 +1068,7 @@ cudaError_t launch_prefill_chain(const kda_params& p, const int32_t* cu, int num
   // Preparation: Z CTAs per (sequence, head), enough for about 8 CTAs per SM
   // when there are few sequences, never more than a sequence can have chunks.
   {
-    auto aligned_rows = [](const kda_view& v) {
-      return (reinterpret_cast<uintptr_t>(v.ptr) & 15u) == 0 && v.b_stride % 8 == 0 && v.h_stride % 8 == 0;
-    };
-    const bool vec = aligned_rows(q.q) && aligned_rows(q.k) && aligned_rows(q.v) && aligned_rows(q.g_raw);
+    const bool vec = prefill_rows_aligned16(q);
     auto kern = vec ? kda_prefill_prepare_kernel<true> : kda_prefill_prepare_kernel<false>;
     const size_t smem = pp_smem_bytes(vec);
     static std::atomic<bool> smem_set_vec{false}, smem_set_plain{false};

@@ -322,12 +322,13 @@ def test_prefill_ws_validation(lib):
     """kda_prefill_ws: configuration 5 needs a workspace of the size
     kda_prefill_workspace_bytes gives, 16-byte aligned and apart from the
     call's other buffers; other configurations go to kda_prefill's checks; the
-    selector takes the two-stage kernels from an average of 512 tokens per
-    sequence."""
+    selector takes the two stages from an average of 512 tokens per
+    sequence, in one launch (6) for at most 32 sequences and 64 chains."""
     p = fake_params(B=40)
     cu = (1 << 32) + 10 * (1 << 24)
     sq = kda.KdaSeqs(cu, 2)
-    need = ((40 + 15) // 16 + 2) * 12 * 45568
+    images = ((40 + 15) // 16 + 2) * 12
+    need = images * 45568 + (images * 4 + 15) // 16 * 16  # the chunk images, then their ready flags
     assert lib.kda_prefill_workspace_bytes(40, 2, 12) == need
     assert [lib.kda_prefill_workspace_bytes(*a) for a in ((0, 2, 12), (40, 0, 12), (40, 2, 0), (-1, 2, 12))] == [0] * 4
     ws = (1 << 32) + 32 * (1 << 24)
@@ -349,7 +350,10 @@ def test_prefill_ws_validation(lib):
     p.K = 64
     assert call(ws, need) == kda.KDA_EUNSUPPORTED
     p.K = 128
-    p.config_override = 6
+    p.config_override = 6  # the one-launch schedule: the same workspace checks
+    assert call(None, need) == kda.KDA_EINVAL and "workspace" in kda.kda_last_error()
+    assert call(ws, need - 16) == kda.KDA_EINVAL and "workspace_bytes" in kda.kda_last_error()
+    p.config_override = 7
     assert call(ws, need) == kda.KDA_EINVAL and "config_override" in kda.kda_last_error()
     p.config_override = 4  # a single-kernel configuration: kda_prefill's checks, no workspace needed
     assert call(None, 0, kda.KdaSeqs(cu + 2, 2)) == kda.KDA_EINVAL and "cu_seqlens" in kda.kda_last_error()
@@ -357,6 +361,7 @@ def test_prefill_ws_validation(lib):
     p.B = 0
     assert call(None, 0) == kda.KDA_OK  # no token rows: nothing launched
     sel = lib.kda_select_prefill_ws_config
-    assert [sel(4096, 1, 12), sel(16384, 1, 16), sel(8 * 2048, 8, 12), sel(512 * 3, 3, 12)] == [5, 5, 5, 5]
+    assert [sel(4096, 1, 12), sel(16384, 1, 16), sel(512 * 3, 3, 12), sel(512 * 4, 4, 16)] == [6, 6, 6, 6]
+    assert [sel(8 * 2048, 8, 12), sel(512 * 40, 40, 1), sel(512 * 5, 5, 13)] == [5, 5, 5]
     assert [sel(64 * 256, 64, 12), sel(512 * 16, 512, 12), sel(511 * 10, 10, 12), sel(100, 0, 12)] == [4, 4, 4, 4]
     assert sel(-1, 1, 12) == -1 and sel(16, -1, 12) == -1 and sel(16, 1, 0) == -1

@@ -1,9 +1,10 @@
-"""kda_prefill_ws in its two-stage configuration (5: the preparation kernel and
-the chain kernel, with a caller's workspace) on the GPU against the fp64
-prefill oracle, through the C ABI, with the tolerances of test_prefill_gpu
-(outputs 2e-2 + 2e-2 |o_ref|; final states 2 bf16 ulps at max(|s_ref|, F_L M));
-and against the single-kernel configurations, which compute the same reading
-with other fp32 rounding.
+"""kda_prefill_ws in its two-stage configurations (5: the preparation kernel,
+then the chain kernel; 6: both in one cooperative launch, the chains waiting
+for each chunk's ready flag; both with a caller's workspace) on the GPU against
+the fp64 prefill oracle, through the C ABI, with the tolerances of
+test_prefill_gpu (outputs 2e-2 + 2e-2 |o_ref|; final states 2 bf16 ulps at
+max(|s_ref|, F_L M)); against the single-kernel configurations, which compute
+the same reading with other fp32 rounding; and 6 against 5, bit for bit.
 """
 
 import numpy as np
@@ -18,6 +19,8 @@ from test_prefill_gpu import LB, LENGTHS, SENTINEL, check_prefill, gpu_prefill
 pytestmark = pytest.mark.gpu
 
 CHAIN = 5
+FUSED = 6
+BOTH = pytest.mark.parametrize("cfg", [CHAIN, FUSED])
 
 
 @pytest.fixture(scope="module")
@@ -33,53 +36,103 @@ def workspace_for(wd):
     return kda.prefill_workspace(wd.q.shape[0], wd.cu_seqlens.shape[0] - 1, wd.H, wd.q.device)
 
 
-def chain_prefill(wd, out=None, workspace=None, **kw):
+def chain_prefill(wd, out=None, workspace=None, cfg=CHAIN, **kw):
     if workspace is None:
         workspace = workspace_for(wd)
-    kw.setdefault("config_override", CHAIN)
+    kw.setdefault("config_override", cfg)
     return gpu_prefill(wd, out=out, workspace=workspace, **kw)
 
 
-def test_chain_matches_oracle(dev):
-    w = workloads.prefill_inputs(LENGTHS, 12, seed=170, inactive_frac=0.25, layout="fused")
+@pytest.mark.parametrize("cfg,H", [(CHAIN, 12), (FUSED, 4)])
+def test_chain_matches_oracle(dev, cfg, H):
+    w = workloads.prefill_inputs(LENGTHS, 12, seed=170, inactive_frac=0.25, layout="fused", H=H)
     wd = w.to(dev)
-    out = chain_prefill(wd)
+    out = chain_prefill(wd, cfg=cfg)
     torch.cuda.synchronize()
     check_prefill(w, wd, out)
 
 
-def test_chain_precomputed_gate_and_scale(dev):
+@BOTH
+def test_chain_precomputed_gate_and_scale(dev, cfg):
     w = workloads.prefill_inputs([7, 20, 1], 5, seed=171, gate_mode=1)
     wd = w.to(dev)
-    out = chain_prefill(wd, scale=0.5)
+    out = chain_prefill(wd, cfg=cfg, scale=0.5)
     torch.cuda.synchronize()
     check_prefill(w, wd, out, scale=0.5)
 
 
-def test_chain_three_heads_packed(dev):
+@BOTH
+def test_chain_three_heads_packed(dev, cfg):
     w = workloads.prefill_inputs([9, 3, 25], 6, seed=172, H=3, layout="packed")
     wd = w.to(dev)
-    out = chain_prefill(wd)
+    out = chain_prefill(wd, cfg=cfg)
     torch.cuda.synchronize()
     check_prefill(w, wd, out)
 
 
-def test_chain_long_sequence(dev):
+@BOTH
+def test_chain_long_sequence(dev, cfg):
     """One 1000-token sequence (63 chunks, prepared by many CTAs) and two short ones."""
     w = workloads.prefill_inputs([1000, 3, 12], 4, seed=173)
     wd = w.to(dev)
-    out = chain_prefill(wd)
+    out = chain_prefill(wd, cfg=cfg)
     torch.cuda.synchronize()
     check_prefill(w, wd, out)
 
 
+@BOTH
 @pytest.mark.parametrize("lengths", [[15, 16, 17], [31, 32, 33, 48], [47, 64, 1, 2]])
-def test_chain_chunk_boundaries(dev, lengths):
+def test_chain_chunk_boundaries(dev, lengths, cfg):
     w = workloads.prefill_inputs(lengths, len(lengths) + 3, seed=185 + sum(lengths))
     wd = w.to(dev)
-    out = chain_prefill(wd)
+    out = chain_prefill(wd, cfg=cfg)
     torch.cuda.synchronize()
     check_prefill(w, wd, out)
+
+
+def test_one_launch_equals_two_launches(dev):
+    """Configurations 6 and 5 run the same arithmetic: the same bits, here on
+    two long sequences (250 and 44 chunks) at H = 8."""
+    w = workloads.prefill_inputs([4000, 700], 3, seed=188, H=8)
+    a, b = w.to(dev), w.to(dev)
+    oa = chain_prefill(a, cfg=FUSED)
+    ob = chain_prefill(b, cfg=CHAIN)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+
+
+def test_one_launch_conditions(dev):
+    """Configuration 6 asked for outside its conditions (too many chains;
+    token rows not 16-byte aligned) is refused; the library's own choice then
+    falls back to configuration 5 (the same bits)."""
+    w = workloads.prefill_inputs([600] * 8, 9, seed=189, H=12)  # 96 chains: more than half the SMs
+    wd = w.to(dev)
+    with pytest.raises(kda.KdaError) as e:
+        chain_prefill(wd, cfg=FUSED)
+    assert e.value.status == kda.KDA_EUNSUPPORTED
+    w = workloads.prefill_inputs([1200, 40], 3, seed=190, H=4)  # 620 tokens per sequence: the library picks 6
+    assert kda.kda_select_prefill_ws_config(1240, 2, 4) == FUSED
+    a, b = w.to(dev), w.to(dev)
+    wide = torch.zeros((b.q.shape[0], 4, 136), dtype=torch.bfloat16, device=dev)
+    wide[:, :, 1:129].copy_(b.q)
+    q_off = wide[:, :, 1:129]  # rows 2 bytes past a 16-byte boundary
+    assert q_off.data_ptr() % 16 == 2
+
+    def call_b(cfg):
+        out = torch.empty((b.q.shape[0], 4, 128), dtype=torch.bfloat16, device=dev)
+        return kda.kda_prefill(b.state, b.state_indices, b.cu_seqlens, q_off, b.k, b.v, b.g_raw, b.beta_logit,
+                               b.A_log, b.dt_bias, out=out, lower_bound=LB, gate_mode=b.gate_mode,
+                               config_override=cfg, workspace=workspace_for(b))
+
+    with pytest.raises(kda.KdaError) as e:
+        call_b(FUSED)
+    assert e.value.status == kda.KDA_EUNSUPPORTED
+    ob = call_b(-1)  # the library's choice (6) falls back to 5
+    oa = chain_prefill(a, cfg=CHAIN)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
 
 
 def test_chain_one_token_sequences_match_decode(dev):
@@ -98,13 +151,14 @@ def test_chain_one_token_sequences_match_decode(dev):
     check_prefill(w, a, out_p)
 
 
-def test_chain_against_single_kernel_configs(dev):
+@BOTH
+def test_chain_against_single_kernel_configs(dev, cfg):
     """Against the chunked single kernel (4) and the token-by-token one (2):
     outputs within the output tolerance, states within the prefill bound."""
     lens = [300, 7, 64, 129, 16]
     w = workloads.prefill_inputs(lens, 8, seed=186, layout="packed")
     a = w.to(dev)
-    oa = chain_prefill(a)
+    oa = chain_prefill(a, cfg=cfg)
     torch.cuda.synchronize()
     for config in (4, 2):
         b = w.to(dev)
@@ -127,7 +181,8 @@ def test_chain_many_items_per_cta(dev):
     check_prefill(w, wd, out)
 
 
-def test_chain_misaligned_pool_same_bits(dev):
+@BOTH
+def test_chain_misaligned_pool_same_bits(dev, cfg):
     """A 2-byte aligned pool takes plain loads and stores: the same bits."""
     w = workloads.prefill_inputs([6, 21, 40], 4, seed=176)
     a, b = w.to(dev), w.to(dev)
@@ -136,13 +191,14 @@ def test_chain_misaligned_pool_same_bits(dev):
     mis.copy_(b.state)
     assert mis.data_ptr() % 16 == 2
     b.state = mis
-    oa, ob = chain_prefill(a), chain_prefill(b)
+    oa, ob = chain_prefill(a, cfg=cfg), chain_prefill(b, cfg=cfg)
     torch.cuda.synchronize()
     assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
     assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
 
 
-def test_chain_bad_bounds_set_the_error_bit(dev):
+@BOTH
+def test_chain_bad_bounds_set_the_error_bit(dev, cfg):
     """Sequences with bad bounds are skipped and flagged; the valid ones keep
     their own chunk images even when a bad sequence sits between two valid
     ones whose rows come out of order (rows 32..47, then 0..31)."""
@@ -150,7 +206,7 @@ def test_chain_bad_bounds_set_the_error_bit(dev):
     w.cu_seqlens = torch.tensor([0, 5, 9, 3], dtype=torch.int32)  # sequence 2 runs backwards
     wd = w.to(dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    out = chain_prefill(wd, error_word=err)
+    out = chain_prefill(wd, cfg=cfg, error_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == kda.KDA_ERR_SEQLENS
     check_prefill(w, wd, out, err_expected=oracle.PREFILL_ERR_SEQLENS)
@@ -159,19 +215,20 @@ def test_chain_bad_bounds_set_the_error_bit(dev):
     w.cu_seqlens = torch.tensor([32, 48, 0, 32], dtype=torch.int32)
     wd = w.to(dev)
     err.zero_()
-    out = chain_prefill(wd, error_word=err)
+    out = chain_prefill(wd, cfg=cfg, error_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == kda.KDA_ERR_SEQLENS
     check_prefill(w, wd, out, err_expected=oracle.PREFILL_ERR_SEQLENS)
 
 
-def test_chain_graph_replays_are_identical(dev):
+@BOTH
+def test_chain_graph_replays_are_identical(dev, cfg):
     w = workloads.prefill_inputs([12, 1, 90], 5, seed=178)
     wd = w.to(dev)
     st0 = wd.state.clone()
     ws = workspace_for(wd)
     out = torch.empty((wd.q.shape[0], 12, 128), dtype=torch.bfloat16, device=dev)
-    fn = lambda: chain_prefill(wd, out=out, workspace=ws)  # noqa: E731
+    fn = lambda: chain_prefill(wd, out=out, workspace=ws, cfg=cfg)  # noqa: E731
     fn()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
@@ -187,15 +244,16 @@ def test_chain_graph_replays_are_identical(dev):
         assert torch.equal(o, res[0][0]) and torch.equal(s, res[0][1])
 
 
-def test_chain_workspace_contents_do_not_matter(dev):
+@BOTH
+def test_chain_workspace_contents_do_not_matter(dev, cfg):
     """A workspace full of garbage, and one reused from a different call, give the same bits."""
     w = workloads.prefill_inputs([33, 70], 3, seed=179)
     a, b = w.to(dev), w.to(dev)
     ws = workspace_for(a)
     ws.fill_(0xFF)
-    oa = chain_prefill(a, workspace=ws)
+    oa = chain_prefill(a, workspace=ws, cfg=cfg)
     ws.random_(0, 256)
-    ob = chain_prefill(b, workspace=ws)
+    ob = chain_prefill(b, workspace=ws, cfg=cfg)
     torch.cuda.synchronize()
     assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
     assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
@@ -225,7 +283,8 @@ def test_chain_rejects_bad_workspaces(dev):
     w = workloads.prefill_inputs([3, 40], 4, seed=181)
     wd = w.to(dev)
     need = kda.prefill_workspace_bytes(wd.q.shape[0], 2, wd.H)
-    assert need == ((43 + 15) // 16 + 2) * 12 * 45568
+    images = ((43 + 15) // 16 + 2) * 12
+    assert need == images * 45568 + (images * 4 + 15) // 16 * 16
     with pytest.raises(kda.KdaError) as e:  # configuration 5 without a workspace
         gpu_prefill(wd, config_override=CHAIN)
     assert e.value.status == kda.KDA_EINVAL
@@ -246,15 +305,16 @@ def test_chain_rejects_bad_workspaces(dev):
 
 
 def test_chain_selector(dev):
-    assert kda.kda_select_prefill_ws_config(4096, 1, 12) == CHAIN
+    assert kda.kda_select_prefill_ws_config(4096, 1, 12) == FUSED
+    assert kda.kda_select_prefill_ws_config(8 * 2048, 8, 12) == CHAIN
     assert kda.kda_select_prefill_ws_config(512 * 16, 512, 12) == 4
     assert kda.kda_select_prefill_ws_config(64 * 256, 64, 12) == 4
     w = workloads.prefill_inputs([700, 400], 3, seed=182)
     a, b = w.to(dev), w.to(dev)
-    oa = chain_prefill(a, config_override=-1)
-    ob = chain_prefill(b)
+    oa = chain_prefill(a, cfg=-1)
+    ob = chain_prefill(b, cfg=FUSED)
     torch.cuda.synchronize()
-    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16)), "the library's choice is configuration 5"
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16)), "the library's choice is configuration 6"
 
 
 def test_chain_bench_shape_1x4096_full(dev):

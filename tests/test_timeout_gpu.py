@@ -124,16 +124,18 @@ def test_prefill_timeout_skips_and_reports(dev, wlib):
     assert torch.equal(wd.state.cpu().view(torch.int16), w.state.view(torch.int16))
 
 
-def test_prefill_two_stage_timeout_skips_and_reports(dev, wlib):
-    """Configuration 5: the chain kernel's waits for the state and for its
-    chunk images run out; the preparation kernel, which waits for nothing,
-    still fills the workspace."""
+@pytest.mark.parametrize("config", [5, 6])
+def test_prefill_two_stage_timeout_skips_and_reports(dev, wlib, config):
+    """Configurations 5 and 6: the chain's waits for the state and for its
+    chunk images run out; the preparation, which waits for nothing (and in
+    configuration 6 publishes every image it writes), still fills the
+    workspace."""
     w = workloads.prefill_inputs([5, 19, 1, 70], 8, seed=735)
     wd = w.to(dev)
     L = w.q.shape[0]
     out, err = _sentinel_out((L, 12, 128), dev), _err(dev)
     p = _params(wd, out, err, n_indices=4)
-    p.config_override = 5
+    p.config_override = config
     sq = kda.KdaSeqs(wd.cu_seqlens.data_ptr(), 4)
     ws = torch.empty(int(wlib.kda_prefill_workspace_bytes(L, 4, 12)), dtype=torch.uint8, device=dev)
     assert wlib.kda_prefill_ws(ctypes.byref(p), ctypes.byref(sq), ws.data_ptr(), ws.numel(),
