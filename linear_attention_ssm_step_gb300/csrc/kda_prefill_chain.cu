@@ -520,13 +520,18 @@ __device__ __forceinline__ bool wait_image_bounded(const uint32_t* flags, long l
 }
 
 // The chain over items it0, it0 + stride, ... (item = (sequence, head)) by
-// one 288-thread CTA with shared memory `sm` (cn_layout). flags: NULL when the
-// images are complete before the chain starts (two launches), else each
-// image's copy waits for its flag (one launch, preparation running beside).
+// one CTA of 288 threads (or 320: a tenth warp that only copies images) with
+// shared memory `sm` (cn_layout). flags: NULL when the images are complete
+// before the chain starts (two launches), else each image's copy waits for
+// its flag (one launch, preparation running beside). Thread `loader` issues
+// the image copies: lane 0 of the issuing warp, or of the tenth warp, which
+// takes part in no per-round barrier, so that a flag wait never holds up a
+// product.
 template <bool TMA>
 __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda_params& p, const int32_t* __restrict__ cu,
                             const int num_seqs, const unsigned char* __restrict__ ws, const long long ws_images,
-                            const uint32_t* flags, const int it0, const int stride, unsigned char* sm) {
+                            const uint32_t* flags, const int it0, const int stride, const int loader,
+                            unsigned char* sm) {
   const CUtensorMap& smap = *smap_p;
   const int tid = threadIdx.x, warp = tid >> 5;
   const bool worker = tid < CN_WORKERS, issuer = warp == CN_MMA_WARP;
@@ -608,7 +613,7 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
         *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, row)) = gstate[(int64_t)r * KD + row];
     }
     for (int j = 0; j < min(CN_NBUF, nch); ++j) {
-      if (tid == 0) issue_image(j, j);
+      if (tid == loader) issue_image(j, j);
       pendI |= 1u << j;
     }
 
@@ -640,7 +645,7 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
       pendI &= ~(1u << b);
       if (j >= 1 && j + 2 < nch) {  // chunk j + 2 into the buffer chunk j - 1 has released
         const int bn = (j + 2) % CN_NBUF;
-        if (tid == CN_WORKERS) issue_image(j + 2, bn);
+        if (tid == loader) issue_image(j + 2, bn);
         pendI |= 1u << bn;
       }
       tc_fence_after();
@@ -858,14 +863,15 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
   unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   // The preparation grid has finished and its chunk images are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  chain_items<TMA>(&smap, p, cu, num_seqs, ws, ws_images, nullptr, blockIdx.x, gridDim.x, sm);
+  chain_items<TMA>(&smap, p, cu, num_seqs, ws, ws_images, nullptr, blockIdx.x, gridDim.x, CN_WORKERS, sm);
 }
 
 // ---------------------------------------------------------------- one launch
 
 // The single-launch schedule (configuration 6), a cooperative grid of one CTA
-// per SM: CTA c < num_seqs * H carries chain c; every other CTA runs two
-// preparation groups (warps 0-3 and 4-7) over the chunk images in chunk-major
+// per SM, 320 threads: CTA c < num_seqs * H carries chain c (its tenth warp
+// copies the images); every other CTA runs two preparation groups (warps 0-3
+// and 4-7) over the chunk images in chunk-major
 // order (chunk 0 of every chain, then chunk 1, ...), publishing each image with
 // a flag that the chains wait for. The preparation never waits for a chain,
 // and every CTA is resident (cooperative launch), so every wait ends.
@@ -875,8 +881,10 @@ static_assert(28672u + 2u * PP_TOK_BYTES + 9u * 512u + 2048u + 128u + 64u + 4u *
                   PP_GROUP_STRIDE,
               "a preparation group's shared memory");
 
+constexpr int FU_THREADS = CN_THREADS + 32;
+
 template <bool TMA>
-__global__ void __launch_bounds__(CN_THREADS, 1)
+__global__ void __launch_bounds__(FU_THREADS, 1)
     kda_prefill_fused_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p,
                              const int32_t* __restrict__ cu, const int num_seqs, unsigned char* __restrict__ ws,
                              const long long ws_images, uint32_t* flags) {
@@ -884,7 +892,7 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
   unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int nchains = num_seqs * p.H;  // at most half the grid (host)
   if ((int)blockIdx.x < nchains) {
-    chain_items<TMA>(&smap, p, cu, num_seqs, ws, ws_images, flags, blockIdx.x, nchains, sm);
+    chain_items<TMA>(&smap, p, cu, num_seqs, ws, ws_images, flags, blockIdx.x, nchains, CN_THREADS, sm);
     return;
   }
   // Sequence table: first row, chunk count, first image, active.
@@ -908,7 +916,7 @@ __global__ void __launch_bounds__(CN_THREADS, 1)
     smax[0] = mx;
   }
   __syncthreads();
-  if (threadIdx.x >= 2 * CH_THREADS) return;  // warp 8 has no preparation role
+  if (threadIdx.x >= 2 * CH_THREADS) return;  // warps 8 and 9 have no preparation role
   const int g = threadIdx.x / CH_THREADS, gtid = threadIdx.x % CH_THREADS;
   const long long Q = 2LL * (gridDim.x - nchains);
   const long long slots = (long long)smax[0] * nchains;
@@ -979,11 +987,11 @@ static cudaError_t launch_fused(const CUtensorMap& map, const kda_params& q, con
   cudaError_t e = set_smem_limit_once(kern, smem, smem_set);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CN_THREADS, smem)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, FU_THREADS, smem)) != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)sms);  // one CTA per SM, all resident
-  cfg.blockDim = dim3(CN_THREADS);
+  cfg.blockDim = dim3(FU_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
