@@ -22,7 +22,8 @@ carries:
   cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload,
                on one core and on all host cores;
   sweep        T=1 decode at B = 1..2048, L2-cold per call and warm in 16-step
-               loops (also on an fp8 pool, and with the pre-computed gate
+               loops (also on an fp8 pool, with T = 8 verify on the fp8 pool
+               at B = 1, 32, 512, and with the pre-computed gate
                convention at B = 8, 512), T=8 verify and T=8 ring verify at
                B = 1, 32, 512 (0/50/100% of rows folding), L2-cold, and the
                varlen prefill at 1 x 4096, 8 x 2048, 64 x 256 and 512 x 16
@@ -415,6 +416,22 @@ def sweep(dev, steps=100, warmup=100):
         res["t1_decode_fp8_state"].append({"B": B, "us": us, "us_p10": p10, "us_p90": p90,
                                            "GB/s": round(nb / us / 1e3, 1),
                                            "us_warm_16step_graph": round(tw * 1e3, 2)})
+        del w, wd, c_d, s_d
+    # T=8 verify on the fp8 pool (kda_verify_fp8): T decode steps per call,
+    # the row requantized after every token
+    res["t8_verify_fp8_state"] = []
+    for B in (1, 32, 512):
+        w = workloads.decode_inputs(B, B + 128, seed=70 + B, T=8, layout="fused")
+        codes, scales = workloads.fp8_pool(B + 128, seed=80 + B)
+        wd = w.to(dev)
+        c_d, s_d = codes.to(dev), scales.to(dev)
+        out = torch.empty((B, 8, 12, 128), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_verify_fp8(c_d, s_d, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
+                                        wd.beta_logit, wd.A_log, wd.dt_bias, out=out)
+        us, p10, p90 = spread(time_calls(graphed(fn), steps, warmup, before=flush))
+        nb = traffic.verify_fp8_bytes(B, 8)
+        res["t8_verify_fp8_state"].append({"B": B, "us": us, "us_p10": p10, "us_p90": p90,
+                                           "GB/s": round(nb / us / 1e3, 1)})
         del w, wd, c_d, s_d
     res["t1_decode_precomputed_gate"] = []
     for B in (8, 512):

@@ -1,5 +1,5 @@
 /*
- * kda_fp8.h - T=1 decode on an fp8 (E4M3) state pool: the C ABI.
+ * kda_fp8.h - T=1 decode and T-token verify on an fp8 (E4M3) state pool: the C ABI.
  *
  * Source: "feat(kda): add packed-input CuTe decode kernel" (PR #4417),
  * section "Nsight Compute": the bf16 decode at B=512 already runs at the
@@ -61,6 +61,20 @@ typedef struct {
    overlapping the codes or the scales; KDA_EUNSUPPORTED for
    config_override 4; otherwise as kda_decode. */
 kda_status kda_decode_fp8(const kda_params* p, const kda_fp8_pool* f, void* stream);
+
+/* T-token speculative verify on an fp8 pool (source: as kda_decode_fp8, with
+   the verify of "feat(kda): ReplaySSM verify+flush decode kernel for Kimi K3
+   (KDA)" (PR #4864), section "API": T draft tokens of each row on one slot).
+   The reading: T kda_decode_fp8 steps in order on the same slot, the row
+   requantized after every token (as kda_verify rounds the bf16 state after
+   every token), so the call equals T kda_decode_fp8 calls bit for bit. p and
+   f as for kda_decode_fp8 with kda_verify's token views ([B][T][H][...] by
+   b_stride / t_stride / h_stride) and out [B][T][H][V]; 1 <= T <= KDA_MAX_T.
+   config_override 0..3 as kda_decode_fp8's; -1: kda_select_config(B, T),
+   with whole-head tiles where that picks configuration 4 (which, like 4
+   given explicitly, has no fp8 form: KDA_EUNSUPPORTED). Errors as
+   kda_decode_fp8 and kda_verify. */
+kda_status kda_verify_fp8(const kda_params* p, int32_t T, const kda_fp8_pool* f, void* stream);
 
 #ifdef __cplusplus
 }

@@ -14,6 +14,9 @@
 namespace kda {
 // T=1 decode on an fp8 pool (kda_fp8.cu); tile_v and bulk as launch_step's.
 cudaError_t launch_decode_fp8(const kda_params& p, const kda_fp8_pool& f, int tile_v, bool bulk, cudaStream_t s);
+// T-token verify on an fp8 pool (kda_fp8.cu); tile_v and bulk as above.
+cudaError_t launch_verify_fp8(const kda_params& p, const kda_fp8_pool& f, int T, int tile_v, bool bulk,
+                              cudaStream_t s);
 // Varlen prefill token by token on the CUDA cores (kda_prefill.cu): num_seqs * H * (128 / tile_v) CTAs.
 cudaError_t launch_prefill(const kda_params& p, const int32_t* cu, int num_seqs, int tile_v, bool bulk,
                            cudaStream_t s);
@@ -384,16 +387,23 @@ kda_status kda_prefill_static(const kda_params* p, const kda_seqs* sq, void* str
   return kda_prefill_ws(&q, sq, ws, KDA_PREFILL_STATIC_BYTES, stream);
 }
 
-kda_status kda_decode_fp8(const kda_params* p, const kda_fp8_pool* f, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The checks of the fp8-pool calls for T tokens: the shared ones without the
+// bf16 pool's, then the fp8 pool's. On success, sets *bulk.
+kda_status check_fp8(const kda_params* p, int T, const kda_fp8_pool* f, bool* bulk_out) {
   if (p == nullptr) return fail(KDA_EINVAL, "params is NULL");
-  // The shared checks without the bf16 pool's (N = 0 there); the fp8 pool's follow.
   kda_params common = *p;
   common.N = 0;
   bool unused = false;
-  kda_status s = check_params(&common, 1, &unused);
+  kda_status s = check_params(&common, T, &unused);
   if (s != KDA_OK) return s;
   if (p->config_override == kTensorCoreConfig)
-    return fail(KDA_EUNSUPPORTED, "config_override = %d (tensor-core verify) needs T > 1", kTensorCoreConfig);
+    return fail(KDA_EUNSUPPORTED, T == 1 ? "config_override = %d (tensor-core verify) needs T > 1"
+                                         : "config_override = %d (tensor-core verify) has no fp8-pool form",
+                kTensorCoreConfig);
   if (f == nullptr) return fail(KDA_EINVAL, "fp8 pool is NULL");
   const int64_t slot = (int64_t)p->H * 128 * 128, sslot = (int64_t)p->H * 128;
   bool bulk = false;
@@ -411,7 +421,7 @@ kda_status kda_decode_fp8(const kda_params* p, const kda_fp8_pool* f, void* stre
            (p->N == 1 || (p->state_slot_stride % 16 == 0 && f->scale_slot_stride % 4 == 0));
     if (p->B > 0) {
       uintptr_t o0, o1;
-      view_extent(p->out, p->B, 1, p->H, 128, p->out_b_stride, p->out_t_stride, p->out_h_stride, o0, o1);
+      view_extent(p->out, p->B, T, p->H, 128, p->out_b_stride, p->out_t_stride, p->out_h_stride, o0, o1);
       const uintptr_t c0 = reinterpret_cast<uintptr_t>(p->state);
       const uintptr_t c1 = c0 + (uintptr_t)((int64_t)(p->N - 1) * p->state_slot_stride + slot);
       const uintptr_t s0 = reinterpret_cast<uintptr_t>(f->scale);
@@ -420,9 +430,35 @@ kda_status kda_decode_fp8(const kda_params* p, const kda_fp8_pool* f, void* stre
       if (overlaps(o0, o1, s0, s1)) return fail(KDA_EINVAL, "out overlaps the fp8 scales");
     }
   }
+  *bulk_out = bulk;
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_decode_fp8(const kda_params* p, const kda_fp8_pool* f, void* stream) {
+  bool bulk = false;
+  const kda_status s = check_fp8(p, 1, f, &bulk);
+  if (s != KDA_OK) return s;
   if (p->B == 0) return ok();
   cudaError_t e = kda::launch_decode_fp8(*p, *f, kTileV[pick_config(p, 1)], bulk, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_decode_fp8 launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+kda_status kda_verify_fp8(const kda_params* p, int32_t T, const kda_fp8_pool* f, void* stream) {
+  bool bulk = false;
+  const kda_status s = check_fp8(p, T, f, &bulk);
+  if (s != KDA_OK) return s;
+  if (p->B == 0) return ok();
+  // The library's choice: kda_select_config's tile, whole heads where it picks
+  // the tensor-core configuration (which has no fp8-pool form).
+  const int cfg = p->config_override >= 0 ? p->config_override : kda_select_config(p->B, T);
+  const int tile_v = cfg == kTensorCoreConfig ? 128 : kTileV[cfg];
+  cudaError_t e = kda::launch_verify_fp8(*p, *f, T, tile_v, bulk, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify_fp8 launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -30,6 +30,7 @@
 
 #include "kda_device.cuh"
 #include "kda_fp8.h"
+#include "kda_launch.h"
 
 namespace kda {
 
@@ -280,6 +281,183 @@ __global__ void __launch_bounds__(NTHREADS, 5)
     outp[out_base + (int64_t)(i / TV) * p.out_h_stride + i % TV] = float_to_bf16_bits(o);
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// T-token verify on the fp8 pool: one CTA of 128 threads per (batch row,
+// head, tile of TV value rows). The T-token prologue of the bf16 verify, then
+// each warp holds its rows' codes and scales in registers across the tokens,
+// and every token dequantizes, steps and requantizes each row exactly as one
+// kda_decode_fp8 call does (row_step_fp8), so that T tokens equal T decode
+// calls bit for bit.
+__host__ __device__ constexpr size_t fp8_verify_smem_bytes(int TV, int T) {
+  return (size_t)TV * F8_ROW_BYTES                    // codes
+         + (size_t)TV * 4                             // row scales
+         + 64                                         // 4 mbarriers (padded)
+         + ((size_t)T * KD * 4                        // kh, qh, dd, gg
+            + (size_t)T * TV * 2                      // vrow, orow
+            + (size_t)KDA_MAX_T * 2 + 3 * KD) * 4;    // beta, kappa, reduction products
+}
+
+template <int TV, bool BULK>
+__global__ void __launch_bounds__(NTHREADS, 3)
+    kda_verify_fp8_kernel(const kda_params p, const kda_fp8_pool f, const int T, const int tiles) {
+  static_assert(TV % 16 == 0 && TV >= 16 && TV <= KD, "tile must be a multiple of 16 rows");
+  constexpr int RW = TV / NWARPS;          // rows per warp
+  constexpr int RQ = RW / ROWS_PER_WARP;   // 4-row groups per warp
+  constexpr int PT = (KDA_MAX_T + NWARPS - 1) / NWARPS;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = blockIdx.x % tiles;
+  const int bh = blockIdx.x / tiles;
+  const int h = bh % p.H;
+  const int b = bh / p.H;
+  const int v0 = tile * TV;
+
+  uint8_t* st = smem;
+  float* ssc = reinterpret_cast<float*>(smem + TV * F8_ROW_BYTES);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + TV * F8_ROW_BYTES + TV * 4);
+  float* fbase = reinterpret_cast<float*>(smem + TV * F8_ROW_BYTES + TV * 4 + 64);
+  TokenSmem ts;
+  ts.kh = fbase;
+  ts.qh = ts.kh + T * KD;
+  ts.dd = ts.qh + T * KD;
+  ts.gg = ts.dd + T * KD;
+  ts.vrow = ts.gg + T * KD;
+  float* orow = ts.vrow + T * TV;
+  ts.beta = orow + T * TV;
+  ts.kappa = ts.beta + KDA_MAX_T;
+  ts.red = ts.kappa + KDA_MAX_T;
+
+  uint16_t* outp = static_cast<uint16_t*>(p.out);
+  const int64_t out_base = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + v0;
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int n = p.state_indices[b];
+  TokenLoads<PT> first;
+  prologue_issue<PT, NWARPS>(p, b, h, T, v0, TV, first);
+  if (n < 0 || n >= p.N) {
+    for (int i = tid; i < T * TV; i += NTHREADS) {
+      const int t = i / TV, r = i - t * TV;
+      outp[out_base + (int64_t)t * p.out_t_stride + r] = 0;
+    }
+    return;
+  }
+
+  const int64_t row0 = (int64_t)h * KD + v0 + warp * RW;
+  uint8_t* gst = static_cast<uint8_t*>(p.state) + (int64_t)n * p.state_slot_stride + row0 * F8_ROW_BYTES;
+  float* gsc = f.scale + (int64_t)n * f.scale_slot_stride + row0;
+  uint8_t* sst = st + warp * RW * F8_ROW_BYTES;
+  float* ssw = ssc + warp * RW;
+  constexpr uint32_t CODE_BYTES = RW * F8_ROW_BYTES, SCALE_BYTES = RW * 4;
+
+  if constexpr (BULK) {
+    if (lane == 0) {
+      mbar_init(&mbar[warp], 1);
+      mbar_expect_tx(&mbar[warp], CODE_BYTES + SCALE_BYTES);
+      bulk_g2s(sst, gst, CODE_BYTES, &mbar[warp]);
+      bulk_g2s(ssw, gsc, SCALE_BYTES, &mbar[warp]);
+    }
+  } else {
+    for (int i = lane; i < (int)CODE_BYTES; i += 32) sst[i] = gst[i];
+    for (int i = lane; i < RW; i += 32) ssw[i] = gsc[i];
+  }
+
+  token_prologue<PT, NWARPS>(p, b, h, T, v0, TV, ts, first);  // ends with a CTA barrier
+
+  bool ok = true;
+  __syncwarp();
+  if constexpr (BULK) ok = mbar_wait_bounded(&mbar[warp], 0);
+  const int r = lane / LPR, j = lane % LPR;  // row within a 4-row group, lane within the row
+
+  if (ok) {
+    uint4 c[RQ];
+    float rs[RQ];
+#pragma unroll
+    for (int q = 0; q < RQ; ++q) {
+      const int row = ROWS_PER_WARP * q + r;
+      c[q] = *reinterpret_cast<const uint4*>(sst + row * F8_ROW_BYTES + 16 * j);
+      rs[q] = ssw[row];
+    }
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+      LaneVecs lv;
+      load_pairs16(ts.kh + t * KD, j, lv.kh);
+      load_pairs16(ts.qh + t * KD, j, lv.qh);
+      load_pairs16(ts.dd + t * KD, j, lv.dd);
+      const float beta = ts.beta[t], kappa = ts.kappa[t];
+#pragma unroll
+      for (int q = 0; q < RQ; ++q) {
+        const int row = warp * RW + ROWS_PER_WARP * q + r;  // within the tile
+        const float o = row_step_fp8(c[q], rs[q], lv, j, beta, kappa, ts.vrow[t * TV + row], p.scale);
+        if (j == 0) orow[t * TV + row] = o;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < RQ; ++q) {
+      const int row = ROWS_PER_WARP * q + r;
+      *reinterpret_cast<uint4*>(sst + row * F8_ROW_BYTES + 16 * j) = c[q];
+      if (j == 0) ssw[row] = rs[q];
+    }
+    if constexpr (BULK) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_s2g(gst, sst, CODE_BYTES);
+        bulk_s2g(gsc, ssw, SCALE_BYTES);
+        bulk_commit();
+        bulk_wait_read_all();
+      }
+    } else {
+      __syncwarp();
+      for (int i = lane; i < (int)CODE_BYTES; i += 32) gst[i] = sst[i];
+      for (int i = lane; i < RW; i += 32) gsc[i] = ssw[i];
+    }
+  } else {
+    if (lane == 0) {
+      if (p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
+      if constexpr (BULK) mbar_drain_bounded(&mbar[warp], 0);
+    }
+    for (int i = lane; i < RW * T; i += 32) orow[(i / RW) * TV + warp * RW + i % RW] = 0.0f;
+  }
+  __syncthreads();
+  for (int i = tid; i < T * TV; i += NTHREADS) {
+    const int t = i / TV, rr = i - t * TV;
+    outp[out_base + (int64_t)t * p.out_t_stride + rr] = float_to_bf16_bits(orow[i]);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <int TV, bool BULK>
+static cudaError_t launch_vf8(const kda_params& p, const kda_fp8_pool& f, int T, cudaStream_t s) {
+  auto kern = kda_verify_fp8_kernel<TV, BULK>;
+  const size_t smem = fp8_verify_smem_bytes(TV, KDA_MAX_T);  // sized for any T, so one attribute call suffices
+  static std::atomic<bool> smem_set{false};
+  cudaError_t e = set_smem_limit_once(kern, smem, smem_set);
+  if (e != cudaSuccess) return e;
+  const int tiles = KD / TV;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((long long)p.B * p.H * tiles));
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = fp8_verify_smem_bytes(TV, T);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, f, T, tiles);
+}
+
+cudaError_t launch_verify_fp8(const kda_params& p, const kda_fp8_pool& f, int T, int tile_v, bool bulk,
+                              cudaStream_t s) {
+  switch (tile_v) {
+    case 16: return bulk ? launch_vf8<16, true>(p, f, T, s) : launch_vf8<16, false>(p, f, T, s);
+    case 32: return bulk ? launch_vf8<32, true>(p, f, T, s) : launch_vf8<32, false>(p, f, T, s);
+    case 64: return bulk ? launch_vf8<64, true>(p, f, T, s) : launch_vf8<64, false>(p, f, T, s);
+    case 128: return bulk ? launch_vf8<128, true>(p, f, T, s) : launch_vf8<128, false>(p, f, T, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int TV, int HP, bool BULK>

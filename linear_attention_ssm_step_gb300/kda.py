@@ -76,6 +76,8 @@ class KdaSeqs(ctypes.Structure):
 EXPORTS = {
     "kda_decode": ([ctypes.POINTER(KdaParams), ctypes.c_void_p], ctypes.c_int),
     "kda_decode_fp8": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaFp8Pool), ctypes.c_void_p], ctypes.c_int),
+    "kda_verify_fp8": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.POINTER(KdaFp8Pool), ctypes.c_void_p],
+                       ctypes.c_int),
     "kda_verify": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "kda_prefill": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaSeqs), ctypes.c_void_p], ctypes.c_int),
     "kda_select_prefill_config": ([ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
@@ -264,6 +266,22 @@ def kda_decode_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_l
                 lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.uint8)
     f = _fp8_pool(codes, scales)
     _check(load_library().kda_decode_fp8(ctypes.byref(p), ctypes.byref(f), _stream_handle(stream, q.device)))
+    return out
+
+
+def kda_verify_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out=None,
+                   lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1, gate_mode=KDA_GATE_RAW,
+                   stream=None):
+    """T-token verify on an fp8 state pool (include/kda_fp8.h): the pool as for
+    kda_decode_fp8, the token views and output as for kda_verify
+    ([B, T, H, 128]); equal to T kda_decode_fp8 calls, bit for bit."""
+    B, T, H = q.shape[0], q.shape[1], q.shape[2]
+    if out is None:
+        out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=q.device)
+    p = _params(codes, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
+                lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.uint8)
+    f = _fp8_pool(codes, scales)
+    _check(load_library().kda_verify_fp8(ctypes.byref(p), T, ctypes.byref(f), _stream_handle(stream, q.device)))
     return out
 
 

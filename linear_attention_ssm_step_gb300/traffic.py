@@ -62,6 +62,11 @@ def decode_fp8_bytes(n_active, n_inactive=0):
             + n_inactive * (INDEX_BYTES + H * V * 2) + PER_CALL_BYTES)
 
 
+def verify_fp8_bytes(n_active, T, n_inactive=0):
+    return (n_active * (2 * FP8_STATE_BYTES + T * TOKEN_IO_BYTES + INDEX_BYTES)
+            + n_inactive * (INDEX_BYTES + T * H * V * 2) + PER_CALL_BYTES)
+
+
 def prefill_bytes(lengths, n_inactive_tokens=0):
     """Active sequences of the given lengths, plus inactive tokens (zero outputs)."""
     return (sum(2 * STATE_BYTES + n * TOKEN_IO_BYTES + INDEX_BYTES + 8 for n in lengths)
