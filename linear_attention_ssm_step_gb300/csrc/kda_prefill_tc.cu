@@ -143,6 +143,10 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
   bool pendA = false, pendD = false, pendU = false;                  // a copy or a product is in flight
   bool broken = false;  // a bounded wait gave up: nothing more is issued
 
+  // The first chunk's token inputs of an item, loaded during the previous
+  // item's last chunk when that item had one (pre_it: the item they are for).
+  TokenRegs<PC> L;
+  int pre_it = -1;
   for (int it = blockIdx.x; it < total; it += gridDim.x) {
     const int seq = it / p.H, h = it - seq * p.H;
     const int t0 = cu[seq], t1 = cu[seq + 1];
@@ -172,9 +176,11 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
         *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, tid)) = gstate[(int64_t)r * KD + tid];
     }
 
-    TokenRegs<PC> L;
-    zero_tokens(L);
-    load_tokens(p, t0, h, min(PC, t1 - t0), L);
+    if (pre_it != it) {
+      zero_tokens(L);
+      load_tokens(p, t0, h, min(PC, t1 - t0), L);
+    }
+    pre_it = -1;
     bool first = true, ok = true;
     for (int c0 = t0; c0 < t1; c0 += PC) {
       const int Tc = min(PC, t1 - c0);
@@ -353,6 +359,15 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
       if (c0 + PC < t1) {  // the next chunk's token inputs fly while this chunk finishes
         zero_tokens(L);
         load_tokens(p, c0 + PC, h, min(PC, t1 - c0 - PC), L);
+      } else if (it + (int)gridDim.x < total) {  // the last chunk: the next item's first chunk
+        const int nit = it + gridDim.x;
+        const int nseq = nit / p.H, nh = nit - nseq * p.H;
+        const int n0 = cu[nseq], n1 = cu[nseq + 1];
+        if (n0 >= 0 && n1 > n0 && n1 <= p.B) {  // a sequence with tokens (loaded even if inactive: unused then)
+          zero_tokens(L);
+          load_tokens(p, n0, nh, min(PC, n1 - n0), L);
+          pre_it = nit;
+        }
       }
       ok = __syncthreads_and(mbar_wait_bounded(barD, phD)) != 0;
       if (!ok) break;
