@@ -883,9 +883,13 @@ static_assert(28672u + 2u * PP_TOK_BYTES + 9u * 512u + 2048u + 128u + 64u + 4u *
 
 constexpr int FU_THREADS = CN_THREADS + 32;
 
+__device__ __noinline__ void fused_prepare_role(const kda_params* pp, const int32_t* __restrict__ cu,
+                                                const int num_seqs, const int nchains, unsigned char* __restrict__ ws,
+                                                const long long ws_images, uint32_t* flags, unsigned char* sm);
+
 template <bool TMA>
 __global__ void __launch_bounds__(FU_THREADS, 1)
-    kda_prefill_fused_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p,
+    kda_prefill_fused_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__ kda_params p,
                              const int32_t* __restrict__ cu, const int num_seqs, unsigned char* __restrict__ ws,
                              const long long ws_images, uint32_t* flags) {
   extern __shared__ unsigned char smem_raw[];
@@ -895,6 +899,16 @@ __global__ void __launch_bounds__(FU_THREADS, 1)
     chain_items<TMA>(&smap, p, cu, num_seqs, ws, ws_images, flags, blockIdx.x, nchains, CN_THREADS, sm);
     return;
   }
+  fused_prepare_role(&p, cu, num_seqs, nchains, ws, ws_images, flags, sm);
+}
+
+// The preparation role of the one-launch kernel, compiled as a function of its
+// own (not inlined), so that its register demand does not shape the chain
+// role's code in the same kernel.
+__device__ __noinline__ void fused_prepare_role(const kda_params* pp, const int32_t* __restrict__ cu,
+                                                const int num_seqs, const int nchains, unsigned char* __restrict__ ws,
+                                                const long long ws_images, uint32_t* flags, unsigned char* sm) {
+  const kda_params& p = *pp;
   // Sequence table: first row, chunk count, first image, active.
   int* st0 = reinterpret_cast<int*>(sm + FU_TABLE);
   int* snch = st0 + FU_MAX_SEQS;

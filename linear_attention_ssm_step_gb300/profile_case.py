@@ -44,8 +44,9 @@ def main():
                                         w.beta_logit, w.A_log, w.dt_bias, config_override=a.config)
     elif a.call == "prefill":
         w = workloads.prefill_inputs([a.len] * a.B, a.B + 8, seed=90 + a.B, layout="fused", H=a.H).to(dev)
+        ws = kda.prefill_workspace(a.len * a.B, a.B, a.H, dev)  # the two-stage configurations' workspace
         fn = lambda: kda.kda_prefill(w.state, w.state_indices, w.cu_seqlens, w.q, w.k, w.v, w.g_raw,  # noqa: E731
-                                     w.beta_logit, w.A_log, w.dt_bias, config_override=a.config)
+                                     w.beta_logit, w.A_log, w.dt_bias, config_override=a.config, workspace=ws)
     elif a.call == "verify":
         w = workloads.decode_inputs(a.B, a.B + 64, seed=3, T=a.T).to(dev)
         fn = lambda: kda.kda_verify(w.state, w.state_indices, w.q, w.k, w.v, w.g_raw, w.beta_logit,  # noqa: E731
