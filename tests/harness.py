@@ -290,6 +290,17 @@ def ring_teacher_forced(w, wd, out, rows=None):
         for i in range(R):
             P = int((cb[i] + base[i] + t) % W)
             u_got, u_ref = uc[i][:, P], ref["u_cache"][i][:, P]  # [H, 128]
+            # k~ = bf16(k_hat) with k_hat computed in fp32 on the GPU: a key
+            # within fp32 rounding of a bf16 midpoint may land on the other
+            # neighbour (checked below: 1 ulp). u~ then follows from that key:
+            # the part sum_k |dk~_k| |(D S)[k, v]| (beta <= 1) of its error is
+            # explained, D S the oracle's decayed state before the update.
+            dk = np.abs(kc[i][:, P] - ref["k_cache"][i][:, P])  # [H, K]
+            if dk.any():
+                DS = ref["state_fp64"][i] - ref["k_cache"][i][:, P][:, :, None] * u_ref[:, None, :]
+                explained = np.einsum("hk,hkv->hv", dk, np.abs(DS))
+                diff = u_got - u_ref
+                u_got = u_ref + np.sign(diff) * np.maximum(np.abs(diff) - explained, 0.0)
             assert_state_close(u_got[:, None, :], u_ref[:, None, :], f"ring token {t} u~ (row {vrows[i]})")
             assert float(state_ulps(kc[i][:, P][:, None, :], ref["k_cache"][i][:, P][:, None, :]).max()) <= 1.0
             G, Gr = gc[i][:, P], ref["g_cache"][i][:, P]
