@@ -42,6 +42,7 @@ from .kda_fp8_oracle import (  # noqa: F401,E402
     requantize_rows,
     dequantize,
     kda_decode_fp8,
+    kda_verify_ring_fp8,
 )
 from .kda_prefill_oracle import (  # noqa: F401,E402
     kda_prefill,

@@ -1,5 +1,5 @@
-"""fp8 (E4M3) state pool for the T=1 decode: the oracle of this library's
-numeric contract for it.
+"""fp8 (E4M3) state pool for the T=1 decode and the ring verify's
+checkpoint: the oracle of this library's numeric contract for it.
 
 TEST INFRASTRUCTURE: only tests/, __graft_entry__.smoke() and bench.py's CPU
 baseline leg use this module. It shares no code with the CUDA library.
@@ -31,7 +31,8 @@ implement:
 
 import numpy as np
 
-from .kda_oracle import _active_mask, decode_step_math, prologue, round_to_bf16, round_to_fp32, GATE_RAW
+from .kda_oracle import (_active_mask, decode_step_math, kda_verify_ring, prologue, round_to_bf16, round_to_fp32,
+                         GATE_RAW)
 
 E4M3_MAX = 448.0
 E4M3_NAN = 0x7F
@@ -158,3 +159,40 @@ def kda_decode_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_l
     out[rows] = round_to_bf16(o)
     info = {"rows": rows, "slots": slots, "S_new": rows_new, "S_new_fp32": s32}
     return new_codes, new_scales, out, info
+
+
+def kda_verify_ring_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
+                        k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush=True,
+                        lower_bound=-5.0, scale=1.0, gate_mode=GATE_RAW, cache_base=None):
+    """Ring-cache verify on an fp8 checkpoint pool: kda_verify_ring ("feat(kda):
+    ReplaySSM verify+flush decode kernel for Kimi K3 (KDA)", sections "What it
+    does" and "Caching") with the pool of this module's reading as its
+    checkpoint.
+
+    The checkpoint is the pool's exact values. A fold requantizes the replayed
+    state (unrounded) row by row as kda_decode_fp8 requantizes a new state -
+    fp32 first, then each value row over its keys - writes codes and scales,
+    and the new tokens continue from their exact values. The ring entries stay
+    as kda_verify_ring writes them (bf16 k~ and u~, fp32 G).
+
+    Returns kda_verify_ring's dict with "codes" and "scales" in place of
+    "state", and "folded": {slot: the unrounded folded state [H, V, K]}.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.float64)
+    new_codes, new_scales = codes.copy(), scales.copy()
+    folded = {}
+
+    def requantize_fold(n, S):  # S: [H, K, V]
+        rows = np.swapaxes(S, -1, -2)  # value rows over their keys
+        c, e = requantize_rows(round_to_fp32(rows))
+        new_codes[n], new_scales[n] = c, np.ldexp(1.0, e)
+        folded[int(n)] = rows
+        return np.swapaxes(dequantize(c, new_scales[n]), -1, -2)
+
+    res = kda_verify_ring(dequantize(codes, scales), state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
+                          k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush, lower_bound, scale,
+                          gate_mode, cache_base, fold_round=requantize_fold)
+    del res["state"]
+    res.update(codes=new_codes, scales=new_scales, folded=folded)
+    return res

@@ -255,7 +255,7 @@ def ring_fold_closed_form(S0, k_hist, u_hist, G_hist):
 def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
                     k_cache, u_cache, g_cache, hist_len, flush_min,
                     restart_hist_on_flush=True, lower_bound=-5.0, scale=1.0, gate_mode=GATE_RAW,
-                    cache_base=None):
+                    cache_base=None, fold_round=None):
     """Ring-cache verify with replay and fold ([ring] "What it does", "API", "Caching").
 
     state (checkpoint): [N, H, V, K]; k_cache: [N, H, W, K] bf16 k_hat;
@@ -283,6 +283,10 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
         G_P) are written at position P.
     The kernel leaves hist_len alone unless it folds: the caller adds the
     number of accepted draft tokens afterwards.
+
+    fold_round(n, S) -> S', for an fp8 checkpoint pool (kda_verify_ring_fp8):
+    the checkpoint a fold of slot n makes of the replayed state S [H, K, V]
+    in place of its bf16 rounding.
 
     Returns a dict with state, k_cache, u_cache, g_cache, hist_len, out
     [B, T, H, V] and error_word, plus the diagnostic state_fp64 [B, H, K, V]:
@@ -330,7 +334,7 @@ def kda_verify_ring(state, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_
         S0 = np.swapaxes(state[n], -1, -2)  # [H, K, V]
         S = ring_replay(S0, k_cache[n][:, live], u_cache[n][:, live], g_cache[n][:, live])
         if h >= flush_min:
-            S = round_to_bf16(S)
+            S = round_to_bf16(S) if fold_round is None else fold_round(n, S)
             new["state"][n] = np.swapaxes(S, -1, -2)
             if restart_hist_on_flush:
                 new["hist_len"][n] = 0

@@ -189,4 +189,114 @@ def pin_fp8_inactive_slots(m8):
     assert np.all(np.isin(np.log2(new_s), np.arange(-200, 200)))  # powers of two
 
 
+# ---------------------------------------------------------------- the ring's checkpoint
+
+def small_ring_fp8_problem(rng, hist, flush_min, T=3, W=8, H=2, K=8, V=8, N=5, zero_history=False):
+    """A ring call on an fp8 pool: slot n's history length hist[n]; rows 0..B-1 on slots 1..B."""
+    B = len(hist)
+    codes, scales = random_pool(rng, N, H, V, K)
+    kc = rng.normal(0, 1, (N, H, W, K))
+    kc = oracle.round_to_bf16(kc / np.linalg.norm(kc, axis=-1, keepdims=True))
+    uc = oracle.round_to_bf16(rng.normal(0, 0.5, (N, H, W, V)))
+    gc = oracle.round_to_fp32(np.cumsum(-rng.uniform(0, 0.5, (N, H, W, K)), axis=2))
+    if zero_history:
+        uc[:] = 0.0
+        gc[:] = 0.0
+    hl = np.zeros(N, dtype=np.int64)
+    hl[1:B + 1] = hist
+    return dict(codes=codes, scales=scales, state_indices=np.arange(1, B + 1), q=bf16_values(rng, (B, T, H, K)),
+                k=bf16_values(rng, (B, T, H, K)), v=bf16_values(rng, (B, T, H, V)),
+                g_raw=bf16_values(rng, (B, T, H, K)), beta_logit=bf16_values(rng, (B, T, H)),
+                A_log=np.log(rng.uniform(1, 16, H)), dt_bias=rng.normal(0, 0.5, (H, K)), k_cache=kc, u_cache=uc,
+                g_cache=gc, hist_len=hl, flush_min=flush_min)
+
+
+def _ring_fp8(m8, P, **kw):
+    return m8.kda_verify_ring_fp8(P["codes"], P["scales"], P["state_indices"], P["q"], P["k"], P["v"], P["g_raw"],
+                                  P["beta_logit"], P["A_log"], P["dt_bias"], P["k_cache"], P["u_cache"],
+                                  P["g_cache"], P["hist_len"], P["flush_min"], lower_bound=LB, **kw)
+
+
+def _ring_bf16(P, state, hist_len=None):
+    return oracle.kda_verify_ring(state, P["state_indices"], P["q"], P["k"], P["v"], P["g_raw"], P["beta_logit"],
+                                  P["A_log"], P["dt_bias"], P["k_cache"], P["u_cache"], P["g_cache"],
+                                  P["hist_len"] if hist_len is None else hist_len, P["flush_min"], lower_bound=LB)
+
+
+def pin_fp8_ring_without_fold_is_bf16_ring_on_dequantized_pool(m8):
+    """No slot reaches flush_min: the (separately pinned) bf16 ring on the
+    pool's exact values, codes and scales untouched."""
+    rng = np.random.default_rng(13)
+    P = small_ring_fp8_problem(rng, hist=[0, 3, 5], flush_min=6)
+    got = _ring_fp8(m8, P)
+    ref = _ring_bf16(P, m8.dequantize(P["codes"], P["scales"]))
+    assert np.array_equal(got["codes"], P["codes"]) and np.array_equal(got["scales"], P["scales"])
+    assert not got["folded"]
+    for name in ("out", "k_cache", "u_cache", "g_cache", "hist_len"):
+        assert np.array_equal(got[name], ref[name], equal_nan=True), name
+
+
+def pin_fp8_ring_fold_requantizes_the_closed_form_state(m8):
+    """A folding slot's codes and scales are the row requantization (fp32
+    values, rows over the keys) of the closed-form replay of its history onto
+    the dequantized checkpoint, and the tokens continue from their exact
+    values: the same call as a bf16 ring call from that checkpoint with no
+    history."""
+    rng = np.random.default_rng(14)
+    P = small_ring_fp8_problem(rng, hist=[6, 2, 7], flush_min=6)
+    got = _ring_fp8(m8, P)
+    deq = m8.dequantize(P["codes"], P["scales"])
+    assert sorted(got["folded"]) == [1, 3]
+    for n in (1, 3):
+        h = int(P["hist_len"][n])
+        S = oracle.ring_fold_closed_form(np.swapaxes(deq[n], -1, -2), P["k_cache"][n][:, :h],
+                                         P["u_cache"][n][:, :h], P["g_cache"][n][:, :h])
+        rows = np.swapaxes(S, -1, -2)  # [H, V, K]
+        c, e = m8.requantize_rows(oracle.round_to_fp32(rows))
+        assert np.array_equal(got["codes"][n], c) and np.array_equal(got["scales"][n], np.ldexp(1.0, e))
+        top = np.max(np.abs(m8.e4m3_decode(got["codes"][n])), axis=-1)
+        assert np.all(top > 224.0) and np.all(top <= 448.0)
+    assert np.array_equal(got["codes"][2], P["codes"][2]), "a slot that does not fold keeps its checkpoint"
+    hist0 = np.where(P["hist_len"] >= P["flush_min"], 0, P["hist_len"])
+    ref = _ring_bf16(P, m8.dequantize(got["codes"], got["scales"]), hist_len=hist0)
+    for name in ("out", "k_cache", "u_cache", "g_cache"):
+        assert np.array_equal(got[name], ref[name], equal_nan=True), name
+    assert list(got["hist_len"][1:4]) == [0, 2, 0]
+
+
+def pin_fp8_ring_lossless_fold_changes_nothing(m8):
+    """A history of zero updates with no decay folds to the checkpoint itself,
+    which the pool holds exactly: the outputs are those of the same call
+    without the fold, value for value."""
+    rng = np.random.default_rng(15)
+    P = small_ring_fp8_problem(rng, hist=[5, 7], flush_min=5, W=12, zero_history=True)
+    a = _ring_fp8(m8, P)
+    P_nofold = dict(P, flush_min=8)
+    b = _ring_fp8(m8, P_nofold)
+    assert sorted(a["folded"]) == [1, 2] and not b["folded"]
+    assert np.array_equal(a["out"], b["out"])
+    assert np.array_equal(m8.dequantize(a["codes"], a["scales"]), m8.dequantize(P["codes"], P["scales"]))
+
+
+def pin_fp8_ring_fold_decides_in_fp32(m8):
+    """The fold's requantization is decided on the fp32 value: a folded value
+    2^-10 (1 + 2^-4 + 2^-34) is 2^-10 (1 + 2^-4) in fp32, the midpoint of two
+    codes at the row's scale 2^-10 (its largest value 448 * 2^-10), which
+    rounds to the even code 1.0; the fp64 value would round up to 1.125."""
+    rng = np.random.default_rng(16)
+    P = small_ring_fp8_problem(rng, hist=[2], flush_min=2, T=1, W=4, H=1, K=8, V=8, N=2)
+    P["codes"][1] = 0
+    P["codes"][1, :, :, 0] = 0x38  # 1.0
+    P["codes"][1, :, :, 1] = 0x7E  # 448
+    P["scales"][1] = 2.0 ** -10
+    P["k_cache"][1] = 0.0
+    P["k_cache"][1, :, :, 0] = 1.0  # both history keys are e_0
+    P["u_cache"][1, :, 0] = 2.0 ** -14
+    P["u_cache"][1, :, 1] = 2.0 ** -44
+    P["g_cache"][1] = 0.0
+    got = _ring_fp8(m8, P)
+    assert np.all(got["scales"][1] == 2.0 ** -10)
+    assert np.all(got["codes"][1, :, :, 0] == 0x38) and np.all(got["codes"][1, :, :, 1] == 0x7E)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -37,6 +37,12 @@ MUTATIONS = [
      "return e4m3_decode(codes)"),
     ("index N active", "idx, active = _active_mask(state_indices, N)",
      "idx, active = _active_mask(state_indices, N + 1)"),
+    ("ring fold continues unrounded", "return np.swapaxes(dequantize(c, new_scales[n]), -1, -2)", "return S"),
+    ("ring fold rounds to bf16", "return np.swapaxes(dequantize(c, new_scales[n]), -1, -2)",
+     "return round_to_bf16(S)"),
+    ("ring fold rows over the values", "rows = np.swapaxes(S, -1, -2)  # value rows over their keys",
+     "rows = S"),
+    ("ring fold skips fp32", "c, e = requantize_rows(round_to_fp32(rows))", "c, e = requantize_rows(rows)"),
 ]
 
 
