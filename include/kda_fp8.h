@@ -1,5 +1,5 @@
 /*
- * kda_fp8.h - T=1 decode and T-token verify on an fp8 (E4M3) state pool: the C ABI.
+ * kda_fp8.h - T=1 decode, T-token verify and the ring verify on an fp8 (E4M3) state pool: the C ABI.
  *
  * Source: "feat(kda): add packed-input CuTe decode kernel" (PR #4417),
  * section "Nsight Compute": the bf16 decode at B=512 already runs at the
@@ -75,6 +75,24 @@ kda_status kda_decode_fp8(const kda_params* p, const kda_fp8_pool* f, void* stre
    given explicitly, has no fp8 form: KDA_EUNSUPPORTED). Errors as
    kda_decode_fp8 and kda_verify. */
 kda_status kda_verify_fp8(const kda_params* p, int32_t T, const kda_fp8_pool* f, void* stream);
+
+/* Ring-cache verify with replay and fold (kda_verify_ring) on an fp8
+   checkpoint pool (source: as kda_verify_fp8; the ring from "feat(kda):
+   ReplaySSM verify+flush decode kernel for Kimi K3 (KDA)" (PR #4864),
+   sections "What it does", "API" and "Caching", whose ring entries k~, u~ stay
+   bf16 and G fp32). The reading: the checkpoint S_0 is the pool's exact
+   values codes * 2^e; the call is kda_verify_ring's on that checkpoint,
+   except that a fold requantizes the folded state row by row by this
+   header's rule (decided in fp32) instead of rounding it to bf16, writes
+   codes and scales in place, and the call continues from their exact values.
+   The kernel reads the checkpoint through the ring's bf16 product operand,
+   exact for every row whose largest magnitude is at least 2^-108. p as for
+   kda_verify_ring with p->state the E4M3 codes (16-byte aligned, slot stride
+   a multiple of 16 when N > 1), r as for kda_verify_ring, f the scales.
+   Errors as kda_verify_ring and kda_decode_fp8, plus KDA_EINVAL for codes not
+   16-byte aligned. */
+kda_status kda_verify_ring_fp8(const kda_params* p, int32_t T, const kda_ring_params* r, const kda_fp8_pool* f,
+                               void* stream);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libkda_gb300.so")
 
 SOURCES = ["kda_api.cu", "kda_step.cu", "kda_ring.cu", "kda_tmap.cu", "kda_verify_tc.cu", "kda_fp8.cu",
            "kda_prefill.cu", "kda_prefill_tc.cu", "kda_prefill_chain.cu"]
-HEADERS = ["kda_device.cuh", "kda_launch.h", "kda_tc.cuh", "kda_chunk.cuh"]
+HEADERS = ["kda_device.cuh", "kda_launch.h", "kda_tc.cuh", "kda_chunk.cuh", "kda_fp8_codec.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # --fmad=false: no implicit mul+add contraction anywhere, so every fused

@@ -234,10 +234,12 @@ kda_status kda_verify(const kda_params* p, int32_t T, void* stream) {
   return ok();
 }
 
-kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params* r, void* stream) {
-  bool bulk = false;
-  kda_status s = check_params(p, T, &bulk);
-  if (s != KDA_OK) return s;
+}  // extern "C"
+
+namespace {
+
+// The ring's own checks (after the shared ones).
+kda_status check_ring(const kda_params* p, int T, const kda_ring_params* r) {
   if (r == nullptr) return fail(KDA_EINVAL, "ring params is NULL");
   if (r->W < 1 || r->W > 64) return fail(KDA_EUNSUPPORTED, "W = %d outside 1..64", r->W);
   if (T > r->W) return fail(KDA_EINVAL, "T = %d exceeds the ring width W = %d", T, r->W);
@@ -261,6 +263,18 @@ kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params
   if (p->config_override >= 0 && p->config_override != kRingConfig)
     return fail(KDA_EUNSUPPORTED, "config_override = %d: kda_verify_ring runs whole-head tiles only (configuration %d)",
                 p->config_override, kRingConfig);
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_verify_ring(const kda_params* p, int32_t T, const kda_ring_params* r, void* stream) {
+  bool bulk = false;
+  kda_status s = check_params(p, T, &bulk);
+  if (s != KDA_OK) return s;
+  if ((s = check_ring(p, T, r)) != KDA_OK) return s;
   if (p->B == 0) return ok();
   cudaError_t e = kda::launch_ring(*p, T, *r, bulk, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify_ring launch: %s", cudaGetErrorString(e));
@@ -459,6 +473,20 @@ kda_status kda_verify_fp8(const kda_params* p, int32_t T, const kda_fp8_pool* f,
   const int tile_v = cfg == kTensorCoreConfig ? 128 : kTileV[cfg];
   cudaError_t e = kda::launch_verify_fp8(*p, *f, T, tile_v, bulk, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify_fp8 launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+kda_status kda_verify_ring_fp8(const kda_params* p, int32_t T, const kda_ring_params* r, const kda_fp8_pool* f,
+                               void* stream) {
+  bool unused = false;
+  kda_status s = check_fp8(p, T, f, &unused);
+  if (s != KDA_OK) return s;
+  if ((s = check_ring(p, T, r)) != KDA_OK) return s;
+  if (p->N > 0 && (!aligned(p->state, 16) || (p->N > 1 && p->state_slot_stride % 16 != 0)))
+    return fail(KDA_EINVAL, "kda_verify_ring_fp8 needs 16-byte aligned codes and a slot stride that is a multiple of 16");
+  if (p->B == 0) return ok();
+  cudaError_t e = kda::launch_ring_fp8(*p, T, *r, *f, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KDA_ELAUNCH, "kda_verify_ring_fp8 launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

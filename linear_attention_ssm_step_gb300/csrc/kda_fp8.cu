@@ -30,6 +30,7 @@
 
 #include "kda_device.cuh"
 #include "kda_fp8.h"
+#include "kda_fp8_codec.cuh"
 #include "kda_launch.h"
 
 namespace kda {
@@ -45,41 +46,6 @@ __host__ __device__ constexpr size_t fp8_smem_bytes(int TV, int HP) {
          + 64                                   // 4 mbarriers (padded)
          + (size_t)HP * fp8_head_floats(TV) * 4 // per-head token vectors
          + (size_t)3 * KD * 4;                  // single-token reduction products
-}
-
-// Two E4M3 codes (low byte first) -> their exact values as an fp32 pair.
-__device__ __forceinline__ f32x2 e4m3x2_to_f32x2(uint32_t two) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two & 0xffffu)));
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  return pk2(f.x, f.y);
-}
-
-// An fp32 pair -> two E4M3 codes (low byte = low value), round to nearest
-// even, saturating at 448.
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(f32x2 v) {
-  float lo, hi;
-  upk2(v, lo, hi);
-  unsigned short r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// 2^e as an fp32 value, exactly, for -149 <= e <= 127.
-__device__ __forceinline__ float pow2f(int e) {
-  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
-}
-
-// The smallest integer e with m 2^-e <= 448 for m >= 0 (fp32 bits): with
-// m = M 2^E, 1 <= M < 2 and 448 = 1.75 2^8, e = E - 8 when M <= 1.75 (the
-// fraction field at most 0x600000), else E - 7; 0 for m = 0 and -134 below
-// the normal range.
-__device__ __forceinline__ int row_exponent(float m) {
-  const uint32_t bits = __float_as_uint(m);
-  if (bits == 0u) return 0;
-  const int biased = (int)(bits >> 23);
-  if (biased == 0) return -134;
-  return biased - 127 - 8 + ((bits & 0x7fffffu) > 0x600000u ? 1 : 0);
 }
 
 // A lane's 16 consecutive keys 16j..16j+15 of one token's vectors, as 8 pairs.

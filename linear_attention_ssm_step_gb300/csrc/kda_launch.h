@@ -7,6 +7,7 @@
 #include <atomic>
 
 #include "kda.h"
+#include "kda_fp8.h"
 
 namespace kda {
 
@@ -39,6 +40,11 @@ cudaError_t launch_verify_tc(const kda_params& p, int T, bool bulk, cudaStream_t
 // selects tensor-map copies of the checkpoint (16-byte aligned pool) over
 // plain loads and stores.
 cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, bool bulk, cudaStream_t s);
+
+// The same with the checkpoint in an fp8 pool (p.state: E4M3 codes; f8: row
+// scales; plain loads and stores).
+cudaError_t launch_ring_fp8(const kda_params& p, int T, const kda_ring_params& r, const kda_fp8_pool& f8,
+                            cudaStream_t s);
 
 // Bytes of one chunk image of the two-stage prefill (kda_prefill_chain.cu):
 // the operands of one 16-token chunk of one head.

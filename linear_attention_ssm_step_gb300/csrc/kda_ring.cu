@@ -59,6 +59,8 @@
 
 #include "kda_chunk.cuh"
 #include "kda_device.cuh"
+#include "kda_fp8.h"
+#include "kda_fp8_codec.cuh"
 #include "kda_launch.h"
 #include "kda_tc.cuh"
 
@@ -135,11 +137,75 @@ __device__ __forceinline__ int64_t ring_row(int cb, int pos, int W) {
 // i+1's checkpoint and its token loads are issued, and land while item i runs
 // its recurrence and item i+1 starts. Padded token slots (t >= T) carry
 // zero inputs through the same arithmetic, so no loop branches on T.
-template <bool TMA, int TT, bool CIRC>
+// Row tid of a fold on an fp8 checkpoint: s = dec * s_0 + D (s_0 the bf16
+// operand row, dec per key, D in tensor memory), in two passes: the row's
+// largest magnitude, then the codes of s 2^-e (to the pool, 16 per store)
+// and their exact values times 2^e back into the operand row as bf16.
+__device__ __noinline__ void fold_row_fp8(uint32_t row_tmem, unsigned char* sA, const float* sdec, uint8_t* gcodes,
+                                          float* gscale) {
+  const int tid = threadIdx.x;
+  float mx = 0.0f;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int e = row_exponent(mx);
+    const int ea = min(-e, 127);  // 2^-e in two exact factors below the normal range
+    const f32x2 ia = pk2(pow2f(ea), pow2f(ea)), ib = pk2(pow2f(-e - ea), pow2f(-e - ea));
+    const f32x2 se = pk2(pow2f(e), pow2f(e));
+#pragma unroll 1
+    for (int cb = 0; cb < KD / 16; ++cb) {
+      float dsum[16];
+      tmem_ld16(row_tmem + cb * 16, dsum);
+      uint32_t cw[4];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int k = cb * 16 + half * 8;
+        uint4* cell = reinterpret_cast<uint4*>(sA + sw128_offset(KD, tid, k));
+        const uint4 raw = *cell;
+        const float4 d0 = *reinterpret_cast<const float4*>(sdec + k);
+        const float4 d1 = *reinterpret_cast<const float4*>(sdec + k + 4);
+        const float* ds = dsum + half * 8;
+        f32x2 sv[4];
+        sv[0] = fma2(pk2(d0.x, d0.y), bf16x2_to_f32x2(raw.x), pk2(ds[0], ds[1]));
+        sv[1] = fma2(pk2(d0.z, d0.w), bf16x2_to_f32x2(raw.y), pk2(ds[2], ds[3]));
+        sv[2] = fma2(pk2(d1.x, d1.y), bf16x2_to_f32x2(raw.z), pk2(ds[4], ds[5]));
+        sv[3] = fma2(pk2(d1.z, d1.w), bf16x2_to_f32x2(raw.w), pk2(ds[6], ds[7]));
+        if (pass == 0) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float lo, hi;
+            upk2(sv[i], lo, hi);
+            mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+          }
+        } else {
+          uint32_t c[4], bw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            c[i] = f32x2_to_e4m3x2(mul2(mul2(sv[i], ia), ib));
+            bw[i] = f32x2_to_bf16x2(mul2(e4m3x2_to_f32x2(c[i]), se));
+          }
+          cw[2 * half] = c[0] | (c[1] << 16);
+          cw[2 * half + 1] = c[2] | (c[3] << 16);
+          *cell = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+        }
+      }
+      if (pass == 1) reinterpret_cast<uint4*>(gcodes)[cb] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    }
+    if (pass == 1) *gscale = pow2f(e);
+  }
+}
+
+// F8: the checkpoint is an fp8 pool (include/kda_fp8.h; p.state the E4M3
+// codes, f8 the row scales), read with plain loads: each row thread
+// dequantizes its row into the bf16 A operand (exact for every row whose
+// largest magnitude is at least 2^-108), and a fold requantizes each folded
+// row by the pool's rule (the row's largest magnitude in fp32, then the
+// codes), writes codes and scale back, and continues from their exact values.
+template <bool TMA, int TT, bool CIRC, bool F8 = false>
 __global__ void __launch_bounds__(RING_THREADS, 3)
     kda_ring_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p, const kda_ring_params rp,
-                    const int T) {
+                    const int T, const kda_fp8_pool f8) {
   static_assert(TT == 8 || TT == 16, "token slots");
+  static_assert(!(TMA && F8), "the fp8 checkpoint takes plain loads");
   constexpr int NB = 2 * TT;            // dot products per row: TT with P_t k~_t, then TT with P_t q_hat_t
   constexpr int NB2 = 2 * NB;           // B operand rows: NB high halves, then NB low halves
   constexpr int CPE = TT == 8 ? 2 : 1;  // history entries per reduction chunk
@@ -222,6 +288,9 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
     uint16_t* uc = static_cast<uint16_t*>(rp.u_cache) + (int64_t)n * rp.u_slot_stride + (int64_t)h * rp.W * KD;
     float* gc = static_cast<float*>(rp.g_cache) + (int64_t)n * rp.g_slot_stride + (int64_t)h * rp.W * KD;
     uint16_t* gstate = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride + (int64_t)h * KD * KD;
+    // fp8 checkpoint: row tid's 128 codes and its scale
+    uint8_t* gcodes = static_cast<uint8_t*>(p.state) + (int64_t)n * p.state_slot_stride + ((int64_t)h * KD + tid) * KD;
+    float* gscale = F8 ? f8.scale + (int64_t)n * f8.scale_slot_stride + (int64_t)h * KD + tid : nullptr;
 
     bool ok = valid && !broken;
     uint16_t vcur[TT];
@@ -249,7 +318,24 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
 #pragma unroll
       for (int j = 0; j < 16; ++j) uh[j] = j < hist ? uc[ring_row<CIRC>(cb, j, W) + tid] : (uint16_t)0;
 
-      if constexpr (!TMA) {  // plain loads into the same swizzled layout
+      if constexpr (F8) {  // row tid: codes * 2^e, exact, as bf16 into the swizzled layout
+        const float sc = *gscale;
+        const f32x2 sc2 = pk2(sc, sc);
+        const uint4* src = reinterpret_cast<const uint4*>(gcodes);
+#pragma unroll 2
+        for (int c16 = 0; c16 < KD / 16; ++c16) {
+          const uint4 cw = src[c16];
+          const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+          uint32_t bw[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            bw[2 * i] = f32x2_to_bf16x2(mul2(e4m3x2_to_f32x2(w[i]), sc2));
+            bw[2 * i + 1] = f32x2_to_bf16x2(mul2(e4m3x2_to_f32x2(w[i] >> 16), sc2));
+          }
+          *reinterpret_cast<uint4*>(sA + sw128_offset(KD, tid, 16 * c16)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+          *reinterpret_cast<uint4*>(sA + sw128_offset(KD, tid, 16 * c16 + 8)) = make_uint4(bw[4], bw[5], bw[6], bw[7]);
+        }
+      } else if constexpr (!TMA) {  // plain loads into the same swizzled layout
         for (int r = 0; r < KD; ++r)
           *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, tid)) = gstate[(int64_t)r * KD + tid];
       }
@@ -492,30 +578,35 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
           }
         }
         if (f_ok) {
-          // Row tid of the folded state: exp(G_{h-1}) s_0 + D, rounded in place.
+          // Row tid of the folded state: exp(G_{h-1}) s_0 + D, rounded in place
+          // (fp8 checkpoint: requantized; the row's largest magnitude first).
           tc_fence_after();
+          if constexpr (!F8) {
 #pragma unroll 1
-          for (int cb = 0; cb < KD / 16; ++cb) {
-            float dsum[16];
-            tmem_ld16(row_tmem + cb * 16, dsum);
+            for (int cb = 0; cb < KD / 16; ++cb) {
+              float dsum[16];
+              tmem_ld16(row_tmem + cb * 16, dsum);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int k = cb * 16 + half * 8;
-              uint4* cell = reinterpret_cast<uint4*>(sA + sw128_offset(KD, tid, k));
-              uint4 raw = *cell;
-              const float4 d0 = *reinterpret_cast<const float4*>(sdec + k);
-              const float4 d1 = *reinterpret_cast<const float4*>(sdec + k + 4);
-              const float* ds = dsum + half * 8;
-              const f32x2 s0 = fma2(pk2(d0.x, d0.y), bf16x2_to_f32x2(raw.x), pk2(ds[0], ds[1]));
-              const f32x2 s1 = fma2(pk2(d0.z, d0.w), bf16x2_to_f32x2(raw.y), pk2(ds[2], ds[3]));
-              const f32x2 s2 = fma2(pk2(d1.x, d1.y), bf16x2_to_f32x2(raw.z), pk2(ds[4], ds[5]));
-              const f32x2 s3 = fma2(pk2(d1.z, d1.w), bf16x2_to_f32x2(raw.w), pk2(ds[6], ds[7]));
-              raw.x = f32x2_to_bf16x2(s0);
-              raw.y = f32x2_to_bf16x2(s1);
-              raw.z = f32x2_to_bf16x2(s2);
-              raw.w = f32x2_to_bf16x2(s3);
-              *cell = raw;
+              for (int half = 0; half < 2; ++half) {
+                const int k = cb * 16 + half * 8;
+                uint4* cell = reinterpret_cast<uint4*>(sA + sw128_offset(KD, tid, k));
+                uint4 raw = *cell;
+                const float4 d0 = *reinterpret_cast<const float4*>(sdec + k);
+                const float4 d1 = *reinterpret_cast<const float4*>(sdec + k + 4);
+                const float* ds = dsum + half * 8;
+                const f32x2 s0 = fma2(pk2(d0.x, d0.y), bf16x2_to_f32x2(raw.x), pk2(ds[0], ds[1]));
+                const f32x2 s1 = fma2(pk2(d0.z, d0.w), bf16x2_to_f32x2(raw.y), pk2(ds[2], ds[3]));
+                const f32x2 s2 = fma2(pk2(d1.x, d1.y), bf16x2_to_f32x2(raw.z), pk2(ds[4], ds[5]));
+                const f32x2 s3 = fma2(pk2(d1.z, d1.w), bf16x2_to_f32x2(raw.w), pk2(ds[6], ds[7]));
+                raw.x = f32x2_to_bf16x2(s0);
+                raw.y = f32x2_to_bf16x2(s1);
+                raw.z = f32x2_to_bf16x2(s2);
+                raw.w = f32x2_to_bf16x2(s3);
+                *cell = raw;
+              }
             }
+          } else {
+            fold_row_fp8(row_tmem, sA, sdec, gcodes, gscale);
           }
           // The B operand overwrites the fold's operands, which its product has read.
 #pragma unroll
@@ -554,7 +645,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
           }
         }
         pendD = true;
-        if (!TMA && fold) {
+        if (!TMA && !F8 && fold) {  // (an fp8 checkpoint was written by its fold)
           for (int r = 0; r < KD; ++r)
             gstate[(int64_t)r * KD + tid] = *reinterpret_cast<const uint16_t*>(sA + sw128_offset(KD, r, tid));
         }
@@ -702,10 +793,10 @@ __global__ void kda_ring_reset_kernel(const kda_params p, const kda_ring_params 
 
 // ---------------------------------------------------------------- host side
 
-template <bool TMA, int TT, bool CIRC>
+template <bool TMA, int TT, bool CIRC, bool F8 = false>
 static cudaError_t launch_ring_one(const CUtensorMap& map, const kda_params& p, int T, const kda_ring_params& r,
-                                   cudaStream_t s) {
-  auto kern = kda_ring_kernel<TMA, TT, CIRC>;
+                                   cudaStream_t s, const kda_fp8_pool& f8 = kda_fp8_pool{}) {
+  auto kern = kda_ring_kernel<TMA, TT, CIRC, F8>;
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
   cudaError_t e = set_smem_limit_once(kern, ring_smem_bytes(TT, 64, 64), smem_set);
   if (e != cudaSuccess) return e;
@@ -738,7 +829,7 @@ static cudaError_t launch_ring_one(const CUtensorMap& map, const kda_params& p, 
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const long long items = (long long)p.B * p.H;
   const long long grid = std::min(items, (long long)sms * per_sm);
-  kern<<<(unsigned)grid, RING_THREADS, smem, s>>>(map, p, r, T);
+  kern<<<(unsigned)grid, RING_THREADS, smem, s>>>(map, p, r, T, f8);
   e = cudaGetLastError();
   if (e != cudaSuccess || !r.restart_hist_on_flush) return e;
   kda_ring_reset_kernel<<<(unsigned)((p.B + 127) / 128), 128, 0, s>>>(p, r);
@@ -751,6 +842,17 @@ static cudaError_t launch_ring_tma(const CUtensorMap& map, const kda_params& p, 
   if (r.cache_base != nullptr)
     return T <= 8 ? launch_ring_one<TMA, 8, true>(map, p, T, r, s) : launch_ring_one<TMA, 16, true>(map, p, T, r, s);
   return T <= 8 ? launch_ring_one<TMA, 8, false>(map, p, T, r, s) : launch_ring_one<TMA, 16, false>(map, p, T, r, s);
+}
+
+cudaError_t launch_ring_fp8(const kda_params& p, int T, const kda_ring_params& r, const kda_fp8_pool& f8,
+                            cudaStream_t s) {
+  CUtensorMap map;
+  memset(&map, 0, sizeof(map));
+  if (r.cache_base != nullptr)
+    return T <= 8 ? launch_ring_one<false, 8, true, true>(map, p, T, r, s, f8)
+                  : launch_ring_one<false, 16, true, true>(map, p, T, r, s, f8);
+  return T <= 8 ? launch_ring_one<false, 8, false, true>(map, p, T, r, s, f8)
+                : launch_ring_one<false, 16, false, true>(map, p, T, r, s, f8);
 }
 
 cudaError_t launch_ring(const kda_params& p, int T, const kda_ring_params& r, bool bulk, cudaStream_t s) {

@@ -78,6 +78,8 @@ EXPORTS = {
     "kda_decode_fp8": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaFp8Pool), ctypes.c_void_p], ctypes.c_int),
     "kda_verify_fp8": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.POINTER(KdaFp8Pool), ctypes.c_void_p],
                        ctypes.c_int),
+    "kda_verify_ring_fp8": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.POINTER(KdaRingParams),
+                             ctypes.POINTER(KdaFp8Pool), ctypes.c_void_p], ctypes.c_int),
     "kda_verify": ([ctypes.POINTER(KdaParams), ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "kda_prefill": ([ctypes.POINTER(KdaParams), ctypes.POINTER(KdaSeqs), ctypes.c_void_p], ctypes.c_int),
     "kda_select_prefill_config": ([ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
@@ -282,6 +284,26 @@ def kda_verify_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_l
                 lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.uint8)
     f = _fp8_pool(codes, scales)
     _check(load_library().kda_verify_fp8(ctypes.byref(p), T, ctypes.byref(f), _stream_handle(stream, q.device)))
+    return out
+
+
+def kda_verify_ring_fp8(codes, scales, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias,
+                        k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush=True,
+                        out=None, lower_bound=-5.0, scale=1.0, error_word=None, config_override=-1,
+                        gate_mode=KDA_GATE_RAW, stream=None, cache_base=None):
+    """Ring-cache verify with replay and fold on an fp8 checkpoint pool
+    (include/kda_fp8.h): codes and scales as kda_decode_fp8's (a fold
+    requantizes the checkpoint in place), the ring and the rest as
+    kda_verify_ring's."""
+    B, T, H = q.shape[0], q.shape[1], q.shape[2]
+    if out is None:
+        out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=q.device)
+    p = _params(codes, state_indices, q, k, v, g_raw, beta_logit, A_log, dt_bias, out, T,
+                lower_bound, scale, error_word, config_override, gate_mode, state_dtype=torch.uint8)
+    r = _ring_params(codes, H, k_cache, u_cache, g_cache, hist_len, flush_min, restart_hist_on_flush, cache_base)
+    f = _fp8_pool(codes, scales)
+    _check(load_library().kda_verify_ring_fp8(ctypes.byref(p), T, ctypes.byref(r), ctypes.byref(f),
+                                              _stream_handle(stream, q.device)))
     return out
 
 
