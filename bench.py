@@ -25,7 +25,8 @@ carries:
                loops (also on an fp8 pool, with T = 8 verify on the fp8 pool
                at B = 1, 32, 512, and with the pre-computed gate
                convention at B = 8, 512), T=8 verify and T=8 ring verify at
-               B = 1, 32, 512 (0/50/100% of rows folding), L2-cold, and the
+               B = 1, 32, 512 (0/50/100% of rows folding; the ring also on an
+               fp8 checkpoint pool at B = 512), L2-cold, and the
                varlen prefill at 1 x 4096, 8 x 2048, 64 x 256 and 512 x 16
                tokens (H = 12) and two shapes of the prefill page (H = 16,
                1 x 16384; H = 4, lengths 1..15) with a caller's workspace
@@ -478,6 +479,8 @@ def sweep(dev, steps=100, warmup=100):
     res["t8_ring_w32"] = t8_ring_points(dev, [(1, 32), (32, 32), (512, 32)], steps, warmup, flush)
     # the pages' own ring width for T = 8, at the serving batch
     res["t8_ring_w16"] = t8_ring_points(dev, [(512, 16)], steps, warmup, flush)
+    # the ring's checkpoint on an fp8 pool, at the serving batch
+    res["t8_ring_fp8_w32"] = t8_ring_points(dev, [(512, 32)], steps, warmup, flush, fp8=True)
     add_fractions(res)
     return res
 
@@ -499,35 +502,46 @@ def t8_verify_points(dev, Bs, steps, warmup, flush):
     return pts
 
 
-def t8_ring_points(dev, cases, steps, warmup, flush):
-    """T = 8 kda_verify_ring, flush_min = 9, for each (B, W) at 0 / 50 / 100 % of rows
-    folding; the pool, the ring and hist_len restored and L2 emptied before every call."""
+def t8_ring_points(dev, cases, steps, warmup, flush, fp8=False):
+    """T = 8 kda_verify_ring (fp8: kda_verify_ring_fp8 on an fp8 checkpoint pool),
+    flush_min = 9, for each (B, W) at 0 / 50 / 100 % of rows folding; the pool,
+    the ring and hist_len restored and L2 emptied before every call."""
     pts = []
     for B, W in cases:
         for fold in (0.0, 0.5, 1.0):
             w = workloads.ring_inputs(B, B + 64, T=8, W=W, flush_min=9, fold_frac=fold, seed=30 + B)
             wd = w.to(dev)
             saved = {k: v.clone() for k, v in wd.ring.items() if isinstance(v, torch.Tensor)}
-            st0 = wd.state.clone()
+            if fp8:
+                codes, scales = (x.to(dev) for x in workloads.fp8_pool(B + 64, seed=31 + B))
+                pool = [codes, scales]
+                wd.state = None  # the bf16 pool is not used
+            else:
+                pool = [wd.state]
+            pool0 = [x.clone() for x in pool]
             out = torch.empty((B, 8, 12, 128), dtype=torch.bfloat16, device=dev)
             r = wd.ring
 
             def restore():
-                wd.state.copy_(st0)
+                for x, x0 in zip(pool, pool0):
+                    x.copy_(x0)
                 for k, v in saved.items():
                     r[k].copy_(v)
                 flush()
 
-            fn = lambda: kda.kda_verify_ring(wd.state, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw,  # noqa: E731
-                                             wd.beta_logit, wd.A_log, wd.dt_bias, r["k_cache"], r["u_cache"],
-                                             r["g_cache"], r["hist_len"], 9, out=out)
+            ring_args = (wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit, wd.A_log, wd.dt_bias,
+                         r["k_cache"], r["u_cache"], r["g_cache"], r["hist_len"], 9)
+            if fp8:
+                fn = lambda: kda.kda_verify_ring_fp8(codes, scales, *ring_args, out=out)  # noqa: E731
+            else:
+                fn = lambda: kda.kda_verify_ring(pool[0], *ring_args, out=out)  # noqa: E731
             us, p10, p90 = spread(time_calls(graphed(fn), steps, warmup, before=restore))
             idx = w.state_indices.to(torch.int64)
             hists = [int(w.ring["hist_len"][n]) for n in idx]
-            nb = traffic.ring_bytes(hists, 8, 9)
+            nb = traffic.ring_bytes(hists, 8, 9, state_bytes=traffic.FP8_STATE_BYTES if fp8 else traffic.STATE_BYTES)
             pts.append({"B": B, "W": W, "fold": fold, "us": us, "us_p10": p10, "us_p90": p90,
                         "GB/s": round(nb / us / 1e3, 1)})
-            del w, wd, saved, st0
+            del w, wd, saved, pool, pool0
     return pts
 
 

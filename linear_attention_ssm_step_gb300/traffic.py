@@ -17,7 +17,9 @@ activations. The same count is used here, per row:
   per call:                A_log H*4 + dt_bias H*128*4
   T=1 decode on an fp8 pool (kda_fp8.h), active row:
                            codes read + write 2*H*V*K + row scales 2*H*V*4
-                           + the same activations, output and index
+                           + the same activations, output and index; the
+                           T-token verify and the ring verify on an fp8 pool
+                           count their checkpoint as codes + scales likewise
   varlen prefill (kda_prefill.h), an active sequence of n tokens:
                            its slot once each way + n x (activations + outputs)
                            + index + two cu_seqlens entries. The prefill is
@@ -46,14 +48,15 @@ def verify_bytes(n_active, T, n_inactive=0):
             + n_inactive * (INDEX_BYTES + T * H * V * 2) + PER_CALL_BYTES)
 
 
-def ring_row_bytes(h, T, fold):
-    return (STATE_BYTES + (h + T) * RING_ENTRY_BYTES + T * TOKEN_IO_BYTES + INDEX_BYTES + 4
-            + (STATE_BYTES if fold else 0))
+def ring_row_bytes(h, T, fold, state_bytes=STATE_BYTES):
+    return (state_bytes + (h + T) * RING_ENTRY_BYTES + T * TOKEN_IO_BYTES + INDEX_BYTES + 4
+            + (state_bytes if fold else 0))
 
 
-def ring_bytes(hists, T, flush_min, n_inactive=0):
-    """hists: hist_len of each active row before the call."""
-    return (sum(ring_row_bytes(h, T, h >= flush_min) for h in hists)
+def ring_bytes(hists, T, flush_min, n_inactive=0, state_bytes=STATE_BYTES):
+    """hists: hist_len of each active row before the call; state_bytes: one
+    checkpoint, one direction (FP8_STATE_BYTES for an fp8 pool)."""
+    return (sum(ring_row_bytes(h, T, h >= flush_min, state_bytes) for h in hists)
             + n_inactive * (INDEX_BYTES + T * H * V * 2) + PER_CALL_BYTES)
 
 

@@ -159,6 +159,30 @@ def test_fp8_decode_timeout_skips_and_reports(dev, wlib):
     assert torch.equal(s_d.cpu().view(torch.int32), scales.view(torch.int32))
 
 
+def test_fp8_ring_timeout_skips_and_reports(dev, wlib):
+    """The ring on an fp8 checkpoint pool: its bulk copy of the codes is never
+    issued, the first wait gives up, and codes, scales and the ring stay as
+    they were (hist_len reset as in the bf16 ring's case)."""
+    w = workloads.ring_inputs(6, 12, T=8, W=32, flush_min=9, fold_frac=0.5, seed=745)
+    codes, scales = workloads.fp8_pool(12, seed=746)
+    wd = w.to(dev)
+    c_d, s_d = codes.to(dev), scales.to(dev)
+    out, err = _sentinel_out((6, 8, 12, 128), dev), _err(dev)
+    p = kda._params(c_d, wd.state_indices, wd.q, wd.k, wd.v, wd.g_raw, wd.beta_logit, wd.A_log, wd.dt_bias, out,
+                    8, LB, 1.0, err, -1, wd.gate_mode, state_dtype=torch.uint8)
+    r = wd.ring
+    rp = kda._ring_params(c_d, 12, r["k_cache"], r["u_cache"], r["g_cache"], r["hist_len"], r["flush_min"],
+                          True, None)
+    f = kda._fp8_pool(c_d, s_d)
+    assert wlib.kda_verify_ring_fp8(ctypes.byref(p), 8, ctypes.byref(rp), ctypes.byref(f),
+                                    kda._stream_handle(None, dev)) == kda.KDA_OK
+    _expect_timeout(err, out)
+    assert torch.equal(c_d.cpu(), codes)
+    assert torch.equal(s_d.cpu().view(torch.int32), scales.view(torch.int32))
+    for name in ("k_cache", "u_cache", "g_cache"):
+        assert np.array_equal(f64(r[name]), f64(w.ring[name]), equal_nan=True), name
+
+
 def test_context_usable_after_timeouts(dev, wlib):
     """After the calls that gave up, the regular library's decode still runs and
     matches the oracle."""
