@@ -208,12 +208,24 @@ __device__ __forceinline__ float load_bf16(const kda_view& vw, int b, int t, int
 template <int PT>
 struct TokenLoads {
   float q[PT][4], k[PT][4], g[PT][4], v[PT][4], bl[PT];
+  float alog, dtb[4];  // A_log[h] and dt_bias[h][lane + 32 i] (raw gate)
 };
+
+// A_log[h] and the lane's four dt_bias values, issued with the token loads.
+template <int PT>
+__device__ __forceinline__ void gate_issue(const kda_params& p, int h, TokenLoads<PT>& L) {
+  const int lane = threadIdx.x & 31;
+  const bool raw = p.gate_mode == KDA_GATE_RAW;
+  L.alog = raw ? p.A_log[h] : 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) L.dtb[i] = raw ? p.dt_bias[(int64_t)h * KD + lane + 32 * i] : 0.0f;
+}
 
 template <int PT, int NW = NWARPS>
 __device__ __forceinline__ void prologue_issue(const kda_params& p, int b, int h, int T, int v0, int TV,
                                                TokenLoads<PT>& L) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  gate_issue(p, h, L);
 #pragma unroll
   for (int s = 0; s < PT; ++s) {
     const int t = warp + NW * s;
@@ -275,10 +287,8 @@ template <int PT, int NW = NWARPS>
 __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h, int T, int v0, int TV,
                                                const TokenSmem& ts, const TokenLoads<PT>& L) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Gate gate(p, h);
-  float dtb[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) dtb[i] = gate.dt_bias(p, h, lane + 32 * i);
+  const Gate gate(p, L.alog, true);
+  const float* dtb = L.dtb;
 #pragma unroll
   for (int s = 0; s < PT; ++s) {
     const int t = warp + NW * s;

@@ -65,10 +65,8 @@ template <int PT, int NW>
 __device__ __forceinline__ void token_prologue_lm(const kda_params& p, int h, int T, int TV, const TokenSmem& ts,
                                                   const TokenLoads<PT>& L) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Gate gate(p, h);
-  float dtb[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) dtb[i] = gate.dt_bias(p, h, lane + 32 * i);
+  const Gate gate(p, L.alog, true);
+  const float* dtb = L.dtb;
 #pragma unroll
   for (int s = 0; s < PT; ++s) {
     const int t = warp + NW * s;

@@ -7,28 +7,40 @@
 // steps). Per token and value row v, with a = d * s_v:
 //   x = a . k_hat = s_v . (d * k_hat),  y = a . q_hat = s_v . (d * q_hat),
 //   u = beta (v - x),  s_v <- bf16(a + k_hat u),  o_v = scale (y + u kappa).
-// Both dot products of all 128 rows form one [128 x 128] x [128 x 2] product
-// of the bf16 state (exact as stored) with the two vectors d * k_hat and
-// d * q_hat, each split into three bf16 parts (exact to 2^-25 relative):
-// one tcgen05.mma of N = 16 (6 columns used) per K step of 16, fp32 sums in
-// tensor memory. The update and the rounding are the CUDA-core kernel's, per
-// element, so only the order of the dot products' sums differs from it.
+// Both dot products of all 128 rows form one [128 x 128] x [128 x N] product
+// of the bf16 state (exact as stored) with the vectors d * k_hat and
+// d * q_hat, each split into a high and a low bf16 part (exact to 2^-17
+// relative): 8 tcgen05.mma of N = 16 per token, fp32 sums in tensor memory.
+// The update and the rounding are the CUDA-core kernel's, per element; the
+// dot products' sums run in another order and on the two-part vectors.
 //
-// One CTA of 128 threads per (batch row, head). Thread v is key channel v in
-// the per-channel work and reads value row v's sums from tensor memory; in the
-// per-row work each thread owns a tile of 16 value rows x 8 keys of the state
-// (held in registers as bf16 pairs): lane l of warp w takes rows
-// 32 w + 16 (l / 16) .. + 15 and keys 8 (l % 16) .. + 7, so a warp holds
-// whole rows 32 w .. 32 w + 31, the rows whose sums it reads.
-//   1. slot index; the state arrives by two tensor-map loads into the
-//      K-major, 128-byte-swizzled layout of the A operand; the per-token
-//      prologue (the CUDA-core verify's, the same bits) runs meanwhile;
-//   2. per token: each thread writes its channel of the B operand; one thread
-//      issues 8 tcgen05.mma; each thread waits for the product itself, reads
-//      its row's sums and computes u and o for that row; u goes to its warp's
-//      shared-memory slot; each thread updates its tile with the u of its 16
-//      rows and the decay and key of its 8 channels, and writes the tile back
-//      to the A operand (one CTA barrier per token, before the product);
+// One CTA of 128 threads per (batch row, head). Rows are independent across
+// the tokens (row v's update needs only row v's u), so the CTA runs two
+// pipelines, one per half of the rows: warps 0-1 own rows 0-63, warps 2-3
+// rows 64-127, and each half issues its own products, into its own 16
+// tensor-memory columns, when its own rows are written back - the halves
+// never wait for one another, and while one waits for its product the other
+// updates. Each half's product reads all 128 rows (M = 128 is the smallest
+// shape whose sums land in the lanes of the warps that own the rows); the
+// sums of the other half's rows, which that half may be rewriting, are not
+// read. Per thread: key channel tid in the per-channel work; value row tid's
+// sums; and in the per-row work a tile of 16 value rows x 8 keys of the state
+// (registers, bf16 pairs): lane l of warp w takes rows 32 w + 16 (l / 16) ..
+// + 15 and keys 8 (l % 16) .. + 7, so a warp holds whole rows 32 w .. + 31.
+//   1. the token inputs (q, k, g_raw and v rows, 256 bytes each) arrive by
+//      bulk copies into the B region, issued before the slot index is known
+//      (plain loads where a view is not 16-byte aligned); the state by two
+//      tensor-map loads into the K-major, 128-byte-swizzled layout of the A
+//      operand; the per-token prologue (the CUDA-core verify's, the same
+//      bits) runs meanwhile, and then every token's B operand is written at
+//      once: token t's four rows
+//      (high parts of d k_hat and d q_hat, then the low parts) at rows
+//      4 (t % 4) .. + 3 of 16-row slice t / 4;
+//   2. per half and token: a named barrier over the half's 64 threads (its
+//      rows are back in the A operand); one warp issues 8 tcgen05.mma on the
+//      slice of the token; every thread of the half waits for the product,
+//      reads its row's sums and computes u and o; u goes to its warp's
+//      shared-memory slot; each thread updates its tile and writes it back;
 //   3. the final rows leave by two tensor-map stores.
 #include <cuda.h>
 
@@ -42,24 +54,24 @@
 namespace kda {
 
 constexpr int VT_THREADS = 128;
-constexpr uint32_t VT_TMEM_COLS = 32;
+constexpr uint32_t VT_TMEM_COLS = 32;  // 16 per half
+constexpr uint32_t VT_SLICE_BYTES = 16u * 256u;  // one B slice: 16 rows x 128 keys bf16
 
 // Shared-memory carve-up (bytes from a 1024-aligned base) for TT token slots.
 struct VerifyLayout {
-  uint32_t a, b, kh, qh, dd, vrow, beta, kappa, su, bar, tslot, total;
+  uint32_t a, b, kh, dd, vrow, beta, kappa, su, bar, tslot, total;
 };
 
 __host__ __device__ inline VerifyLayout verify_layout(int TT) {
   VerifyLayout L{};
   const uint32_t tok = (uint32_t)TT * KD * 4u;
+  const uint32_t bsz = (uint32_t)((TT + 3) / 4) * VT_SLICE_BYTES;
   uint32_t o = 0;
   L.a = o;
   o += 128u * 256u;  // state, 128 rows x 128 keys bf16
-  L.b = o;           // B operand, 16 rows x 128 keys bf16; the prologue's g before it
-  o += tok > 4096u ? tok : 4096u;
+  L.b = o;           // B slices; before them the prologue's g and q_hat (tok bytes each)
+  o += bsz > 2u * tok ? bsz : 2u * tok;
   L.kh = o;
-  o += tok;
-  L.qh = o;
   o += tok;
   L.dd = o;
   o += tok;
@@ -71,8 +83,8 @@ __host__ __device__ inline VerifyLayout verify_layout(int TT) {
   o += KDA_MAX_T * 4u;
   L.su = o;  // per-warp slots of the rows' u
   o += 128u * 4u;
-  L.bar = o;
-  o += 16u;
+  L.bar = o;  // the state copy's mbarrier, one per half, the token inputs'
+  o += 32u;
   L.tslot = o;
   o += 16u;
   L.total = o;
@@ -81,24 +93,43 @@ __host__ __device__ inline VerifyLayout verify_layout(int TT) {
 
 __host__ __device__ inline size_t verify_tc_smem_bytes(int TT) { return (size_t)verify_layout(TT).total + 1024; }
 
-// x as three bf16 parts at rows r, r + 2, r + 4 of the B operand, column c.
-__device__ __forceinline__ void store_split3_b(unsigned char* sb, int r, int c, float x) {
+// x as two bf16 parts at rows r and r + 2 of a B slice, column c.
+__device__ __forceinline__ void store_split2_b(unsigned char* sb, int r, int c, float x) {
   const uint16_t x0 = float_to_bf16_bits(x);
-  const float r1 = __fsub_rn(x, bf16_bits_to_float(x0));
-  const uint16_t x1 = float_to_bf16_bits(r1);
-  const uint16_t x2 = float_to_bf16_bits(__fsub_rn(r1, bf16_bits_to_float(x1)));
+  const uint16_t x1 = float_to_bf16_bits(__fsub_rn(x, bf16_bits_to_float(x0)));
   *reinterpret_cast<uint16_t*>(sb + sw128_offset(16, r, c)) = x0;
   *reinterpret_cast<uint16_t*>(sb + sw128_offset(16, r + 2, c)) = x1;
-  *reinterpret_cast<uint16_t*>(sb + sw128_offset(16, r + 4, c)) = x2;
 }
 
-template <bool TMA, int TT>
+// An AND over the `count` threads of named barrier `id`, which it also syncs.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "barrier.red.and.pred q, %2, %3, p;\n\t"
+      "selp.b32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// Row (b, t, h) of a token view: 128 bf16 values.
+__device__ __forceinline__ const uint16_t* token_row(const kda_view& vw, int b, int t, int h) {
+  return static_cast<const uint16_t*>(vw.ptr) + ((int64_t)b * vw.b_stride + (int64_t)t * vw.t_stride +
+                                                 (int64_t)h * vw.h_stride);
+}
+
+// TOK: the token inputs arrive by bulk copies (every view 16-byte aligned).
+template <bool TMA, int TT, bool TOK>
 __global__ void __launch_bounds__(VT_THREADS, 4)
     kda_verify_tc_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p, const int T) {
   static_assert(TT == 8 || TT == 16, "token slots");
   constexpr int NW = VT_THREADS / 32;
   constexpr int PT = TT / NW;  // prologue tokens per warp
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int half = warp >> 1;
   const int h = blockIdx.x % p.H;
   const int b = blockIdx.x / p.H;
 
@@ -109,31 +140,60 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   unsigned char* sB = sm + SL.b;
   TokenSmem ts;
   ts.kh = reinterpret_cast<float*>(sm + SL.kh);
-  ts.qh = reinterpret_cast<float*>(sm + SL.qh);
+  ts.qh = reinterpret_cast<float*>(sB + TT * KD * 4);  // q_hat and g are not needed after the B slices
   ts.dd = reinterpret_cast<float*>(sm + SL.dd);
-  ts.gg = reinterpret_cast<float*>(sB);  // g is not needed after the prologue
+  ts.gg = reinterpret_cast<float*>(sB);
   ts.vrow = reinterpret_cast<float*>(sm + SL.vrow);
   ts.beta = reinterpret_cast<float*>(sm + SL.beta);
   ts.kappa = reinterpret_cast<float*>(sm + SL.kappa);
   ts.red = nullptr;
   uint64_t* barA = reinterpret_cast<uint64_t*>(sm + SL.bar);
-  uint64_t* barD = barA + 1;
+  uint64_t* barH = barA + 1 + half;  // this half's products
+  uint64_t* barT = barA + 3;         // the token inputs' bulk copies
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL.tslot);
 
   uint16_t* outp = static_cast<uint16_t*>(p.out);
   const int64_t obase = (int64_t)b * p.out_b_stride + (int64_t)h * p.out_h_stride + tid;
 
+  // Token inputs: row t of q, k, g_raw, v at byte (4 t + j) 256 of the B
+  // region (bulk copies), or plain loads into registers.
+  const uint16_t* stage = reinterpret_cast<const uint16_t*>(sB);
+  TokenLoads<PT> first;
+  if constexpr (TOK) {
+    if (tid == 0) {
+      mbar_init(barT, 1);
+      mbar_expect_tx(barT, (uint32_t)T * 4u * 256u);
+      for (int t = 0; t < T; ++t) {
+        bulk_g2s(sB + (4 * t + 0) * 256, token_row(p.q, b, t, h), 256, barT);
+        bulk_g2s(sB + (4 * t + 1) * 256, token_row(p.k, b, t, h), 256, barT);
+        bulk_g2s(sB + (4 * t + 2) * 256, token_row(p.g_raw, b, t, h), 256, barT);
+        bulk_g2s(sB + (4 * t + 3) * 256, token_row(p.v, b, t, h), 256, barT);
+      }
+    }
+    gate_issue(p, h, first);
+#pragma unroll
+    for (int s2 = 0; s2 < PT; ++s2) {  // beta's logits: one value per token
+      const int t = warp + NW * s2;
+      first.bl[s2] = (t < T && lane == 0)
+                         ? bf16_bits_to_float(static_cast<const uint16_t*>(p.beta_logit.ptr)[
+                               (int64_t)b * p.beta_logit.b_stride + (int64_t)t * p.beta_logit.t_stride +
+                               (int64_t)h * p.beta_logit.h_stride])
+                         : 0.0f;
+    }
+  } else {
+    prologue_issue<PT, NW>(p, b, h, T, 0, KD, first);  // issued alongside the index load
+  }
   const int n = p.state_indices[b];
-  TokenLoads<PT> first;  // issued alongside the index load
-  prologue_issue<PT, NW>(p, b, h, T, 0, KD, first);
   if (n < 0 || n >= p.N) {
     for (int t = 0; t < T; ++t) outp[obase + (int64_t)t * p.out_t_stride] = 0;
+    if (TOK && tid == 0) mbar_drain_bounded(barT, 0);  // the copies land before the CTA leaves
     return;
   }
   uint16_t* gstate = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride + (int64_t)h * KD * KD;
   if (tid == 0) {
     mbar_init(barA, 1);
-    mbar_init(barD, 1);
+    mbar_init(barA + 1, 1);
+    mbar_init(barA + 2, 1);
     if constexpr (TMA) {
       mbar_expect_tx(barA, KD * KD * 2);
       tma_load_3d(sA, &smap, 0, h * KD, n, barA);
@@ -145,23 +205,59 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
       *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, tid)) = gstate[(int64_t)r * KD + tid];
   }
   if (warp == 0) tmem_alloc(tslot, VT_TMEM_COLS);
+  bool tok_ok = true;
+  if constexpr (TOK) {  // this warp's tokens into registers, as the plain loads give them
+    __syncthreads();      // the mbarrier's initialisation
+    tok_ok = mbar_wait_bounded(barT, 0);
+#pragma unroll
+    for (int s2 = 0; s2 < PT; ++s2) {
+      const int t = warp + NW * s2;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = lane + 32 * i;
+        const bool in = t < T && tok_ok;
+        first.q[s2][i] = in ? bf16_bits_to_float(stage[(4 * t + 0) * KD + c]) : 0.0f;
+        first.k[s2][i] = in ? bf16_bits_to_float(stage[(4 * t + 1) * KD + c]) : 0.0f;
+        first.g[s2][i] = in ? bf16_bits_to_float(stage[(4 * t + 2) * KD + c]) : 0.0f;
+        first.v[s2][i] = in ? bf16_bits_to_float(stage[(4 * t + 3) * KD + c]) : 0.0f;
+      }
+    }
+    __syncthreads();  // the prologue writes over the staged inputs
+  }
   tc_fence_before();
   token_prologue<PT, NW>(p, b, h, T, 0, KD, ts, first);  // ends with a CTA barrier
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t row_tmem = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t dcol = tmem + 16u * (uint32_t)half;                          // this half's sums
+  const uint32_t row_tmem = tmem + ((uint32_t)(warp * 32) << 16) + 16u * (uint32_t)half;  // row tid's
 
-  // B rows 6..15 stay zero (the prologue's g occupied them).
+  // Every token's B rows of channel tid (zero past T), through registers: the
+  // slices overwrite g and q_hat.
+  {
+    float xk[TT], xq[TT];
 #pragma unroll
-  for (int r = 6; r < 16; ++r) *reinterpret_cast<uint16_t*>(sB + sw128_offset(16, r, tid)) = 0;
+    for (int t = 0; t < TT; ++t) {
+      const float d = t < T ? ts.dd[t * KD + tid] : 0.0f;
+      xk[t] = t < T ? __fmul_rn(d, ts.kh[t * KD + tid]) : 0.0f;
+      xq[t] = t < T ? __fmul_rn(d, ts.qh[t * KD + tid]) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      unsigned char* slice = sB + (t >> 2) * VT_SLICE_BYTES;
+      store_split2_b(slice, 4 * (t & 3), tid, xk[t]);
+      store_split2_b(slice, 4 * (t & 3) + 1, tid, xq[t]);
+    }
+  }
+  fence_proxy_async_smem();  // the B slices are read by the tensor core
 
-  bool ok = true;
-  if constexpr (TMA) ok = mbar_wait_bounded(barA, 0);
-  ok = __syncthreads_and(ok) != 0;
+  bool ok = tok_ok;
+  if constexpr (TMA) ok = mbar_wait_bounded(barA, 0) && ok;
+  ok = __syncthreads_and(ok) != 0;  // also publishes the B slices
   if (!ok && tid == 0 && p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
 
   // This thread's tile: rows r0 .. r0 + 15, keys 8 kg .. 8 kg + 7 (4 bf16 pairs per row).
-  const int lane = tid & 31, kg = lane & 15;
+  const int kg = lane & 15;
   const int r0 = warp * 32 + (lane >> 4) * 16;
   uint32_t rw[16][4];
 #pragma unroll
@@ -174,43 +270,39 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   }
   float* su = reinterpret_cast<float*>(sm + SL.su) + warp * 32;  // u of rows 32 warp .. + 31
 
-  bool pendD = false;  // a product is in flight, issued with parity pend_par
+  bool pendD = false;  // a product of this half is in flight, issued with parity pend_par
   uint32_t pend_par = 0;
   for (int t = 0; t < T; ++t) {
-    if (ok) {
-      // B operand of token t: rows 0, 2, 4 = d * k_hat, rows 1, 3, 5 = d * q_hat.
-      const float d = ts.dd[t * KD + tid];
-      store_split3_b(sB, 0, tid, __fmul_rn(d, ts.kh[t * KD + tid]));
-      store_split3_b(sB, 1, tid, __fmul_rn(d, ts.qh[t * KD + tid]));
-      fence_proxy_async_smem();  // B and the tiles written back are read by the tensor core
-    }
+    // The half's rows of token t are in the A operand (written and fenced by
+    // both of its warps), and its last product's sums have been read.
     tc_fence_before();
-    ok = __syncthreads_and(ok) != 0;
+    ok = bar_and(1 + half, 64, ok);
     float o = 0.0f;
     if (ok) {
-      if (tid == 0) {
+      if (warp == 2 * half) {
         tc_fence_after();
         constexpr uint32_t idesc = idesc_bf16_f32(128, 16);
-        const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB);
+        const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB) + (uint32_t)(t >> 2) * VT_SLICE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_bf16(tmem, sw128_desc(a0 + (kk >> 2) * (KD * 128) + (kk & 3) * 32),
-                      sw128_desc(b0 + (kk >> 2) * (16 * 128) + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
-        tc_commit(barD);
+          tc_mma_bf16_w(dcol, sw128_desc(a0 + (kk >> 2) * (KD * 128) + (kk & 3) * 32),
+                        sw128_desc(b0 + (kk >> 2) * (16 * 128) + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
+        tc_commit_w(barH);
       }
       pendD = true;
       pend_par = (uint32_t)(t & 1);
-      ok = mbar_wait_bounded(barD, pend_par);  // every thread waits for the product itself
+      ok = mbar_wait_bounded(barH, pend_par);  // every thread of the half waits for the product itself
       if (!ok) {
         if (p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
       } else {
         pendD = false;
         tc_fence_after();
-        // Row tid's sums: x and y in three parts each, then u and o of the row.
+        // Row tid's sums for token t: columns 4 (t % 4) .. + 3 (x high, y high, x low, y low).
         float c[8];
-        tmem_ld8(row_tmem, c);
-        const float x = __fadd_rn(__fadd_rn(c[0], c[2]), c[4]);
-        const float y = __fadd_rn(__fadd_rn(c[1], c[3]), c[5]);
+        tmem_ld8(row_tmem + 8u * (uint32_t)((t >> 1) & 1), c);
+        const bool odd = (t & 1) != 0;
+        const float x = __fadd_rn(odd ? c[4] : c[0], odd ? c[6] : c[2]);
+        const float y = __fadd_rn(odd ? c[5] : c[1], odd ? c[7] : c[3]);
         const float u = __fmul_rn(ts.beta[t], __fsub_rn(ts.vrow[t * KD + tid], x));
         o = __fmul_rn(p.scale, __fmaf_rn(u, ts.kappa[t], y));
         su[lane] = u;
@@ -252,6 +344,7 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
               make_uint4(rw[i][0], rw[i][1], rw[i][2], rw[i][3]);
         }
       }
+      fence_proxy_async_smem();  // the tile written back is read by the tensor core
     }
     outp[obase + (int64_t)t * p.out_t_stride] = ok ? float_to_bf16_bits(o) : (uint16_t)0;
   }
@@ -275,8 +368,8 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
     }
   }
   // A product that did not finish in time gets one more bounded wait before
-  // its tensor memory is released.
-  if (pendD && tid == 0) mbar_wait_bounded(barD, pend_par);
+  // its tensor memory is released (one thread per half).
+  if (pendD && (tid & 63) == 0) mbar_wait_bounded(barH, pend_par);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -285,9 +378,9 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   }
 }
 
-template <bool TMA, int TT>
+template <bool TMA, int TT, bool TOK>
 static cudaError_t launch_vtc(const CUtensorMap& map, const kda_params& p, int T, cudaStream_t s) {
-  auto kern = kda_verify_tc_kernel<TMA, TT>;
+  auto kern = kda_verify_tc_kernel<TMA, TT, TOK>;
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
   cudaError_t e = set_smem_limit_once(kern, verify_tc_smem_bytes(TT), smem_set);
   if (e != cudaSuccess) return e;
@@ -302,15 +395,23 @@ static cudaError_t launch_vtc(const CUtensorMap& map, const kda_params& p, int T
   return cudaGetLastError();
 }
 
+// Every row (b, t, h) of the view starts on a 16-byte boundary.
+static bool rows_aligned16(const kda_view& vw) {
+  return reinterpret_cast<uintptr_t>(vw.ptr) % 16 == 0 && vw.b_stride % 8 == 0 && vw.t_stride % 8 == 0 &&
+         vw.h_stride % 8 == 0;
+}
+
 cudaError_t launch_verify_tc(const kda_params& p, int T, bool bulk, cudaStream_t s) {
   CUtensorMap map;
   memset(&map, 0, sizeof(map));
   if (bulk) {
     const cudaError_t e = state_tensor_map(p, &map);
     if (e != cudaSuccess) return e;
-    return T <= 8 ? launch_vtc<true, 8>(map, p, T, s) : launch_vtc<true, 16>(map, p, T, s);
+    if (rows_aligned16(p.q) && rows_aligned16(p.k) && rows_aligned16(p.g_raw) && rows_aligned16(p.v))
+      return T <= 8 ? launch_vtc<true, 8, true>(map, p, T, s) : launch_vtc<true, 16, true>(map, p, T, s);
+    return T <= 8 ? launch_vtc<true, 8, false>(map, p, T, s) : launch_vtc<true, 16, false>(map, p, T, s);
   }
-  return T <= 8 ? launch_vtc<false, 8>(map, p, T, s) : launch_vtc<false, 16>(map, p, T, s);
+  return T <= 8 ? launch_vtc<false, 8, false>(map, p, T, s) : launch_vtc<false, 16, false>(map, p, T, s);
 }
 
 }  // namespace kda
