@@ -4,6 +4,7 @@ profilers (Nsight Compute) that need a short, clean stream of launches.
   python -m linear_attention_ssm_step_gb300.profile_case decode 512
   python -m linear_attention_ssm_step_gb300.profile_case verify 512 --T 8
   python -m linear_attention_ssm_step_gb300.profile_case ring 512 --T 8 --fold 0.5
+  python -m linear_attention_ssm_step_gb300.profile_case ring_fp8 512 --T 8 --fold 0.5
   python -m linear_attention_ssm_step_gb300.profile_case decode_fp8 512
   python -m linear_attention_ssm_step_gb300.profile_case prefill 8 --len 2048
 
@@ -22,7 +23,7 @@ from . import kda, workloads
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("call", choices=["decode", "verify", "ring", "decode_fp8", "prefill"])
+    ap.add_argument("call", choices=["decode", "verify", "ring", "ring_fp8", "decode_fp8", "prefill"])
     ap.add_argument("B", type=int)
     ap.add_argument("--T", type=int, default=8)
     ap.add_argument("--fold", type=float, default=0.0)
@@ -51,12 +52,22 @@ def main():
         w = workloads.decode_inputs(a.B, a.B + 64, seed=3, T=a.T).to(dev)
         fn = lambda: kda.kda_verify(w.state, w.state_indices, w.q, w.k, w.v, w.g_raw, w.beta_logit,  # noqa: E731
                                     w.A_log, w.dt_bias, config_override=a.config)
-    else:
+    elif a.call == "ring":
         w = workloads.ring_inputs(a.B, a.B + 64, T=a.T, W=32, flush_min=9, fold_frac=a.fold, seed=4).to(dev)
         r = w.ring
         fn = lambda: kda.kda_verify_ring(w.state, w.state_indices, w.q, w.k, w.v, w.g_raw,  # noqa: E731
                                          w.beta_logit, w.A_log, w.dt_bias, r["k_cache"], r["u_cache"],
                                          r["g_cache"], r["hist_len"], r["flush_min"], config_override=a.config)
+    else:  # ring_fp8: the ring on an fp8 checkpoint pool
+        w = workloads.ring_inputs(a.B, a.B + 64, T=a.T, W=32, flush_min=9, fold_frac=a.fold, seed=4)
+        codes, scales = (t.to(dev) for t in workloads.fp8_pool(a.B + 64, seed=5))
+        w.state = None  # the bf16 pool is not used
+        w = w.to(dev)
+        r = w.ring
+        fn = lambda: kda.kda_verify_ring_fp8(codes, scales, w.state_indices, w.q, w.k, w.v, w.g_raw,  # noqa: E731
+                                             w.beta_logit, w.A_log, w.dt_bias, r["k_cache"], r["u_cache"],
+                                             r["g_cache"], r["hist_len"], r["flush_min"],
+                                             config_override=a.config)
     for _ in range(a.reps):
         fn()
         torch.cuda.synchronize()
