@@ -139,11 +139,14 @@ __device__ __forceinline__ int64_t ring_row(int cb, int pos, int W) {
 // zero inputs through the same arithmetic, so no loop branches on T.
 // Row tid of a fold on an fp8 checkpoint: s = dec * s_0 + D (s_0 the bf16
 // operand row, dec per key, D in tensor memory), in two passes: the row's
-// largest magnitude, then the codes of s 2^-e (to the pool, 16 per store)
-// and their exact values times 2^e back into the operand row as bf16.
-__device__ __forceinline__ void fold_row_fp8(uint32_t row_tmem, unsigned char* sA, const float* sdec, uint8_t* gcodes,
-                                          float* gscale) {
-  const int tid = threadIdx.x;
+// largest magnitude, then the codes of s 2^-e and their exact values times 2^e
+// back into the operand row as bf16. The codes go through the warp's
+// transpose tile (row lane at 144 bytes apart), so that the warp writes its
+// 32 rows to the pool as whole 128-byte lines (wcodes: the warp's first row).
+__device__ __forceinline__ void fold_row_fp8(uint32_t row_tmem, unsigned char* sA, const float* sdec,
+                                             uint8_t* wcodes, float* gscale, float* xtile) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  unsigned char* xrow = reinterpret_cast<unsigned char*>(xtile) + lane * (XPOSE_LD * 4);
   float mx = 0.0f;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
@@ -188,10 +191,19 @@ __device__ __forceinline__ void fold_row_fp8(uint32_t row_tmem, unsigned char* s
           *cell = make_uint4(bw[0], bw[1], bw[2], bw[3]);
         }
       }
-      if (pass == 1) reinterpret_cast<uint4*>(gcodes)[cb] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      if (pass == 1) *reinterpret_cast<uint4*>(xrow + 16 * cb) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
     }
     if (pass == 1) *gscale = pow2f(e);
   }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {  // rows 4 i .. 4 i + 3 of the warp, lane = 8 (row - 4 i) + 16-byte unit
+    const int row = 4 * i + (lane >> 3), unit = lane & 7;
+    const uint4 v =
+        *reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(xtile) + row * (XPOSE_LD * 4) + 16 * unit);
+    *reinterpret_cast<uint4*>(wcodes + row * KD + 16 * unit) = v;
+  }
+  __syncwarp();
 }
 
 // Row `row` of an fp8 checkpoint into the bf16 A operand: codes x sc, exact.
@@ -335,8 +347,9 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
     uint16_t* uc = static_cast<uint16_t*>(rp.u_cache) + (int64_t)n * rp.u_slot_stride + (int64_t)h * rp.W * KD;
     float* gc = static_cast<float*>(rp.g_cache) + (int64_t)n * rp.g_slot_stride + (int64_t)h * rp.W * KD;
     uint16_t* gstate = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride + (int64_t)h * KD * KD;
-    // fp8 checkpoint: row tid's 128 codes and its scale
-    uint8_t* gcodes = static_cast<uint8_t*>(p.state) + (int64_t)n * p.state_slot_stride + ((int64_t)h * KD + tid) * KD;
+    // fp8 checkpoint: the warp's rows of codes and row tid's scale
+    uint8_t* wcodes =
+        static_cast<uint8_t*>(p.state) + (int64_t)n * p.state_slot_stride + ((int64_t)h * KD + 32 * warp) * KD;
     float* gscale = F8 ? f8.scale + (int64_t)n * f8.scale_slot_stride + (int64_t)h * KD + tid : nullptr;
     const float sc = sc_next;  // fp8: row tid's scale
 
@@ -643,7 +656,7 @@ __global__ void __launch_bounds__(RING_THREADS, 3)
               }
             }
           } else {
-            fold_row_fp8(row_tmem, sA, sdec, gcodes, gscale);
+            fold_row_fp8(row_tmem, sA, sdec, wcodes, gscale, xtile);
           }
           // The B operand overwrites the fold's operands, which its product has read.
 #pragma unroll

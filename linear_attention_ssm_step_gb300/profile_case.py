@@ -11,7 +11,9 @@ profilers (Nsight Compute) that need a short, clean stream of launches.
 For prefill, B is the number of sequences, each of --len tokens.
 
 Each call is launched --reps times (default 3) on the same inputs, with a
-device synchronize after each; nothing is timed here.
+device synchronize after each; nothing is timed here. For the ring, hist_len
+is restored before every launch (a fold resets it), so that every launch
+folds the same rows.
 """
 
 import argparse
@@ -68,7 +70,10 @@ def main():
                                              w.beta_logit, w.A_log, w.dt_bias, r["k_cache"], r["u_cache"],
                                              r["g_cache"], r["hist_len"], r["flush_min"],
                                              config_override=a.config)
+    hist0 = w.ring["hist_len"].clone() if a.call in ("ring", "ring_fp8") else None
     for _ in range(a.reps):
+        if hist0 is not None:
+            w.ring["hist_len"].copy_(hist0)
         fn()
         torch.cuda.synchronize()
     print(f"{a.call} B={a.B} ran {a.reps} times")
