@@ -289,32 +289,39 @@ __device__ __forceinline__ void token_prologue(const kda_params& p, int b, int h
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Gate gate(p, L.alog, true);
   const float* dtb = L.dtb;
+  // The sums of all of the warp's tokens first, then their per-channel work,
+  // so that the tokens' dependent chains overlap. Slots past T hold zero
+  // inputs and store nothing.
+  float rq[PT], rk[PT], sqk[PT];
+#pragma unroll
+  for (int s = 0; s < PT; ++s) {
+    float qq[4], kk[4], qk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      qq[i] = __fmul_rn(L.q[s][i], L.q[s][i]);
+      kk[i] = __fmul_rn(L.k[s][i], L.k[s][i]);
+      qk[i] = __fmul_rn(L.q[s][i], L.k[s][i]);
+    }
+    rq[s] = inv_norm(sum_channels(qq[0], qq[1], qq[2], qq[3]));
+    rk[s] = inv_norm(sum_channels(kk[0], kk[1], kk[2], kk[3]));
+    sqk[s] = sum_channels(qk[0], qk[1], qk[2], qk[3]);
+  }
 #pragma unroll
   for (int s = 0; s < PT; ++s) {
     const int t = warp + NW * s;
     if (t < T) {
-      float qq[4], kk[4], qk[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        qq[i] = __fmul_rn(L.q[s][i], L.q[s][i]);
-        kk[i] = __fmul_rn(L.k[s][i], L.k[s][i]);
-        qk[i] = __fmul_rn(L.q[s][i], L.k[s][i]);
-      }
-      const float rq = inv_norm(sum_channels(qq[0], qq[1], qq[2], qq[3]));
-      const float rk = inv_norm(sum_channels(kk[0], kk[1], kk[2], kk[3]));
-      const float sqk = sum_channels(qk[0], qk[1], qk[2], qk[3]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int c = lane + 32 * i;
         const float g = gate.g(L.g[s][i], dtb[i]);
         ts.gg[t * KD + c] = g;
         ts.dd[t * KD + c] = expf(g);
-        ts.qh[t * KD + c] = __fmul_rn(L.q[s][i], rq);
-        ts.kh[t * KD + c] = __fmul_rn(L.k[s][i], rk);
+        ts.qh[t * KD + c] = __fmul_rn(L.q[s][i], rq[s]);
+        ts.kh[t * KD + c] = __fmul_rn(L.k[s][i], rk[s]);
         if (c < TV) ts.vrow[t * TV + c] = L.v[s][i];
       }
       if (lane == 0) {
-        ts.kappa[t] = __fmul_rn(__fmul_rn(sqk, rq), rk);
+        ts.kappa[t] = __fmul_rn(__fmul_rn(sqk[s], rq[s]), rk[s]);
         ts.beta[t] = gate.beta(L.bl[s]);
       }
     }
