@@ -160,14 +160,16 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   const uint16_t* stage = reinterpret_cast<const uint16_t*>(sB);
   TokenLoads<PT> first;
   if constexpr (TOK) {
-    if (tid == 0) {
-      mbar_init(barT, 1);
-      mbar_expect_tx(barT, (uint32_t)T * 4u * 256u);
-      for (int t = 0; t < T; ++t) {
-        bulk_g2s(sB + (4 * t + 0) * 256, token_row(p.q, b, t, h), 256, barT);
-        bulk_g2s(sB + (4 * t + 1) * 256, token_row(p.k, b, t, h), 256, barT);
-        bulk_g2s(sB + (4 * t + 2) * 256, token_row(p.g_raw, b, t, h), 256, barT);
-        bulk_g2s(sB + (4 * t + 3) * 256, token_row(p.v, b, t, h), 256, barT);
+    if (warp == 1) {  // one copy per lane (lane = 4 t + j), so that warp 0 starts the state copy at once
+      if (lane == 0) {
+        mbar_init(barT, 1);
+        mbar_expect_tx(barT, (uint32_t)T * 4u * 256u);
+      }
+      __syncwarp();
+      for (int r = lane; r < 4 * T; r += 32) {
+        const int t = r >> 2, j = r & 3;
+        const kda_view& vw = j == 0 ? p.q : j == 1 ? p.k : j == 2 ? p.g_raw : p.v;
+        bulk_g2s(sB + r * 256, token_row(vw, b, t, h), 256, barT);
       }
     }
     gate_issue(p, h, first);
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   const int n = p.state_indices[b];
   if (n < 0 || n >= p.N) {
     for (int t = 0; t < T; ++t) outp[obase + (int64_t)t * p.out_t_stride] = 0;
-    if (TOK && tid == 0) mbar_drain_bounded(barT, 0);  // the copies land before the CTA leaves
+    if (TOK && tid == 32) mbar_drain_bounded(barT, 0);  // the copies land before the CTA leaves
     return;
   }
   uint16_t* gstate = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride + (int64_t)h * KD * KD;
