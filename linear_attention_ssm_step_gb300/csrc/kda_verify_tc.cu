@@ -14,33 +14,26 @@
 // The update and the rounding are the CUDA-core kernel's, per element; the
 // dot products' sums run in another order and on the two-part vectors.
 //
-// One CTA of 128 threads per (batch row, head). Rows are independent across
-// the tokens (row v's update needs only row v's u), so the CTA runs two
-// pipelines, one per half of the rows: warps 0-1 own rows 0-63, warps 2-3
-// rows 64-127, and each half issues its own products, into its own 16
-// tensor-memory columns, when its own rows are written back - the halves
-// never wait for one another, and while one waits for its product the other
-// updates. Each half's product reads all 128 rows (M = 128 is the smallest
-// shape whose sums land in the lanes of the warps that own the rows); the
-// sums of the other half's rows, which that half may be rewriting, are not
-// read. Per thread: key channel tid in the per-channel work; value row tid's
-// sums; and in the per-row work a tile of 16 value rows x 8 keys of the state
-// (registers, bf16 pairs): lane l of warp w takes rows 32 w + 16 (l / 16) ..
-// + 15 and keys 8 (l % 16) .. + 7, so a warp holds whole rows 32 w .. + 31.
+// One CTA of 128 threads per (batch row, head). Per thread: key channel tid in
+// the per-channel work; value row tid's sums; and in the per-row work a tile
+// of 16 value rows x 8 keys of the state (registers, bf16 pairs): lane l of
+// warp w takes rows 32 w + 16 (l / 16) .. + 15 and keys 8 (l % 16) .. + 7, so
+// a warp holds whole rows 32 w .. + 31, the rows whose sums it reads.
 //   1. the token inputs (q, k, g_raw and v rows, 256 bytes each) arrive by
 //      bulk copies into the B region, issued before the slot index is known
 //      (plain loads where a view is not 16-byte aligned); the state by two
 //      tensor-map loads into the K-major, 128-byte-swizzled layout of the A
 //      operand; the per-token prologue (the CUDA-core verify's, the same
 //      bits) runs meanwhile, and then every token's B operand is written at
-//      once: token t's four rows
-//      (high parts of d k_hat and d q_hat, then the low parts) at rows
-//      4 (t % 4) .. + 3 of 16-row slice t / 4;
-//   2. per half and token: a named barrier over the half's 64 threads (its
-//      rows are back in the A operand); one warp issues 8 tcgen05.mma on the
-//      slice of the token; every thread of the half waits for the product,
-//      reads its row's sums and computes u and o; u goes to its warp's
-//      shared-memory slot; each thread updates its tile and writes it back;
+//      once: token t's four rows (high parts of d k_hat and d q_hat, then the
+//      low parts) at rows 4 (t % 4) .. + 3 of 16-row slice t / 4;
+//   2. per token: a CTA barrier (every row is back in the A operand); warp 0
+//      issues 8 tcgen05.mma on the slice of the token; every thread waits for
+//      the product, reads its row's sums and computes u and o; u goes to its
+//      warp's shared-memory slot; each thread updates its tile and writes it
+//      back. (Independent product chains per half or per warp of the rows,
+//      each product reading all 128 rows, were measured slower: the tensor
+//      core's queue grows with the number of products.)
 //   3. the final rows leave by two tensor-map stores.
 #include <cuda.h>
 
@@ -54,7 +47,7 @@
 namespace kda {
 
 constexpr int VT_THREADS = 128;
-constexpr uint32_t VT_TMEM_COLS = 32;  // 16 per half
+constexpr uint32_t VT_TMEM_COLS = 32;  // the sums: 16 columns
 constexpr uint32_t VT_SLICE_BYTES = 16u * 256u;  // one B slice: 16 rows x 128 keys bf16
 
 // Shared-memory carve-up (bytes from a 1024-aligned base) for TT token slots.
@@ -83,7 +76,7 @@ __host__ __device__ inline VerifyLayout verify_layout(int TT) {
   o += KDA_MAX_T * 4u;
   L.su = o;  // per-warp slots of the rows' u
   o += 128u * 4u;
-  L.bar = o;  // the state copy's mbarrier, one per half, the token inputs'
+  L.bar = o;  // the state copy's mbarrier, the token inputs', the products'
   o += 32u;
   L.tslot = o;
   o += 16u;
@@ -101,20 +94,6 @@ __device__ __forceinline__ void store_split2_b(unsigned char* sb, int r, int c, 
   *reinterpret_cast<uint16_t*>(sb + sw128_offset(16, r + 2, c)) = x1;
 }
 
-// An AND over the `count` threads of named barrier `id`, which it also syncs.
-__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.b32 p, %1, 0;\n\t"
-      "barrier.red.and.pred q, %2, %3, p;\n\t"
-      "selp.b32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-
 // Row (b, t, h) of a token view: 128 bf16 values.
 __device__ __forceinline__ const uint16_t* token_row(const kda_view& vw, int b, int t, int h) {
   return static_cast<const uint16_t*>(vw.ptr) + ((int64_t)b * vw.b_stride + (int64_t)t * vw.t_stride +
@@ -129,7 +108,6 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   constexpr int NW = VT_THREADS / 32;
   constexpr int PT = TT / NW;  // prologue tokens per warp
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int half = warp >> 1;
   const int h = blockIdx.x % p.H;
   const int b = blockIdx.x / p.H;
 
@@ -148,8 +126,8 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   ts.kappa = reinterpret_cast<float*>(sm + SL.kappa);
   ts.red = nullptr;
   uint64_t* barA = reinterpret_cast<uint64_t*>(sm + SL.bar);
-  uint64_t* barH = barA + 1 + half;  // this half's products
-  uint64_t* barT = barA + 3;         // the token inputs' bulk copies
+  uint64_t* barT = barA + 1;  // the token inputs' bulk copies
+  uint64_t* barD = barA + 2;  // the products
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL.tslot);
 
   uint16_t* outp = static_cast<uint16_t*>(p.out);
@@ -194,8 +172,7 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   uint16_t* gstate = static_cast<uint16_t*>(p.state) + (int64_t)n * p.state_slot_stride + (int64_t)h * KD * KD;
   if (tid == 0) {
     mbar_init(barA, 1);
-    mbar_init(barA + 1, 1);
-    mbar_init(barA + 2, 1);
+    mbar_init(barD, 1);
     if constexpr (TMA) {
       mbar_expect_tx(barA, KD * KD * 2);
       tma_load_3d(sA, &smap, 0, h * KD, n, barA);
@@ -230,8 +207,7 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   token_prologue<PT, NW>(p, b, h, T, 0, KD, ts, first);  // ends with a CTA barrier
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t dcol = tmem + 16u * (uint32_t)half;                          // this half's sums
-  const uint32_t row_tmem = tmem + ((uint32_t)(warp * 32) << 16) + 16u * (uint32_t)half;  // row tid's
+  const uint32_t row_tmem = tmem + ((uint32_t)(warp * 32) << 16);  // row tid's sums
 
   // Every token's B rows of channel tid (zero past T), through registers: the
   // slices overwrite g and q_hat.
@@ -272,28 +248,28 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   }
   float* su = reinterpret_cast<float*>(sm + SL.su) + warp * 32;  // u of rows 32 warp .. + 31
 
-  bool pendD = false;  // a product of this half is in flight, issued with parity pend_par
+  bool pendD = false;  // a product is in flight, issued with parity pend_par
   uint32_t pend_par = 0;
   for (int t = 0; t < T; ++t) {
-    // The half's rows of token t are in the A operand (written and fenced by
-    // both of its warps), and its last product's sums have been read.
+    // The rows of token t are in the A operand (written and fenced by every
+    // warp), and the last product's sums have been read.
     tc_fence_before();
-    ok = bar_and(1 + half, 64, ok);
+    ok = __syncthreads_and(ok) != 0;
     float o = 0.0f;
     if (ok) {
-      if (warp == 2 * half) {
+      if (warp == 0) {
         tc_fence_after();
         constexpr uint32_t idesc = idesc_bf16_f32(128, 16);
         const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB) + (uint32_t)(t >> 2) * VT_SLICE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_bf16_w(dcol, sw128_desc(a0 + (kk >> 2) * (KD * 128) + (kk & 3) * 32),
+          tc_mma_bf16_w(tmem, sw128_desc(a0 + (kk >> 2) * (KD * 128) + (kk & 3) * 32),
                         sw128_desc(b0 + (kk >> 2) * (16 * 128) + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
-        tc_commit_w(barH);
+        tc_commit_w(barD);
       }
       pendD = true;
       pend_par = (uint32_t)(t & 1);
-      ok = mbar_wait_bounded(barH, pend_par);  // every thread of the half waits for the product itself
+      ok = mbar_wait_bounded(barD, pend_par);  // every thread waits for the product itself
       if (!ok) {
         if (p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
       } else {
@@ -370,8 +346,8 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
     }
   }
   // A product that did not finish in time gets one more bounded wait before
-  // its tensor memory is released (one thread per half).
-  if (pendD && (tid & 63) == 0) mbar_wait_bounded(barH, pend_par);
+  // its tensor memory is released.
+  if (pendD && tid == 0) mbar_wait_bounded(barD, pend_par);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
