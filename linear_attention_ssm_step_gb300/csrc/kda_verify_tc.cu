@@ -23,8 +23,8 @@
 //      bulk copies into the B region, issued before the slot index is known
 //      (plain loads where a view is not 16-byte aligned); the state by two
 //      tensor-map loads into the K-major, 128-byte-swizzled layout of the A
-//      operand; the per-token prologue (the CUDA-core verify's, the same
-//      bits) runs meanwhile, and then every token's B operand is written at
+//      operand; the per-token prologue (the CUDA-core verify's quantities with
+//      the fast gate) runs meanwhile, and then every token's B operand is written at
 //      once: token t's four rows (high parts of d k_hat and d q_hat, then the
 //      low parts) at rows 4 (t % 4) .. + 3 of 16-row slice t / 4;
 //   2. per token: a CTA barrier (every row is back in the A operand); warp 0
@@ -40,6 +40,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "kda_chunk.cuh"
 #include "kda_device.cuh"
 #include "kda_launch.h"
 #include "kda_tc.cuh"
@@ -92,6 +93,52 @@ __device__ __forceinline__ void store_split2_b(unsigned char* sb, int r, int c, 
   const uint16_t x1 = float_to_bf16_bits(__fsub_rn(x, bf16_bits_to_float(x0)));
   *reinterpret_cast<uint16_t*>(sb + sw128_offset(16, r, c)) = x0;
   *reinterpret_cast<uint16_t*>(sb + sw128_offset(16, r + 2, c)) = x1;
+}
+
+// token_prologue's quantities from the same loads (k_hat, q_hat, the decay
+// d = exp(g), the v rows, kappa and beta; g itself is not kept), with the
+// chunk kernels' fast gate (FastGate: __expf and the approximate reciprocal)
+// and rsqrt for the norms. Their relative errors, a few 1e-7, are far inside
+// the verify's tolerances; configurations 0-3 keep the IEEE forms, whose
+// bits the decode shares.
+template <int PT, int NW>
+__device__ __forceinline__ void token_prologue_fast(const kda_params& p, int T, const TokenSmem& ts,
+                                                    const TokenLoads<PT>& L) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const FastGate gate(p, L.alog);
+  float rq[PT], rk[PT], sqk[PT];
+#pragma unroll
+  for (int s = 0; s < PT; ++s) {
+    float qq[4], kk[4], qk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      qq[i] = __fmul_rn(L.q[s][i], L.q[s][i]);
+      kk[i] = __fmul_rn(L.k[s][i], L.k[s][i]);
+      qk[i] = __fmul_rn(L.q[s][i], L.k[s][i]);
+    }
+    rq[s] = rsqrtf(__fadd_rn(sum_channels(qq[0], qq[1], qq[2], qq[3]), L2_EPS));
+    rk[s] = rsqrtf(__fadd_rn(sum_channels(kk[0], kk[1], kk[2], kk[3]), L2_EPS));
+    sqk[s] = sum_channels(qk[0], qk[1], qk[2], qk[3]);
+  }
+#pragma unroll
+  for (int s = 0; s < PT; ++s) {
+    const int t = warp + NW * s;
+    if (t < T) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = lane + 32 * i;
+        ts.dd[t * KD + c] = __expf(gate.g(L.g[s][i], L.dtb[i]));
+        ts.qh[t * KD + c] = __fmul_rn(L.q[s][i], rq[s]);
+        ts.kh[t * KD + c] = __fmul_rn(L.k[s][i], rk[s]);
+        ts.vrow[t * KD + c] = L.v[s][i];
+      }
+      if (lane == 0) {
+        ts.kappa[t] = __fmul_rn(__fmul_rn(sqk[s], rq[s]), rk[s]);
+        ts.beta[t] = gate.beta(L.bl[s]);
+      }
+    }
+  }
+  __syncthreads();
 }
 
 // Row (b, t, h) of a token view: 128 bf16 values.
@@ -204,7 +251,7 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
     __syncthreads();  // the prologue writes over the staged inputs
   }
   tc_fence_before();
-  token_prologue<PT, NW>(p, b, h, T, 0, KD, ts, first);  // ends with a CTA barrier
+  token_prologue_fast<PT, NW>(p, T, ts, first);  // ends with a CTA barrier
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t row_tmem = tmem + ((uint32_t)(warp * 32) << 16);  // row tid's sums
