@@ -316,7 +316,11 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
       }
       pendD = true;
       pend_par = (uint32_t)(t & 1);
-      ok = mbar_wait_bounded(barD, pend_par);  // every thread waits for the product itself
+      // One warp polls the product's mbarrier; the others sleep at the CTA
+      // barrier, leaving the issue slots to the SM's other CTAs.
+      bool d_ok = true;
+      if (warp == 0) d_ok = mbar_wait_bounded(barD, pend_par);
+      ok = __syncthreads_or(!d_ok) == 0;
       if (!ok) {
         if (p.error_word != nullptr) atomicOr(p.error_word, KDA_ERR_TIMEOUT);
       } else {
