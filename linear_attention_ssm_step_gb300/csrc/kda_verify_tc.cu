@@ -24,9 +24,9 @@
 //      (plain loads where a view is not 16-byte aligned); the state by two
 //      tensor-map loads into the K-major, 128-byte-swizzled layout of the A
 //      operand; the per-token prologue (the CUDA-core verify's quantities with
-//      the fast gate) runs meanwhile, and then every token's B operand is written at
-//      once: token t's four rows (high parts of d k_hat and d q_hat, then the
-//      low parts) at rows 4 (t % 4) .. + 3 of 16-row slice t / 4;
+//      the fast gate) runs meanwhile and writes every token's B operand:
+//      token t's four rows (high parts of d k_hat and d q_hat, then the low
+//      parts) at rows 4 (t % 4) .. + 3 of 16-row slice t / 4;
 //   2. per token: a CTA barrier (every row is back in the A operand); warp 0
 //      issues 8 tcgen05.mma on the slice of the token; every thread waits for
 //      the product, reads its row's sums and computes u and o; u goes to its
@@ -95,15 +95,17 @@ __device__ __forceinline__ void store_split2_b(unsigned char* sb, int r, int c, 
   *reinterpret_cast<uint16_t*>(sb + sw128_offset(16, r + 2, c)) = x1;
 }
 
-// token_prologue's quantities from the same loads (k_hat, q_hat, the decay
-// d = exp(g), the v rows, kappa and beta; g itself is not kept), with the
+// token_prologue's quantities from the same loads (k_hat, the decay d =
+// exp(g), the v rows, kappa and beta; g and q_hat are not kept), and every
+// token's B rows (d k_hat and d q_hat as high and low parts; zero past T)
+// written straight into the B slices, with the
 // chunk kernels' fast gate (FastGate: __expf and the approximate reciprocal)
 // and rsqrt for the norms. Their relative errors, a few 1e-7, are far inside
 // the verify's tolerances; configurations 0-3 keep the IEEE forms, whose
 // bits the decode shares.
 template <int PT, int NW>
 __device__ __forceinline__ void token_prologue_fast(const kda_params& p, int T, const TokenSmem& ts,
-                                                    const TokenLoads<PT>& L) {
+                                                    const TokenLoads<PT>& L, unsigned char* sB) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const FastGate gate(p, L.alog);
   float rq[PT], rk[PT], sqk[PT];
@@ -123,21 +125,32 @@ __device__ __forceinline__ void token_prologue_fast(const kda_params& p, int T, 
 #pragma unroll
   for (int s = 0; s < PT; ++s) {
     const int t = warp + NW * s;
+    unsigned char* slice = sB + (t >> 2) * VT_SLICE_BYTES;
     if (t < T) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int c = lane + 32 * i;
-        ts.dd[t * KD + c] = __expf(gate.g(L.g[s][i], L.dtb[i]));
-        ts.qh[t * KD + c] = __fmul_rn(L.q[s][i], rq[s]);
-        ts.kh[t * KD + c] = __fmul_rn(L.k[s][i], rk[s]);
+        const float d = __expf(gate.g(L.g[s][i], L.dtb[i]));
+        const float kh = __fmul_rn(L.k[s][i], rk[s]);
+        ts.dd[t * KD + c] = d;
+        ts.kh[t * KD + c] = kh;
         ts.vrow[t * KD + c] = L.v[s][i];
+        store_split2_b(slice, 4 * (t & 3), c, __fmul_rn(d, kh));
+        store_split2_b(slice, 4 * (t & 3) + 1, c, __fmul_rn(d, __fmul_rn(L.q[s][i], rq[s])));
       }
       if (lane == 0) {
         ts.kappa[t] = __fmul_rn(__fmul_rn(sqk[s], rq[s]), rk[s]);
         ts.beta[t] = gate.beta(L.bl[s]);
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        store_split2_b(slice, 4 * (t & 3), lane + 32 * i, 0.0f);
+        store_split2_b(slice, 4 * (t & 3) + 1, lane + 32 * i, 0.0f);
+      }
     }
   }
+  fence_proxy_async_smem();  // the B slices are read by the tensor core
   __syncthreads();
 }
 
@@ -165,9 +178,9 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   unsigned char* sB = sm + SL.b;
   TokenSmem ts;
   ts.kh = reinterpret_cast<float*>(sm + SL.kh);
-  ts.qh = reinterpret_cast<float*>(sB + TT * KD * 4);  // q_hat and g are not needed after the B slices
+  ts.qh = nullptr;  // q_hat and g are not kept: q_hat goes straight into the B slices
   ts.dd = reinterpret_cast<float*>(sm + SL.dd);
-  ts.gg = reinterpret_cast<float*>(sB);
+  ts.gg = nullptr;
   ts.vrow = reinterpret_cast<float*>(sm + SL.vrow);
   ts.beta = reinterpret_cast<float*>(sm + SL.beta);
   ts.kappa = reinterpret_cast<float*>(sm + SL.kappa);
@@ -251,30 +264,10 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
     __syncthreads();  // the prologue writes over the staged inputs
   }
   tc_fence_before();
-  token_prologue_fast<PT, NW>(p, T, ts, first);  // ends with a CTA barrier
+  token_prologue_fast<PT, NW>(p, T, ts, first, sB);  // writes the B slices; ends with a CTA barrier
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t row_tmem = tmem + ((uint32_t)(warp * 32) << 16);  // row tid's sums
-
-  // Every token's B rows of channel tid (zero past T), through registers: the
-  // slices overwrite g and q_hat.
-  {
-    float xk[TT], xq[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      const float d = t < T ? ts.dd[t * KD + tid] : 0.0f;
-      xk[t] = t < T ? __fmul_rn(d, ts.kh[t * KD + tid]) : 0.0f;
-      xq[t] = t < T ? __fmul_rn(d, ts.qh[t * KD + tid]) : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      unsigned char* slice = sB + (t >> 2) * VT_SLICE_BYTES;
-      store_split2_b(slice, 4 * (t & 3), tid, xk[t]);
-      store_split2_b(slice, 4 * (t & 3) + 1, tid, xq[t]);
-    }
-  }
-  fence_proxy_async_smem();  // the B slices are read by the tensor core
 
   bool ok = tok_ok;
   if constexpr (TMA) ok = mbar_wait_bounded(barA, 0) && ok;
