@@ -31,6 +31,8 @@ cudaError_t launch_step(const kda_params& p, int T, int tile_v, bool bulk, cudaS
 // slots}, {64, 128, 1} boxes, 128-byte swizzle (the tensor core's K-major
 // operand layout); needs a 16-byte aligned pool and slot stride.
 cudaError_t state_tensor_map(const kda_params& p, CUtensorMap* out);
+// A token view as {128 values, H heads, rows} in {128, 1, 16} boxes (kda_tmap.cu).
+cudaError_t token_tensor_map(const kda_view& v, int rows, int H, CUtensorMap* out);
 
 // T-token verify with the two dot products of every state row per token on
 // the tensor cores; one CTA per (row, head). bulk as above.

@@ -39,7 +39,10 @@
 //      in tensor memory (first chunk: the slot's bf16 state, which arrived by
 //      tensor-map loads straight into the first part);
 //   3. X/Y product (one thread issues 8 or 16 tcgen05.mma, N = 64); the next
-//      chunk's token loads are issued meanwhile;
+//      chunk's token inputs are fetched meanwhile: where every token view is
+//      16-byte aligned (TOK) by four tensor-map copies (16 rows of one head of
+//      q, k, g_raw and v each) into the transpose tiles, which the chunk has
+//      finished with, else by per-lane loads into registers;
 //   4. row i: the recurrence, the outputs of the chunk's tokens;
 //   5. U (row i) and the decayed keys W (channel i) as bf16 parts, then the
 //      update product accumulates onto S; it runs while the next chunk's
@@ -100,12 +103,45 @@ __host__ __device__ inline PcLayout pc_layout() {
 
 __host__ __device__ inline size_t pc_smem_bytes() { return (size_t)pc_layout().total + 1024; }
 
+// The tensor maps of the token views (TOK): q, k, g_raw, v.
+struct TokenMaps {
+  CUtensorMap m[4];
+};
+
+// The scalar inputs load_tokens also fetches: beta's logits (thread t < T),
+// A_log and dt_bias of channel tid (raw gate).
+template <int TT>
+__device__ __forceinline__ void load_token_scalars(const kda_params& p, int b, int h, int T, TokenRegs<TT>& L) {
+  const int tid = threadIdx.x;
+  if (tid < T) L.blogit = load_bits(p.beta_logit, b, tid, h, 0);
+  if (p.gate_mode == KDA_GATE_RAW) {
+    L.alog = p.A_log[h];
+    L.dtb = p.dt_bias[(int64_t)h * KD + tid];
+  }
+}
+
+// Channel tid's values of the staged chunk (zero past T), as load_tokens gives
+// them: view j's 16 rows at j * 4096 bytes of the stage.
+template <int TT>
+__device__ __forceinline__ void tokens_from_stage(const unsigned char* stage, int T, TokenRegs<TT>& L) {
+  const uint16_t* st = reinterpret_cast<const uint16_t*>(stage);
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    const bool in = t < T;
+    L.qv[t] = in ? st[0 * 2048 + t * KD + tid] : (uint16_t)0;
+    L.kv[t] = in ? st[1 * 2048 + t * KD + tid] : (uint16_t)0;
+    L.gv[t] = in ? st[2 * 2048 + t * KD + tid] : (uint16_t)0;
+    L.vv[t] = in ? st[3 * 2048 + t * KD + tid] : (uint16_t)0;
+  }
+}
+
 // p: the call's parameters with t_stride = b_stride in q, k, v, g_raw and
 // beta_logit, so that token t of a chunk starting at row c0 is (b = c0, t).
-template <bool TMA>
+template <bool TMA, bool TOK>
 __global__ void __launch_bounds__(PC_THREADS, 2)
-    kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p, const int32_t* __restrict__ cu,
-                          const int num_seqs) {
+    kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__ TokenMaps tmaps,
+                          const kda_params p, const int32_t* __restrict__ cu, const int num_seqs) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int total = num_seqs * p.H;
 
@@ -125,6 +161,9 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
   uint64_t* barA = reinterpret_cast<uint64_t*>(sm + SL.bar);  // the slot's state copy
   uint64_t* barD = barA + 1;                                   // X/Y product
   uint64_t* barU = barA + 2;                                   // update product
+  uint64_t* barT = barA + 3;                                   // a chunk's token inputs (TOK)
+  // ... staged in the transpose tiles, from their first 128-byte boundary
+  unsigned char* stage = sm + ((SL.xpose + 127u) & ~127u);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL.tslot);
   uint16_t* outp = static_cast<uint16_t*>(p.out);
 
@@ -132,6 +171,7 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
     mbar_init(barA, 1);
     mbar_init(barD, 1);
     mbar_init(barU, 1);
+    mbar_init(barT, 1);
   }
   if (warp == 0) tmem_alloc(tslot, PC_TMEM_COLS);
   tc_fence_before();
@@ -141,12 +181,36 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
   const uint32_t row_tmem = tmem + ((uint32_t)(warp * 32) << 16);  // lane tid, column 0
   uint32_t phA = 0, phD = 0, phU = 0;                                // mbarrier phases
   bool pendA = false, pendD = false, pendU = false;                  // a copy or a product is in flight
+  uint32_t phT = 0;
+  bool pendT = false;  // a chunk's token copies are in flight (TOK)
   bool broken = false;  // a bounded wait gave up: nothing more is issued
 
   // The first chunk's token inputs of an item, loaded during the previous
   // item's last chunk when that item had one (pre_it: the item they are for).
   TokenRegs<PC> L;
   int pre_it = -1;
+  // TOK: the staged chunk has landed (a CTA-uniform answer; false if the
+  // bounded wait gave up).
+  auto wait_stage = [&]() -> bool {
+    const bool w = __syncthreads_and(mbar_wait_bounded(barT, phT)) != 0;
+    if (w) {
+      phT ^= 1u;
+      pendT = false;
+    }
+    return w;
+  };
+  // TOK: stage the chunk of 16 rows from activation row b, head h, after any
+  // staged chunk still in flight (an item that was skipped) has landed.
+  auto stage_next = [&](int b, int h) -> bool {
+    if (pendT && !wait_stage()) return false;
+    if (tid == 0) {
+      mbar_expect_tx(barT, 4u * 4096u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tma_load_3d(stage + j * 4096, &tmaps.m[j], 0, h, b, barT);
+    }
+    pendT = true;
+    return true;
+  };
   for (int it = blockIdx.x; it < total; it += gridDim.x) {
     const int seq = it / p.H, h = it - seq * p.H;
     const int t0 = cu[seq], t1 = cu[seq + 1];
@@ -176,14 +240,29 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
         *reinterpret_cast<uint16_t*>(sA + sw128_offset(KD, r, tid)) = gstate[(int64_t)r * KD + tid];
     }
 
+    bool first = true, ok = true;
     if (pre_it != it) {
       zero_tokens(L);
-      load_tokens(p, t0, h, min(PC, t1 - t0), L);
+      if constexpr (TOK) {
+        fence_proxy_async_smem();  // the last item's generic uses of the tiles come before the copies
+        __syncthreads();
+        ok = stage_next(t0, h);
+        load_token_scalars(p, t0, h, min(PC, t1 - t0), L);
+      } else {
+        load_tokens(p, t0, h, min(PC, t1 - t0), L);
+      }
     }
     pre_it = -1;
-    bool first = true, ok = true;
-    for (int c0 = t0; c0 < t1; c0 += PC) {
+    for (int c0 = t0; c0 < t1 && ok; c0 += PC) {
       const int Tc = min(PC, t1 - c0);
+      if constexpr (TOK) {  // the chunk's staged tokens into registers; the tiles are written next
+        if (!wait_stage()) {
+          ok = false;
+          break;
+        }
+        tokens_from_stage(stage, Tc, L);
+        __syncthreads();
+      }
 
       // 1. L2 norms: block sums of q_t^2 (value t) and k_t^2 (value PC + t).
 #pragma unroll
@@ -356,20 +435,34 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
       uint16_t vcur[PC];
 #pragma unroll
       for (int t = 0; t < PC; ++t) vcur[t] = L.vv[t];
-      if (c0 + PC < t1) {  // the next chunk's token inputs fly while this chunk finishes
+      // The next chunk's token inputs fly while this chunk finishes (TOK: the
+      // tiles' last reads, the coefficient sums, came before the product's
+      // barrier and its proxy fence).
+      bool s_ok = true;
+      if (c0 + PC < t1) {
         zero_tokens(L);
-        load_tokens(p, c0 + PC, h, min(PC, t1 - c0 - PC), L);
+        if constexpr (TOK) {
+          s_ok = stage_next(c0 + PC, h);
+          load_token_scalars(p, c0 + PC, h, min(PC, t1 - c0 - PC), L);
+        } else {
+          load_tokens(p, c0 + PC, h, min(PC, t1 - c0 - PC), L);
+        }
       } else if (it + (int)gridDim.x < total) {  // the last chunk: the next item's first chunk
         const int nit = it + gridDim.x;
         const int nseq = nit / p.H, nh = nit - nseq * p.H;
         const int n0 = cu[nseq], n1 = cu[nseq + 1];
         if (n0 >= 0 && n1 > n0 && n1 <= p.B) {  // a sequence with tokens (loaded even if inactive: unused then)
           zero_tokens(L);
-          load_tokens(p, n0, nh, min(PC, n1 - n0), L);
+          if constexpr (TOK) {
+            s_ok = stage_next(n0, nh);
+            load_token_scalars(p, n0, nh, min(PC, n1 - n0), L);
+          } else {
+            load_tokens(p, n0, nh, min(PC, n1 - n0), L);
+          }
           pre_it = nit;
         }
       }
-      ok = __syncthreads_and(mbar_wait_bounded(barD, phD)) != 0;
+      ok = __syncthreads_and(mbar_wait_bounded(barD, phD) && s_ok) != 0;
       if (!ok) break;
       phD ^= 1u;
       pendD = false;
@@ -487,6 +580,7 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
     if (pendA) mbar_wait_bounded(barA, phA);
     if (pendD) mbar_wait_bounded(barD, phD);
     if (pendU) mbar_wait_bounded(barU, phU);
+    if (pendT) mbar_wait_bounded(barT, phT);
   }
   tc_fence_before();
   __syncthreads();
@@ -498,10 +592,10 @@ __global__ void __launch_bounds__(PC_THREADS, 2)
 
 // ---------------------------------------------------------------- host side
 
-template <bool TMA>
-static cudaError_t launch_pftc(const CUtensorMap& map, const kda_params& p, const int32_t* cu, int num_seqs,
-                               cudaStream_t s) {
-  auto kern = kda_prefill_tc_kernel<TMA>;
+template <bool TMA, bool TOK>
+static cudaError_t launch_pftc(const CUtensorMap& map, const TokenMaps& tm, const kda_params& p, const int32_t* cu,
+                               int num_seqs, cudaStream_t s) {
+  auto kern = kda_prefill_tc_kernel<TMA, TOK>;
   const size_t smem = pc_smem_bytes();
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
   cudaError_t e = set_smem_limit_once(kern, smem, smem_set);
@@ -538,7 +632,7 @@ static cudaError_t launch_pftc(const CUtensorMap& map, const kda_params& p, cons
   q.v.t_stride = q.v.b_stride;
   q.g_raw.t_stride = q.g_raw.b_stride;
   q.beta_logit.t_stride = q.beta_logit.b_stride;
-  kern<<<(unsigned)grid, PC_THREADS, smem, s>>>(map, q, cu, num_seqs);
+  kern<<<(unsigned)grid, PC_THREADS, smem, s>>>(map, tm, q, cu, num_seqs);
   return cudaGetLastError();
 }
 
@@ -548,9 +642,21 @@ cudaError_t launch_prefill_tc(const kda_params& p, const int32_t* cu, int num_se
   if (bulk) {
     const cudaError_t e = state_tensor_map(p, &map);
     if (e != cudaSuccess) return e;
-    return launch_pftc<true>(map, p, cu, num_seqs, s);
+    TokenMaps tm;
+    memset(&tm, 0, sizeof(tm));
+    if (prefill_rows_aligned16(p)) {  // the token views by tensor maps ({128, H, rows} in 16-row boxes)
+      const kda_view* vw[4] = {&p.q, &p.k, &p.g_raw, &p.v};
+      for (int j = 0; j < 4; ++j) {
+        const cudaError_t ej = token_tensor_map(*vw[j], p.B, p.H, &tm.m[j]);
+        if (ej != cudaSuccess) return ej;
+      }
+      return launch_pftc<true, true>(map, tm, p, cu, num_seqs, s);
+    }
+    return launch_pftc<true, false>(map, tm, p, cu, num_seqs, s);
   }
-  return launch_pftc<false>(map, p, cu, num_seqs, s);
+  TokenMaps tm;
+  memset(&tm, 0, sizeof(tm));
+  return launch_pftc<false, false>(map, tm, p, cu, num_seqs, s);
 }
 
 }  // namespace kda

@@ -62,4 +62,46 @@ cudaError_t state_tensor_map(const kda_params& p, CUtensorMap* out) {
   return cudaSuccess;
 }
 
+// A token view (q, k, v or g_raw: bf16 rows of H heads x 128 values) as a 3-D
+// tensor {128 values, H heads, rows} read in {128, 1, 16} boxes without
+// swizzle: one box is 16 consecutive rows of one head, rows past the last
+// reading as zeros. Needs every row 16-byte aligned. Four maps are kept per
+// host thread, keyed by address, strides and shape.
+cudaError_t token_tensor_map(const kda_view& v, int rows, int H, CUtensorMap* out) {
+  struct Cached {
+    const void* ptr = nullptr;
+    int rows = 0, H = 0;
+    int64_t b_stride = 0, h_stride = 0;
+    CUtensorMap map;
+  };
+  thread_local Cached cache[4];
+  thread_local int next = 0;
+  for (const Cached& c : cache)
+    if (c.ptr == v.ptr && c.rows == rows && c.H == H && c.b_stride == v.b_stride && c.h_stride == v.h_stride) {
+      *out = c.map;
+      return cudaSuccess;
+    }
+  const EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)KD, (cuuint64_t)H, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)v.h_stride * 2, (cuuint64_t)v.b_stride * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)KD, 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMap map;
+  const CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v.ptr), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  Cached& c = cache[next];
+  next = (next + 1) % 4;
+  c.ptr = v.ptr;
+  c.rows = rows;
+  c.H = H;
+  c.b_stride = v.b_stride;
+  c.h_stride = v.h_stride;
+  c.map = map;
+  *out = map;
+  return cudaSuccess;
+}
+
 }  // namespace kda
