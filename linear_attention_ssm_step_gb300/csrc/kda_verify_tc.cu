@@ -59,12 +59,11 @@ struct VerifyLayout {
 __host__ __device__ inline VerifyLayout verify_layout(int TT) {
   VerifyLayout L{};
   const uint32_t tok = (uint32_t)TT * KD * 4u;
-  const uint32_t bsz = (uint32_t)((TT + 3) / 4) * VT_SLICE_BYTES;
   uint32_t o = 0;
   L.a = o;
   o += 128u * 256u;  // state, 128 rows x 128 keys bf16
-  L.b = o;           // B slices; before them the prologue's g and q_hat (tok bytes each)
-  o += bsz > 2u * tok ? bsz : 2u * tok;
+  L.b = o;           // the staged token inputs (TT x 4 rows of 256 bytes), then the B slices
+  o += (uint32_t)((TT + 3) / 4) * VT_SLICE_BYTES;  // = TT x 1024
   L.kh = o;
   o += tok;
   L.dd = o;
@@ -98,11 +97,10 @@ __device__ __forceinline__ void store_split2_b(unsigned char* sb, int r, int c, 
 // token_prologue's quantities from the same loads (k_hat, the decay d =
 // exp(g), the v rows, kappa and beta; g and q_hat are not kept), and every
 // token's B rows (d k_hat and d q_hat as high and low parts; zero past T)
-// written straight into the B slices, with the
-// chunk kernels' fast gate (FastGate: __expf and the approximate reciprocal)
-// and rsqrt for the norms. Their relative errors, a few 1e-7, are far inside
-// the verify's tolerances; configurations 0-3 keep the IEEE forms, whose
-// bits the decode shares.
+// written straight into the B slices, with the chunk kernels' fast gate
+// (FastGate: __expf and the approximate reciprocal) and rsqrt for the norms.
+// Their relative errors, a few 1e-7, are far inside the verify's tolerances;
+// configurations 0-3 keep the IEEE forms, whose bits the decode shares.
 template <int PT, int NW>
 __device__ __forceinline__ void token_prologue_fast(const kda_params& p, int T, const TokenSmem& ts,
                                                     const TokenLoads<PT>& L, unsigned char* sB) {
