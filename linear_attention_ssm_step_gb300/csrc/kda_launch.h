@@ -33,6 +33,8 @@ cudaError_t launch_step(const kda_params& p, int T, int tile_v, bool bulk, cudaS
 cudaError_t state_tensor_map(const kda_params& p, CUtensorMap* out);
 // A token view as {128 values, H heads, rows} in {128, 1, 16} boxes (kda_tmap.cu).
 cudaError_t token_tensor_map(const kda_view& v, int rows, int H, CUtensorMap* out);
+// A T-token view as {128 values, H heads, T tokens, B rows} in {128, 1, TT, 1} boxes (kda_tmap.cu).
+cudaError_t token_tensor_map_bt(const kda_view& v, int B, int T, int H, int TT, CUtensorMap* out);
 
 // T-token verify with the two dot products of every state row per token on
 // the tensor cores; one CTA per (row, head). bulk as above.

@@ -19,9 +19,9 @@
 // of 16 value rows x 8 keys of the state (registers, bf16 pairs): lane l of
 // warp w takes rows 32 w + 16 (l / 16) .. + 15 and keys 8 (l % 16) .. + 7, so
 // a warp holds whole rows 32 w .. + 31, the rows whose sums it reads.
-//   1. the token inputs (q, k, g_raw and v rows, 256 bytes each) arrive by
-//      bulk copies into the B region, issued before the slot index is known
-//      (plain loads where a view is not 16-byte aligned); the state by two
+//   1. the token inputs (the T token rows of q, k, g_raw and v) arrive by four
+//      tensor-map copies into the B region, issued before the slot index is
+//      known (plain loads where a view is not 16-byte aligned); the state by two
 //      tensor-map loads into the K-major, 128-byte-swizzled layout of the A
 //      operand; the per-token prologue (the CUDA-core verify's quantities with
 //      the fast gate) runs meanwhile and writes every token's B operand:
@@ -152,16 +152,18 @@ __device__ __forceinline__ void token_prologue_fast(const kda_params& p, int T, 
   __syncthreads();
 }
 
-// Row (b, t, h) of a token view: 128 bf16 values.
-__device__ __forceinline__ const uint16_t* token_row(const kda_view& vw, int b, int t, int h) {
-  return static_cast<const uint16_t*>(vw.ptr) + ((int64_t)b * vw.b_stride + (int64_t)t * vw.t_stride +
-                                                 (int64_t)h * vw.h_stride);
-}
+// The tensor maps of the token views (TOK): q, k, g_raw, v as {128, H, T, B}
+// tensors in {128, 1, TT, 1} boxes.
+struct VerifyTokenMaps {
+  CUtensorMap m[4];
+};
 
-// TOK: the token inputs arrive by bulk copies (every view 16-byte aligned).
+// TOK: the token inputs arrive by four tensor-map copies (every view 16-byte
+// aligned): view j's TT token slots at j TT 256 bytes of the B region.
 template <bool TMA, int TT, bool TOK>
 __global__ void __launch_bounds__(VT_THREADS, 4)
-    kda_verify_tc_kernel(const __grid_constant__ CUtensorMap smap, const kda_params p, const int T) {
+    kda_verify_tc_kernel(const __grid_constant__ CUtensorMap smap, const __grid_constant__ VerifyTokenMaps tmaps,
+                         const kda_params p, const int T) {
   static_assert(TT == 8 || TT == 16, "token slots");
   constexpr int NW = VT_THREADS / 32;
   constexpr int PT = TT / NW;  // prologue tokens per warp
@@ -196,17 +198,11 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   const uint16_t* stage = reinterpret_cast<const uint16_t*>(sB);
   TokenLoads<PT> first;
   if constexpr (TOK) {
-    if (warp == 1) {  // one copy per lane (lane = 4 t + j), so that warp 0 starts the state copy at once
-      if (lane == 0) {
-        mbar_init(barT, 1);
-        mbar_expect_tx(barT, (uint32_t)T * 4u * 256u);
-      }
-      __syncwarp();
-      for (int r = lane; r < 4 * T; r += 32) {
-        const int t = r >> 2, j = r & 3;
-        const kda_view& vw = j == 0 ? p.q : j == 1 ? p.k : j == 2 ? p.g_raw : p.v;
-        bulk_g2s(sB + r * 256, token_row(vw, b, t, h), 256, barT);
-      }
+    if (tid == 32) {  // warp 1, so that warp 0 starts the state copy at once
+      mbar_init(barT, 1);
+      mbar_expect_tx(barT, 4u * TT * 256u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tma_load_4d(sB + j * TT * 256, &tmaps.m[j], 0, h, 0, b, barT);
     }
     gate_issue(p, h, first);
 #pragma unroll
@@ -253,10 +249,10 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
       for (int i = 0; i < 4; ++i) {
         const int c = lane + 32 * i;
         const bool in = t < T && tok_ok;
-        first.q[s2][i] = in ? bf16_bits_to_float(stage[(4 * t + 0) * KD + c]) : 0.0f;
-        first.k[s2][i] = in ? bf16_bits_to_float(stage[(4 * t + 1) * KD + c]) : 0.0f;
-        first.g[s2][i] = in ? bf16_bits_to_float(stage[(4 * t + 2) * KD + c]) : 0.0f;
-        first.v[s2][i] = in ? bf16_bits_to_float(stage[(4 * t + 3) * KD + c]) : 0.0f;
+        first.q[s2][i] = in ? bf16_bits_to_float(stage[(0 * TT + t) * KD + c]) : 0.0f;
+        first.k[s2][i] = in ? bf16_bits_to_float(stage[(1 * TT + t) * KD + c]) : 0.0f;
+        first.g[s2][i] = in ? bf16_bits_to_float(stage[(2 * TT + t) * KD + c]) : 0.0f;
+        first.v[s2][i] = in ? bf16_bits_to_float(stage[(3 * TT + t) * KD + c]) : 0.0f;
       }
     }
     __syncthreads();  // the prologue writes over the staged inputs
@@ -401,6 +397,15 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
 template <bool TMA, int TT, bool TOK>
 static cudaError_t launch_vtc(const CUtensorMap& map, const kda_params& p, int T, cudaStream_t s) {
   auto kern = kda_verify_tc_kernel<TMA, TT, TOK>;
+  VerifyTokenMaps tm;
+  memset(&tm, 0, sizeof(tm));
+  if (TOK) {
+    const kda_view* vw[4] = {&p.q, &p.k, &p.g_raw, &p.v};
+    for (int j = 0; j < 4; ++j) {
+      const cudaError_t ej = token_tensor_map_bt(*vw[j], p.B, T, p.H, TT, &tm.m[j]);
+      if (ej != cudaSuccess) return ej;
+    }
+  }
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
   cudaError_t e = set_smem_limit_once(kern, verify_tc_smem_bytes(TT), smem_set);
   if (e != cudaSuccess) return e;
@@ -411,7 +416,7 @@ static cudaError_t launch_vtc(const CUtensorMap& map, const kda_params& p, int T
       return e;
     carveout_set.store(true, std::memory_order_release);
   }
-  kern<<<(unsigned)((long long)p.B * p.H), VT_THREADS, verify_tc_smem_bytes(TT), s>>>(map, p, T);
+  kern<<<(unsigned)((long long)p.B * p.H), VT_THREADS, verify_tc_smem_bytes(TT), s>>>(map, tm, p, T);
   return cudaGetLastError();
 }
 
