@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
   ts.kappa = reinterpret_cast<float*>(sm + SL.kappa);
   ts.red = nullptr;
   uint64_t* barA = reinterpret_cast<uint64_t*>(sm + SL.bar);
-  uint64_t* barT = barA + 1;  // the token inputs' bulk copies
+  uint64_t* barT = barA + 1;  // the token inputs' tensor-map copies
   uint64_t* barD = barA + 2;  // the products
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL.tslot);
 
