@@ -220,6 +220,26 @@ def test_prefill_misaligned_pool_same_bits(dev, config):
     assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
 
 
+def test_prefill_misaligned_token_views_same_bits(dev):
+    """Token views off a 16-byte boundary take per-lane loads in place of the
+    chunked kernel's tensor-map copies of the token rows: the same bits."""
+    w = workloads.prefill_inputs([6, 40, 17], 5, seed=78)
+    a, b = w.to(dev), w.to(dev)
+
+    def shifted(x):
+        flat = torch.empty(x.numel() + 8, dtype=x.dtype, device=dev)
+        y = flat[1:1 + x.numel()].view(x.shape)
+        y.copy_(x)
+        return y
+
+    b.q_sep, b.k_sep, b.v_sep, b.g_raw = (shifted(x) for x in (b.q_sep, b.k_sep, b.v_sep, b.g_raw))
+    assert b.q_sep.data_ptr() % 16 == 2
+    oa, ob = gpu_prefill(a, config_override=4), gpu_prefill(b, config_override=4)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+
+
 def test_prefill_bad_bounds_set_the_error_bit(dev):
     w = workloads.prefill_inputs([5, 4, 6], 6, seed=77)
     w.cu_seqlens = torch.tensor([0, 5, 9, 3], dtype=torch.int32)  # sequence 2 runs backwards

@@ -138,6 +138,27 @@ def test_verify_tensor_cores_misaligned_state_same_bits(dev):
     assert torch.equal(mis.view(torch.int16), ref.state.view(torch.int16))
 
 
+def _shifted(x, dev):
+    """x copied to a buffer one element (2 bytes) off a 16-byte boundary."""
+    flat = torch.empty(x.numel() + 8, dtype=x.dtype, device=dev)
+    y = flat[1:1 + x.numel()].view(x.shape)
+    y.copy_(x)
+    return y
+
+
+def test_verify_tensor_cores_misaligned_token_views_same_bits(dev):
+    """Token views off a 16-byte boundary take per-lane loads in place of the
+    tensor-map copies of the token inputs: the same values, the same bits."""
+    w = workloads.decode_inputs(6, 10, seed=17, T=8, inactive_frac=0.2)
+    a, b = w.to(dev), w.to(dev)
+    b.q_sep, b.k_sep, b.v_sep, b.g_raw = (_shifted(x, dev) for x in (b.q_sep, b.k_sep, b.v_sep, b.g_raw))
+    assert b.q_sep.data_ptr() % 16 == 2
+    oa, ob = gpu_verify(a, config_override=TC), gpu_verify(b, config_override=TC)
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(a.state.view(torch.int16), b.state.view(torch.int16))
+
+
 def test_verify_tensor_cores_cuda_graph_bitwise(dev):
     w = workloads.decode_inputs(6, 10, seed=6, T=8)
     wd = w.to(dev)
