@@ -644,14 +644,12 @@ cudaError_t launch_prefill_tc(const kda_params& p, const int32_t* cu, int num_se
     if (e != cudaSuccess) return e;
     TokenMaps tm;
     memset(&tm, 0, sizeof(tm));
-    if (prefill_rows_aligned16(p)) {  // the token views by tensor maps ({128, H, rows} in 16-row boxes)
-      const kda_view* vw[4] = {&p.q, &p.k, &p.g_raw, &p.v};
-      for (int j = 0; j < 4; ++j) {
-        const cudaError_t ej = token_tensor_map(*vw[j], p.B, p.H, &tm.m[j]);
-        if (ej != cudaSuccess) return ej;
-      }
-      return launch_pftc<true, true>(map, tm, p, cu, num_seqs, s);
-    }
+    // The token views by tensor maps ({128, H, rows} in 16-row boxes) where
+    // every row is 16-byte aligned and the maps can be formed, else plain loads.
+    bool tok = prefill_rows_aligned16(p);
+    const kda_view* vw[4] = {&p.q, &p.k, &p.g_raw, &p.v};
+    for (int j = 0; j < 4 && tok; ++j) tok = token_tensor_map(*vw[j], p.B, p.H, &tm.m[j]) == cudaSuccess;
+    if (tok) return launch_pftc<true, true>(map, tm, p, cu, num_seqs, s);
     return launch_pftc<true, false>(map, tm, p, cu, num_seqs, s);
   }
   TokenMaps tm;

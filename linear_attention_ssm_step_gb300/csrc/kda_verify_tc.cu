@@ -395,17 +395,9 @@ __global__ void __launch_bounds__(VT_THREADS, 4)
 }
 
 template <bool TMA, int TT, bool TOK>
-static cudaError_t launch_vtc(const CUtensorMap& map, const kda_params& p, int T, cudaStream_t s) {
+static cudaError_t launch_vtc(const CUtensorMap& map, const VerifyTokenMaps& tm, const kda_params& p, int T,
+                              cudaStream_t s) {
   auto kern = kda_verify_tc_kernel<TMA, TT, TOK>;
-  VerifyTokenMaps tm;
-  memset(&tm, 0, sizeof(tm));
-  if (TOK) {
-    const kda_view* vw[4] = {&p.q, &p.k, &p.g_raw, &p.v};
-    for (int j = 0; j < 4; ++j) {
-      const cudaError_t ej = token_tensor_map_bt(*vw[j], p.B, T, p.H, TT, &tm.m[j]);
-      if (ej != cudaSuccess) return ej;
-    }
-  }
   static std::atomic<bool> smem_set{false};  // one flag per instantiation
   cudaError_t e = set_smem_limit_once(kern, verify_tc_smem_bytes(TT), smem_set);
   if (e != cudaSuccess) return e;
@@ -426,17 +418,30 @@ static bool rows_aligned16(const kda_view& vw) {
          vw.h_stride % 8 == 0;
 }
 
+// The token views' tensor maps for TT token slots; false (plain loads) where
+// a view is not 16-byte aligned or a map cannot be formed.
+static bool verify_token_maps(const kda_params& p, int T, int TT, VerifyTokenMaps* tm) {
+  const kda_view* vw[4] = {&p.q, &p.k, &p.g_raw, &p.v};
+  for (int j = 0; j < 4; ++j)
+    if (!rows_aligned16(*vw[j]) || token_tensor_map_bt(*vw[j], p.B, T, p.H, TT, &tm->m[j]) != cudaSuccess)
+      return false;
+  return true;
+}
+
 cudaError_t launch_verify_tc(const kda_params& p, int T, bool bulk, cudaStream_t s) {
   CUtensorMap map;
   memset(&map, 0, sizeof(map));
+  VerifyTokenMaps tm;
+  memset(&tm, 0, sizeof(tm));
+  const int TT = T <= 8 ? 8 : 16;
   if (bulk) {
     const cudaError_t e = state_tensor_map(p, &map);
     if (e != cudaSuccess) return e;
-    if (rows_aligned16(p.q) && rows_aligned16(p.k) && rows_aligned16(p.g_raw) && rows_aligned16(p.v))
-      return T <= 8 ? launch_vtc<true, 8, true>(map, p, T, s) : launch_vtc<true, 16, true>(map, p, T, s);
-    return T <= 8 ? launch_vtc<true, 8, false>(map, p, T, s) : launch_vtc<true, 16, false>(map, p, T, s);
+    if (verify_token_maps(p, T, TT, &tm))
+      return TT == 8 ? launch_vtc<true, 8, true>(map, tm, p, T, s) : launch_vtc<true, 16, true>(map, tm, p, T, s);
+    return TT == 8 ? launch_vtc<true, 8, false>(map, tm, p, T, s) : launch_vtc<true, 16, false>(map, tm, p, T, s);
   }
-  return T <= 8 ? launch_vtc<false, 8, false>(map, p, T, s) : launch_vtc<false, 16, false>(map, p, T, s);
+  return TT == 8 ? launch_vtc<false, 8, false>(map, tm, p, T, s) : launch_vtc<false, 16, false>(map, tm, p, T, s);
 }
 
 }  // namespace kda
