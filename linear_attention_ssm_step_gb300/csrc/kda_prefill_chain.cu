@@ -28,9 +28,12 @@
 // U and O in fp32 and P_{C-1}. The chain, per chunk, for value row i:
 //   1. S_0 row i (tensor memory) -> two bf16 parts (the A operand), and
 //      S <- diag(P_{C-1}) S_0 in tensor memory;
-//   2. D = S_0^T [-W | Q] on the tensor cores (N = 32; the products
-//      hi.hi, lo.hi and hi.lo of the parts, the state and the vectors exact to
-//      about 2^-17);
+//   2. D = S_0^T [-W | Q] on the tensor cores (the products hi.hi, lo.hi
+//      and hi.lo of the parts, the state and the vectors exact to about
+//      2^-17: per K step one N = 64 product of the state's high part with
+//      both parts of the vectors, whose rows lie together in the image, and
+//      one N = 32 product of its low part with their high part; the hi.lo
+//      sums, in their own columns, are added when D is read);
 //   3. u_t = U_t + D_t, as three bf16 parts;
 //   4. S += sum_t K~_t u_t^T on the tensor cores (the six products of order
 //      <= 2 of the parts, exact to about 2^-24), while o_t = scale (D_{16+t} + O_t)
@@ -467,7 +470,7 @@ constexpr int CN_WORKERS = 256;
 constexpr int CN_THREADS = CN_WORKERS + 32;
 constexpr int CN_MMA_WARP = CN_WORKERS / 32;
 constexpr uint32_t CN_TMEM_COLS = 512;
-constexpr uint32_t CN_D = 128;   // D of the first product: columns 128..159
+constexpr uint32_t CN_D = 128;   // D of the first product: columns 128..191 (hi.hi + lo.hi, then hi.lo)
 constexpr uint32_t CN_AS = 256;  // S as two bf16 parts, the first product's A operand: part p at 256 + 64 p
 constexpr uint32_t CN_AU = 384;  // u as three bf16 parts, the update's A operand: part p at 384 + 8 p
 constexpr int CN_NBUF = 3;       // chunk images in flight
@@ -712,14 +715,13 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
         // the products alone.
         const uint32_t x0 = smem_addr(im + IMG_XB);
         const uint32_t tb = __shfl_sync(0xffffffffu, tmem, 0), xb = __shfl_sync(0xffffffffu, x0, 0);
-        constexpr uint32_t idesc = idesc_bf16_f32(128, 2 * CH);
-        uint64_t bh[8], bl[8];
+        // N = 64 (the 32 high rows of XB, then its 32 low rows) and N = 32
+        // (the high rows alone) from the same K-step address.
+        constexpr uint32_t idesc64 = idesc_bf16_f32(128, 4 * CH), idesc32 = idesc_bf16_f32(128, 2 * CH);
+        static_assert(IMG_XB_LO == 32u * 128u, "the low rows follow the high rows");
+        uint64_t bh[8];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t xk = xb + (kk >> 2) * (64 * 128) + (kk & 3) * 32;
-          bh[kk] = sw128_desc(xk);
-          bl[kk] = sw128_desc(xk + IMG_XB_LO);
-        }
+        for (int kk = 0; kk < 8; ++kk) bh[kk] = sw128_desc(xb + (kk >> 2) * (64 * 128) + (kk & 3) * 32);
         const uint32_t dcol = tb + CN_D, acol = tb + CN_AS;
 #pragma unroll
         for (int rd = 0; rd < 2; ++rd) {
@@ -728,9 +730,8 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
 #pragma unroll
           for (int i = 0; i < 4; ++i) {  // K steps of blocks rd and 2 + rd
             const int kk = (i < 2 ? 2 * rd : 4 + 2 * rd) + (i & 1);
-            tc_mma_bf16_ta_w(dcol, acol + kk * 8, bh[kk], idesc, (rd > 0 || i > 0) ? 1u : 0u);
-            tc_mma_bf16_ta_w(dcol, acol + kk * 8, bl[kk], idesc, 1u);
-            tc_mma_bf16_ta_w(dcol, acol + 64 + kk * 8, bh[kk], idesc, 1u);
+            tc_mma_bf16_ta_w(dcol, acol + kk * 8, bh[kk], idesc64, (rd > 0 || i > 0) ? 1u : 0u);
+            tc_mma_bf16_ta_w(dcol, acol + 64 + kk * 8, bh[kk], idesc32, 1u);
           }
         }
         tc_commit_w(barD);
@@ -747,9 +748,16 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
       // issues S += sum_t u_t K~_t (the products of order <= 2 of the three
       // parts of each) while the state warps form the chunk's outputs.
       if (worker) {
-        float dx[8], dy[8];
+        float dx[8], dy[8], ex[8], ey[8];
         tmem_ld8(row_tmem + CN_D + 8 * hf, dx);
         tmem_ld8(row_tmem + CN_D + CH + 8 * hf, dy);
+        tmem_ld8(row_tmem + CN_D + 2 * CH + 8 * hf, ex);  // the hi.lo sums
+        tmem_ld8(row_tmem + CN_D + 3 * CH + 8 * hf, ey);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          dx[i] = __fadd_rn(dx[i], ex[i]);
+          dy[i] = __fadd_rn(dy[i], ey[i]);
+        }
         const float* gu = reinterpret_cast<const float*>(im + IMG_U) + (8 * hf) * KD + row;
         {
           uint32_t w0[4], w1[4], w2[4];
