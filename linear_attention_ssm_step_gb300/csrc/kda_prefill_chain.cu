@@ -655,9 +655,10 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
 
       // 2. In two rounds, each half of the state warps converts one 32-column
       // block of row `row`: S into its bf16 parts (tensor memory, the A
-      // operand) and S <- P_{C-1} S; after each round the issuing warp issues
-      // the first product's K steps that the round completed (block cb holds
-      // K steps 2 cb and 2 cb + 1). D[row][t'] = sum_k S[row][k] XB[t'][k]:
+      // operand), then signals the issuing warp, which issues the first
+      // product's K steps that the round completed (block cb holds K steps
+      // 2 cb and 2 cb + 1); then S <- P_{C-1} S, off the products' path (the
+      // update, which adds to it, comes after the u phase's store wait). D[row][t'] = sum_k S[row][k] XB[t'][k]:
       // the high parts of both, the low part of S with the high rows of XB,
       // the high part of S with the low rows (the first chunk's S is exact in
       // one part; its low part is written as zero).
@@ -696,6 +697,9 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
             tmem_st16(row_tmem + CN_AS + cb * 16, hw);
             tmem_st16(row_tmem + CN_AS + 64 + cb * 16, lw);
           }
+          tmem_st_wait();
+          tc_fence_before();
+          bar_arrive(rd == 0 ? CN_BAR_ROUND0 : CN_BAR_ROUND1, CN_THREADS);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const float4 pl = *reinterpret_cast<const float4*>(splast + cb * 32 + 4 * c);
@@ -704,10 +708,7 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
             upk2(a, s[4 * c], s[4 * c + 1]);
             upk2(bb, s[4 * c + 2], s[4 * c + 3]);
           }
-          tmem_st32(row_tmem + cb * 32, s);
-          tmem_st_wait();
-          tc_fence_before();
-          bar_arrive(rd == 0 ? CN_BAR_ROUND0 : CN_BAR_ROUND1, CN_THREADS);
+          tmem_st32(row_tmem + cb * 32, s);  // waited for by the u phase's tmem_st_wait, before the update
         }
       } else if (issuer) {
         // Every operand is formed before the first barrier, so that the issue
@@ -801,6 +802,7 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
       pendU = true;
       first = false;
     }
+    if (worker) tmem_st_wait();  // a rescale still in flight after a wait that gave up
 
     if (ok) {  // the final state, rounded to bf16 once; row `row`, columns 64 hf .. 64 hf + 63, into the slot
       ok = __syncthreads_and(mbar_wait_bounded(barU, phU)) != 0;
