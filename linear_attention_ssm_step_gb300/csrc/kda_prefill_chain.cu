@@ -653,21 +653,23 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
       }
       tc_fence_after();
 
-      // 2. In two rounds, each half of the state warps converts one 32-column
-      // block of row `row`: S into its bf16 parts (tensor memory, the A
-      // operand), then signals the issuing warp, which issues the first
-      // product's K steps that the round completed (block cb holds K steps
-      // 2 cb and 2 cb + 1); then S <- P_{C-1} S, off the products' path (the
-      // update, which adds to it, comes after the u phase's store wait). D[row][t'] = sum_k S[row][k] XB[t'][k]:
+      // 2. Each half of the state warps loads its two 32-column blocks of row
+      // `row` at once; in two rounds it converts one block into its bf16
+      // parts (tensor memory, the A operand) and signals the issuing warp,
+      // which issues the first product's K steps that the round completed
+      // (block cb holds K steps 2 cb and 2 cb + 1); then S <- P_{C-1} S for
+      // both blocks, off the products' path (the update, which adds to S,
+      // comes after the u phase's store wait). D[row][t'] = sum_k S[row][k] XB[t'][k]:
       // the high parts of both, the low part of S with the high rows of XB,
       // the high part of S with the low rows (the first chunk's S is exact in
       // one part; its low part is written as zero).
       if (worker) {
         const float* splast = reinterpret_cast<const float*>(im + IMG_PL);
+        float s[2][32];  // the thread's two 32-column blocks, cb = 2 hf and 2 hf + 1
+        if (!first) tmem_ld32x2(row_tmem + 64 * hf, s[0], s[1]);
 #pragma unroll
         for (int rd = 0; rd < 2; ++rd) {
           const int cb = 2 * hf + rd;
-          float s[32];
           if (first) {  // the slot's bf16 row, exact: one part
             uint32_t hw[16];
 #pragma unroll
@@ -679,18 +681,17 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
               hw[4 * c + 3] = raw.w;
             }
 #pragma unroll
-            for (int q = 0; q < 16; ++q) unpack_bf16x2(hw[q], s[2 * q], s[2 * q + 1]);
+            for (int q = 0; q < 16; ++q) unpack_bf16x2(hw[q], s[rd][2 * q], s[rd][2 * q + 1]);
             tmem_st16(row_tmem + CN_AS + cb * 16, hw);
             uint32_t zw[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) zw[q] = 0u;
             tmem_st16(row_tmem + CN_AS + 64 + cb * 16, zw);  // the low part of an exact state is zero
           } else {
-            tmem_ld32(row_tmem + cb * 32, s);
             uint32_t hw[16], lw[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-              const float s0 = s[2 * q], s1 = s[2 * q + 1];
+              const float s0 = s[rd][2 * q], s1 = s[rd][2 * q + 1];
               hw[q] = pack_bf16x2(s0, s1);
               lw[q] = f32x2_to_bf16x2(sub2(pk2(s0, s1), bf16x2_to_f32x2(hw[q])));
             }
@@ -700,15 +701,19 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
           tmem_st_wait();
           tc_fence_before();
           bar_arrive(rd == 0 ? CN_BAR_ROUND0 : CN_BAR_ROUND1, CN_THREADS);
+        }
+#pragma unroll
+        for (int rd = 0; rd < 2; ++rd) {  // S <- P_{C-1} S, both blocks after both rounds
+          const int cb = 2 * hf + rd;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const float4 pl = *reinterpret_cast<const float4*>(splast + cb * 32 + 4 * c);
-            f32x2 a = mul2(pk2(pl.x, pl.y), pk2(s[4 * c], s[4 * c + 1]));
-            f32x2 bb = mul2(pk2(pl.z, pl.w), pk2(s[4 * c + 2], s[4 * c + 3]));
-            upk2(a, s[4 * c], s[4 * c + 1]);
-            upk2(bb, s[4 * c + 2], s[4 * c + 3]);
+            f32x2 a = mul2(pk2(pl.x, pl.y), pk2(s[rd][4 * c], s[rd][4 * c + 1]));
+            f32x2 bb = mul2(pk2(pl.z, pl.w), pk2(s[rd][4 * c + 2], s[rd][4 * c + 3]));
+            upk2(a, s[rd][4 * c], s[rd][4 * c + 1]);
+            upk2(bb, s[rd][4 * c + 2], s[rd][4 * c + 3]);
           }
-          tmem_st32(row_tmem + cb * 32, s);  // waited for by the u phase's tmem_st_wait, before the update
+          tmem_st32(row_tmem + cb * 32, s[rd]);  // waited for by the u phase's tmem_st_wait, before the update
         }
       } else if (issuer) {
         // Every operand is formed before the first barrier, so that the issue
