@@ -754,15 +754,18 @@ __device__ __forceinline__ void chain_items(const CUtensorMap* smap_p, const kda
       // issues S += sum_t u_t K~_t (the products of order <= 2 of the three
       // parts of each) while the state warps form the chunk's outputs.
       if (worker) {
-        float dx[8], dy[8], ex[8], ey[8];
-        tmem_ld8(row_tmem + CN_D + 8 * hf, dx);
-        tmem_ld8(row_tmem + CN_D + CH + 8 * hf, dy);
-        tmem_ld8(row_tmem + CN_D + 2 * CH + 8 * hf, ex);  // the hi.lo sums
-        tmem_ld8(row_tmem + CN_D + 3 * CH + 8 * hf, ey);
+        float dx[8], dy[8];
+        {
+          // x and y of tokens 8 hf .., then their hi.lo sums, by one wait
+          const uint32_t at[4] = {row_tmem + CN_D + 8 * hf, row_tmem + CN_D + CH + 8 * hf,
+                                  row_tmem + CN_D + 2 * CH + 8 * hf, row_tmem + CN_D + 3 * CH + 8 * hf};
+          float d4[4][8];
+          tmem_ld8x4(at, d4);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          dx[i] = __fadd_rn(dx[i], ex[i]);
-          dy[i] = __fadd_rn(dy[i], ey[i]);
+          for (int i = 0; i < 8; ++i) {
+            dx[i] = __fadd_rn(d4[0][i], d4[2][i]);
+            dy[i] = __fadd_rn(d4[1][i], d4[3][i]);
+          }
         }
         const float* gu = reinterpret_cast<const float*>(im + IMG_U) + (8 * hf) * KD + row;
         {

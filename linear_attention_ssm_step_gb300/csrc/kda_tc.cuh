@@ -220,6 +220,32 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&out)[32]) {
   for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(r[i]);
 }
 
+// Four runs of 8 fp32 columns of this thread's tensor-memory lane (at
+// taddr[0..3]) by four loads and one wait (as tmem_ld8).
+__device__ __forceinline__ void tmem_ld8x4(const uint32_t (&taddr)[4], float (&out)[4][8]) {
+  uint32_t r[32];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    uint32_t* q = r + 8 * b;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7])
+                 : "r"(taddr[b])
+                 : "memory");
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+#pragma unroll
+  for (int b = 0; b < 4; ++b)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[b][i] = __uint_as_float(r[8 * b + i]);
+}
+
 // 64 consecutive fp32 columns of this thread's tensor-memory lane as two
 // 32-column loads and one wait (as tmem_ld32); the empty statement after the
 // wait names the second block's registers, so no use of them moves above it.
