@@ -141,7 +141,7 @@ int32_t kda_select_prefill_ws_config(int32_t B, int32_t num_seqs, int32_t H);
 
 /*
  * Two-stage prefill that allocates nothing, with the workspace inside the
- * library. The paper has no counterpart: this entry point exists for callers
+ * library. No source page describes it: this entry point exists for callers
  * of this library that cannot call cudaMalloc when they run a prefill (a
  * step captured into a CUDA graph in global capture mode, where allocation
  * calls are not permitted; a plugin whose host framework owns all device
