@@ -367,3 +367,27 @@ def test_chain_h16_16384_against_chunked_kernel(dev):
     assert_output_close(f64(oa), f64(ob), "two-stage against chunked outputs")
     n = int(w.state_indices[0])
     assert_prefill_state_close(f64(a.state)[n], f64(b.state)[n], 16384, "final state")
+
+
+def test_chain_h16_16384_sampled_heads_against_oracle(dev):
+    """The pages' H16 x 16384-token shape in the library's launch
+    configuration (one launch, two stages): two sampled heads' outputs for
+    every token and their final states against the oracle (heads are
+    independent; the oracle runs those two alone)."""
+    L = 16384
+    w = workloads.prefill_inputs([L], 2, seed=96, layout="fused", H=16)
+    wd = w.to(dev)
+    assert kda.kda_select_prefill_ws_config(L, 1, 16) == FUSED
+    out = chain_prefill(wd, config_override=-1)
+    torch.cuda.synchronize()
+    got_out, got_state = f64(out), f64(wd.state)
+    n = int(w.state_indices[0])
+    for h in (3, 12):
+        hs = slice(h, h + 1)
+        ref_state, ref_out, _, err = oracle.kda_prefill(
+            f64(w.state[n:n + 1, hs]), np.array([0]), np.array([0, L]), f64(w.q[:, hs]), f64(w.k[:, hs]),
+            f64(w.v[:, hs]), f64(w.g_raw[:, hs]), f64(w.beta_logit[:, hs]), f64(w.A_log[hs]),
+            f64(w.dt_bias[hs]), lower_bound=LB)
+        assert err == 0
+        assert_output_close(got_out[:, hs], ref_out, f"outputs of head {h}")
+        assert_prefill_state_close(got_state[n, hs], ref_state[0], L, f"final state of head {h}")
